@@ -1,0 +1,472 @@
+/*
+ * oracle.c -- plain CPU reference for one decode step of hierarchically pruned,
+ * block-sparse attention over a paged KV cache whose keys are int8, per-channel
+ * quantised.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library. The product path never
+ * links, loads or calls it, and it shares no code, header, table or constant
+ * with the CUDA library.
+ *
+ * Sources (web pages; cited by page title and section):
+ *  [HiP]  "韩国通过卸载键值缓存节约英伟达GPU内存，实现18.95倍解码加速" (163.com article on
+ *         InfiniteHiP), section "实现 7.24 倍的端到端解码加速": each pruning module cuts
+ *         its input into fixed-length chunks, finds each chunk's top-scoring token in
+ *         parallel and passes only the top-K chunks on; stacking modules refines a
+ *         block-sparse attention mask.
+ *  [HCA]  "HCAttention: Extreme KV cache compression via heterogeneous attention
+ *         computing for LLMs" (ebiotrade.com excerpt), abstract and contribution list:
+ *         keys are quantised and kept on the GPU for a global approximate scoring of
+ *         every token; values are fetched late, only for the final aggregation.
+ *  [KVN]  "KV Cache 与长上下文推理" (jeffliulab notes), section "KV Cache 回顾", the
+ *         attention equation softmax(q K^T / sqrt(d_k)) V; section "KV Cache 量化"
+ *         (INT8 keys); section "Token Eviction 与 Sparse Attention" (StreamingLLM:
+ *         attention sinks plus a sliding window); section "MQA 与 GQA" (G key/value
+ *         heads shared by H query heads).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - key scale per (sequence, kv head, channel) over the whole context:
+ *      s_c = f32(amax_c / 127), code = clamp(rint_even(f32(k / s_c)), -127, 127),
+ *      s_c = 0 gives code 0;
+ *  - the key scales are folded into the query, q'_{j,c} = f32(q_{j,c} * s_c), and the
+ *    group of G query heads sharing a kv head is quantised with ONE scale
+ *      A = max |q'|, sq = f32(A / 127), qq = clamp(rint_even(f32(q' / sq)), -127, 127);
+ *  - token score g_t = max over the group of the exact integer dot qq_j . kq_t;
+ *  - candidate region C = [sink, N - window); chunks and blocks are aligned to token 0
+ *    and only their tokens inside C count; a chunk or block with no token in C is
+ *    never selected;
+ *  - ties: the lower index wins at both levels; index lists are returned ascending;
+ *  - attended set T = [0, min(S,N)) u [max(N-W, min(S,N)), N) u (kept blocks n C).
+ *
+ * Precision: attention in fp64 from the exact bf16 values. The quantisation steps
+ * decide integers in IEEE fp32, emulated as ONE fp64 operation followed by a cast to
+ * float: exact for a product of two floats (48 significant bits < 53) and correctly
+ * rounded for a quotient of two floats (53 >= 2*24 + 2, Figueroa 1995). Build with
+ * -ffp-contract=off so that no product is fused into an add.
+ *
+ * Pins (what ties this file to something other than itself): hand-worked examples
+ * under tests/golden, brute force on tiny inputs, the closed form "two-stage top-K
+ * equals the single-stage top-K2 of blocks whenever K1 >= K2", K1/K2 covering every
+ * block reproducing dense attention, K1 = K2 = 0 reproducing sink + window
+ * attention, the quantisation error bound, power-of-two scale invariance, and the
+ * restriction identity linking sparse output, dense output and recall.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+  int32_t batch, hq, hkv, head_dim, page_size, max_pages_per_seq, num_pages;
+  int32_t chunk, block, k1, k2, sink, window;
+  double sm_scale; /* <= 0 means 1/sqrt(head_dim) */
+} oracle_dims;
+
+/* ---------------------------------------------------------------- helpers */
+
+static double bf16_value(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Index of element (token t, channel c) of kv head h of sequence b in a paged
+ * cache laid out [page][kv head][slot in page][channel]. */
+static size_t cache_index(const oracle_dims* d, const int32_t* page_table, int b, int h,
+                          int64_t t, int c) {
+  int64_t page = page_table[(int64_t)b * d->max_pages_per_seq + t / d->page_size];
+  int64_t slot = t % d->page_size;
+  return (size_t)(((page * d->hkv + h) * d->page_size + slot) * d->head_dim + c);
+}
+
+static int dims_ok(const oracle_dims* d) {
+  if (!d) return 0;
+  if (d->batch <= 0 || d->hq <= 0 || d->hkv <= 0 || d->head_dim <= 0) return 0;
+  if (d->hq % d->hkv) return 0;
+  if (d->page_size <= 0 || d->max_pages_per_seq <= 0 || d->num_pages <= 0) return 0;
+  if (d->chunk <= 0 || d->block <= 0 || d->chunk % d->block) return 0;
+  if (d->k1 < 0 || d->k2 < 0 || d->sink < 0 || d->window < 0) return 0;
+  return 1;
+}
+
+static int seq_ok(const oracle_dims* d, const int32_t* page_table, const int32_t* lens, int b) {
+  int64_t n = lens[b];
+  if (n < 0 || n > (int64_t)d->max_pages_per_seq * d->page_size) return 0;
+  for (int64_t p = 0; p * d->page_size < n; p++) {
+    int32_t pg = page_table[(int64_t)b * d->max_pages_per_seq + p];
+    if (pg < 0 || pg >= d->num_pages) return 0;
+  }
+  return 1;
+}
+
+static int wanted(const int32_t* bh_mask, const oracle_dims* d, int b, int h) {
+  return bh_mask == NULL || bh_mask[b * d->hkv + h] != 0;
+}
+
+/* fp32 round-to-nearest-even code of x / s, clamped to the symmetric int8 range. */
+static int8_t int8_code(double x, float s) {
+  if (s == 0.0f) return 0;
+  float ratio = (float)(x / (double)s);
+  double r = nearbyint((double)ratio); /* default rounding mode: half to even */
+  if (r > 127.0) r = 127.0;
+  if (r < -127.0) r = -127.0;
+  return (int8_t)r;
+}
+
+/* ----------------------------------------------- key scales and int8 codes */
+
+/* [HCA] quantised keys on the GPU; [KVN] "KV Cache 量化" (INT8 keys).
+ * Full mode: per (b, h, c) amax over tokens t < N_b, then every token's code.
+ * Slots of the last page past N_b get code 0. */
+int oracle_quantize_keys(const oracle_dims* d, const uint16_t* k, const int32_t* page_table,
+                         const int32_t* lens, const int32_t* bh_mask, int8_t* kq, float* scale) {
+  if (!dims_ok(d) || !k || !page_table || !lens || !kq || !scale) return 1;
+  for (int b = 0; b < d->batch; b++)
+    if (!seq_ok(d, page_table, lens, b)) return 2;
+  const int D = d->head_dim;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int bh = 0; bh < d->batch * d->hkv; bh++) {
+    int b = bh / d->hkv, h = bh % d->hkv;
+    if (!wanted(bh_mask, d, b, h)) continue;
+    int64_t n = lens[b];
+    for (int c = 0; c < D; c++) {
+      double amax = 0.0;
+      for (int64_t t = 0; t < n; t++) {
+        double x = fabs(bf16_value(k[cache_index(d, page_table, b, h, t, c)]));
+        if (x > amax) amax = x;
+      }
+      float s = (float)(amax / 127.0);
+      scale[((int64_t)b * d->hkv + h) * D + c] = s;
+      for (int64_t t = 0; t < n; t++) {
+        size_t i = cache_index(d, page_table, b, h, t, c);
+        kq[i] = int8_code(bf16_value(k[i]), s);
+      }
+      int64_t end = ((n + d->page_size - 1) / d->page_size) * d->page_size;
+      for (int64_t t = n; t < end; t++) kq[cache_index(d, page_table, b, h, t, c)] = 0;
+    }
+  }
+  return 0;
+}
+
+/* Append mode: codes of tokens [from_b, N_b) with the scales already stored;
+ * from < 0 means each sequence's last token (the decode-step append). */
+int oracle_quantize_append(const oracle_dims* d, const uint16_t* k, const int32_t* page_table,
+                           const int32_t* lens, int32_t from, const float* scale, int8_t* kq) {
+  if (!dims_ok(d) || !k || !page_table || !lens || !kq || !scale) return 1;
+  for (int b = 0; b < d->batch; b++) {
+    if (!seq_ok(d, page_table, lens, b)) return 2;
+    int64_t n = lens[b];
+    int64_t t0 = from < 0 ? n - 1 : from;
+    if (t0 < 0) t0 = 0;
+    for (int h = 0; h < d->hkv; h++)
+      for (int64_t t = t0; t < n; t++)
+        for (int c = 0; c < d->head_dim; c++) {
+          size_t i = cache_index(d, page_table, b, h, t, c);
+          kq[i] = int8_code(bf16_value(k[i]), scale[((int64_t)b * d->hkv + h) * d->head_dim + c]);
+        }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------ query int8 codes */
+
+/* [HCA] scoring against quantised keys: the key scales are folded into the query
+ * (q' = q * s) and the G query heads of one kv head share one quantisation scale, so
+ * that the integer scores of the group are in the same units and their max is
+ * meaningful. qq: [B][Hkv][G][D]; q_scale: [B][Hkv] (sq = A / 127). */
+static void query_codes_one(const oracle_dims* d, const uint16_t* q, const float* scale, int b,
+                            int h, int8_t* qq, float* sq_out) {
+  const int D = d->head_dim, G = d->hq / d->hkv;
+  const float* s = scale + ((int64_t)b * d->hkv + h) * D;
+  float* qf = (float*)malloc(sizeof(float) * (size_t)G * D);
+  float amax = 0.0f;
+  for (int j = 0; j < G; j++)
+    for (int c = 0; c < D; c++) {
+      double qv = bf16_value(q[((int64_t)b * d->hq + h * G + j) * D + c]);
+      float folded = (float)(qv * (double)s[c]);
+      qf[j * D + c] = folded;
+      if (fabsf(folded) > amax) amax = fabsf(folded);
+    }
+  float sq = (float)((double)amax / 127.0);
+  for (int j = 0; j < G; j++)
+    for (int c = 0; c < D; c++) qq[j * D + c] = int8_code((double)qf[j * D + c], sq);
+  if (sq_out) *sq_out = sq;
+  free(qf);
+}
+
+int oracle_query_codes(const oracle_dims* d, const uint16_t* q, const float* scale, int8_t* qq,
+                       float* q_scale) {
+  if (!dims_ok(d) || !q || !scale || !qq) return 1;
+  const int D = d->head_dim, G = d->hq / d->hkv;
+  for (int b = 0; b < d->batch; b++)
+    for (int h = 0; h < d->hkv; h++)
+      query_codes_one(d, q, scale, b, h, qq + ((int64_t)b * d->hkv + h) * G * D,
+                      q_scale ? q_scale + (int64_t)b * d->hkv + h : NULL);
+  return 0;
+}
+
+/* ------------------------------------------------------ the two modules */
+
+typedef struct {
+  int64_t score;
+  int64_t index;
+} ranked;
+
+/* higher score first; equal scores: lower index first */
+static int by_score_then_index(const void* a, const void* b) {
+  const ranked* x = (const ranked*)a;
+  const ranked* y = (const ranked*)b;
+  if (x->score != y->score) return x->score > y->score ? -1 : 1;
+  return (x->index > y->index) - (x->index < y->index);
+}
+
+static int by_index(const void* a, const void* b) {
+  const ranked* x = (const ranked*)a;
+  const ranked* y = (const ranked*)b;
+  return (x->index > y->index) - (x->index < y->index);
+}
+
+/* [HiP] two stacked pruning modules over the candidate region C = [S, N - W):
+ *  module 1: chunks of `chunk` tokens; a chunk's score is the max token score over
+ *            its tokens in C; the top-K1 chunks pass on;
+ *  module 2: the kept chunks are cut into blocks of `block` tokens; a block's score is
+ *            the max token score over its tokens in C; the top-K2 blocks are kept.
+ * A token's score is the max over the group's query heads of the exact integer dot
+ * product of the query codes with the key codes ([HCA] global approximate scoring).
+ * Outputs (per (b, h)): block_max [B][Hkv][max_pages_per_seq*page_size/block]
+ * (INT32_MIN where a block has no token in C; nullable), chunk_idx [B][Hkv][K1]
+ * and block_idx [B][Hkv][K2] ascending and padded with -1, n_chunks / n_blocks
+ * [B][Hkv] (nullable). */
+int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, const int8_t* kq,
+                  const int32_t* page_table, const int32_t* lens, const int32_t* bh_mask,
+                  int32_t* block_max, int32_t* chunk_idx, int32_t* n_chunks, int32_t* block_idx,
+                  int32_t* n_blocks) {
+  if (!dims_ok(d) || !q || !scale || !kq || !page_table || !lens || !chunk_idx || !block_idx)
+    return 1;
+  for (int b = 0; b < d->batch; b++)
+    if (!seq_ok(d, page_table, lens, b)) return 2;
+  const int D = d->head_dim, G = d->hq / d->hkv;
+  const int64_t max_tokens = (int64_t)d->max_pages_per_seq * d->page_size;
+  const int64_t max_blocks = (max_tokens + d->block - 1) / d->block;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int bh = 0; bh < d->batch * d->hkv; bh++) {
+    int b = bh / d->hkv, h = bh % d->hkv;
+    if (!wanted(bh_mask, d, b, h)) continue;
+    int64_t n = lens[b];
+    int64_t lo = d->sink, hi = n - d->window; /* C = [lo, hi) */
+    int8_t* qq = (int8_t*)malloc((size_t)G * D);
+    query_codes_one(d, q, scale, b, h, qq, NULL);
+
+    int64_t n_chunk_all = (max_tokens + d->chunk - 1) / d->chunk;
+    int64_t* cmax = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_chunk_all + 1));
+    int64_t* bmax = (int64_t*)malloc(sizeof(int64_t) * (size_t)(max_blocks + 1));
+    char* cvalid = (char*)calloc((size_t)n_chunk_all + 1, 1);
+    char* bvalid = (char*)calloc((size_t)max_blocks + 1, 1);
+    if (!qq || !cmax || !bmax || !cvalid || !bvalid) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+      /* token scores, folded straight into the chunk and block maxima */
+      for (int64_t t = lo; t < hi; t++) {
+        int64_t g = INT64_MIN;
+        for (int j = 0; j < G; j++) {
+          int64_t dot = 0;
+          for (int c = 0; c < D; c++)
+            dot += (int64_t)qq[j * D + c] * (int64_t)kq[cache_index(d, page_table, b, h, t, c)];
+          if (dot > g) g = dot;
+        }
+        int64_t ci = t / d->chunk, bi = t / d->block;
+        if (!cvalid[ci] || g > cmax[ci]) cmax[ci] = g;
+        if (!bvalid[bi] || g > bmax[bi]) bmax[bi] = g;
+        cvalid[ci] = 1;
+        bvalid[bi] = 1;
+      }
+      if (block_max) {
+        int32_t* out = block_max + ((int64_t)b * d->hkv + h) * max_blocks;
+        for (int64_t k = 0; k < max_blocks; k++) out[k] = bvalid[k] ? (int32_t)bmax[k] : INT32_MIN;
+      }
+      /* module 1: top-K1 chunks */
+      ranked* list = (ranked*)malloc(sizeof(ranked) * (size_t)(n_chunk_all + max_blocks + 1));
+      int64_t nc = 0;
+      for (int64_t c = 0; c < n_chunk_all; c++)
+        if (cvalid[c]) {
+          list[nc].score = cmax[c];
+          list[nc].index = c;
+          nc++;
+        }
+      qsort(list, (size_t)nc, sizeof(ranked), by_score_then_index);
+      int64_t keep1 = nc < d->k1 ? nc : d->k1;
+      qsort(list, (size_t)keep1, sizeof(ranked), by_index);
+      int32_t* cout = chunk_idx + ((int64_t)b * d->hkv + h) * d->k1;
+      for (int64_t i = 0; i < d->k1; i++) cout[i] = i < keep1 ? (int32_t)list[i].index : -1;
+      if (n_chunks) n_chunks[b * d->hkv + h] = (int32_t)keep1;
+      /* module 2: the kept chunks' blocks, top-K2 */
+      ranked* blist = list + keep1;
+      int64_t nb = 0;
+      const int per = d->chunk / d->block;
+      for (int64_t i = 0; i < keep1; i++)
+        for (int64_t k = list[i].index * per; k < (list[i].index + 1) * per; k++)
+          if (k < max_blocks && bvalid[k]) {
+            blist[nb].score = bmax[k];
+            blist[nb].index = k;
+            nb++;
+          }
+      qsort(blist, (size_t)nb, sizeof(ranked), by_score_then_index);
+      int64_t keep2 = nb < d->k2 ? nb : d->k2;
+      qsort(blist, (size_t)keep2, sizeof(ranked), by_index);
+      int32_t* bout = block_idx + ((int64_t)b * d->hkv + h) * d->k2;
+      for (int64_t i = 0; i < d->k2; i++) bout[i] = i < keep2 ? (int32_t)blist[i].index : -1;
+      if (n_blocks) n_blocks[b * d->hkv + h] = (int32_t)keep2;
+      free(list);
+    }
+    free(qq);
+    free(cmax);
+    free(bmax);
+    free(cvalid);
+    free(bvalid);
+  }
+  return bad ? 3 : 0;
+}
+
+/* ---------------------------------------------------------- attention */
+
+/* Membership of token t in the attended set T of (b, h):
+ * sink [0, min(S,N)), window [max(N-W, min(S,N)), N), and the kept blocks' tokens
+ * inside C = [S, N-W). The three parts are disjoint. `kept` flags blocks. */
+static int attended(const oracle_dims* d, int64_t n, int64_t t, const char* kept) {
+  int64_t sink_end = d->sink < n ? d->sink : n;
+  int64_t win_start = n - d->window;
+  if (win_start < sink_end) win_start = sink_end;
+  if (t < sink_end) return 1;
+  if (t >= win_start) return 1;
+  if (kept && t >= d->sink && t < n - d->window && kept[t / d->block]) return 1;
+  return 0;
+}
+
+/* [KVN] "KV Cache 回顾": out = softmax(q K_T^T / sqrt(d)) V_T over the attended set T,
+ * in fp64 from the exact bf16 values; lse = log sum_t exp(l_t). When `all` is set, T
+ * is the whole context [0, N) (dense decode). When `recall` is given, the function
+ * instead returns sum_{t in T} p_t with p the dense softmax over [0, N). */
+static int attention_common(const oracle_dims* d, const uint16_t* q, const uint16_t* k,
+                            const uint16_t* v, const int32_t* page_table, const int32_t* lens,
+                            const int32_t* block_idx, const int32_t* n_blocks,
+                            const int32_t* qh_mask, int all, double* out, double* lse,
+                            double* recall) {
+  const int D = d->head_dim, G = d->hq / d->hkv;
+  const double scale = d->sm_scale > 0 ? d->sm_scale : 1.0 / sqrt((double)D);
+  const int64_t max_tokens = (int64_t)d->max_pages_per_seq * d->page_size;
+  const int64_t max_blocks = (max_tokens + d->block - 1) / d->block;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int bj = 0; bj < d->batch * d->hq; bj++) {
+    int b = bj / d->hq, j = bj % d->hq, h = j / G;
+    if (qh_mask && !qh_mask[bj]) continue;
+    int64_t n = lens[b];
+    char* kept = NULL;
+    if (!all) {
+      kept = (char*)calloc((size_t)max_blocks + 1, 1);
+      if (!kept) {
+#pragma omp atomic write
+        bad = 1;
+        continue;
+      }
+      int nk = n_blocks ? n_blocks[b * d->hkv + h] : d->k2;
+      const int32_t* list = block_idx + ((int64_t)b * d->hkv + h) * d->k2;
+      for (int i = 0; i < nk && i < d->k2; i++)
+        if (list[i] >= 0 && list[i] < max_blocks) kept[list[i]] = 1;
+    }
+    double* logit = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!logit || !qv) {
+#pragma omp atomic write
+      bad = 1;
+      free(kept);
+      free(logit);
+      free(qv);
+      continue;
+    }
+    for (int c = 0; c < D; c++) qv[c] = bf16_value(q[((int64_t)b * d->hq + j) * D + c]);
+    int dense_for_recall = recall != NULL;
+    double m = -INFINITY;
+    for (int64_t t = 0; t < n; t++) {
+      int in_t = all || dense_for_recall || attended(d, n, t, kept);
+      if (!in_t) continue;
+      double dot = 0.0;
+      for (int c = 0; c < D; c++) dot += qv[c] * bf16_value(k[cache_index(d, page_table, b, h, t, c)]);
+      logit[t] = dot * scale;
+      if (logit[t] > m) m = logit[t];
+    }
+    double z = 0.0, zt = 0.0;
+    for (int64_t t = 0; t < n; t++) {
+      int in_t = all || attended(d, n, t, kept);
+      if (!(in_t || dense_for_recall)) continue;
+      double e = exp(logit[t] - m);
+      z += e;
+      if (in_t) zt += e;
+    }
+    if (recall) {
+      recall[bj] = n > 0 ? zt / z : 0.0;
+    } else {
+      double* o = out + (int64_t)bj * D;
+      for (int c = 0; c < D; c++) o[c] = 0.0;
+      for (int64_t t = 0; t < n; t++) {
+        if (!(all || attended(d, n, t, kept))) continue;
+        double p = exp(logit[t] - m) / z;
+        for (int c = 0; c < D; c++) o[c] += p * bf16_value(v[cache_index(d, page_table, b, h, t, c)]);
+      }
+      if (lse) lse[bj] = n > 0 ? m + log(z) : -INFINITY;
+    }
+    free(kept);
+    free(logit);
+    free(qv);
+  }
+  return bad ? 3 : 0;
+}
+
+/* Sparse decode attention over T (sink, window and the kept blocks inside C).
+ * out [B][Hq][D], lse [B][Hq] (nullable); qh_mask [B][Hq] selects query heads
+ * (nullable = all). */
+int oracle_attend(const oracle_dims* d, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                  const int32_t* page_table, const int32_t* lens, const int32_t* block_idx,
+                  const int32_t* n_blocks, const int32_t* qh_mask, double* out, double* lse) {
+  if (!dims_ok(d) || !q || !k || !v || !page_table || !lens || !block_idx || !out) return 1;
+  for (int b = 0; b < d->batch; b++)
+    if (!seq_ok(d, page_table, lens, b)) return 2;
+  return attention_common(d, q, k, v, page_table, lens, block_idx, n_blocks, qh_mask, 0, out, lse,
+                          NULL);
+}
+
+/* Dense decode attention over the whole context [0, N). */
+int oracle_dense(const oracle_dims* d, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                 const int32_t* page_table, const int32_t* lens, const int32_t* qh_mask,
+                 double* out, double* lse) {
+  if (!dims_ok(d) || !q || !k || !v || !page_table || !lens || !out) return 1;
+  for (int b = 0; b < d->batch; b++)
+    if (!seq_ok(d, page_table, lens, b)) return 2;
+  return attention_common(d, q, k, v, page_table, lens, NULL, NULL, qh_mask, 1, out, lse, NULL);
+}
+
+/* Attention-mass recall of T against dense attention ([HiP], latency section: recall of
+ * the attention probability of the important tokens): R = sum_{t in T} p_dense(t). */
+int oracle_recall(const oracle_dims* d, const uint16_t* q, const uint16_t* k,
+                  const int32_t* page_table, const int32_t* lens, const int32_t* block_idx,
+                  const int32_t* n_blocks, const int32_t* qh_mask, double* recall) {
+  if (!dims_ok(d) || !q || !k || !page_table || !lens || !block_idx || !recall) return 1;
+  for (int b = 0; b < d->batch; b++)
+    if (!seq_ok(d, page_table, lens, b)) return 2;
+  return attention_common(d, q, k, NULL, page_table, lens, block_idx, n_blocks, qh_mask, 0, NULL,
+                          NULL, recall);
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,205 @@
+"""ctypes front end of the C oracle (``oracle.c``); numpy in, numpy out.
+
+TEST INFRASTRUCTURE (see the package docstring). bf16 tensors travel as their raw
+16-bit patterns (``numpy.uint16``); the C side widens them exactly.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+
+class _CDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "hq", "hkv", "head_dim", "page_size", "max_pages_per_seq", "num_pages",
+        "chunk", "block", "k1", "k2", "sink", "window")] + [("sm_scale", ctypes.c_double)]
+
+
+@dataclasses.dataclass
+class Dims:
+    """Problem sizes; the same fields as the CUDA library's descriptor, kept separately."""
+    batch: int
+    hq: int
+    hkv: int
+    head_dim: int
+    page_size: int
+    max_pages_per_seq: int
+    num_pages: int
+    chunk: int
+    block: int
+    k1: int
+    k2: int
+    sink: int
+    window: int
+    sm_scale: float = 0.0
+
+    def c(self) -> _CDims:
+        return _CDims(*[int(getattr(self, f[0])) for f in _CDims._fields_[:-1]],
+                      float(self.sm_scale))
+
+    @property
+    def group(self) -> int:
+        return self.hq // self.hkv
+
+    @property
+    def max_blocks(self) -> int:
+        return -(-self.max_pages_per_seq * self.page_size // self.block)
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        D = ctypes.POINTER(_CDims)
+        sigs = {
+            "oracle_quantize_keys": [D, P, P, P, P, P, P],
+            "oracle_quantize_append": [D, P, P, P, ctypes.c_int32, P, P],
+            "oracle_query_codes": [D, P, P, P, P],
+            "oracle_select": [D, P, P, P, P, P, P, P, P, P, P, P],
+            "oracle_attend": [D, P, P, P, P, P, P, P, P, P, P],
+            "oracle_dense": [D, P, P, P, P, P, P, P, P],
+            "oracle_recall": [D, P, P, P, P, P, P, P, P],
+        }
+        for name, args in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _LIB = lib
+    return _LIB
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, "bf16 tensors are passed as raw uint16 bit patterns"
+    return a
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _check(rc: int, name: str) -> None:
+    if rc != 0:
+        raise ValueError(f"{name} rejected its arguments (code {rc})")
+
+
+def num_threads() -> int:
+    return int(_lib().oracle_num_threads())
+
+
+def quantize_keys(d: Dims, k: np.ndarray, page_table, seq_lens, bh_mask=None):
+    """Full key quantisation: returns (kq int8 same shape as k, k_scale f32 [B][Hkv][D])."""
+    k = _u16(k)
+    kq = np.zeros(k.shape, dtype=np.int8)
+    scale = np.zeros((d.batch, d.hkv, d.head_dim), dtype=np.float32)
+    cd = d.c()
+    _check(_lib().oracle_quantize_keys(ctypes.byref(cd), _ptr(k), _ptr(_i32(page_table)),
+                                       _ptr(_i32(seq_lens)),
+                                       _ptr(None if bh_mask is None else _i32(bh_mask)),
+                                       _ptr(kq), _ptr(scale)), "oracle_quantize_keys")
+    return kq, scale
+
+
+def quantize_append(d: Dims, k: np.ndarray, page_table, seq_lens, start: int,
+                    k_scale: np.ndarray, kq: np.ndarray) -> np.ndarray:
+    """Codes of tokens [start, N_b) (start < 0: each sequence's last token) with the
+    stored scales; returns an updated copy of ``kq``."""
+    kq = np.array(kq, dtype=np.int8, copy=True, order="C")
+    cd = d.c()
+    _check(_lib().oracle_quantize_append(ctypes.byref(cd), _ptr(_u16(k)), _ptr(_i32(page_table)),
+                                         _ptr(_i32(seq_lens)), int(start),
+                                         _ptr(np.ascontiguousarray(k_scale, dtype=np.float32)),
+                                         _ptr(kq)), "oracle_quantize_append")
+    return kq
+
+
+def query_codes(d: Dims, q: np.ndarray, k_scale: np.ndarray):
+    """Query codes qq [B][Hkv][G][D] int8 and the group scales sq [B][Hkv] f32."""
+    qq = np.zeros((d.batch, d.hkv, d.group, d.head_dim), dtype=np.int8)
+    sq = np.zeros((d.batch, d.hkv), dtype=np.float32)
+    cd = d.c()
+    _check(_lib().oracle_query_codes(ctypes.byref(cd), _ptr(_u16(q)),
+                                     _ptr(np.ascontiguousarray(k_scale, dtype=np.float32)),
+                                     _ptr(qq), _ptr(sq)), "oracle_query_codes")
+    return qq, sq
+
+
+def select(d: Dims, q: np.ndarray, k_scale: np.ndarray, kq: np.ndarray, page_table, seq_lens,
+           bh_mask=None, want_block_max: bool = False):
+    """The two pruning modules. Returns a dict with chunk_idx [B][Hkv][K1],
+    n_chunks [B][Hkv], block_idx [B][Hkv][K2], n_blocks [B][Hkv] and, on request,
+    block_max [B][Hkv][max_blocks] (INT32_MIN where a block has no candidate token)."""
+    B, H = d.batch, d.hkv
+    out = {
+        "chunk_idx": np.full((B, H, max(d.k1, 0)), -1, dtype=np.int32),
+        "n_chunks": np.zeros((B, H), dtype=np.int32),
+        "block_idx": np.full((B, H, max(d.k2, 0)), -1, dtype=np.int32),
+        "n_blocks": np.zeros((B, H), dtype=np.int32),
+    }
+    bm = np.zeros((B, H, d.max_blocks), dtype=np.int32) if want_block_max else None
+    cd = d.c()
+    kq = np.ascontiguousarray(kq)
+    assert kq.dtype == np.int8
+    _check(_lib().oracle_select(ctypes.byref(cd), _ptr(_u16(q)),
+                                _ptr(np.ascontiguousarray(k_scale, dtype=np.float32)), _ptr(kq),
+                                _ptr(_i32(page_table)), _ptr(_i32(seq_lens)),
+                                _ptr(None if bh_mask is None else _i32(bh_mask)), _ptr(bm),
+                                _ptr(out["chunk_idx"]), _ptr(out["n_chunks"]),
+                                _ptr(out["block_idx"]), _ptr(out["n_blocks"])), "oracle_select")
+    if want_block_max:
+        out["block_max"] = bm
+    return out
+
+
+def attend(d: Dims, q, k, v, page_table, seq_lens, block_idx, n_blocks, qh_mask=None):
+    """Sparse decode attention: returns (out f64 [B][Hq][D], lse f64 [B][Hq])."""
+    out = np.zeros((d.batch, d.hq, d.head_dim), dtype=np.float64)
+    lse = np.zeros((d.batch, d.hq), dtype=np.float64)
+    cd = d.c()
+    _check(_lib().oracle_attend(ctypes.byref(cd), _ptr(_u16(q)), _ptr(_u16(k)), _ptr(_u16(v)),
+                                _ptr(_i32(page_table)), _ptr(_i32(seq_lens)),
+                                _ptr(_i32(block_idx)), _ptr(_i32(n_blocks)),
+                                _ptr(None if qh_mask is None else _i32(qh_mask)),
+                                _ptr(out), _ptr(lse)), "oracle_attend")
+    return out, lse
+
+
+def dense(d: Dims, q, k, v, page_table, seq_lens, qh_mask=None):
+    """Dense decode attention over [0, N): returns (out f64 [B][Hq][D], lse f64 [B][Hq])."""
+    out = np.zeros((d.batch, d.hq, d.head_dim), dtype=np.float64)
+    lse = np.zeros((d.batch, d.hq), dtype=np.float64)
+    cd = d.c()
+    _check(_lib().oracle_dense(ctypes.byref(cd), _ptr(_u16(q)), _ptr(_u16(k)), _ptr(_u16(v)),
+                               _ptr(_i32(page_table)), _ptr(_i32(seq_lens)),
+                               _ptr(None if qh_mask is None else _i32(qh_mask)),
+                               _ptr(out), _ptr(lse)), "oracle_dense")
+    return out, lse
+
+
+def recall(d: Dims, q, k, page_table, seq_lens, block_idx, n_blocks, qh_mask=None):
+    """Attention-mass recall of the attended set against dense attention, [B][Hq]."""
+    r = np.zeros((d.batch, d.hq), dtype=np.float64)
+    cd = d.c()
+    _check(_lib().oracle_recall(ctypes.byref(cd), _ptr(_u16(q)), _ptr(_u16(k)),
+                                _ptr(_i32(page_table)), _ptr(_i32(seq_lens)),
+                                _ptr(_i32(block_idx)), _ptr(_i32(n_blocks)),
+                                _ptr(None if qh_mask is None else _i32(qh_mask)), _ptr(r)),
+           "oracle_recall")
+    return r

@@ -1,0 +1,511 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself: the
+hand-worked examples under tests/golden, closed forms, special cases that reduce to a
+textbook routine, invariants, and defining properties checked by brute force on tiny
+inputs. A plausible slip anywhere in the oracle (a dropped term, a wrong sign or index,
+a transposed operand, a wrong rounding mode or cast point) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp, softmax
+
+from conftest import bf16_bits, bits_to_f64, read_golden
+
+import oracle
+from oracle import Dims
+
+INT32_MIN = np.iinfo(np.int32).min
+
+
+# ------------------------------------------------------------------ helpers
+
+def paged(values_btd: list, page: int, hkv: int, perm=None):
+    """Lay per-sequence [Hkv][N_b][D] float32 arrays out as a paged cache
+    [pages][Hkv][page][D]; returns (cache, page_table, lens). Slots past N_b are filled
+    with a recognisable junk value."""
+    lens = [v.shape[1] for v in values_btd]
+    D = values_btd[0].shape[2]
+    pages_per = [-(-n // page) for n in lens]
+    total = sum(pages_per)
+    order = np.arange(total) if perm is None else np.asarray(perm)
+    cache = np.full((total, hkv, page, D), 1.5, dtype=np.float32)
+    pt = np.full((len(lens), max(pages_per)), -1, dtype=np.int32)
+    off = 0
+    for b, v in enumerate(values_btd):
+        for p in range(pages_per[b]):
+            pg = order[off + p]
+            pt[b, p] = pg
+            t0, t1 = p * page, min((p + 1) * page, lens[b])
+            cache[pg, :, : t1 - t0, :] = v[:, t0:t1, :]
+        off += pages_per[b]
+    return cache, pt, np.asarray(lens, dtype=np.int32)
+
+
+def to_bf16(x):
+    """Round float32 values to bf16 (nearest even) and return them as float32."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return u.astype(np.uint32).view(np.float32)
+
+
+def random_case(rng, B=1, hq=4, hkv=1, D=8, lens=(200,), page=16, perm=False):
+    lens = list(lens)
+    ks = [to_bf16(rng.standard_normal((hkv, n, D))) for n in lens]
+    vs = [to_bf16(rng.standard_normal((hkv, n, D))) for n in lens]
+    total = sum(-(-n // page) for n in lens)
+    order = rng.permutation(total) if perm else None
+    kc, pt, ln = paged(ks, page, hkv, order)
+    vc, _, _ = paged(vs, page, hkv, order)
+    q = to_bf16(rng.standard_normal((B, hq, D)))
+    return dict(k=kc, v=vc, pt=pt, lens=ln, q=q, ks=ks, vs=vs, page=page)
+
+
+def dims_for(case, hq, hkv, D, chunk=32, block=16, k1=4, k2=4, sink=8, window=16, scale=0.0):
+    return Dims(batch=len(case["lens"]), hq=hq, hkv=hkv, head_dim=D, page_size=case["page"],
+                max_pages_per_seq=case["pt"].shape[1], num_pages=case["k"].shape[0],
+                chunk=chunk, block=block, k1=k1, k2=k2, sink=sink, window=window,
+                sm_scale=scale)
+
+
+def run_all(d, case):
+    kb, vb, qb = bf16_bits(case["k"]), bf16_bits(case["v"]), bf16_bits(case["q"])
+    kq, sc = oracle.quantize_keys(d, kb, case["pt"], case["lens"])
+    sel = oracle.select(d, qb, sc, kq, case["pt"], case["lens"], want_block_max=True)
+    out, lse = oracle.attend(d, qb, kb, vb, case["pt"], case["lens"], sel["block_idx"],
+                             sel["n_blocks"])
+    return kq, sc, sel, out, lse
+
+
+def logical_codes(kq, pt, lens, page, hkv):
+    """Per sequence [Hkv][N_b][D] view of a paged code array."""
+    res = []
+    for b, n in enumerate(lens):
+        rows = [kq[pt[b, t // page], :, t % page, :] for t in range(n)]
+        res.append(np.stack(rows, axis=1))
+    return res
+
+
+# ------------------------------------------------------------- worked examples
+
+def test_key_codes_worked_example():
+    g = read_golden("key_codes_d4.txt")
+    keys = np.array(g["keys"], dtype=np.float32)            # [t][c]
+    n, D = keys.shape
+    cache, pt, lens = paged([keys[None]], int(g["page_size"]), 1)
+    d = Dims(1, 1, 1, D, int(g["page_size"]), pt.shape[1], cache.shape[0], 1, 1, 0, 0, 0, 0)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(cache), pt, lens)
+    np.testing.assert_array_equal(sc[0, 0], np.array(g["scales"][0], dtype=np.float32))
+    assert sc[0, 0, 2] == np.float32(8454660 * 2.0 ** -27)
+    codes = logical_codes(kq, pt, lens, int(g["page_size"]), 1)[0][0]
+    np.testing.assert_array_equal(codes, np.array(g["codes"], dtype=np.int8))
+    # the tail slot of the page (past N) is code 0
+    assert kq[0, 0, n:, :].tolist() == [[0] * D] * (int(g["page_size"]) - n)
+
+
+def test_query_codes_scores_and_modules_worked_example():
+    gk = read_golden("key_codes_d4.txt")
+    g = read_golden("query_scores_d4.txt")
+    keys = np.array(gk["keys"], dtype=np.float32)
+    q = np.array(g["query"], dtype=np.float32)[None]        # [1][G][D]
+    G, D = q.shape[1], q.shape[2]
+    cache, pt, lens = paged([keys[None]], int(gk["page_size"]), 1)
+    d = Dims(1, G, 1, D, int(gk["page_size"]), pt.shape[1], cache.shape[0],
+             int(g["chunk"]), int(g["block"]), int(g["k1"]), int(g["k2"]), int(g["sink"]),
+             int(g["window"]))
+    kq, sc = oracle.quantize_keys(d, bf16_bits(cache), pt, lens)
+    qq, sq = oracle.query_codes(d, bf16_bits(q), sc)
+    assert sq[0, 0] == np.float32(g["q_scale"])
+    np.testing.assert_array_equal(qq[0, 0], np.array(g["query_codes"], dtype=np.int8))
+    sel = oracle.select(d, bf16_bits(q), sc, kq, pt, lens, want_block_max=True)
+    assert sel["block_max"][0, 0, :3].tolist() == [int(x) for x in g["token_scores"][0]]
+    assert sel["chunk_idx"][0, 0].tolist() == [int(x) for x in g["chunk_idx"]]
+    assert sel["block_idx"][0, 0].tolist() == [int(x) for x in g["block_idx"]]
+    assert sel["n_blocks"][0, 0] == 2 and sel["n_chunks"][0, 0] == 3
+
+
+@pytest.mark.parametrize("case_no", [0, 1, 2])
+def test_tie_break_worked_example(case_no):
+    g = read_golden("tie_break_d4.txt")
+    c = g["cases"][case_no]
+    k0 = np.array(g["key_channel0"][0], dtype=np.float32)
+    keys = np.zeros((k0.size, 4), dtype=np.float32)
+    keys[:, 0] = k0
+    cache, pt, lens = paged([keys[None]], 4, 1)
+    q = np.array(g["query"], dtype=np.float32)[None]
+    k1, k2 = int(c["k1"]), int(c["k2"])
+    d = Dims(1, 1, 1, 4, 4, pt.shape[1], cache.shape[0], 2, 1, k1, k2, 0, 0)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(cache), pt, lens)
+    qq, _ = oracle.query_codes(d, bf16_bits(q), sc)
+    assert qq[0, 0, 0].tolist() == [127, 0, 0, 0]
+    sel = oracle.select(d, bf16_bits(q), sc, kq, pt, lens, want_block_max=True)
+    assert sel["block_max"][0, 0, :8].tolist() == [4064, 8128, 8128, 2032, 16129, 4064, 8128,
+                                                    -8128]
+    want_c = [int(x) for x in c["chunk_idx"].split(",")]
+    want_b = [int(x) for x in c["block_idx"].split(",")]
+    assert sel["chunk_idx"][0, 0].tolist() == want_c + [-1] * (k1 - len(want_c))
+    assert sel["block_idx"][0, 0].tolist() == want_b + [-1] * (k2 - len(want_b))
+
+
+def test_attention_two_tokens_worked_example():
+    g = read_golden("attention_two_tokens.txt")
+    k = np.array([[0.0, 1.0], [1.0, 0.0]], dtype=np.float32)
+    v = np.array([[1.0, 0.0], [0.0, 1.0]], dtype=np.float32)
+    kc, pt, lens = paged([k[None]], 16, 1)
+    vc, _, _ = paged([v[None]], 16, 1)
+    q = np.array([[[1.0, 0.0]]], dtype=np.float32)
+    d = Dims(1, 1, 1, 2, 16, 1, 1, 16, 16, 0, 0, 0, 0, sm_scale=1.0)
+    out, lse = oracle.dense(d, bf16_bits(q), bf16_bits(kc), bf16_bits(vc), pt, lens)
+    np.testing.assert_allclose(out[0, 0], g["out"], rtol=0, atol=1e-15)
+    assert abs(lse[0, 0] - g["lse"]) < 1e-14
+    # sink = window = 0 and nothing selected leaves an empty set for the sparse form...
+    out2, _ = oracle.attend(d, bf16_bits(q), bf16_bits(kc), bf16_bits(vc), pt, lens,
+                            np.zeros((1, 1, 0), np.int32), np.zeros((1, 1), np.int32))
+    # ...and with sink 2 both tokens are attended again
+    d2 = Dims(1, 1, 1, 2, 16, 1, 1, 16, 16, 0, 0, 2, 0, sm_scale=1.0)
+    out3, lse3 = oracle.attend(d2, bf16_bits(q), bf16_bits(kc), bf16_bits(vc), pt, lens,
+                               np.zeros((1, 1, 0), np.int32), np.zeros((1, 1), np.int32))
+    np.testing.assert_allclose(out3[0, 0], g["out"], atol=1e-15)
+    assert abs(lse3[0, 0] - g["lse"]) < 1e-14
+
+
+# ------------------------------------------------------------ quantisation
+
+def test_key_code_error_bound_and_extremes():
+    rng = np.random.default_rng(1)
+    case = random_case(rng, B=2, hq=4, hkv=2, D=16, lens=(97, 300), page=16, perm=True)
+    for b in range(2):
+        case["ks"][b][:, :, 3] = 0.0                         # a zero channel
+        case["ks"][b][:, :, 5] *= 8.0                         # an outlier channel
+    kc, pt, lens = paged(case["ks"], 16, 2, None)
+    d = Dims(2, 4, 2, 16, 16, pt.shape[1], kc.shape[0], 32, 16, 2, 2, 8, 16)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, lens)
+    codes = logical_codes(kq, pt, lens, 16, 2)
+    for b in range(2):
+        k = case["ks"][b].astype(np.float64)                 # [Hkv][N][D]
+        s = sc[b].astype(np.float64)[:, None, :]
+        err = np.abs(codes[b] * s - k)
+        # rint of the fp32 quotient: at most half a unit plus the quotient's own rounding
+        # (half an ulp of a value below 128, 2^-18)
+        assert np.all(err <= s * (0.5 + 2.0 ** -17))
+        amax = np.abs(k).max(axis=1)
+        assert np.all(sc[b][amax > 0] > 0) and np.all(sc[b][amax == 0] == 0)
+        # the element of largest magnitude of every nonzero channel codes to +-127
+        top = np.abs(codes[b]).max(axis=1)
+        assert np.all(top[amax > 0] == 127) and np.all(top[amax == 0] == 0)
+        # codes carry the sign of the key
+        assert np.all(np.sign(codes[b]) * np.sign(k) >= 0)
+        # scale is the fp32 quotient amax / 127
+        np.testing.assert_array_equal(sc[b], (amax / 127.0).astype(np.float32))
+
+
+@pytest.mark.parametrize("m", [-3, 2])
+def test_power_of_two_rescale_invariance(m):
+    rng = np.random.default_rng(2)
+    case = random_case(rng, B=1, hq=4, hkv=1, D=16, lens=(400,), page=16)
+    d = dims_for(case, 4, 1, 16, chunk=32, block=16, k1=4, k2=3, sink=8, window=16)
+    kq, sc, sel, out, _ = run_all(d, case)
+    case2 = dict(case)
+    case2["k"] = case["k"] * np.float32(2.0 ** m)
+    case2["q"] = case["q"] * np.float32(2.0 ** -m)
+    kq2, sc2, sel2, out2, _ = run_all(d, case2)
+    np.testing.assert_array_equal(kq2, kq)
+    np.testing.assert_array_equal(sc2, sc * np.float32(2.0 ** m))
+    for key in ("chunk_idx", "block_idx", "block_max"):
+        np.testing.assert_array_equal(sel2[key], sel[key])
+    np.testing.assert_allclose(out2, out, atol=1e-12)
+
+
+def test_page_permutation_invariance():
+    rng = np.random.default_rng(3)
+    base = random_case(rng, B=3, hq=8, hkv=2, D=16, lens=(150, 33, 260), page=16)
+    total = base["k"].shape[0]
+    perm = rng.permutation(total)
+    kc, pt, lens = paged(base["ks"], 16, 2, perm)
+    vc, _, _ = paged(base["vs"], 16, 2, perm)
+    other = dict(base, k=kc, v=vc, pt=pt)
+    d = dims_for(base, 8, 2, 16, chunk=32, block=16, k1=3, k2=3, sink=8, window=16)
+    kq, sc, sel, out, lse = run_all(d, base)
+    kq2, sc2, sel2, out2, lse2 = run_all(d, other)
+    for a, b in zip(logical_codes(kq, base["pt"], lens, 16, 2), logical_codes(kq2, pt, lens, 16, 2)):
+        np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(sc, sc2)
+    for key in ("chunk_idx", "block_idx", "n_blocks", "block_max"):
+        np.testing.assert_array_equal(sel[key], sel2[key])
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_append_reuses_stored_scales_and_saturates():
+    rng = np.random.default_rng(4)
+    case = random_case(rng, B=2, hq=4, hkv=2, D=16, lens=(70, 129), page=16)
+    d = dims_for(case, 4, 2, 16)
+    kb = bf16_bits(case["k"])
+    kq, sc = oracle.quantize_keys(d, kb, case["pt"], case["lens"])
+    wiped = kq.copy()
+    for b, n in enumerate(case["lens"]):
+        wiped[case["pt"][b, (n - 1) // 16], :, (n - 1) % 16, :] = 0
+    again = oracle.quantize_append(d, kb, case["pt"], case["lens"], -1, sc, wiped)
+    np.testing.assert_array_equal(again, kq)
+    # a new last token beyond the stored range saturates at +-127
+    big = case["k"].copy()
+    for b, n in enumerate(case["lens"]):
+        big[case["pt"][b, (n - 1) // 16], :, (n - 1) % 16, :] = 64.0
+        big[case["pt"][b, (n - 1) // 16], :, (n - 1) % 16, 0] = -64.0
+    sat = oracle.quantize_append(d, bf16_bits(big), case["pt"], case["lens"], -1, sc, kq)
+    for b, n in enumerate(case["lens"]):
+        row = sat[case["pt"][b, (n - 1) // 16], :, (n - 1) % 16, :]
+        assert np.all(row[:, 1:] == 127) and np.all(row[:, 0] == -127)
+
+
+def test_query_codes_bound_and_zero():
+    rng = np.random.default_rng(5)
+    case = random_case(rng, B=2, hq=8, hkv=2, D=16, lens=(50, 80), page=16)
+    d = dims_for(case, 8, 2, 16)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(case["k"]), case["pt"], case["lens"])
+    qq, sq = oracle.query_codes(d, bf16_bits(case["q"]), sc)
+    G = 4
+    for b in range(2):
+        for h in range(2):
+            qf = (case["q"][b, h * G:(h + 1) * G].astype(np.float64) * sc[b, h]).astype(np.float32)
+            assert np.abs(qq[b, h]).max() == 127
+            err = np.abs(qq[b, h] * np.float64(sq[b, h]) - qf)
+            assert np.all(err <= sq[b, h] * (0.5 + 2.0 ** -17))
+    qz, sz = oracle.query_codes(d, bf16_bits(np.zeros_like(case["q"])), sc)
+    assert not qz.any() and not sz.any()
+
+
+# ---------------------------------------------------------------- selection
+
+def _block_max_by_definition(qq, codes, n, sink, window, block):
+    """Block maxima written from the definition: every candidate token's score is the
+    largest of the group's integer dot products."""
+    lo, hi = sink, n - window
+    out = {}
+    for t in range(lo, hi):
+        g = max(int(np.dot(qq[j].astype(np.int64), codes[t].astype(np.int64)))
+                for j in range(qq.shape[0]))
+        out[t // block] = max(out.get(t // block, g), g)
+    return out
+
+
+def _beats(a_score, a_idx, b_score, b_idx):
+    return a_score > b_score or (a_score == b_score and a_idx < b_idx)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_modules_defining_property_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    D, hkv, G = 8, 2, 2
+    lens = tuple(int(x) for x in rng.integers(1, 520, size=2))
+    case = random_case(rng, B=2, hq=hkv * G, hkv=hkv, D=D, lens=lens, page=16, perm=True)
+    block = int(rng.choice([16, 32]))
+    chunk = block * int(rng.choice([1, 2, 4]))
+    k1, k2 = int(rng.integers(0, 9)), int(rng.integers(0, 12))
+    sink, window = int(rng.integers(0, 40)), int(rng.integers(0, 60))
+    # integer-valued keys make ties frequent
+    for b in range(2):
+        case["ks"][b] = np.round(case["ks"][b] * 2) / 2
+    kc, pt, ln = paged(case["ks"], 16, hkv, None)
+    case.update(k=kc, pt=pt)
+    d = dims_for(case, hkv * G, hkv, D, chunk=chunk, block=block, k1=k1, k2=k2, sink=sink,
+                 window=window)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, ln)
+    qq, _ = oracle.query_codes(d, bf16_bits(case["q"]), sc)
+    sel = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln, want_block_max=True)
+    codes = logical_codes(kq, pt, ln, 16, hkv)
+    per = chunk // block
+    for b in range(2):
+        for h in range(hkv):
+            n = int(ln[b])
+            bm = _block_max_by_definition(qq[b, h], codes[b][h], n, sink, window, block)
+            got = sel["block_max"][b, h]
+            for k in range(got.size):
+                assert got[k] == bm.get(k, INT32_MIN)
+            cm = {}
+            for k, s in bm.items():
+                cm[k // per] = max(cm.get(k // per, s), s)
+            kept_c = [c for c in sel["chunk_idx"][b, h] if c >= 0]
+            assert kept_c == sorted(kept_c) and len(kept_c) == min(k1, len(cm))
+            assert sel["n_chunks"][b, h] == len(kept_c)
+            for c in kept_c:
+                for c2 in cm:
+                    if c2 not in kept_c:
+                        assert _beats(cm[c], c, cm[c2], c2)
+            cand = [k for k in bm if k // per in kept_c]
+            kept_b = [k for k in sel["block_idx"][b, h] if k >= 0]
+            assert kept_b == sorted(kept_b) and len(kept_b) == min(k2, len(cand))
+            assert sel["n_blocks"][b, h] == len(kept_b)
+            for k in kept_b:
+                assert k in cand
+                for k2_ in cand:
+                    if k2_ not in kept_b:
+                        assert _beats(bm[k], k, bm[k2_], k2_)
+            if k1 >= k2:
+                # closed form: the two stages equal the single-stage top-K2 of all blocks
+                ranked = sorted(bm, key=lambda k: (-bm[k], k))[:k2]
+                assert sorted(ranked) == kept_b
+
+
+def test_candidate_region_masks_sink_and_window_tokens():
+    """A huge key in the sink part of a block that straddles the sink boundary, and one in
+    the window, must not lift any block score."""
+    D, n, sink, window = 4, 64, 8, 20
+    keys = np.zeros((n, D), dtype=np.float32)
+    keys[3, 0] = 8.0       # sink token inside block 0
+    keys[50, 0] = 8.0      # window token (window = [44, 64)) inside block 3 = [48, 64)
+    keys[10, 0] = 1.0      # candidate token in block 0
+    keys[40, 0] = 0.5      # candidate token in block 2
+    keys[46, 0] = 0.25     # candidate token of block 2 (block 2 = [32, 48) straddles 44)
+    kc, pt, ln = paged([keys[None]], 16, 1)
+    q = np.array([[[1.0, 0, 0, 0]]], dtype=np.float32)
+    d = Dims(1, 1, 1, D, 16, pt.shape[1], kc.shape[0], 16, 16, 4, 4, sink, window)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, ln)
+    sel = oracle.select(d, bf16_bits(q), sc, kq, pt, ln, want_block_max=True)
+    # s = f32(8/127): keys 1, 0.5, 0.25 code to 16, 8, 4; the query codes are (127, 0, 0, 0)
+    codes = logical_codes(kq, pt, ln, 16, 1)[0][0][:, 0].astype(np.int64)
+    assert [codes[10], codes[40], codes[46]] == [16, 8, 4]
+    bm = sel["block_max"][0, 0]
+    assert bm[0] == 127 * max(codes[8:16])          # tokens 8..15 only
+    assert bm[1] == 127 * max(codes[16:32])
+    assert bm[2] == 127 * max(codes[32:44])         # tokens 44..47 are in the window
+    assert bm[3] == INT32_MIN                       # block 3 lies in the window
+    assert codes[3] == 127 and codes[50] == 127
+
+
+def test_no_candidates_when_context_fits_sink_and_window():
+    rng = np.random.default_rng(6)
+    case = random_case(rng, B=2, hq=4, hkv=1, D=8, lens=(40, 24), page=16)
+    d = dims_for(case, 4, 1, 8, chunk=32, block=16, k1=4, k2=4, sink=16, window=24)
+    kq, sc, sel, out, lse = run_all(d, case)
+    assert sel["n_blocks"].tolist() == [[0], [0]] and sel["n_chunks"].tolist() == [[0], [0]]
+    assert (sel["block_idx"] == -1).all()
+    od, ld = oracle.dense(d, bf16_bits(case["q"]), bf16_bits(case["k"]), bf16_bits(case["v"]),
+                          case["pt"], case["lens"])
+    np.testing.assert_allclose(out, od, atol=1e-13)
+    np.testing.assert_allclose(lse, ld, atol=1e-13)
+
+
+# ---------------------------------------------------------------- attention
+
+def _softmax_attention(q, K, V, scale):
+    logits = (K.astype(np.float64) @ q.astype(np.float64)) * scale
+    return softmax(logits) @ V.astype(np.float64), logsumexp(logits)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_dense_matches_library_softmax(seed):
+    rng = np.random.default_rng(200 + seed)
+    case = random_case(rng, B=2, hq=4, hkv=2, D=8, lens=(37, 70), page=16, perm=True)
+    d = dims_for(case, 4, 2, 8)
+    out, lse = oracle.dense(d, bf16_bits(case["q"]), bf16_bits(case["k"]), bf16_bits(case["v"]),
+                            case["pt"], case["lens"])
+    for b in range(2):
+        for j in range(4):
+            h = j // 2
+            o, l = _softmax_attention(case["q"][b, j], case["ks"][b][h], case["vs"][b][h],
+                                      1 / math.sqrt(8))
+            np.testing.assert_allclose(out[b, j], o, rtol=0, atol=1e-12)
+            assert abs(lse[b, j] - l) < 1e-12
+
+
+def test_sink_and_window_special_case():
+    """K1 = K2 = 0 is attention over the sink tokens plus the sliding window."""
+    rng = np.random.default_rng(7)
+    case = random_case(rng, B=1, hq=4, hkv=1, D=8, lens=(300,), page=16)
+    d = dims_for(case, 4, 1, 8, k1=0, k2=0, sink=5, window=23)
+    _, _, sel, out, lse = run_all(d, case)
+    assert sel["block_idx"].size == 0 and sel["n_blocks"].tolist() == [[0]]
+    keep = list(range(5)) + list(range(300 - 23, 300))
+    for j in range(4):
+        o, l = _softmax_attention(case["q"][0, j], case["ks"][0][0][keep], case["vs"][0][0][keep],
+                                  1 / math.sqrt(8))
+        np.testing.assert_allclose(out[0, j], o, atol=1e-12)
+        assert abs(lse[0, j] - l) < 1e-12
+
+
+def test_selected_blocks_special_case():
+    """The attended set is sink + window + the kept blocks' candidate tokens."""
+    rng = np.random.default_rng(8)
+    case = random_case(rng, B=1, hq=4, hkv=1, D=8, lens=(333,), page=16)
+    d = dims_for(case, 4, 1, 8, chunk=32, block=16, k1=3, k2=4, sink=20, window=30)
+    _, _, sel, out, lse = run_all(d, case)
+    kept = [k for k in sel["block_idx"][0, 0] if k >= 0]
+    assert len(kept) == 4
+    toks = set(range(20)) | set(range(303, 333))
+    for k in kept:
+        toks |= {t for t in range(16 * k, 16 * k + 16) if 20 <= t < 303}
+    keep = sorted(toks)
+    for j in range(4):
+        o, l = _softmax_attention(case["q"][0, j], case["ks"][0][0][keep], case["vs"][0][0][keep],
+                                  1 / math.sqrt(8))
+        np.testing.assert_allclose(out[0, j], o, atol=1e-12)
+        assert abs(lse[0, j] - l) < 1e-12
+
+
+def test_everything_selected_equals_dense():
+    rng = np.random.default_rng(9)
+    case = random_case(rng, B=2, hq=8, hkv=2, D=16, lens=(500, 257), page=16, perm=True)
+    d = dims_for(case, 8, 2, 16, chunk=64, block=16, k1=100, k2=100, sink=7, window=9)
+    _, _, sel, out, lse = run_all(d, case)
+    od, ld = oracle.dense(d, bf16_bits(case["q"]), bf16_bits(case["k"]), bf16_bits(case["v"]),
+                          case["pt"], case["lens"])
+    np.testing.assert_allclose(out, od, atol=1e-12)
+    np.testing.assert_allclose(lse, ld, atol=1e-12)
+    r = oracle.recall(d, bf16_bits(case["q"]), bf16_bits(case["k"]), case["pt"], case["lens"],
+                      sel["block_idx"], sel["n_blocks"])
+    np.testing.assert_allclose(r, 1.0, atol=1e-13)
+
+
+def test_identical_keys_give_the_mean_of_values():
+    """All keys equal: the softmax is uniform over the attended set, out is the mean of
+    its values and lse = logit + log |T|."""
+    rng = np.random.default_rng(10)
+    n, D = 200, 8
+    key = to_bf16(rng.standard_normal(D))
+    ks = [np.tile(key, (1, n, 1)).astype(np.float32)]
+    vs = [to_bf16(rng.standard_normal((1, n, D)))]
+    kc, pt, ln = paged(ks, 16, 1)
+    vc, _, _ = paged(vs, 16, 1)
+    q = to_bf16(rng.standard_normal((1, 2, D)))
+    d = Dims(1, 2, 1, D, 16, pt.shape[1], kc.shape[0], 32, 16, 0, 0, 10, 15)
+    out, lse = oracle.attend(d, bf16_bits(q), bf16_bits(kc), bf16_bits(vc), pt, ln,
+                             np.zeros((1, 1, 0), np.int32), np.zeros((1, 1), np.int32))
+    keep = list(range(10)) + list(range(185, 200))
+    for j in range(2):
+        np.testing.assert_allclose(out[0, j], vs[0][0][keep].astype(np.float64).mean(0), atol=1e-13)
+        logit = float(np.dot(q[0, j].astype(np.float64), key.astype(np.float64))) / math.sqrt(D)
+        assert abs(lse[0, j] - (logit + math.log(len(keep)))) < 1e-12
+
+
+def test_recall_restriction_identity():
+    """R = sum over T of the dense probabilities = exp(lse_T - lse_all), and the sparse
+    output is the dense probabilities over T renormalised by R."""
+    rng = np.random.default_rng(11)
+    case = random_case(rng, B=1, hq=4, hkv=1, D=8, lens=(410,), page=16)
+    d = dims_for(case, 4, 1, 8, chunk=32, block=16, k1=4, k2=5, sink=16, window=32)
+    _, _, sel, out, lse = run_all(d, case)
+    qb, kb = bf16_bits(case["q"]), bf16_bits(case["k"])
+    _, ld = oracle.dense(d, qb, kb, bf16_bits(case["v"]), case["pt"], case["lens"])
+    r = oracle.recall(d, qb, kb, case["pt"], case["lens"], sel["block_idx"], sel["n_blocks"])
+    np.testing.assert_allclose(r, np.exp(lse - ld), rtol=1e-12)
+    assert np.all(r > 0) and np.all(r < 1)
+
+
+def test_tokens_past_the_end_are_ignored():
+    """Junk in the slots of a last page past N changes nothing."""
+    rng = np.random.default_rng(12)
+    case = random_case(rng, B=2, hq=4, hkv=1, D=8, lens=(101, 77), page=16)
+    d = dims_for(case, 4, 1, 8, chunk=32, block=16, k1=2, k2=3, sink=4, window=9)
+    res1 = run_all(d, case)
+    junk = dict(case, k=case["k"].copy(), v=case["v"].copy())
+    for b, n in enumerate(case["lens"]):
+        pg = case["pt"][b, (n - 1) // 16]
+        junk["k"][pg, :, (n % 16):, :] = 96.0
+        junk["v"][pg, :, (n % 16):, :] = -96.0
+    res2 = run_all(d, junk)
+    np.testing.assert_array_equal(res1[1], res2[1])
+    for key in ("block_idx", "chunk_idx", "block_max"):
+        np.testing.assert_array_equal(res1[2][key], res2[2][key])
+    np.testing.assert_array_equal(res1[3], res2[3])
