@@ -1,0 +1,226 @@
+/*
+ * hsa.h -- C ABI of libhsa: one decode step of hierarchically pruned, block-sparse
+ * attention over a paged KV cache with int8 per-channel-quantised keys, on one GB300
+ * GPU (sm_103a).
+ *
+ * The step (sources, by page title and section):
+ *   1. append the new token's key and value to its page and give the key its int8
+ *      codes with the stored channel scales;
+ *   2. fold the key scales into the query and quantise it (one scale per group of
+ *      query heads), score every candidate token exactly in int32 against the int8
+ *      keys -- "HCAttention: Extreme KV cache compression via heterogeneous attention
+ *      computing for LLMs", abstract and contribution list (quantised keys kept on the
+ *      GPU for a global approximate scoring; values fetched late);
+ *   3. module 1: cut the context into chunks, score each by its best token, keep the
+ *      top-K1; module 2: cut the survivors into 16-token blocks, keep the top-K2 --
+ *      InfiniteHiP article (163.com, "韩国通过卸载键值缓存节约英伟达GPU内存，实现18.95倍
+ *      解码加速"), section "实现 7.24 倍的端到端解码加速" (modular hierarchical pruning);
+ *   4. exact softmax attention over the attention sinks, the recent window and the
+ *      kept blocks, from the bf16 K/V, split over many CTAs and merged by log-sum-exp
+ *      -- "KV Cache 与长上下文推理", sections "KV Cache 回顾" (decode attention
+ *      equation) and "Token Eviction 与 Sparse Attention" (StreamingLLM sinks +
+ *      sliding window).
+ *
+ * Conventions shared by every call:
+ *  - Every pointer is a DEVICE pointer unless a flag below says otherwise. The caller
+ *    owns every buffer and the stream; the library never allocates or frees memory,
+ *    never synchronises (except hsa_read_device_error, which says so), and never
+ *    aborts or traps. `stream` is a cudaStream_t (NULL = legacy default stream).
+ *  - Paged cache layout: [num_pages][hkv][page_size=16][head_dim=128], bf16 for K and
+ *    V, int8 for the key codes; token t of sequence b lives in page
+ *    page_table[b * max_pages_per_seq + t / 16], slot t % 16. page_table is int32
+ *    [batch][max_pages_per_seq]; entries past a sequence's last page are never read.
+ *  - seq_lens int32 [batch]: N_b, the context INCLUDING the current token.
+ *  - Query q: bf16 [batch][hq][128]; query head j uses kv head j / (hq / hkv).
+ *  - Candidate region of sequence b: C_b = [sink, N_b - window) (empty when
+ *    N_b <= sink + window). Chunks [c*chunk, (c+1)*chunk) and blocks [16k, 16k+16)
+ *    are aligned to token 0; only their tokens inside C_b count, and a chunk or block
+ *    with no token in C_b is never selected.
+ *  - Attended set T_b = [0, min(sink,N)) u [max(N-window, min(sink,N)), N) u
+ *    (kept blocks n C_b).
+ *  - Ties in either module: the lower index wins. Index lists are ascending and padded
+ *    with -1.
+ *  - Key scales (int8 reading): s_c = f32(amax_c / 127) over the whole context of one
+ *    (sequence, kv head, channel); code = clamp(rint_half_even(f32(k / s_c)), +-127);
+ *    s_c = 0 gives code 0. Query: q'_{j,c} = f32(q_{j,c} s_c); A = max |q'| over the
+ *    group; sq = f32(A / 127); qq = clamp(rint_half_even(f32(q' / sq)), +-127).
+ *    Token score: max over the group of sum_c qq_{j,c} kq_{t,c} (exact int32).
+ *  - Workspace: caller-allocated device memory of at least hsa_workspace_bytes(d, op)
+ *    bytes, 256-byte aligned, ZERO-FILLED ONCE before its first use. Calls leave the
+ *    counters they use at zero again, so one workspace serves any number of calls,
+ *    but two calls that run at the same time must not share a workspace. Word 0 of
+ *    every workspace is a device error word (see hsa_read_device_error).
+ *  - Return value: HSA_OK or an HSA_ERR_* code; on error nothing was launched unless
+ *    the code is HSA_ERR_CUDA.
+ */
+#ifndef HSA_H_
+#define HSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum hsa_status {
+  HSA_OK = 0,
+  HSA_ERR_INVALID_ARG = 1,          /* null pointer, bad size, misaligned pointer */
+  HSA_ERR_UNSUPPORTED = 2,          /* head_dim != 128, page/block != 16, group not 1/2/4, ... */
+  HSA_ERR_CUDA = 3,                 /* a CUDA runtime call or a launch failed */
+  HSA_ERR_TIMEOUT = 4,              /* a bounded device wait ran out (reported by the error word) */
+  HSA_ERR_WORKSPACE_TOO_SMALL = 5,
+  HSA_ERR_DEVICE_CHECK = 6          /* a device-side bounds check failed (bad page-table entry) */
+};
+
+/* Problem descriptor. Only the fields an entry point uses need to be valid for it. */
+typedef struct hsa_dims {
+  int32_t batch;             /* sequences in the step (>= 1) */
+  int32_t hq;                /* query heads */
+  int32_t hkv;               /* key/value heads; hq % hkv == 0 and hq / hkv in {1, 2, 4} */
+  int32_t head_dim;          /* must be 128 */
+  int32_t page_size;         /* must be 16 */
+  int32_t max_pages_per_seq; /* row length of page_table (>= 1) */
+  int32_t num_pages;         /* pages in the pool; every page-table entry read must be < this */
+  int32_t chunk;             /* module-1 chunk length in tokens: a positive multiple of 16 */
+  int32_t block;             /* module-2 block length in tokens: must be 16 */
+  int32_t k1;                /* chunks kept by module 1 (>= 0) */
+  int32_t k2;                /* blocks kept by module 2 (>= 0) */
+  int32_t sink;              /* leading tokens always attended (>= 0) */
+  int32_t window;            /* trailing tokens always attended (>= 0) */
+  float sm_scale;            /* softmax scale of q.k; <= 0 selects 1/sqrt(head_dim) */
+  int32_t kv_on_host;        /* 1: the bf16 K/V caches given to hsa_attend, dense_decode,
+                                hsa_append_kv and hsa_decode_step are PINNED HOST memory
+                                (cudaHostAlloc / cudaHostRegister); the kernels read them
+                                through the mapped device aliases */
+} hsa_dims;
+
+/* Operation ids for hsa_workspace_bytes. */
+enum hsa_op {
+  HSA_OP_QUANTIZE = 0,
+  HSA_OP_SELECT = 1,
+  HSA_OP_ATTEND = 2,
+  HSA_OP_DENSE = 3,
+  HSA_OP_STEP = 4
+};
+
+/* Workspace bytes `op` needs for descriptor `d` (0 if `d` is invalid). */
+size_t hsa_workspace_bytes(const hsa_dims* d, int32_t op);
+
+/* Short English text for a status code (static storage). */
+const char* hsa_status_string(int32_t status);
+
+/*
+ * Key quantisation (HCAttention abstract: quantised keys kept on the GPU;
+ * "KV Cache 与长上下文推理", section "KV Cache 量化": INT8 keys).
+ *  mode 0 (FULL): k_scale[b][h][c] = f32(amax / 127) over tokens t < N_b, and the codes
+ *    of every token t < N_b; slots of a last page past N_b get code 0. Needs
+ *    HSA_OP_QUANTIZE workspace.
+ *  mode 1 (APPEND): codes of tokens [append_from, N_b) of every sequence with the
+ *    stored k_scale (append_from < 0: each sequence's last token); values beyond the
+ *    stored range saturate at +-127. Workspace may be NULL.
+ * k_cache: bf16 paged cache (device, or pinned host when d->kv_on_host). kq: int8
+ * paged codes, same layout. k_scale: f32 [batch][hkv][128].
+ */
+int32_t hsa_quantize_keys(const hsa_dims* d, const void* k_cache, const int32_t* page_table,
+                          const int32_t* seq_lens, int32_t mode, int32_t append_from,
+                          int8_t* kq, float* k_scale, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
+ * Decode-step append ("KV Cache 与长上下文推理", section "KV Cache 回顾": each step
+ * computes the new token's k and v and appends them to the cache). Writes k_new and
+ * v_new (bf16 [batch][hkv][128]) into slot N_b - 1 of each sequence's bf16 caches and
+ * the new key's int8 codes into kq with the stored k_scale (saturating).
+ */
+int32_t hsa_append_kv(const hsa_dims* d, const void* k_new, const void* v_new, void* k_cache,
+                      void* v_cache, int8_t* kq, const float* k_scale,
+                      const int32_t* page_table, const int32_t* seq_lens, void* stream);
+
+/*
+ * Scoring step alone: query folding/quantisation and the exact int32 scores, reduced to
+ * one maximum per 16-token block. block_max: int32 [batch][hkv][max_pages_per_seq];
+ * entries of blocks that hold a candidate token are written, all others are left
+ * untouched. (HCAttention: global approximate scoring over quantised keys.)
+ */
+int32_t hsa_score_blocks(const hsa_dims* d, const void* q, const int8_t* kq,
+                         const float* k_scale, const int32_t* page_table,
+                         const int32_t* seq_lens, int32_t* block_max, void* stream);
+
+/*
+ * The two pruning modules on precomputed block maxima (InfiniteHiP article, section
+ * "实现 7.24 倍的端到端解码加速"). chunk_idx int32 [batch][hkv][k1] (nullable),
+ * n_chunks int32 [batch][hkv] (nullable), block_idx int32 [batch][hkv][k2],
+ * n_blocks int32 [batch][hkv]. Limit: at most 53248 chunks per sequence
+ * (ceil(max_pages_per_seq * 16 / chunk)); larger returns HSA_ERR_UNSUPPORTED.
+ */
+int32_t hsa_prune(const hsa_dims* d, const int32_t* seq_lens, const int32_t* block_max,
+                  int32_t* chunk_idx, int32_t* n_chunks, int32_t* block_idx, int32_t* n_blocks,
+                  void* stream);
+
+/*
+ * hsa_score_blocks followed by hsa_prune, with the block maxima kept in the
+ * HSA_OP_SELECT workspace. chunk_idx and n_chunks are nullable.
+ */
+int32_t hsa_select(const hsa_dims* d, const void* q, const int8_t* kq, const float* k_scale,
+                   const int32_t* page_table, const int32_t* seq_lens, int32_t* chunk_idx,
+                   int32_t* n_chunks, int32_t* block_idx, int32_t* n_blocks, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
+ * Sparse decode attention over T_b ("KV Cache 与长上下文推理", section "KV Cache 回顾":
+ * softmax(q K^T / sqrt(d_k)) V, restricted to T_b). block_idx / n_blocks as produced by
+ * hsa_select (entries outside [0, n_blocks) are ignored; kept blocks are clipped to
+ * C_b). out: f32 [batch][hq][128]; lse: f32 [batch][hq] (natural log of the softmax
+ * denominator of the scaled logits; nullable). With d->kv_on_host the K/V pages are read
+ * from pinned host memory, only for the attended blocks (HCAttention: values stay in
+ * CPU memory and are fetched late; InfiniteHiP article, latency section: the attention
+ * kernel reads CPU memory while it runs).
+ */
+int32_t hsa_attend(const hsa_dims* d, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* page_table, const int32_t* seq_lens, const int32_t* block_idx,
+                   const int32_t* n_blocks, float* out, float* lse, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
+ * Dense decode attention over every token [0, N_b): the in-run comparison point (same
+ * kernels as hsa_attend with every block attended). Arguments as hsa_attend.
+ */
+int32_t dense_decode(const hsa_dims* d, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* page_table, const int32_t* seq_lens, float* out, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Inputs and outputs of one whole decode step. */
+typedef struct hsa_step_io {
+  const void* q;      /* bf16 [batch][hq][128] */
+  const void* k_new;  /* bf16 [batch][hkv][128]: the new token's key */
+  const void* v_new;  /* bf16 [batch][hkv][128]: the new token's value */
+  float* out;         /* f32 [batch][hq][128] */
+  float* lse;         /* f32 [batch][hq] (nullable) */
+  int32_t io_on_host; /* 1: the five pointers above are PINNED HOST memory; the call copies
+                         the inputs in and the outputs back on `stream` (the caller
+                         synchronises before reading them) */
+} hsa_step_io;
+
+/*
+ * One whole decode step: hsa_append_kv, hsa_select, hsa_attend on `stream`. seq_lens
+ * already count the new token. block_idx / n_blocks receive the selection (device,
+ * nullable: then the HSA_OP_STEP workspace holds it). Needs HSA_OP_STEP workspace.
+ */
+int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache, void* v_cache,
+                        int8_t* kq, const float* k_scale, const int32_t* page_table,
+                        const int32_t* seq_lens, int32_t* block_idx, int32_t* n_blocks,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Reads and clears the device error word of `workspace` after synchronising `stream`:
+ * *code receives HSA_OK, HSA_ERR_TIMEOUT or HSA_ERR_DEVICE_CHECK. This is the one call
+ * that synchronises.
+ */
+int32_t hsa_read_device_error(void* workspace, void* stream, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSA_H_ */

@@ -1,0 +1,462 @@
+// api.cu -- the C ABI of libhsa (declared in include/hsa.h): argument checks, workspace
+// layout, TMA descriptor encoding and kernel launches. No allocation, no synchronisation
+// (hsa_read_device_error excepted), no abort.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/hsa.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+using hsa::Shape;
+
+constexpr size_t kAlign = 256;
+constexpr size_t kErrBytes = 256;   // the error word sits at offset 0 of every workspace
+constexpr int kMaxSplits = 64;      // split-K partial buffers are sized for this many
+constexpr int kMaxBatch = 1024;
+constexpr int kMaxHkv = 64;
+
+inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+inline bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Structural checks of the descriptor; fills `s`. `need_prune` adds the module fields.
+int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
+  if (d == nullptr) return HSA_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->hq < 1 || d->hkv < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1)
+    return HSA_ERR_INVALID_ARG;
+  if (d->hq % d->hkv != 0) return HSA_ERR_INVALID_ARG;
+  if (d->head_dim != hsa::kHeadDim || d->page_size != hsa::kPage) return HSA_ERR_UNSUPPORTED;
+  const int g = d->hq / d->hkv;
+  if (g != 1 && g != 2 && g != 4) return HSA_ERR_UNSUPPORTED;
+  if (d->batch > kMaxBatch || d->hkv > kMaxHkv) return HSA_ERR_UNSUPPORTED;
+  if ((long long)d->num_pages * d->hkv * hsa::kPage > INT32_MAX ||
+      (long long)d->max_pages_per_seq * hsa::kPage > INT32_MAX / 2)
+    return HSA_ERR_UNSUPPORTED;
+  if (d->sink < 0 || d->window < 0 || d->k1 < 0 || d->k2 < 0) return HSA_ERR_INVALID_ARG;
+  if (need_prune) {
+    if (d->block != hsa::kPage) return HSA_ERR_UNSUPPORTED;
+    if (d->chunk <= 0 || d->chunk % d->block != 0) return HSA_ERR_INVALID_ARG;
+  }
+  if (!(d->sm_scale == d->sm_scale)) return HSA_ERR_INVALID_ARG;  // NaN
+  s.batch = d->batch;
+  s.hq = d->hq;
+  s.hkv = d->hkv;
+  s.group = g;
+  s.max_pages = d->max_pages_per_seq;
+  s.num_pages = d->num_pages;
+  s.chunk = d->chunk;
+  s.k1 = d->k1;
+  s.k2 = d->k2;
+  s.sink = d->sink;
+  s.window = d->window;
+  s.sm_scale = d->sm_scale > 0.0f ? d->sm_scale : 1.0f / std::sqrt((float)hsa::kHeadDim);
+  return HSA_OK;
+}
+
+// ---- workspace layouts
+size_t quantize_ws(const Shape& s) { return kErrBytes + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 4); }
+size_t select_ws(const Shape& s) { return kErrBytes + up((size_t)s.batch * s.hkv * s.max_pages * 4); }
+struct AttendLayout {
+  size_t counters, part_ml, part_o, end;
+};
+AttendLayout attend_layout(const Shape& s, size_t base) {
+  AttendLayout l;
+  l.counters = base;
+  l.part_ml = l.counters + up((size_t)s.batch * s.hkv * 4);
+  l.part_o = l.part_ml + up((size_t)s.batch * s.hq * kMaxSplits * 2 * 4);
+  l.end = l.part_o + up((size_t)s.batch * s.hq * kMaxSplits * hsa::kHeadDim * 4);
+  return l;
+}
+size_t attend_ws(const Shape& s) { return attend_layout(s, kErrBytes).end; }
+struct StepLayout {
+  size_t block_max, block_idx, n_blocks, q, k_new, v_new, out, lse;
+  AttendLayout att;
+  size_t end;
+};
+StepLayout step_layout(const Shape& s) {
+  StepLayout l;
+  l.block_max = kErrBytes;
+  l.block_idx = l.block_max + up((size_t)s.batch * s.hkv * s.max_pages * 4);
+  l.n_blocks = l.block_idx + up((size_t)s.batch * s.hkv * std::max(s.k2, 1) * 4);
+  l.q = l.n_blocks + up((size_t)s.batch * s.hkv * 4);
+  l.k_new = l.q + up((size_t)s.batch * s.hq * hsa::kHeadDim * 2);
+  l.v_new = l.k_new + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 2);
+  l.out = l.v_new + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 2);
+  l.lse = l.out + up((size_t)s.batch * s.hq * hsa::kHeadDim * 4);
+  l.att = attend_layout(s, l.lse + up((size_t)s.batch * s.hq * 4));
+  l.end = l.att.end;
+  return l;
+}
+
+int32_t check_ws(const Shape& s, void* ws, size_t bytes, size_t need) {
+  if (ws == nullptr || !aligned(ws, kAlign)) return HSA_ERR_INVALID_ARG;
+  if (bytes < need) return HSA_ERR_WORKSPACE_TOO_SMALL;
+  (void)s;
+  return HSA_OK;
+}
+
+// ---- device facts (cached per device)
+int num_sms() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  int v = cache[dev].load();
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    cache[dev].store(v);
+  }
+  return v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view of the int8 code cache: rows of 128 bytes, one per (page, head, slot); a box is
+// one (page, head) block of 16 rows, stored with the 128-byte swizzle.
+int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return HSA_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)hsa::kHeadDim,
+                        (cuuint64_t)s.num_pages * s.hkv * hsa::kPage};
+  cuuint64_t strides[1] = {(cuuint64_t)hsa::kHeadDim};
+  cuuint32_t box[2] = {(cuuint32_t)hsa::kHeadDim, (cuuint32_t)hsa::kPage};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(kq), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HSA_OK : HSA_ERR_CUDA;
+}
+
+// Device alias of a pinned host buffer (kv_on_host) or the pointer itself.
+int32_t kv_pointer(const hsa_dims* d, const void* p, const void** out) {
+  if (!d->kv_on_host) {
+    *out = p;
+    return HSA_OK;
+  }
+  void* dp = nullptr;
+  if (cudaHostGetDevicePointer(&dp, const_cast<void*>(p), 0) != cudaSuccess || dp == nullptr) {
+    cudaGetLastError();
+    return HSA_ERR_INVALID_ARG;
+  }
+  *out = dp;
+  return HSA_OK;
+}
+
+inline int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? HSA_OK : HSA_ERR_CUDA; }
+
+inline cudaStream_t as_stream(void* p) { return reinterpret_cast<cudaStream_t>(p); }
+
+int32_t do_score(const Shape& s, const void* q, const int8_t* kq, const float* k_scale,
+                 const int32_t* page_table, const int32_t* seq_lens, int32_t* block_max, int* err,
+                 cudaStream_t st) {
+  CUtensorMap map;
+  int32_t rc = encode_kq_map(s, kq, &map);
+  if (rc != HSA_OK) return rc;
+  return cuda_status(hsa::launch_score_blocks(s, map, q, k_scale, page_table, seq_lens, block_max,
+                                              err, num_sms(), st));
+}
+
+int32_t check_prune_fits(const Shape& s) {
+  const long long n1max = ((long long)s.max_pages * hsa::kPage + s.chunk - 1) / s.chunk;
+  if (n1max > hsa::prune_max_chunks()) return HSA_ERR_UNSUPPORTED;
+  if (hsa::prune_smem_bytes(s) > 227 * 1024) return HSA_ERR_UNSUPPORTED;
+  return HSA_OK;
+}
+
+int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, const void* k,
+                  const void* v, const int32_t* pt, const int32_t* lens, const int32_t* bidx,
+                  const int32_t* nb, float* out, float* lse, char* ws, const AttendLayout& l,
+                  cudaStream_t st) {
+  const void* kd = nullptr;
+  const void* vd = nullptr;
+  int32_t rc = kv_pointer(d, k, &kd);
+  if (rc != HSA_OK) return rc;
+  rc = kv_pointer(d, v, &vd);
+  if (rc != HSA_OK) return rc;
+  const bool host = d->kv_on_host != 0;
+  hsa::AttendBuffers buf;
+  buf.counters = reinterpret_cast<int*>(ws + l.counters);
+  buf.part_ml = reinterpret_cast<float*>(ws + l.part_ml);
+  buf.part_o = reinterpret_cast<float*>(ws + l.part_o);
+  buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(s, dense, host, num_sms()));
+  return cuda_status(hsa::launch_attend(s, dense, host, q, kd, vd, pt, lens, bidx, nb, out, lse,
+                                        buf, reinterpret_cast<int*>(ws), st));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t hsa_workspace_bytes(const hsa_dims* d, int32_t op) {
+  Shape s;
+  const bool prune = op == HSA_OP_SELECT || op == HSA_OP_STEP;
+  if (check_dims(d, s, prune) != HSA_OK) return 0;
+  switch (op) {
+    case HSA_OP_QUANTIZE: return quantize_ws(s);
+    case HSA_OP_SELECT: return select_ws(s);
+    case HSA_OP_ATTEND:
+    case HSA_OP_DENSE: return attend_ws(s);
+    case HSA_OP_STEP: return step_layout(s).end;
+    default: return 0;
+  }
+}
+
+const char* hsa_status_string(int32_t status) {
+  switch (status) {
+    case HSA_OK: return "ok";
+    case HSA_ERR_INVALID_ARG: return "invalid argument";
+    case HSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case HSA_ERR_CUDA: return "CUDA error";
+    case HSA_ERR_TIMEOUT: return "device wait timed out";
+    case HSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case HSA_ERR_DEVICE_CHECK: return "device bounds check failed";
+    default: return "unknown status";
+  }
+}
+
+int32_t hsa_quantize_keys(const hsa_dims* d, const void* k_cache, const int32_t* page_table,
+                          const int32_t* seq_lens, int32_t mode, int32_t append_from,
+                          int8_t* kq, float* k_scale, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, false);
+  if (rc != HSA_OK) return rc;
+  if (!k_cache || !page_table || !seq_lens || !kq || !k_scale) return HSA_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(kq, 16) || !aligned(k_scale, 16)) return HSA_ERR_INVALID_ARG;
+  if (mode != 0 && mode != 1) return HSA_ERR_INVALID_ARG;
+  const void* kd = nullptr;
+  rc = kv_pointer(d, k_cache, &kd);
+  if (rc != HSA_OK) return rc;
+  cudaStream_t st = as_stream(stream);
+  if (mode == 0) {
+    rc = check_ws(s, workspace, workspace_bytes, quantize_ws(s));
+    if (rc != HSA_OK) return rc;
+    char* ws = static_cast<char*>(workspace);
+    unsigned* amax = reinterpret_cast<unsigned*>(ws + kErrBytes);
+    int* err = reinterpret_cast<int*>(ws);
+    cudaError_t e = cudaMemsetAsync(amax, 0, (size_t)s.batch * s.hkv * hsa::kHeadDim * 4, st);
+    if (e == cudaSuccess) e = hsa::launch_key_amax(s, kd, page_table, seq_lens, amax, err, st);
+    if (e == cudaSuccess)
+      e = hsa::launch_key_codes(s, kd, page_table, seq_lens, amax, nullptr, k_scale, 0, true, kq,
+                                err, st);
+    return cuda_status(e);
+  }
+  if (append_from >= s.max_pages * hsa::kPage) return HSA_ERR_INVALID_ARG;
+  int* err = nullptr;
+  if (workspace != nullptr) {
+    if (!aligned(workspace, kAlign) || workspace_bytes < kErrBytes) return HSA_ERR_INVALID_ARG;
+    err = static_cast<int*>(workspace);
+  }
+  return cuda_status(hsa::launch_key_codes(s, kd, page_table, seq_lens, nullptr, k_scale, nullptr,
+                                           append_from, false, kq, err, st));
+}
+
+int32_t hsa_append_kv(const hsa_dims* d, const void* k_new, const void* v_new, void* k_cache,
+                      void* v_cache, int8_t* kq, const float* k_scale,
+                      const int32_t* page_table, const int32_t* seq_lens, void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, false);
+  if (rc != HSA_OK) return rc;
+  if (!k_new || !v_new || !k_cache || !v_cache || !kq || !k_scale || !page_table || !seq_lens)
+    return HSA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(kq, 16))
+    return HSA_ERR_INVALID_ARG;
+  const void* kd = nullptr;
+  const void* vd = nullptr;
+  rc = kv_pointer(d, k_cache, &kd);
+  if (rc != HSA_OK) return rc;
+  rc = kv_pointer(d, v_cache, &vd);
+  if (rc != HSA_OK) return rc;
+  return cuda_status(hsa::launch_append_kv(s, k_new, v_new, const_cast<void*>(kd),
+                                           const_cast<void*>(vd), kq, k_scale, page_table,
+                                           seq_lens, nullptr, as_stream(stream)));
+}
+
+int32_t hsa_score_blocks(const hsa_dims* d, const void* q, const int8_t* kq,
+                         const float* k_scale, const int32_t* page_table,
+                         const int32_t* seq_lens, int32_t* block_max, void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, false);
+  if (rc != HSA_OK) return rc;
+  if (!q || !kq || !k_scale || !page_table || !seq_lens || !block_max) return HSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kq, 16) || !aligned(k_scale, 16)) return HSA_ERR_INVALID_ARG;
+  return do_score(s, q, kq, k_scale, page_table, seq_lens, block_max, nullptr, as_stream(stream));
+}
+
+int32_t hsa_prune(const hsa_dims* d, const int32_t* seq_lens, const int32_t* block_max,
+                  int32_t* chunk_idx, int32_t* n_chunks, int32_t* block_idx, int32_t* n_blocks,
+                  void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, true);
+  if (rc != HSA_OK) return rc;
+  if (!seq_lens || !block_max || !n_blocks || (!block_idx && s.k2 > 0)) return HSA_ERR_INVALID_ARG;
+  rc = check_prune_fits(s);
+  if (rc != HSA_OK) return rc;
+  return cuda_status(hsa::launch_prune(s, seq_lens, block_max, chunk_idx, n_chunks, block_idx,
+                                       n_blocks, nullptr, as_stream(stream)));
+}
+
+int32_t hsa_select(const hsa_dims* d, const void* q, const int8_t* kq, const float* k_scale,
+                   const int32_t* page_table, const int32_t* seq_lens, int32_t* chunk_idx,
+                   int32_t* n_chunks, int32_t* block_idx, int32_t* n_blocks, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, true);
+  if (rc != HSA_OK) return rc;
+  if (!q || !kq || !k_scale || !page_table || !seq_lens || !n_blocks || (!block_idx && s.k2 > 0))
+    return HSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kq, 16) || !aligned(k_scale, 16)) return HSA_ERR_INVALID_ARG;
+  rc = check_prune_fits(s);
+  if (rc != HSA_OK) return rc;
+  rc = check_ws(s, workspace, workspace_bytes, select_ws(s));
+  if (rc != HSA_OK) return rc;
+  char* ws = static_cast<char*>(workspace);
+  int* err = reinterpret_cast<int*>(ws);
+  int32_t* bm = reinterpret_cast<int32_t*>(ws + kErrBytes);
+  cudaStream_t st = as_stream(stream);
+  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, err, st);
+  if (rc != HSA_OK) return rc;
+  return cuda_status(
+      hsa::launch_prune(s, seq_lens, bm, chunk_idx, n_chunks, block_idx, n_blocks, err, st));
+}
+
+int32_t hsa_attend(const hsa_dims* d, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* page_table, const int32_t* seq_lens, const int32_t* block_idx,
+                   const int32_t* n_blocks, float* out, float* lse, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, false);
+  if (rc != HSA_OK) return rc;
+  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !n_blocks || !out ||
+      (!block_idx && s.k2 > 0))
+    return HSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return HSA_ERR_INVALID_ARG;
+  rc = check_ws(s, workspace, workspace_bytes, attend_ws(s));
+  if (rc != HSA_OK) return rc;
+  char* ws = static_cast<char*>(workspace);
+  return do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks,
+                   out, lse, ws, attend_layout(s, kErrBytes), as_stream(stream));
+}
+
+int32_t dense_decode(const hsa_dims* d, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* page_table, const int32_t* seq_lens, float* out, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, false);
+  if (rc != HSA_OK) return rc;
+  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !out) return HSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return HSA_ERR_INVALID_ARG;
+  rc = check_ws(s, workspace, workspace_bytes, attend_ws(s));
+  if (rc != HSA_OK) return rc;
+  char* ws = static_cast<char*>(workspace);
+  return do_attend(d, s, true, q, k_cache, v_cache, page_table, seq_lens, nullptr, nullptr, out,
+                   lse, ws, attend_layout(s, kErrBytes), as_stream(stream));
+}
+
+int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache, void* v_cache,
+                        int8_t* kq, const float* k_scale, const int32_t* page_table,
+                        const int32_t* seq_lens, int32_t* block_idx, int32_t* n_blocks,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, true);
+  if (rc != HSA_OK) return rc;
+  if (!io || !io->q || !io->k_new || !io->v_new || !io->out || !k_cache || !v_cache || !kq ||
+      !k_scale || !page_table || !seq_lens)
+    return HSA_ERR_INVALID_ARG;
+  if (!aligned(io->q, 16) || !aligned(io->k_new, 16) || !aligned(io->v_new, 16) ||
+      !aligned(io->out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(kq, 16) || !aligned(k_scale, 16))
+    return HSA_ERR_INVALID_ARG;
+  rc = check_prune_fits(s);
+  if (rc != HSA_OK) return rc;
+  const StepLayout l = step_layout(s);
+  rc = check_ws(s, workspace, workspace_bytes, l.end);
+  if (rc != HSA_OK) return rc;
+  char* ws = static_cast<char*>(workspace);
+  int* err = reinterpret_cast<int*>(ws);
+  cudaStream_t st = as_stream(stream);
+  const void* q = io->q;
+  const void* kn = io->k_new;
+  const void* vn = io->v_new;
+  float* out = io->out;
+  float* lse = io->lse;
+  const size_t qb = (size_t)s.batch * s.hq * hsa::kHeadDim * 2;
+  const size_t kvb = (size_t)s.batch * s.hkv * hsa::kHeadDim * 2;
+  if (io->io_on_host) {
+    cudaError_t e = cudaMemcpyAsync(ws + l.q, io->q, qb, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + l.k_new, io->k_new, kvb, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + l.v_new, io->v_new, kvb, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return HSA_ERR_CUDA;
+    q = ws + l.q;
+    kn = ws + l.k_new;
+    vn = ws + l.v_new;
+    out = reinterpret_cast<float*>(ws + l.out);
+    lse = io->lse ? reinterpret_cast<float*>(ws + l.lse) : nullptr;
+  }
+  const void* kd = nullptr;
+  const void* vd = nullptr;
+  rc = kv_pointer(d, k_cache, &kd);
+  if (rc != HSA_OK) return rc;
+  rc = kv_pointer(d, v_cache, &vd);
+  if (rc != HSA_OK) return rc;
+  cudaError_t e = hsa::launch_append_kv(s, kn, vn, const_cast<void*>(kd), const_cast<void*>(vd),
+                                        kq, k_scale, page_table, seq_lens, err, st);
+  if (e != cudaSuccess) return HSA_ERR_CUDA;
+  int32_t* bm = reinterpret_cast<int32_t*>(ws + l.block_max);
+  int32_t* bidx = block_idx ? block_idx : reinterpret_cast<int32_t*>(ws + l.block_idx);
+  int32_t* nb = n_blocks ? n_blocks : reinterpret_cast<int32_t*>(ws + l.n_blocks);
+  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, err, st);
+  if (rc != HSA_OK) return rc;
+  e = hsa::launch_prune(s, seq_lens, bm, nullptr, nullptr, bidx, nb, err, st);
+  if (e != cudaSuccess) return HSA_ERR_CUDA;
+  rc = do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, bidx, nb, out, lse, ws,
+                 l.att, st);
+  if (rc != HSA_OK) return rc;
+  if (io->io_on_host) {
+    e = cudaMemcpyAsync(io->out, out, (size_t)s.batch * s.hq * hsa::kHeadDim * 4,
+                        cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && io->lse)
+      e = cudaMemcpyAsync(io->lse, lse, (size_t)s.batch * s.hq * 4, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return HSA_ERR_CUDA;
+  }
+  return HSA_OK;
+}
+
+int32_t hsa_read_device_error(void* workspace, void* stream, int32_t* code) {
+  if (workspace == nullptr || code == nullptr || !aligned(workspace, kAlign))
+    return HSA_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  int v = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return HSA_ERR_CUDA;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HSA_ERR_CUDA;
+  if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return HSA_ERR_CUDA;
+  *code = v;
+  return HSA_OK;
+}
+
+}  // extern "C"

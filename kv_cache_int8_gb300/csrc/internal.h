@@ -1,0 +1,56 @@
+// internal.h -- launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace hsa {
+
+// Problem sizes copied out of the public descriptor after validation.
+struct Shape {
+  int batch, hq, hkv, group, max_pages, num_pages;
+  int chunk, k1, k2, sink, window;
+  float sm_scale;  // resolved (> 0)
+};
+
+// ---- quantize.cu
+cudaError_t launch_key_amax(const Shape& s, const void* k_cache, const int32_t* page_table,
+                            const int32_t* seq_lens, unsigned* amax_bits, int* err,
+                            cudaStream_t st);
+cudaError_t launch_key_codes(const Shape& s, const void* k_cache, const int32_t* page_table,
+                             const int32_t* seq_lens, const unsigned* amax_bits,
+                             const float* k_scale_in, float* k_scale_out, int append_from,
+                             bool full, int8_t* kq, int* err, cudaStream_t st);
+cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_new,
+                             void* k_cache, void* v_cache, int8_t* kq, const float* k_scale,
+                             const int32_t* page_table, const int32_t* seq_lens, int* err,
+                             cudaStream_t st);
+
+// ---- select.cu
+cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const void* q,
+                                const float* k_scale, const int32_t* page_table,
+                                const int32_t* seq_lens, int32_t* block_max, int* err,
+                                int num_sms, cudaStream_t st);
+cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t* block_max,
+                         int32_t* chunk_idx, int32_t* n_chunks, int32_t* block_idx,
+                         int32_t* n_blocks, int* err, cudaStream_t st);
+int prune_max_chunks();
+size_t prune_smem_bytes(const Shape& s);
+
+// ---- attend.cu
+struct AttendBuffers {
+  float* part_ml;   // [B][Hq][nsplit] (m, l) pairs
+  float* part_o;    // [B][Hq][nsplit][128]
+  int* counters;    // [B][Hkv]
+  int nsplit;
+};
+int attend_splits(const Shape& s, bool dense, bool host, int num_sms);
+cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
+                          const void* k_cache, const void* v_cache, const int32_t* page_table,
+                          const int32_t* seq_lens, const int32_t* block_idx,
+                          const int32_t* n_blocks, float* out, float* lse,
+                          const AttendBuffers& buf, int* err, cudaStream_t st);
+
+}  // namespace hsa

@@ -1,0 +1,215 @@
+// quantize.cu -- int8 per-channel key codes: full-context scales, codes, decode-step append.
+//
+// Source: "HCAttention: Extreme KV cache compression via heterogeneous attention computing
+// for LLMs", abstract and contribution list (keys are quantised and kept on the GPU for
+// global scoring); "KV Cache 与长上下文推理", section "KV Cache 量化" (INT8 keys) and
+// section "KV Cache 回顾" (each decode step appends the new token's k, v).
+//
+// Reading: one scale per (sequence, kv head, channel) over the whole context,
+// s = f32(amax / 127); code = clamp(rint_half_even(f32(k / s)), -127, 127); s = 0 -> 0.
+// All decisions are taken in IEEE fp32 (__fdiv_rn, no fast math).
+//
+// Data: a CTA owns one (sequence, kv head) and a run of pages; thread t owns token slot
+// t / 16 and the 8 channels [8 (t % 16), 8 (t % 16) + 8) of every page it visits, so each
+// warp reads 512 contiguous bytes of bf16 per page with 16-byte loads.
+#include "common.cuh"
+#include "internal.h"
+
+namespace hsa {
+namespace {
+
+constexpr int kThreads = 256;        // 16 slots x 16 channel groups of 8
+constexpr int kPagesPerCta = 32;
+
+__device__ __forceinline__ bool seq_ok(int n, int max_pages) {
+  return n >= 0 && n <= max_pages * kPage;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float f[8]) {
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+  f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+  f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+
+__device__ __forceinline__ uint2 pack_codes(const int c[8]) {
+  uint2 r;
+  r.x = (c[0] & 0xFF) | ((c[1] & 0xFF) << 8) | ((c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
+  r.y = (c[4] & 0xFF) | ((c[5] & 0xFF) << 8) | ((c[6] & 0xFF) << 16) | ((uint32_t)(c[7] & 0xFF) << 24);
+  return r;
+}
+
+// Pass 1 of full quantisation: amax per (b, h, channel) over tokens t < N_b, as the bit
+// pattern of a non-negative float (ordered like the value), merged with atomicMax.
+__global__ void __launch_bounds__(kThreads) key_amax_kernel(
+    const __nv_bfloat16* __restrict__ k_cache, const int32_t* __restrict__ page_table,
+    const int32_t* __restrict__ seq_lens, unsigned* __restrict__ amax_bits, int hkv,
+    int max_pages, int num_pages, int* err) {
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int slot = threadIdx.x >> 4, grp = threadIdx.x & 15;
+  const int n = seq_lens[b];
+  __shared__ unsigned am[kHeadDim];
+  if (threadIdx.x < kHeadDim) am[threadIdx.x] = 0u;
+  __syncthreads();
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) mx[i] = 0.0f;
+  if (seq_ok(n, max_pages)) {
+    const int p0 = blockIdx.x * kPagesPerCta;
+    const int p1 = min(p0 + kPagesPerCta, (n + kPage - 1) / kPage);
+    for (int p = p0; p < p1; p++) {
+      const int t = p * kPage + slot;
+      if (t >= n) continue;
+      const int page = page_table[(size_t)b * max_pages + p];
+      if (page < 0 || page >= num_pages) {
+        set_error(err, kDevErrCheck);
+        continue;
+      }
+      const size_t off = (((size_t)page * hkv + h) * kPage + slot) * kHeadDim + grp * 8;
+      float f[8];
+      unpack8(ldg128_nc(k_cache + off), f);
+#pragma unroll
+      for (int i = 0; i < 8; i++) mx[i] = fmaxf(mx[i], fabsf(f[i]));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i++) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 16));
+  if ((threadIdx.x & 31) < 16) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) atomicMax(&am[grp * 8 + i], __float_as_uint(mx[i]));
+  }
+  __syncthreads();
+  if (threadIdx.x < kHeadDim && am[threadIdx.x] != 0u)
+    atomicMax(&amax_bits[((size_t)b * hkv + h) * kHeadDim + threadIdx.x], am[threadIdx.x]);
+}
+
+// Pass 2 (full) or append: codes of tokens [t_begin, N_b) with per-channel scales
+// (full: s = f32(amax / 127), also stored; append: the stored scales). Full mode zeroes
+// the codes of last-page slots past N_b.
+__global__ void __launch_bounds__(kThreads) key_codes_kernel(
+    const __nv_bfloat16* __restrict__ k_cache, const int32_t* __restrict__ page_table,
+    const int32_t* __restrict__ seq_lens, const unsigned* __restrict__ amax_bits,
+    const float* __restrict__ k_scale_in, float* __restrict__ k_scale_out, int append_from,
+    int full, int8_t* __restrict__ kq, int hkv, int max_pages, int num_pages, int* err) {
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int slot = threadIdx.x >> 4, grp = threadIdx.x & 15;
+  const int n = seq_lens[b];
+  if (!seq_ok(n, max_pages)) {
+    if (threadIdx.x == 0) set_error(err, kDevErrCheck);
+    return;
+  }
+  const size_t sbase = ((size_t)b * hkv + h) * kHeadDim + grp * 8;
+  float s[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++)
+    s[i] = full ? __fdiv_rn(__uint_as_float(amax_bits[sbase + i]), 127.0f) : k_scale_in[sbase + i];
+  if (full && blockIdx.x == 0 && slot == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) k_scale_out[sbase + i] = s[i];
+  }
+  int t_begin = 0;
+  if (!full) t_begin = append_from < 0 ? n - 1 : append_from;
+  t_begin = max(t_begin, 0);
+  const int p_begin = t_begin / kPage;
+  const int p0 = p_begin + blockIdx.x * kPagesPerCta;
+  const int p1 = min(p0 + kPagesPerCta, (n + kPage - 1) / kPage);
+  for (int p = p0; p < p1; p++) {
+    const int t = p * kPage + slot;
+    if (t < t_begin) continue;
+    const int page = page_table[(size_t)b * max_pages + p];
+    if (page < 0 || page >= num_pages) {
+      set_error(err, kDevErrCheck);
+      continue;
+    }
+    const size_t off = (((size_t)page * hkv + h) * kPage + slot) * kHeadDim + grp * 8;
+    int c[8];
+    if (t < n) {
+      float f[8];
+      unpack8(ldg128_nc(k_cache + off), f);
+#pragma unroll
+      for (int i = 0; i < 8; i++) c[i] = int8_code(f[i], s[i]);
+    } else {
+      if (!full) continue;
+#pragma unroll
+      for (int i = 0; i < 8; i++) c[i] = 0;
+    }
+    *reinterpret_cast<uint2*>(kq + off) = pack_codes(c);
+  }
+}
+
+// Decode-step append: slot N_b - 1 of every sequence receives k_new, v_new and the codes
+// of k_new under the stored scales. One CTA per sequence, thread = (head, channel group).
+__global__ void append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                 __nv_bfloat16* k_cache, __nv_bfloat16* v_cache, int8_t* kq,
+                                 const float* __restrict__ k_scale,
+                                 const int32_t* __restrict__ page_table,
+                                 const int32_t* __restrict__ seq_lens, int hkv, int max_pages,
+                                 int num_pages, int* err) {
+  const int b = blockIdx.x;
+  const int h = threadIdx.x >> 4, grp = threadIdx.x & 15;
+  if (h >= hkv) return;
+  const int n = seq_lens[b];
+  if (n < 1 || n > max_pages * kPage) {
+    set_error(err, kDevErrCheck);
+    return;
+  }
+  const int t = n - 1;
+  const int page = page_table[(size_t)b * max_pages + t / kPage];
+  if (page < 0 || page >= num_pages) {
+    set_error(err, kDevErrCheck);
+    return;
+  }
+  const size_t off = (((size_t)page * hkv + h) * kPage + t % kPage) * kHeadDim + grp * 8;
+  const size_t src = ((size_t)b * hkv + h) * (kHeadDim / 8) + grp;
+  const uint4 kv = k_new[src];
+  *reinterpret_cast<uint4*>(k_cache + off) = kv;
+  *reinterpret_cast<uint4*>(v_cache + off) = v_new[src];
+  float f[8];
+  unpack8(kv, f);
+  const float* s = k_scale + ((size_t)b * hkv + h) * kHeadDim + grp * 8;
+  int c[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) c[i] = int8_code(f[i], s[i]);
+  *reinterpret_cast<uint2*>(kq + off) = pack_codes(c);
+}
+
+}  // namespace
+
+cudaError_t launch_key_amax(const Shape& s, const void* k_cache, const int32_t* page_table,
+                            const int32_t* seq_lens, unsigned* amax_bits, int* err,
+                            cudaStream_t st) {
+  dim3 grid((s.max_pages + kPagesPerCta - 1) / kPagesPerCta, s.hkv, s.batch);
+  key_amax_kernel<<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(k_cache),
+                                             page_table, seq_lens, amax_bits, s.hkv, s.max_pages,
+                                             s.num_pages, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_key_codes(const Shape& s, const void* k_cache, const int32_t* page_table,
+                             const int32_t* seq_lens, const unsigned* amax_bits,
+                             const float* k_scale_in, float* k_scale_out, int append_from,
+                             bool full, int8_t* kq, int* err, cudaStream_t st) {
+  int pages = s.max_pages;
+  if (!full) pages = append_from < 0 ? 1 : s.max_pages - append_from / kPage;
+  if (pages <= 0) return cudaSuccess;
+  dim3 grid((pages + kPagesPerCta - 1) / kPagesPerCta, s.hkv, s.batch);
+  key_codes_kernel<<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(k_cache),
+                                              page_table, seq_lens, amax_bits, k_scale_in,
+                                              k_scale_out, append_from, full ? 1 : 0, kq, s.hkv,
+                                              s.max_pages, s.num_pages, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_new,
+                             void* k_cache, void* v_cache, int8_t* kq, const float* k_scale,
+                             const int32_t* page_table, const int32_t* seq_lens, int* err,
+                             cudaStream_t st) {
+  const int threads = ((s.hkv * 16 + 31) / 32) * 32;
+  append_kv_kernel<<<s.batch, threads, 0, st>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+      static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), kq, k_scale,
+      page_table, seq_lens, s.hkv, s.max_pages, s.num_pages, err);
+  return cudaGetLastError();
+}
+
+}  // namespace hsa

@@ -1,0 +1,230 @@
+"""Thin ctypes binding of libhsa (``include/hsa.h``), same names as the C ABI.
+
+Arguments are marshalled only: torch tensors become raw pointers, the current torch
+stream becomes the ``void* stream`` argument, and a nonzero status raises ``HsaError``.
+Every step of the decode path runs in the CUDA library; nothing here computes. When the
+library is missing or fails to load, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libhsa.so")
+
+HSA_OK = 0
+HSA_ERR_INVALID_ARG = 1
+HSA_ERR_UNSUPPORTED = 2
+HSA_ERR_CUDA = 3
+HSA_ERR_TIMEOUT = 4
+HSA_ERR_WORKSPACE_TOO_SMALL = 5
+HSA_ERR_DEVICE_CHECK = 6
+
+HSA_OP_QUANTIZE = 0
+HSA_OP_SELECT = 1
+HSA_OP_ATTEND = 2
+HSA_OP_DENSE = 3
+HSA_OP_STEP = 4
+
+# Every entry point declared in include/hsa.h.
+EXPORTS = (
+    "hsa_workspace_bytes", "hsa_status_string", "hsa_quantize_keys", "hsa_append_kv",
+    "hsa_score_blocks", "hsa_prune", "hsa_select", "hsa_attend", "dense_decode",
+    "hsa_decode_step", "hsa_read_device_error",
+)
+
+
+class HsaError(RuntimeError):
+    def __init__(self, name: str, code: int, text: str):
+        super().__init__(f"{name} failed: {text} (status {code})")
+        self.code = code
+
+
+class hsa_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "hq", "hkv", "head_dim", "page_size", "max_pages_per_seq", "num_pages",
+        "chunk", "block", "k1", "k2", "sink", "window")] + [
+        ("sm_scale", ctypes.c_float), ("kv_on_host", ctypes.c_int32)]
+
+
+class hsa_step_io(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("io_on_host", ctypes.c_int32)]
+
+
+@dataclasses.dataclass
+class Dims:
+    batch: int
+    hq: int
+    hkv: int
+    max_pages_per_seq: int
+    num_pages: int
+    chunk: int = 64
+    k1: int = 16
+    k2: int = 16
+    sink: int = 64
+    window: int = 256
+    head_dim: int = 128
+    page_size: int = 16
+    block: int = 16
+    sm_scale: float = 0.0
+    kv_on_host: bool = False
+
+    def c(self) -> hsa_dims:
+        return hsa_dims(self.batch, self.hq, self.hkv, self.head_dim, self.page_size,
+                        self.max_pages_per_seq, self.num_pages, self.chunk, self.block, self.k1,
+                        self.k2, self.sink, self.window, float(self.sm_scale),
+                        1 if self.kv_on_host else 0)
+
+
+_LIB = None
+
+
+def load(path: Optional[str] = None):
+    """Load libhsa.so (once). Raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"libhsa.so is not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    D = ctypes.POINTER(hsa_dims)
+    sig = {
+        "hsa_workspace_bytes": (SZ, [D, I32]),
+        "hsa_status_string": (ctypes.c_char_p, [I32]),
+        "hsa_quantize_keys": (I32, [D, P, P, P, I32, I32, P, P, P, SZ, P]),
+        "hsa_append_kv": (I32, [D, P, P, P, P, P, P, P, P, P]),
+        "hsa_score_blocks": (I32, [D, P, P, P, P, P, P, P]),
+        "hsa_prune": (I32, [D, P, P, P, P, P, P, P]),
+        "hsa_select": (I32, [D, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "hsa_attend": (I32, [D, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "dense_decode": (I32, [D, P, P, P, P, P, P, P, P, SZ, P]),
+        "hsa_decode_step": (I32, [D, ctypes.POINTER(hsa_step_io), P, P, P, P, P, P, P, P, P,
+                                  SZ, P]),
+        "hsa_read_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(name: str, rc: int) -> None:
+    if rc != HSA_OK:
+        raise HsaError(name, rc, load().hsa_status_string(rc).decode())
+
+
+def hsa_status_string(code: int) -> str:
+    return load().hsa_status_string(code).decode()
+
+
+def hsa_workspace_bytes(d: Dims, op: int) -> int:
+    cd = d.c()
+    return int(load().hsa_workspace_bytes(ctypes.byref(cd), op))
+
+
+def workspace(d: Dims, op: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace tensor of the size `op` needs (256-byte aligned storage)."""
+    n = hsa_workspace_bytes(d, op)
+    if n == 0:
+        raise HsaError("hsa_workspace_bytes", HSA_ERR_INVALID_ARG, "invalid descriptor")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def hsa_quantize_keys(d: Dims, k_cache, page_table, seq_lens, mode: int, append_from: int, kq,
+                      k_scale, ws=None, stream=None) -> None:
+    cd = d.c()
+    _check("hsa_quantize_keys", load().hsa_quantize_keys(
+        ctypes.byref(cd), _p(k_cache), _p(page_table), _p(seq_lens), mode, append_from, _p(kq),
+        _p(k_scale), _p(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def hsa_append_kv(d: Dims, k_new, v_new, k_cache, v_cache, kq, k_scale, page_table, seq_lens,
+                  stream=None) -> None:
+    cd = d.c()
+    _check("hsa_append_kv", load().hsa_append_kv(
+        ctypes.byref(cd), _p(k_new), _p(v_new), _p(k_cache), _p(v_cache), _p(kq), _p(k_scale),
+        _p(page_table), _p(seq_lens), _stream(stream)))
+
+
+def hsa_score_blocks(d: Dims, q, kq, k_scale, page_table, seq_lens, block_max,
+                     stream=None) -> None:
+    cd = d.c()
+    _check("hsa_score_blocks", load().hsa_score_blocks(
+        ctypes.byref(cd), _p(q), _p(kq), _p(k_scale), _p(page_table), _p(seq_lens),
+        _p(block_max), _stream(stream)))
+
+
+def hsa_prune(d: Dims, seq_lens, block_max, chunk_idx, n_chunks, block_idx, n_blocks,
+              stream=None) -> None:
+    cd = d.c()
+    _check("hsa_prune", load().hsa_prune(
+        ctypes.byref(cd), _p(seq_lens), _p(block_max), _p(chunk_idx), _p(n_chunks),
+        _p(block_idx), _p(n_blocks), _stream(stream)))
+
+
+def hsa_select(d: Dims, q, kq, k_scale, page_table, seq_lens, chunk_idx, n_chunks, block_idx,
+               n_blocks, ws, stream=None) -> None:
+    cd = d.c()
+    _check("hsa_select", load().hsa_select(
+        ctypes.byref(cd), _p(q), _p(kq), _p(k_scale), _p(page_table), _p(seq_lens),
+        _p(chunk_idx), _p(n_chunks), _p(block_idx), _p(n_blocks), _p(ws), ws.numel(),
+        _stream(stream)))
+
+
+def hsa_attend(d: Dims, q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks, out,
+               lse, ws, stream=None) -> None:
+    cd = d.c()
+    _check("hsa_attend", load().hsa_attend(
+        ctypes.byref(cd), _p(q), _p(k_cache), _p(v_cache), _p(page_table), _p(seq_lens),
+        _p(block_idx), _p(n_blocks), _p(out), _p(lse), _p(ws), ws.numel(), _stream(stream)))
+
+
+def dense_decode(d: Dims, q, k_cache, v_cache, page_table, seq_lens, out, lse, ws,
+                 stream=None) -> None:
+    cd = d.c()
+    _check("dense_decode", load().dense_decode(
+        ctypes.byref(cd), _p(q), _p(k_cache), _p(v_cache), _p(page_table), _p(seq_lens),
+        _p(out), _p(lse), _p(ws), ws.numel(), _stream(stream)))
+
+
+def hsa_decode_step(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_scale,
+                    page_table, seq_lens, block_idx, n_blocks, ws, io_on_host: bool = False,
+                    stream=None) -> None:
+    cd = d.c()
+    io = hsa_step_io(_p(q), _p(k_new), _p(v_new), _p(out), _p(lse), 1 if io_on_host else 0)
+    _check("hsa_decode_step", load().hsa_decode_step(
+        ctypes.byref(cd), ctypes.byref(io), _p(k_cache), _p(v_cache), _p(kq), _p(k_scale),
+        _p(page_table), _p(seq_lens), _p(block_idx), _p(n_blocks), _p(ws), ws.numel(),
+        _stream(stream)))
+
+
+def hsa_read_device_error(ws, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check("hsa_read_device_error", load().hsa_read_device_error(
+        _p(ws), _stream(stream), ctypes.byref(code)))
+    return int(code.value)

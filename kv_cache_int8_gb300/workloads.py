@@ -160,7 +160,7 @@ def make_workload(cfg: Config, seed: int = 0, device: str = "cpu",
             u = qf[b, h * G:(h + 1) * G].mean(dim=0)
             u = u / u.norm()
             pos = torch.randperm(lens[b], generator=gen, device=dev)[:n_plant]
-            noise = torch.randn((n_plant, D), generator=gen, device=dev, dtype=torch.float32)
+            noise = torch.randn((pos.numel(), D), generator=gen, device=dev, dtype=torch.float32)
             keys = (3.0 * u[None, :] + 0.3 * noise).to(torch.bfloat16)
             pos_cpu = pos.cpu().long()
             pages = page_table[b, (pos_cpu // PAGE)].long().to(dev)

@@ -1,0 +1,154 @@
+"""Shared helpers of the parity tests: run one decode step through the C ABI and through
+the CPU oracle on the same seeded inputs, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from kv_cache_int8_gb300 import hsa
+from kv_cache_int8_gb300 import workloads as W
+
+INT32_MIN = np.iinfo(np.int32).min
+
+# Output tolerance of the sparse and dense attention against the fp64 oracle.
+MAX_ABS_ERR = 1e-2
+MAX_REL_L2 = 5e-3
+
+
+def dims_pair(wl: dict, **over):
+    """(hsa.Dims, oracle.Dims) for a workload, with optional overrides of k1, k2, sink,
+    window, chunk."""
+    cfg = wl["config"]
+    p = dict(k1=cfg.k1, k2=cfg.k2, sink=cfg.sink, window=cfg.window, chunk=cfg.chunk)
+    p.update(over)
+    hd = hsa.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, max_pages_per_seq=wl["max_pages"],
+                  num_pages=wl["num_pages"], chunk=p["chunk"], k1=p["k1"], k2=p["k2"],
+                  sink=p["sink"], window=p["window"],
+                  kv_on_host=wl["k_cache"].device.type == "cpu" and wl["k_cache"].is_pinned())
+    od = oracle.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, head_dim=W.HEAD_DIM,
+                     page_size=W.PAGE, max_pages_per_seq=wl["max_pages"],
+                     num_pages=wl["num_pages"], chunk=p["chunk"], block=16, k1=p["k1"],
+                     k2=p["k2"], sink=p["sink"], window=p["window"])
+    return hd, od
+
+
+def to_cuda(wl: dict) -> dict:
+    out = dict(wl)
+    for key in ("q", "page_table", "seq_lens"):
+        out[key] = wl[key].cuda()
+    for key in ("k_cache", "v_cache"):
+        t = wl[key]
+        out[key] = t if (t.device.type == "cpu" and t.is_pinned()) else t.cuda()
+    return out
+
+
+def gpu_step(wl: dict, d: hsa.Dims, dense: bool = True) -> dict:
+    """Quantise the keys, score, prune, attend (and dense decode) through the C ABI."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv = d.batch, d.hq, d.hkv
+    kq = torch.zeros(wl["k_cache"].shape, dtype=torch.int8, device=dev)
+    k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
+    wq = hsa.workspace(d, hsa.HSA_OP_QUANTIZE)
+    hsa.hsa_quantize_keys(d, wl["k_cache"], wl["page_table"], wl["seq_lens"], 0, 0, kq, k_scale, wq)
+    bm = torch.full((B, Hkv, d.max_pages_per_seq), INT32_MIN, dtype=torch.int32, device=dev)
+    hsa.hsa_score_blocks(d, wl["q"], kq, k_scale, wl["page_table"], wl["seq_lens"], bm)
+    chunk_idx = torch.full((B, Hkv, max(d.k1, 1)), -7, dtype=torch.int32, device=dev)
+    n_chunks = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+    block_idx = torch.full((B, Hkv, max(d.k2, 1)), -7, dtype=torch.int32, device=dev)
+    n_blocks = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+    ws = hsa.workspace(d, hsa.HSA_OP_SELECT)
+    hsa.hsa_select(d, wl["q"], kq, k_scale, wl["page_table"], wl["seq_lens"], chunk_idx, n_chunks,
+                   block_idx, n_blocks, ws)
+    wa = hsa.workspace(d, hsa.HSA_OP_ATTEND)
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev)
+    hsa.hsa_attend(d, wl["q"], wl["k_cache"], wl["v_cache"], wl["page_table"], wl["seq_lens"],
+                   block_idx, n_blocks, out, lse, wa)
+    res = {"kq": kq, "k_scale": k_scale, "block_max": bm, "chunk_idx": chunk_idx[..., :d.k1],
+           "n_chunks": n_chunks, "block_idx": block_idx[..., :d.k2], "n_blocks": n_blocks,
+           "out": out, "lse": lse}
+    if dense:
+        wd = hsa.workspace(d, hsa.HSA_OP_DENSE)
+        out_d = torch.full_like(out, float("nan"))
+        lse_d = torch.full_like(lse, float("nan"))
+        hsa.dense_decode(d, wl["q"], wl["k_cache"], wl["v_cache"], wl["page_table"],
+                         wl["seq_lens"], out_d, lse_d, wd)
+        res["out_dense"], res["lse_dense"] = out_d, lse_d
+    torch.cuda.synchronize()
+    for name, w in (("quantize", wq), ("select", ws), ("attend", wa)):
+        assert hsa.hsa_read_device_error(w) == 0, f"device error word set by {name}"
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
+def host_arrays(wl: dict) -> dict:
+    return {
+        "q": W.to_numpy_bits(wl["q"]),
+        "k": W.to_numpy_bits(wl["k_cache"]),
+        "v": W.to_numpy_bits(wl["v_cache"]),
+        "pt": wl["page_table"].cpu().numpy(),
+        "lens": wl["seq_lens"].cpu().numpy(),
+    }
+
+
+def oracle_step(h: dict, od: oracle.Dims, bh_mask=None, qh_mask=None, dense: bool = True) -> dict:
+    kq, sc = oracle.quantize_keys(od, h["k"], h["pt"], h["lens"], bh_mask=bh_mask)
+    sel = oracle.select(od, h["q"], sc, kq, h["pt"], h["lens"], bh_mask=bh_mask,
+                        want_block_max=True)
+    out, lse = oracle.attend(od, h["q"], h["k"], h["v"], h["pt"], h["lens"], sel["block_idx"],
+                             sel["n_blocks"], qh_mask=qh_mask)
+    res = dict(sel, kq=kq, k_scale=sc, out=out, lse=lse)
+    if dense:
+        res["out_dense"], res["lse_dense"] = oracle.dense(od, h["q"], h["k"], h["v"], h["pt"],
+                                                          h["lens"], qh_mask=qh_mask)
+    return res
+
+
+def err_stats(got: np.ndarray, want: np.ndarray):
+    got = got.astype(np.float64)
+    diff = got - want
+    max_abs = float(np.abs(diff).max()) if diff.size else 0.0
+    denom = float(np.linalg.norm(want))
+    rel = float(np.linalg.norm(diff) / denom) if denom > 0 else float(np.linalg.norm(diff))
+    return max_abs, rel
+
+
+def assert_close(got, want, what: str):
+    max_abs, rel = err_stats(got, want)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    assert max_abs <= MAX_ABS_ERR and rel <= MAX_REL_L2, (
+        f"{what}: max|err| {max_abs:.3e} (bound {MAX_ABS_ERR}), rel L2 {rel:.3e} "
+        f"(bound {MAX_REL_L2})")
+    return max_abs, rel
+
+
+def logical_rows(arr: np.ndarray, pt: np.ndarray, lens, b: int, h: int) -> np.ndarray:
+    """[N_b][128] rows of (b, h) from a paged [P][Hkv][16][128] array."""
+    n = int(lens[b])
+    pages = pt[b, : (n + 15) // 16]
+    rows = arr[pages, h].reshape(-1, arr.shape[-1])
+    return rows[:n]
+
+
+def compare_step(g: dict, o: dict, h: dict, od: oracle.Dims, bh_pairs, dense: bool = True):
+    """Bit-exact integer outputs and toleranced float outputs on the (b, h) pairs given."""
+    G = od.hq // od.hkv
+    stats = []
+    for b, hh in bh_pairs:
+        np.testing.assert_array_equal(g["k_scale"][b, hh], o["k_scale"][b, hh])
+        np.testing.assert_array_equal(logical_rows(g["kq"], h["pt"], h["lens"], b, hh),
+                                      logical_rows(o["kq"], h["pt"], h["lens"], b, hh))
+        np.testing.assert_array_equal(g["block_max"][b, hh], o["block_max"][b, hh])
+        np.testing.assert_array_equal(g["chunk_idx"][b, hh], o["chunk_idx"][b, hh])
+        np.testing.assert_array_equal(g["n_chunks"][b, hh], o["n_chunks"][b, hh])
+        np.testing.assert_array_equal(g["block_idx"][b, hh], o["block_idx"][b, hh])
+        np.testing.assert_array_equal(g["n_blocks"][b, hh], o["n_blocks"][b, hh])
+        rows = slice(hh * G, (hh + 1) * G)
+        stats.append(assert_close(g["out"][b, rows], o["out"][b, rows], f"sparse out b{b} h{hh}"))
+        np.testing.assert_allclose(g["lse"][b, rows], o["lse"][b, rows], atol=2e-4, rtol=1e-5)
+        if dense:
+            stats.append(assert_close(g["out_dense"][b, rows], o["out_dense"][b, rows],
+                                      f"dense out b{b} h{hh}"))
+            np.testing.assert_allclose(g["lse_dense"][b, rows], o["lse_dense"][b, rows],
+                                       atol=2e-4, rtol=1e-5)
+    return stats

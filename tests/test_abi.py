@@ -1,0 +1,138 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports every entry point
+include/hsa.h declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "hsa.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc is needed to build libhsa.so")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_int8_gb300 import build, hsa
+    build.build()
+    return hsa
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_binding_exports():
+    from kv_cache_int8_gb300 import hsa
+    assert declared_functions() == sorted(hsa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    path = lib.LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, f"not exported: {missing}"
+    handle = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert getattr(handle, n) is not None
+
+
+def _dims(lib, **kw):
+    base = dict(batch=1, hq=32, hkv=8, max_pages_per_seq=8192, num_pages=8192, chunk=64, k1=256,
+                k2=128, sink=128, window=1024)
+    base.update(kw)
+    return lib.Dims(**base)
+
+
+def test_status_strings(lib):
+    assert lib.hsa_status_string(0) == "ok"
+    assert "workspace" in lib.hsa_status_string(lib.HSA_ERR_WORKSPACE_TOO_SMALL)
+    assert lib.hsa_status_string(999) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    d = _dims(lib)
+    for op in range(5):
+        assert lib.hsa_workspace_bytes(d, op) > 0
+    assert lib.hsa_workspace_bytes(d, 9) == 0
+    # block maxima of every (b, h, page) plus the error word
+    assert lib.hsa_workspace_bytes(d, lib.HSA_OP_SELECT) >= 8 * 8192 * 4 + 256
+    assert lib.hsa_workspace_bytes(_dims(lib, head_dim=64), 0) == 0
+    assert lib.hsa_workspace_bytes(_dims(lib, hq=12, hkv=8), 0) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=64), 2), (dict(page_size=32), 2), (dict(block=32), 2), (dict(hq=24), 2),
+    (dict(hq=30), 1), (dict(batch=0), 1), (dict(k1=-1), 1), (dict(window=-3), 1),
+    (dict(chunk=40), 1), (dict(chunk=0), 1), (dict(batch=2000), 2),
+])
+def test_select_rejects_bad_descriptors(lib, kw, code):
+    d = _dims(lib, **kw)
+    fake = 1 << 20  # never dereferenced: validation fails first
+    with pytest.raises(lib.HsaError) as e:
+        lib.hsa_select(d, fake, fake, fake, fake, fake, None, None, fake, fake,
+                       _FakeWs(fake, 1 << 40), stream=0)
+    assert e.value.code == code
+
+
+class _FakeWs:
+    def __init__(self, ptr, n):
+        self.ptr, self.n = ptr, n
+
+    def data_ptr(self):
+        return self.ptr
+
+    def numel(self):
+        return self.n
+
+
+def test_null_and_misaligned_pointers(lib):
+    d = _dims(lib)
+    ok = 1 << 20
+    with pytest.raises(lib.HsaError) as e:
+        lib.hsa_select(d, None, ok, ok, ok, ok, None, None, ok, ok, _FakeWs(ok, 1 << 40), stream=0)
+    assert e.value.code == lib.HSA_ERR_INVALID_ARG
+    with pytest.raises(lib.HsaError) as e:
+        lib.hsa_select(d, ok + 4, ok, ok, ok, ok, None, None, ok, ok, _FakeWs(ok, 1 << 40),
+                       stream=0)
+    assert e.value.code == lib.HSA_ERR_INVALID_ARG
+    with pytest.raises(lib.HsaError) as e:
+        lib.hsa_attend(d, ok, ok + 8, ok, ok, ok, ok, ok, ok, None, _FakeWs(ok, 1 << 40), stream=0)
+    assert e.value.code == lib.HSA_ERR_INVALID_ARG
+    with pytest.raises(lib.HsaError) as e:  # workspace not 256-byte aligned
+        lib.hsa_attend(d, ok, ok, ok, ok, ok, ok, ok, ok, None, _FakeWs(ok + 16, 1 << 40),
+                       stream=0)
+    assert e.value.code == lib.HSA_ERR_INVALID_ARG
+
+
+def test_workspace_too_small(lib):
+    d = _dims(lib)
+    ok = 1 << 20
+    need = lib.hsa_workspace_bytes(d, lib.HSA_OP_SELECT)
+    with pytest.raises(lib.HsaError) as e:
+        lib.hsa_select(d, ok, ok, ok, ok, ok, None, None, ok, ok, _FakeWs(ok, need - 1), stream=0)
+    assert e.value.code == lib.HSA_ERR_WORKSPACE_TOO_SMALL
+    need = lib.hsa_workspace_bytes(d, lib.HSA_OP_DENSE)
+    with pytest.raises(lib.HsaError) as e:
+        lib.dense_decode(d, ok, ok, ok, ok, ok, ok, None, _FakeWs(ok, need - 1), stream=0)
+    assert e.value.code == lib.HSA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_prune_rejects_too_many_chunks(lib):
+    d = _dims(lib, max_pages_per_seq=60000 * 4, num_pages=60000 * 4)
+    ok = 1 << 20
+    with pytest.raises(lib.HsaError) as e:
+        lib.hsa_prune(d, ok, ok, None, None, ok, ok, stream=0)
+    assert e.value.code == lib.HSA_ERR_UNSUPPORTED

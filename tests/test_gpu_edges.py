@@ -1,0 +1,205 @@
+"""GPU parity on edge cases: ragged and tiny contexts, empty candidate regions, zero and
+all-covering budgets, other chunk sizes and group sizes, mixed batches, the decode-step
+append and whole-step entry points, and the device-side bounds checks."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+import oracle
+from kv_cache_int8_gb300 import hsa
+from kv_cache_int8_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+BASE = W.CONFIGS["llama3-8b-128k"]
+
+
+def _cfg(**kw):
+    return dataclasses.replace(BASE, **kw)
+
+
+def _check(wl, dense=True, **over):
+    hd, od = H.dims_pair(wl, **over)
+    h = H.host_arrays(wl)
+    g = H.gpu_step(H.to_cuda(wl), hd, dense=dense)
+    o = H.oracle_step(h, od, dense=dense)
+    pairs = [(b, hh) for b in range(od.batch) for hh in range(od.hkv)]
+    H.compare_step(g, o, h, od, pairs, dense=dense)
+    return g, o
+
+
+@pytest.mark.parametrize("n", [1, 7, 16, 17, 63, 64, 65, 1000, 1153, 1154, 5003])
+def test_ragged_context_lengths(n):
+    wl = W.make_workload(_cfg(context=n, batch=1, hq=8, hkv=2, k1=8, k2=6, sink=20, window=100),
+                         seed=n)
+    g, _ = _check(wl)
+    if n <= 120:
+        assert (g["n_blocks"] == 0).all()
+
+
+def test_mixed_batch_permuted_pages():
+    cfg = _cfg(context=None, context_range=(1, 9000), batch=12, hq=16, hkv=4, k1=9, k2=13,
+               sink=33, window=77, paged_permuted=True)
+    wl = W.make_workload(cfg, seed=5)
+    _check(wl)
+
+
+@pytest.mark.parametrize("k1,k2", [(0, 0), (0, 5), (5, 0), (1, 1), (3, 40)])
+def test_small_and_zero_budgets(k1, k2):
+    wl = W.make_workload(_cfg(context=4099, batch=2, hq=8, hkv=2), seed=11)
+    _check(wl, k1=k1, k2=k2, sink=16, window=64)
+
+
+def test_budget_covering_everything_equals_dense():
+    wl = W.make_workload(_cfg(context=3001, batch=2, hq=8, hkv=2), seed=12)
+    g, o = _check(wl, k1=10000, k2=10000, sink=5, window=9)
+    H.assert_close(g["out"], o["out_dense"], "sparse with every block vs dense oracle")
+    np.testing.assert_allclose(g["out"], g["out_dense"], atol=5e-6, rtol=0)
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 128, 256])
+def test_other_chunk_sizes(chunk):
+    wl = W.make_workload(_cfg(context=20000, batch=1, hq=8, hkv=2), seed=chunk)
+    _check(wl, chunk=chunk, k1=40, k2=30, sink=64, window=128)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (4, 1)])
+def test_group_sizes(hq, hkv):
+    wl = W.make_workload(_cfg(context=12345, batch=2, hq=hq, hkv=hkv, k1=20, k2=17), seed=hq + hkv)
+    _check(wl, sink=40, window=200)
+
+
+def test_unaligned_sink_and_window():
+    wl = W.make_workload(_cfg(context=7777, batch=3, hq=8, hkv=2), seed=21)
+    _check(wl, k1=11, k2=19, sink=37, window=101)
+
+
+def test_window_only_and_sink_only():
+    wl = W.make_workload(_cfg(context=2222, batch=1, hq=4, hkv=1), seed=22)
+    _check(wl, k1=4, k2=4, sink=0, window=0)
+    _check(wl, k1=4, k2=4, sink=0, window=300)
+    _check(wl, k1=4, k2=4, sink=300, window=0)
+
+
+def test_many_ties_lower_index_wins():
+    """Constant keys make every chunk and block tie: the lowest indices must be kept."""
+    wl = W.make_workload(_cfg(context=5000, batch=1, hq=4, hkv=1), seed=23)
+    wl["k_cache"][:] = 0.5
+    g, o = _check(wl, k1=6, k2=9, sink=64, window=128)
+    assert g["block_idx"][0, 0].tolist() == list(range(4, 13))
+
+
+def test_append_then_step_matches_oracle():
+    """hsa_append_kv writes the new token and its codes with the stored scales; the whole
+    step entry point gives the same result as the separate calls."""
+    cfg = _cfg(context=None, context_range=(3000, 9000), batch=3, hq=8, hkv=2, k1=12, k2=10,
+               sink=32, window=96, paged_permuted=True)
+    wl = W.make_workload(cfg, seed=31)
+    hd, od = H.dims_pair(wl)
+    dwl = H.to_cuda(wl)
+    dev = torch.device("cuda")
+    B, Hkv = cfg.batch, cfg.hkv
+    gen = torch.Generator(device="cpu").manual_seed(99)
+    k_new = (torch.randn((B, Hkv, 128), generator=gen) * 9).to(torch.bfloat16)
+    v_new = torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16)
+    kq = torch.zeros(dwl["k_cache"].shape, dtype=torch.int8, device=dev)
+    k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
+    hsa.hsa_quantize_keys(hd, dwl["k_cache"], dwl["page_table"], dwl["seq_lens"], 0, 0, kq,
+                          k_scale, hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
+    kc2, vc2, kq2 = dwl["k_cache"].clone(), dwl["v_cache"].clone(), kq.clone()
+    hsa.hsa_append_kv(hd, k_new.cuda(), v_new.cuda(), kc2, vc2, kq2, k_scale, dwl["page_table"],
+                      dwl["seq_lens"])
+    torch.cuda.synchronize()
+    # oracle: write the token into a host copy, codes with the stored scales
+    kh = wl["k_cache"].clone()
+    vh = wl["v_cache"].clone()
+    pt = wl["page_table"].numpy()
+    for b, n in enumerate(wl["lens"]):
+        kh[pt[b, (n - 1) // 16], :, (n - 1) % 16] = k_new[b]
+        vh[pt[b, (n - 1) // 16], :, (n - 1) % 16] = v_new[b]
+    np.testing.assert_array_equal(kc2.cpu().view(torch.int16).numpy(), kh.view(torch.int16).numpy())
+    np.testing.assert_array_equal(vc2.cpu().view(torch.int16).numpy(), vh.view(torch.int16).numpy())
+    # the oracle's own scales and codes of the cache before the append
+    kq_full, sc_o = oracle.quantize_keys(od, W.to_numpy_bits(wl["k_cache"]), pt,
+                                         wl["seq_lens"].numpy())
+    np.testing.assert_array_equal(k_scale.cpu().numpy(), sc_o)
+    kq_o = oracle.quantize_append(od, W.to_numpy_bits(kh), pt, wl["seq_lens"].numpy(), -1,
+                                  sc_o, kq_full)
+    np.testing.assert_array_equal(kq2.cpu().numpy(), kq_o)
+    # the APPEND mode of hsa_quantize_keys agrees
+    kq3 = kq.clone()
+    hsa.hsa_quantize_keys(hd, kc2, dwl["page_table"], dwl["seq_lens"], 1, -1, kq3, k_scale)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(kq3.cpu().numpy(), kq_o)
+
+    # whole step (device io) == separate calls
+    out_a = torch.zeros((B, cfg.hq, 128), dtype=torch.float32, device=dev)
+    lse_a = torch.zeros((B, cfg.hq), dtype=torch.float32, device=dev)
+    bidx = torch.zeros((B, Hkv, cfg.k2), dtype=torch.int32, device=dev)
+    nb = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+    wst = hsa.workspace(hd, hsa.HSA_OP_STEP)
+    kc4, vc4, kq4 = dwl["k_cache"].clone(), dwl["v_cache"].clone(), kq.clone()
+    hsa.hsa_decode_step(hd, dwl["q"], k_new.cuda(), v_new.cuda(), out_a, lse_a, kc4, vc4, kq4,
+                        k_scale, dwl["page_table"], dwl["seq_lens"], bidx, nb, wst)
+    ws = hsa.workspace(hd, hsa.HSA_OP_SELECT)
+    ci = torch.zeros((B, Hkv, cfg.k1), dtype=torch.int32, device=dev)
+    nc = torch.zeros((B, Hkv), dtype=torch.int32, device=dev)
+    bidx2 = torch.zeros_like(bidx)
+    nb2 = torch.zeros_like(nb)
+    hsa.hsa_select(hd, dwl["q"], kq2, k_scale, dwl["page_table"], dwl["seq_lens"], ci, nc, bidx2,
+                   nb2, ws)
+    out_b = torch.zeros_like(out_a)
+    lse_b = torch.zeros_like(lse_a)
+    hsa.hsa_attend(hd, dwl["q"], kc2, vc2, dwl["page_table"], dwl["seq_lens"], bidx2, nb2, out_b,
+                   lse_b, hsa.workspace(hd, hsa.HSA_OP_ATTEND))
+    torch.cuda.synchronize()
+    assert torch.equal(bidx, bidx2) and torch.equal(nb, nb2)
+    assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+    assert torch.equal(kq4, kq2) and torch.equal(kc4, kc2)
+    # whole step with pinned host io
+    q_h = wl["q"].pin_memory()
+    out_h = torch.zeros((B, cfg.hq, 128), dtype=torch.float32).pin_memory()
+    lse_h = torch.zeros((B, cfg.hq), dtype=torch.float32).pin_memory()
+    kc5, vc5, kq5 = dwl["k_cache"].clone(), dwl["v_cache"].clone(), kq.clone()
+    hsa.hsa_decode_step(hd, q_h, k_new.pin_memory(), v_new.pin_memory(), out_h, lse_h, kc5, vc5,
+                        kq5, k_scale, dwl["page_table"], dwl["seq_lens"], None, None, wst,
+                        io_on_host=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_a.cpu()) and torch.equal(lse_h, lse_a.cpu())
+    assert hsa.hsa_read_device_error(wst) == 0
+
+
+def test_device_bounds_checks_report_without_faulting():
+    """A page-table entry past the pool and a sequence longer than its table are caught by
+    the kernels' own checks: the error word reports them and no access goes out of range."""
+    wl = W.make_workload(_cfg(context=4000, batch=2, hq=8, hkv=2, k1=8, k2=8, sink=16,
+                              window=64), seed=41)
+    hd, _ = H.dims_pair(wl)
+    dwl = H.to_cuda(wl)
+    dev = torch.device("cuda")
+    kq = torch.zeros(dwl["k_cache"].shape, dtype=torch.int8, device=dev)
+    k_scale = torch.zeros((2, 2, 128), dtype=torch.float32, device=dev)
+    hsa.hsa_quantize_keys(hd, dwl["k_cache"], dwl["page_table"], dwl["seq_lens"], 0, 0, kq,
+                          k_scale, hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
+    bad_pt = dwl["page_table"].clone()
+    bad_pt[1, 100] = hd.num_pages + 5
+    bidx = torch.zeros((2, 2, 8), dtype=torch.int32, device=dev)
+    nb = torch.zeros((2, 2), dtype=torch.int32, device=dev)
+    ws = hsa.workspace(hd, hsa.HSA_OP_SELECT)
+    hsa.hsa_select(hd, dwl["q"], kq, k_scale, bad_pt, dwl["seq_lens"], None, None, bidx, nb, ws)
+    assert hsa.hsa_read_device_error(ws) == hsa.HSA_ERR_DEVICE_CHECK
+    assert hsa.hsa_read_device_error(ws) == 0  # cleared by the read
+    long_lens = dwl["seq_lens"].clone()
+    long_lens[0] = hd.max_pages_per_seq * 16 + 1
+    out = torch.zeros((2, 8, 128), dtype=torch.float32, device=dev)
+    wa = hsa.workspace(hd, hsa.HSA_OP_ATTEND)
+    hsa.hsa_attend(hd, dwl["q"], dwl["k_cache"], dwl["v_cache"], dwl["page_table"], long_lens,
+                   bidx, nb, out, None, wa)
+    assert hsa.hsa_read_device_error(wa) == hsa.HSA_ERR_DEVICE_CHECK
+    # the context is still usable
+    hsa.hsa_select(hd, dwl["q"], kq, k_scale, dwl["page_table"], dwl["seq_lens"], None, None,
+                   bidx, nb, ws)
+    assert hsa.hsa_read_device_error(ws) == 0
