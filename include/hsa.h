@@ -141,22 +141,27 @@ int32_t hsa_append_kv(const hsa_dims* d, const void* k_new, const void* v_new, v
  * Scoring step alone: query folding/quantisation and the exact int32 scores, reduced to
  * one maximum per 16-token block. block_max: int32 [batch][hkv][max_pages_per_seq];
  * entries of blocks that hold a candidate token are written, all others are left
- * untouched. (HCAttention: global approximate scoring over quantised keys.)
+ * untouched. tile_max (nullable): int32 [batch][hkv][ceil(max_pages_per_seq / 4)], the
+ * maximum of each 64-token tile's candidate tokens (tile c = tokens [64c, 64c + 64)),
+ * written for tiles holding a candidate token; with 64-token chunks it is the module-1
+ * chunk score. (HCAttention: global approximate scoring over quantised keys.)
  */
 int32_t hsa_score_blocks(const hsa_dims* d, const void* q, const int8_t* kq,
                          const float* k_scale, const int32_t* page_table,
-                         const int32_t* seq_lens, int32_t* block_max, void* stream);
+                         const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
+                         void* stream);
 
 /*
  * The two pruning modules on precomputed block maxima (InfiniteHiP article, section
- * "实现 7.24 倍的端到端解码加速"). chunk_idx int32 [batch][hkv][k1] (nullable),
- * n_chunks int32 [batch][hkv] (nullable), block_idx int32 [batch][hkv][k2],
- * n_blocks int32 [batch][hkv]. Limit: at most 53248 chunks per sequence
+ * "实现 7.24 倍的端到端解码加速"). tile_max (nullable) as written by hsa_score_blocks; it is
+ * read instead of reducing block_max when d->chunk == 64. chunk_idx int32
+ * [batch][hkv][k1] (nullable), n_chunks int32 [batch][hkv] (nullable), block_idx int32
+ * [batch][hkv][k2], n_blocks int32 [batch][hkv]. Limit: at most 53248 chunks per sequence
  * (ceil(max_pages_per_seq * 16 / chunk)); larger returns HSA_ERR_UNSUPPORTED.
  */
 int32_t hsa_prune(const hsa_dims* d, const int32_t* seq_lens, const int32_t* block_max,
-                  int32_t* chunk_idx, int32_t* n_chunks, int32_t* block_idx, int32_t* n_blocks,
-                  void* stream);
+                  const int32_t* tile_max, int32_t* chunk_idx, int32_t* n_chunks,
+                  int32_t* block_idx, int32_t* n_blocks, void* stream);
 
 /*
  * hsa_score_blocks followed by hsa_prune, with the block maxima kept in the

@@ -64,7 +64,11 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
 
 // ---- workspace layouts
 size_t quantize_ws(const Shape& s) { return kErrBytes + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 4); }
-size_t select_ws(const Shape& s) { return kErrBytes + up((size_t)s.batch * s.hkv * s.max_pages * 4); }
+size_t select_bm_bytes(const Shape& s) { return up((size_t)s.batch * s.hkv * s.max_pages * 4); }
+size_t select_tm_bytes(const Shape& s) {
+  return up((size_t)s.batch * s.hkv * hsa::score_max_tiles(s) * 4);
+}
+size_t select_ws(const Shape& s) { return kErrBytes + select_bm_bytes(s) + select_tm_bytes(s); }
 struct AttendLayout {
   size_t counters, part_ml, part_o, end;
 };
@@ -78,14 +82,15 @@ AttendLayout attend_layout(const Shape& s, size_t base) {
 }
 size_t attend_ws(const Shape& s) { return attend_layout(s, kErrBytes).end; }
 struct StepLayout {
-  size_t block_max, block_idx, n_blocks, q, k_new, v_new, out, lse;
+  size_t block_max, tile_max, block_idx, n_blocks, q, k_new, v_new, out, lse;
   AttendLayout att;
   size_t end;
 };
 StepLayout step_layout(const Shape& s) {
   StepLayout l;
   l.block_max = kErrBytes;
-  l.block_idx = l.block_max + up((size_t)s.batch * s.hkv * s.max_pages * 4);
+  l.tile_max = l.block_max + select_bm_bytes(s);
+  l.block_idx = l.tile_max + select_tm_bytes(s);
   l.n_blocks = l.block_idx + up((size_t)s.batch * s.hkv * std::max(s.k2, 1) * 4);
   l.q = l.n_blocks + up((size_t)s.batch * s.hkv * 4);
   l.k_new = l.q + up((size_t)s.batch * s.hq * hsa::kHeadDim * 2);
@@ -168,13 +173,13 @@ inline int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? HSA_OK : H
 inline cudaStream_t as_stream(void* p) { return reinterpret_cast<cudaStream_t>(p); }
 
 int32_t do_score(const Shape& s, const void* q, const int8_t* kq, const float* k_scale,
-                 const int32_t* page_table, const int32_t* seq_lens, int32_t* block_max, int* err,
-                 cudaStream_t st) {
+                 const int32_t* page_table, const int32_t* seq_lens, int32_t* block_max,
+                 int32_t* tile_max, int* err, cudaStream_t st) {
   CUtensorMap map;
   int32_t rc = encode_kq_map(s, kq, &map);
   if (rc != HSA_OK) return rc;
   return cuda_status(hsa::launch_score_blocks(s, map, q, k_scale, page_table, seq_lens, block_max,
-                                              err, num_sms(), st));
+                                              tile_max, err, num_sms(), st));
 }
 
 int32_t check_prune_fits(const Shape& s) {
@@ -296,26 +301,28 @@ int32_t hsa_append_kv(const hsa_dims* d, const void* k_new, const void* v_new, v
 
 int32_t hsa_score_blocks(const hsa_dims* d, const void* q, const int8_t* kq,
                          const float* k_scale, const int32_t* page_table,
-                         const int32_t* seq_lens, int32_t* block_max, void* stream) {
+                         const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
+                         void* stream) {
   Shape s;
   int32_t rc = check_dims(d, s, false);
   if (rc != HSA_OK) return rc;
   if (!q || !kq || !k_scale || !page_table || !seq_lens || !block_max) return HSA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kq, 16) || !aligned(k_scale, 16)) return HSA_ERR_INVALID_ARG;
-  return do_score(s, q, kq, k_scale, page_table, seq_lens, block_max, nullptr, as_stream(stream));
+  return do_score(s, q, kq, k_scale, page_table, seq_lens, block_max, tile_max, nullptr,
+                  as_stream(stream));
 }
 
 int32_t hsa_prune(const hsa_dims* d, const int32_t* seq_lens, const int32_t* block_max,
-                  int32_t* chunk_idx, int32_t* n_chunks, int32_t* block_idx, int32_t* n_blocks,
-                  void* stream) {
+                  const int32_t* tile_max, int32_t* chunk_idx, int32_t* n_chunks,
+                  int32_t* block_idx, int32_t* n_blocks, void* stream) {
   Shape s;
   int32_t rc = check_dims(d, s, true);
   if (rc != HSA_OK) return rc;
   if (!seq_lens || !block_max || !n_blocks || (!block_idx && s.k2 > 0)) return HSA_ERR_INVALID_ARG;
   rc = check_prune_fits(s);
   if (rc != HSA_OK) return rc;
-  return cuda_status(hsa::launch_prune(s, seq_lens, block_max, chunk_idx, n_chunks, block_idx,
-                                       n_blocks, nullptr, as_stream(stream)));
+  return cuda_status(hsa::launch_prune(s, seq_lens, block_max, tile_max, chunk_idx, n_chunks,
+                                       block_idx, n_blocks, nullptr, as_stream(stream)));
 }
 
 int32_t hsa_select(const hsa_dims* d, const void* q, const int8_t* kq, const float* k_scale,
@@ -335,11 +342,12 @@ int32_t hsa_select(const hsa_dims* d, const void* q, const int8_t* kq, const flo
   char* ws = static_cast<char*>(workspace);
   int* err = reinterpret_cast<int*>(ws);
   int32_t* bm = reinterpret_cast<int32_t*>(ws + kErrBytes);
+  int32_t* tm = reinterpret_cast<int32_t*>(ws + kErrBytes + select_bm_bytes(s));
   cudaStream_t st = as_stream(stream);
-  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, err, st);
+  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st);
   if (rc != HSA_OK) return rc;
   return cuda_status(
-      hsa::launch_prune(s, seq_lens, bm, chunk_idx, n_chunks, block_idx, n_blocks, err, st));
+      hsa::launch_prune(s, seq_lens, bm, tm, chunk_idx, n_chunks, block_idx, n_blocks, err, st));
 }
 
 int32_t hsa_attend(const hsa_dims* d, const void* q, const void* k_cache, const void* v_cache,
@@ -427,11 +435,12 @@ int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
                                         kq, k_scale, page_table, seq_lens, err, st);
   if (e != cudaSuccess) return HSA_ERR_CUDA;
   int32_t* bm = reinterpret_cast<int32_t*>(ws + l.block_max);
+  int32_t* tm = reinterpret_cast<int32_t*>(ws + l.tile_max);
   int32_t* bidx = block_idx ? block_idx : reinterpret_cast<int32_t*>(ws + l.block_idx);
   int32_t* nb = n_blocks ? n_blocks : reinterpret_cast<int32_t*>(ws + l.n_blocks);
-  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, err, st);
+  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st);
   if (rc != HSA_OK) return rc;
-  e = hsa::launch_prune(s, seq_lens, bm, nullptr, nullptr, bidx, nb, err, st);
+  e = hsa::launch_prune(s, seq_lens, bm, tm, nullptr, nullptr, bidx, nb, err, st);
   if (e != cudaSuccess) return HSA_ERR_CUDA;
   rc = do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, bidx, nb, out, lse, ws,
                  l.att, st);

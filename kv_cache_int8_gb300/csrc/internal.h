@@ -29,13 +29,16 @@ cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_ne
                              cudaStream_t st);
 
 // ---- select.cu
+// block_max: [B][Hkv][max_pages]; tile_max (nullable): [B][Hkv][score_max_tiles], the max of
+// each 64-token tile, which the prune kernel uses as the chunk score when chunks are 64.
+int score_max_tiles(const Shape& s);
 cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const void* q,
                                 const float* k_scale, const int32_t* page_table,
-                                const int32_t* seq_lens, int32_t* block_max, int* err,
-                                int num_sms, cudaStream_t st);
+                                const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
+                                int* err, int num_sms, cudaStream_t st);
 cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t* block_max,
-                         int32_t* chunk_idx, int32_t* n_chunks, int32_t* block_idx,
-                         int32_t* n_blocks, int* err, cudaStream_t st);
+                         const int32_t* tile_max, int32_t* chunk_idx, int32_t* n_chunks,
+                         int32_t* block_idx, int32_t* n_blocks, int* err, cudaStream_t st);
 int prune_max_chunks();
 size_t prune_smem_bytes(const Shape& s);
 

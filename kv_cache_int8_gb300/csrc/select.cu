@@ -16,11 +16,12 @@
 // G x 32 packed int8 query words sit in registers, dp4a gives the G exact int32 dot
 // products, their max is the token score and a 16-lane max gives the block maximum.
 //
-// prune_kernel: one CTA per (sequence, kv head). Chunk scores (max of their blocks'
-// maxima) are staged in shared memory; the K-th largest value is found by histogram
-// refinement over the value range (2048 bins per pass), ties at the threshold are broken
-// toward lower indices with a block-wide prefix count, and the kept indices are written
-// in ascending order. Module 2 repeats this on the blocks of the kept chunks.
+// prune_kernel: one CTA per (sequence, kv head). Chunk scores (the scorer's per-tile maxima
+// for 64-token chunks, else the max of their blocks' maxima) are staged in shared memory;
+// the K-th largest value is found by radix selection on 8-bit digits of (value - min) with
+// per-warp histograms; ties at the threshold are broken toward lower indices by ballots
+// over warp-contiguous ranges, which also write the kept indices in ascending order.
+// Module 2 repeats this on the blocks of the kept chunks.
 #include <algorithm>
 #include <climits>
 
@@ -47,8 +48,9 @@ struct ScoreArgs {
   const int32_t* page_table;
   const int32_t* seq_lens;
   int32_t* block_max;
+  int32_t* tile_max;  // nullable: max of each 64-token tile's blocks (= chunk max for chunk 64)
   int* err;
-  int batch, hkv, max_pages, num_pages, sink, window;
+  int batch, hkv, max_pages, max_tiles, num_pages, sink, window;
 };
 
 // Candidate region of one sequence in block and tile units.
@@ -164,46 +166,69 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
 
   if (warp == kScoreWarps) {
     // ------------------------------------------------------------ producer
-    if (lane != 0) return;
-    SeqRange sr = seq_range(a, b);
+    // The whole warp resolves the page ids of the next 32 tiles at once (one coalesced
+    // round trip), then lane 0 issues their copies in order as ring slots free up.
     bool ok = true;
-    for (int j = 0; f0 + j < f1; j++) {
-      const int f = f0 + j;
-      const int s = j % kScoreStages;
-      if (j >= kScoreStages && !mbar_wait(&empty[s], ((j / kScoreStages) - 1) & 1)) {
-        set_error(a.err, kDevErrTimeout);
-        ok = false;
-        break;
-      }
-      while (prefix[b + 1] <= f) {
-        b++;
-        sr = seq_range(a, b);
-      }
-      const int r = f - prefix[b];
-      const int h = r / sr.ntile;
-      const int tile = sr.tile_lo + r % sr.ntile;
+    int bw = b;  // sequence of tile f0 + jb (warp-uniform)
+    for (int jb = 0; ok && f0 + jb < f1; jb += 32) {
+      const int f = f0 + jb + lane;
       int rows[kTileBlocks];
-      uint32_t bytes = 0;
 #pragma unroll
-      for (int i = 0; i < kTileBlocks; i++) {
-        const int k = tile * kTileBlocks + i;
-        rows[i] = -1;
-        if (k < sr.k_lo || k >= sr.k_hi) continue;
-        const int page = a.page_table[(size_t)b * a.max_pages + k];
-        if (page < 0 || page >= a.num_pages) {
-          set_error(a.err, kDevErrCheck);
-          continue;
+      for (int i = 0; i < kTileBlocks; i++) rows[i] = -1;
+      if (f < f1) {
+        int bl = bw;
+        while (prefix[bl + 1] <= f) bl++;
+        const SeqRange sr = seq_range(a, bl);
+        const int r = f - prefix[bl];
+        const int h = r / sr.ntile;
+        const int tile = sr.tile_lo + r % sr.ntile;
+        const int32_t* row = a.page_table + (size_t)bl * a.max_pages;
+        int pg[kTileBlocks];
+#pragma unroll
+        for (int i = 0; i < kTileBlocks; i++) {
+          const int k = tile * kTileBlocks + i;
+          pg[i] = (k >= sr.k_lo && k < sr.k_hi) ? row[k] : -2;
         }
-        rows[i] = (page * a.hkv + h) * kPage;
-        bytes += kBlockBytesI8;
-      }
-      mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
-      for (int i = 0; i < kTileBlocks; i++)
-        if (rows[i] >= 0)
-          tma_load_2d(ring + s * kStageBytes + i * kBlockBytesI8, &kq_map, 0, rows[i], &full[s]);
+        for (int i = 0; i < kTileBlocks; i++) {
+          if (pg[i] == -2) continue;
+          if (pg[i] < 0 || pg[i] >= a.num_pages) {
+            set_error(a.err, kDevErrCheck);
+            continue;
+          }
+          rows[i] = (pg[i] * a.hkv + h) * kPage;
+        }
+      }
+      const int n = min(32, f1 - f0 - jb);
+      for (int i = 0; i < n; i++) {
+        int rr[kTileBlocks];
+#pragma unroll
+        for (int q = 0; q < kTileBlocks; q++) rr[q] = __shfl_sync(0xffffffffu, rows[q], i);
+        if (lane == 0) {
+          const int j = jb + i;
+          const int s = j % kScoreStages;
+          if (j >= kScoreStages && !mbar_wait(&empty[s], ((j / kScoreStages) - 1) & 1)) {
+            set_error(a.err, kDevErrTimeout);
+            ok = false;
+          } else {
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int q = 0; q < kTileBlocks; q++) bytes += rr[q] >= 0 ? kBlockBytesI8 : 0;
+            mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+            for (int q = 0; q < kTileBlocks; q++)
+              if (rr[q] >= 0)
+                tma_load_2d(ring + s * kStageBytes + q * kBlockBytesI8, &kq_map, 0, rr[q], &full[s]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      // advance the warp's sequence cursor to the first tile of the next batch
+      const int fn = f0 + jb + 32;
+      while (bw + 1 < a.batch && prefix[bw + 1] <= fn) bw++;
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       // let the copies already issued land before the CTA exits (bounded)
       const int issued = f1 - f0;
       for (int j = max(0, issued - kScoreStages); j < issued; j++)
@@ -237,6 +262,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     }
     const uint32_t sbase = smem_addr(ring + s * kStageBytes);
     int32_t* out = a.block_max + ((size_t)b * a.hkv + h) * a.max_pages;
+    int tmax = INT_MIN;
 #pragma unroll
     for (int half = 0; half < 2; half++) {
       const int row = half * 32 + lane;           // token within the tile
@@ -268,7 +294,11 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         const int k = tile * kTileBlocks + half * 2 + (lane >> 4);
         if (k >= sr.k_lo && k < sr.k_hi) out[k] = g;
       }
+      tmax = max(tmax, g);
     }
+    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+    if (a.tile_max != nullptr && lane == 0)
+      a.tile_max[((size_t)b * a.hkv + h) * a.max_tiles + tile] = tmax;
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
@@ -283,14 +313,15 @@ size_t score_smem_bytes(int batch) {
 
 constexpr int kPruneThreads = 512;
 constexpr int kPruneWarps = kPruneThreads / 32;
-constexpr int kBins = 2048;
-constexpr int kBinsPerThread = kBins / kPruneThreads;
+constexpr int kDigitBins = 256;
 constexpr int kMaxChunks = 53248;
 constexpr size_t kSmemLimit = 227 * 1024;
 
 struct PruneArgs {
   const int32_t* seq_lens;
   const int32_t* block_max;
+  const int32_t* tile_max;  // nullable; used when chunks are 64 tokens
+  int max_tiles;
   int32_t* chunk_idx;
   int32_t* n_chunks;
   int32_t* block_idx;
@@ -299,145 +330,187 @@ struct PruneArgs {
   int hkv, max_pages, chunk_blocks, k1, k2, sink, window, vals_cap, cand_cap;
 };
 
-// Exclusive prefix sum over the CTA; `total` receives the sum. All threads must call.
-__device__ int block_exclusive_scan(int v, int* scratch, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kPruneWarps ? scratch[lane] : 0;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, off);
-      if (lane >= off) w += y;
-    }
-    if (lane < kPruneWarps) scratch[lane] = w;
-  }
-  __syncthreads();
-  const int base = warp > 0 ? scratch[warp - 1] : 0;
-  total = scratch[kPruneWarps - 1];
-  __syncthreads();
-  return base + x - v;
+// Shared scratch of the selection: per-warp digit histograms and per-warp totals.
+struct SelectScratch {
+  unsigned hist[kPruneWarps][kDigitBins];
+  int w_a[kPruneWarps], w_b[kPruneWarps];
+  int red[kPruneWarps];
+  int decided[4];
+};
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
 }
 
-__device__ int block_min_max(int v, bool want_max, int* scratch) {
+// Min of the entries that are not INT_MIN (placeholders), or INT_MAX if none.
+__device__ int block_min_valid(const int* vals, int n, SelectScratch& ss) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int m = INT_MAX;
+  for (int i = threadIdx.x; i < n; i += kPruneThreads)
+    if (vals[i] != INT_MIN) m = min(m, vals[i]);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const int y = __shfl_xor_sync(0xffffffffu, v, off);
-    v = want_max ? max(v, y) : min(v, y);
-  }
-  if (lane == 0) scratch[warp] = v;
+  for (int off = 16; off > 0; off >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) ss.red[warp] = m;
   __syncthreads();
-  int r = scratch[0];
-  for (int w = 1; w < kPruneWarps; w++) r = want_max ? max(r, scratch[w]) : min(r, scratch[w]);
+  int r = ss.red[0];
+#pragma unroll
+  for (int w = 1; w < kPruneWarps; w++) r = min(r, ss.red[w]);
   __syncthreads();
   return r;
 }
 
-// Contiguous ownership: thread t owns [t m, min((t+1) m, n)).
-__device__ __forceinline__ void own_range(int n, int& i0, int& i1) {
-  const int m = (n + kPruneThreads - 1) / kPruneThreads;
-  i0 = min(n, (int)threadIdx.x * m);
-  i1 = min(n, i0 + m);
+// Order-preserving key of a value relative to the smallest valid value; placeholders get 0.
+__device__ __forceinline__ unsigned rel_key(int v, int vmin) {
+  return v == INT_MIN ? 0u : (unsigned)((long long)v - vmin) + 1u;
 }
 
-// Finds T, the K-th largest of vals[0..n) (0 < K < n), and need_eq = how many of the
-// values equal to T are kept (the lowest-index ones): K - #(values > T).
-__device__ void kth_largest(const int* vals, int n, int K, int* hist, int* scratch, int& T,
+// The K-th largest value T of vals[0..n) (0 < K < number of valid entries) by radix
+// selection on 8-bit digits of the keys, from the highest digit in which they differ;
+// need_eq = K - #(values > T), i.e. how many of the entries equal to T are kept (the
+// lowest-index ones). Two CTA barriers per digit.
+__device__ void kth_largest(const int* vals, int n, int K, SelectScratch& ss, int& T,
                             int& need_eq) {
-  int i0, i1;
-  own_range(n, i0, i1);
-  int lmin = INT_MAX, lmax = INT_MIN;
-  for (int i = i0; i < i1; i++) {
-    lmin = min(lmin, vals[i]);
-    lmax = max(lmax, vals[i]);
-  }
-  long long lo = block_min_max(lmin, false, scratch);
-  long long hi = block_min_max(lmax, true, scratch);
-  int above = 0;  // values known to lie above the current range
-  while (lo < hi) {
-    const unsigned long long range = (unsigned long long)(hi - lo);
-    int bits = 64 - __clzll(range);
-    const int shift = max(0, bits - 11);
-    const int nb = (int)(range >> shift) + 1;
-    for (int i = threadIdx.x; i < nb; i += kPruneThreads) hist[i] = 0;
-    __syncthreads();
-    for (int i = i0; i < i1; i++) {
-      const long long v = vals[i];
-      if (v >= lo && v <= hi) atomicAdd(&hist[(int)((unsigned long long)(v - lo) >> shift)], 1);
-    }
-    __syncthreads();
-    int local = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int vmin = block_min_valid(vals, n, ss);
+  unsigned kmax = 0;
+  for (int i = threadIdx.x; i < n; i += kPruneThreads) kmax = max(kmax, rel_key(vals[i], vmin));
 #pragma unroll
-    for (int q = 0; q < kBinsPerThread; q++) {
-      const int bin = threadIdx.x * kBinsPerThread + q;
-      if (bin < nb) local += hist[bin];
+  for (int off = 16; off > 0; off >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+  if (lane == 0) ss.red[warp] = (int)kmax;
+  __syncthreads();
+  kmax = 0;
+#pragma unroll
+  for (int w = 0; w < kPruneWarps; w++) kmax = max(kmax, (unsigned)ss.red[w]);
+  int shift = kmax > 0 ? ((31 - __clz(kmax)) / 8) * 8 : 0;
+  unsigned prefix = 0;  // decided high bits of T's key
+  int above = 0;        // entries known to lie above T
+  for (;;) {
+    unsigned* hist = ss.hist[warp];
+#pragma unroll
+    for (int q = 0; q < kDigitBins / 32; q++) hist[lane * (kDigitBins / 32) + q] = 0;
+    __syncwarp();
+    const int hi_shift = shift + 8;
+    for (int i = threadIdx.x; i < n; i += kPruneThreads) {
+      const unsigned key = rel_key(vals[i], vmin);
+      const bool match = hi_shift >= 32 || (key >> hi_shift) == (prefix >> hi_shift);
+      if (match) atomicAdd(&hist[(key >> shift) & 0xFF], 1u);
     }
-    int tot;
-    const int before = block_exclusive_scan(local, scratch, tot);
-    int higher = above + (tot - before - local);  // values in bins of later threads
-    for (int q = kBinsPerThread - 1; q >= 0; q--) {
-      const int bin = threadIdx.x * kBinsPerThread + q;
-      if (bin >= nb) continue;
-      const int c = hist[bin];
-      if (higher < K && higher + c >= K) {
-        scratch[40] = bin;
-        scratch[41] = higher;
+    __syncthreads();
+    if (warp == 0) {
+      // lane owns digits [8 lane, 8 lane + 8); counts summed over the warps
+      unsigned c[8];
+      unsigned mine = 0;
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        unsigned t = 0;
+#pragma unroll
+        for (int w = 0; w < kPruneWarps; w++) t += ss.hist[w][lane * 8 + q];
+        c[q] = t;
+        mine += t;
       }
-      higher += c;
+      // entries in the digits of higher lanes
+      unsigned incl = mine;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const unsigned y = __shfl_down_sync(0xffffffffu, incl, off);
+        if (lane + off < 32) incl += y;
+      }
+      unsigned higher = above + (incl - mine);
+#pragma unroll
+      for (int q = 7; q >= 0; q--) {
+        if (higher < (unsigned)K && higher + c[q] >= (unsigned)K) {
+          ss.decided[0] = lane * 8 + q;
+          ss.decided[1] = (int)higher;
+        }
+        higher += c[q];
+      }
     }
     __syncthreads();
-    const int bin = scratch[40];
-    above = scratch[41];
-    lo = lo + ((long long)bin << shift);
-    hi = min(hi, lo + ((1LL << shift) - 1));
-    __syncthreads();
+    prefix |= (unsigned)ss.decided[0] << shift;
+    above = ss.decided[1];
+    if (shift == 0) break;
+    shift -= 8;
   }
-  T = (int)lo;
+  T = (int)((long long)vmin + (long long)prefix - 1);
   need_eq = K - above;
+  __syncthreads();
 }
 
-// Writes, in ascending index order, every i with vals[i] > T plus the first need_eq
-// indices with vals[i] == T, calling emit(position, i). Returns the number kept.
+// Emits, in ascending index order, every i with vals[i] > T plus the first need_eq indices
+// with vals[i] == T, calling emit(position, i); returns how many. Warp w owns a contiguous
+// range, scanned 32 entries at a time with ballots (conflict-free, one CTA barrier).
 template <typename Emit>
-__device__ int collect(const int* vals, int n, int T, int need_eq, int* scratch, Emit emit) {
-  int i0, i1;
-  own_range(n, i0, i1);
-  int n_eq = 0;
-  for (int i = i0; i < i1; i++) n_eq += vals[i] == T;
-  int tot;
-  int eq_rank = block_exclusive_scan(n_eq, scratch, tot);
-  const int eq_rank0 = eq_rank;
-  int n_take = 0;
-  for (int i = i0; i < i1; i++) {
-    const int v = vals[i];
-    if (v > T || (v == T && eq_rank++ < need_eq)) n_take++;
+__device__ int collect(const int* vals, int n, int T, int need_eq, SelectScratch& ss, Emit emit) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = ((n + kPruneWarps * 32 - 1) / (kPruneWarps * 32)) * 32;
+  const int w0 = min(n, warp * per), w1 = min(n, w0 + per);
+  int n_gt = 0, n_eq = 0;
+  for (int i = w0 + lane; i < w1; i += 32) {
+    n_gt += vals[i] > T;
+    n_eq += vals[i] == T;
   }
-  int kept;
-  int pos = block_exclusive_scan(n_take, scratch, kept);
-  eq_rank = eq_rank0;
-  for (int i = i0; i < i1; i++) {
-    const int v = vals[i];
-    if (v > T || (v == T && eq_rank++ < need_eq)) emit(pos++, i);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    n_gt += __shfl_xor_sync(0xffffffffu, n_gt, off);
+    n_eq += __shfl_xor_sync(0xffffffffu, n_eq, off);
+  }
+  if (lane == 0) {
+    ss.w_a[warp] = n_gt;
+    ss.w_b[warp] = n_eq;
   }
   __syncthreads();
-  return kept;
+  // per warp: entries kept = all above T plus the ties still allowed after the earlier warps
+  int eq_acc = 0, pos = 0, total = 0, eq_base = 0;
+  for (int w = 0; w < kPruneWarps; w++) {
+    const int kept_w = ss.w_a[w] + min(max(need_eq - eq_acc, 0), ss.w_b[w]);
+    if (w == warp) {
+      pos = total;
+      eq_base = eq_acc;
+    }
+    total += kept_w;
+    eq_acc += ss.w_b[w];
+  }
+  const unsigned lt = lanemask_lt();
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const int v = i < w1 ? vals[i] : INT_MIN;
+    const bool gt = i < w1 && v > T, eq = i < w1 && v == T;
+    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+    const bool take = gt || (eq && eq_base + __popc(eqm & lt) < need_eq);
+    const unsigned tm = __ballot_sync(0xffffffffu, take);
+    if (take) emit(pos + __popc(tm & lt), i);
+    eq_base += __popc(eqm);
+    pos += __popc(tm);
+  }
+  __syncthreads();
+  return total;
+}
+
+template <int UNROLL>
+__device__ __forceinline__ void gather_strided(int* dst, const int32_t* __restrict__ src, int n) {
+  for (int i0 = threadIdx.x; i0 < n; i0 += UNROLL * kPruneThreads) {
+    int v[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; u++) {
+      const int i = i0 + u * kPruneThreads;
+      v[u] = i < n ? __ldg(src + i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; u++) {
+      const int i = i0 + u * kPruneThreads;
+      if (i < n) dst[i] = v[u];
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const PruneArgs a) {
-  extern __shared__ int psmem[];
-  int* vals = psmem;                     // vals_cap
-  int* cand = vals + a.vals_cap;         // cand_cap block ids of module 2
-  int* kept_chunks = cand + a.cand_cap;  // k1
-  int* hist = kept_chunks + a.k1;        // kBins
-  int* scratch = hist + kBins;           // 64
+  extern __shared__ __align__(16) int psmem[];
+  SelectScratch& ss = *reinterpret_cast<SelectScratch*>(psmem);
+  int* vals = psmem + sizeof(SelectScratch) / sizeof(int);  // vals_cap
+  int* cand = vals + a.vals_cap;                            // cand_cap block ids of module 2
+  int* kept_chunks = cand + a.cand_cap;                     // k1
 
   const int h = blockIdx.x, b = blockIdx.y;
   const int n = a.seq_lens[b];
@@ -458,20 +531,23 @@ __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const PruneArgs a)
   const size_t bh = (size_t)b * a.hkv + h;
 
   // ---- module 1: chunk scores, top-K1
-  for (int i = threadIdx.x; i < n1; i += kPruneThreads) {
-    const int c = c_lo + i;
-    const int kb0 = max(c * P, k_lo), kb1 = min(c * P + P, k_hi);
-    int m = INT_MIN;
-    for (int k = kb0; k < kb1; k++) m = max(m, bm[k]);
-    vals[i] = m;
+  if (a.tile_max != nullptr && P == 4) {
+    gather_strided<8>(vals, a.tile_max + bh * a.max_tiles + c_lo, n1);
+  } else {
+    for (int i = threadIdx.x; i < n1; i += kPruneThreads) vals[i] = INT_MIN;
+    __syncthreads();
+    // every candidate block once (independent, coalesced loads); max into its chunk
+#pragma unroll 4
+    for (int k = k_lo + threadIdx.x; k < k_hi; k += kPruneThreads)
+      atomicMax(&vals[k / P - c_lo], __ldg(bm + k));
   }
   __syncthreads();
   const int keep1 = min(a.k1, n1);
-  int T = INT_MIN, need_eq = n1;
-  if (keep1 < n1 && keep1 > 0) kth_largest(vals, n1, keep1, hist, scratch, T, need_eq);
+  int T = INT_MIN, need_eq = 0;
+  if (keep1 < n1 && keep1 > 0) kth_largest(vals, n1, keep1, ss, T, need_eq);
   int got1 = 0;
   if (keep1 > 0) {
-    got1 = collect(vals, n1, T, need_eq, scratch, [&](int pos, int i) {
+    got1 = collect(vals, n1, T, need_eq, ss, [&](int pos, int i) {
       kept_chunks[pos] = c_lo + i;
       if (a.chunk_idx) a.chunk_idx[bh * a.k1 + pos] = c_lo + i;
     });
@@ -481,32 +557,43 @@ __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const PruneArgs a)
   if (a.n_chunks && threadIdx.x == 0) a.n_chunks[bh] = got1;
   __syncthreads();
 
-  // ---- module 2: the kept chunks' blocks, top-K2
-  int i0, i1;
-  own_range(got1, i0, i1);
-  int mine = 0;
-  for (int i = i0; i < i1; i++) {
-    const int c = kept_chunks[i];
-    mine += min(c * P + P, k_hi) - max(c * P, k_lo);
-  }
-  int n2;
-  int off = block_exclusive_scan(mine, scratch, n2);
-  for (int i = i0; i < i1; i++) {
-    const int c = kept_chunks[i];
-    for (int k = max(c * P, k_lo); k < min(c * P + P, k_hi); k++) {
-      cand[off] = k;
-      vals[off] = bm[k];
-      off++;
+  // ---- module 2: the kept chunks' blocks (P per chunk, ascending; blocks outside the
+  // candidate region are INT_MIN placeholders that are never kept), top-K2
+  const int n2 = got1 * P;
+  int valid_local = 0;
+  for (int x0 = threadIdx.x; x0 < n2; x0 += 4 * kPruneThreads) {
+    int v[4], kk[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int x = x0 + u * kPruneThreads;
+      kk[u] = x < n2 ? kept_chunks[x / P] * P + x % P : -1;
+      v[u] = (kk[u] >= k_lo && kk[u] < k_hi) ? __ldg(bm + kk[u]) : INT_MIN;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int x = x0 + u * kPruneThreads;
+      if (x < n2) {
+        cand[x] = kk[u];
+        vals[x] = v[u];
+        valid_local += v[u] != INT_MIN;
+      }
     }
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) valid_local += __shfl_xor_sync(0xffffffffu, valid_local, off);
+  if ((threadIdx.x & 31) == 0) ss.red[threadIdx.x >> 5] = valid_local;
   __syncthreads();
-  const int keep2 = min(a.k2, n2);
+  int n2_valid = 0;
+#pragma unroll
+  for (int w = 0; w < kPruneWarps; w++) n2_valid += ss.red[w];
+  __syncthreads();
+  const int keep2 = min(a.k2, n2_valid);
   T = INT_MIN;
-  need_eq = n2;
-  if (keep2 < n2 && keep2 > 0) kth_largest(vals, n2, keep2, hist, scratch, T, need_eq);
+  need_eq = 0;
+  if (keep2 < n2_valid && keep2 > 0) kth_largest(vals, n2, keep2, ss, T, need_eq);
   int got2 = 0;
   if (keep2 > 0) {
-    got2 = collect(vals, n2, T, need_eq, scratch, [&](int pos, int i) {
+    got2 = collect(vals, n2, T, need_eq, ss, [&](int pos, int i) {
       a.block_idx[bh * a.k2 + pos] = cand[i];
     });
   }
@@ -518,7 +605,7 @@ int prune_caps(const Shape& s, int& vals_cap, int& cand_cap) {
   const int P = s.chunk / kPage;
   const long long n1max = ((long long)s.max_pages + P - 1) / P;
   const long long keep1 = std::min<long long>(s.k1, n1max);
-  const long long n2max = std::min<long long>(keep1 * P, s.max_pages);
+  const long long n2max = keep1 * P;
   if (n1max > kMaxChunks) return -1;
   vals_cap = (int)std::max(n1max, n2max);
   cand_cap = (int)n2max;
@@ -532,13 +619,15 @@ int prune_max_chunks() { return kMaxChunks; }
 size_t prune_smem_bytes(const Shape& s) {
   int vals_cap, cand_cap;
   if (prune_caps(s, vals_cap, cand_cap) != 0) return ~size_t(0);
-  return sizeof(int) * ((size_t)vals_cap + cand_cap + s.k1 + kBins + 64);
+  return sizeof(SelectScratch) + sizeof(int) * ((size_t)vals_cap + cand_cap + s.k1);
 }
+
+int score_max_tiles(const Shape& s) { return (s.max_pages + kTileBlocks - 1) / kTileBlocks; }
 
 cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const void* q,
                                 const float* k_scale, const int32_t* page_table,
-                                const int32_t* seq_lens, int32_t* block_max, int* err,
-                                int num_sms, cudaStream_t st) {
+                                const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
+                                int* err, int num_sms, cudaStream_t st) {
   if (s.batch > kMaxBatch) return cudaErrorInvalidValue;
   ScoreArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -546,10 +635,12 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const
   a.page_table = page_table;
   a.seq_lens = seq_lens;
   a.block_max = block_max;
+  a.tile_max = tile_max;
   a.err = err;
   a.batch = s.batch;
   a.hkv = s.hkv;
   a.max_pages = s.max_pages;
+  a.max_tiles = score_max_tiles(s);
   a.num_pages = s.num_pages;
   a.sink = s.sink;
   a.window = s.window;
@@ -585,14 +676,16 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const
 }
 
 cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t* block_max,
-                         int32_t* chunk_idx, int32_t* n_chunks, int32_t* block_idx,
-                         int32_t* n_blocks, int* err, cudaStream_t st) {
+                         const int32_t* tile_max, int32_t* chunk_idx, int32_t* n_chunks,
+                         int32_t* block_idx, int32_t* n_blocks, int* err, cudaStream_t st) {
   PruneArgs a;
   if (prune_caps(s, a.vals_cap, a.cand_cap) != 0) return cudaErrorInvalidValue;
   const size_t smem = prune_smem_bytes(s);
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
   a.seq_lens = seq_lens;
   a.block_max = block_max;
+  a.tile_max = tile_max;
+  a.max_tiles = score_max_tiles(s);
   a.chunk_idx = chunk_idx;
   a.n_chunks = n_chunks;
   a.block_idx = block_idx;

@@ -102,8 +102,8 @@ def load(path: Optional[str] = None):
         "hsa_status_string": (ctypes.c_char_p, [I32]),
         "hsa_quantize_keys": (I32, [D, P, P, P, I32, I32, P, P, P, SZ, P]),
         "hsa_append_kv": (I32, [D, P, P, P, P, P, P, P, P, P]),
-        "hsa_score_blocks": (I32, [D, P, P, P, P, P, P, P]),
-        "hsa_prune": (I32, [D, P, P, P, P, P, P, P]),
+        "hsa_score_blocks": (I32, [D, P, P, P, P, P, P, P, P]),
+        "hsa_prune": (I32, [D, P, P, P, P, P, P, P, P]),
         "hsa_select": (I32, [D, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "hsa_attend": (I32, [D, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "dense_decode": (I32, [D, P, P, P, P, P, P, P, P, SZ, P]),
@@ -171,20 +171,20 @@ def hsa_append_kv(d: Dims, k_new, v_new, k_cache, v_cache, kq, k_scale, page_tab
         _p(page_table), _p(seq_lens), _stream(stream)))
 
 
-def hsa_score_blocks(d: Dims, q, kq, k_scale, page_table, seq_lens, block_max,
+def hsa_score_blocks(d: Dims, q, kq, k_scale, page_table, seq_lens, block_max, tile_max=None,
                      stream=None) -> None:
     cd = d.c()
     _check("hsa_score_blocks", load().hsa_score_blocks(
         ctypes.byref(cd), _p(q), _p(kq), _p(k_scale), _p(page_table), _p(seq_lens),
-        _p(block_max), _stream(stream)))
+        _p(block_max), _p(tile_max), _stream(stream)))
 
 
-def hsa_prune(d: Dims, seq_lens, block_max, chunk_idx, n_chunks, block_idx, n_blocks,
+def hsa_prune(d: Dims, seq_lens, block_max, tile_max, chunk_idx, n_chunks, block_idx, n_blocks,
               stream=None) -> None:
     cd = d.c()
     _check("hsa_prune", load().hsa_prune(
-        ctypes.byref(cd), _p(seq_lens), _p(block_max), _p(chunk_idx), _p(n_chunks),
-        _p(block_idx), _p(n_blocks), _stream(stream)))
+        ctypes.byref(cd), _p(seq_lens), _p(block_max), _p(tile_max), _p(chunk_idx),
+        _p(n_chunks), _p(block_idx), _p(n_blocks), _stream(stream)))
 
 
 def hsa_select(d: Dims, q, kq, k_scale, page_table, seq_lens, chunk_idx, n_chunks, block_idx,

@@ -60,6 +60,22 @@ def gpu_step(wl: dict, d: hsa.Dims, dense: bool = True) -> dict:
     ws = hsa.workspace(d, hsa.HSA_OP_SELECT)
     hsa.hsa_select(d, wl["q"], kq, k_scale, wl["page_table"], wl["seq_lens"], chunk_idx, n_chunks,
                    block_idx, n_blocks, ws)
+    # the split entry points (score with per-tile maxima, then prune) agree with hsa_select
+    bm2 = torch.full_like(bm, INT32_MIN)
+    tm = torch.full((B, Hkv, (d.max_pages_per_seq + 3) // 4), INT32_MIN, dtype=torch.int32,
+                    device=dev)
+    hsa.hsa_score_blocks(d, wl["q"], kq, k_scale, wl["page_table"], wl["seq_lens"], bm2, tm)
+    bi2 = torch.full_like(block_idx, -7)
+    nb2 = torch.full_like(n_blocks, -7)
+    ci2 = torch.full_like(chunk_idx, -7)
+    hsa.hsa_prune(d, wl["seq_lens"], bm2, tm, ci2, None, bi2, nb2)
+    torch.cuda.synchronize()
+    assert torch.equal(bm2, bm)
+    k_tiles = tm.shape[-1]
+    pad = torch.full((B, Hkv, 4 * k_tiles - bm.shape[-1]), INT32_MIN, dtype=torch.int32, device=dev)
+    assert torch.equal(tm, torch.cat([bm, pad], dim=-1).view(B, Hkv, k_tiles, 4).amax(-1))
+    assert torch.equal(bi2, block_idx) and torch.equal(nb2, n_blocks)
+    assert torch.equal(ci2, chunk_idx)
     wa = hsa.workspace(d, hsa.HSA_OP_ATTEND)
     out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
     lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev)

@@ -134,5 +134,5 @@ def test_prune_rejects_too_many_chunks(lib):
     d = _dims(lib, max_pages_per_seq=60000 * 4, num_pages=60000 * 4)
     ok = 1 << 20
     with pytest.raises(lib.HsaError) as e:
-        lib.hsa_prune(d, ok, ok, None, None, ok, ok, stream=0)
+        lib.hsa_prune(d, ok, ok, None, None, None, ok, ok, stream=0)
     assert e.value.code == lib.HSA_ERR_UNSUPPORTED
