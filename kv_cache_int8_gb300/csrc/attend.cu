@@ -11,16 +11,21 @@
 //
 // Work: the attended set of (sequence b, kv head h) is a list of segments, each a
 // 16-token page clipped to a token range: the sink pages, the kept blocks (clipped to the
-// candidate region), the window pages. Dense decode uses every page of [0, N). A CTA
-// takes a contiguous share of the list for all G query heads of the group, so every K/V
-// byte is read once per group. Within a segment, warp w handles tokens 4w..4w+3 and 8
-// lanes share a token (16 channels each); each 8-lane group keeps its own online-softmax
-// state (log2 domain), merged across the CTA at the end; CTAs of one (b, h) are merged by
-// the last one to finish (atomic counter, no waiting).
+// candidate region), the window pages. Dense decode uses every page of [0, N). A CTA takes
+// a contiguous share of the list for all G query heads of the group, so every K/V byte is
+// read once per group. Per segment, in shared memory:
+//   scores: warp w takes tokens 4w..4w+3, 8 lanes per token (16 channels each), G partial
+//           dot products reduced over the 8 lanes with a transposing butterfly;
+//   softmax: warp j (< G) owns head j's running max and sum (log2 domain), turns the 16
+//           scores into weights and the rescale factor of the running state;
+//   values: warp w owns channels [64 (w & 1) + 2 lane, +2) of tokens 8 (w >> 1) .. +8 for
+//           all G heads (8 accumulators per lane).
+// CTAs of one (b, h) are merged by the last one to finish (atomic counter, no waiting).
 //
 // HBM path: a producer lane fills a ring of 8 KiB slots (K page then V page of one head,
 // 4 KiB each) with cp.async.bulk copies tracked by mbarriers. Host path: K/V live in
-// pinned host memory; each lane issues its own 16-byte loads through the mapped alias.
+// pinned host memory; the compute warps copy each segment into shared memory with 16-byte
+// loads through the mapped alias, one segment ahead.
 #include <algorithm>
 #include <cfloat>
 
@@ -30,14 +35,16 @@
 namespace hsa {
 namespace {
 
-constexpr int kWarps = 4;                              // compute warps: 16 tokens per segment
+constexpr int kWarps = 4;                        // compute warps
+constexpr int kCompute = kWarps * 32;
 constexpr int kStages = 8;
-constexpr int kSlotBytes = 2 * kBlockBytesBf16;        // K page + V page of one head
-constexpr int kTmaThreads = (kWarps + 1) * 32;
-constexpr int kHostThreads = kWarps * 32;
+constexpr int kSlotBytes = 2 * kBlockBytesBf16;  // K page + V page of one head
+constexpr int kTmaThreads = kCompute + 32;
+constexpr int kHostThreads = kCompute;
 constexpr int kMaxSplits = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNeg = -FLT_MAX;                 // "no token" score
 
 struct AttArgs {
   const __nv_bfloat16* q;
@@ -58,7 +65,7 @@ struct AttArgs {
 };
 
 struct Segments {
-  int n;                 // context length
+  int n;  // context length
   int n_sink, n_sel, n_win;
   int sink_end, cand_hi, w0, win_k0;
   const int32_t* sel;
@@ -118,13 +125,6 @@ __device__ __forceinline__ void segment_at(const Segments& s, int i, int sink, i
   }
 }
 
-// Per-lane online-softmax state for the G heads over 16 channels.
-template <int G>
-struct State {
-  float m[G], l[G], o[G][16];
-};
-
-template <int G>
 __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float f[16]) {
   f[0] = bf16_lo(a.x); f[1] = bf16_hi(a.x); f[2] = bf16_lo(a.y); f[3] = bf16_hi(a.y);
   f[4] = bf16_lo(a.z); f[5] = bf16_hi(a.z); f[6] = bf16_lo(a.w); f[7] = bf16_hi(a.w);
@@ -132,42 +132,55 @@ __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float f
   f[12] = bf16_lo(b.z); f[13] = bf16_hi(b.z); f[14] = bf16_lo(b.w); f[15] = bf16_hi(b.w);
 }
 
-// One token: scores of the G heads (8-lane butterfly), online update, value accumulation.
-// Every lane of the warp must call (the shuffles span the warp); `valid` is per 8-lane group.
+__device__ __forceinline__ void compute_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
+}
+
+// Shared memory of the compute warps besides the K/V slots.
+struct Scratch {
+  float score[kPage][4];  // per token, per head (log2-scaled logits)
+  float prob[kPage][4];   // softmax weights of the segment
+  float rescale[4];       // factor applied to the running state of each head
+  float m[4], l[4];       // final running max / sum per head
+};
+
+// Running state of one lane.
 template <int G>
-__device__ __forceinline__ void attend_token(State<G>& st, const float (&qf)[G][16],
-                                             const uint4& k0, const uint4& k1, const uint4& v0,
-                                             const uint4& v1, bool valid) {
-  float kf[16];
-  unpack16<G>(k0, k1, kf);
-  float s[G];
-#pragma unroll
-  for (int j = 0; j < G; j++) {
-    float acc = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 16; e++) acc = fmaf(qf[j][e], kf[e], acc);
-    s[j] = acc;
-  }
-#pragma unroll
-  for (int off = 1; off < 8; off <<= 1)
-#pragma unroll
-    for (int j = 0; j < G; j++) s[j] += __shfl_xor_sync(0xffffffffu, s[j], off);
-  if (!valid) return;
-  float vf[16];
-  unpack16<G>(v0, v1, vf);
-#pragma unroll
-  for (int j = 0; j < G; j++) {
-    if (s[j] > st.m[j]) {
-      const float c = exp2f(st.m[j] - s[j]);
-      st.m[j] = s[j];
-      st.l[j] *= c;
-#pragma unroll
-      for (int e = 0; e < 16; e++) st.o[j][e] *= c;
-    }
-    const float p = exp2f(s[j] - st.m[j]);
-    st.l[j] += p;
-#pragma unroll
-    for (int e = 0; e < 16; e++) st.o[j][e] = fmaf(p, vf[e], st.o[j][e]);
+struct State {
+  float acc[G][2];  // weighted value sums, 2 channels x G heads
+  float m, l;       // running max / sum of head `warp` (meaningful in warps < G, lane 0)
+};
+
+// The G dot products of a token, reduced over its 8 lanes: afterwards lane `sl` holds the
+// full score of head hidx(sl). Partner lanes exchange halves of their vectors at each step.
+template <int G>
+__device__ __forceinline__ float reduce_scores(float (&v)[G], int sl, int& hidx) {
+  if constexpr (G == 4) {
+    const bool b2 = sl & 4, b1 = sl & 2;
+    const float s0 = b2 ? v[0] : v[2], s1 = b2 ? v[1] : v[3];
+    const float r0 = __shfl_xor_sync(0xffffffffu, s0, 4);
+    const float r1 = __shfl_xor_sync(0xffffffffu, s1, 4);
+    const float u0 = (b2 ? v[2] : v[0]) + r0, u1 = (b2 ? v[3] : v[1]) + r1;
+    const float r = __shfl_xor_sync(0xffffffffu, b1 ? u0 : u1, 2);
+    float w = (b1 ? u1 : u0) + r;
+    w += __shfl_xor_sync(0xffffffffu, w, 1);
+    hidx = (b2 ? 2 : 0) + (b1 ? 1 : 0);
+    return w;
+  } else if constexpr (G == 2) {
+    const bool b2 = sl & 4;
+    const float r = __shfl_xor_sync(0xffffffffu, b2 ? v[0] : v[1], 4);
+    float w = (b2 ? v[1] : v[0]) + r;
+    w += __shfl_xor_sync(0xffffffffu, w, 2);
+    w += __shfl_xor_sync(0xffffffffu, w, 1);
+    hidx = b2 ? 1 : 0;
+    return w;
+  } else {
+    float w = v[0];
+    w += __shfl_xor_sync(0xffffffffu, w, 4);
+    w += __shfl_xor_sync(0xffffffffu, w, 2);
+    w += __shfl_xor_sync(0xffffffffu, w, 1);
+    hidx = 0;
+    return w;
   }
 }
 
@@ -180,64 +193,128 @@ __device__ __forceinline__ void load_query(float (&qf)[G][16], const AttArgs& a,
     const uint4 u0 = *reinterpret_cast<const uint4*>(qp + 8 * sl);
     const uint4 u1 = *reinterpret_cast<const uint4*>(qp + 64 + 8 * sl);
     float f[16];
-    unpack16<G>(u0, u1, f);
+    unpack16(u0, u1, f);
 #pragma unroll
     for (int e = 0; e < 16; e++) qf[j][e] = f[e] * a.qscale;
   }
 }
 
-// Merge of the 16 per-group states of a CTA, then either the final output (one split) or
-// a partial plus the last-CTA combine. `red` is shared memory of at least
-// 16 * G * (2 + 128) floats. Called by all threads of the CTA.
+// One segment held in shared memory at `slot` (K page, then V page): scores, softmax and
+// value accumulation. Called by the 128 compute threads together.
 template <int G>
-__device__ void finish(const AttArgs& a, const State<G>& st, int b, int h, int split,
-                       float* red, int nthreads) {
+__device__ __forceinline__ void process_segment(State<G>& st, const float (&qf)[G][16],
+                                                Scratch& sc, uint32_t slot, int k, int t0,
+                                                int t1) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int grp = lane >> 3, sl = lane & 7;
-  float* rm = red;                       // [16][G]
-  float* rl = rm + 16 * G;               // [16][G]
-  float* ro = rl + 16 * G;               // [16][G][128]
-  __shared__ int is_last;
-  if (warp < kWarps) {
+  // scores
+  {
+    const int grp = lane >> 3, sl = lane & 7;
     const int r = warp * 4 + grp;
+    const uint32_t kb = slot + r * (kHeadDim * 2);
+    const uint4 k0 = lds128(kb + sl * 16), k1 = lds128(kb + (sl + 8) * 16);
+    float kf[16];
+    unpack16(k0, k1, kf);
+    float v[G];
 #pragma unroll
     for (int j = 0; j < G; j++) {
-      if (sl == 0) {
-        rm[r * G + j] = st.m[j];
-        rl[r * G + j] = st.l[j];
-      }
+      float acc = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 8; e++) {
-        ro[(r * G + j) * kHeadDim + 8 * sl + e] = st.o[j][e];
-        ro[(r * G + j) * kHeadDim + 64 + 8 * sl + e] = st.o[j][8 + e];
+      for (int e = 0; e < 16; e++) acc = fmaf(qf[j][e], kf[e], acc);
+      v[j] = acc;
+    }
+    int hidx;
+    const float s = reduce_scores<G>(v, sl, hidx);
+    const int t = k * kPage + r;
+    constexpr int kOwners = 8 / G;  // lanes holding the same head; the first one writes
+    if ((sl & (kOwners - 1)) == 0) sc.score[r][hidx] = (t >= t0 && t < t1) ? s : kNeg;
+  }
+  compute_bar();
+  // softmax of the segment, one warp per head (lanes 0..15 carry the 16 tokens)
+  if (warp < G) {
+    const float s = lane < kPage ? sc.score[lane][warp] : kNeg;
+    float mx = s;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float m_new = fmaxf(st.m, mx);
+    const float c = exp2f(st.m - m_new);
+    const float p = s == kNeg ? 0.0f : exp2f(s - m_new);
+    float ps = p;
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    st.l = st.l * c + ps;
+    st.m = m_new;
+    if (lane < kPage) sc.prob[lane][warp] = p;
+    if (lane == 0) sc.rescale[warp] = c;
+  }
+  compute_bar();
+  // values
+  {
+    const int d = (warp & 1) * 64 + 2 * lane;
+    const int th = warp >> 1;
+#pragma unroll
+    for (int j = 0; j < G; j++) {
+      const float c = sc.rescale[j];
+      st.acc[j][0] *= c;
+      st.acc[j][1] *= c;
+    }
+    const uint32_t vb = slot + kBlockBytesBf16 + d * 2;
+    const int tb = k * kPage + th * 8;
+#pragma unroll
+    for (int tt = 0; tt < 8; tt++) {
+      const int t = tb + tt;
+      if (t < t0 || t >= t1) continue;  // warp-uniform; skipped slots may hold any bits
+      uint32_t w;
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(vb + (th * 8 + tt) * kHeadDim * 2));
+      const float lo = bf16_lo(w), hi = bf16_hi(w);
+      const float4 p4 = *reinterpret_cast<const float4*>(sc.prob[th * 8 + tt]);
+      const float p[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+      for (int j = 0; j < G; j++) {
+        st.acc[j][0] = fmaf(p[j], lo, st.acc[j][0]);
+        st.acc[j][1] = fmaf(p[j], hi, st.acc[j][1]);
       }
     }
   }
-  __syncthreads();
-  const int hq = a.hkv * G;
-  if (tid < kHeadDim) {
-    const int d = tid;
+  // the next segment's score writes are ordered after these reads by its first barrier
+}
+
+// Final merge: the two token halves, then either the output (one split) or a partial plus
+// the last-CTA combine over all splits. `red` is shared memory of at least
+// max(G * 128, G * kMaxSplits + 8) floats. Called by all threads of the CTA.
+template <int G>
+__device__ void finish(const AttArgs& a, State<G>& st, Scratch& sc, int b, int h, int split,
+                       float* red) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ int is_last;
+  const int d = (warp & 1) * 64 + 2 * lane;
+  if (warp < kWarps && (warp >> 1) == 1) {
 #pragma unroll
     for (int j = 0; j < G; j++) {
-      float M = -FLT_MAX;
-      for (int r = 0; r < 16; r++) M = fmaxf(M, rm[r * G + j]);
-      float L = 0.0f, O = 0.0f;
-      for (int r = 0; r < 16; r++) {
-        const float w = rl[r * G + j] > 0.0f ? exp2f(rm[r * G + j] - M) : 0.0f;
-        L = fmaf(rl[r * G + j], w, L);
-        O = fmaf(ro[(r * G + j) * kHeadDim + d], w, O);
-      }
+      red[j * kHeadDim + d] = st.acc[j][0];
+      red[j * kHeadDim + d + 1] = st.acc[j][1];
+    }
+  }
+  if (warp < G && lane == 0) {
+    sc.m[warp] = st.m;
+    sc.l[warp] = st.l;
+  }
+  __syncthreads();
+  const int hq = a.hkv * G;
+  if (warp < kWarps && (warp >> 1) == 0) {
+#pragma unroll
+    for (int j = 0; j < G; j++) {
+      const float o0 = st.acc[j][0] + red[j * kHeadDim + d];
+      const float o1 = st.acc[j][1] + red[j * kHeadDim + d + 1];
       const size_t row = (size_t)b * hq + (size_t)h * G + j;
+      const float L = sc.l[j];
       if (a.nsplit == 1) {
-        a.out[row * kHeadDim + d] = L > 0.0f ? O / L : 0.0f;
-        if (d == 0 && a.lse) a.lse[row] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        *reinterpret_cast<float2*>(a.out + row * kHeadDim + d) = make_float2(o0 * inv, o1 * inv);
+        if (d == 0 && a.lse) a.lse[row] = L > 0.0f ? (sc.m[j] + log2f(L)) * kLn2 : -INFINITY;
       } else {
         const size_t p = row * a.nsplit + split;
-        a.part_o[p * kHeadDim + d] = O;
-        if (d == 0) {
-          a.part_ml[2 * p] = M;
-          a.part_ml[2 * p + 1] = L;
-        }
+        *reinterpret_cast<float2*>(a.part_o + p * kHeadDim + d) = make_float2(o0, o1);
+        if (d == 0) *reinterpret_cast<float2*>(a.part_ml + 2 * p) = make_float2(sc.m[j], L);
       }
     }
   }
@@ -251,25 +328,65 @@ __device__ void finish(const AttArgs& a, const State<G>& st, int b, int h, int s
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  if (tid < kHeadDim) {
-    const int d = tid;
+  // weights of the splits: warp j handles head j
+  float* wgt = red;                   // [G][kMaxSplits]
+  float* tot = red + G * kMaxSplits;  // [G] sum of weighted l
+  float* mm = tot + 4;                // [G] max
+  if (warp < G) {
+    const size_t row = (size_t)b * hq + (size_t)h * G + warp;
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + row * a.nsplit;
+    float2 v0 = make_float2(kNeg, 0.0f), v1 = make_float2(kNeg, 0.0f);
+    if (lane < a.nsplit) v0 = __ldcg(ml + lane);
+    if (lane + 32 < a.nsplit) v1 = __ldcg(ml + lane + 32);
+    float M = fmaxf(v0.x, v1.x);
 #pragma unroll
-    for (int j = 0; j < G; j++) {
-      const size_t row = (size_t)b * hq + (size_t)h * G + j;
-      const float* ml = a.part_ml + 2 * row * a.nsplit;
-      const float* po = a.part_o + row * a.nsplit * kHeadDim;
-      float M = -FLT_MAX;
-      for (int sp = 0; sp < a.nsplit; sp++) M = fmaxf(M, __ldcg(ml + 2 * sp));
-      float L = 0.0f, O = 0.0f;
-      for (int sp = 0; sp < a.nsplit; sp++) {
-        const float l = __ldcg(ml + 2 * sp + 1);
-        const float w = l > 0.0f ? exp2f(__ldcg(ml + 2 * sp) - M) : 0.0f;
-        L = fmaf(l, w, L);
-        O = fmaf(__ldcg(po + (size_t)sp * kHeadDim + d), w, O);
-      }
-      a.out[row * kHeadDim + d] = L > 0.0f ? O / L : 0.0f;
-      if (d == 0 && a.lse) a.lse[row] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w0 = v0.y > 0.0f ? exp2f(v0.x - M) : 0.0f;
+    const float w1 = v1.y > 0.0f ? exp2f(v1.x - M) : 0.0f;
+    if (lane < a.nsplit) wgt[warp * kMaxSplits + lane] = w0;
+    if (lane + 32 < a.nsplit) wgt[warp * kMaxSplits + lane + 32] = w1;
+    float L = v0.y * w0 + v1.y * w1;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) {
+      tot[warp] = L;
+      mm[warp] = M;
     }
+  }
+  __syncthreads();
+  // outputs: thread -> (head j, 4 channels), float4 loads of all splits in flight
+  if (tid < G * 32) {
+    const int j = tid >> 5, d4 = (tid & 31) * 4;
+    const size_t row = (size_t)b * hq + (size_t)h * G + j;
+    const float4* po = reinterpret_cast<const float4*>(a.part_o + row * a.nsplit * kHeadDim + d4);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    int sp = 0;
+    for (; sp + 8 <= a.nsplit; sp += 8) {
+      float4 x[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) x[u] = __ldcg(po + (size_t)(sp + u) * (kHeadDim / 4));
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const float w = wgt[j * kMaxSplits + sp + u];
+        o.x = fmaf(x[u].x, w, o.x);
+        o.y = fmaf(x[u].y, w, o.y);
+        o.z = fmaf(x[u].z, w, o.z);
+        o.w = fmaf(x[u].w, w, o.w);
+      }
+    }
+    for (; sp < a.nsplit; sp++) {
+      const float4 x = __ldcg(po + (size_t)sp * (kHeadDim / 4));
+      const float w = wgt[j * kMaxSplits + sp];
+      o.x = fmaf(x.x, w, o.x);
+      o.y = fmaf(x.y, w, o.y);
+      o.z = fmaf(x.z, w, o.z);
+      o.w = fmaf(x.w, w, o.w);
+    }
+    const float L = tot[j];
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    *reinterpret_cast<float4*>(a.out + row * kHeadDim + d4) =
+        make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+    if (d4 == 0 && a.lse) a.lse[row] = L > 0.0f ? (mm[j] + log2f(L)) * kLn2 : -INFINITY;
   }
   if (tid == 0) a.counters[(size_t)b * a.hkv + h] = 0;
 }
@@ -277,24 +394,26 @@ __device__ void finish(const AttArgs& a, const State<G>& st, int b, int h, int s
 template <int G>
 __device__ __forceinline__ void init_state(State<G>& st) {
 #pragma unroll
-  for (int j = 0; j < G; j++) {
-    st.m[j] = -FLT_MAX;
-    st.l[j] = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 16; e++) st.o[j][e] = 0.0f;
-  }
+  for (int j = 0; j < G; j++) st.acc[j][0] = st.acc[j][1] = 0.0f;
+  st.m = kNeg;
+  st.l = 0.0f;
+}
+
+size_t red_floats(int G) {
+  return std::max<size_t>((size_t)G * kHeadDim, (size_t)G * kMaxSplits + 8);
 }
 
 // ------------------------------------------------------------------ HBM path
 
 template <int G, bool DENSE>
-__global__ void __launch_bounds__(kTmaThreads, 2) attend_tma_kernel(const AttArgs a) {
+__global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kSlotBytes);
   uint64_t* empty = full + kStages;
+  Scratch& sc = *reinterpret_cast<Scratch*>(empty + kStages);
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -352,10 +471,8 @@ __global__ void __launch_bounds__(kTmaThreads, 2) attend_tma_kernel(const AttArg
       }
     }
   } else {
-    const int grp = lane >> 3, sl = lane & 7;
-    const int r = warp * 4 + grp;  // token slot within the page
     float qf[G][16];
-    load_query<G>(qf, a, b, h, sl);
+    load_query<G>(qf, a, b, h, lane & 7);
     for (int i = i0; i < i1; i++) {
       const int j = i - i0, s = j % kStages;
       if (!mbar_wait(&full[s], (j / kStages) & 1)) {
@@ -364,32 +481,29 @@ __global__ void __launch_bounds__(kTmaThreads, 2) attend_tma_kernel(const AttArg
       }
       int k, t0, t1;
       segment_at(S, i, a.sink, k, t0, t1);
-      if (t0 < t1) {
-        const int t = k * kPage + r;
-        const uint32_t kb = smem_addr(ring + s * kSlotBytes) + r * (kHeadDim * 2);
-        const uint32_t vb = kb + kBlockBytesBf16;
-        const uint4 k0 = lds128(kb + sl * 16), k1 = lds128(kb + (sl + 8) * 16);
-        const uint4 v0 = lds128(vb + sl * 16), v1 = lds128(vb + (sl + 8) * 16);
-        attend_token<G>(st, qf, k0, k1, v0, v1, t >= t0 && t < t1);
-      }
+      if (t0 < t1) process_segment<G>(st, qf, sc, smem_addr(ring + s * kSlotBytes), k, t0, t1);
+      // each compute warp is done with slot s once its own reads are behind it
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
   __syncthreads();
-  finish<G>(a, st, b, h, split, reinterpret_cast<float*>(ring), kTmaThreads);
+  finish<G>(a, st, sc, b, h, split, reinterpret_cast<float*>(ring));
 }
 
 // ---------------------------------------------------------- mapped-host path
 
 template <int G, bool DENSE>
-__global__ void __launch_bounds__(kHostThreads, 2) attend_host_kernel(const AttArgs a) {
+__global__ void __launch_bounds__(kHostThreads, 3) attend_host_kernel(const AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  float* red = reinterpret_cast<float*>(smem_raw);
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* slots = smem;  // two slots: the segment in use and the next one
+  Scratch& sc = *reinterpret_cast<Scratch*>(smem + 2 * kSlotBytes);
+  float* red = reinterpret_cast<float*>(smem + 2 * kSlotBytes + sizeof(Scratch));
+
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int grp = lane >> 3, sl = lane & 7;
-  const int r = warp * 4 + grp;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int n_raw = a.seq_lens[b];
   if (tid == 0 && split == 0 && h == 0 && (n_raw < 0 || n_raw > a.max_pages * kPage))
     set_error(a.err, kDevErrCheck);
@@ -399,56 +513,68 @@ __global__ void __launch_bounds__(kHostThreads, 2) attend_host_kernel(const AttA
   State<G> st;
   init_state<G>(st);
   float qf[G][16];
-  load_query<G>(qf, a, b, h, sl);
-  // two segments per round, all eight 16-byte loads of a lane in flight together
-  for (int i = i0; i < i1; i += 2) {
-    uint4 kk[2][2], vv[2][2];
-    int k[2], t0[2], t1[2];
-    bool live[2];
-#pragma unroll
-    for (int u = 0; u < 2; u++) {
-      live[u] = false;
-      if (i + u < i1) {
-        segment_at(S, i + u, a.sink, k[u], t0[u], t1[u]);
-        if (t0[u] < t1[u]) {
-          const int page = a.page_table[(size_t)b * a.max_pages + k[u]];
-          if (page >= 0 && page < a.num_pages) {
-            live[u] = true;
-            const size_t off = (((size_t)page * a.hkv + h) * kPage + r) * kHeadDim;
-            kk[u][0] = ldg128_nc(a.k + off + 8 * sl);
-            kk[u][1] = ldg128_nc(a.k + off + 64 + 8 * sl);
-            vv[u][0] = ldg128_nc(a.v + off + 8 * sl);
-            vv[u][1] = ldg128_nc(a.v + off + 64 + 8 * sl);
-          } else {
-            set_error(a.err, kDevErrCheck);
-          }
-        }
-      }
+  load_query<G>(qf, a, b, h, lane & 7);
+
+  // each thread copies 64 of the segment's 8192 bytes: K bytes [32 tid, +32), then V
+  auto fetch = [&](int i, uint4 (&buf)[4], int& k, int& t0, int& t1) {
+    segment_at(S, i, a.sink, k, t0, t1);
+    if (t0 >= t1) return;
+    const int page = a.page_table[(size_t)b * a.max_pages + k];
+    if (page < 0 || page >= a.num_pages) {
+      set_error(a.err, kDevErrCheck);
+      t0 = t1 = 0;
+      return;
     }
-#pragma unroll
-    for (int u = 0; u < 2; u++) {
-      if (!live[u]) continue;  // uniform across the warp: same segment for all lanes
-      const int t = k[u] * kPage + r;
-      attend_token<G>(st, qf, kk[u][0], kk[u][1], vv[u][0], vv[u][1], t >= t0[u] && t < t1[u]);
-    }
+    const size_t off = ((size_t)page * a.hkv + h) * kPage * kHeadDim;
+    const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k + off);
+    const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v + off);
+    buf[0] = ldg128_nc(kp + tid * 32);
+    buf[1] = ldg128_nc(kp + tid * 32 + 16);
+    buf[2] = ldg128_nc(vp + tid * 32);
+    buf[3] = ldg128_nc(vp + tid * 32 + 16);
+  };
+  auto store = [&](int slot, const uint4 (&buf)[4]) {
+    uint4* kd = reinterpret_cast<uint4*>(slots + slot * kSlotBytes + tid * 32);
+    uint4* vd = reinterpret_cast<uint4*>(slots + slot * kSlotBytes + kBlockBytesBf16 + tid * 32);
+    kd[0] = buf[0];
+    kd[1] = buf[1];
+    vd[0] = buf[2];
+    vd[1] = buf[3];
+  };
+  uint4 nxt[4];
+  int kn = 0, t0n = 0, t1n = 0;
+  if (i0 < i1) fetch(i0, nxt, kn, t0n, t1n);
+  for (int i = i0; i < i1; i++) {
+    const int slot = (i - i0) & 1;
+    const int k = kn, t0 = t0n, t1 = t1n;
+    if (t0 < t1) store(slot, nxt);
+    if (i + 1 < i1) fetch(i + 1, nxt, kn, t0n, t1n);  // in flight while this one computes
+    compute_bar();
+    if (t0 < t1) process_segment<G>(st, qf, sc, smem_addr(slots + slot * kSlotBytes), k, t0, t1);
   }
   __syncthreads();
-  finish<G>(a, st, b, h, split, red, kHostThreads);
+  finish<G>(a, st, sc, b, h, split, red);
 }
 
-size_t red_bytes(int G) { return sizeof(float) * 16 * G * (2 + kHeadDim); }
+size_t tma_smem(int G) {
+  const size_t ring = (size_t)kStages * kSlotBytes + 2 * kStages * sizeof(uint64_t) + sizeof(Scratch);
+  return 128 + std::max(ring, red_floats(G) * sizeof(float) + 2 * kStages * 8 + sizeof(Scratch));
+}
+
+size_t host_smem(int G) {
+  return 128 + 2 * kSlotBytes + sizeof(Scratch) + red_floats(G) * sizeof(float);
+}
 
 template <int G, bool DENSE>
 cudaError_t launch_g(const AttArgs& a, dim3 grid, bool host, cudaStream_t st) {
   if (host) {
-    const size_t smem = red_bytes(G);
+    const size_t smem = host_smem(G);
     cudaError_t e = cudaFuncSetAttribute(attend_host_kernel<G, DENSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attend_host_kernel<G, DENSE><<<grid, kHostThreads, smem, st>>>(a);
   } else {
-    const size_t ring = (size_t)kStages * kSlotBytes + 2 * kStages * sizeof(uint64_t);
-    const size_t smem = 128 + std::max(ring, red_bytes(G));
+    const size_t smem = tma_smem(G);
     cudaError_t e = cudaFuncSetAttribute(attend_tma_kernel<G, DENSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -461,16 +587,16 @@ cudaError_t launch_g(const AttArgs& a, dim3 grid, bool host, cudaStream_t st) {
 
 int attend_splits(const Shape& s, bool dense, bool host, int num_sms) {
   const long long units = (long long)s.batch * s.hkv;
-  const int per_sm = host ? 4 : 2;
   long long segs;
   if (dense) {
     segs = s.max_pages;
   } else {
     segs = (s.sink + kPage - 1) / kPage + 1 + s.k2 + (s.window + kPage - 1) / kPage + 1;
   }
+  // dense: about three CTAs per SM; sparse: about one, each with several segments
+  const int per_sm = host ? 4 : (dense ? 3 : 1);
   long long want = ((long long)num_sms * per_sm + units - 1) / units;
-  // at least two segments per CTA so that loads and compute overlap
-  want = std::min<long long>(want, std::max<long long>(1, segs / 2));
+  want = std::min<long long>(want, std::max<long long>(1, segs / 4));
   return (int)std::max<long long>(1, std::min<long long>(want, kMaxSplits));
 }
 
