@@ -1,0 +1,48 @@
+"""The benchmark's multi-rank host logic on CPU: two gloo ranks, each timing its own
+independent decode problem; the job's step time is the max over ranks and the whole-job
+value divides it by the rank count (weak scaling, no data-path collective)."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w, r, local = bench.dist_env()
+        assert (w, r, local) == (world, rank, rank)
+        step_ms = 0.050 + 0.010 * rank          # rank 1 is the slower one
+        worst = bench.reduce_max(step_ms, world)
+        bench.barrier(world)
+        out[rank] = (worst, bench.job_value(worst, world))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_max_and_job_value():
+    world = 2
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
+    for rank in range(world):
+        worst, value = out[rank]
+        assert worst == pytest.approx(0.060)
+        assert value == pytest.approx(0.060 * 1e3 / 2)
+
+
+def test_single_rank_is_plain():
+    import bench
+    assert bench.reduce_max(1.25, 1) == 1.25
+    assert bench.job_value(0.1, 1) == pytest.approx(100.0)
