@@ -218,6 +218,29 @@ int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * hsa_select without a workspace, for callers that cannot allocate device memory: code
+ * embedded in a host program that owns every device allocation through its own pool, or
+ * that runs on a latency-critical path where cudaMalloc (which can synchronise the device)
+ * is not allowed. Nothing in the method calls for this; the pages have no counterpart.
+ * Same arguments and results as hsa_select minus the workspace. Its scratch (block and
+ * tile score maxima) is one fixed 4 MiB device array inside the library, held by every GPU
+ * that loads the library until the process exits: shapes with
+ *   round256(4 * batch * hkv * max_pages_per_seq)
+ *   + round256(4 * batch * hkv * ceil(max_pages_per_seq / 4)) > 4 MiB
+ * (e.g. more than about 800K 16-token blocks summed over sequences and kv heads) return
+ * HSA_ERR_WORKSPACE_TOO_SMALL. The array's device address is looked up on the first call on
+ * each device (make that first call before any stream capture). All calls share the array
+ * and it keeps the last call's contents (each call writes every entry it then reads, so
+ * nothing needs clearing); calls that may overlap on the GPU, on any stream, race on it and
+ * must be ordered by the caller. Device-side bounds-check failures are skipped but not
+ * reported (there is no error word). Calls no allocating routine.
+ */
+int32_t hsa_select_noalloc(const hsa_dims* d, const void* q, const int8_t* kq,
+                           const float* k_scale, const int32_t* page_table,
+                           const int32_t* seq_lens, int32_t* chunk_idx, int32_t* n_chunks,
+                           int32_t* block_idx, int32_t* n_blocks, void* stream);
+
+/*
  * Reads and clears the device error word of `workspace` after synchronising `stream`:
  * *code receives HSA_OK, HSA_ERR_TIMEOUT or HSA_ERR_DEVICE_CHECK. This is the one call
  * that synchronises.

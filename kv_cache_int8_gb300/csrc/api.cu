@@ -468,4 +468,70 @@ int32_t hsa_read_device_error(void* workspace, void* stream, int32_t* code) {
   return HSA_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+// hsa_select_noalloc: hsa_select for callers that cannot allocate device memory. Its
+// scratch (the per-block and per-tile score maxima) lives in one fixed array that every
+// GPU loading this library holds until the process exits.
+
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+__device__ __align__(256) static unsigned char g_select_scratch[kNoAllocScratchBytes];
+
+// Device address of g_select_scratch on the current device, looked up once per device
+// (host code only sees a stand-in for the array, never its device address).
+int32_t noalloc_scratch(char** out) {
+  static std::mutex mu;
+  static char* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return HSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return HSA_ERR_CUDA;
+    }
+    addr[dev] = static_cast<char*>(p);
+  }
+  *out = addr[dev];
+  return HSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t hsa_select_noalloc(const hsa_dims* d, const void* q, const int8_t* kq,
+                           const float* k_scale, const int32_t* page_table,
+                           const int32_t* seq_lens, int32_t* chunk_idx, int32_t* n_chunks,
+                           int32_t* block_idx, int32_t* n_blocks, void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, true);
+  if (rc != HSA_OK) return rc;
+  if (!q || !kq || !k_scale || !page_table || !seq_lens || !n_blocks || (!block_idx && s.k2 > 0))
+    return HSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kq, 16) || !aligned(k_scale, 16)) return HSA_ERR_INVALID_ARG;
+  rc = check_prune_fits(s);
+  if (rc != HSA_OK) return rc;
+  // block maxima then tile maxima, as in the select workspace (without its error word)
+  if (select_bm_bytes(s) + select_tm_bytes(s) > kNoAllocScratchBytes)
+    return HSA_ERR_WORKSPACE_TOO_SMALL;
+  char* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != HSA_OK) return rc;
+  int32_t* bm = reinterpret_cast<int32_t*>(scratch);
+  int32_t* tm = reinterpret_cast<int32_t*>(scratch + select_bm_bytes(s));
+  cudaStream_t st = as_stream(stream);
+  // Every entry of the scratch that the prune kernel reads is written by the scorer in the
+  // same call, so nothing has to be cleared; device-side check failures are skipped, not
+  // reported (there is no error word).
+  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, nullptr, st);
+  if (rc != HSA_OK) return rc;
+  return cuda_status(hsa::launch_prune(s, seq_lens, bm, tm, chunk_idx, n_chunks, block_idx,
+                                       n_blocks, nullptr, st));
+}
+
 }  // extern "C"

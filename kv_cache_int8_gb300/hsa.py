@@ -35,7 +35,7 @@ HSA_OP_STEP = 4
 EXPORTS = (
     "hsa_workspace_bytes", "hsa_status_string", "hsa_quantize_keys", "hsa_append_kv",
     "hsa_score_blocks", "hsa_prune", "hsa_select", "hsa_attend", "dense_decode",
-    "hsa_decode_step", "hsa_read_device_error",
+    "hsa_decode_step", "hsa_read_device_error", "hsa_select_noalloc",
 )
 
 
@@ -110,6 +110,7 @@ def load(path: Optional[str] = None):
         "hsa_decode_step": (I32, [D, ctypes.POINTER(hsa_step_io), P, P, P, P, P, P, P, P, P,
                                   SZ, P]),
         "hsa_read_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
+        "hsa_select_noalloc": (I32, [D, P, P, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -194,6 +195,17 @@ def hsa_select(d: Dims, q, kq, k_scale, page_table, seq_lens, chunk_idx, n_chunk
         ctypes.byref(cd), _p(q), _p(kq), _p(k_scale), _p(page_table), _p(seq_lens),
         _p(chunk_idx), _p(n_chunks), _p(block_idx), _p(n_blocks), _p(ws), ws.numel(),
         _stream(stream)))
+
+
+def hsa_select_noalloc(d: Dims, q, kq, k_scale, page_table, seq_lens, chunk_idx, n_chunks,
+                       block_idx, n_blocks, stream=None) -> None:
+    """hsa_select for callers that cannot allocate device memory: the scratch is a fixed
+    4 MiB array inside the library (see include/hsa.h for the size limit and the sharing
+    rules)."""
+    cd = d.c()
+    _check("hsa_select_noalloc", load().hsa_select_noalloc(
+        ctypes.byref(cd), _p(q), _p(kq), _p(k_scale), _p(page_table), _p(seq_lens),
+        _p(chunk_idx), _p(n_chunks), _p(block_idx), _p(n_blocks), _stream(stream)))
 
 
 def hsa_attend(d: Dims, q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks, out,
