@@ -192,7 +192,7 @@ int32_t check_prune_fits(const Shape& s) {
 int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, const void* k,
                   const void* v, const int32_t* pt, const int32_t* lens, const int32_t* bidx,
                   const int32_t* nb, float* out, float* lse, char* ws, const AttendLayout& l,
-                  cudaStream_t st) {
+                  cudaStream_t st, bool early) {
   const void* kd = nullptr;
   const void* vd = nullptr;
   int32_t rc = kv_pointer(d, k, &kd);
@@ -206,7 +206,7 @@ int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, 
   buf.part_o = reinterpret_cast<float*>(ws + l.part_o);
   buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(s, dense, host, num_sms()));
   return cuda_status(hsa::launch_attend(s, dense, host, q, kd, vd, pt, lens, bidx, nb, out, lse,
-                                        buf, reinterpret_cast<int*>(ws), st));
+                                        buf, reinterpret_cast<int*>(ws), st, early));
 }
 
 }  // namespace
@@ -296,7 +296,7 @@ int32_t hsa_append_kv(const hsa_dims* d, const void* k_new, const void* v_new, v
   if (rc != HSA_OK) return rc;
   return cuda_status(hsa::launch_append_kv(s, k_new, v_new, const_cast<void*>(kd),
                                            const_cast<void*>(vd), kq, k_scale, page_table,
-                                           seq_lens, nullptr, as_stream(stream)));
+                                           seq_lens, nullptr, as_stream(stream), false));
 }
 
 int32_t hsa_score_blocks(const hsa_dims* d, const void* q, const int8_t* kq,
@@ -366,7 +366,7 @@ int32_t hsa_attend(const hsa_dims* d, const void* q, const void* k_cache, const 
   if (rc != HSA_OK) return rc;
   char* ws = static_cast<char*>(workspace);
   return do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks,
-                   out, lse, ws, attend_layout(s, kErrBytes), as_stream(stream));
+                   out, lse, ws, attend_layout(s, kErrBytes), as_stream(stream), false);
 }
 
 int32_t dense_decode(const hsa_dims* d, const void* q, const void* k_cache, const void* v_cache,
@@ -382,7 +382,7 @@ int32_t dense_decode(const hsa_dims* d, const void* q, const void* k_cache, cons
   if (rc != HSA_OK) return rc;
   char* ws = static_cast<char*>(workspace);
   return do_attend(d, s, true, q, k_cache, v_cache, page_table, seq_lens, nullptr, nullptr, out,
-                   lse, ws, attend_layout(s, kErrBytes), as_stream(stream));
+                   lse, ws, attend_layout(s, kErrBytes), as_stream(stream), false);
 }
 
 int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache, void* v_cache,
@@ -431,19 +431,30 @@ int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
   if (rc != HSA_OK) return rc;
   rc = kv_pointer(d, v_cache, &vd);
   if (rc != HSA_OK) return rc;
-  cudaError_t e = hsa::launch_append_kv(s, kn, vn, const_cast<void*>(kd), const_cast<void*>(vd),
-                                        kq, k_scale, page_table, seq_lens, err, st);
-  if (e != cudaSuccess) return HSA_ERR_CUDA;
   int32_t* bm = reinterpret_cast<int32_t*>(ws + l.block_max);
   int32_t* tm = reinterpret_cast<int32_t*>(ws + l.tile_max);
   int32_t* bidx = block_idx ? block_idx : reinterpret_cast<int32_t*>(ws + l.block_idx);
   int32_t* nb = n_blocks ? n_blocks : reinterpret_cast<int32_t*>(ws + l.n_blocks);
+  cudaError_t e;
+  // With a window of at least one token the new token (slot N - 1) is never a scored
+  // candidate, so the append runs beside the scorer; with no window it goes first.
+  const bool beside = s.window >= 1;
+  if (!beside) {
+    e = hsa::launch_append_kv(s, kn, vn, const_cast<void*>(kd), const_cast<void*>(vd), kq,
+                              k_scale, page_table, seq_lens, err, st, false);
+    if (e != cudaSuccess) return HSA_ERR_CUDA;
+  }
   rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st);
   if (rc != HSA_OK) return rc;
+  if (beside) {
+    e = hsa::launch_append_kv(s, kn, vn, const_cast<void*>(kd), const_cast<void*>(vd), kq,
+                              k_scale, page_table, seq_lens, err, st, true);
+    if (e != cudaSuccess) return HSA_ERR_CUDA;
+  }
   e = hsa::launch_prune(s, seq_lens, bm, tm, nullptr, nullptr, bidx, nb, err, st);
   if (e != cudaSuccess) return HSA_ERR_CUDA;
   rc = do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, bidx, nb, out, lse, ws,
-                 l.att, st);
+                 l.att, st, true);
   if (rc != HSA_OK) return rc;
   if (io->io_on_host) {
     e = cudaMemcpyAsync(io->out, out, (size_t)s.batch * s.hq * hsa::kHeadDim * 4,

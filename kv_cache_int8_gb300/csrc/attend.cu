@@ -13,19 +13,18 @@
 // 16-token page clipped to a token range: the sink pages, the kept blocks (clipped to the
 // candidate region), the window pages. Dense decode uses every page of [0, N). A CTA takes
 // a contiguous share of the list for all G query heads of the group, so every K/V byte is
-// read once per group. Per segment, in shared memory:
-//   scores: warp w takes tokens 4w..4w+3, 8 lanes per token (16 channels each), G partial
-//           dot products reduced over the 8 lanes with a transposing butterfly;
-//   softmax: warp j (< G) owns head j's running max and sum (log2 domain), turns the 16
-//           scores into weights and the rescale factor of the running state;
-//   values: warp w owns channels [64 (w & 1) + 2 lane, +2) of tokens 8 (w >> 1) .. +8 for
-//           all G heads (8 accumulators per lane).
-// CTAs of one (b, h) are merged by the last one to finish (atomic counter, no waiting).
+// read once per group. Scores of a token: 8 lanes (16 channels each) form G partial dot
+// products and reduce them with a transposing butterfly; softmax in the log2 domain with a
+// running max and sum per head; CTAs of one (b, h) are merged by the last one to finish
+// (atomic counter, no waiting).
 //
 // HBM path: a producer lane fills a ring of 8 KiB slots (K page then V page of one head,
-// 4 KiB each) with cp.async.bulk copies tracked by mbarriers. Host path: K/V live in
-// pinned host memory; the compute warps copy each segment into shared memory with 16-byte
-// loads through the mapped alias, one segment ahead.
+// 4 KiB each) with cp.async.bulk copies tracked by mbarriers; each compute warp owns two
+// slots and processes whole segments on its own (see the HBM-path section).
+// Host path: K/V live in pinned host memory; the compute warps copy each segment into
+// shared memory with 16-byte loads through the mapped alias, one segment ahead, and
+// process it together (scores: warp w takes tokens 4w..4w+3; softmax: warp j owns head j;
+// values: warp w owns channels [64 (w & 1) + 2 lane, +2) of tokens 8 (w >> 1) .. +8).
 #include <algorithm>
 #include <cfloat>
 
@@ -62,66 +61,81 @@ struct AttArgs {
   int* err;
   int hkv, max_pages, num_pages, k2, sink, window, nsplit;
   float qscale;  // sm_scale * log2(e)
+  int early;     // K/V, q, page table are ready before the selection (whole decode step)
 };
 
 struct Segments {
   int n;  // context length
-  int n_sink, n_sel, n_win;
+  int n_sink, n_win, n_sel_max, n_sel;
   int sink_end, cand_hi, w0, win_k0;
   const int32_t* sel;
-  int total;
+  int total;  // n_sink + n_win + n_sel_max: the split ranges are known before the selection
 };
 
+// The attended set as a list of segments: the sink pages, the window pages, then up to K2
+// kept blocks. Everything but the number of kept blocks (n_sel, see read_selection) is
+// known from the sequence length alone.
 template <bool DENSE>
 __device__ __forceinline__ Segments make_segments(const AttArgs& a, int b, int h) {
   Segments s;
   int n = a.seq_lens[b];
   if (n < 0 || n > a.max_pages * kPage) n = 0;  // reported by the caller's check
   s.n = n;
+  s.sel = nullptr;
+  s.n_sel = 0;
   if (DENSE) {
     s.n_sink = 0;
-    s.n_sel = 0;
+    s.n_sel_max = 0;
     s.n_win = (n + kPage - 1) / kPage;
     s.sink_end = 0;
     s.cand_hi = 0;
     s.w0 = 0;
     s.win_k0 = 0;
-    s.sel = nullptr;
   } else {
     s.sink_end = min(a.sink, n);
     s.n_sink = (s.sink_end + kPage - 1) / kPage;
     s.cand_hi = n - a.window;
-    s.sel = a.block_idx + ((size_t)b * a.hkv + h) * a.k2;
-    s.n_sel = s.cand_hi > a.sink ? max(0, min(a.n_blocks[(size_t)b * a.hkv + h], a.k2)) : 0;
+    s.n_sel_max = s.cand_hi > a.sink ? a.k2 : 0;
     s.w0 = max(n - a.window, s.sink_end);
     s.win_k0 = s.w0 / kPage;
     s.n_win = s.w0 < n ? (n + kPage - 1) / kPage - s.win_k0 : 0;
   }
-  s.total = s.n_sink + s.n_sel + s.n_win;
+  s.total = s.n_sink + s.n_win + s.n_sel_max;
   return s;
 }
 
-// Segment i: page index k (token block) and the attended token range [t0, t1).
+// The kept blocks of (b, h), written by the previous kernel: read after grid_dep_wait().
+__device__ __forceinline__ void read_selection(Segments& s, const AttArgs& a, int b, int h) {
+  if (s.n_sel_max == 0) return;
+  s.sel = a.block_idx + ((size_t)b * a.hkv + h) * a.k2;
+  s.n_sel = max(0, min(a.n_blocks[(size_t)b * a.hkv + h], s.n_sel_max));
+}
+
+// Segment i: page index k (token block) and the attended token range [t0, t1) (empty when
+// t0 >= t1).
 __device__ __forceinline__ void segment_at(const Segments& s, int i, int sink, int& k, int& t0,
                                            int& t1) {
   if (i < s.n_sink) {
     k = i;
     t0 = i * kPage;
     t1 = min(t0 + kPage, s.sink_end);
-  } else if (i < s.n_sink + s.n_sel) {
-    k = s.sel[i - s.n_sink];
+  } else if (i < s.n_sink + s.n_win) {
+    k = s.win_k0 + (i - s.n_sink);
+    t0 = max(k * kPage, s.w0);
+    t1 = min(k * kPage + kPage, s.n);
+  } else {
+    const int r = i - s.n_sink - s.n_win;
+    k = 0;
+    t0 = t1 = 0;
+    if (r >= s.n_sel) return;
+    k = s.sel[r];
     const int kmax = (s.n + kPage - 1) / kPage;
     if (k < 0 || k >= kmax) {
       k = 0;
-      t0 = t1 = 0;
       return;
     }
     t0 = max(k * kPage, sink);
     t1 = min(k * kPage + kPage, s.cand_hi);
-  } else {
-    k = s.win_k0 + (i - s.n_sink - s.n_sel);
-    t0 = max(k * kPage, s.w0);
-    t1 = min(k * kPage + kPage, s.n);
   }
 }
 
@@ -278,43 +292,28 @@ __device__ __forceinline__ void process_segment(State<G>& st, const float (&qf)[
   // the next segment's score writes are ordered after these reads by its first barrier
 }
 
-// Final merge: the two token halves, then either the output (one split) or a partial plus
-// the last-CTA combine over all splits. `red` is shared memory of at least
-// max(G * 128, G * kMaxSplits + 8) floats. Called by all threads of the CTA.
+// Output of a CTA from its merged state in shared memory (o[G][128], m[G], l[G]): either the
+// final result (one split) or a partial, and then the combine over all splits by the last
+// CTA of (b, h) to finish. `red` (shared, at least G * kMaxSplits + 8 floats) may alias
+// `o`. Called by all threads of the CTA after the merged state is complete.
 template <int G>
-__device__ void finish(const AttArgs& a, State<G>& st, Scratch& sc, int b, int h, int split,
-                       float* red) {
+__device__ void finish_common(const AttArgs& a, int b, int h, int split, const float* o,
+                              const float* m, const float* l, float* red) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ int is_last;
-  const int d = (warp & 1) * 64 + 2 * lane;
-  if (warp < kWarps && (warp >> 1) == 1) {
-#pragma unroll
-    for (int j = 0; j < G; j++) {
-      red[j * kHeadDim + d] = st.acc[j][0];
-      red[j * kHeadDim + d + 1] = st.acc[j][1];
-    }
-  }
-  if (warp < G && lane == 0) {
-    sc.m[warp] = st.m;
-    sc.l[warp] = st.l;
-  }
-  __syncthreads();
   const int hq = a.hkv * G;
-  if (warp < kWarps && (warp >> 1) == 0) {
-#pragma unroll
-    for (int j = 0; j < G; j++) {
-      const float o0 = st.acc[j][0] + red[j * kHeadDim + d];
-      const float o1 = st.acc[j][1] + red[j * kHeadDim + d + 1];
+  if (tid < kCompute) {
+    for (int x = tid; x < G * kHeadDim; x += kCompute) {
+      const int j = x / kHeadDim, d = x % kHeadDim;
       const size_t row = (size_t)b * hq + (size_t)h * G + j;
-      const float L = sc.l[j];
+      const float L = l[j];
       if (a.nsplit == 1) {
-        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-        *reinterpret_cast<float2*>(a.out + row * kHeadDim + d) = make_float2(o0 * inv, o1 * inv);
-        if (d == 0 && a.lse) a.lse[row] = L > 0.0f ? (sc.m[j] + log2f(L)) * kLn2 : -INFINITY;
+        a.out[row * kHeadDim + d] = L > 0.0f ? o[x] / L : 0.0f;
+        if (d == 0 && a.lse) a.lse[row] = L > 0.0f ? (m[j] + log2f(L)) * kLn2 : -INFINITY;
       } else {
         const size_t p = row * a.nsplit + split;
-        *reinterpret_cast<float2*>(a.part_o + p * kHeadDim + d) = make_float2(o0, o1);
-        if (d == 0) *reinterpret_cast<float2*>(a.part_ml + 2 * p) = make_float2(sc.m[j], L);
+        a.part_o[p * kHeadDim + d] = o[x];
+        if (d == 0) *reinterpret_cast<float2*>(a.part_ml + 2 * p) = make_float2(m[j], L);
       }
     }
   }
@@ -359,7 +358,7 @@ __device__ void finish(const AttArgs& a, State<G>& st, Scratch& sc, int b, int h
     const int j = tid >> 5, d4 = (tid & 31) * 4;
     const size_t row = (size_t)b * hq + (size_t)h * G + j;
     const float4* po = reinterpret_cast<const float4*>(a.part_o + row * a.nsplit * kHeadDim + d4);
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int sp = 0;
     for (; sp + 8 <= a.nsplit; sp += 8) {
       float4 x[8];
@@ -368,27 +367,57 @@ __device__ void finish(const AttArgs& a, State<G>& st, Scratch& sc, int b, int h
 #pragma unroll
       for (int u = 0; u < 8; u++) {
         const float w = wgt[j * kMaxSplits + sp + u];
-        o.x = fmaf(x[u].x, w, o.x);
-        o.y = fmaf(x[u].y, w, o.y);
-        o.z = fmaf(x[u].z, w, o.z);
-        o.w = fmaf(x[u].w, w, o.w);
+        acc.x = fmaf(x[u].x, w, acc.x);
+        acc.y = fmaf(x[u].y, w, acc.y);
+        acc.z = fmaf(x[u].z, w, acc.z);
+        acc.w = fmaf(x[u].w, w, acc.w);
       }
     }
     for (; sp < a.nsplit; sp++) {
       const float4 x = __ldcg(po + (size_t)sp * (kHeadDim / 4));
       const float w = wgt[j * kMaxSplits + sp];
-      o.x = fmaf(x.x, w, o.x);
-      o.y = fmaf(x.y, w, o.y);
-      o.z = fmaf(x.z, w, o.z);
-      o.w = fmaf(x.w, w, o.w);
+      acc.x = fmaf(x.x, w, acc.x);
+      acc.y = fmaf(x.y, w, acc.y);
+      acc.z = fmaf(x.z, w, acc.z);
+      acc.w = fmaf(x.w, w, acc.w);
     }
     const float L = tot[j];
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     *reinterpret_cast<float4*>(a.out + row * kHeadDim + d4) =
-        make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     if (d4 == 0 && a.lse) a.lse[row] = L > 0.0f ? (mm[j] + log2f(L)) * kLn2 : -INFINITY;
   }
   if (tid == 0) a.counters[(size_t)b * a.hkv + h] = 0;
+}
+
+// Block-level state (host path): the two token halves merged into o[G][128]; m, l from the
+// softmax warps. `red` holds at least G * 128 + 8 floats.
+template <int G>
+__device__ void finish(const AttArgs& a, State<G>& st, Scratch& sc, int b, int h, int split,
+                       float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int d = (warp & 1) * 64 + 2 * lane;
+  if (warp < kWarps && (warp >> 1) == 1) {
+#pragma unroll
+    for (int j = 0; j < G; j++) {
+      red[j * kHeadDim + d] = st.acc[j][0];
+      red[j * kHeadDim + d + 1] = st.acc[j][1];
+    }
+  }
+  if (warp < G && lane == 0) {
+    sc.m[warp] = st.m;
+    sc.l[warp] = st.l;
+  }
+  __syncthreads();
+  if (warp < kWarps && (warp >> 1) == 0) {
+#pragma unroll
+    for (int j = 0; j < G; j++) {
+      red[j * kHeadDim + d] += st.acc[j][0];
+      red[j * kHeadDim + d + 1] += st.acc[j][1];
+    }
+  }
+  __syncthreads();
+  finish_common<G>(a, b, h, split, red, sc.m, sc.l, red);
 }
 
 template <int G>
@@ -404,6 +433,100 @@ size_t red_floats(int G) {
 }
 
 // ------------------------------------------------------------------ HBM path
+//
+// Warp-per-segment: compute warp w owns ring slots w, w + 4 and processes its segments
+// start to finish on its own (no CTA barrier per segment), so four segments are in
+// flight per CTA. Per segment: 4 rounds of (4 tokens x 8 lanes) give each lane the scores
+// of tokens 4r + lane / 8 for head hidx(lane % 8); the per-head running max and sum are
+// kept by every lane of that head; the weights go through the warp's own shared scratch
+// to the value phase, where lane l owns channels 4l .. 4l + 3 of all G heads.
+
+struct WarpScratch {
+  float prob[kPage][4];  // weights of the segment's tokens, per head
+  float rescale[4];      // factor applied to the running sums of each head
+  float pad[4];
+};
+
+template <int G>
+struct WarpState {
+  float acc[G][4];  // weighted value sums: channels 4 lane .. 4 lane + 3, per head
+  float m, l;       // running max / sum of head hidx (this lane's head)
+};
+
+template <int G>
+__device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)[G][16],
+                                             WarpScratch& ws, uint32_t slot, int k, int t0,
+                                             int t1) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 3, sl = lane & 7;
+  float sc[4];
+  int hidx = 0;
+#pragma unroll
+  for (int it = 0; it < 4; it++) {
+    const int r = 4 * it + g;
+    const uint32_t kb = slot + r * (kHeadDim * 2);
+    const uint4 k0 = lds128(kb + sl * 16), k1 = lds128(kb + (sl + 8) * 16);
+    float kf[16];
+    unpack16(k0, k1, kf);
+    float v[G];
+#pragma unroll
+    for (int j = 0; j < G; j++) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 16; e++) acc = fmaf(qf[j][e], kf[e], acc);
+      v[j] = acc;
+    }
+    const float s = reduce_scores<G>(v, sl, hidx);
+    const int t = k * kPage + r;
+    sc[it] = (t >= t0 && t < t1) ? s : kNeg;
+  }
+  // softmax of the segment for head hidx: max and sum over the 4 token groups
+  float bm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+  bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+  bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+  const float m_new = fmaxf(st.m, bm);
+  const float c = exp2f(st.m - m_new);
+  float p[4], ps = 0.0f;
+#pragma unroll
+  for (int it = 0; it < 4; it++) {
+    p[it] = sc[it] == kNeg ? 0.0f : exp2f(sc[it] - m_new);
+    ps += p[it];
+  }
+  ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+  ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+  st.l = st.l * c + ps;
+  st.m = m_new;
+  constexpr int kOwners = 8 / G;  // lanes of a group holding the same head; the first writes
+  if ((sl & (kOwners - 1)) == 0) {
+#pragma unroll
+    for (int it = 0; it < 4; it++) ws.prob[4 * it + g][hidx] = p[it];
+    if (g == 0) ws.rescale[hidx] = c;
+  }
+  __syncwarp();
+  // values: lane owns channels 4 lane .. 4 lane + 3
+  const float4 c4 = *reinterpret_cast<const float4*>(ws.rescale);
+  const float cj[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+  for (int j = 0; j < G; j++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) st.acc[j][e] *= cj[j];
+  const uint32_t vb = slot + kBlockBytesBf16 + lane * 8;
+#pragma unroll 4
+  for (int r = 0; r < kPage; r++) {
+    const int t = k * kPage + r;
+    if (t < t0 || t >= t1) continue;  // warp-uniform; skipped slots may hold any bits
+    uint32_t w0, w1;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(vb + r * kHeadDim * 2));
+    const float vf[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+    const float4 p4 = *reinterpret_cast<const float4*>(ws.prob[r]);
+    const float pj[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+    for (int j = 0; j < G; j++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) st.acc[j][e] = fmaf(pj[j], vf[e], st.acc[j][e]);
+  }
+  __syncwarp();  // the next segment rewrites the scratch
+}
 
 template <int G, bool DENSE>
 __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArgs a) {
@@ -413,41 +536,52 @@ __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArg
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kSlotBytes);
   uint64_t* empty = full + kStages;
-  Scratch& sc = *reinterpret_cast<Scratch*>(empty + kStages);
+  WarpScratch* wscr = reinterpret_cast<WarpScratch*>(empty + kStages);  // [kWarps]
+  float* mstate = reinterpret_cast<float*>(wscr + kWarps);             // [kWarps][2][4]
+  int4* meta = reinterpret_cast<int4*>(mstate + 2 * kWarps * 4);        // [kStages] (k, t0, t1)
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Early mode: only the kept blocks come from the previous kernel; the producer waits for
+  // it just before its first kept block. Otherwise every input may, so wait first.
+  if (!a.early) grid_dep_wait();
+  grid_dep_launch();
   const int n_raw = a.seq_lens[b];
   if (tid == 0 && split == 0 && h == 0 && (n_raw < 0 || n_raw > a.max_pages * kPage))
     set_error(a.err, kDevErrCheck);
-  const Segments S = make_segments<DENSE>(a, b, h);
+  Segments S = make_segments<DENSE>(a, b, h);
   const int i0 = (int)((long long)S.total * split / a.nsplit);
   const int i1 = (int)((long long)S.total * (split + 1) / a.nsplit);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; s++) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
+      mbar_init(&empty[s], 1);  // the slot's owning warp
     }
     fence_barrier_init();
   }
   __syncthreads();
 
-  State<G> st;
-  init_state<G>(st);
+  WarpState<G> st;
+#pragma unroll
+  for (int j = 0; j < G; j++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) st.acc[j][e] = 0.0f;
+  st.m = kNeg;
+  st.l = 0.0f;
   if (warp == kWarps) {
-    if (lane == 0) {
-      bool ok = true;
-      for (int i = i0; i < i1; i++) {
-        const int j = i - i0, s = j % kStages;
-        if (j >= kStages && !mbar_wait(&empty[s], ((j / kStages) - 1) & 1)) {
-          set_error(a.err, kDevErrTimeout);
-          ok = false;
-          break;
-        }
-        int k, t0, t1;
-        segment_at(S, i, a.sink, k, t0, t1);
-        int page = -1;
+    // producer warp: the lanes resolve the block and page ids of 32 segments at once; lane 0
+    // then publishes each segment's (block, t0, t1) with its slot and issues the copies
+    bool ok = true, have_sel = false;
+    for (int ib = i0; ok && ib < i1; ib += 32) {
+      if (!have_sel && min(i1, ib + 32) > S.n_sink + S.n_win) {
+        grid_dep_wait();
+        read_selection(S, a, b, h);
+        have_sel = true;
+      }
+      int k = 0, t0 = 0, t1 = 0, page = -1;
+      if (ib + lane < i1) {
+        segment_at(S, ib + lane, a.sink, k, t0, t1);
         if (t0 < t1) {
           page = a.page_table[(size_t)b * a.max_pages + k];
           if (page < 0 || page >= a.num_pages) {
@@ -455,40 +589,105 @@ __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArg
             page = -1;
           }
         }
-        if (page >= 0) {
-          const size_t off = ((size_t)page * a.hkv + h) * kPage * kHeadDim;
-          mbar_arrive_expect_tx(&full[s], kSlotBytes);
-          bulk_load(ring + s * kSlotBytes, a.k + off, kBlockBytesBf16, &full[s]);
-          bulk_load(ring + s * kSlotBytes + kBlockBytesBf16, a.v + off, kBlockBytesBf16, &full[s]);
-        } else {
-          mbar_arrive(&full[s]);
+        if (page < 0) t0 = t1 = 0;
+      }
+      const int n = min(32, i1 - ib);
+      for (int q = 0; q < n; q++) {
+        const int kq = __shfl_sync(0xffffffffu, k, q);
+        const int t0q = __shfl_sync(0xffffffffu, t0, q);
+        const int t1q = __shfl_sync(0xffffffffu, t1, q);
+        const int pq = __shfl_sync(0xffffffffu, page, q);
+        if (lane == 0) {
+          const int j = ib + q - i0, s = j % kStages;
+          if (j >= kStages && !mbar_wait(&empty[s], ((j / kStages) - 1) & 1)) {
+            set_error(a.err, kDevErrTimeout);
+            ok = false;
+          } else {
+            meta[s] = make_int4(kq, t0q, t1q, 0);
+            if (pq >= 0) {
+              const size_t off = ((size_t)pq * a.hkv + h) * kPage * kHeadDim;
+              mbar_arrive_expect_tx(&full[s], kSlotBytes);
+              bulk_load(ring + s * kSlotBytes, a.k + off, kBlockBytesBf16, &full[s]);
+              bulk_load(ring + s * kSlotBytes + kBlockBytesBf16, a.v + off, kBlockBytesBf16,
+                        &full[s]);
+            } else {
+              mbar_arrive(&full[s]);
+            }
+          }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
       }
-      if (!ok) {
-        const int issued = i1 - i0;
-        for (int j = max(0, issued - kStages); j < issued; j++)
-          mbar_wait(&full[j % kStages], (j / kStages) & 1);
-      }
+    }
+    if (!ok && lane == 0) {
+      const int issued = i1 - i0;
+      for (int j = max(0, issued - kStages); j < issued; j++)
+        mbar_wait(&full[j % kStages], (j / kStages) & 1);
     }
   } else {
     float qf[G][16];
     load_query<G>(qf, a, b, h, lane & 7);
-    for (int i = i0; i < i1; i++) {
-      const int j = i - i0, s = j % kStages;
+    for (int j = warp; i0 + j < i1; j += kWarps) {
+      const int s = j % kStages;
       if (!mbar_wait(&full[s], (j / kStages) & 1)) {
         set_error(a.err, kDevErrTimeout);
         break;
       }
-      int k, t0, t1;
-      segment_at(S, i, a.sink, k, t0, t1);
-      if (t0 < t1) process_segment<G>(st, qf, sc, smem_addr(ring + s * kSlotBytes), k, t0, t1);
-      // each compute warp is done with slot s once its own reads are behind it
+      const int4 m4 = meta[s];  // written before the producer's arrive on full[s]
+      if (m4.y < m4.z)
+        warp_segment<G>(st, qf, wscr[warp], smem_addr(ring + s * kSlotBytes), m4.x, m4.y, m4.z);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
+  grid_dep_wait();  // completion of this grid implies completion of the previous one
   __syncthreads();
-  finish<G>(a, st, sc, b, h, split, reinterpret_cast<float*>(ring));
+  // merge the warps: o[j][d] = sum_w acc_w * 2^(m_w - M_j), l likewise
+  float* o = reinterpret_cast<float*>(ring);  // [kWarps][G][128], then the merged [G][128]
+  float* mw = mstate;                          // [kWarps][4] max, then [kWarps][4] sum
+  float* lw = mstate + kWarps * 4;
+  if (warp < kWarps) {
+    const int sl = lane & 7;
+    constexpr int kOwners = 8 / G;
+    int hidx = 0;
+    if constexpr (G == 4) hidx = ((sl & 4) ? 2 : 0) + ((sl & 2) ? 1 : 0);
+    if constexpr (G == 2) hidx = (sl & 4) ? 1 : 0;
+    if (lane < 8 && (sl & (kOwners - 1)) == 0) {
+      mw[warp * 4 + hidx] = st.m;
+      lw[warp * 4 + hidx] = st.l;
+    }
+#pragma unroll
+    for (int j = 0; j < G; j++)
+      *reinterpret_cast<float4*>(o + (warp * G + j) * kHeadDim + 4 * lane) =
+          make_float4(st.acc[j][0], st.acc[j][1], st.acc[j][2], st.acc[j][3]);
+  }
+  __syncthreads();
+  float* mo = o + kWarps * G * kHeadDim;  // merged [G][128]
+  float* mm = mo + G * kHeadDim;          // [4]
+  float* ml = mm + 4;                     // [4]
+  if (tid < kCompute) {
+    for (int x = tid; x < G * kHeadDim; x += kCompute) {
+      const int j = x / kHeadDim, d = x % kHeadDim;
+      float M = kNeg;
+#pragma unroll
+      for (int w = 0; w < kWarps; w++) M = fmaxf(M, mw[w * 4 + j]);
+      float O = 0.0f, L = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kWarps; w++) {
+        const float lv = lw[w * 4 + j];
+        const float wt = lv > 0.0f ? exp2f(mw[w * 4 + j] - M) : 0.0f;
+        O = fmaf(o[(w * G + j) * kHeadDim + d], wt, O);
+        L = fmaf(lv, wt, L);
+      }
+      mo[x] = O;
+      if (d == 0) {
+        mm[j] = M;
+        ml[j] = L;
+      }
+    }
+  }
+  __syncthreads();
+  finish_common<G>(a, b, h, split, mo, mm, ml, o);
 }
 
 // ---------------------------------------------------------- mapped-host path
@@ -504,10 +703,13 @@ __global__ void __launch_bounds__(kHostThreads, 3) attend_host_kernel(const AttA
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31;
+  grid_dep_wait();
+  grid_dep_launch();
   const int n_raw = a.seq_lens[b];
   if (tid == 0 && split == 0 && h == 0 && (n_raw < 0 || n_raw > a.max_pages * kPage))
     set_error(a.err, kDevErrCheck);
-  const Segments S = make_segments<DENSE>(a, b, h);
+  Segments S = make_segments<DENSE>(a, b, h);
+  read_selection(S, a, b, h);
   const int i0 = (int)((long long)S.total * split / a.nsplit);
   const int i1 = (int)((long long)S.total * (split + 1) / a.nsplit);
   State<G> st;
@@ -557,13 +759,15 @@ __global__ void __launch_bounds__(kHostThreads, 3) attend_host_kernel(const AttA
 }
 
 size_t tma_smem(int G) {
-  const size_t ring = (size_t)kStages * kSlotBytes + 2 * kStages * sizeof(uint64_t) + sizeof(Scratch);
-  return 128 + std::max(ring, red_floats(G) * sizeof(float) + 2 * kStages * 8 + sizeof(Scratch));
+  (void)G;  // the merge area ((kWarps + 1) * G * 128 + 8 floats) fits in the ring
+  return 128 + (size_t)kStages * kSlotBytes + 2 * kStages * sizeof(uint64_t) +
+         kWarps * sizeof(WarpScratch) + 2 * kWarps * 4 * sizeof(float) + kStages * sizeof(int4);
 }
 
 size_t host_smem(int G) {
   return 128 + 2 * kSlotBytes + sizeof(Scratch) + red_floats(G) * sizeof(float);
 }
+static_assert(kStages % kWarps == 0, "each compute warp owns fixed ring slots");
 
 template <int G, bool DENSE>
 cudaError_t launch_g(const AttArgs& a, dim3 grid, bool host, cudaStream_t st) {
@@ -572,13 +776,15 @@ cudaError_t launch_g(const AttArgs& a, dim3 grid, bool host, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(attend_host_kernel<G, DENSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attend_host_kernel<G, DENSE><<<grid, kHostThreads, smem, st>>>(a);
+    e = launch_kernel(attend_host_kernel<G, DENSE>, grid, dim3(kHostThreads), smem, st, true, a);
+    if (e != cudaSuccess) return e;
   } else {
     const size_t smem = tma_smem(G);
     cudaError_t e = cudaFuncSetAttribute(attend_tma_kernel<G, DENSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attend_tma_kernel<G, DENSE><<<grid, kTmaThreads, smem, st>>>(a);
+    e = launch_kernel(attend_tma_kernel<G, DENSE>, grid, dim3(kTmaThreads), smem, st, true, a);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -591,7 +797,7 @@ int attend_splits(const Shape& s, bool dense, bool host, int num_sms) {
   if (dense) {
     segs = s.max_pages;
   } else {
-    segs = (s.sink + kPage - 1) / kPage + 1 + s.k2 + (s.window + kPage - 1) / kPage + 1;
+    segs = (s.sink + kPage - 1) / kPage + s.k2 + (s.window + kPage - 1) / kPage + 1;
   }
   // dense: about three CTAs per SM; sparse: about one, each with several segments
   const int per_sm = host ? 4 : (dense ? 3 : 1);
@@ -604,7 +810,7 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
                           const void* k_cache, const void* v_cache, const int32_t* page_table,
                           const int32_t* seq_lens, const int32_t* block_idx,
                           const int32_t* n_blocks, float* out, float* lse,
-                          const AttendBuffers& buf, int* err, cudaStream_t st) {
+                          const AttendBuffers& buf, int* err, cudaStream_t st, bool early) {
   if (buf.nsplit < 1 || buf.nsplit > kMaxSplits) return cudaErrorInvalidValue;
   AttArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -628,6 +834,7 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
   a.window = s.window;
   a.nsplit = buf.nsplit;
   a.qscale = s.sm_scale * kLog2e;
+  a.early = (early && !host) ? 1 : 0;
   dim3 grid(buf.nsplit, s.hkv, s.batch);
   switch (s.group) {
     case 1:

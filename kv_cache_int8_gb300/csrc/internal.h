@@ -23,10 +23,12 @@ cudaError_t launch_key_codes(const Shape& s, const void* k_cache, const int32_t*
                              const int32_t* seq_lens, const unsigned* amax_bits,
                              const float* k_scale_in, float* k_scale_out, int append_from,
                              bool full, int8_t* kq, int* err, cudaStream_t st);
+// beside: launched to run concurrently with the scorer of the same decode step (see
+// hsa_decode_step); false for a standalone append.
 cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_new,
                              void* k_cache, void* v_cache, int8_t* kq, const float* k_scale,
                              const int32_t* page_table, const int32_t* seq_lens, int* err,
-                             cudaStream_t st);
+                             cudaStream_t st, bool beside);
 
 // ---- select.cu
 // block_max: [B][Hkv][max_pages]; tile_max (nullable): [B][Hkv][score_max_tiles], the max of
@@ -43,6 +45,9 @@ int prune_max_chunks();
 size_t prune_smem_bytes(const Shape& s);
 
 // ---- attend.cu
+// early: the caller guarantees that K/V, q, the page table and the lengths are complete when
+// the kernel starts (only the selection comes from the previous kernel), as in the whole
+// decode step; the sink and window pages are then fetched before waiting for the selection.
 struct AttendBuffers {
   float* part_ml;   // [B][Hq][nsplit] (m, l) pairs
   float* part_o;    // [B][Hq][nsplit][128]
@@ -54,6 +59,6 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
                           const void* k_cache, const void* v_cache, const int32_t* page_table,
                           const int32_t* seq_lens, const int32_t* block_idx,
                           const int32_t* n_blocks, float* out, float* lse,
-                          const AttendBuffers& buf, int* err, cudaStream_t st);
+                          const AttendBuffers& buf, int* err, cudaStream_t st, bool early);
 
 }  // namespace hsa

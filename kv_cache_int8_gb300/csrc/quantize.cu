@@ -139,12 +139,37 @@ __global__ void __launch_bounds__(kThreads) key_codes_kernel(
 
 // Decode-step append: slot N_b - 1 of every sequence receives k_new, v_new and the codes
 // of k_new under the stored scales. One CTA per sequence, thread = (head, channel group).
+// With `beside` (whole decode step only, where the predecessor is the scorer, which neither
+// writes this kernel's inputs nor reads the slot it writes) the kernel runs concurrently
+// with its predecessor and waits for it only before exiting; otherwise it waits first.
+__device__ __forceinline__ void append_body(const uint4* __restrict__ k_new,
+                                            const uint4* __restrict__ v_new,
+                                            __nv_bfloat16* k_cache, __nv_bfloat16* v_cache,
+                                            int8_t* kq, const float* __restrict__ k_scale,
+                                            const int32_t* __restrict__ page_table,
+                                            const int32_t* __restrict__ seq_lens, int hkv,
+                                            int max_pages, int num_pages, int* err);
+
 __global__ void append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                                  __nv_bfloat16* k_cache, __nv_bfloat16* v_cache, int8_t* kq,
                                  const float* __restrict__ k_scale,
                                  const int32_t* __restrict__ page_table,
                                  const int32_t* __restrict__ seq_lens, int hkv, int max_pages,
-                                 int num_pages, int* err) {
+                                 int num_pages, int* err, int beside) {
+  if (!beside) grid_dep_wait();
+  grid_dep_launch();
+  append_body(k_new, v_new, k_cache, v_cache, kq, k_scale, page_table, seq_lens, hkv, max_pages,
+              num_pages, err);
+  grid_dep_wait();
+}
+
+__device__ __forceinline__ void append_body(const uint4* __restrict__ k_new,
+                                            const uint4* __restrict__ v_new,
+                                            __nv_bfloat16* k_cache, __nv_bfloat16* v_cache,
+                                            int8_t* kq, const float* __restrict__ k_scale,
+                                            const int32_t* __restrict__ page_table,
+                                            const int32_t* __restrict__ seq_lens, int hkv,
+                                            int max_pages, int num_pages, int* err) {
   const int b = blockIdx.x;
   const int h = threadIdx.x >> 4, grp = threadIdx.x & 15;
   if (h >= hkv) return;
@@ -203,13 +228,13 @@ cudaError_t launch_key_codes(const Shape& s, const void* k_cache, const int32_t*
 cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_new,
                              void* k_cache, void* v_cache, int8_t* kq, const float* k_scale,
                              const int32_t* page_table, const int32_t* seq_lens, int* err,
-                             cudaStream_t st) {
+                             cudaStream_t st, bool beside) {
   const int threads = ((s.hkv * 16 + 31) / 32) * 32;
-  append_kv_kernel<<<s.batch, threads, 0, st>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-      static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), kq, k_scale,
-      page_table, seq_lens, s.hkv, s.max_pages, s.num_pages, err);
-  return cudaGetLastError();
+  return launch_kernel(append_kv_kernel, dim3(s.batch), dim3(threads), 0, st, beside,
+                       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                       static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache),
+                       kq, k_scale, page_table, seq_lens, s.hkv, s.max_pages, s.num_pages, err,
+                       beside ? 1 : 0);
 }
 
 }  // namespace hsa

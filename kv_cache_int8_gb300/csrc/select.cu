@@ -131,6 +131,9 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     }
     fence_barrier_init();
   }
+  // inputs may come from the previous kernel of the stream; then let the next one launch
+  grid_dep_wait();
+  grid_dep_launch();
   if (warp == kScoreWarps && lane == 0) tma_prefetch_descriptor(&kq_map);
   // tiles per sequence (x hkv), exclusive prefix sum by warp 0
   if (warp == 0) {
@@ -513,6 +516,8 @@ __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const PruneArgs a)
   int* kept_chunks = cand + a.cand_cap;                     // k1
 
   const int h = blockIdx.x, b = blockIdx.y;
+  grid_dep_wait();  // the scores come from the previous kernel
+  grid_dep_launch();
   const int n = a.seq_lens[b];
   const int P = a.chunk_blocks;
   int lo = a.sink, hi = n - a.window;
@@ -655,19 +660,25 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const
       e = cudaFuncSetAttribute(score_blocks_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
       if (e != cudaSuccess) return e;
-      score_blocks_kernel<1><<<grid, kScoreThreads, smem, st>>>(kq_map, a);
+      e = launch_kernel(score_blocks_kernel<1>, dim3(grid), dim3(kScoreThreads), smem, st, true,
+                        kq_map, a);
+      if (e != cudaSuccess) return e;
       break;
     case 2:
       e = cudaFuncSetAttribute(score_blocks_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
       if (e != cudaSuccess) return e;
-      score_blocks_kernel<2><<<grid, kScoreThreads, smem, st>>>(kq_map, a);
+      e = launch_kernel(score_blocks_kernel<2>, dim3(grid), dim3(kScoreThreads), smem, st, true,
+                        kq_map, a);
+      if (e != cudaSuccess) return e;
       break;
     case 4:
       e = cudaFuncSetAttribute(score_blocks_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
       if (e != cudaSuccess) return e;
-      score_blocks_kernel<4><<<grid, kScoreThreads, smem, st>>>(kq_map, a);
+      e = launch_kernel(score_blocks_kernel<4>, dim3(grid), dim3(kScoreThreads), smem, st, true,
+                        kq_map, a);
+      if (e != cudaSuccess) return e;
       break;
     default:
       return cudaErrorInvalidValue;
@@ -701,8 +712,7 @@ cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t*
   cudaError_t e =
       cudaFuncSetAttribute(prune_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  prune_kernel<<<dim3(s.hkv, s.batch), kPruneThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(prune_kernel, dim3(s.hkv, s.batch), dim3(kPruneThreads), smem, st, true, a);
 }
 
 }  // namespace hsa

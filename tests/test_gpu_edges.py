@@ -203,3 +203,65 @@ def test_device_bounds_checks_report_without_faulting():
     hsa.hsa_select(hd, dwl["q"], kq, k_scale, dwl["page_table"], dwl["seq_lens"], None, None,
                    bidx, nb, ws)
     assert hsa.hsa_read_device_error(ws) == 0
+
+
+@pytest.mark.parametrize("window,k1,k2", [(0, 6, 9), (1, 6, 9), (5, 3, 0), (300, 8, 8)])
+def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2):
+    """The whole step (append ordered before or beside the scorer, prune, attend with the
+    sink and window pages fetched early) equals the separate calls bit for bit, and the
+    oracle on the appended cache."""
+    cfg = _cfg(context=None, context_range=(700, 5000), batch=3, hq=8, hkv=2, k1=k1, k2=k2,
+               sink=20, window=window, paged_permuted=True)
+    wl = W.make_workload(cfg, seed=40 + window)
+    hd, od = H.dims_pair(wl)
+    dwl = H.to_cuda(wl)
+    dev = torch.device("cuda")
+    B, Hkv = cfg.batch, cfg.hkv
+    gen = torch.Generator(device="cpu").manual_seed(7 + window)
+    k_new = torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16)
+    v_new = torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16)
+    kq = torch.zeros(dwl["k_cache"].shape, dtype=torch.int8, device=dev)
+    k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
+    hsa.hsa_quantize_keys(hd, dwl["k_cache"], dwl["page_table"], dwl["seq_lens"], 0, 0, kq,
+                          k_scale, hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
+    # whole step
+    kc1, vc1, kq1 = dwl["k_cache"].clone(), dwl["v_cache"].clone(), kq.clone()
+    out1 = torch.zeros((B, cfg.hq, 128), dtype=torch.float32, device=dev)
+    lse1 = torch.zeros((B, cfg.hq), dtype=torch.float32, device=dev)
+    bidx1 = torch.full((B, Hkv, max(k2, 1)), -7, dtype=torch.int32, device=dev)
+    nb1 = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+    wst = hsa.workspace(hd, hsa.HSA_OP_STEP)
+    for _ in range(2):  # the second call finds the first call's workspace contents
+        hsa.hsa_decode_step(hd, dwl["q"], k_new.cuda(), v_new.cuda(), out1, lse1, kc1, vc1, kq1,
+                            k_scale, dwl["page_table"], dwl["seq_lens"], bidx1, nb1, wst)
+    # separate calls
+    kc2, vc2, kq2 = dwl["k_cache"].clone(), dwl["v_cache"].clone(), kq.clone()
+    hsa.hsa_append_kv(hd, k_new.cuda(), v_new.cuda(), kc2, vc2, kq2, k_scale, dwl["page_table"],
+                      dwl["seq_lens"])
+    bidx2 = torch.full_like(bidx1, -7)
+    nb2 = torch.full_like(nb1, -7)
+    hsa.hsa_select(hd, dwl["q"], kq2, k_scale, dwl["page_table"], dwl["seq_lens"], None, None,
+                   bidx2, nb2, hsa.workspace(hd, hsa.HSA_OP_SELECT))
+    out2 = torch.zeros_like(out1)
+    lse2 = torch.zeros_like(lse1)
+    hsa.hsa_attend(hd, dwl["q"], kc2, vc2, dwl["page_table"], dwl["seq_lens"], bidx2, nb2, out2,
+                   lse2, hsa.workspace(hd, hsa.HSA_OP_ATTEND))
+    torch.cuda.synchronize()
+    assert hsa.hsa_read_device_error(wst) == 0
+    assert torch.equal(kq1, kq2) and torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
+    assert torch.equal(nb1, nb2) and torch.equal(bidx1, bidx2)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    # oracle on the appended cache
+    kh, vh = kc2.cpu(), vc2.cpu()
+    h = {"q": W.to_numpy_bits(wl["q"]), "k": W.to_numpy_bits(kh), "v": W.to_numpy_bits(vh),
+         "pt": wl["page_table"].numpy(), "lens": wl["seq_lens"].numpy()}
+    kq_o, sc_o = oracle.quantize_keys(od, W.to_numpy_bits(wl["k_cache"]), h["pt"], h["lens"])
+    kq_o = oracle.quantize_append(od, h["k"], h["pt"], h["lens"], -1, sc_o, kq_o)
+    np.testing.assert_array_equal(kq1.cpu().numpy(), kq_o)
+    sel = oracle.select(od, h["q"], sc_o, kq_o, h["pt"], h["lens"])
+    np.testing.assert_array_equal(nb1.cpu().numpy(), sel["n_blocks"])
+    np.testing.assert_array_equal(bidx1.cpu().numpy()[..., :k2], sel["block_idx"])
+    out_o, lse_o = oracle.attend(od, h["q"], h["k"], h["v"], h["pt"], h["lens"], sel["block_idx"],
+                                 sel["n_blocks"])
+    H.assert_close(out1.cpu().numpy(), out_o, "whole-step output")
+    np.testing.assert_allclose(lse1.cpu().numpy(), lse_o, atol=2e-4, rtol=1e-5)
