@@ -31,14 +31,23 @@
 #include "common.cuh"
 #include "internal.h"
 
+// Split-K grid sizing (CTAs per SM); overridable at build time for tuning.
+#ifndef HSA_SPARSE_CTAS_PER_SM
+#define HSA_SPARSE_CTAS_PER_SM 1
+#endif
+#ifndef HSA_DENSE_CTAS_PER_SM
+#define HSA_DENSE_CTAS_PER_SM 3
+#endif
+
 namespace hsa {
 namespace {
 
-constexpr int kWarps = 4;                        // compute warps
+constexpr int kWarps = 4;                        // compute warps of the host path
 constexpr int kCompute = kWarps * 32;
 constexpr int kStages = 8;
+constexpr int kSparseWarps = 8, kSparseStages = 16;  // HBM path, sparse attend
+constexpr int kDenseWarps = 4, kDenseStages = 8;     // HBM path, dense decode
 constexpr int kSlotBytes = 2 * kBlockBytesBf16;  // K page + V page of one head
-constexpr int kTmaThreads = kCompute + 32;
 constexpr int kHostThreads = kCompute;
 constexpr int kMaxSplits = 64;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -298,12 +307,12 @@ __device__ __forceinline__ void process_segment(State<G>& st, const float (&qf)[
 // `o`. Called by all threads of the CTA after the merged state is complete.
 template <int G>
 __device__ void finish_common(const AttArgs& a, int b, int h, int split, const float* o,
-                              const float* m, const float* l, float* red) {
+                              const float* m, const float* l, float* red, int nthreads) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ int is_last;
   const int hq = a.hkv * G;
-  if (tid < kCompute) {
-    for (int x = tid; x < G * kHeadDim; x += kCompute) {
+  if (tid < nthreads) {
+    for (int x = tid; x < G * kHeadDim; x += nthreads) {
       const int j = x / kHeadDim, d = x % kHeadDim;
       const size_t row = (size_t)b * hq + (size_t)h * G + j;
       const float L = l[j];
@@ -327,65 +336,47 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  // weights of the splits: warp j handles head j
-  float* wgt = red;                   // [G][kMaxSplits]
-  float* tot = red + G * kMaxSplits;  // [G] sum of weighted l
-  float* mm = tot + 4;                // [G] max
-  if (warp < G) {
-    const size_t row = (size_t)b * hq + (size_t)h * G + warp;
-    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + row * a.nsplit;
-    float2 v0 = make_float2(kNeg, 0.0f), v1 = make_float2(kNeg, 0.0f);
-    if (lane < a.nsplit) v0 = __ldcg(ml + lane);
-    if (lane + 32 < a.nsplit) v1 = __ldcg(ml + lane + 32);
-    float M = fmaxf(v0.x, v1.x);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float w0 = v0.y > 0.0f ? exp2f(v0.x - M) : 0.0f;
-    const float w1 = v1.y > 0.0f ? exp2f(v1.x - M) : 0.0f;
-    if (lane < a.nsplit) wgt[warp * kMaxSplits + lane] = w0;
-    if (lane + 32 < a.nsplit) wgt[warp * kMaxSplits + lane + 32] = w1;
-    float L = v0.y * w0 + v1.y * w1;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (lane == 0) {
-      tot[warp] = L;
-      mm[warp] = M;
-    }
-  }
-  __syncthreads();
-  // outputs: thread -> (head j, 4 channels), float4 loads of all splits in flight
-  if (tid < G * 32) {
-    const int j = tid >> 5, d4 = (tid & 31) * 4;
+  // every thread streams the (m, l) pair and its 4 channels of all splits together (one
+  // round trip per batch of splits) and merges them online: the running state is kept
+  // relative to the largest m seen so far
+  (void)red;
+  for (int x = tid; x < G * 32; x += blockDim.x) {
+    const int j = x >> 5, d4 = (x & 31) * 4;
     const size_t row = (size_t)b * hq + (size_t)h * G + j;
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + row * a.nsplit;
     const float4* po = reinterpret_cast<const float4*>(a.part_o + row * a.nsplit * kHeadDim + d4);
+    float M = kNeg, L = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int sp = 0;
-    for (; sp + 8 <= a.nsplit; sp += 8) {
-      float4 x[8];
-#pragma unroll
-      for (int u = 0; u < 8; u++) x[u] = __ldcg(po + (size_t)(sp + u) * (kHeadDim / 4));
+    for (int sp0 = 0; sp0 < a.nsplit; sp0 += 8) {
+      float2 mlv[8];
+      float4 ov[8];
 #pragma unroll
       for (int u = 0; u < 8; u++) {
-        const float w = wgt[j * kMaxSplits + sp + u];
-        acc.x = fmaf(x[u].x, w, acc.x);
-        acc.y = fmaf(x[u].y, w, acc.y);
-        acc.z = fmaf(x[u].z, w, acc.z);
-        acc.w = fmaf(x[u].w, w, acc.w);
+        if (sp0 + u < a.nsplit) {
+          mlv[u] = __ldcg(ml + sp0 + u);
+          ov[u] = __ldcg(po + (size_t)(sp0 + u) * (kHeadDim / 4));
+        } else {
+          mlv[u] = make_float2(kNeg, 0.0f);
+          ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        if (!(mlv[u].y > 0.0f)) continue;
+        const float m_new = fmaxf(M, mlv[u].x);
+        const float c = exp2f(M - m_new), w = exp2f(mlv[u].x - m_new);
+        L = L * c + mlv[u].y * w;
+        acc.x = acc.x * c + ov[u].x * w;
+        acc.y = acc.y * c + ov[u].y * w;
+        acc.z = acc.z * c + ov[u].z * w;
+        acc.w = acc.w * c + ov[u].w * w;
+        M = m_new;
       }
     }
-    for (; sp < a.nsplit; sp++) {
-      const float4 x = __ldcg(po + (size_t)sp * (kHeadDim / 4));
-      const float w = wgt[j * kMaxSplits + sp];
-      acc.x = fmaf(x.x, w, acc.x);
-      acc.y = fmaf(x.y, w, acc.y);
-      acc.z = fmaf(x.z, w, acc.z);
-      acc.w = fmaf(x.w, w, acc.w);
-    }
-    const float L = tot[j];
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     *reinterpret_cast<float4*>(a.out + row * kHeadDim + d4) =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (d4 == 0 && a.lse) a.lse[row] = L > 0.0f ? (mm[j] + log2f(L)) * kLn2 : -INFINITY;
+    if (d4 == 0 && a.lse) a.lse[row] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
   if (tid == 0) a.counters[(size_t)b * a.hkv + h] = 0;
 }
@@ -417,7 +408,7 @@ __device__ void finish(const AttArgs& a, State<G>& st, Scratch& sc, int b, int h
     }
   }
   __syncthreads();
-  finish_common<G>(a, b, h, split, red, sc.m, sc.l, red);
+  finish_common<G>(a, b, h, split, red, sc.m, sc.l, red, kCompute);
 }
 
 template <int G>
@@ -528,17 +519,22 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
   __syncwarp();  // the next segment rewrites the scratch
 }
 
-template <int G, bool DENSE>
-__global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArgs a) {
+// W compute warps and NS ring slots (NS a multiple of W): the sparse path uses 8 warps and 16
+// slots so that every segment of a CTA is in flight at once; dense decode uses 4 and 8 with
+// three CTAs per SM.
+template <int G, bool DENSE, int W, int NS>
+__global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_kernel(const AttArgs a) {
+  static_assert(NS % W == 0, "each compute warp owns fixed ring slots");
+  constexpr int kThreads = (W + 1) * 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kSlotBytes);
-  uint64_t* empty = full + kStages;
-  WarpScratch* wscr = reinterpret_cast<WarpScratch*>(empty + kStages);  // [kWarps]
-  float* mstate = reinterpret_cast<float*>(wscr + kWarps);             // [kWarps][2][4]
-  int4* meta = reinterpret_cast<int4*>(mstate + 2 * kWarps * 4);        // [kStages] (k, t0, t1)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * kSlotBytes);
+  uint64_t* empty = full + NS;
+  WarpScratch* wscr = reinterpret_cast<WarpScratch*>(empty + NS);  // [W]
+  float* mstate = reinterpret_cast<float*>(wscr + W);             // [W][2][4]
+  int4* meta = reinterpret_cast<int4*>(mstate + 2 * W * 4);       // [NS] (k, t0, t1)
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -554,7 +550,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArg
   const int i1 = (int)((long long)S.total * (split + 1) / a.nsplit);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; s++) {
+    for (int s = 0; s < NS; s++) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);  // the slot's owning warp
     }
@@ -569,7 +565,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArg
     for (int e = 0; e < 4; e++) st.acc[j][e] = 0.0f;
   st.m = kNeg;
   st.l = 0.0f;
-  if (warp == kWarps) {
+  if (warp == W) {
     // producer warp: the lanes resolve the block and page ids of 32 segments at once; lane 0
     // then publishes each segment's (block, t0, t1) with its slot and issues the copies
     bool ok = true, have_sel = false;
@@ -598,8 +594,8 @@ __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArg
         const int t1q = __shfl_sync(0xffffffffu, t1, q);
         const int pq = __shfl_sync(0xffffffffu, page, q);
         if (lane == 0) {
-          const int j = ib + q - i0, s = j % kStages;
-          if (j >= kStages && !mbar_wait(&empty[s], ((j / kStages) - 1) & 1)) {
+          const int j = ib + q - i0, s = j % NS;
+          if (j >= NS && !mbar_wait(&empty[s], ((j / NS) - 1) & 1)) {
             set_error(a.err, kDevErrTimeout);
             ok = false;
           } else {
@@ -621,15 +617,14 @@ __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArg
     }
     if (!ok && lane == 0) {
       const int issued = i1 - i0;
-      for (int j = max(0, issued - kStages); j < issued; j++)
-        mbar_wait(&full[j % kStages], (j / kStages) & 1);
+      for (int j = max(0, issued - NS); j < issued; j++) mbar_wait(&full[j % NS], (j / NS) & 1);
     }
   } else {
     float qf[G][16];
     load_query<G>(qf, a, b, h, lane & 7);
-    for (int j = warp; i0 + j < i1; j += kWarps) {
-      const int s = j % kStages;
-      if (!mbar_wait(&full[s], (j / kStages) & 1)) {
+    for (int j = warp; i0 + j < i1; j += W) {
+      const int s = j % NS;
+      if (!mbar_wait(&full[s], (j / NS) & 1)) {
         set_error(a.err, kDevErrTimeout);
         break;
       }
@@ -643,10 +638,10 @@ __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArg
   grid_dep_wait();  // completion of this grid implies completion of the previous one
   __syncthreads();
   // merge the warps: o[j][d] = sum_w acc_w * 2^(m_w - M_j), l likewise
-  float* o = reinterpret_cast<float*>(ring);  // [kWarps][G][128], then the merged [G][128]
-  float* mw = mstate;                          // [kWarps][4] max, then [kWarps][4] sum
-  float* lw = mstate + kWarps * 4;
-  if (warp < kWarps) {
+  float* o = reinterpret_cast<float*>(ring);  // [W][G][128], then the merged [G][128]
+  float* mw = mstate;                          // [W][4] max, then [W][4] sum
+  float* lw = mstate + W * 4;
+  if (warp < W) {
     const int sl = lane & 7;
     constexpr int kOwners = 8 / G;
     int hidx = 0;
@@ -662,18 +657,18 @@ __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArg
           make_float4(st.acc[j][0], st.acc[j][1], st.acc[j][2], st.acc[j][3]);
   }
   __syncthreads();
-  float* mo = o + kWarps * G * kHeadDim;  // merged [G][128]
+  float* mo = o + W * G * kHeadDim;  // merged [G][128]
   float* mm = mo + G * kHeadDim;          // [4]
   float* ml = mm + 4;                     // [4]
-  if (tid < kCompute) {
-    for (int x = tid; x < G * kHeadDim; x += kCompute) {
+  if (tid < W * 32) {
+    for (int x = tid; x < G * kHeadDim; x += W * 32) {
       const int j = x / kHeadDim, d = x % kHeadDim;
       float M = kNeg;
 #pragma unroll
-      for (int w = 0; w < kWarps; w++) M = fmaxf(M, mw[w * 4 + j]);
+      for (int w = 0; w < W; w++) M = fmaxf(M, mw[w * 4 + j]);
       float O = 0.0f, L = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kWarps; w++) {
+      for (int w = 0; w < W; w++) {
         const float lv = lw[w * 4 + j];
         const float wt = lv > 0.0f ? exp2f(mw[w * 4 + j] - M) : 0.0f;
         O = fmaf(o[(w * G + j) * kHeadDim + d], wt, O);
@@ -687,7 +682,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) attend_tma_kernel(const AttArg
     }
   }
   __syncthreads();
-  finish_common<G>(a, b, h, split, mo, mm, ml, o);
+  finish_common<G>(a, b, h, split, mo, mm, ml, o, W * 32);
 }
 
 // ---------------------------------------------------------- mapped-host path
@@ -758,10 +753,11 @@ __global__ void __launch_bounds__(kHostThreads, 3) attend_host_kernel(const AttA
   finish<G>(a, st, sc, b, h, split, red);
 }
 
-size_t tma_smem(int G) {
-  (void)G;  // the merge area ((kWarps + 1) * G * 128 + 8 floats) fits in the ring
-  return 128 + (size_t)kStages * kSlotBytes + 2 * kStages * sizeof(uint64_t) +
-         kWarps * sizeof(WarpScratch) + 2 * kWarps * 4 * sizeof(float) + kStages * sizeof(int4);
+template <int W, int NS>
+constexpr size_t tma_smem() {
+  // the merge area ((W + 1) * G * 128 + 8 floats) fits in the ring
+  return 128 + (size_t)NS * kSlotBytes + 2 * NS * sizeof(uint64_t) + W * sizeof(WarpScratch) +
+         2 * W * 4 * sizeof(float) + NS * sizeof(int4);
 }
 
 size_t host_smem(int G) {
@@ -770,23 +766,21 @@ size_t host_smem(int G) {
 static_assert(kStages % kWarps == 0, "each compute warp owns fixed ring slots");
 
 template <int G, bool DENSE>
-cudaError_t launch_g(const AttArgs& a, dim3 grid, bool host, cudaStream_t st) {
+cudaError_t launch_g(AttArgs a, dim3 grid, bool host, cudaStream_t st) {
   if (host) {
     const size_t smem = host_smem(G);
     cudaError_t e = cudaFuncSetAttribute(attend_host_kernel<G, DENSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_kernel(attend_host_kernel<G, DENSE>, grid, dim3(kHostThreads), smem, st, true, a);
-    if (e != cudaSuccess) return e;
-  } else {
-    const size_t smem = tma_smem(G);
-    cudaError_t e = cudaFuncSetAttribute(attend_tma_kernel<G, DENSE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = launch_kernel(attend_tma_kernel<G, DENSE>, grid, dim3(kTmaThreads), smem, st, true, a);
-    if (e != cudaSuccess) return e;
+    return launch_kernel(attend_host_kernel<G, DENSE>, grid, dim3(kHostThreads), smem, st, true, a);
   }
-  return cudaGetLastError();
+  constexpr int W = DENSE ? kDenseWarps : kSparseWarps;
+  constexpr int NS = DENSE ? kDenseStages : kSparseStages;
+  constexpr size_t smem = tma_smem<W, NS>();
+  auto kern = attend_tma_kernel<G, DENSE, W, NS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, grid, dim3((W + 1) * 32), smem, st, true, a);
 }
 
 }  // namespace
@@ -799,8 +793,8 @@ int attend_splits(const Shape& s, bool dense, bool host, int num_sms) {
   } else {
     segs = (s.sink + kPage - 1) / kPage + s.k2 + (s.window + kPage - 1) / kPage + 1;
   }
-  // dense: about three CTAs per SM; sparse: about one, each with several segments
-  const int per_sm = host ? 4 : (dense ? 3 : 1);
+  // dense: about three CTAs per SM; sparse: fewer, each with several segments
+  const int per_sm = host ? 4 : (dense ? HSA_DENSE_CTAS_PER_SM : HSA_SPARSE_CTAS_PER_SM);
   long long want = ((long long)num_sms * per_sm + units - 1) / units;
   want = std::min<long long>(want, std::max<long long>(1, segs / 4));
   return (int)std::max<long long>(1, std::min<long long>(want, kMaxSplits));

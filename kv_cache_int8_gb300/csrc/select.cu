@@ -314,7 +314,10 @@ size_t score_smem_bytes(int batch) {
 
 // -------------------------------------------------------------------- prune
 
-constexpr int kPruneThreads = 512;
+#ifndef HSA_PRUNE_THREADS
+#define HSA_PRUNE_THREADS 512
+#endif
+constexpr int kPruneThreads = HSA_PRUNE_THREADS;  // overridable at build time for tuning
 constexpr int kPruneWarps = kPruneThreads / 32;
 constexpr int kDigitBins = 256;
 constexpr int kMaxChunks = 53248;
