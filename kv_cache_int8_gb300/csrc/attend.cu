@@ -308,7 +308,7 @@ __device__ __forceinline__ void process_segment(State<G>& st, const float (&qf)[
 template <int G>
 __device__ void finish_common(const AttArgs& a, int b, int h, int split, const float* o,
                               const float* m, const float* l, float* red, int nthreads) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   __shared__ int is_last;
   const int hq = a.hkv * G;
   if (tid < nthreads) {
@@ -525,7 +525,6 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
 template <int G, bool DENSE, int W, int NS>
 __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_kernel(const AttArgs a) {
   static_assert(NS % W == 0, "each compute warp owns fixed ring slots");
-  constexpr int kThreads = (W + 1) * 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
