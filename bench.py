@@ -163,25 +163,35 @@ class Case:
 
     KERNELS = ("step", "append", "score", "prune", "attend", "dense")
 
-    def __init__(self, name: str, seed: int, device):
+    def __init__(self, name: str, seed: int, device, dense: bool = True):
         import torch
         from kv_cache_int8_gb300 import hsa
         from kv_cache_int8_gb300 import workloads as W
         self.torch, self.hsa = torch, hsa
         self.cfg = W.CONFIGS[name]
         cfg = self.cfg
-        wl = W.make_workload(cfg, seed=seed, device=str(device))
+        self.kernels = self.KERNELS if dense else tuple(k for k in self.KERNELS if k != "dense")
+        # offloaded K/V: one pinned host copy (both "replicas" alias it; steps are separated by
+        # an L2 flush instead, see timed_steps)
+        wl = W.make_workload(cfg, seed=seed, device=str(device), host_pinned=cfg.kv_on_host)
         self.wl = wl
+        self.flush = None
+        if cfg.kv_on_host:
+            self.flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
         self.d = hsa.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv,
                           max_pages_per_seq=wl["max_pages"], num_pages=wl["num_pages"],
                           chunk=cfg.chunk, k1=cfg.k1, k2=cfg.k2, sink=cfg.sink,
-                          window=cfg.window)
+                          window=cfg.window, kv_on_host=cfg.kv_on_host)
         d = self.d
         B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
         self.q = wl["q"]
         self.pt, self.lens = wl["page_table"], wl["seq_lens"]
-        self.k = [wl["k_cache"], wl["k_cache"].clone()]
-        self.v = [wl["v_cache"], wl["v_cache"].clone()]
+        if cfg.kv_on_host:
+            self.k = [wl["k_cache"], wl["k_cache"]]
+            self.v = [wl["v_cache"], wl["v_cache"]]
+        else:
+            self.k = [wl["k_cache"], wl["k_cache"].clone()]
+            self.v = [wl["v_cache"], wl["v_cache"].clone()]
         self.kq = [torch.zeros(self.k[0].shape, dtype=torch.int8, device=device) for _ in range(2)]
         self.ks = [torch.zeros((B, Hkv, 128), dtype=torch.float32, device=device)
                    for _ in range(2)]
@@ -197,11 +207,12 @@ class Case:
         # the new token of the step: re-append the current last token (cache unchanged)
         lens = wl["lens"]
         ptc = wl["page_table"].cpu()
+        kdev = self.k[0].device
         pages = torch.tensor([int(ptc[b, (n - 1) // 16]) for b, n in enumerate(lens)],
-                             device=device)
-        slots = torch.tensor([(n - 1) % 16 for n in lens], device=device)
-        self.k_new = self.k[0][pages, :, slots].contiguous()
-        self.v_new = self.v[0][pages, :, slots].contiguous()
+                             device=kdev)
+        slots = torch.tensor([(n - 1) % 16 for n in lens], device=kdev)
+        self.k_new = self.k[0][pages, :, slots].contiguous().to(device)
+        self.v_new = self.v[0][pages, :, slots].contiguous().to(device)
         self.ws_sel = hsa.workspace(d, hsa.HSA_OP_SELECT)
         self.ws_att = hsa.workspace(d, hsa.HSA_OP_ATTEND)
         self.ws_den = hsa.workspace(d, hsa.HSA_OP_DENSE)
@@ -251,12 +262,12 @@ class Case:
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             for r in range(2):
-                for name in self.KERNELS:
+                for name in self.kernels:
                     getattr(self, name)(r)
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         for r in range(2):
-            for name in self.KERNELS:
+            for name in self.kernels:
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
                     getattr(self, name)(r)
@@ -316,6 +327,8 @@ def timed_steps(case, steps: int, names, sampler=None):
     for i in range(steps):
         r = i & 1
         ev = evs[i]
+        if case.flush is not None:
+            case.flush.fill_(i & 0xFF)  # evict the previous step's data from L2
         ev[0].record()
         for j, name in enumerate(names):
             case.graphs[(name, r)].replay()
@@ -355,10 +368,10 @@ def e2e_steps(case, steps: int):
     return statistics.fmean(times), h2d, d2h
 
 
-def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1):
+def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, dense=True):
     import torch
     from kv_cache_int8_gb300 import hsa
-    case = Case(name, seed, device)
+    case = Case(name, seed, device, dense)
     case.capture()
     names = ("append", "score", "prune", "attend")
     # the timed region: K whole steps, one graph replay each
@@ -370,12 +383,17 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1):
     bsteps = max(3, min(steps, 2000))
     timed_steps(case, max(3, warmup), names)
     per, split_ms = timed_steps(case, bsteps, names)
-    timed_steps(case, max(3, warmup), ("dense",))
-    dper, _ = timed_steps(case, bsteps, ("dense",))
+    if dense:
+        timed_steps(case, max(3, warmup), ("dense",))
+        dper, _ = timed_steps(case, bsteps, ("dense",))
+    else:
+        dper = {"dense": float("nan")}
     for w in (case.ws_step, case.ws_sel, case.ws_att, case.ws_den):
         code = hsa.hsa_read_device_error(w)
         assert code == 0, f"device error word {code}"
     recall = torch.exp(case.lse.double() - case.lse_d.double())  # restriction identity
+    if not dense:
+        recall = torch.full_like(recall, float("nan"))
     sel_ms = per["score"] + per["prune"]
     res = {
         "case": case,
@@ -515,6 +533,22 @@ def main():
     torch.cuda.empty_cache()
 
     extra = {}
+    if not args.no_extra:
+        # the batched paged configuration and the 3M-token offloaded one (K/V in pinned host
+        # memory, read over the host link by the attend kernel)
+        for name, dense in (("paged-b8-32k-128k", True), ("llama3-8b-3m-offload", False)):
+            r = gpu_case_numbers(name, rank, device, min(args.steps, 500), args.warmup, None,
+                                 peak, world, dense=dense)
+            del r["case"]
+            torch.cuda.empty_cache()
+            extra[name] = {
+                "us_per_step": r["step_ms"] * 1e3, "score_us": r["per_ms"]["score"] * 1e3,
+                "prune_us": r["per_ms"]["prune"] * 1e3, "attend_us": r["per_ms"]["attend"] * 1e3,
+                "dense_us": r["dense_ms"] * 1e3 if dense else None,
+                "score_gbs": r["gbs"]["score"],
+                "attend_gbs" + ("_host_link" if not dense else ""): r["gbs"]["attend"],
+                "bytes": r["bytes"], "quantize_keys_ms": r["quantize_ms"],
+            }
     if not args.no_extra and args.config != EXTRA_CONFIG:
         r = gpu_case_numbers(EXTRA_CONFIG, rank, device, min(args.steps, 1500), args.warmup, None,
                              peak, world)

@@ -205,15 +205,23 @@ def test_device_bounds_checks_report_without_faulting():
     assert hsa.hsa_read_device_error(ws) == 0
 
 
-@pytest.mark.parametrize("window,k1,k2", [(0, 6, 9), (1, 6, 9), (5, 3, 0), (300, 8, 8)])
-def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2):
+def _clone(t):
+    """A copy on the same side: device, or pinned host for an offloaded cache."""
+    return t.clone().pin_memory() if t.device.type == "cpu" else t.clone()
+
+
+@pytest.mark.parametrize("window,k1,k2,on_host", [(0, 6, 9, False), (1, 6, 9, False),
+                                                  (5, 3, 0, False), (300, 8, 8, False),
+                                                  (0, 6, 9, True), (300, 8, 8, True)])
+def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2, on_host):
     """The whole step (append ordered before or beside the scorer, prune, attend with the
     sink and window pages fetched early) equals the separate calls bit for bit, and the
-    oracle on the appended cache."""
+    oracle on the appended cache; also with K/V in mapped pinned host memory."""
     cfg = _cfg(context=None, context_range=(700, 5000), batch=3, hq=8, hkv=2, k1=k1, k2=k2,
                sink=20, window=window, paged_permuted=True)
-    wl = W.make_workload(cfg, seed=40 + window)
+    wl = W.make_workload(cfg, seed=40 + window, host_pinned=on_host)
     hd, od = H.dims_pair(wl)
+    assert bool(hd.kv_on_host) == on_host
     dwl = H.to_cuda(wl)
     dev = torch.device("cuda")
     B, Hkv = cfg.batch, cfg.hkv
@@ -225,7 +233,7 @@ def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2):
     hsa.hsa_quantize_keys(hd, dwl["k_cache"], dwl["page_table"], dwl["seq_lens"], 0, 0, kq,
                           k_scale, hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
     # whole step
-    kc1, vc1, kq1 = dwl["k_cache"].clone(), dwl["v_cache"].clone(), kq.clone()
+    kc1, vc1, kq1 = _clone(dwl["k_cache"]), _clone(dwl["v_cache"]), kq.clone()
     out1 = torch.zeros((B, cfg.hq, 128), dtype=torch.float32, device=dev)
     lse1 = torch.zeros((B, cfg.hq), dtype=torch.float32, device=dev)
     bidx1 = torch.full((B, Hkv, max(k2, 1)), -7, dtype=torch.int32, device=dev)
@@ -235,7 +243,7 @@ def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2):
         hsa.hsa_decode_step(hd, dwl["q"], k_new.cuda(), v_new.cuda(), out1, lse1, kc1, vc1, kq1,
                             k_scale, dwl["page_table"], dwl["seq_lens"], bidx1, nb1, wst)
     # separate calls
-    kc2, vc2, kq2 = dwl["k_cache"].clone(), dwl["v_cache"].clone(), kq.clone()
+    kc2, vc2, kq2 = _clone(dwl["k_cache"]), _clone(dwl["v_cache"]), kq.clone()
     hsa.hsa_append_kv(hd, k_new.cuda(), v_new.cuda(), kc2, vc2, kq2, k_scale, dwl["page_table"],
                       dwl["seq_lens"])
     bidx2 = torch.full_like(bidx1, -7)
