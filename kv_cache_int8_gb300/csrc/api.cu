@@ -82,7 +82,7 @@ AttendLayout attend_layout(const Shape& s, size_t base) {
 }
 size_t attend_ws(const Shape& s) { return attend_layout(s, kErrBytes).end; }
 struct StepLayout {
-  size_t block_max, tile_max, block_idx, n_blocks, q, k_new, v_new, out, lse;
+  size_t block_max, tile_max, block_idx, n_blocks, sel_pages, q, k_new, v_new, out, lse;
   AttendLayout att;
   size_t end;
 };
@@ -92,7 +92,8 @@ StepLayout step_layout(const Shape& s) {
   l.tile_max = l.block_max + select_bm_bytes(s);
   l.block_idx = l.tile_max + select_tm_bytes(s);
   l.n_blocks = l.block_idx + up((size_t)s.batch * s.hkv * std::max(s.k2, 1) * 4);
-  l.q = l.n_blocks + up((size_t)s.batch * s.hkv * 4);
+  l.sel_pages = l.n_blocks + up((size_t)s.batch * s.hkv * 4);
+  l.q = l.sel_pages + up((size_t)s.batch * s.hkv * std::max(s.k2, 1) * 4);
   l.k_new = l.q + up((size_t)s.batch * s.hq * hsa::kHeadDim * 2);
   l.v_new = l.k_new + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 2);
   l.out = l.v_new + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 2);
@@ -192,7 +193,7 @@ int32_t check_prune_fits(const Shape& s) {
 int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, const void* k,
                   const void* v, const int32_t* pt, const int32_t* lens, const int32_t* bidx,
                   const int32_t* nb, float* out, float* lse, char* ws, const AttendLayout& l,
-                  cudaStream_t st, bool early) {
+                  cudaStream_t st, bool early, const int32_t* sel_pages = nullptr) {
   const void* kd = nullptr;
   const void* vd = nullptr;
   int32_t rc = kv_pointer(d, k, &kd);
@@ -205,6 +206,7 @@ int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, 
   buf.part_ml = reinterpret_cast<float*>(ws + l.part_ml);
   buf.part_o = reinterpret_cast<float*>(ws + l.part_o);
   buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(s, dense, host, num_sms()));
+  buf.sel_pages = sel_pages;
   return cuda_status(hsa::launch_attend(s, dense, host, q, kd, vd, pt, lens, bidx, nb, out, lse,
                                         buf, reinterpret_cast<int*>(ws), st, early));
 }
@@ -322,7 +324,8 @@ int32_t hsa_prune(const hsa_dims* d, const int32_t* seq_lens, const int32_t* blo
   rc = check_prune_fits(s);
   if (rc != HSA_OK) return rc;
   return cuda_status(hsa::launch_prune(s, seq_lens, block_max, tile_max, chunk_idx, n_chunks,
-                                       block_idx, n_blocks, nullptr, as_stream(stream)));
+                                       block_idx, n_blocks, nullptr, nullptr, nullptr,
+                                       as_stream(stream)));
 }
 
 int32_t hsa_select(const hsa_dims* d, const void* q, const int8_t* kq, const float* k_scale,
@@ -347,7 +350,8 @@ int32_t hsa_select(const hsa_dims* d, const void* q, const int8_t* kq, const flo
   rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st);
   if (rc != HSA_OK) return rc;
   return cuda_status(
-      hsa::launch_prune(s, seq_lens, bm, tm, chunk_idx, n_chunks, block_idx, n_blocks, err, st));
+      hsa::launch_prune(s, seq_lens, bm, tm, chunk_idx, n_chunks, block_idx, n_blocks, nullptr,
+                        nullptr, err, st));
 }
 
 int32_t hsa_attend(const hsa_dims* d, const void* q, const void* k_cache, const void* v_cache,
@@ -451,10 +455,13 @@ int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
                               k_scale, page_table, seq_lens, err, st, true);
     if (e != cudaSuccess) return HSA_ERR_CUDA;
   }
-  e = hsa::launch_prune(s, seq_lens, bm, tm, nullptr, nullptr, bidx, nb, err, st);
+  // the prune also resolves the kept blocks' pages, so the attend needs one round trip for them
+  int32_t* sel_pages = reinterpret_cast<int32_t*>(ws + l.sel_pages);
+  e = hsa::launch_prune(s, seq_lens, bm, tm, nullptr, nullptr, bidx, nb, page_table, sel_pages,
+                        err, st);
   if (e != cudaSuccess) return HSA_ERR_CUDA;
   rc = do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, bidx, nb, out, lse, ws,
-                 l.att, st, true);
+                 l.att, st, true, sel_pages);
   if (rc != HSA_OK) return rc;
   if (io->io_on_host) {
     e = cudaMemcpyAsync(io->out, out, (size_t)s.batch * s.hq * hsa::kHeadDim * 4,
@@ -542,7 +549,7 @@ int32_t hsa_select_noalloc(const hsa_dims* d, const void* q, const int8_t* kq,
   rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, nullptr, st);
   if (rc != HSA_OK) return rc;
   return cuda_status(hsa::launch_prune(s, seq_lens, bm, tm, chunk_idx, n_chunks, block_idx,
-                                       n_blocks, nullptr, st));
+                                       n_blocks, nullptr, nullptr, nullptr, st));
 }
 
 }  // extern "C"

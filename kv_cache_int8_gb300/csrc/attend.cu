@@ -12,14 +12,15 @@
 // Work: the attended set of (sequence b, kv head h) is a list of segments, each a
 // 16-token page clipped to a token range: the sink pages, the kept blocks (clipped to the
 // candidate region), the window pages. Dense decode uses every page of [0, N). A CTA takes
-// a contiguous share of the list for all G query heads of the group, so every K/V byte is
-// read once per group. Scores of a token: 8 lanes (16 channels each) form G partial dot
-// products and reduce them with a transposing butterfly; softmax in the log2 domain with a
-// running max and sum per head; CTAs of one (b, h) are merged by the last one to finish
-// (atomic counter, no waiting).
+// a share of the list (sparse attend: every nsplit-th segment; dense decode: a contiguous
+// range) for all G query heads of the group, so every K/V byte is read once per group.
+// Scores of a token: 8 lanes (16 channels each) form G partial dot products and reduce them
+// with a transposing butterfly; softmax in the log2 domain with a running max and sum per
+// head; CTAs of one (b, h) are merged by the last one to finish (atomic counter, no
+// waiting).
 //
 // HBM path: a producer lane fills a ring of 8 KiB slots (K page then V page of one head,
-// 4 KiB each) with cp.async.bulk copies tracked by mbarriers; each compute warp owns two
+// 4 KiB each) with cp.async.bulk copies tracked by mbarriers; each compute warp owns fixed
 // slots and processes whole segments on its own (see the HBM-path section).
 // Host path: K/V live in pinned host memory; the compute warps copy each segment into
 // shared memory with 16-byte loads through the mapped alias, one segment ahead, and
@@ -45,7 +46,10 @@ namespace {
 constexpr int kWarps = 4;                        // compute warps of the host path
 constexpr int kCompute = kWarps * 32;
 constexpr int kStages = 8;
-constexpr int kSparseWarps = 8, kSparseStages = 16;  // HBM path, sparse attend
+// HBM path, sparse attend: 7 compute warps + the producer = 8 warps, two on each SM
+// sub-partition, so a prune CTA (whose kernel runs while the attend starts) still fits beside
+// it in every sub-partition's register file and in shared memory.
+constexpr int kSparseWarps = 7, kSparseStages = 14;
 constexpr int kDenseWarps = 4, kDenseStages = 8;     // HBM path, dense decode
 constexpr int kSlotBytes = 2 * kBlockBytesBf16;  // K page + V page of one head
 constexpr int kHostThreads = kCompute;
@@ -62,6 +66,7 @@ struct AttArgs {
   const int32_t* seq_lens;
   const int32_t* block_idx;
   const int32_t* n_blocks;
+  const int32_t* sel_pages;  // nullable: page of each kept block, beside block_idx
   float* out;
   float* lse;
   float* part_ml;
@@ -120,6 +125,21 @@ __device__ __forceinline__ void read_selection(Segments& s, const AttArgs& a, in
   s.n_sel = max(0, min(a.n_blocks[(size_t)b * a.hkv + h], s.n_sel_max));
 }
 
+// Kept block r of the list, whose id kk was read from it: its page index k and token range
+// [t0, t1) inside the candidate region (empty past the count of kept blocks or for an id
+// outside the sequence).
+__device__ __forceinline__ void kept_segment(const Segments& s, int r, int kk, int sink, int& k,
+                                             int& t0, int& t1) {
+  k = 0;
+  t0 = t1 = 0;
+  if (r >= s.n_sel) return;
+  const int kmax = (s.n + kPage - 1) / kPage;
+  if (kk < 0 || kk >= kmax) return;
+  k = kk;
+  t0 = max(k * kPage, sink);
+  t1 = min(k * kPage + kPage, s.cand_hi);
+}
+
 // Segment i: page index k (token block) and the attended token range [t0, t1) (empty when
 // t0 >= t1).
 __device__ __forceinline__ void segment_at(const Segments& s, int i, int sink, int& k, int& t0,
@@ -133,18 +153,7 @@ __device__ __forceinline__ void segment_at(const Segments& s, int i, int sink, i
     t0 = max(k * kPage, s.w0);
     t1 = min(k * kPage + kPage, s.n);
   } else {
-    const int r = i - s.n_sink - s.n_win;
-    k = 0;
-    t0 = t1 = 0;
-    if (r >= s.n_sel) return;
-    k = s.sel[r];
-    const int kmax = (s.n + kPage - 1) / kPage;
-    if (k < 0 || k >= kmax) {
-      k = 0;
-      return;
-    }
-    t0 = max(k * kPage, sink);
-    t1 = min(k * kPage + kPage, s.cand_hi);
+    kept_segment(s, i - s.n_sink - s.n_win, s.sel[i - s.n_sink - s.n_win], sink, k, t0, t1);
   }
 }
 
@@ -304,8 +313,9 @@ __device__ __forceinline__ void process_segment(State<G>& st, const float (&qf)[
 // Output of a CTA from its merged state in shared memory (o[G][128], m[G], l[G]): either the
 // final result (one split) or a partial, and then the combine over all splits by the last
 // CTA of (b, h) to finish. `red` (shared, at least G * kMaxSplits + 8 floats) may alias
-// `o`. Called by all threads of the CTA after the merged state is complete.
-template <int G>
+// `o`. Called by all threads of the CTA after the merged state is complete. NB: splits a
+// thread of the combine loads per round trip.
+template <int G, int NB>
 __device__ void finish_common(const AttArgs& a, int b, int h, int split, const float* o,
                               const float* m, const float* l, float* red, int nthreads) {
   const int tid = threadIdx.x;
@@ -327,32 +337,39 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
     }
   }
   if (a.nsplit == 1) return;
-  __threadfence();
+  // One acquire-release increment by thread 0 between two CTA barriers: the first barrier
+  // orders every thread's partial writes before the release, the second orders the last
+  // CTA's reads of the other partials after the acquire (the pattern of a grid barrier).
   __syncthreads();
   if (tid == 0) {
-    const int prev = atomicAdd(&a.counters[(size_t)b * a.hkv + h], 1);
+    const int prev = atomic_add_acq_rel_gpu(&a.counters[(size_t)b * a.hkv + h], 1);
     is_last = prev == a.nsplit - 1;
   }
   __syncthreads();
   if (!is_last) return;
-  __threadfence();
-  // every thread streams the (m, l) pair and its 4 channels of all splits together (one
-  // round trip per batch of splits) and merges them online: the running state is kept
-  // relative to the largest m seen so far
+  // Two threads per (head, 4 channels), each taking one half of the splits: a thread loads
+  // the (m, l) pairs and partial outputs of up to NB splits before it uses any (one round
+  // trip per NB splits) and merges them online, keeping its state relative to the largest m
+  // seen so far; then the two threads of a pair (adjacent lanes) merge their states. Both
+  // 2 * G * 32 and the block size are multiples of 32, so every warp takes part in an
+  // iteration with all its lanes or not at all.
   (void)red;
-  for (int x = tid; x < G * 32; x += blockDim.x) {
-    const int j = x >> 5, d4 = (x & 31) * 4;
+  const int per = (a.nsplit + 1) >> 1;
+  for (int x = tid; x < 2 * G * 32; x += blockDim.x) {
+    const int it = x >> 1, half = x & 1;
+    const int j = it >> 5, d4 = (it & 31) * 4;
     const size_t row = (size_t)b * hq + (size_t)h * G + j;
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + row * a.nsplit;
     const float4* po = reinterpret_cast<const float4*>(a.part_o + row * a.nsplit * kHeadDim + d4);
+    const int s_lo = half * per, s_hi = min(a.nsplit, s_lo + per);
     float M = kNeg, L = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int sp0 = 0; sp0 < a.nsplit; sp0 += 8) {
-      float2 mlv[8];
-      float4 ov[8];
+    for (int sp0 = s_lo; sp0 < s_hi; sp0 += NB) {
+      float2 mlv[NB];
+      float4 ov[NB];
 #pragma unroll
-      for (int u = 0; u < 8; u++) {
-        if (sp0 + u < a.nsplit) {
+      for (int u = 0; u < NB; u++) {
+        if (sp0 + u < s_hi) {
           mlv[u] = __ldcg(ml + sp0 + u);
           ov[u] = __ldcg(po + (size_t)(sp0 + u) * (kHeadDim / 4));
         } else {
@@ -361,7 +378,7 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
         }
       }
 #pragma unroll
-      for (int u = 0; u < 8; u++) {
+      for (int u = 0; u < NB; u++) {
         if (!(mlv[u].y > 0.0f)) continue;
         const float m_new = fmaxf(M, mlv[u].x);
         const float c = exp2f(M - m_new), w = exp2f(mlv[u].x - m_new);
@@ -373,10 +390,28 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
         M = m_new;
       }
     }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    *reinterpret_cast<float4*>(a.out + row * kHeadDim + d4) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (d4 == 0 && a.lse) a.lse[row] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    // the pair: a state with l = 0 has m = kNeg and contributes nothing
+    const float Mo = __shfl_xor_sync(0xffffffffu, M, 1);
+    const float Lo = __shfl_xor_sync(0xffffffffu, L, 1);
+    float4 ao;
+    ao.x = __shfl_xor_sync(0xffffffffu, acc.x, 1);
+    ao.y = __shfl_xor_sync(0xffffffffu, acc.y, 1);
+    ao.z = __shfl_xor_sync(0xffffffffu, acc.z, 1);
+    ao.w = __shfl_xor_sync(0xffffffffu, acc.w, 1);
+    if (half == 0) {
+      const float Mn = fmaxf(M, Mo);
+      const float c = L > 0.0f ? exp2f(M - Mn) : 0.0f;
+      const float co = Lo > 0.0f ? exp2f(Mo - Mn) : 0.0f;
+      L = L * c + Lo * co;
+      acc.x = acc.x * c + ao.x * co;
+      acc.y = acc.y * c + ao.y * co;
+      acc.z = acc.z * c + ao.z * co;
+      acc.w = acc.w * c + ao.w * co;
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      *reinterpret_cast<float4*>(a.out + row * kHeadDim + d4) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (d4 == 0 && a.lse) a.lse[row] = L > 0.0f ? (Mn + log2f(L)) * kLn2 : -INFINITY;
+    }
   }
   if (tid == 0) a.counters[(size_t)b * a.hkv + h] = 0;
 }
@@ -408,7 +443,7 @@ __device__ void finish(const AttArgs& a, State<G>& st, Scratch& sc, int b, int h
     }
   }
   __syncthreads();
-  finish_common<G>(a, b, h, split, red, sc.m, sc.l, red, kCompute);
+  finish_common<G, 8>(a, b, h, split, red, sc.m, sc.l, red, kCompute);
 }
 
 template <int G>
@@ -519,9 +554,9 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
   __syncwarp();  // the next segment rewrites the scratch
 }
 
-// W compute warps and NS ring slots (NS a multiple of W): the sparse path uses 8 warps and 16
-// slots so that every segment of a CTA is in flight at once; dense decode uses 4 and 8 with
-// three CTAs per SM.
+// W compute warps and NS ring slots (NS a multiple of W): the sparse path uses 7 warps and 14
+// slots, enough for every segment of a CTA to be in flight at once; dense decode uses 4 and 8
+// with three CTAs per SM.
 template <int G, bool DENSE, int W, int NS>
 __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_kernel(const AttArgs a) {
   static_assert(NS % W == 0, "each compute warp owns fixed ring slots");
@@ -545,8 +580,22 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
   if (tid == 0 && split == 0 && h == 0 && (n_raw < 0 || n_raw > a.max_pages * kPage))
     set_error(a.err, kDevErrCheck);
   Segments S = make_segments<DENSE>(a, b, h);
-  const int i0 = (int)((long long)S.total * split / a.nsplit);
-  const int i1 = (int)((long long)S.total * (split + 1) / a.nsplit);
+  // The CTA's segments, local index j -> segment first + j * stride. Sparse attend deals the
+  // list out round-robin, so that the kept blocks (known last) are spread over every CTA of
+  // (b, h); dense decode takes a contiguous range of pages.
+  int first, stride, cnt;
+  if (DENSE) {
+    first = (int)((long long)S.total * split / a.nsplit);
+    cnt = (int)((long long)S.total * (split + 1) / a.nsplit) - first;
+    stride = 1;
+  } else {
+    first = split;
+    stride = a.nsplit;
+    cnt = S.total > split ? (S.total - split + a.nsplit - 1) / a.nsplit : 0;
+  }
+  // local segments [0, n_pre) are sink or window pages: they need no selection
+  const int n_sw = S.n_sink + S.n_win;
+  const int n_pre = n_sw <= first ? 0 : min(cnt, (n_sw - first + stride - 1) / stride);
 
   if (tid == 0) {
     for (int s = 0; s < NS; s++) {
@@ -568,32 +617,46 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
     // producer warp: the lanes resolve the block and page ids of 32 segments at once; lane 0
     // then publishes each segment's (block, t0, t1) with its slot and issues the copies
     bool ok = true, have_sel = false;
-    for (int ib = i0; ok && ib < i1; ib += 32) {
-      if (!have_sel && min(i1, ib + 32) > S.n_sink + S.n_win) {
+    const uint64_t policy = l2_evict_first_policy();  // each K/V page is read once
+    for (int jb = 0; ok && jb < cnt;) {
+      // batches of up to 32 segments, none straddling n_pre: the sink and window pages are
+      // fetched before the wait for the selection
+      const int jend = jb < n_pre ? min(n_pre, jb + 32) : min(cnt, jb + 32);
+      if (!have_sel && jb >= n_pre) {
         grid_dep_wait();
         read_selection(S, a, b, h);
         have_sel = true;
       }
       int k = 0, t0 = 0, t1 = 0, page = -1;
-      if (ib + lane < i1) {
-        segment_at(S, ib + lane, a.sink, k, t0, t1);
-        if (t0 < t1) {
-          page = a.page_table[(size_t)b * a.max_pages + k];
-          if (page < 0 || page >= a.num_pages) {
-            set_error(a.err, kDevErrCheck);
-            page = -1;
-          }
+      if (jb + lane < jend) {
+        const int i = first + (jb + lane) * stride;
+        if (i < n_sw) {
+          segment_at(S, i, a.sink, k, t0, t1);
+          if (t0 < t1) page = a.page_table[(size_t)b * a.max_pages + k];
+        } else {
+          // a kept block: its id and (when given) its page are read in the same round trip
+          // as the count of kept blocks (both lists hold K2 entries; r < K2)
+          const int r = i - n_sw;
+          const size_t at = ((size_t)b * a.hkv + h) * a.k2 + r;
+          const int kk = a.block_idx[at];
+          const int pp = a.sel_pages ? a.sel_pages[at] : -1;
+          kept_segment(S, r, kk, a.sink, k, t0, t1);
+          if (t0 < t1) page = a.sel_pages ? pp : a.page_table[(size_t)b * a.max_pages + k];
+        }
+        if (t0 < t1 && (page < 0 || page >= a.num_pages)) {
+          set_error(a.err, kDevErrCheck);
+          page = -1;
         }
         if (page < 0) t0 = t1 = 0;
       }
-      const int n = min(32, i1 - ib);
+      const int n = jend - jb;
       for (int q = 0; q < n; q++) {
         const int kq = __shfl_sync(0xffffffffu, k, q);
         const int t0q = __shfl_sync(0xffffffffu, t0, q);
         const int t1q = __shfl_sync(0xffffffffu, t1, q);
         const int pq = __shfl_sync(0xffffffffu, page, q);
         if (lane == 0) {
-          const int j = ib + q - i0, s = j % NS;
+          const int j = jb + q, s = j % NS;
           if (j >= NS && !mbar_wait(&empty[s], ((j / NS) - 1) & 1)) {
             set_error(a.err, kDevErrTimeout);
             ok = false;
@@ -602,9 +665,9 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
             if (pq >= 0) {
               const size_t off = ((size_t)pq * a.hkv + h) * kPage * kHeadDim;
               mbar_arrive_expect_tx(&full[s], kSlotBytes);
-              bulk_load(ring + s * kSlotBytes, a.k + off, kBlockBytesBf16, &full[s]);
-              bulk_load(ring + s * kSlotBytes + kBlockBytesBf16, a.v + off, kBlockBytesBf16,
-                        &full[s]);
+              bulk_load_hint(ring + s * kSlotBytes, a.k + off, kBlockBytesBf16, &full[s], policy);
+              bulk_load_hint(ring + s * kSlotBytes + kBlockBytesBf16, a.v + off, kBlockBytesBf16,
+                             &full[s], policy);
             } else {
               mbar_arrive(&full[s]);
             }
@@ -613,15 +676,16 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
       }
+      jb = jend;
     }
     if (!ok && lane == 0) {
-      const int issued = i1 - i0;
+      const int issued = cnt;
       for (int j = max(0, issued - NS); j < issued; j++) mbar_wait(&full[j % NS], (j / NS) & 1);
     }
   } else {
     float qf[G][16];
     load_query<G>(qf, a, b, h, lane & 7);
-    for (int j = warp; i0 + j < i1; j += W) {
+    for (int j = warp; j < cnt; j += W) {
       const int s = j % NS;
       if (!mbar_wait(&full[s], (j / NS) & 1)) {
         set_error(a.err, kDevErrTimeout);
@@ -681,7 +745,7 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
     }
   }
   __syncthreads();
-  finish_common<G>(a, b, h, split, mo, mm, ml, o, W * 32);
+  finish_common<G, DENSE ? 8 : 16>(a, b, h, split, mo, mm, ml, o, W * 32);
 }
 
 // ---------------------------------------------------------- mapped-host path
@@ -768,8 +832,7 @@ template <int G, bool DENSE>
 cudaError_t launch_g(AttArgs a, dim3 grid, bool host, cudaStream_t st) {
   if (host) {
     const size_t smem = host_smem(G);
-    cudaError_t e = cudaFuncSetAttribute(attend_host_kernel<G, DENSE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_kernel_smem(attend_host_kernel<G, DENSE>, smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(attend_host_kernel<G, DENSE>, grid, dim3(kHostThreads), smem, st, true, a);
   }
@@ -777,7 +840,7 @@ cudaError_t launch_g(AttArgs a, dim3 grid, bool host, cudaStream_t st) {
   constexpr int NS = DENSE ? kDenseStages : kSparseStages;
   constexpr size_t smem = tma_smem<W, NS>();
   auto kern = attend_tma_kernel<G, DENSE, W, NS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_kernel_smem(kern, smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, grid, dim3((W + 1) * 32), smem, st, true, a);
 }
@@ -813,6 +876,7 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
   a.seq_lens = seq_lens;
   a.block_idx = block_idx;
   a.n_blocks = n_blocks;
+  a.sel_pages = buf.sel_pages;
   a.out = out;
   a.lse = lse;
   a.part_ml = buf.part_ml;

@@ -38,9 +38,12 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const
                                 const float* k_scale, const int32_t* page_table,
                                 const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
                                 int* err, int num_sms, cudaStream_t st);
+// page_table / sel_pages (both nullable): also write the page of every kept block into
+// sel_pages [B][Hkv][K2], entries [0, n_blocks) (for launch_attend's sel_pages).
 cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t* block_max,
                          const int32_t* tile_max, int32_t* chunk_idx, int32_t* n_chunks,
-                         int32_t* block_idx, int32_t* n_blocks, int* err, cudaStream_t st);
+                         int32_t* block_idx, int32_t* n_blocks, const int32_t* page_table,
+                         int32_t* sel_pages, int* err, cudaStream_t st);
 int prune_max_chunks();
 size_t prune_smem_bytes(const Shape& s);
 
@@ -53,6 +56,7 @@ struct AttendBuffers {
   float* part_o;    // [B][Hq][nsplit][128]
   int* counters;    // [B][Hkv]
   int nsplit;
+  const int32_t* sel_pages = nullptr;  // optional: the kept blocks' pages, from launch_prune
 };
 int attend_splits(const Shape& s, bool dense, bool host, int num_sms);
 cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,

@@ -230,6 +230,8 @@ cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_ne
                              const int32_t* page_table, const int32_t* seq_lens, int* err,
                              cudaStream_t st, bool beside) {
   const int threads = ((s.hkv * 16 + 31) / 32) * 32;
+  const cudaError_t e = set_kernel_smem(append_kv_kernel, 0);
+  if (e != cudaSuccess) return e;
   return launch_kernel(append_kv_kernel, dim3(s.batch), dim3(threads), 0, st, beside,
                        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
                        static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache),

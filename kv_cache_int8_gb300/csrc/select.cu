@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     // The whole warp resolves the page ids of the next 32 tiles at once (one coalesced
     // round trip), then lane 0 issues their copies in order as ring slots free up.
     bool ok = true;
+    const uint64_t policy = l2_evict_first_policy();  // each code is read once
     int bw = b;  // sequence of tile f0 + jb (warp-uniform)
     for (int jb = 0; ok && f0 + jb < f1; jb += 32) {
       const int f = f0 + jb + lane;
@@ -221,7 +222,8 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
 #pragma unroll
             for (int q = 0; q < kTileBlocks; q++)
               if (rr[q] >= 0)
-                tma_load_2d(ring + s * kStageBytes + q * kBlockBytesI8, &kq_map, 0, rr[q], &full[s]);
+                tma_load_2d_hint(ring + s * kStageBytes + q * kBlockBytesI8, &kq_map, 0, rr[q],
+                                 &full[s], policy);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -332,6 +334,8 @@ struct PruneArgs {
   int32_t* n_chunks;
   int32_t* block_idx;
   int32_t* n_blocks;
+  const int32_t* page_table;  // with sel_pages: the page of every kept block is written too
+  int32_t* sel_pages;         // nullable, [B][Hkv][K2] beside block_idx
   int* err;
   int hkv, max_pages, chunk_blocks, k1, k2, sink, window, vals_cap, cand_cap;
 };
@@ -511,12 +515,16 @@ __device__ __forceinline__ void gather_strided(int* dst, const int32_t* __restri
   }
 }
 
-__global__ void __launch_bounds__(kPruneThreads) prune_kernel(const PruneArgs a) {
+// At most 40 registers a thread (three 512-thread CTAs' worth per SM): a prune CTA and a
+// CTA of the sparse attend, which is launched while the prune runs, then fit on one SM
+// together, and no attend CTA has to wait for the prune to leave its SM.
+__global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_kernel(const PruneArgs a) {
   extern __shared__ __align__(16) int psmem[];
   SelectScratch& ss = *reinterpret_cast<SelectScratch*>(psmem);
   int* vals = psmem + sizeof(SelectScratch) / sizeof(int);  // vals_cap
   int* cand = vals + a.vals_cap;                            // cand_cap block ids of module 2
   int* kept_chunks = cand + a.cand_cap;                     // k1
+  int* cand_page = kept_chunks + a.k1;                      // cand_cap pages (with sel_pages)
 
   const int h = blockIdx.x, b = blockIdx.y;
   grid_dep_wait();  // the scores come from the previous kernel
@@ -568,14 +576,19 @@ __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const PruneArgs a)
   // ---- module 2: the kept chunks' blocks (P per chunk, ascending; blocks outside the
   // candidate region are INT_MIN placeholders that are never kept), top-K2
   const int n2 = got1 * P;
+  // with sel_pages, each candidate's page id is loaded beside its block maximum (same round
+  // trip), so the next kernel reads the pages of the kept blocks directly
+  const int32_t* prow = a.sel_pages ? a.page_table + (size_t)b * a.max_pages : nullptr;
   int valid_local = 0;
   for (int x0 = threadIdx.x; x0 < n2; x0 += 4 * kPruneThreads) {
-    int v[4], kk[4];
+    int v[4], kk[4], pg[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       const int x = x0 + u * kPruneThreads;
       kk[u] = x < n2 ? kept_chunks[x / P] * P + x % P : -1;
-      v[u] = (kk[u] >= k_lo && kk[u] < k_hi) ? __ldg(bm + kk[u]) : INT_MIN;
+      const bool in = kk[u] >= k_lo && kk[u] < k_hi;
+      v[u] = in ? __ldg(bm + kk[u]) : INT_MIN;
+      pg[u] = (in && prow) ? __ldg(prow + kk[u]) : -1;
     }
 #pragma unroll
     for (int u = 0; u < 4; u++) {
@@ -583,6 +596,7 @@ __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const PruneArgs a)
       if (x < n2) {
         cand[x] = kk[u];
         vals[x] = v[u];
+        if (prow) cand_page[x] = pg[u];
         valid_local += v[u] != INT_MIN;
       }
     }
@@ -603,6 +617,7 @@ __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const PruneArgs a)
   if (keep2 > 0) {
     got2 = collect(vals, n2, T, need_eq, ss, [&](int pos, int i) {
       a.block_idx[bh * a.k2 + pos] = cand[i];
+      if (prow) a.sel_pages[bh * a.k2 + pos] = cand_page[i];
     });
   }
   for (int i = got2 + threadIdx.x; i < a.k2; i += kPruneThreads) a.block_idx[bh * a.k2 + i] = -1;
@@ -627,7 +642,7 @@ int prune_max_chunks() { return kMaxChunks; }
 size_t prune_smem_bytes(const Shape& s) {
   int vals_cap, cand_cap;
   if (prune_caps(s, vals_cap, cand_cap) != 0) return ~size_t(0);
-  return sizeof(SelectScratch) + sizeof(int) * ((size_t)vals_cap + cand_cap + s.k1);
+  return sizeof(SelectScratch) + sizeof(int) * ((size_t)vals_cap + 2 * (size_t)cand_cap + s.k1);
 }
 
 int score_max_tiles(const Shape& s) { return (s.max_pages + kTileBlocks - 1) / kTileBlocks; }
@@ -660,24 +675,21 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const
   cudaError_t e;
   switch (s.group) {
     case 1:
-      e = cudaFuncSetAttribute(score_blocks_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
+      e = set_kernel_smem(score_blocks_kernel<1>, smem);
       if (e != cudaSuccess) return e;
       e = launch_kernel(score_blocks_kernel<1>, dim3(grid), dim3(kScoreThreads), smem, st, true,
                         kq_map, a);
       if (e != cudaSuccess) return e;
       break;
     case 2:
-      e = cudaFuncSetAttribute(score_blocks_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
+      e = set_kernel_smem(score_blocks_kernel<2>, smem);
       if (e != cudaSuccess) return e;
       e = launch_kernel(score_blocks_kernel<2>, dim3(grid), dim3(kScoreThreads), smem, st, true,
                         kq_map, a);
       if (e != cudaSuccess) return e;
       break;
     case 4:
-      e = cudaFuncSetAttribute(score_blocks_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
+      e = set_kernel_smem(score_blocks_kernel<4>, smem);
       if (e != cudaSuccess) return e;
       e = launch_kernel(score_blocks_kernel<4>, dim3(grid), dim3(kScoreThreads), smem, st, true,
                         kq_map, a);
@@ -691,7 +703,9 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const
 
 cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t* block_max,
                          const int32_t* tile_max, int32_t* chunk_idx, int32_t* n_chunks,
-                         int32_t* block_idx, int32_t* n_blocks, int* err, cudaStream_t st) {
+                         int32_t* block_idx, int32_t* n_blocks, const int32_t* page_table,
+                         int32_t* sel_pages, int* err, cudaStream_t st) {
+  if (sel_pages != nullptr && page_table == nullptr) return cudaErrorInvalidValue;
   PruneArgs a;
   if (prune_caps(s, a.vals_cap, a.cand_cap) != 0) return cudaErrorInvalidValue;
   const size_t smem = prune_smem_bytes(s);
@@ -704,6 +718,8 @@ cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t*
   a.n_chunks = n_chunks;
   a.block_idx = block_idx;
   a.n_blocks = n_blocks;
+  a.page_table = page_table;
+  a.sel_pages = sel_pages;
   a.err = err;
   a.hkv = s.hkv;
   a.max_pages = s.max_pages;
@@ -712,8 +728,7 @@ cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t*
   a.k2 = s.k2;
   a.sink = s.sink;
   a.window = s.window;
-  cudaError_t e =
-      cudaFuncSetAttribute(prune_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_kernel_smem(prune_kernel, smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(prune_kernel, dim3(s.hkv, s.batch), dim3(kPruneThreads), smem, st, true, a);
 }
