@@ -153,11 +153,12 @@ int32_t hsa_score_blocks(const hsa_dims* d, const void* q, const int8_t* kq,
 
 /*
  * The two pruning modules on precomputed block maxima (InfiniteHiP article, section
- * "实现 7.24 倍的端到端解码加速"). tile_max (nullable) as written by hsa_score_blocks; it is
- * read instead of reducing block_max when d->chunk == 64. chunk_idx int32
- * [batch][hkv][k1] (nullable), n_chunks int32 [batch][hkv] (nullable), block_idx int32
- * [batch][hkv][k2], n_blocks int32 [batch][hkv]. Limit: at most 53248 chunks per sequence
- * (ceil(max_pages_per_seq * 16 / chunk)); larger returns HSA_ERR_UNSUPPORTED.
+ * "实现 7.24 倍的端到端解码加速"). tile_max (nullable) as written by hsa_score_blocks; with
+ * d->chunk == 64 it may be read instead of reducing block_max (the two must agree).
+ * block_max and tile_max must be 16-byte aligned (else HSA_ERR_INVALID_ARG). chunk_idx
+ * int32 [batch][hkv][k1] (nullable), n_chunks int32 [batch][hkv] (nullable), block_idx
+ * int32 [batch][hkv][k2], n_blocks int32 [batch][hkv]. Limit: at most 53248 chunks per
+ * sequence (ceil(max_pages_per_seq * 16 / chunk)); larger returns HSA_ERR_UNSUPPORTED.
  */
 int32_t hsa_prune(const hsa_dims* d, const int32_t* seq_lens, const int32_t* block_max,
                   const int32_t* tile_max, int32_t* chunk_idx, int32_t* n_chunks,

@@ -321,6 +321,7 @@ int32_t hsa_prune(const hsa_dims* d, const int32_t* seq_lens, const int32_t* blo
   int32_t rc = check_dims(d, s, true);
   if (rc != HSA_OK) return rc;
   if (!seq_lens || !block_max || !n_blocks || (!block_idx && s.k2 > 0)) return HSA_ERR_INVALID_ARG;
+  if (!aligned(block_max, 16) || !aligned(tile_max, 16)) return HSA_ERR_INVALID_ARG;
   rc = check_prune_fits(s);
   if (rc != HSA_OK) return rc;
   return cuda_status(hsa::launch_prune(s, seq_lens, block_max, tile_max, chunk_idx, n_chunks,

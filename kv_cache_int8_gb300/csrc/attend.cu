@@ -39,6 +39,14 @@
 #ifndef HSA_DENSE_CTAS_PER_SM
 #define HSA_DENSE_CTAS_PER_SM 3
 #endif
+#ifndef HSA_SPARSE_WARPS
+#define HSA_SPARSE_WARPS 8
+#endif
+// Sparse attend: leave one SM per (sequence, kv head) to the prune kernel that is still
+// running when the attend starts, when that costs at most a quarter of the splits.
+#ifndef HSA_SPARSE_RESERVE
+#define HSA_SPARSE_RESERVE 1
+#endif
 
 namespace hsa {
 namespace {
@@ -46,10 +54,10 @@ namespace {
 constexpr int kWarps = 4;                        // compute warps of the host path
 constexpr int kCompute = kWarps * 32;
 constexpr int kStages = 8;
-// HBM path, sparse attend: 7 compute warps + the producer = 8 warps, two on each SM
-// sub-partition, so a prune CTA (whose kernel runs while the attend starts) still fits beside
-// it in every sub-partition's register file and in shared memory.
-constexpr int kSparseWarps = 7, kSparseStages = 14;
+// HBM path, sparse attend: 8 compute warps + the producer. A CTA of it does not fit beside a
+// prune CTA (the three warps on one SM sub-partition take its register file), so the prune
+// keeps its SMs to itself; the attend's grid leaves those SMs free (HSA_SPARSE_RESERVE).
+constexpr int kSparseWarps = HSA_SPARSE_WARPS, kSparseStages = 2 * HSA_SPARSE_WARPS;
 constexpr int kDenseWarps = 4, kDenseStages = 8;     // HBM path, dense decode
 constexpr int kSlotBytes = 2 * kBlockBytesBf16;  // K page + V page of one head
 constexpr int kHostThreads = kCompute;
@@ -554,7 +562,7 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
   __syncwarp();  // the next segment rewrites the scratch
 }
 
-// W compute warps and NS ring slots (NS a multiple of W): the sparse path uses 7 warps and 14
+// W compute warps and NS ring slots (NS a multiple of W): the sparse path uses 8 warps and 16
 // slots, enough for every segment of a CTA to be in flight at once; dense decode uses 4 and 8
 // with three CTAs per SM.
 template <int G, bool DENSE, int W, int NS>
@@ -858,6 +866,10 @@ int attend_splits(const Shape& s, bool dense, bool host, int num_sms) {
   // dense: about three CTAs per SM; sparse: fewer, each with several segments
   const int per_sm = host ? 4 : (dense ? HSA_DENSE_CTAS_PER_SM : HSA_SPARSE_CTAS_PER_SM);
   long long want = ((long long)num_sms * per_sm + units - 1) / units;
+  if (!dense && !host && HSA_SPARSE_RESERVE && num_sms > units) {
+    const long long reserved = std::max<long long>(1, (num_sms - units) / units);
+    if (4 * reserved >= 3 * want) want = reserved;
+  }
   want = std::min<long long>(want, std::max<long long>(1, segs / 4));
   return (int)std::max<long long>(1, std::min<long long>(want, kMaxSplits));
 }

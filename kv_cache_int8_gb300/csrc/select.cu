@@ -17,11 +17,13 @@
 // products, their max is the token score and a 16-lane max gives the block maximum.
 //
 // prune_kernel: one CTA per (sequence, kv head). Chunk scores (the scorer's per-tile maxima
-// for 64-token chunks, else the max of their blocks' maxima) are staged in shared memory;
-// the K-th largest value is found by radix selection on 8-bit digits of (value - min) with
-// per-warp histograms; ties at the threshold are broken toward lower indices by ballots
-// over warp-contiguous ranges, which also write the kept indices in ascending order.
-// Module 2 repeats this on the blocks of the kept chunks.
+// for 64-token chunks, else the max of their blocks' maxima) are staged in shared memory
+// with bulk copies, and so are the whole row of block maxima and page ids when they fit;
+// the K-th largest value is found by radix selection on 8-bit digits (two CTA barriers a
+// digit); ties
+// at the threshold are broken toward lower indices by ballots over warp-contiguous ranges,
+// which also write the kept indices in ascending order. Module 2 repeats this on the blocks
+// of the kept chunks.
 #include <algorithm>
 #include <climits>
 
@@ -321,9 +323,13 @@ size_t score_smem_bytes(int batch) {
 #endif
 constexpr int kPruneThreads = HSA_PRUNE_THREADS;  // overridable at build time for tuning
 constexpr int kPruneWarps = kPruneThreads / 32;
-constexpr int kDigitBins = 256;
 constexpr int kMaxChunks = 53248;
+constexpr int kRowCap = 16384;  // block-maxima rows up to this many blocks are staged whole
 constexpr size_t kSmemLimit = 227 * 1024;
+constexpr int kDigitBins = 256;
+constexpr int kHistCopies = kPruneWarps / 2;
+static_assert(kPruneThreads >= kDigitBins && kPruneThreads % 64 == 0,
+              "one scan thread per digit, two warps per histogram");
 
 struct PruneArgs {
   const int32_t* seq_lens;
@@ -337,15 +343,19 @@ struct PruneArgs {
   const int32_t* page_table;  // with sel_pages: the page of every kept block is written too
   int32_t* sel_pages;         // nullable, [B][Hkv][K2] beside block_idx
   int* err;
-  int hkv, max_pages, chunk_blocks, k1, k2, sink, window, vals_cap, cand_cap;
+  int hkv, max_pages, chunk_blocks, k1, k2, sink, window;
+  int vals_cap, cand_cap, kept_cap, row_cap, prow_cap;  // shared-memory array sizes (0: none)
 };
 
-// Shared scratch of the selection: per-warp digit histograms and per-warp totals.
-struct SelectScratch {
-  unsigned hist[kPruneWarps][kDigitBins];
-  int w_a[kPruneWarps], w_b[kPruneWarps];
-  int red[kPruneWarps];
-  int decided[4];
+// Shared scratch of the selection.
+struct PruneShared {
+  unsigned hist[kHistCopies][kDigitBins];  // digit histograms (warp w counts into w / 2), zero
+                                           // between selections
+  int sfx[kDigitBins];                     // per digit: in-group suffix count
+  int tot[kPruneWarps];                    // per-group / per-warp totals
+  int mn[kPruneWarps], mx[kPruneWarps];    // per-warp min / max of the valid values
+  int w_a[kPruneWarps], w_b[kPruneWarps];  // per-warp counts of the collect
+  uint64_t bar;                            // completion of the staging copies
 };
 
 __device__ __forceinline__ unsigned lanemask_lt() {
@@ -354,93 +364,166 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
-// Min of the entries that are not INT_MIN (placeholders), or INT_MAX if none.
-__device__ int block_min_valid(const int* vals, int n, SelectScratch& ss) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int m = INT_MAX;
-  for (int i = threadIdx.x; i < n; i += kPruneThreads)
-    if (vals[i] != INT_MIN) m = min(m, vals[i]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if (lane == 0) ss.red[warp] = m;
-  __syncthreads();
-  int r = ss.red[0];
-#pragma unroll
-  for (int w = 1; w < kPruneWarps; w++) r = min(r, ss.red[w]);
-  __syncthreads();
-  return r;
-}
-
 // Order-preserving key of a value relative to the smallest valid value; placeholders get 0.
 __device__ __forceinline__ unsigned rel_key(int v, int vmin) {
   return v == INT_MIN ? 0u : (unsigned)((long long)v - vmin) + 1u;
 }
 
-// The K-th largest value T of vals[0..n) (0 < K < number of valid entries) by radix
-// selection on 8-bit digits of the keys, from the highest digit in which they differ;
-// need_eq = K - #(values > T), i.e. how many of the entries equal to T are kept (the
-// lowest-index ones). Two CTA barriers per digit.
-__device__ void kth_largest(const int* vals, int n, int K, SelectScratch& ss, int& T,
-                            int& need_eq) {
+// A row src[0, n) of ints in global memory (in an array whose base is 16-byte aligned) to be
+// staged in shared memory at dst_base (16-byte aligned, room for n + 3 ints): the copy of
+// src[i] lands at dst_base[o + i]. The 16-byte-aligned span [src - o, src - o + body) is
+// copied in bulk, the ragged tail with plain loads.
+struct StagedRow {
+  const int32_t* s0;  // src - o, 16-byte aligned, inside the array
+  int* dst_base;
+  int o, body, n;
+  __device__ int* dst() const { return dst_base + o; }
+  __device__ uint32_t bytes() const { return (uint32_t)body * 4u; }
+};
+
+__device__ __forceinline__ StagedRow plan_row(int* dst_base, const int32_t* src, int n) {
+  StagedRow r;
+  r.o = (int)((reinterpret_cast<uintptr_t>(src) >> 2) & 3);
+  r.s0 = src - r.o;
+  r.body = ((n + r.o) / 4) * 4;
+  r.dst_base = dst_base;
+  r.n = n;
+  return r;
+}
+
+// Thread 0: the bulk copies of a planned row (at most 64 KiB each), completing on `bar`.
+__device__ __forceinline__ void issue_row(const StagedRow& r, uint64_t* bar) {
+  for (int off = 0; off < r.body; off += 16384)
+    bulk_load(r.dst_base + off, r.s0 + off, (uint32_t)min(16384, r.body - off) * 4u, bar);
+}
+
+// All threads: the ragged tail of a planned row.
+__device__ __forceinline__ void tail_row(const StagedRow& r) {
+  for (int i = r.body + threadIdx.x; i < r.n + r.o; i += kPruneThreads)
+    r.dst_base[i] = __ldg(r.s0 + i);
+}
+
+// Issue (thread 0) and tail of a planned row; returns where src[0] lands.
+__device__ __forceinline__ int* stage(const StagedRow& r, uint64_t* bar) {
+  if (threadIdx.x == 0) issue_row(r, bar);
+  tail_row(r);
+  return r.dst();
+}
+
+// Min and max of the valid (not INT_MIN) entries of vals[0, n), for every thread; an empty
+// set gives (INT_MAX, INT_MIN). One CTA barrier.
+__device__ __forceinline__ void block_min_max(const int* vals, int n, PruneShared& ps, int& mn,
+                                              int& mx) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int vmin = block_min_valid(vals, n, ss);
-  unsigned kmax = 0;
-  for (int i = threadIdx.x; i < n; i += kPruneThreads) kmax = max(kmax, rel_key(vals[i], vmin));
+  mn = INT_MAX;
+  mx = INT_MIN;
+  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * kPruneThreads) {
+    int v[4];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
-  if (lane == 0) ss.red[warp] = (int)kmax;
+    for (int u = 0; u < 4; u++) {
+      const int i = i0 + u * kPruneThreads;
+      v[u] = i < n ? vals[i] : INT_MIN;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      if (v[u] != INT_MIN) {
+        mn = min(mn, v[u]);
+        mx = max(mx, v[u]);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  if (lane == 0) {
+    ps.mn[warp] = mn;
+    ps.mx[warp] = mx;
+  }
   __syncthreads();
-  kmax = 0;
+  mn = ps.mn[0];
+  mx = ps.mx[0];
 #pragma unroll
-  for (int w = 0; w < kPruneWarps; w++) kmax = max(kmax, (unsigned)ss.red[w]);
-  int shift = kmax > 0 ? ((31 - __clz(kmax)) / 8) * 8 : 0;
+  for (int w = 1; w < kPruneWarps; w++) {
+    mn = min(mn, ps.mn[w]);
+    mx = max(mx, ps.mx[w]);
+  }
+}
+
+// The K-th largest value T of vals[0, n) (0 < K < number of valid entries), by radix
+// selection on 8-bit digits of the keys rel_key(v, min), from the highest digit in which
+// they can differ. need_eq = K - #(values > T): how many of the entries equal to T are kept
+// (the lowest-index ones); eq_total = #(values == T).
+//
+// Each digit, two CTA barriers: the warps count the matching keys into the histograms (two
+// warps to one, loads batched ahead of the atomics); then threads 0..255 own one digit
+// each, sum it over the histograms (zeroing them for the next digit) and scan within their
+// warp by shuffles, publishing every digit's in-warp suffix count and each warp's total;
+// then every thread finds the digit holding the K-th key from those by itself. The
+// histograms are zero on entry and on return.
+__device__ void kth_largest(const int* vals, int n, int K, PruneShared& ps, int& T, int& need_eq,
+                            int& eq_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+  int vmin, vmax;
+  block_min_max(vals, n, ps, vmin, vmax);
+  const unsigned kmax = (unsigned)((long long)vmax - vmin) + 1u;
+  int shift = ((31 - __clz(kmax)) / 8) * 8;
   unsigned prefix = 0;  // decided high bits of T's key
   int above = 0;        // entries known to lie above T
+  unsigned* hist = ps.hist[warp >> 1];
   for (;;) {
-    unsigned* hist = ss.hist[warp];
-#pragma unroll
-    for (int q = 0; q < kDigitBins / 32; q++) hist[lane * (kDigitBins / 32) + q] = 0;
-    __syncwarp();
     const int hi_shift = shift + 8;
-    for (int i = threadIdx.x; i < n; i += kPruneThreads) {
-      const unsigned key = rel_key(vals[i], vmin);
-      const bool match = hi_shift >= 32 || (key >> hi_shift) == (prefix >> hi_shift);
-      if (match) atomicAdd(&hist[(key >> shift) & 0xFF], 1u);
+    for (int i0 = tid; i0 < n; i0 += 4 * kPruneThreads) {
+      unsigned key[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int i = i0 + u * kPruneThreads;
+        key[u] = i < n ? rel_key(vals[i], vmin) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const bool match = hi_shift >= 32 || (key[u] >> hi_shift) == (prefix >> hi_shift);
+        if (match && key[u] != 0u) atomicAdd(&hist[(key[u] >> shift) & 0xFF], 1u);
+      }
     }
     __syncthreads();
-    if (warp == 0) {
-      // lane owns digits [8 lane, 8 lane + 8); counts summed over the warps
-      unsigned c[8];
-      unsigned mine = 0;
+    if (tid < kDigitBins) {
+      int c = 0;
 #pragma unroll
-      for (int q = 0; q < 8; q++) {
-        unsigned t = 0;
-#pragma unroll
-        for (int w = 0; w < kPruneWarps; w++) t += ss.hist[w][lane * 8 + q];
-        c[q] = t;
-        mine += t;
+      for (int r = 0; r < kHistCopies; r++) {
+        c += ps.hist[r][tid];
+        ps.hist[r][tid] = 0;
       }
-      // entries in the digits of higher lanes
-      unsigned incl = mine;
+      // s = matching keys with this digit or a higher one, within this warp's 32 digits
+      int s = c;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        const unsigned y = __shfl_down_sync(0xffffffffu, incl, off);
-        if (lane + off < 32) incl += y;
+        const int y = __shfl_down_sync(0xffffffffu, s, off);
+        if (lane + off < 32) s += y;
       }
-      unsigned higher = above + (incl - mine);
-#pragma unroll
-      for (int q = 7; q >= 0; q--) {
-        if (higher < (unsigned)K && higher + c[q] >= (unsigned)K) {
-          ss.decided[0] = lane * 8 + q;
-          ss.decided[1] = (int)higher;
-        }
-        higher += c[q];
-      }
+      ps.sfx[tid] = s;
+      if (lane == 0) ps.tot[warp] = s;
     }
     __syncthreads();
-    prefix |= (unsigned)ss.decided[0] << shift;
-    above = ss.decided[1];
-    if (shift == 0) break;
+    // the digit group (32 digits) holding the K-th key, then the digit within it
+    int hi_groups = 0, g = kDigitBins / 32 - 1;
+    for (; g > 0; g--) {
+      if (above + hi_groups + ps.tot[g] >= K) break;
+      hi_groups += ps.tot[g];
+    }
+    const int base = above + hi_groups;
+    const int sl = base + ps.sfx[g * 32 + lane];  // keys at or above digit 32 g + lane
+    const unsigned ok = __ballot_sync(0xffffffffu, sl >= K);
+    const int dl = 31 - __clz(ok);  // the highest digit of the group whose suffix reaches K
+    const int d = g * 32 + dl;
+    const int in_digit = ps.sfx[d] - (dl < 31 ? ps.sfx[d + 1] : 0);
+    prefix |= (unsigned)d << shift;
+    above = base + ps.sfx[d] - in_digit;  // keys strictly above digit d
+    if (shift == 0) {
+      eq_total = in_digit;
+      break;
+    }
     shift -= 8;
   }
   T = (int)((long long)vmin + (long long)prefix - 1);
@@ -450,12 +533,54 @@ __device__ void kth_largest(const int* vals, int n, int K, SelectScratch& ss, in
 
 // Emits, in ascending index order, every i with vals[i] > T plus the first need_eq indices
 // with vals[i] == T, calling emit(position, i); returns how many. Warp w owns a contiguous
-// range, scanned 32 entries at a time with ballots (conflict-free, one CTA barrier).
+// range, read 4 x 32 entries at a time; positions come from ballots (one CTA barrier for
+// the per-warp counts). When all entries equal to T are kept (need_eq == eq_total), or none
+// are, the test is a plain threshold and no tie ranks are needed.
 template <typename Emit>
-__device__ int collect(const int* vals, int n, int T, int need_eq, SelectScratch& ss, Emit emit) {
+__device__ int collect(const int* vals, int n, int T, int need_eq, int eq_total, PruneShared& ps,
+                       Emit emit) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int per = ((n + kPruneWarps * 32 - 1) / (kPruneWarps * 32)) * 32;
   const int w0 = min(n, warp * per), w1 = min(n, w0 + per);
+  const unsigned lt = lanemask_lt();
+  const bool ties_split = need_eq > 0 && need_eq < eq_total;
+  // threshold form: keep v > t_lo (placeholders INT_MIN are never kept: t_lo >= INT_MIN)
+  const int t_lo = (need_eq > 0 && !ties_split) ? T - 1 : T;
+  if (!ties_split) {
+    int cnt = 0;
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int i = i0 + 32 * u + lane;
+        cnt += (i < w1 && vals[i] > t_lo) ? 1 : 0;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    if (lane == 0) ps.w_a[warp] = cnt;
+    __syncthreads();
+    int pos = 0, total = 0;
+    for (int w = 0; w < kPruneWarps; w++) {
+      if (w == warp) pos = total;
+      total += ps.w_a[w];
+    }
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+      bool take[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int i = i0 + 32 * u + lane;
+        take[u] = i < w1 && vals[i] > t_lo;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const unsigned tm = __ballot_sync(0xffffffffu, take[u]);
+        if (take[u]) emit(pos + __popc(tm & lt), i0 + 32 * u + lane);
+        pos += __popc(tm);
+      }
+    }
+    __syncthreads();
+    return total;
+  }
   int n_gt = 0, n_eq = 0;
   for (int i = w0 + lane; i < w1; i += 32) {
     n_gt += vals[i] > T;
@@ -467,22 +592,21 @@ __device__ int collect(const int* vals, int n, int T, int need_eq, SelectScratch
     n_eq += __shfl_xor_sync(0xffffffffu, n_eq, off);
   }
   if (lane == 0) {
-    ss.w_a[warp] = n_gt;
-    ss.w_b[warp] = n_eq;
+    ps.w_a[warp] = n_gt;
+    ps.w_b[warp] = n_eq;
   }
   __syncthreads();
   // per warp: entries kept = all above T plus the ties still allowed after the earlier warps
   int eq_acc = 0, pos = 0, total = 0, eq_base = 0;
   for (int w = 0; w < kPruneWarps; w++) {
-    const int kept_w = ss.w_a[w] + min(max(need_eq - eq_acc, 0), ss.w_b[w]);
+    const int kept_w = ps.w_a[w] + min(max(need_eq - eq_acc, 0), ps.w_b[w]);
     if (w == warp) {
       pos = total;
       eq_base = eq_acc;
     }
     total += kept_w;
-    eq_acc += ss.w_b[w];
+    eq_acc += ps.w_b[w];
   }
-  const unsigned lt = lanemask_lt();
   for (int i0 = w0; i0 < w1; i0 += 32) {
     const int i = i0 + lane;
     const int v = i < w1 ? vals[i] : INT_MIN;
@@ -498,42 +622,41 @@ __device__ int collect(const int* vals, int n, int T, int need_eq, SelectScratch
   return total;
 }
 
-template <int UNROLL>
-__device__ __forceinline__ void gather_strided(int* dst, const int32_t* __restrict__ src, int n) {
-  for (int i0 = threadIdx.x; i0 < n; i0 += UNROLL * kPruneThreads) {
-    int v[UNROLL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; u++) {
-      const int i = i0 + u * kPruneThreads;
-      v[u] = i < n ? __ldg(src + i) : 0;
-    }
-#pragma unroll
-    for (int u = 0; u < UNROLL; u++) {
-      const int i = i0 + u * kPruneThreads;
-      if (i < n) dst[i] = v[u];
-    }
-  }
-}
-
 // At most 40 registers a thread (three 512-thread CTAs' worth per SM): a prune CTA and a
 // CTA of the sparse attend, which is launched while the prune runs, then fit on one SM
 // together, and no attend CTA has to wait for the prune to leave its SM.
+//
+// Shared memory: PruneShared, vals [vals_cap + 4], cand [cand_cap] (module 2's block ids),
+// cand_page [cand_cap] (with
+// sel_pages), kept [kept_cap], row [row_cap + 4] (the sequence's block maxima, staged whole
+// when they fit), prow [prow_cap + 4] (its page ids, with sel_pages).
 __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_kernel(const PruneArgs a) {
-  extern __shared__ __align__(16) int psmem[];
-  SelectScratch& ss = *reinterpret_cast<SelectScratch*>(psmem);
-  int* vals = psmem + sizeof(SelectScratch) / sizeof(int);  // vals_cap
-  int* cand = vals + a.vals_cap;                            // cand_cap block ids of module 2
-  int* kept_chunks = cand + a.cand_cap;                     // k1
-  int* cand_page = kept_chunks + a.k1;                      // cand_cap pages (with sel_pages)
+  extern __shared__ __align__(16) unsigned char psmem_raw[];
+  PruneShared& ps = *reinterpret_cast<PruneShared*>(psmem_raw);
+  int* arr = reinterpret_cast<int*>(psmem_raw + ((sizeof(PruneShared) + 15) / 16) * 16);
+  int* vals_base = arr;                              // vals_cap + 4
+  int* cand = vals_base + a.vals_cap + 4;            // cand_cap
+  int* cand_page = cand + a.cand_cap;                // cand_cap
+  int* kept_chunks = cand_page + a.cand_cap;         // kept_cap
+  int* row_base = kept_chunks + a.kept_cap;          // row_cap + 4 (16-byte aligned)
+  int* prow_base = row_base + (a.row_cap > 0 ? a.row_cap + 4 : 0);  // prow_cap + 4
 
   const int h = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(&ps.bar, 1);
+    fence_barrier_init();
+  }
+  for (int i = tid; i < kHistCopies * kDigitBins; i += kPruneThreads) (&ps.hist[0][0])[i] = 0u;
+  // the sequence length is an input of the step, not written by the previous kernel: it is
+  // read before the wait
+  const int n = a.seq_lens[b];
   grid_dep_wait();  // the scores come from the previous kernel
   grid_dep_launch();
-  const int n = a.seq_lens[b];
   const int P = a.chunk_blocks;
   int lo = a.sink, hi = n - a.window;
   if (n < 0 || n > a.max_pages * kPage) {
-    if (threadIdx.x == 0) set_error(a.err, kDevErrCheck);
+    if (tid == 0) set_error(a.err, kDevErrCheck);
     hi = lo;
   }
   int k_lo = 0, k_hi = 0, c_lo = 0, n1 = 0;
@@ -545,50 +668,78 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
   }
   const int32_t* bm = a.block_max + ((size_t)b * a.hkv + h) * a.max_pages;
   const size_t bh = (size_t)b * a.hkv + h;
+  __syncthreads();  // the barrier's initialisation is visible
 
-  // ---- module 1: chunk scores, top-K1
-  if (a.tile_max != nullptr && P == 4) {
-    gather_strided<8>(vals, a.tile_max + bh * a.max_tiles + c_lo, n1);
-  } else {
-    for (int i = threadIdx.x; i < n1; i += kPruneThreads) vals[i] = INT_MIN;
+  // ---- stage the scores, all copies in one round trip: the 64-token tile maxima when the
+  // scorer wrote them (chunk c of 64 tokens == tile c), the whole row of block maxima and of
+  // page ids when they fit; whatever is not staged is gathered from global memory
+  const bool use_tiles = a.tile_max != nullptr && P == 4;
+  const bool use_row = a.row_cap > 0;
+  const bool use_prow = a.prow_cap > 0 && a.sel_pages != nullptr;
+  const int32_t* t_src = a.tile_max + bh * a.max_tiles + c_lo;
+  const int32_t* p_src = a.page_table + (size_t)b * a.max_pages + k_lo;
+  uint32_t bytes = 0;  // every bulk copy's bytes, announced before the first one is issued
+  if (use_tiles) bytes += plan_row(vals_base, t_src, n1).bytes();
+  if (use_row) bytes += plan_row(row_base, bm + k_lo, k_hi - k_lo).bytes();
+  if (use_prow) bytes += plan_row(prow_base, p_src, k_hi - k_lo).bytes();
+  if (tid == 0 && bytes > 0) mbar_arrive_expect_tx(&ps.bar, bytes);
+  int* vals = use_tiles ? stage(plan_row(vals_base, t_src, n1), &ps.bar) : vals_base;
+  const int* row =  // row[k - k_lo] = block maximum of block k
+      use_row ? stage(plan_row(row_base, bm + k_lo, k_hi - k_lo), &ps.bar) : nullptr;
+  const int* prow_s =  // prow_s[k - k_lo] = page of block k
+      use_prow ? stage(plan_row(prow_base, p_src, k_hi - k_lo), &ps.bar) : nullptr;
+  if (bytes > 0 && !mbar_wait(&ps.bar, 0)) set_error(a.err, kDevErrTimeout);
+  __syncthreads();
+  if (!use_tiles && use_row) {
+    for (int c = tid; c < n1; c += kPruneThreads) {
+      const int k0 = max((c_lo + c) * P, k_lo), k1 = min((c_lo + c) * P + P, k_hi);
+      int m = INT_MIN;
+      for (int k = k0; k < k1; k++) m = max(m, row[k - k_lo]);
+      vals[c] = m;
+    }
+    __syncthreads();
+  } else if (!use_tiles) {
+    for (int i = tid; i < n1; i += kPruneThreads) vals[i] = INT_MIN;
     __syncthreads();
     // every candidate block once (independent, coalesced loads); max into its chunk
 #pragma unroll 4
-    for (int k = k_lo + threadIdx.x; k < k_hi; k += kPruneThreads)
+    for (int k = k_lo + tid; k < k_hi; k += kPruneThreads)
       atomicMax(&vals[k / P - c_lo], __ldg(bm + k));
+    __syncthreads();
   }
-  __syncthreads();
+
+  // ---- module 1: top-K1 chunks
   const int keep1 = min(a.k1, n1);
-  int T = INT_MIN, need_eq = 0;
-  if (keep1 < n1 && keep1 > 0) kth_largest(vals, n1, keep1, ss, T, need_eq);
+  int T = INT_MIN, need_eq = 0, eq_total = 0;
+  if (keep1 < n1 && keep1 > 0) kth_largest(vals, n1, keep1, ps, T, need_eq, eq_total);
   int got1 = 0;
   if (keep1 > 0) {
-    got1 = collect(vals, n1, T, need_eq, ss, [&](int pos, int i) {
+    got1 = collect(vals, n1, T, need_eq, eq_total, ps, [&](int pos, int i) {
       kept_chunks[pos] = c_lo + i;
       if (a.chunk_idx) a.chunk_idx[bh * a.k1 + pos] = c_lo + i;
     });
   }
   if (a.chunk_idx)
-    for (int i = got1 + threadIdx.x; i < a.k1; i += kPruneThreads) a.chunk_idx[bh * a.k1 + i] = -1;
-  if (a.n_chunks && threadIdx.x == 0) a.n_chunks[bh] = got1;
+    for (int i = got1 + tid; i < a.k1; i += kPruneThreads) a.chunk_idx[bh * a.k1 + i] = -1;
+  if (a.n_chunks && tid == 0) a.n_chunks[bh] = got1;
   __syncthreads();
 
   // ---- module 2: the kept chunks' blocks (P per chunk, ascending; blocks outside the
-  // candidate region are INT_MIN placeholders that are never kept), top-K2
+  // candidate region are INT_MIN placeholders that are never kept), top-K2. With sel_pages,
+  // each candidate's page id is loaded beside its block maximum, so the next kernel reads
+  // the pages of the kept blocks directly.
   const int n2 = got1 * P;
-  // with sel_pages, each candidate's page id is loaded beside its block maximum (same round
-  // trip), so the next kernel reads the pages of the kept blocks directly
   const int32_t* prow = a.sel_pages ? a.page_table + (size_t)b * a.max_pages : nullptr;
   int valid_local = 0;
-  for (int x0 = threadIdx.x; x0 < n2; x0 += 4 * kPruneThreads) {
+  for (int x0 = tid; x0 < n2; x0 += 4 * kPruneThreads) {
     int v[4], kk[4], pg[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) {
       const int x = x0 + u * kPruneThreads;
       kk[u] = x < n2 ? kept_chunks[x / P] * P + x % P : -1;
       const bool in = kk[u] >= k_lo && kk[u] < k_hi;
-      v[u] = in ? __ldg(bm + kk[u]) : INT_MIN;
-      pg[u] = (in && prow) ? __ldg(prow + kk[u]) : -1;
+      v[u] = in ? (use_row ? row[kk[u] - k_lo] : __ldg(bm + kk[u])) : INT_MIN;
+      pg[u] = (in && prow) ? (prow_s ? prow_s[kk[u] - k_lo] : __ldg(prow + kk[u])) : -1;
     }
 #pragma unroll
     for (int u = 0; u < 4; u++) {
@@ -601,38 +752,54 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
       }
     }
   }
+  const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) valid_local += __shfl_xor_sync(0xffffffffu, valid_local, off);
-  if ((threadIdx.x & 31) == 0) ss.red[threadIdx.x >> 5] = valid_local;
+  if (lane == 0) ps.tot[warp] = valid_local;
   __syncthreads();
   int n2_valid = 0;
 #pragma unroll
-  for (int w = 0; w < kPruneWarps; w++) n2_valid += ss.red[w];
+  for (int w = 0; w < kPruneWarps; w++) n2_valid += ps.tot[w];
   __syncthreads();
   const int keep2 = min(a.k2, n2_valid);
   T = INT_MIN;
   need_eq = 0;
-  if (keep2 < n2_valid && keep2 > 0) kth_largest(vals, n2, keep2, ss, T, need_eq);
+  eq_total = 0;
+  if (keep2 < n2_valid && keep2 > 0) kth_largest(vals, n2, keep2, ps, T, need_eq, eq_total);
   int got2 = 0;
   if (keep2 > 0) {
-    got2 = collect(vals, n2, T, need_eq, ss, [&](int pos, int i) {
+    got2 = collect(vals, n2, T, need_eq, eq_total, ps, [&](int pos, int i) {
       a.block_idx[bh * a.k2 + pos] = cand[i];
       if (prow) a.sel_pages[bh * a.k2 + pos] = cand_page[i];
     });
   }
-  for (int i = got2 + threadIdx.x; i < a.k2; i += kPruneThreads) a.block_idx[bh * a.k2 + i] = -1;
-  if (threadIdx.x == 0) a.n_blocks[bh] = got2;
+  for (int i = got2 + tid; i < a.k2; i += kPruneThreads) a.block_idx[bh * a.k2 + i] = -1;
+  if (tid == 0) a.n_blocks[bh] = got2;
 }
 
-int prune_caps(const Shape& s, int& vals_cap, int& cand_cap) {
+// stage_pages: also stage the page-table row (only with sel_pages and a 16-byte-aligned page
+// table).
+int prune_caps(const Shape& s, PruneArgs& a, bool stage_pages) {
   const int P = s.chunk / kPage;
   const long long n1max = ((long long)s.max_pages + P - 1) / P;
   const long long keep1 = std::min<long long>(s.k1, n1max);
   const long long n2max = keep1 * P;
   if (n1max > kMaxChunks) return -1;
-  vals_cap = (int)std::max(n1max, n2max);
-  cand_cap = (int)n2max;
+  // every array a multiple of 4 ints, so that each one starts 16-byte aligned
+  auto up4 = [](long long x) { return (int)((x + 3) / 4 * 4); };
+  a.vals_cap = up4(std::max(n1max, n2max));
+  a.cand_cap = up4(n2max);
+  a.kept_cap = up4(std::max<long long>(keep1, 1));
+  a.row_cap = s.max_pages <= kRowCap ? up4(s.max_pages) : 0;
+  a.prow_cap = stage_pages ? a.row_cap : 0;
   return 0;
+}
+
+size_t prune_smem(const PruneArgs& a) {
+  return ((sizeof(PruneShared) + 15) / 16) * 16 +
+         sizeof(int) * ((size_t)a.vals_cap + 4 + 2 * (size_t)a.cand_cap + a.kept_cap +
+                        (a.row_cap > 0 ? a.row_cap + 4 : 0) +
+                        (a.prow_cap > 0 ? a.prow_cap + 4 : 0));
 }
 
 }  // namespace
@@ -640,9 +807,9 @@ int prune_caps(const Shape& s, int& vals_cap, int& cand_cap) {
 int prune_max_chunks() { return kMaxChunks; }
 
 size_t prune_smem_bytes(const Shape& s) {
-  int vals_cap, cand_cap;
-  if (prune_caps(s, vals_cap, cand_cap) != 0) return ~size_t(0);
-  return sizeof(SelectScratch) + sizeof(int) * ((size_t)vals_cap + 2 * (size_t)cand_cap + s.k1);
+  PruneArgs a;
+  if (prune_caps(s, a, true) != 0) return ~size_t(0);
+  return prune_smem(a);
 }
 
 int score_max_tiles(const Shape& s) { return (s.max_pages + kTileBlocks - 1) / kTileBlocks; }
@@ -707,9 +874,15 @@ cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t*
                          int32_t* sel_pages, int* err, cudaStream_t st) {
   if (sel_pages != nullptr && page_table == nullptr) return cudaErrorInvalidValue;
   PruneArgs a;
-  if (prune_caps(s, a.vals_cap, a.cand_cap) != 0) return cudaErrorInvalidValue;
-  const size_t smem = prune_smem_bytes(s);
+  const bool stage_pages =
+      sel_pages != nullptr && (reinterpret_cast<uintptr_t>(page_table) & 15) == 0;
+  if (prune_caps(s, a, stage_pages) != 0) return cudaErrorInvalidValue;
+  const size_t smem = prune_smem(a);
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
+  // the staging copies start from the 16-byte boundary at or below a row's first entry
+  if ((reinterpret_cast<uintptr_t>(block_max) & 15) != 0 ||
+      (reinterpret_cast<uintptr_t>(tile_max) & 15) != 0)
+    return cudaErrorInvalidValue;
   a.seq_lens = seq_lens;
   a.block_max = block_max;
   a.tile_max = tile_max;

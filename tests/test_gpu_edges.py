@@ -273,3 +273,73 @@ def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2, on_host):
                                  sel["n_blocks"])
     H.assert_close(out1.cpu().numpy(), out_o, "whole-step output")
     np.testing.assert_allclose(lse1.cpu().numpy(), lse_o, atol=2e-4, rtol=1e-5)
+
+
+def _prune_reference(row, n, chunk, k1, k2, sink, window):
+    """Both modules by their definition on one row of block maxima: chunk score = max of its
+    candidate blocks' maxima; keep the top K1 chunks, then the top K2 of their candidate
+    blocks, by (score descending, index ascending); both lists returned ascending."""
+    P = chunk // 16
+    lo, hi = sink, n - window
+    if hi <= lo:
+        return [], []
+    k_lo, k_hi = lo // 16, (hi + 15) // 16
+    c_lo = k_lo // P
+    c_hi = (k_hi + P - 1) // P
+    score = {c: max(int(row[k]) for k in range(max(c * P, k_lo), min(c * P + P, k_hi)))
+             for c in range(c_lo, c_hi)}
+    kept = sorted(sorted(score, key=lambda c: (-score[c], c))[:k1])
+    blocks = [k for c in kept for k in range(c * P, c * P + P) if k_lo <= k < k_hi]
+    return kept, sorted(sorted(blocks, key=lambda k: (-int(row[k]), k))[:k2])
+
+
+@pytest.mark.parametrize("max_pages,chunk,with_tiles", [
+    (16384, 64, True), (16384, 128, False), (40000, 64, True), (40000, 64, False),
+    (40000, 32, True)])
+@pytest.mark.parametrize("dist", ["spread", "ties", "const", "wide"])
+def test_prune_on_synthetic_maxima(max_pages, chunk, with_tiles, dist):
+    """hsa_prune alone on seeded block maxima: the whole row staged in shared memory (up to
+    16384 blocks) or the 64-token tile maxima or a gather from global memory; large chunk
+    counts (the threshold digit's keys compacted); many ties at the threshold. Entries
+    outside the candidate region hold values that would win if they were read."""
+    B, Hkv, sink, window = 2, 2, 128, 2048
+    gen = np.random.default_rng(max_pages + chunk + len(dist) + int(with_tiles))
+    lens = [max_pages * 16, max_pages * 16 - 12345]
+    if dist == "spread":
+        bm = gen.integers(-2_000_000, 2_000_000, size=(B, Hkv, max_pages))
+    elif dist == "ties":
+        levels = gen.integers(-1_000_000, 1_000_000, size=200)
+        bm = levels[gen.integers(0, 200, size=(B, Hkv, max_pages))]
+    elif dist == "wide":  # nearly the whole int32 range (INT_MIN is the placeholder)
+        bm = gen.integers(-(2 ** 31) + 1, 2 ** 31, size=(B, Hkv, max_pages))
+    else:
+        bm = np.full((B, Hkv, max_pages), 777)
+    bm = bm.astype(np.int32)
+    n_tiles = (max_pages + 3) // 4
+    tm = np.full((B, Hkv, n_tiles), 2_000_000_000, dtype=np.int32)
+    for b, n in enumerate(lens):
+        k_lo, k_hi = sink // 16, (n - window + 15) // 16
+        bm[b, :, :k_lo] = 2_000_000_000            # never a candidate
+        bm[b, :, k_hi:] = 2_000_000_000
+        for t in range(k_lo // 4, (k_hi + 3) // 4):
+            tm[b, :, t] = bm[b, :, max(4 * t, k_lo):min(4 * t + 4, k_hi)].max(axis=-1)
+    k1, k2 = 512, 256
+    d = hsa.Dims(batch=B, hq=Hkv * 4, hkv=Hkv, max_pages_per_seq=max_pages, num_pages=B * max_pages,
+                 chunk=chunk, k1=k1, k2=k2, sink=sink, window=window)
+    dev = torch.device("cuda")
+    bm_d = torch.from_numpy(bm).to(dev)
+    tm_d = torch.from_numpy(tm).to(dev) if with_tiles else None
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+    ci = torch.full((B, Hkv, k1), -7, dtype=torch.int32, device=dev)
+    nc = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+    bi = torch.full((B, Hkv, k2), -7, dtype=torch.int32, device=dev)
+    nb = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+    hsa.hsa_prune(d, lens_d, bm_d, tm_d, ci, nc, bi, nb)
+    torch.cuda.synchronize()
+    ci, nc, bi, nb = (x.cpu().numpy() for x in (ci, nc, bi, nb))
+    for b, n in enumerate(lens):
+        for h in range(Hkv):
+            chunks, blocks = _prune_reference(bm[b, h], n, chunk, k1, k2, sink, window)
+            assert nc[b, h] == len(chunks) and nb[b, h] == len(blocks)
+            np.testing.assert_array_equal(ci[b, h], chunks + [-1] * (k1 - len(chunks)))
+            np.testing.assert_array_equal(bi[b, h], blocks + [-1] * (k2 - len(blocks)))
