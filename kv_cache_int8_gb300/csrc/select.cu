@@ -355,7 +355,7 @@ struct PruneShared {
   int tot[kPruneWarps];                    // per-group / per-warp totals
   int mn[kPruneWarps], mx[kPruneWarps];    // per-warp min / max of the valid values
   int w_a[kPruneWarps], w_b[kPruneWarps];  // per-warp counts of the collect
-  uint64_t bar;                            // completion of the staging copies
+  uint64_t bar[2];                         // staging copies: [0] module 1's, [1] the rest
 };
 
 __device__ __forceinline__ unsigned lanemask_lt() {
@@ -454,7 +454,8 @@ __device__ __forceinline__ void block_min_max(const int* vals, int n, PruneShare
 // The K-th largest value T of vals[0, n) (0 < K < number of valid entries), by radix
 // selection on 8-bit digits of the keys rel_key(v, min), from the highest digit in which
 // they can differ. need_eq = K - #(values > T): how many of the entries equal to T are kept
-// (the lowest-index ones); eq_total = #(values == T).
+// (the lowest-index ones); eq_total = #(values == T). The valid values' min and max are
+// computed here unless the caller has them (have_range).
 //
 // Each digit, two CTA barriers: the warps count the matching keys into the histograms (two
 // warps to one, loads batched ahead of the atomics); then threads 0..255 own one digit
@@ -463,10 +464,9 @@ __device__ __forceinline__ void block_min_max(const int* vals, int n, PruneShare
 // then every thread finds the digit holding the K-th key from those by itself. The
 // histograms are zero on entry and on return.
 __device__ void kth_largest(const int* vals, int n, int K, PruneShared& ps, int& T, int& need_eq,
-                            int& eq_total) {
+                            int& eq_total, bool have_range = false, int vmin = 0, int vmax = 0) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
-  int vmin, vmax;
-  block_min_max(vals, n, ps, vmin, vmax);
+  if (!have_range) block_min_max(vals, n, ps, vmin, vmax);
   const unsigned kmax = (unsigned)((long long)vmax - vmin) + 1u;
   int shift = ((31 - __clz(kmax)) / 8) * 8;
   unsigned prefix = 0;  // decided high bits of T's key
@@ -644,7 +644,8 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x;
   if (tid == 0) {
-    mbar_init(&ps.bar, 1);
+    mbar_init(&ps.bar[0], 1);
+    mbar_init(&ps.bar[1], 1);
     fence_barrier_init();
   }
   for (int i = tid; i < kHistCopies * kDigitBins; i += kPruneThreads) (&ps.hist[0][0])[i] = 0u;
@@ -670,26 +671,33 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
   const size_t bh = (size_t)b * a.hkv + h;
   __syncthreads();  // the barrier's initialisation is visible
 
-  // ---- stage the scores, all copies in one round trip: the 64-token tile maxima when the
-  // scorer wrote them (chunk c of 64 tokens == tile c), the whole row of block maxima and of
-  // page ids when they fit; whatever is not staged is gathered from global memory
+  // ---- stage the scores: the 64-token tile maxima when the scorer wrote them (chunk c of 64
+  // tokens == tile c) on barrier 0, the whole row of block maxima and of page ids when they
+  // fit on barrier 1 (module 2 needs them only later); whatever is not staged is gathered
+  // from global memory
   const bool use_tiles = a.tile_max != nullptr && P == 4;
   const bool use_row = a.row_cap > 0;
   const bool use_prow = a.prow_cap > 0 && a.sel_pages != nullptr;
   const int32_t* t_src = a.tile_max + bh * a.max_tiles + c_lo;
   const int32_t* p_src = a.page_table + (size_t)b * a.max_pages + k_lo;
-  uint32_t bytes = 0;  // every bulk copy's bytes, announced before the first one is issued
-  if (use_tiles) bytes += plan_row(vals_base, t_src, n1).bytes();
-  if (use_row) bytes += plan_row(row_base, bm + k_lo, k_hi - k_lo).bytes();
-  if (use_prow) bytes += plan_row(prow_base, p_src, k_hi - k_lo).bytes();
-  if (tid == 0 && bytes > 0) mbar_arrive_expect_tx(&ps.bar, bytes);
-  int* vals = use_tiles ? stage(plan_row(vals_base, t_src, n1), &ps.bar) : vals_base;
+  // each barrier's bytes are announced before its first copy is issued
+  const uint32_t bytes0 = use_tiles ? plan_row(vals_base, t_src, n1).bytes() : 0u;
+  const uint32_t bytes1 = (use_row ? plan_row(row_base, bm + k_lo, k_hi - k_lo).bytes() : 0u) +
+                          (use_prow ? plan_row(prow_base, p_src, k_hi - k_lo).bytes() : 0u);
+  if (tid == 0 && bytes0 > 0) mbar_arrive_expect_tx(&ps.bar[0], bytes0);
+  if (tid == 0 && bytes1 > 0) mbar_arrive_expect_tx(&ps.bar[1], bytes1);
+  int* vals = use_tiles ? stage(plan_row(vals_base, t_src, n1), &ps.bar[0]) : vals_base;
   const int* row =  // row[k - k_lo] = block maximum of block k
-      use_row ? stage(plan_row(row_base, bm + k_lo, k_hi - k_lo), &ps.bar) : nullptr;
+      use_row ? stage(plan_row(row_base, bm + k_lo, k_hi - k_lo), &ps.bar[1]) : nullptr;
   const int* prow_s =  // prow_s[k - k_lo] = page of block k
-      use_prow ? stage(plan_row(prow_base, p_src, k_hi - k_lo), &ps.bar) : nullptr;
-  if (bytes > 0 && !mbar_wait(&ps.bar, 0)) set_error(a.err, kDevErrTimeout);
-  __syncthreads();
+      use_prow ? stage(plan_row(prow_base, p_src, k_hi - k_lo), &ps.bar[1]) : nullptr;
+  // module 1 reads the tiles, or the block row when it reduces chunks itself
+  const bool need1_now = !use_tiles && use_row;
+  bool ok1 = true;
+  if (bytes0 > 0 && !mbar_wait(&ps.bar[0], 0)) ok1 = false;
+  if (need1_now && bytes1 > 0 && !mbar_wait(&ps.bar[1], 0)) ok1 = false;
+  if (!ok1) set_error(a.err, kDevErrTimeout);
+  __syncthreads();  // the plain-load tails are visible
   if (!use_tiles && use_row) {
     for (int c = tid; c < n1; c += kPruneThreads) {
       const int k0 = max((c_lo + c) * P, k_lo), k1 = min((c_lo + c) * P + P, k_hi);
@@ -730,7 +738,8 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
   // the pages of the kept blocks directly.
   const int n2 = got1 * P;
   const int32_t* prow = a.sel_pages ? a.page_table + (size_t)b * a.max_pages : nullptr;
-  int valid_local = 0;
+  if (!need1_now && bytes1 > 0 && !mbar_wait(&ps.bar[1], 0)) set_error(a.err, kDevErrTimeout);
+  int valid_local = 0, mn2 = INT_MAX, mx2 = INT_MIN;
   for (int x0 = tid; x0 < n2; x0 += 4 * kPruneThreads) {
     int v[4], kk[4], pg[4];
 #pragma unroll
@@ -748,24 +757,41 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
         cand[x] = kk[u];
         vals[x] = v[u];
         if (prow) cand_page[x] = pg[u];
-        valid_local += v[u] != INT_MIN;
+        if (v[u] != INT_MIN) {
+          valid_local++;
+          mn2 = min(mn2, v[u]);
+          mx2 = max(mx2, v[u]);
+        }
       }
     }
   }
   const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) valid_local += __shfl_xor_sync(0xffffffffu, valid_local, off);
-  if (lane == 0) ps.tot[warp] = valid_local;
+  for (int off = 16; off > 0; off >>= 1) {
+    valid_local += __shfl_xor_sync(0xffffffffu, valid_local, off);
+    mn2 = min(mn2, __shfl_xor_sync(0xffffffffu, mn2, off));
+    mx2 = max(mx2, __shfl_xor_sync(0xffffffffu, mx2, off));
+  }
+  if (lane == 0) {
+    ps.tot[warp] = valid_local;
+    ps.mn[warp] = mn2;
+    ps.mx[warp] = mx2;
+  }
   __syncthreads();
   int n2_valid = 0;
 #pragma unroll
-  for (int w = 0; w < kPruneWarps; w++) n2_valid += ps.tot[w];
+  for (int w = 0; w < kPruneWarps; w++) {
+    n2_valid += ps.tot[w];
+    mn2 = min(mn2, ps.mn[w]);
+    mx2 = max(mx2, ps.mx[w]);
+  }
   __syncthreads();
   const int keep2 = min(a.k2, n2_valid);
   T = INT_MIN;
   need_eq = 0;
   eq_total = 0;
-  if (keep2 < n2_valid && keep2 > 0) kth_largest(vals, n2, keep2, ps, T, need_eq, eq_total);
+  if (keep2 < n2_valid && keep2 > 0)
+    kth_largest(vals, n2, keep2, ps, T, need_eq, eq_total, true, mn2, mx2);
   int got2 = 0;
   if (keep2 > 0) {
     got2 = collect(vals, n2, T, need_eq, eq_total, ps, [&](int pos, int i) {
