@@ -8,9 +8,10 @@ Prints ONE JSON line (rank 0). Timing: the whole step (hsa_decode_step on device
 is captured once in a CUDA graph per cache replica; the timed loop replays it K times with
 CUDA events around each replay on the launching stream. Two replicas of the whole cache
 alternate, so each step reads data the previous step did not touch (146 MB per step at
-128K tokens, more than the 129 MB L2). A second loop replays the four kernels of the step
-one graph each, for the per-kernel breakdown and the scorer's roofline. `--impl reference`
-times the CPU oracle on the host cores instead.
+128K tokens, more than the 129 MB L2). For the per-kernel breakdown and the scorer's
+roofline, each kernel is captured 10 times back to back in one graph (replicas alternating)
+and the graph's event time is divided by 10. `--impl reference` times the CPU oracle on the
+host cores instead.
 """
 from __future__ import annotations
 
@@ -162,6 +163,7 @@ class Case:
     buffers, and the captured graphs."""
 
     KERNELS = ("step", "append", "score", "prune", "attend", "dense")
+    BURST = 10
 
     def __init__(self, name: str, seed: int, device, dense: bool = True):
         import torch
@@ -272,6 +274,18 @@ class Case:
                 with torch.cuda.graph(g):
                     getattr(self, name)(r)
                 self.graphs[(name, r)] = g
+        # per-kernel durations: BURST launches of one kernel in one graph, replicas
+        # alternating (so that every launch of the scan reads data the previous one did not)
+        self.burst = {}
+        if self.flush is None:
+            for name in self.kernels:
+                if name == "step":
+                    continue
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(self.BURST):
+                        getattr(self, name)(i & 1)
+                self.burst[name] = g
         torch.cuda.synchronize()
 
     # ---- algorithmic bytes (what the method must move; see the design notes)
@@ -342,6 +356,33 @@ def timed_steps(case, steps: int, names, sampler=None):
     return per, step
 
 
+def burst_times(case, names, reps: int):
+    """Average duration of one launch of each kernel: `reps` replays of its burst graph
+    (BURST launches back to back) with CUDA events around each replay, after 3 warm-up
+    replays; falls back to one-launch graphs (timed_steps) when there are no bursts."""
+    torch = case.torch
+    if not case.burst:
+        timed_steps(case, 3, names)
+        per, _ = timed_steps(case, reps, names)
+        return per
+    out = {}
+    for name in names:
+        g = case.burst[name]
+        for _ in range(3):
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(2_000_000)
+        for a, b in evs:
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        out[name] = statistics.fmean(a.elapsed_time(b) for a, b in evs) / case.BURST
+    return out
+
+
 def e2e_steps(case, steps: int):
     """The public whole-step call with pinned host inputs/outputs, synchronised per step."""
     torch, hsa = case.torch, case.hsa
@@ -379,13 +420,11 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
     barrier(world)
     _, step_ms = timed_steps(case, steps, ("step",), sampler)
     barrier(world)
-    # kernel breakdown: the same four kernels replayed one graph each
-    bsteps = max(3, min(steps, 2000))
-    timed_steps(case, max(3, warmup), names)
-    per, split_ms = timed_steps(case, bsteps, names)
+    # kernel breakdown: the average launch duration of each of the four kernels
+    bsteps = max(3, min(steps // 10, 200))
+    per = burst_times(case, names, bsteps)
     if dense:
-        timed_steps(case, max(3, warmup), ("dense",))
-        dper, _ = timed_steps(case, bsteps, ("dense",))
+        dper = burst_times(case, ("dense",), max(3, bsteps // 4))
     else:
         dper = {"dense": float("nan")}
     for w in (case.ws_step, case.ws_sel, case.ws_att, case.ws_den):
@@ -398,7 +437,6 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
     res = {
         "case": case,
         "step_ms": step_ms,
-        "split_step_ms": split_ms,
         "per_ms": per,
         "select_ms": sel_ms,
         "dense_ms": dper["dense"],
@@ -483,6 +521,26 @@ def run_reference(args, world, rank):
     return 0
 
 
+def profile_steps(name, device, steps, warmup):
+    """Direct launches of the whole step (and of dense decode) for a profiler's launch list:
+    `warmup` steps, then `steps` steps and steps // 2 dense decodes, replicas alternating."""
+    import torch
+    case = Case(name, 0, device)
+    for i in range(warmup):
+        case.step(i & 1)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        case.step(i & 1)
+    for i in range(steps // 2):
+        case.dense(i & 1)
+    torch.cuda.synchronize()
+    for w in (case.ws_step, case.ws_den):
+        code = case.hsa.hsa_read_device_error(w)
+        assert code == 0, f"device error word {code}"
+    print(f"profiled {steps} steps and {steps // 2} dense decodes of {name}")
+    return 0
+
+
 def workload_text(cfg):
     return (f"{cfg.name}: batch {cfg.batch}, Hq {cfg.hq}, Hkv {cfg.hkv}, d 128, context "
             f"{cfg.context}, chunk {cfg.chunk} keep K1 {cfg.k1}, block 16 keep K2 {cfg.k2}, "
@@ -500,6 +558,9 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 1M-token extra case")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="for profilers: run this many whole steps with direct launches (no "
+                         "CUDA graphs), then half as many dense decodes, and exit")
     args = ap.parse_args()
     world, rank, local = dist_env()
 
@@ -519,6 +580,9 @@ def main():
     device = torch.device("cuda", torch.cuda.current_device())
     peak, peak_kind = peaks()
     sampler = ClockSampler(local) if rank == 0 else None
+
+    if args.profile_steps > 0:
+        return profile_steps(args.config, device, args.profile_steps, args.warmup)
 
     main_res = gpu_case_numbers(args.config, rank, device, args.steps, args.warmup, sampler, peak,
                                 world)
@@ -555,7 +619,7 @@ def main():
         del r["case"]
         torch.cuda.empty_cache()
         extra[EXTRA_CONFIG] = {
-            "us_per_step": r["step_ms"] * 1e3, "split_step_us": r["split_step_ms"] * 1e3,
+            "us_per_step": r["step_ms"] * 1e3,
             "select_us": r["select_ms"] * 1e3, "score_us": r["per_ms"]["score"] * 1e3,
             "prune_us": r["per_ms"]["prune"] * 1e3, "attend_us": r["per_ms"]["attend"] * 1e3,
             "dense_us": r["dense_ms"] * 1e3,
@@ -574,7 +638,7 @@ def main():
         cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc}
 
     per = main_res["per_ms"]
-    traffic = traffic_record("select.cu", "score_blocks_llama3-8b-128k.md")
+    traffic = traffic_record("score.cu", "score_blocks_llama3-8b-128k.md")
     cfg = W.CONFIGS[args.config]
     line = {
         "metric": METRIC,
@@ -617,10 +681,10 @@ def main():
         "gpu_launches": 4 * args.steps,
         "timing": "value: K replays of one CUDA graph holding the whole step (hsa_decode_step "
                   "with device buffers), CUDA events around each replay; breakdown and "
-                  "roofline: the four kernels replayed one graph each (each time includes its "
-                  "graph launch gap)",
+                  "roofline: average launch duration of each kernel, from graphs of 10 "
+                  "back-to-back launches of it (cache replicas alternating), CUDA events "
+                  "around each graph",
         "clocks": clocks,
-        "split_step_us": main_res["split_step_ms"] * 1e3,
         "breakdown_us": {k: v * 1e3 for k, v in per.items()},
         "select_us": main_res["select_ms"] * 1e3,
         "dense_us": main_res["dense_ms"] * 1e3,

@@ -30,7 +30,7 @@ cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_ne
                              const int32_t* page_table, const int32_t* seq_lens, int* err,
                              cudaStream_t st, bool beside);
 
-// ---- select.cu
+// ---- score.cu
 // block_max: [B][Hkv][max_pages]; tile_max (nullable): [B][Hkv][score_max_tiles], the max of
 // each 64-token tile, which the prune kernel uses as the chunk score when chunks are 64.
 int score_max_tiles(const Shape& s);
@@ -38,6 +38,8 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const
                                 const float* k_scale, const int32_t* page_table,
                                 const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
                                 int* err, int num_sms, cudaStream_t st);
+
+// ---- prune.cu
 // page_table / sel_pages (both nullable): also write the page of every kept block into
 // sel_pages [B][Hkv][K2], entries [0, n_blocks) (for launch_attend's sel_pages).
 cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t* block_max,

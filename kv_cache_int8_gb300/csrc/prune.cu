@@ -1,29 +1,16 @@
-// select.cu -- global int8 scoring of every candidate token and the two pruning modules.
+// prune.cu -- the two pruning modules: top-K1 chunks, then top-K2 blocks of those chunks.
 //
-// Sources: "HCAttention: Extreme KV cache compression via heterogeneous attention computing
-// for LLMs", abstract and contribution list (global approximate attention scoring over the
-// GPU-resident quantised keys); InfiniteHiP article (163.com), section "实现 7.24 倍的端到端
-// 解码加速" (a pruning module cuts the context into fixed-length chunks, finds each chunk's
-// best token in parallel and passes the top-K chunks on; stacked modules refine a
-// block-sparse mask); "KV Cache 与长上下文推理", section "MQA 与 GQA" (G query heads share
-// one kv head).
-//
-// score_blocks_kernel (the HBM-bound scan): a persistent grid walks the flattened list of
-// 64-token tiles (sequence, kv head, tile). One producer lane per CTA streams each tile's
-// four 2 KiB (page, head) blocks into a shared-memory ring with TMA tensor copies
-// (128-byte swizzle, so the token-per-lane reads below are bank-conflict free) and
-// mbarrier transaction counts. Consumer warps own fixed ring slots; lane = token, the
-// G x 32 packed int8 query words sit in registers, dp4a gives the G exact int32 dot
-// products, their max is the token score and a 16-lane max gives the block maximum.
+// Source: InfiniteHiP article (163.com), section "实现 7.24 倍的端到端解码加速" (a pruning
+// module cuts the context into fixed-length chunks, finds each chunk's best token in
+// parallel and passes the top-K chunks on; stacked modules refine a block-sparse mask).
 //
 // prune_kernel: one CTA per (sequence, kv head). Chunk scores (the scorer's per-tile maxima
 // for 64-token chunks, else the max of their blocks' maxima) are staged in shared memory
 // with bulk copies, and so are the whole row of block maxima and page ids when they fit;
 // the K-th largest value is found by radix selection on 8-bit digits (two CTA barriers a
-// digit); ties
-// at the threshold are broken toward lower indices by ballots over warp-contiguous ranges,
-// which also write the kept indices in ascending order. Module 2 repeats this on the blocks
-// of the kept chunks.
+// digit); ties at the threshold are broken toward lower indices by ballots over
+// warp-contiguous ranges, which also write the kept indices in ascending order. Module 2
+// repeats this on the blocks of the kept chunks.
 #include <algorithm>
 #include <climits>
 
@@ -32,289 +19,6 @@
 
 namespace hsa {
 namespace {
-
-// ------------------------------------------------------------------ scorer
-
-constexpr int kTileBlocks = 4;                             // blocks per ring slot (64 tokens)
-constexpr int kTileTokens = kTileBlocks * kPage;
-constexpr int kStageBytes = kTileBlocks * kBlockBytesI8;   // 8 KiB
-constexpr int kScoreWarps = 4;                             // consumer warps
-constexpr int kScoreStages = 8;                            // ring slots (multiple of kScoreWarps)
-constexpr int kScoreThreads = (kScoreWarps + 1) * 32;
-constexpr int kMaxBatch = 1024;
-static_assert(kScoreStages % kScoreWarps == 0, "each consumer warp owns fixed ring slots");
-
-struct ScoreArgs {
-  const __nv_bfloat16* q;
-  const float* k_scale;
-  const int32_t* page_table;
-  const int32_t* seq_lens;
-  int32_t* block_max;
-  int32_t* tile_max;  // nullable: max of each 64-token tile's blocks (= chunk max for chunk 64)
-  int* err;
-  int batch, hkv, max_pages, max_tiles, num_pages, sink, window;
-};
-
-// Candidate region of one sequence in block and tile units.
-struct SeqRange {
-  int lo, hi;          // candidate tokens [lo, hi)
-  int k_lo, k_hi;      // blocks holding a candidate token
-  int tile_lo, ntile;  // tiles covering [k_lo, k_hi)
-};
-
-__device__ __forceinline__ SeqRange seq_range(const ScoreArgs& a, int b) {
-  SeqRange r;
-  const int n = a.seq_lens[b];
-  r.lo = a.sink;
-  r.hi = n - a.window;
-  if (n < 0 || n > a.max_pages * kPage || r.hi <= r.lo) {
-    r.hi = r.lo;
-    r.k_lo = r.k_hi = r.tile_lo = r.ntile = 0;
-    return r;
-  }
-  r.k_lo = r.lo / kPage;
-  r.k_hi = (r.hi + kPage - 1) / kPage;
-  r.tile_lo = r.k_lo / kTileBlocks;
-  r.ntile = (r.k_hi + kTileBlocks - 1) / kTileBlocks - r.tile_lo;
-  return r;
-}
-
-// Query folding and quantisation for (b, h), executed by one whole warp. Lane l computes
-// channels [4l, 4l+4) of each of the G heads; the packed code words are then broadcast so
-// that every lane holds all G x 32 words (uniform registers of the dot-product loop).
-template <int G>
-__device__ __forceinline__ void load_query_codes(int (&qq)[G][32], const ScoreArgs& a, int b,
-                                                 int h, int lane) {
-  const float4 s4 =
-      *reinterpret_cast<const float4*>(a.k_scale + ((size_t)b * a.hkv + h) * kHeadDim + 4 * lane);
-  float qp[G][4];
-  float amax = 0.0f;
-#pragma unroll
-  for (int j = 0; j < G; j++) {
-    const uint2 w = *reinterpret_cast<const uint2*>(
-        a.q + ((size_t)b * a.hkv * G + (size_t)h * G + j) * kHeadDim + 4 * lane);
-    qp[j][0] = __fmul_rn(bf16_lo(w.x), s4.x);
-    qp[j][1] = __fmul_rn(bf16_hi(w.x), s4.y);
-    qp[j][2] = __fmul_rn(bf16_lo(w.y), s4.z);
-    qp[j][3] = __fmul_rn(bf16_hi(w.y), s4.w);
-#pragma unroll
-    for (int i = 0; i < 4; i++) amax = fmaxf(amax, fabsf(qp[j][i]));
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float sq = __fdiv_rn(amax, 127.0f);
-#pragma unroll
-  for (int j = 0; j < G; j++) {
-    int word = 0;
-#pragma unroll
-    for (int i = 0; i < 4; i++) word |= (int8_code(qp[j][i], sq) & 0xFF) << (8 * i);
-#pragma unroll
-    for (int c = 0; c < 32; c++) qq[j][c] = __shfl_sync(0xffffffffu, word, c);
-  }
-}
-
-template <int G>
-__global__ void __launch_bounds__(kScoreThreads, 2)
-    score_blocks_kernel(const __grid_constant__ CUtensorMap kq_map, const ScoreArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kScoreStages * kStageBytes);
-  uint64_t* empty = full + kScoreStages;
-  int* prefix = reinterpret_cast<int*>(empty + kScoreStages);  // [batch + 1] tiles before b
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kScoreStages; s++) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    fence_barrier_init();
-  }
-  // inputs may come from the previous kernel of the stream; then let the next one launch
-  grid_dep_wait();
-  grid_dep_launch();
-  if (warp == kScoreWarps && lane == 0) tma_prefetch_descriptor(&kq_map);
-  // tiles per sequence (x hkv), exclusive prefix sum by warp 0
-  if (warp == 0) {
-    int carry = 0;
-    for (int b0 = 0; b0 < a.batch; b0 += 32) {
-      const int b = b0 + lane;
-      int v = 0;
-      if (b < a.batch) {
-        const int n = a.seq_lens[b];
-        if (n < 0 || n > a.max_pages * kPage) set_error(a.err, kDevErrCheck);
-        v = seq_range(a, b).ntile * a.hkv;
-      }
-      int x = v;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off) x += y;
-      }
-      if (b < a.batch) prefix[b] = carry + x - v;
-      carry += __shfl_sync(0xffffffffu, x, 31);
-    }
-    if (lane == 0) prefix[a.batch] = carry;
-  }
-  __syncthreads();
-
-  const long long total = prefix[a.batch];
-  const int f0 = (int)(total * blockIdx.x / gridDim.x);
-  const int f1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
-  if (f0 >= f1) return;
-
-  int b = 0;
-  while (prefix[b + 1] <= f0) b++;
-
-  if (warp == kScoreWarps) {
-    // ------------------------------------------------------------ producer
-    // The whole warp resolves the page ids of the next 32 tiles at once (one coalesced
-    // round trip), then lane 0 issues their copies in order as ring slots free up.
-    bool ok = true;
-    const uint64_t policy = l2_evict_first_policy();  // each code is read once
-    int bw = b;  // sequence of tile f0 + jb (warp-uniform)
-    for (int jb = 0; ok && f0 + jb < f1; jb += 32) {
-      const int f = f0 + jb + lane;
-      int rows[kTileBlocks];
-#pragma unroll
-      for (int i = 0; i < kTileBlocks; i++) rows[i] = -1;
-      if (f < f1) {
-        int bl = bw;
-        while (prefix[bl + 1] <= f) bl++;
-        const SeqRange sr = seq_range(a, bl);
-        const int r = f - prefix[bl];
-        const int h = r / sr.ntile;
-        const int tile = sr.tile_lo + r % sr.ntile;
-        const int32_t* row = a.page_table + (size_t)bl * a.max_pages;
-        int pg[kTileBlocks];
-#pragma unroll
-        for (int i = 0; i < kTileBlocks; i++) {
-          const int k = tile * kTileBlocks + i;
-          pg[i] = (k >= sr.k_lo && k < sr.k_hi) ? row[k] : -2;
-        }
-#pragma unroll
-        for (int i = 0; i < kTileBlocks; i++) {
-          if (pg[i] == -2) continue;
-          if (pg[i] < 0 || pg[i] >= a.num_pages) {
-            set_error(a.err, kDevErrCheck);
-            continue;
-          }
-          rows[i] = (pg[i] * a.hkv + h) * kPage;
-        }
-      }
-      const int n = min(32, f1 - f0 - jb);
-      for (int i = 0; i < n; i++) {
-        int rr[kTileBlocks];
-#pragma unroll
-        for (int q = 0; q < kTileBlocks; q++) rr[q] = __shfl_sync(0xffffffffu, rows[q], i);
-        if (lane == 0) {
-          const int j = jb + i;
-          const int s = j % kScoreStages;
-          if (j >= kScoreStages && !mbar_wait(&empty[s], ((j / kScoreStages) - 1) & 1)) {
-            set_error(a.err, kDevErrTimeout);
-            ok = false;
-          } else {
-            uint32_t bytes = 0;
-#pragma unroll
-            for (int q = 0; q < kTileBlocks; q++) bytes += rr[q] >= 0 ? kBlockBytesI8 : 0;
-            mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-            for (int q = 0; q < kTileBlocks; q++)
-              if (rr[q] >= 0)
-                tma_load_2d_hint(ring + s * kStageBytes + q * kBlockBytesI8, &kq_map, 0, rr[q],
-                                 &full[s], policy);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-      }
-      // advance the warp's sequence cursor to the first tile of the next batch
-      const int fn = f0 + jb + 32;
-      while (bw + 1 < a.batch && prefix[bw + 1] <= fn) bw++;
-    }
-    if (!ok && lane == 0) {
-      // let the copies already issued land before the CTA exits (bounded)
-      const int issued = f1 - f0;
-      for (int j = max(0, issued - kScoreStages); j < issued; j++)
-        mbar_wait(&full[j % kScoreStages], (j / kScoreStages) & 1);
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  int qq[G][32];
-  int cur_b = -1, cur_h = -1;
-  SeqRange sr = seq_range(a, b);
-  for (int j = warp; f0 + j < f1; j += kScoreWarps) {
-    const int f = f0 + j;
-    while (prefix[b + 1] <= f) {
-      b++;
-      sr = seq_range(a, b);
-    }
-    const int r = f - prefix[b];
-    const int h = r / sr.ntile;
-    const int tile = sr.tile_lo + r % sr.ntile;
-    if (b != cur_b || h != cur_h) {
-      load_query_codes<G>(qq, a, b, h, lane);
-      cur_b = b;
-      cur_h = h;
-    }
-    const int s = j % kScoreStages;
-    if (!mbar_wait(&full[s], (j / kScoreStages) & 1)) {
-      set_error(a.err, kDevErrTimeout);
-      break;
-    }
-    const uint32_t sbase = smem_addr(ring + s * kStageBytes);
-    int32_t* out = a.block_max + ((size_t)b * a.hkv + h) * a.max_pages;
-    int tmax = INT_MIN;
-#pragma unroll
-    for (int half = 0; half < 2; half++) {
-      const int row = half * 32 + lane;           // token within the tile
-      const int t = tile * kTileTokens + row;
-      const uint32_t rbase = sbase + row * kHeadDim;
-      int acc[G];
-#pragma unroll
-      for (int jj = 0; jj < G; jj++) acc[jj] = 0;
-#pragma unroll
-      for (int c = 0; c < 8; c++) {
-        const uint4 kv = lds128(rbase + ((c ^ (row & 7)) << 4));
-#pragma unroll
-        for (int jj = 0; jj < G; jj++) {
-          acc[jj] = __dp4a((int)kv.x, qq[jj][4 * c + 0], acc[jj]);
-          acc[jj] = __dp4a((int)kv.y, qq[jj][4 * c + 1], acc[jj]);
-          acc[jj] = __dp4a((int)kv.z, qq[jj][4 * c + 2], acc[jj]);
-          acc[jj] = __dp4a((int)kv.w, qq[jj][4 * c + 3], acc[jj]);
-        }
-      }
-      int g = acc[0];
-#pragma unroll
-      for (int jj = 1; jj < G; jj++) g = max(g, acc[jj]);
-      if (t < sr.lo || t >= sr.hi) g = INT_MIN;
-      g = max(g, __shfl_xor_sync(0xffffffffu, g, 8));
-      g = max(g, __shfl_xor_sync(0xffffffffu, g, 4));
-      g = max(g, __shfl_xor_sync(0xffffffffu, g, 2));
-      g = max(g, __shfl_xor_sync(0xffffffffu, g, 1));
-      if ((lane & 15) == 0) {
-        const int k = tile * kTileBlocks + half * 2 + (lane >> 4);
-        if (k >= sr.k_lo && k < sr.k_hi) out[k] = g;
-      }
-      tmax = max(tmax, g);
-    }
-    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-    if (a.tile_max != nullptr && lane == 0)
-      a.tile_max[((size_t)b * a.hkv + h) * a.max_tiles + tile] = tmax;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-  }
-}
-
-size_t score_smem_bytes(int batch) {
-  return 1024 + kScoreStages * kStageBytes + 2 * kScoreStages * sizeof(uint64_t) +
-         (batch + 1) * sizeof(int);
-}
 
 // -------------------------------------------------------------------- prune
 
@@ -344,7 +48,7 @@ struct PruneArgs {
   int32_t* sel_pages;         // nullable, [B][Hkv][K2] beside block_idx
   int* err;
   int hkv, max_pages, chunk_blocks, k1, k2, sink, window;
-  int vals_cap, cand_cap, kept_cap, row_cap, prow_cap;  // shared-memory array sizes (0: none)
+  int vals_cap, cand_cap, kept_cap, row_cap, prow_cap, sel_cap;  // shared-memory array sizes
 };
 
 // Shared scratch of the selection.
@@ -410,13 +114,11 @@ __device__ __forceinline__ int* stage(const StagedRow& r, uint64_t* bar) {
   return r.dst();
 }
 
-// Min and max of the valid (not INT_MIN) entries of vals[0, n), for every thread; an empty
+// (min, max) of the valid (not INT_MIN) entries of vals[0, n), for every thread; an empty
 // set gives (INT_MAX, INT_MIN). One CTA barrier.
-__device__ __forceinline__ void block_min_max(const int* vals, int n, PruneShared& ps, int& mn,
-                                              int& mx) {
+__device__ __noinline__ int2 block_min_max(const int* vals, int n, PruneShared& ps) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  mn = INT_MAX;
-  mx = INT_MIN;
+  int mn = INT_MAX, mx = INT_MIN;
   for (int i0 = threadIdx.x; i0 < n; i0 += 4 * kPruneThreads) {
     int v[4];
 #pragma unroll
@@ -449,9 +151,11 @@ __device__ __forceinline__ void block_min_max(const int* vals, int n, PruneShare
     mn = min(mn, ps.mn[w]);
     mx = max(mx, ps.mx[w]);
   }
+  return make_int2(mn, mx);
 }
 
-// The K-th largest value T of vals[0, n) (0 < K < number of valid entries), by radix
+// Returns (T, need_eq, eq_total). The K-th largest value T of vals[0, n) (0 < K < number of
+// valid entries), by radix
 // selection on 8-bit digits of the keys rel_key(v, min), from the highest digit in which
 // they can differ. need_eq = K - #(values > T): how many of the entries equal to T are kept
 // (the lowest-index ones); eq_total = #(values == T). The valid values' min and max are
@@ -463,10 +167,15 @@ __device__ __forceinline__ void block_min_max(const int* vals, int n, PruneShare
 // warp by shuffles, publishing every digit's in-warp suffix count and each warp's total;
 // then every thread finds the digit holding the K-th key from those by itself. The
 // histograms are zero on entry and on return.
-__device__ void kth_largest(const int* vals, int n, int K, PruneShared& ps, int& T, int& need_eq,
-                            int& eq_total, bool have_range = false, int vmin = 0, int vmax = 0) {
+__device__ __noinline__ int3 kth_largest(const int* vals, int n, int K, PruneShared& ps,
+                                         bool have_range, int vmin, int vmax) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
-  if (!have_range) block_min_max(vals, n, ps, vmin, vmax);
+  if (!have_range) {
+    const int2 r = block_min_max(vals, n, ps);
+    vmin = r.x;
+    vmax = r.y;
+  }
+  int eq_total = 0;
   const unsigned kmax = (unsigned)((long long)vmax - vmin) + 1u;
   int shift = ((31 - __clz(kmax)) / 8) * 8;
   unsigned prefix = 0;  // decided high bits of T's key
@@ -526,19 +235,17 @@ __device__ void kth_largest(const int* vals, int n, int K, PruneShared& ps, int&
     }
     shift -= 8;
   }
-  T = (int)((long long)vmin + (long long)prefix - 1);
-  need_eq = K - above;
   __syncthreads();
+  return make_int3((int)((long long)vmin + (long long)prefix - 1), K - above, eq_total);
 }
 
 // Emits, in ascending index order, every i with vals[i] > T plus the first need_eq indices
-// with vals[i] == T, calling emit(position, i); returns how many. Warp w owns a contiguous
+// with vals[i] == T, writing out[position] = add + i; returns how many. Warp w owns a contiguous
 // range, read 4 x 32 entries at a time; positions come from ballots (one CTA barrier for
 // the per-warp counts). When all entries equal to T are kept (need_eq == eq_total), or none
 // are, the test is a plain threshold and no tie ranks are needed.
-template <typename Emit>
-__device__ int collect(const int* vals, int n, int T, int need_eq, int eq_total, PruneShared& ps,
-                       Emit emit) {
+__device__ __noinline__ int collect(const int* vals, int n, int T, int need_eq, int eq_total,
+                                    PruneShared& ps, int* out, int add) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int per = ((n + kPruneWarps * 32 - 1) / (kPruneWarps * 32)) * 32;
   const int w0 = min(n, warp * per), w1 = min(n, w0 + per);
@@ -574,7 +281,7 @@ __device__ int collect(const int* vals, int n, int T, int need_eq, int eq_total,
 #pragma unroll
       for (int u = 0; u < 4; u++) {
         const unsigned tm = __ballot_sync(0xffffffffu, take[u]);
-        if (take[u]) emit(pos + __popc(tm & lt), i0 + 32 * u + lane);
+        if (take[u]) out[pos + __popc(tm & lt)] = add + i0 + 32 * u + lane;
         pos += __popc(tm);
       }
     }
@@ -614,7 +321,7 @@ __device__ int collect(const int* vals, int n, int T, int need_eq, int eq_total,
     const unsigned eqm = __ballot_sync(0xffffffffu, eq);
     const bool take = gt || (eq && eq_base + __popc(eqm & lt) < need_eq);
     const unsigned tm = __ballot_sync(0xffffffffu, take);
-    if (take) emit(pos + __popc(tm & lt), i);
+    if (take) out[pos + __popc(tm & lt)] = add + i;
     eq_base += __popc(eqm);
     pos += __popc(tm);
   }
@@ -629,7 +336,8 @@ __device__ int collect(const int* vals, int n, int T, int need_eq, int eq_total,
 // Shared memory: PruneShared, vals [vals_cap + 4], cand [cand_cap] (module 2's block ids),
 // cand_page [cand_cap] (with
 // sel_pages), kept [kept_cap], row [row_cap + 4] (the sequence's block maxima, staged whole
-// when they fit), prow [prow_cap + 4] (its page ids, with sel_pages).
+// when they fit), prow [prow_cap + 4] (its page ids, with sel_pages), sel_pos [sel_cap]
+// (module 2's kept positions in cand).
 __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_kernel(const PruneArgs a) {
   extern __shared__ __align__(16) unsigned char psmem_raw[];
   PruneShared& ps = *reinterpret_cast<PruneShared*>(psmem_raw);
@@ -640,6 +348,7 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
   int* kept_chunks = cand_page + a.cand_cap;         // kept_cap
   int* row_base = kept_chunks + a.kept_cap;          // row_cap + 4 (16-byte aligned)
   int* prow_base = row_base + (a.row_cap > 0 ? a.row_cap + 4 : 0);  // prow_cap + 4
+  int* sel_pos = prow_base + (a.prow_cap > 0 ? a.prow_cap + 4 : 0);  // sel_cap
 
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x;
@@ -719,16 +428,19 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
   // ---- module 1: top-K1 chunks
   const int keep1 = min(a.k1, n1);
   int T = INT_MIN, need_eq = 0, eq_total = 0;
-  if (keep1 < n1 && keep1 > 0) kth_largest(vals, n1, keep1, ps, T, need_eq, eq_total);
+  if (keep1 < n1 && keep1 > 0) {
+    const int3 r = kth_largest(vals, n1, keep1, ps, false, 0, 0);
+    T = r.x;
+    need_eq = r.y;
+    eq_total = r.z;
+  }
   int got1 = 0;
   if (keep1 > 0) {
-    got1 = collect(vals, n1, T, need_eq, eq_total, ps, [&](int pos, int i) {
-      kept_chunks[pos] = c_lo + i;
-      if (a.chunk_idx) a.chunk_idx[bh * a.k1 + pos] = c_lo + i;
-    });
+    got1 = collect(vals, n1, T, need_eq, eq_total, ps, kept_chunks, c_lo);
   }
   if (a.chunk_idx)
-    for (int i = got1 + tid; i < a.k1; i += kPruneThreads) a.chunk_idx[bh * a.k1 + i] = -1;
+    for (int i = tid; i < a.k1; i += kPruneThreads)
+      a.chunk_idx[bh * a.k1 + i] = i < got1 ? kept_chunks[i] : -1;
   if (a.n_chunks && tid == 0) a.n_chunks[bh] = got1;
   __syncthreads();
 
@@ -790,16 +502,21 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
   T = INT_MIN;
   need_eq = 0;
   eq_total = 0;
-  if (keep2 < n2_valid && keep2 > 0)
-    kth_largest(vals, n2, keep2, ps, T, need_eq, eq_total, true, mn2, mx2);
+  if (keep2 < n2_valid && keep2 > 0) {
+    const int3 r = kth_largest(vals, n2, keep2, ps, true, mn2, mx2);
+    T = r.x;
+    need_eq = r.y;
+    eq_total = r.z;
+  }
   int got2 = 0;
   if (keep2 > 0) {
-    got2 = collect(vals, n2, T, need_eq, eq_total, ps, [&](int pos, int i) {
-      a.block_idx[bh * a.k2 + pos] = cand[i];
-      if (prow) a.sel_pages[bh * a.k2 + pos] = cand_page[i];
-    });
+    got2 = collect(vals, n2, T, need_eq, eq_total, ps, sel_pos, 0);
   }
-  for (int i = got2 + tid; i < a.k2; i += kPruneThreads) a.block_idx[bh * a.k2 + i] = -1;
+  for (int i = tid; i < a.k2; i += kPruneThreads) {
+    const int x = i < got2 ? sel_pos[i] : -1;
+    a.block_idx[bh * a.k2 + i] = x >= 0 ? cand[x] : -1;
+    if (prow && x >= 0) a.sel_pages[bh * a.k2 + i] = cand_page[x];
+  }
   if (tid == 0) a.n_blocks[bh] = got2;
 }
 
@@ -818,6 +535,7 @@ int prune_caps(const Shape& s, PruneArgs& a, bool stage_pages) {
   a.kept_cap = up4(std::max<long long>(keep1, 1));
   a.row_cap = s.max_pages <= kRowCap ? up4(s.max_pages) : 0;
   a.prow_cap = stage_pages ? a.row_cap : 0;
+  a.sel_cap = up4(std::max<long long>(std::min<long long>(s.k2, n2max), 1));
   return 0;
 }
 
@@ -825,7 +543,7 @@ size_t prune_smem(const PruneArgs& a) {
   return ((sizeof(PruneShared) + 15) / 16) * 16 +
          sizeof(int) * ((size_t)a.vals_cap + 4 + 2 * (size_t)a.cand_cap + a.kept_cap +
                         (a.row_cap > 0 ? a.row_cap + 4 : 0) +
-                        (a.prow_cap > 0 ? a.prow_cap + 4 : 0));
+                        (a.prow_cap > 0 ? a.prow_cap + 4 : 0) + a.sel_cap);
 }
 
 }  // namespace
@@ -836,62 +554,6 @@ size_t prune_smem_bytes(const Shape& s) {
   PruneArgs a;
   if (prune_caps(s, a, true) != 0) return ~size_t(0);
   return prune_smem(a);
-}
-
-int score_max_tiles(const Shape& s) { return (s.max_pages + kTileBlocks - 1) / kTileBlocks; }
-
-cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const void* q,
-                                const float* k_scale, const int32_t* page_table,
-                                const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
-                                int* err, int num_sms, cudaStream_t st) {
-  if (s.batch > kMaxBatch) return cudaErrorInvalidValue;
-  ScoreArgs a;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k_scale = k_scale;
-  a.page_table = page_table;
-  a.seq_lens = seq_lens;
-  a.block_max = block_max;
-  a.tile_max = tile_max;
-  a.err = err;
-  a.batch = s.batch;
-  a.hkv = s.hkv;
-  a.max_pages = s.max_pages;
-  a.max_tiles = score_max_tiles(s);
-  a.num_pages = s.num_pages;
-  a.sink = s.sink;
-  a.window = s.window;
-  const size_t smem = score_smem_bytes(s.batch);
-  // upper bound of the tile count; the kernel splits the true count evenly
-  const long long tiles_max =
-      (long long)s.batch * s.hkv * ((s.max_pages + kTileBlocks - 1) / kTileBlocks + 1);
-  const int grid = (int)std::min<long long>(tiles_max, 2LL * num_sms);
-  cudaError_t e;
-  switch (s.group) {
-    case 1:
-      e = set_kernel_smem(score_blocks_kernel<1>, smem);
-      if (e != cudaSuccess) return e;
-      e = launch_kernel(score_blocks_kernel<1>, dim3(grid), dim3(kScoreThreads), smem, st, true,
-                        kq_map, a);
-      if (e != cudaSuccess) return e;
-      break;
-    case 2:
-      e = set_kernel_smem(score_blocks_kernel<2>, smem);
-      if (e != cudaSuccess) return e;
-      e = launch_kernel(score_blocks_kernel<2>, dim3(grid), dim3(kScoreThreads), smem, st, true,
-                        kq_map, a);
-      if (e != cudaSuccess) return e;
-      break;
-    case 4:
-      e = set_kernel_smem(score_blocks_kernel<4>, smem);
-      if (e != cudaSuccess) return e;
-      e = launch_kernel(score_blocks_kernel<4>, dim3(grid), dim3(kScoreThreads), smem, st, true,
-                        kq_map, a);
-      if (e != cudaSuccess) return e;
-      break;
-    default:
-      return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t* block_max,
