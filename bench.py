@@ -356,6 +356,23 @@ def timed_steps(case, steps: int, names, sampler=None):
     return per, step
 
 
+def host_link_copy_gbs(device, mib: int = 512) -> float:
+    """Pinned host -> device copy-engine rate (GB/s): the host link's measured read rate, the
+    denominator for kernels that read K/V from mapped host memory."""
+    import torch
+    h = torch.empty(mib << 20, dtype=torch.uint8).pin_memory()
+    d = torch.empty(mib << 20, dtype=torch.uint8, device=device)
+    d.copy_(h, non_blocking=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(3):
+        d.copy_(h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    return 3 * (mib << 20) / (e0.elapsed_time(e1) * 1e6)
+
+
 def burst_times(case, names, reps: int):
     """Average duration of one launch of each kernel: `reps` replays of its burst graph
     (BURST launches back to back) with CUDA events around each replay, after 3 warm-up
@@ -607,6 +624,7 @@ def main():
             torch.cuda.empty_cache()
             extra[name] = {
                 "us_per_step": r["step_ms"] * 1e3, "score_us": r["per_ms"]["score"] * 1e3,
+                **({"host_link_copy_gbs": host_link_copy_gbs(device)} if not dense else {}),
                 "prune_us": r["per_ms"]["prune"] * 1e3, "attend_us": r["per_ms"]["attend"] * 1e3,
                 "dense_us": r["dense_ms"] * 1e3 if dense else None,
                 "score_gbs": r["gbs"]["score"],

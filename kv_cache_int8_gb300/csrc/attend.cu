@@ -39,6 +39,9 @@
 #ifndef HSA_DENSE_CTAS_PER_SM
 #define HSA_DENSE_CTAS_PER_SM 3
 #endif
+#ifndef HSA_HOST_CTAS_PER_SM
+#define HSA_HOST_CTAS_PER_SM 3
+#endif
 #ifndef HSA_SPARSE_WARPS
 #define HSA_SPARSE_WARPS 8
 #endif
@@ -61,6 +64,7 @@ constexpr int kSparseWarps = HSA_SPARSE_WARPS, kSparseStages = 2 * HSA_SPARSE_WA
 constexpr int kDenseWarps = 4, kDenseStages = 8;     // HBM path, dense decode
 constexpr int kSlotBytes = 2 * kBlockBytesBf16;  // K page + V page of one head
 constexpr int kHostThreads = kCompute;
+static_assert(kHostThreads * 16 * 2 == kBlockBytesBf16, "a host-path segment copy: 2 x 16 B a thread");
 constexpr int kMaxSplits = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -783,7 +787,9 @@ __global__ void __launch_bounds__(kHostThreads, 3) attend_host_kernel(const AttA
   float qf[G][16];
   load_query<G>(qf, a, b, h, lane & 7);
 
-  // each thread copies 64 of the segment's 8192 bytes: K bytes [32 tid, +32), then V
+  // each thread copies 64 of the segment's 8192 bytes: 16 bytes at 16 tid and at 2048 + 16 tid
+  // of K, then of V, so that every warp load reads a contiguous, fully used 512-byte span
+  // (each sector crosses the host link once)
   auto fetch = [&](int i, uint4 (&buf)[4], int& k, int& t0, int& t1) {
     segment_at(S, i, a.sink, k, t0, t1);
     if (t0 >= t1) return;
@@ -796,18 +802,18 @@ __global__ void __launch_bounds__(kHostThreads, 3) attend_host_kernel(const AttA
     const size_t off = ((size_t)page * a.hkv + h) * kPage * kHeadDim;
     const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k + off);
     const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v + off);
-    buf[0] = ldg128_nc(kp + tid * 32);
-    buf[1] = ldg128_nc(kp + tid * 32 + 16);
-    buf[2] = ldg128_nc(vp + tid * 32);
-    buf[3] = ldg128_nc(vp + tid * 32 + 16);
+    buf[0] = ldg128_nc(kp + tid * 16);
+    buf[1] = ldg128_nc(kp + kBlockBytesBf16 / 2 + tid * 16);
+    buf[2] = ldg128_nc(vp + tid * 16);
+    buf[3] = ldg128_nc(vp + kBlockBytesBf16 / 2 + tid * 16);
   };
   auto store = [&](int slot, const uint4 (&buf)[4]) {
-    uint4* kd = reinterpret_cast<uint4*>(slots + slot * kSlotBytes + tid * 32);
-    uint4* vd = reinterpret_cast<uint4*>(slots + slot * kSlotBytes + kBlockBytesBf16 + tid * 32);
-    kd[0] = buf[0];
-    kd[1] = buf[1];
-    vd[0] = buf[2];
-    vd[1] = buf[3];
+    uint8_t* kd = slots + slot * kSlotBytes + tid * 16;
+    uint8_t* vd = kd + kBlockBytesBf16;
+    *reinterpret_cast<uint4*>(kd) = buf[0];
+    *reinterpret_cast<uint4*>(kd + kBlockBytesBf16 / 2) = buf[1];
+    *reinterpret_cast<uint4*>(vd) = buf[2];
+    *reinterpret_cast<uint4*>(vd + kBlockBytesBf16 / 2) = buf[3];
   };
   uint4 nxt[4];
   int kn = 0, t0n = 0, t1n = 0;
@@ -864,7 +870,8 @@ int attend_splits(const Shape& s, bool dense, bool host, int num_sms) {
     segs = (s.sink + kPage - 1) / kPage + s.k2 + (s.window + kPage - 1) / kPage + 1;
   }
   // dense: about three CTAs per SM; sparse: fewer, each with several segments
-  const int per_sm = host ? 4 : (dense ? HSA_DENSE_CTAS_PER_SM : HSA_SPARSE_CTAS_PER_SM);
+  const int per_sm =
+      host ? HSA_HOST_CTAS_PER_SM : (dense ? HSA_DENSE_CTAS_PER_SM : HSA_SPARSE_CTAS_PER_SM);
   long long want = ((long long)num_sms * per_sm + units - 1) / units;
   if (!dense && !host && HSA_SPARSE_RESERVE && num_sms > units) {
     const long long reserved = std::max<long long>(1, (num_sms - units) / units);
