@@ -695,7 +695,9 @@ def main():
         "e2e": None if e2e_ms is None else {
             "value": job_value(e2e_ms, world), "unit": "us/step", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "path": "hsa_decode_step with pinned host q/k_new/v_new/out/lse, synchronised per step"},
+            "path": "hsa_decode_step with pinned host q/k_new/v_new/out/lse (mapped: a kernel "
+                    "stages the inputs, the attention writes the outputs to host memory), "
+                    "synchronised per step"},
         "gpu_launches": 4 * args.steps,
         "timing": "value: K replays of one CUDA graph holding the whole step (hsa_decode_step "
                   "with device buffers), CUDA events around each replay; breakdown and "

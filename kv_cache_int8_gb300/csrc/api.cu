@@ -141,6 +141,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D view of the int8 code cache: rows of 128 bytes, one per (page, head, slot); a box is
 // one (page, head) block of 16 rows, stored with the 128-byte swizzle.
 int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map) {
+  // the map depends only on the base pointer and the row count: the last one of this thread
+  // is reused
+  struct Last {
+    const int8_t* kq = nullptr;
+    long long rows = -1;
+    CUtensorMap map;
+  };
+  thread_local Last last;
+  const long long rows = (long long)s.num_pages * s.hkv * hsa::kPage;
+  if (last.kq == kq && last.rows == rows) {
+    *map = last.map;
+    return HSA_OK;
+  }
   auto fn = encode_fn();
   if (fn == nullptr) return HSA_ERR_CUDA;
   cuuint64_t dims[2] = {(cuuint64_t)hsa::kHeadDim,
@@ -151,7 +164,22 @@ int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map) {
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(kq), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? HSA_OK : HSA_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return HSA_ERR_CUDA;
+  last.kq = kq;
+  last.rows = rows;
+  last.map = *map;
+  return HSA_OK;
+}
+
+// Device alias of a mapped pinned host buffer; false (error state cleared) if it has none.
+bool host_alias(const void* p, void** out) {
+  void* dp = nullptr;
+  if (cudaHostGetDevicePointer(&dp, const_cast<void*>(p), 0) != cudaSuccess || dp == nullptr) {
+    cudaGetLastError();
+    return false;
+  }
+  *out = dp;
+  return true;
 }
 
 // Device alias of a pinned host buffer (kv_on_host) or the pointer itself.
@@ -419,16 +447,35 @@ int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
   float* lse = io->lse;
   const size_t qb = (size_t)s.batch * s.hq * hsa::kHeadDim * 2;
   const size_t kvb = (size_t)s.batch * s.hkv * hsa::kHeadDim * 2;
+  // Host I/O: with mapped pinned buffers (the default for pinned memory on this platform) a
+  // small kernel stages the inputs and the attend writes the outputs straight to host
+  // memory; otherwise copy-engine transfers through the workspace.
+  bool direct_out = false;
   if (io->io_on_host) {
-    cudaError_t e = cudaMemcpyAsync(ws + l.q, io->q, qb, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + l.k_new, io->k_new, kvb, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + l.v_new, io->v_new, kvb, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return HSA_ERR_CUDA;
+    void *hq = nullptr, *hkn = nullptr, *hvn = nullptr, *hout = nullptr, *hlse = nullptr;
+    const bool mapped = host_alias(io->q, &hq) && host_alias(io->k_new, &hkn) &&
+                        host_alias(io->v_new, &hvn) && host_alias(io->out, &hout) &&
+                        (io->lse == nullptr || host_alias(io->lse, &hlse));
+    if (mapped) {
+      if (hsa::launch_stage_io(s, hq, hkn, hvn, ws + l.q, ws + l.k_new, ws + l.v_new, num_sms(),
+                               st) != cudaSuccess)
+        return HSA_ERR_CUDA;
+      out = static_cast<float*>(hout);
+      lse = static_cast<float*>(hlse);
+      direct_out = true;
+    } else {
+      cudaError_t e = cudaMemcpyAsync(ws + l.q, io->q, qb, cudaMemcpyHostToDevice, st);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ws + l.k_new, io->k_new, kvb, cudaMemcpyHostToDevice, st);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ws + l.v_new, io->v_new, kvb, cudaMemcpyHostToDevice, st);
+      if (e != cudaSuccess) return HSA_ERR_CUDA;
+      out = reinterpret_cast<float*>(ws + l.out);
+      lse = io->lse ? reinterpret_cast<float*>(ws + l.lse) : nullptr;
+    }
     q = ws + l.q;
     kn = ws + l.k_new;
     vn = ws + l.v_new;
-    out = reinterpret_cast<float*>(ws + l.out);
-    lse = io->lse ? reinterpret_cast<float*>(ws + l.lse) : nullptr;
   }
   const void* kd = nullptr;
   const void* vd = nullptr;
@@ -464,7 +511,7 @@ int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
   rc = do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, bidx, nb, out, lse, ws,
                  l.att, st, true, sel_pages);
   if (rc != HSA_OK) return rc;
-  if (io->io_on_host) {
+  if (io->io_on_host && !direct_out) {
     e = cudaMemcpyAsync(io->out, out, (size_t)s.batch * s.hq * hsa::kHeadDim * 4,
                         cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess && io->lse)

@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <map>
+#include <mutex>
 #include <utility>
 
 namespace hsa {
@@ -156,13 +159,39 @@ __device__ __forceinline__ void grid_dep_launch() {
 // step overlap on an SM (the next one is launched while the previous one runs), and an SM
 // configured for a kernel with little shared memory could not take the next kernel's CTAs
 // until it drains.
+// The attributes are set once per (kernel, device) and raised when a launch needs more (a
+// cudaDeviceReset would drop them; the library never calls it).
+struct SmemAttrCache {
+  std::mutex mu;
+  std::map<std::pair<const void*, int>, size_t> bytes;  // dynamic bytes already allowed
+};
+inline SmemAttrCache& smem_attr_cache() {
+  static SmemAttrCache c;
+  return c;
+}
+
 template <typename Kernel>
 cudaError_t set_kernel_smem(Kernel kernel, size_t dynamic_bytes) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)dynamic_bytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              (int)cudaSharedmemCarveoutMaxShared);
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+  SmemAttrCache& c = smem_attr_cache();
+  {
+    std::lock_guard<std::mutex> g(c.mu);
+    const auto it = c.bytes.find(key);
+    if (it != c.bytes.end() && it->second >= dynamic_bytes) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)dynamic_bytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> g(c.mu);
+  size_t& have = c.bytes[key];
+  have = std::max(have, dynamic_bytes);
+  return cudaSuccess;
 }
 
 // Launch with (pdl) or without programmatic stream serialisation.

@@ -30,6 +30,11 @@ cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_ne
                              const int32_t* page_table, const int32_t* seq_lens, int* err,
                              cudaStream_t st, bool beside);
 
+// Copies q [B][Hq][128], k_new and v_new [B][Hkv][128] (bf16, 16-byte aligned, readable by
+// the device: mapped pinned host memory) into the device buffers dq, dk_new, dv_new.
+cudaError_t launch_stage_io(const Shape& s, const void* q, const void* k_new, const void* v_new,
+                            void* dq, void* dk_new, void* dv_new, int num_sms, cudaStream_t st);
+
 // ---- score.cu
 // block_max: [B][Hkv][max_pages]; tile_max (nullable): [B][Hkv][score_max_tiles], the max of
 // each 64-token tile, which the prune kernel uses as the chunk score when chunks are 64.

@@ -225,6 +225,49 @@ cudaError_t launch_key_codes(const Shape& s, const void* k_cache, const int32_t*
   return cudaGetLastError();
 }
 
+// The decode step's inputs (q, k_new, v_new), staged from mapped pinned host memory into
+// device buffers by 16-byte loads over the host link, four in flight per thread: one small
+// kernel instead of three copy-engine transfers.
+__global__ void __launch_bounds__(256) stage_io_kernel(const uint4* q, const uint4* kn,
+                                                       const uint4* vn, uint4* dq, uint4* dkn,
+                                                       uint4* dvn, int nq, int nkv) {
+  grid_dep_wait();  // the previous step's kernels may still read the staged copies
+  grid_dep_launch();
+  const int total = nq + 2 * nkv;
+  const int stride = gridDim.x * blockDim.x;
+  for (int i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int i = i0 + u * stride;
+      if (i < nq) v[u] = q[i];
+      else if (i < nq + nkv) v[u] = kn[i - nq];
+      else if (i < total) v[u] = vn[i - nq - nkv];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int i = i0 + u * stride;
+      if (i < nq) dq[i] = v[u];
+      else if (i < nq + nkv) dkn[i - nq] = v[u];
+      else if (i < total) dvn[i - nq - nkv] = v[u];
+    }
+  }
+}
+
+cudaError_t launch_stage_io(const Shape& s, const void* q, const void* k_new, const void* v_new,
+                            void* dq, void* dk_new, void* dv_new, int num_sms, cudaStream_t st) {
+  const int nq = s.batch * s.hq * kHeadDim * 2 / 16;
+  const int nkv = s.batch * s.hkv * kHeadDim * 2 / 16;
+  const int total = nq + 2 * nkv;
+  const int grid = std::max(1, std::min(num_sms, (total + 4 * 256 - 1) / (4 * 256)));
+  const cudaError_t e = set_kernel_smem(stage_io_kernel, 0);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(stage_io_kernel, dim3(grid), dim3(256), 0, st, true,
+                       static_cast<const uint4*>(q), static_cast<const uint4*>(k_new),
+                       static_cast<const uint4*>(v_new), static_cast<uint4*>(dq),
+                       static_cast<uint4*>(dk_new), static_cast<uint4*>(dv_new), nq, nkv);
+}
+
 cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_new,
                              void* k_cache, void* v_cache, int8_t* kq, const float* k_scale,
                              const int32_t* page_table, const int32_t* seq_lens, int* err,

@@ -58,6 +58,9 @@ class hsa_step_io(ctypes.Structure):
                 ("io_on_host", ctypes.c_int32)]
 
 
+_DIMS_CACHE: dict = {}  # field values -> their C struct (read-only to the library)
+
+
 @dataclasses.dataclass
 class Dims:
     batch: int
@@ -77,10 +80,17 @@ class Dims:
     kv_on_host: bool = False
 
     def c(self) -> hsa_dims:
-        return hsa_dims(self.batch, self.hq, self.hkv, self.head_dim, self.page_size,
-                        self.max_pages_per_seq, self.num_pages, self.chunk, self.block, self.k1,
-                        self.k2, self.sink, self.window, float(self.sm_scale),
-                        1 if self.kv_on_host else 0)
+        """The C struct, built once per set of field values (every call of a step passes it)."""
+        key = (self.batch, self.hq, self.hkv, self.head_dim, self.page_size,
+               self.max_pages_per_seq, self.num_pages, self.chunk, self.block, self.k1,
+               self.k2, self.sink, self.window, float(self.sm_scale),
+               1 if self.kv_on_host else 0)
+        c = _DIMS_CACHE.get(key)
+        if c is None:
+            if len(_DIMS_CACHE) > 256:
+                _DIMS_CACHE.clear()
+            c = _DIMS_CACHE[key] = hsa_dims(*key)
+        return c
 
 
 _LIB = None
