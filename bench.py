@@ -164,6 +164,7 @@ class Case:
 
     KERNELS = ("step", "append", "score", "prune", "attend", "dense")
     BURST = 10
+    REFRESH = 4
 
     def __init__(self, name: str, seed: int, device, dense: bool = True):
         import torch
@@ -237,6 +238,13 @@ class Case:
                                  self.k[r], self.v[r], self.kq[r], self.ks[r], self.pt,
                                  self.lens, self.block_idx, self.n_blocks, self.ws_step)
 
+    def reuse(self, r):
+        """A step that reuses the last whole step's selection (append + attend)."""
+        self.hsa.hsa_decode_step_reuse(self.d, self.q, self.k_new, self.v_new, self.out,
+                                       self.lse, self.k[r], self.v[r], self.kq[r], self.ks[r],
+                                       self.pt, self.lens, self.block_idx, self.n_blocks,
+                                       self.ws_step)
+
     def append(self, r):
         self.hsa.hsa_append_kv(self.d, self.k_new, self.v_new, self.k[r], self.v[r], self.kq[r],
                                self.ks[r], self.pt, self.lens)
@@ -274,6 +282,22 @@ class Case:
                 with torch.cuda.graph(g):
                     getattr(self, name)(r)
                 self.graphs[(name, r)] = g
+        # the decode loop: a whole step, then REFRESH - 1 steps reusing its selection
+        for r in range(2):
+            self.step(r)
+            self.reuse(r)
+        torch.cuda.synchronize()
+        for r in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.step(r)
+                for _ in range(self.REFRESH - 1):
+                    self.reuse(r)
+            self.graphs[("loop", r)] = g
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.reuse(r)
+            self.graphs[("reuse", r)] = g
         # per-kernel durations: BURST launches of one kernel in one graph, replicas
         # alternating (so that every launch of the scan reads data the previous one did not)
         self.burst = {}
@@ -437,6 +461,10 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
     barrier(world)
     _, step_ms = timed_steps(case, steps, ("step",), sampler)
     barrier(world)
+    # the decode loop (selection refreshed every REFRESH steps) and the reuse step alone
+    lsteps = max(3, min(steps // case.REFRESH, 500))
+    timed_steps(case, 3, ("loop", "reuse"))
+    lper, _ = timed_steps(case, lsteps, ("loop", "reuse"))
     # kernel breakdown: the average launch duration of each of the four kernels
     bsteps = max(3, min(steps // 10, 200))
     per = burst_times(case, names, bsteps)
@@ -454,6 +482,8 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
     res = {
         "case": case,
         "step_ms": step_ms,
+        "loop_step_ms": lper["loop"] / case.REFRESH,
+        "reuse_step_ms": lper["reuse"],
         "per_ms": per,
         "select_ms": sel_ms,
         "dense_ms": dper["dense"],
@@ -709,6 +739,12 @@ def main():
         "select_us": main_res["select_ms"] * 1e3,
         "dense_us": main_res["dense_ms"] * 1e3,
         "speedup_vs_dense": main_res["dense_ms"] / step_ms,
+        "decode_loop": {
+            "refresh_every": Case.REFRESH,
+            "us_per_step": main_res["loop_step_ms"] * 1e3,
+            "reuse_step_us": main_res["reuse_step_ms"] * 1e3,
+            "timing": "graph of one whole step + 3 steps reusing its selection, per step",
+        },
         "gbs": main_res["gbs"],
         "frac_of_peak": main_res["frac"],
         "bytes": main_res["bytes"],

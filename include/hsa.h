@@ -224,6 +224,20 @@ int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * A decode step that reuses an earlier step's selection (InfiniteHiP article, section
+ * "实现 7.24 倍的端到端解码加速": the pruning result is kept for several decode steps and
+ * refreshed every few): hsa_append_kv, then hsa_attend over the sink, the window and the
+ * kept blocks block_idx / n_blocks (device inputs, as written by a previous hsa_decode_step;
+ * required when k2 > 0), each clipped to the current candidate region [sink, N - window).
+ * No scoring and no pruning. Same io, workspace (HSA_OP_STEP) and errors as hsa_decode_step.
+ */
+int32_t hsa_decode_step_reuse(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
+                              void* v_cache, int8_t* kq, const float* k_scale,
+                              const int32_t* page_table, const int32_t* seq_lens,
+                              const int32_t* block_idx, const int32_t* n_blocks, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * hsa_select without a workspace, for callers that cannot allocate device memory: code
  * embedded in a host program that owns every device allocation through its own pool, or
  * that runs on a latency-critical path where cudaMalloc (which can synchronise the device)

@@ -239,6 +239,17 @@ int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, 
                                         buf, reinterpret_cast<int*>(ws), st, early));
 }
 
+// The outputs of a host-I/O step that were computed into the workspace: copied back.
+int32_t copy_outputs_back(const Shape& s, const hsa_step_io* io, const float* out,
+                          const float* lse, bool direct_out, cudaStream_t st) {
+  if (!io->io_on_host || direct_out) return HSA_OK;
+  cudaError_t e = cudaMemcpyAsync(io->out, out, (size_t)s.batch * s.hq * hsa::kHeadDim * 4,
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && io->lse)
+    e = cudaMemcpyAsync(io->lse, lse, (size_t)s.batch * s.hq * 4, cudaMemcpyDeviceToHost, st);
+  return e == cudaSuccess ? HSA_OK : HSA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -418,22 +429,28 @@ int32_t dense_decode(const hsa_dims* d, const void* q, const void* k_cache, cons
                    lse, ws, attend_layout(s, kErrBytes), as_stream(stream), false);
 }
 
-int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache, void* v_cache,
-                        int8_t* kq, const float* k_scale, const int32_t* page_table,
-                        const int32_t* seq_lens, int32_t* block_idx, int32_t* n_blocks,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+// The whole step (reuse = false) or its append + attend with a selection given by the
+// caller (reuse = true: block_idx / n_blocks are inputs).
+static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
+                                void* v_cache, int8_t* kq, const float* k_scale,
+                                const int32_t* page_table, const int32_t* seq_lens,
+                                int32_t* block_idx, int32_t* n_blocks, void* workspace,
+                                size_t workspace_bytes, void* stream, bool reuse) {
   Shape s;
-  int32_t rc = check_dims(d, s, true);
+  int32_t rc = check_dims(d, s, !reuse);
   if (rc != HSA_OK) return rc;
   if (!io || !io->q || !io->k_new || !io->v_new || !io->out || !k_cache || !v_cache || !kq ||
       !k_scale || !page_table || !seq_lens)
     return HSA_ERR_INVALID_ARG;
+  if (reuse && s.k2 > 0 && (!block_idx || !n_blocks)) return HSA_ERR_INVALID_ARG;
   if (!aligned(io->q, 16) || !aligned(io->k_new, 16) || !aligned(io->v_new, 16) ||
       !aligned(io->out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(kq, 16) || !aligned(k_scale, 16))
     return HSA_ERR_INVALID_ARG;
-  rc = check_prune_fits(s);
-  if (rc != HSA_OK) return rc;
+  if (!reuse) {
+    rc = check_prune_fits(s);
+    if (rc != HSA_OK) return rc;
+  }
   const StepLayout l = step_layout(s);
   rc = check_ws(s, workspace, workspace_bytes, l.end);
   if (rc != HSA_OK) return rc;
@@ -488,6 +505,17 @@ int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
   int32_t* bidx = block_idx ? block_idx : reinterpret_cast<int32_t*>(ws + l.block_idx);
   int32_t* nb = n_blocks ? n_blocks : reinterpret_cast<int32_t*>(ws + l.n_blocks);
   cudaError_t e;
+  if (reuse) {
+    // the new token first (the attend reads it among the window's tokens), then the attend
+    // over sink + window + the given kept blocks, clipped to the current candidate region
+    e = hsa::launch_append_kv(s, kn, vn, const_cast<void*>(kd), const_cast<void*>(vd), kq,
+                              k_scale, page_table, seq_lens, err, st, false);
+    if (e != cudaSuccess) return HSA_ERR_CUDA;
+    rc = do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks,
+                   out, lse, ws, l.att, st, false);
+    if (rc != HSA_OK) return rc;
+    return copy_outputs_back(s, io, out, lse, direct_out, st);
+  }
   // With a window of at least one token the new token (slot N - 1) is never a scored
   // candidate, so the append runs beside the scorer; with no window it goes first.
   const bool beside = s.window >= 1;
@@ -511,14 +539,25 @@ int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
   rc = do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, bidx, nb, out, lse, ws,
                  l.att, st, true, sel_pages);
   if (rc != HSA_OK) return rc;
-  if (io->io_on_host && !direct_out) {
-    e = cudaMemcpyAsync(io->out, out, (size_t)s.batch * s.hq * hsa::kHeadDim * 4,
-                        cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess && io->lse)
-      e = cudaMemcpyAsync(io->lse, lse, (size_t)s.batch * s.hq * 4, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return HSA_ERR_CUDA;
-  }
-  return HSA_OK;
+  return copy_outputs_back(s, io, out, lse, direct_out, st);
+}
+
+int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache, void* v_cache,
+                        int8_t* kq, const float* k_scale, const int32_t* page_table,
+                        const int32_t* seq_lens, int32_t* block_idx, int32_t* n_blocks,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_step_impl(d, io, k_cache, v_cache, kq, k_scale, page_table, seq_lens, block_idx,
+                          n_blocks, workspace, workspace_bytes, stream, false);
+}
+
+int32_t hsa_decode_step_reuse(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
+                              void* v_cache, int8_t* kq, const float* k_scale,
+                              const int32_t* page_table, const int32_t* seq_lens,
+                              const int32_t* block_idx, const int32_t* n_blocks, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return decode_step_impl(d, io, k_cache, v_cache, kq, k_scale, page_table, seq_lens,
+                          const_cast<int32_t*>(block_idx), const_cast<int32_t*>(n_blocks),
+                          workspace, workspace_bytes, stream, true);
 }
 
 int32_t hsa_read_device_error(void* workspace, void* stream, int32_t* code) {

@@ -35,7 +35,7 @@ HSA_OP_STEP = 4
 EXPORTS = (
     "hsa_workspace_bytes", "hsa_status_string", "hsa_quantize_keys", "hsa_append_kv",
     "hsa_score_blocks", "hsa_prune", "hsa_select", "hsa_attend", "dense_decode",
-    "hsa_decode_step", "hsa_read_device_error", "hsa_select_noalloc",
+    "hsa_decode_step", "hsa_decode_step_reuse", "hsa_read_device_error", "hsa_select_noalloc",
 )
 
 
@@ -119,6 +119,8 @@ def load(path: Optional[str] = None):
         "dense_decode": (I32, [D, P, P, P, P, P, P, P, P, SZ, P]),
         "hsa_decode_step": (I32, [D, ctypes.POINTER(hsa_step_io), P, P, P, P, P, P, P, P, P,
                                   SZ, P]),
+        "hsa_decode_step_reuse": (I32, [D, ctypes.POINTER(hsa_step_io), P, P, P, P, P, P, P, P,
+                                        P, SZ, P]),
         "hsa_read_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
         "hsa_select_noalloc": (I32, [D, P, P, P, P, P, P, P, P, P, P]),
     }
@@ -240,6 +242,18 @@ def hsa_decode_step(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_
     cd = d.c()
     io = hsa_step_io(_p(q), _p(k_new), _p(v_new), _p(out), _p(lse), 1 if io_on_host else 0)
     _check("hsa_decode_step", load().hsa_decode_step(
+        ctypes.byref(cd), ctypes.byref(io), _p(k_cache), _p(v_cache), _p(kq), _p(k_scale),
+        _p(page_table), _p(seq_lens), _p(block_idx), _p(n_blocks), _p(ws), ws.numel(),
+        _stream(stream)))
+
+
+def hsa_decode_step_reuse(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_scale,
+                          page_table, seq_lens, block_idx, n_blocks, ws, io_on_host: bool = False,
+                          stream=None) -> None:
+    """Append + attend with the selection block_idx / n_blocks of an earlier step."""
+    cd = d.c()
+    io = hsa_step_io(_p(q), _p(k_new), _p(v_new), _p(out), _p(lse), 1 if io_on_host else 0)
+    _check("hsa_decode_step_reuse", load().hsa_decode_step_reuse(
         ctypes.byref(cd), ctypes.byref(io), _p(k_cache), _p(v_cache), _p(kq), _p(k_scale),
         _p(page_table), _p(seq_lens), _p(block_idx), _p(n_blocks), _p(ws), ws.numel(),
         _stream(stream)))

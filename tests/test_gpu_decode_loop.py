@@ -1,0 +1,85 @@
+"""A decode loop over several steps: a whole step (scoring and both pruning modules) every
+`refresh` steps, and between them steps that reuse that selection (append + attend only),
+as the InfiniteHiP article's decoding reuses its pruning results for several steps. Every
+step is checked against the oracle on the cache as it stands after that step's append:
+codes and selections bit-exact, outputs within the tolerance of the attention tests."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+import oracle
+from kv_cache_int8_gb300 import hsa
+from kv_cache_int8_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _clone(t):
+    return t.clone().pin_memory() if t.device.type == "cpu" else t.clone()
+
+
+@pytest.mark.parametrize("refresh,on_host", [(3, False), (2, True), (1, False)])
+def test_decode_loop_with_selection_reuse(refresh, on_host):
+    steps = 6
+    cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None,
+                              context_range=(3000, 6000), batch=2, hq=8, hkv=2, k1=12, k2=10,
+                              sink=32, window=96, paged_permuted=True)
+    wl = W.make_workload(cfg, seed=77 + refresh, host_pinned=on_host)
+    hd, od = H.dims_pair(wl)
+    dwl = H.to_cuda(wl)
+    dev = torch.device("cuda")
+    B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
+    # the caches are sized for the final lengths; the loop starts `steps` tokens earlier
+    start = wl["seq_lens"] - steps
+    pt = wl["page_table"].numpy()
+    kc, vc = _clone(dwl["k_cache"]), _clone(dwl["v_cache"])
+    kq = torch.zeros(kc.shape, dtype=torch.int8, device=dev)
+    k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
+    hsa.hsa_quantize_keys(hd, kc, dwl["page_table"], start.to(dev), 0, 0, kq, k_scale,
+                          hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
+    k_host = W.to_numpy_bits(wl["k_cache"]).copy()
+    v_host = W.to_numpy_bits(wl["v_cache"]).copy()
+    kq_o, sc_o = oracle.quantize_keys(od, k_host, pt, start.numpy())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(k_scale.cpu().numpy(), sc_o)
+
+    gen = torch.Generator(device="cpu").manual_seed(1234 + refresh)
+    ws = hsa.workspace(hd, hsa.HSA_OP_STEP)
+    bidx = torch.full((B, Hkv, cfg.k2), -7, dtype=torch.int32, device=dev)
+    nb = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+    sel = None
+    for i in range(steps):
+        lens = start + 1 + i
+        q = torch.randn((B, Hq, 128), generator=gen).to(torch.bfloat16)
+        k_new = torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16)
+        v_new = torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16)
+        out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
+        lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev)
+        args = (hd, q.to(dev), k_new.to(dev), v_new.to(dev), out, lse, kc, vc, kq, k_scale,
+                dwl["page_table"], lens.to(dev), bidx, nb, ws)
+        full = i % refresh == 0
+        (hsa.hsa_decode_step if full else hsa.hsa_decode_step_reuse)(*args)
+        torch.cuda.synchronize()
+        assert hsa.hsa_read_device_error(ws) == 0
+        # oracle: the same append on a host copy, codes with the stored scales
+        kb, vb = W.to_numpy_bits(k_new), W.to_numpy_bits(v_new)
+        for b in range(B):
+            n = int(lens[b])
+            k_host[pt[b, (n - 1) // 16], :, (n - 1) % 16] = kb[b]
+            v_host[pt[b, (n - 1) // 16], :, (n - 1) % 16] = vb[b]
+        np.testing.assert_array_equal(W.to_numpy_bits(kc.cpu()), k_host)
+        np.testing.assert_array_equal(W.to_numpy_bits(vc.cpu()), v_host)
+        kq_o = oracle.quantize_append(od, k_host, pt, lens.numpy(), -1, sc_o, kq_o)
+        np.testing.assert_array_equal(kq.cpu().numpy(), kq_o)
+        qb = W.to_numpy_bits(q)
+        if full:
+            sel = oracle.select(od, qb, sc_o, kq_o, pt, lens.numpy())
+            np.testing.assert_array_equal(nb.cpu().numpy(), sel["n_blocks"])
+            np.testing.assert_array_equal(bidx.cpu().numpy(), sel["block_idx"])
+        out_o, lse_o = oracle.attend(od, qb, k_host, v_host, pt, lens.numpy(), sel["block_idx"],
+                                     sel["n_blocks"])
+        H.assert_close(out.cpu().numpy(), out_o, f"step {i} output")
+        np.testing.assert_allclose(lse.cpu().numpy(), lse_o, atol=2e-4, rtol=1e-5)
