@@ -165,6 +165,7 @@ class Case:
     KERNELS = ("step", "append", "score", "prune", "attend", "dense")
     BURST = 10
     REFRESH = 4
+    CACHE_SLOTS = 8192  # GPU block cache of the offloaded case: 64 MiB of K/V blocks
 
     def __init__(self, name: str, seed: int, device, dense: bool = True):
         import torch
@@ -174,6 +175,8 @@ class Case:
         self.cfg = W.CONFIGS[name]
         cfg = self.cfg
         self.kernels = self.KERNELS if dense else tuple(k for k in self.KERNELS if k != "dense")
+        if cfg.kv_on_host:  # the step and the attention through the GPU block cache too
+            self.kernels = self.kernels + ("step_cached", "attend_cached")
         # offloaded K/V: one pinned host copy (both "replicas" alias it; steps are separated by
         # an L2 flush instead, see timed_steps)
         wl = W.make_workload(cfg, seed=seed, device=str(device), host_pinned=cfg.kv_on_host)
@@ -220,6 +223,10 @@ class Case:
         self.ws_att = hsa.workspace(d, hsa.HSA_OP_ATTEND)
         self.ws_den = hsa.workspace(d, hsa.HSA_OP_DENSE)
         self.ws_step = hsa.workspace(d, hsa.HSA_OP_STEP)
+        if cfg.kv_on_host:
+            self.cache_capacity = self.CACHE_SLOTS
+            self.cache = hsa.block_cache(d, self.cache_capacity)
+            self.ws_cached = hsa.workspace(d, hsa.HSA_OP_CACHED)
         self.bm = torch.zeros((B, Hkv, d.max_pages_per_seq), dtype=torch.int32, device=device)
         self.tm = torch.zeros((B, Hkv, (d.max_pages_per_seq + 3) // 4), dtype=torch.int32,
                               device=device)
@@ -237,6 +244,17 @@ class Case:
         self.hsa.hsa_decode_step(self.d, self.q, self.k_new, self.v_new, self.out, self.lse,
                                  self.k[r], self.v[r], self.kq[r], self.ks[r], self.pt,
                                  self.lens, self.block_idx, self.n_blocks, self.ws_step)
+
+    def step_cached(self, r):
+        self.hsa.hsa_decode_step_cached(self.d, self.q, self.k_new, self.v_new, self.out,
+                                        self.lse, self.k[r], self.v[r], self.kq[r], self.ks[r],
+                                        self.pt, self.lens, self.block_idx, self.n_blocks,
+                                        self.cache, self.cache_capacity, self.ws_step)
+
+    def attend_cached(self, r):
+        self.hsa.hsa_attend_cached(self.d, self.q, self.k[r], self.v[r], self.pt, self.lens,
+                                   self.block_idx, self.n_blocks, self.cache,
+                                   self.cache_capacity, self.out, self.lse, self.ws_cached)
 
     def reuse(self, r):
         """A step that reuses the last whole step's selection (append + attend)."""
@@ -465,6 +483,10 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
     lsteps = max(3, min(steps // case.REFRESH, 500))
     timed_steps(case, 3, ("loop", "reuse"))
     lper, _ = timed_steps(case, lsteps, ("loop", "reuse"))
+    cached = {}
+    if getattr(case, "cache", None) is not None:
+        timed_steps(case, 3, ("step_cached", "attend_cached"))
+        cached, _ = timed_steps(case, max(3, min(steps, 300)), ("step_cached", "attend_cached"))
     # kernel breakdown: the average launch duration of each of the four kernels
     bsteps = max(3, min(steps // 10, 200))
     per = burst_times(case, names, bsteps)
@@ -472,7 +494,8 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
         dper = burst_times(case, ("dense",), max(3, bsteps // 4))
     else:
         dper = {"dense": float("nan")}
-    for w in (case.ws_step, case.ws_sel, case.ws_att, case.ws_den):
+    for w in (case.ws_step, case.ws_sel, case.ws_att, case.ws_den) + (
+            (case.ws_cached,) if getattr(case, "cache", None) is not None else ()):
         code = hsa.hsa_read_device_error(w)
         assert code == 0, f"device error word {code}"
     recall = torch.exp(case.lse.double() - case.lse_d.double())  # restriction identity
@@ -484,6 +507,7 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
         "step_ms": step_ms,
         "loop_step_ms": lper["loop"] / case.REFRESH,
         "reuse_step_ms": lper["reuse"],
+        "cached_ms": cached,
         "per_ms": per,
         "select_ms": sel_ms,
         "dense_ms": dper["dense"],
@@ -654,7 +678,10 @@ def main():
             torch.cuda.empty_cache()
             extra[name] = {
                 "us_per_step": r["step_ms"] * 1e3, "score_us": r["per_ms"]["score"] * 1e3,
-                **({"host_link_copy_gbs": host_link_copy_gbs(device)} if not dense else {}),
+                **({"host_link_copy_gbs": host_link_copy_gbs(device),
+                    "us_per_step_block_cache": r["cached_ms"]["step_cached"] * 1e3,
+                    "attend_block_cache_us": r["cached_ms"]["attend_cached"] * 1e3,
+                    "block_cache_slots": Case.CACHE_SLOTS} if not dense else {}),
                 "prune_us": r["per_ms"]["prune"] * 1e3, "attend_us": r["per_ms"]["attend"] * 1e3,
                 "dense_us": r["dense_ms"] * 1e3 if dense else None,
                 "score_gbs": r["gbs"]["score"],

@@ -101,7 +101,8 @@ enum hsa_op {
   HSA_OP_SELECT = 1,
   HSA_OP_ATTEND = 2,
   HSA_OP_DENSE = 3,
-  HSA_OP_STEP = 4
+  HSA_OP_STEP = 4,
+  HSA_OP_CACHED = 5
 };
 
 /* Workspace bytes `op` needs for descriptor `d` (0 if `d` is invalid). */
@@ -236,6 +237,50 @@ int32_t hsa_decode_step_reuse(const hsa_dims* d, const hsa_step_io* io, void* k_
                               const int32_t* page_table, const int32_t* seq_lens,
                               const int32_t* block_idx, const int32_t* n_blocks, void* workspace,
                               size_t workspace_bytes, void* stream);
+
+/*
+ * GPU block cache in front of K/V in host memory (InfiniteHiP article, section "实现 7.24 倍
+ * 的端到端解码加速": the GPU keeps a cache of recently used KV blocks with an LRU policy and
+ * the rest stays in host memory). One caller-owned device buffer of hsa_block_cache_bytes
+ * bytes, 256-byte aligned and zero-filled before its first use, holds up to `capacity`
+ * (page, kv head) blocks of bf16 K and V (8 KiB each) and their bookkeeping; it belongs to
+ * one descriptor's cache (same num_pages, hkv) and must not be used by two calls that may
+ * overlap on the GPU. capacity: at least batch * hkv * (ceil(sink / 16) + ceil(window / 16)
+ * + 1 + k2) (one call's blocks) and at most 32768; otherwise hsa_block_cache_bytes returns 0
+ * and the calls HSA_ERR_INVALID_ARG / HSA_ERR_UNSUPPORTED.
+ *
+ * Each call: its blocks (sink pages, window pages, kept blocks of every sequence and kv head)
+ * are looked up; a hit counts as a use; every miss takes the slot, among those this call
+ * does not use, that was used longest ago (ties: the lower slot), and is copied in over the
+ * host link; the page that holds each sequence's last token is copied again on every call
+ * (the append writes it). The host K/V of pages held in the cache must not change otherwise.
+ * Two sequences may not share a page (reported as HSA_ERR_DEVICE_CHECK through the error
+ * word).
+ */
+size_t hsa_block_cache_bytes(const hsa_dims* d, int32_t capacity);
+
+/*
+ * hsa_attend for K/V in pinned host memory (d->kv_on_host = 1, mapped) through the block
+ * cache: the attention itself reads the cached copies in device memory. Needs the
+ * HSA_OP_CACHED workspace. Results equal hsa_attend's within floating-point rounding.
+ */
+int32_t hsa_attend_cached(const hsa_dims* d, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* page_table,
+                          const int32_t* seq_lens, const int32_t* block_idx,
+                          const int32_t* n_blocks, void* block_cache, int32_t capacity,
+                          float* out, float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
+ * hsa_decode_step for K/V in pinned host memory with its attention through the block cache
+ * (see hsa_attend_cached). Needs the HSA_OP_STEP workspace.
+ */
+int32_t hsa_decode_step_cached(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
+                               void* v_cache, int8_t* kq, const float* k_scale,
+                               const int32_t* page_table, const int32_t* seq_lens,
+                               int32_t* block_idx, int32_t* n_blocks, void* block_cache,
+                               int32_t capacity, void* workspace, size_t workspace_bytes,
+                               void* stream);
 
 /*
  * hsa_select without a workspace, for callers that cannot allocate device memory: code

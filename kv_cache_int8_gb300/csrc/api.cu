@@ -81,9 +81,64 @@ AttendLayout attend_layout(const Shape& s, size_t base) {
   return l;
 }
 size_t attend_ws(const Shape& s) { return attend_layout(s, kErrBytes).end; }
+
+// Per-call scratch of the block cache: seg_slot [B][Hkv][stride], the fill list, its count.
+struct CacheScratch {
+  size_t seg_slot, fill, n_fill, end;
+};
+CacheScratch cache_scratch(const Shape& s, size_t base) {
+  const size_t F = (size_t)s.batch * s.hkv * hsa::block_cache_seg_stride(s);
+  CacheScratch c;
+  c.seg_slot = base;
+  c.fill = c.seg_slot + up(F * 4);
+  c.n_fill = c.fill + up(F * 16);
+  c.end = c.n_fill + kAlign;
+  return c;
+}
+size_t cached_ws(const Shape& s) {
+  return cache_scratch(s, attend_layout(s, kErrBytes).end).end;
+}
+
+// The block cache buffer: header, slot_of [num_pages * hkv], slot_key / slot_stamp
+// [capacity], data [capacity][8 KiB].
+constexpr int kMaxCacheSlots = 32768;
+struct CacheLayout {
+  size_t slot_of, slot_key, slot_stamp, data, end;
+};
+CacheLayout cache_layout(const Shape& s, int capacity) {
+  CacheLayout l;
+  l.slot_of = kAlign;
+  l.slot_key = l.slot_of + up((size_t)s.num_pages * s.hkv * 4);
+  l.slot_stamp = l.slot_key + up((size_t)capacity * 4);
+  l.data = l.slot_stamp + up((size_t)capacity * 4);
+  l.end = l.data + (size_t)capacity * 2 * hsa::kBlockBytesBf16;
+  return l;
+}
+// The capacity must hold one call's working set (every segment of every (sequence, kv
+// head)) and fit the plan's shared memory.
+int32_t check_cache_capacity(const Shape& s, int capacity) {
+  if (capacity < s.batch * s.hkv * hsa::block_cache_seg_stride(s)) return HSA_ERR_INVALID_ARG;
+  if (capacity > kMaxCacheSlots) return HSA_ERR_UNSUPPORTED;
+  if (hsa::block_cache_plan_smem(s, capacity) > 227 * 1024) return HSA_ERR_UNSUPPORTED;
+  return HSA_OK;
+}
+hsa::BlockCache block_cache_at(const Shape& s, void* buf, int capacity) {
+  const CacheLayout l = cache_layout(s, capacity);
+  char* p = static_cast<char*>(buf);
+  hsa::BlockCache c;
+  c.header = reinterpret_cast<int32_t*>(p);
+  c.slot_of = reinterpret_cast<int32_t*>(p + l.slot_of);
+  c.slot_key = reinterpret_cast<int32_t*>(p + l.slot_key);
+  c.slot_stamp = reinterpret_cast<int32_t*>(p + l.slot_stamp);
+  c.data = p + l.data;
+  c.capacity = capacity;
+  return c;
+}
+
 struct StepLayout {
   size_t block_max, tile_max, block_idx, n_blocks, sel_pages, q, k_new, v_new, out, lse;
   AttendLayout att;
+  CacheScratch cache;
   size_t end;
 };
 StepLayout step_layout(const Shape& s) {
@@ -99,7 +154,8 @@ StepLayout step_layout(const Shape& s) {
   l.out = l.v_new + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 2);
   l.lse = l.out + up((size_t)s.batch * s.hq * hsa::kHeadDim * 4);
   l.att = attend_layout(s, l.lse + up((size_t)s.batch * s.hq * 4));
-  l.end = l.att.end;
+  l.cache = cache_scratch(s, l.att.end);
+  l.end = l.cache.end;
   return l;
 }
 
@@ -239,6 +295,37 @@ int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, 
                                         buf, reinterpret_cast<int*>(ws), st, early));
 }
 
+// The attention over K/V in host memory through the block cache: plan (lookups, LRU victims),
+// fill (the misses copied in over the host link), then the HBM attention reading the slots.
+// kd / vd: device aliases of the host K/V.
+int32_t do_attend_cached(const Shape& s, const void* q, const void* kd, const void* vd,
+                         const int32_t* pt, const int32_t* lens, const int32_t* bidx,
+                         const int32_t* nb, float* out, float* lse, char* ws,
+                         const AttendLayout& l, const CacheScratch& cs, void* cache,
+                         int capacity, cudaStream_t st) {
+  int* err = reinterpret_cast<int*>(ws);
+  const hsa::BlockCache c = block_cache_at(s, cache, capacity);
+  int32_t* seg_slot = reinterpret_cast<int32_t*>(ws + cs.seg_slot);
+  void* fill = ws + cs.fill;
+  int32_t* n_fill = reinterpret_cast<int32_t*>(ws + cs.n_fill);
+  if (hsa::launch_cache_plan(s, lens, pt, bidx, nb, c, seg_slot, fill, n_fill, err, st) !=
+      cudaSuccess)
+    return HSA_ERR_CUDA;
+  if (hsa::launch_cache_fill(s, c, fill, n_fill, kd, vd, err, num_sms(), st) != cudaSuccess)
+    return HSA_ERR_CUDA;
+  hsa::AttendBuffers buf;
+  buf.counters = reinterpret_cast<int*>(ws + l.counters);
+  buf.part_ml = reinterpret_cast<float*>(ws + l.part_ml);
+  buf.part_o = reinterpret_cast<float*>(ws + l.part_o);
+  buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(s, false, false, num_sms()));
+  buf.seg_slots = seg_slot;
+  buf.seg_stride = hsa::block_cache_seg_stride(s);
+  buf.cache_capacity = capacity;
+  const char* data = static_cast<const char*>(c.data);
+  return cuda_status(hsa::launch_attend(s, false, false, q, data, data + hsa::kBlockBytesBf16, pt,
+                                        lens, bidx, nb, out, lse, buf, err, st, false));
+}
+
 // The outputs of a host-I/O step that were computed into the workspace: copied back.
 int32_t copy_outputs_back(const Shape& s, const hsa_step_io* io, const float* out,
                           const float* lse, bool direct_out, cudaStream_t st) {
@@ -264,6 +351,7 @@ size_t hsa_workspace_bytes(const hsa_dims* d, int32_t op) {
     case HSA_OP_ATTEND:
     case HSA_OP_DENSE: return attend_ws(s);
     case HSA_OP_STEP: return step_layout(s).end;
+    case HSA_OP_CACHED: return cached_ws(s);
     default: return 0;
   }
 }
@@ -435,10 +523,16 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
                                 void* v_cache, int8_t* kq, const float* k_scale,
                                 const int32_t* page_table, const int32_t* seq_lens,
                                 int32_t* block_idx, int32_t* n_blocks, void* workspace,
-                                size_t workspace_bytes, void* stream, bool reuse) {
+                                size_t workspace_bytes, void* stream, bool reuse,
+                                void* block_cache = nullptr, int32_t capacity = 0) {
   Shape s;
   int32_t rc = check_dims(d, s, !reuse);
   if (rc != HSA_OK) return rc;
+  if (block_cache != nullptr) {
+    if (!d->kv_on_host || !aligned(block_cache, kAlign)) return HSA_ERR_INVALID_ARG;
+    rc = check_cache_capacity(s, capacity);
+    if (rc != HSA_OK) return rc;
+  }
   if (!io || !io->q || !io->k_new || !io->v_new || !io->out || !k_cache || !v_cache || !kq ||
       !k_scale || !page_table || !seq_lens)
     return HSA_ERR_INVALID_ARG;
@@ -511,8 +605,10 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
     e = hsa::launch_append_kv(s, kn, vn, const_cast<void*>(kd), const_cast<void*>(vd), kq,
                               k_scale, page_table, seq_lens, err, st, false);
     if (e != cudaSuccess) return HSA_ERR_CUDA;
-    rc = do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks,
-                   out, lse, ws, l.att, st, false);
+    rc = block_cache ? do_attend_cached(s, q, kd, vd, page_table, seq_lens, block_idx, n_blocks,
+                                        out, lse, ws, l.att, l.cache, block_cache, capacity, st)
+                     : do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens,
+                                 block_idx, n_blocks, out, lse, ws, l.att, st, false);
     if (rc != HSA_OK) return rc;
     return copy_outputs_back(s, io, out, lse, direct_out, st);
   }
@@ -536,10 +632,61 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
   e = hsa::launch_prune(s, seq_lens, bm, tm, nullptr, nullptr, bidx, nb, page_table, sel_pages,
                         err, st);
   if (e != cudaSuccess) return HSA_ERR_CUDA;
-  rc = do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, bidx, nb, out, lse, ws,
-                 l.att, st, true, sel_pages);
+  rc = block_cache ? do_attend_cached(s, q, kd, vd, page_table, seq_lens, bidx, nb, out, lse, ws,
+                                      l.att, l.cache, block_cache, capacity, st)
+                   : do_attend(d, s, false, q, k_cache, v_cache, page_table, seq_lens, bidx, nb,
+                               out, lse, ws, l.att, st, true, sel_pages);
   if (rc != HSA_OK) return rc;
   return copy_outputs_back(s, io, out, lse, direct_out, st);
+}
+
+int32_t hsa_decode_step_cached(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
+                               void* v_cache, int8_t* kq, const float* k_scale,
+                               const int32_t* page_table, const int32_t* seq_lens,
+                               int32_t* block_idx, int32_t* n_blocks, void* block_cache,
+                               int32_t capacity, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (block_cache == nullptr) return HSA_ERR_INVALID_ARG;
+  return decode_step_impl(d, io, k_cache, v_cache, kq, k_scale, page_table, seq_lens, block_idx,
+                          n_blocks, workspace, workspace_bytes, stream, false, block_cache,
+                          capacity);
+}
+
+size_t hsa_block_cache_bytes(const hsa_dims* d, int32_t capacity) {
+  Shape s;
+  if (check_dims(d, s, false) != HSA_OK) return 0;
+  if (check_cache_capacity(s, capacity) != HSA_OK) return 0;
+  return cache_layout(s, capacity).end;
+}
+
+int32_t hsa_attend_cached(const hsa_dims* d, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* page_table,
+                          const int32_t* seq_lens, const int32_t* block_idx,
+                          const int32_t* n_blocks, void* block_cache, int32_t capacity,
+                          float* out, float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  Shape s;
+  int32_t rc = check_dims(d, s, false);
+  if (rc != HSA_OK) return rc;
+  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !out || !block_cache ||
+      (s.k2 > 0 && (!block_idx || !n_blocks)))
+    return HSA_ERR_INVALID_ARG;
+  if (!d->kv_on_host || !aligned(q, 16) || !aligned(out, 16) || !aligned(block_cache, kAlign))
+    return HSA_ERR_INVALID_ARG;
+  rc = check_cache_capacity(s, capacity);
+  if (rc != HSA_OK) return rc;
+  rc = check_ws(s, workspace, workspace_bytes, cached_ws(s));
+  if (rc != HSA_OK) return rc;
+  const void* kd = nullptr;
+  const void* vd = nullptr;
+  rc = kv_pointer(d, k_cache, &kd);
+  if (rc != HSA_OK) return rc;
+  rc = kv_pointer(d, v_cache, &vd);
+  if (rc != HSA_OK) return rc;
+  char* ws = static_cast<char*>(workspace);
+  const AttendLayout l = attend_layout(s, kErrBytes);
+  return do_attend_cached(s, q, kd, vd, page_table, seq_lens, block_idx, n_blocks, out, lse, ws,
+                          l, cache_scratch(s, l.end), block_cache, capacity, as_stream(stream));
 }
 
 int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache, void* v_cache,

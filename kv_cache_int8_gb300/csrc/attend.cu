@@ -79,6 +79,9 @@ struct AttArgs {
   const int32_t* block_idx;
   const int32_t* n_blocks;
   const int32_t* sel_pages;  // nullable: page of each kept block, beside block_idx
+  const int32_t* seg_slots;  // nullable: block-cache slot of every segment (then k / v point
+                             // at the cache's K and V halves and num_pages is its capacity)
+  int seg_stride;
   float* out;
   float* lse;
   float* part_ml;
@@ -642,18 +645,21 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
       int k = 0, t0 = 0, t1 = 0, page = -1;
       if (jb + lane < jend) {
         const int i = first + (jb + lane) * stride;
+        const size_t sbase = ((size_t)b * a.hkv + h) * a.seg_stride;
         if (i < n_sw) {
           segment_at(S, i, a.sink, k, t0, t1);
-          if (t0 < t1) page = a.page_table[(size_t)b * a.max_pages + k];
+          if (t0 < t1)
+            page = a.seg_slots ? a.seg_slots[sbase + i] : a.page_table[(size_t)b * a.max_pages + k];
         } else {
           // a kept block: its id and (when given) its page are read in the same round trip
           // as the count of kept blocks (both lists hold K2 entries; r < K2)
           const int r = i - n_sw;
           const size_t at = ((size_t)b * a.hkv + h) * a.k2 + r;
           const int kk = a.block_idx[at];
-          const int pp = a.sel_pages ? a.sel_pages[at] : -1;
+          const int pp = a.seg_slots ? a.seg_slots[sbase + i] : (a.sel_pages ? a.sel_pages[at] : -1);
           kept_segment(S, r, kk, a.sink, k, t0, t1);
-          if (t0 < t1) page = a.sel_pages ? pp : a.page_table[(size_t)b * a.max_pages + k];
+          if (t0 < t1)
+            page = (a.seg_slots || a.sel_pages) ? pp : a.page_table[(size_t)b * a.max_pages + k];
         }
         if (t0 < t1 && (page < 0 || page >= a.num_pages)) {
           set_error(a.err, kDevErrCheck);
@@ -675,7 +681,9 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
           } else {
             meta[s] = make_int4(kq, t0q, t1q, 0);
             if (pq >= 0) {
-              const size_t off = ((size_t)pq * a.hkv + h) * kPage * kHeadDim;
+              // a page of the cache, or one slot (K block then V block) of the block cache
+              const size_t off = a.seg_slots ? (size_t)pq * (2 * kPage * kHeadDim)
+                                             : ((size_t)pq * a.hkv + h) * kPage * kHeadDim;
               mbar_arrive_expect_tx(&full[s], kSlotBytes);
               bulk_load_hint(ring + s * kSlotBytes, a.k + off, kBlockBytesBf16, &full[s], policy);
               bulk_load_hint(ring + s * kSlotBytes + kBlockBytesBf16, a.v + off, kBlockBytesBf16,
@@ -830,6 +838,41 @@ __global__ void __launch_bounds__(kHostThreads, 3) attend_host_kernel(const AttA
   finish<G>(a, st, sc, b, h, split, red);
 }
 
+// ---------------------------------------------------------- block-cache fill
+
+// One warp per fill entry (slot, page, head): the 4 KiB K block and the 4 KiB V block are
+// read from host memory (each warp load a contiguous 512-byte span) into the slot.
+__global__ void __launch_bounds__(256) cache_fill_kernel(const int4* fill, const int32_t* n_fill,
+                                                         const uint8_t* k_host,
+                                                         const uint8_t* v_host, uint8_t* data,
+                                                         int hkv, int num_pages, int capacity,
+                                                         int* err) {
+  grid_dep_wait();  // the plan comes from the previous kernel
+  grid_dep_launch();
+  const int n = *n_fill;
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); j < n; j += nwarps) {
+    const int4 e = fill[j];
+    if (e.x < 0 || e.x >= capacity || e.y < 0 || e.y >= num_pages || e.z < 0 || e.z >= hkv) {
+      if (lane == 0) set_error(err, kDevErrCheck);
+      continue;
+    }
+    const size_t src = ((size_t)e.y * hkv + e.z) * kBlockBytesBf16;
+    uint8_t* dst = data + (size_t)e.x * kSlotBytes;
+    uint4 r[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) r[u] = ldg128_nc(k_host + src + u * 512 + lane * 16);
+#pragma unroll
+    for (int u = 0; u < 8; u++) *reinterpret_cast<uint4*>(dst + u * 512 + lane * 16) = r[u];
+#pragma unroll
+    for (int u = 0; u < 8; u++) r[u] = ldg128_nc(v_host + src + u * 512 + lane * 16);
+#pragma unroll
+    for (int u = 0; u < 8; u++)
+      *reinterpret_cast<uint4*>(dst + kBlockBytesBf16 + u * 512 + lane * 16) = r[u];
+  }
+}
+
 template <int W, int NS>
 constexpr size_t tma_smem() {
   // the merge area ((W + 1) * G * 128 + 8 floats) fits in the ring
@@ -881,6 +924,17 @@ int attend_splits(const Shape& s, bool dense, bool host, int num_sms) {
   return (int)std::max<long long>(1, std::min<long long>(want, kMaxSplits));
 }
 
+cudaError_t launch_cache_fill(const Shape& s, const BlockCache& c, const void* fill,
+                              const int32_t* n_fill, const void* k_host, const void* v_host,
+                              int* err, int num_sms, cudaStream_t st) {
+  const cudaError_t e = set_kernel_smem(cache_fill_kernel, 0);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(cache_fill_kernel, dim3(2 * num_sms), dim3(256), 0, st, true,
+                       static_cast<const int4*>(fill), n_fill,
+                       static_cast<const uint8_t*>(k_host), static_cast<const uint8_t*>(v_host),
+                       static_cast<uint8_t*>(c.data), s.hkv, s.num_pages, c.capacity, err);
+}
+
 cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
                           const void* k_cache, const void* v_cache, const int32_t* page_table,
                           const int32_t* seq_lens, const int32_t* block_idx,
@@ -896,6 +950,8 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
   a.block_idx = block_idx;
   a.n_blocks = n_blocks;
   a.sel_pages = buf.sel_pages;
+  a.seg_slots = buf.seg_slots;
+  a.seg_stride = buf.seg_stride;
   a.out = out;
   a.lse = lse;
   a.part_ml = buf.part_ml;
@@ -904,7 +960,7 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
   a.err = err;
   a.hkv = s.hkv;
   a.max_pages = s.max_pages;
-  a.num_pages = s.num_pages;
+  a.num_pages = buf.seg_slots ? buf.cache_capacity : s.num_pages;
   a.k2 = s.k2;
   a.sink = s.sink;
   a.window = s.window;

@@ -54,6 +54,25 @@ cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t*
 int prune_max_chunks();
 size_t prune_smem_bytes(const Shape& s);
 
+// The GPU block cache: device arrays in one caller-owned, zero-initialised buffer.
+struct BlockCache {
+  int32_t* header;      // [0]: step counter
+  int32_t* slot_of;     // [num_pages * hkv]: slot + 1, 0 when absent
+  int32_t* slot_key;    // [capacity]: page * hkv + head + 1, 0 when free
+  int32_t* slot_stamp;  // [capacity]: last step that used the slot
+  void* data;           // [capacity][2][16][128] bf16: K block then V block of each slot
+  int capacity;
+};
+// Segments per (sequence, kv head) in the plan's seg_slot and fill arrays.
+int block_cache_seg_stride(const Shape& s);
+size_t block_cache_plan_smem(const Shape& s, int capacity);
+// One CTA: looks up the attention's segments, picks LRU victims for the misses, writes
+// seg_slot [B][Hkv][stride] and the fill list (int4 [B * Hkv * stride], count in n_fill).
+cudaError_t launch_cache_plan(const Shape& s, const int32_t* seq_lens, const int32_t* page_table,
+                              const int32_t* block_idx, const int32_t* n_blocks,
+                              const BlockCache& c, int32_t* seg_slot, void* fill,
+                              int32_t* n_fill, int* err, cudaStream_t st);
+
 // ---- attend.cu
 // early: the caller guarantees that K/V, q, the page table and the lengths are complete when
 // the kernel starts (only the selection comes from the previous kernel), as in the whole
@@ -64,7 +83,15 @@ struct AttendBuffers {
   int* counters;    // [B][Hkv]
   int nsplit;
   const int32_t* sel_pages = nullptr;  // optional: the kept blocks' pages, from launch_prune
+  const int32_t* seg_slots = nullptr;  // optional: block-cache slots of the segments (then
+  int seg_stride = 0;                  // k / v are the cache's K and V halves)
+  int cache_capacity = 0;
 };
+// Copies the block cache's fill list (from launch_cache_plan) in from host memory:
+// k_host / v_host are device aliases of the pinned host K/V.
+cudaError_t launch_cache_fill(const Shape& s, const BlockCache& c, const void* fill,
+                              const int32_t* n_fill, const void* k_host, const void* v_host,
+                              int* err, int num_sms, cudaStream_t st);
 int attend_splits(const Shape& s, bool dense, bool host, int num_sms);
 cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
                           const void* k_cache, const void* v_cache, const int32_t* page_table,

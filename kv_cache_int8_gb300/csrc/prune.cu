@@ -546,9 +546,239 @@ size_t prune_smem(const PruneArgs& a) {
                         (a.prow_cap > 0 ? a.prow_cap + 4 : 0) + a.sel_cap);
 }
 
+
+// ------------------------------------------------------- GPU block cache plan
+
+// A device cache of (page, kv head) K/V blocks in front of K/V in host memory (InfiniteHiP
+// article: the GPU keeps recently used blocks, least recently used first out, and the rest
+// of the cache lives in host memory). One plan per attention call, in one CTA:
+//  - the call's segments (sink pages, window pages, kept blocks of every (sequence, kv
+//    head), in the attention's order) are looked up; hits are stamped with the call's
+//    step number; the page that holds the sequence's last token is always copied again
+//    (an append may have changed it) into the slot it has;
+//  - the misses, in segment order, take the slots not used by this call with the oldest
+//    stamps (ties: lower slot), found by the prune's selection over -stamp;
+//  - every segment's slot goes to seg_slot, every slot to fill goes to the fill list.
+struct CachePlanArgs {
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  const int32_t* block_idx;  // [B][Hkv][k2] (k2 > 0)
+  const int32_t* n_blocks;   // [B][Hkv]
+  int32_t* header;           // [0]: step counter
+  int32_t* slot_of;          // [num_pages * hkv]: slot + 1, 0 when absent
+  int32_t* slot_key;         // [capacity]: page * hkv + head + 1, 0 when free
+  int32_t* slot_stamp;       // [capacity]: last step that used the slot, 0 never
+  int32_t* seg_slot;         // [B][Hkv][seg_stride]: slot of each segment, -1 empty
+  int4* fill;                // [B * Hkv * seg_stride]: (slot, page, head) to copy in
+  int32_t* n_fill;
+  int* err;
+  int batch, hkv, max_pages, num_pages, k2, sink, window, seg_stride, capacity;
+};
+
+struct CachePlanShared {
+  PruneShared ps;
+  int warp_cnt[kPruneWarps];  // per-warp counts of one 512-entry chunk
+  int step, n_miss, n_refresh;
+};
+
+// Segment i of (b, h): block k, or -1 when empty (same order and clipping as the attention).
+__device__ int cache_segment_block(const CachePlanArgs& a, int b, int h, int i, int n) {
+  const int sink_end = min(a.sink, n);
+  const int n_sink = (sink_end + kPage - 1) / kPage;
+  const int cand_hi = n - a.window;
+  const int n_sel_max = cand_hi > a.sink ? a.k2 : 0;
+  const int w0 = max(n - a.window, sink_end);
+  const int win_k0 = w0 / kPage;
+  const int n_win = w0 < n ? (n + kPage - 1) / kPage - win_k0 : 0;
+  if (i < n_sink) return i;
+  if (i < n_sink + n_win) return win_k0 + (i - n_sink);
+  const int r = i - n_sink - n_win;
+  if (r >= n_sel_max) return -1;
+  const int nsel = max(0, min(a.n_blocks[(size_t)b * a.hkv + h], n_sel_max));
+  if (r >= nsel) return -1;
+  const int k = a.block_idx[((size_t)b * a.hkv + h) * a.k2 + r];
+  if (k < 0 || k >= (n + kPage - 1) / kPage) return -1;
+  // a kept block is attended only inside the candidate region
+  if (max(k * kPage, a.sink) >= min(k * kPage + kPage, cand_hi)) return -1;
+  return k;
+}
+
+__global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePlanArgs a) {
+  extern __shared__ __align__(16) unsigned char csmem_raw[];
+  CachePlanShared& cs = *reinterpret_cast<CachePlanShared*>(csmem_raw);
+  int* vals = reinterpret_cast<int*>(csmem_raw + ((sizeof(CachePlanShared) + 15) / 16) * 16);
+  int* miss_f = vals + a.capacity;              // [B * Hkv * seg_stride] segment of miss j
+  int* victims = miss_f + a.batch * a.hkv * a.seg_stride;  // same size
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kHistCopies * kDigitBins; i += kPruneThreads) (&cs.ps.hist[0][0])[i] = 0u;
+  grid_dep_wait();  // the selection and the cache state come from earlier kernels
+  grid_dep_launch();
+  if (tid == 0) {
+    cs.step = a.header[0] + 1;
+    a.header[0] = cs.step;
+    cs.n_miss = 0;
+    cs.n_refresh = 0;
+  }
+  __syncthreads();
+  const int step = cs.step;
+  const unsigned lt = lanemask_lt();
+
+  // ---- lookups, in segment order; misses are listed in that order
+  const int F = a.batch * a.hkv * a.seg_stride;
+  for (int f0 = 0; f0 < F; f0 += kPruneThreads) {
+    const int f = f0 + tid;
+    bool miss = false;
+    if (f < F) {
+      const int bh = f / a.seg_stride, i = f % a.seg_stride;
+      const int b = bh / a.hkv, h = bh % a.hkv;
+      int n = a.seq_lens[b];
+      if (n < 0 || n > a.max_pages * kPage) n = 0;
+      const int k = n > 0 ? cache_segment_block(a, b, h, i, n) : -1;
+      int slot = -1;
+      if (k >= 0) {
+        const int page = a.page_table[(size_t)b * a.max_pages + k];
+        if (page < 0 || page >= a.num_pages) {
+          set_error(a.err, kDevErrCheck);
+        } else {
+          const int key = page * a.hkv + h;
+          slot = a.slot_of[key] - 1;
+          if (slot >= 0) {
+            a.slot_stamp[slot] = step;
+            if (k == (n - 1) / kPage) {  // the last token's page: copy it again
+              const int j = atomicAdd(&cs.n_refresh, 1);
+              a.fill[j] = make_int4(slot, page, h, 0);
+            }
+          } else {
+            miss = true;
+          }
+        }
+      }
+      a.seg_slot[f] = slot;  // misses are overwritten below
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, miss);
+    if (lane == 0) cs.warp_cnt[warp] = __popc(bal);
+    __syncthreads();
+    int base = cs.n_miss;
+    for (int w = 0; w < warp; w++) base += cs.warp_cnt[w];
+    if (miss) miss_f[base + __popc(bal & lt)] = f;
+    __syncthreads();
+    if (tid == 0) {
+      int tot = 0;
+      for (int w = 0; w < kPruneWarps; w++) tot += cs.warp_cnt[w];
+      cs.n_miss += tot;
+    }
+    __syncthreads();
+  }
+  const int M = cs.n_miss, R = cs.n_refresh;
+
+  // ---- victims: the M slots not used by this call with the oldest stamps (lower slot
+  // first), ascending by slot; the fill list holds the refreshes, then the misses
+  int got = 0;
+  if (M > 0) {
+    int valid = 0;
+    for (int s = tid; s < a.capacity; s += kPruneThreads) {
+      const int st = a.slot_stamp[s];
+      vals[s] = st < step ? -st : INT_MIN;
+      valid += st < step;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, off);
+    if (lane == 0) cs.ps.tot[warp] = valid;
+    __syncthreads();
+    int n_valid = 0;
+    for (int w = 0; w < kPruneWarps; w++) n_valid += cs.ps.tot[w];
+    __syncthreads();
+    if (n_valid < M) {
+      if (tid == 0) set_error(a.err, kDevErrCheck);  // capacity below the call's working set
+    } else {
+      int T = INT_MIN, need_eq = 0, eq_total = 0;
+      if (M < n_valid) {
+        const int3 r = kth_largest(vals, a.capacity, M, cs.ps, false, 0, 0);
+        T = r.x;
+        need_eq = r.y;
+        eq_total = r.z;
+      }
+      got = collect(vals, a.capacity, T, need_eq, eq_total, cs.ps, victims, 0);
+    }
+  }
+  // evict the victims' old keys first (none of them is looked up by this call)
+  for (int j = tid; j < got; j += kPruneThreads) {
+    const int old = a.slot_key[victims[j]] - 1;
+    if (old >= 0) a.slot_of[old] = 0;
+  }
+  __syncthreads();
+  for (int j = tid; j < got; j += kPruneThreads) {
+    const int v = victims[j], f = miss_f[j];
+    const int bh = f / a.seg_stride, i = f % a.seg_stride;
+    const int b = bh / a.hkv, h = bh % a.hkv;
+    const int k = cache_segment_block(a, b, h, i, a.seq_lens[b]);
+    const int page = a.page_table[(size_t)b * a.max_pages + k];
+    const int key = page * a.hkv + h;
+    a.slot_of[key] = v + 1;
+    a.slot_key[v] = key + 1;
+    a.slot_stamp[v] = step;
+    a.seg_slot[f] = v;
+    a.fill[R + j] = make_int4(v, page, h, 0);
+  }
+  __syncthreads();
+  // two segments of one call on the same (page, head) (pages shared between sequences) are
+  // not supported: reported through the error word
+  for (int j = tid; j < got; j += kPruneThreads) {
+    const int v = victims[j];
+    if (a.slot_of[a.slot_key[v] - 1] != v + 1) set_error(a.err, kDevErrCheck);
+  }
+  if (tid == 0) *a.n_fill = R + got;
+}
+
+int cache_plan_seg_stride(const Shape& s) {
+  return (s.sink + kPage - 1) / kPage + (s.window + kPage - 1) / kPage + 1 + s.k2;
+}
+
+size_t cache_plan_smem(const Shape& s, int capacity) {
+  const size_t F = (size_t)s.batch * s.hkv * cache_plan_seg_stride(s);
+  return ((sizeof(CachePlanShared) + 15) / 16) * 16 + sizeof(int) * ((size_t)capacity + 2 * F);
+}
+
 }  // namespace
 
 int prune_max_chunks() { return kMaxChunks; }
+
+int block_cache_seg_stride(const Shape& s) { return cache_plan_seg_stride(s); }
+
+size_t block_cache_plan_smem(const Shape& s, int capacity) { return cache_plan_smem(s, capacity); }
+
+cudaError_t launch_cache_plan(const Shape& s, const int32_t* seq_lens, const int32_t* page_table,
+                              const int32_t* block_idx, const int32_t* n_blocks,
+                              const BlockCache& c, int32_t* seg_slot, void* fill,
+                              int32_t* n_fill, int* err, cudaStream_t st) {
+  CachePlanArgs a;
+  a.seq_lens = seq_lens;
+  a.page_table = page_table;
+  a.block_idx = block_idx;
+  a.n_blocks = n_blocks;
+  a.header = c.header;
+  a.slot_of = c.slot_of;
+  a.slot_key = c.slot_key;
+  a.slot_stamp = c.slot_stamp;
+  a.seg_slot = seg_slot;
+  a.fill = static_cast<int4*>(fill);
+  a.n_fill = n_fill;
+  a.err = err;
+  a.batch = s.batch;
+  a.hkv = s.hkv;
+  a.max_pages = s.max_pages;
+  a.num_pages = s.num_pages;
+  a.k2 = s.k2;
+  a.sink = s.sink;
+  a.window = s.window;
+  a.seg_stride = cache_plan_seg_stride(s);
+  a.capacity = c.capacity;
+  const size_t smem = cache_plan_smem(s, c.capacity);
+  if (smem > kSmemLimit) return cudaErrorInvalidValue;
+  const cudaError_t e = set_kernel_smem(cache_plan_kernel, smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(cache_plan_kernel, dim3(1), dim3(kPruneThreads), smem, st, true, a);
+}
 
 size_t prune_smem_bytes(const Shape& s) {
   PruneArgs a;

@@ -30,12 +30,14 @@ HSA_OP_SELECT = 1
 HSA_OP_ATTEND = 2
 HSA_OP_DENSE = 3
 HSA_OP_STEP = 4
+HSA_OP_CACHED = 5
 
 # Every entry point declared in include/hsa.h.
 EXPORTS = (
     "hsa_workspace_bytes", "hsa_status_string", "hsa_quantize_keys", "hsa_append_kv",
     "hsa_score_blocks", "hsa_prune", "hsa_select", "hsa_attend", "dense_decode",
     "hsa_decode_step", "hsa_decode_step_reuse", "hsa_read_device_error", "hsa_select_noalloc",
+    "hsa_block_cache_bytes", "hsa_attend_cached", "hsa_decode_step_cached",
 )
 
 
@@ -121,6 +123,10 @@ def load(path: Optional[str] = None):
                                   SZ, P]),
         "hsa_decode_step_reuse": (I32, [D, ctypes.POINTER(hsa_step_io), P, P, P, P, P, P, P, P,
                                         P, SZ, P]),
+        "hsa_block_cache_bytes": (SZ, [D, I32]),
+        "hsa_attend_cached": (I32, [D, P, P, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
+        "hsa_decode_step_cached": (I32, [D, ctypes.POINTER(hsa_step_io), P, P, P, P, P, P, P, P,
+                                         P, I32, P, SZ, P]),
         "hsa_read_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
         "hsa_select_noalloc": (I32, [D, P, P, P, P, P, P, P, P, P, P]),
     }
@@ -257,6 +263,34 @@ def hsa_decode_step_reuse(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, 
         ctypes.byref(cd), ctypes.byref(io), _p(k_cache), _p(v_cache), _p(kq), _p(k_scale),
         _p(page_table), _p(seq_lens), _p(block_idx), _p(n_blocks), _p(ws), ws.numel(),
         _stream(stream)))
+
+
+def block_cache(d: Dims, capacity: int):
+    """A zeroed device buffer for the GPU block cache (see hsa_block_cache_bytes)."""
+    n = load().hsa_block_cache_bytes(ctypes.byref(d.c()), capacity)
+    if n == 0:
+        raise HsaError("hsa_block_cache_bytes", HSA_ERR_INVALID_ARG, "capacity or shape rejected")
+    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+def hsa_attend_cached(d: Dims, q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks,
+                      cache, capacity: int, out, lse, ws, stream=None) -> None:
+    cd = d.c()
+    _check("hsa_attend_cached", load().hsa_attend_cached(
+        ctypes.byref(cd), _p(q), _p(k_cache), _p(v_cache), _p(page_table), _p(seq_lens),
+        _p(block_idx), _p(n_blocks), _p(cache), capacity, _p(out), _p(lse), _p(ws), ws.numel(),
+        _stream(stream)))
+
+
+def hsa_decode_step_cached(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_scale,
+                           page_table, seq_lens, block_idx, n_blocks, cache, capacity: int, ws,
+                           io_on_host: bool = False, stream=None) -> None:
+    cd = d.c()
+    io = hsa_step_io(_p(q), _p(k_new), _p(v_new), _p(out), _p(lse), 1 if io_on_host else 0)
+    _check("hsa_decode_step_cached", load().hsa_decode_step_cached(
+        ctypes.byref(cd), ctypes.byref(io), _p(k_cache), _p(v_cache), _p(kq), _p(k_scale),
+        _p(page_table), _p(seq_lens), _p(block_idx), _p(n_blocks), _p(cache), capacity, _p(ws),
+        ws.numel(), _stream(stream)))
 
 
 def hsa_read_device_error(ws, stream=None) -> int:

@@ -1,0 +1,192 @@
+"""The GPU block cache in front of K/V in host memory: attention through the cache against
+the oracle, the cache's state after every call against an LRU model written here (hits
+refresh a block's age; misses take the slots used longest ago, lower slot first; the page
+holding a sequence's last token is copied again), and the cached blocks' bytes against the
+host K/V."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+import oracle
+from kv_cache_int8_gb300 import hsa
+from kv_cache_int8_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _up(x):
+    return (x + 255) // 256 * 256
+
+
+def _segments(lens, sink, window, k2, bidx, nb, b, h):
+    """Blocks of the call's segments of (b, h) in the attention's order (None: empty)."""
+    n = int(lens[b])
+    sink_end = min(sink, n)
+    n_sink = (sink_end + 15) // 16
+    cand_hi = n - window
+    n_sel_max = k2 if cand_hi > sink else 0
+    w0 = max(n - window, sink_end)
+    win_k0 = w0 // 16
+    n_win = (n + 15) // 16 - win_k0 if w0 < n else 0
+    stride = (sink + 15) // 16 + (window + 15) // 16 + 1 + k2
+    out = []
+    for i in range(stride):
+        if i < n_sink:
+            out.append(i)
+        elif i < n_sink + n_win:
+            out.append(win_k0 + i - n_sink)
+        else:
+            r = i - n_sink - n_win
+            k = None
+            if r < min(max(int(nb[b, h]), 0), n_sel_max):
+                kk = int(bidx[b, h, r])
+                if 0 <= kk < (n + 15) // 16 and max(kk * 16, sink) < min(kk * 16 + 16, cand_hi):
+                    k = kk
+            out.append(k)
+    return out
+
+
+class LruModel:
+    def __init__(self, num_pages, hkv, capacity):
+        self.hkv, self.cap = hkv, capacity
+        self.slot_of = np.zeros(num_pages * hkv, dtype=np.int64)   # slot + 1
+        self.key = np.zeros(capacity, dtype=np.int64)              # key + 1
+        self.stamp = np.zeros(capacity, dtype=np.int64)
+        self.step = 0
+
+    def call(self, segs_by_bh, pt):
+        self.step += 1
+        misses = []
+        for (b, h), segs in segs_by_bh:
+            for k in segs:
+                if k is None:
+                    continue
+                key = int(pt[b, k]) * self.hkv + h
+                s = self.slot_of[key] - 1
+                if s >= 0:
+                    self.stamp[s] = self.step
+                else:
+                    misses.append(key)
+        free = [s for s in range(self.cap) if self.stamp[s] < self.step]
+        victims = sorted(free, key=lambda s: (self.stamp[s], s))[:len(misses)]
+        victims.sort()
+        for v in victims:
+            if self.key[v] > 0:
+                self.slot_of[self.key[v] - 1] = 0
+        for v, key in zip(victims, misses):
+            self.slot_of[key] = v + 1
+            self.key[v] = key + 1
+            self.stamp[v] = self.step
+        return len(misses)
+
+
+def test_block_cache_lru_and_attention():
+    cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None, context_range=(2000, 4000),
+                              batch=2, hq=8, hkv=2, k1=20, k2=12, sink=32, window=64,
+                              paged_permuted=True)
+    wl = W.make_workload(cfg, seed=91, host_pinned=True)
+    hd, od = H.dims_pair(wl)
+    dwl = H.to_cuda(wl)
+    dev = torch.device("cuda")
+    B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
+    stride = (cfg.sink + 15) // 16 + (cfg.window + 15) // 16 + 1 + cfg.k2
+    capacity = B * Hkv * stride + 9  # little room beyond one call: evictions every call
+    assert hsa.load().hsa_block_cache_bytes(hd.c(), B * Hkv * stride - 1) == 0
+    cache = hsa.block_cache(hd, capacity)
+    ws = hsa.workspace(hd, hsa.HSA_OP_CACHED)
+    h = H.host_arrays(wl)
+    pt, lens = h["pt"], h["lens"]
+    model = LruModel(wl["num_pages"], Hkv, capacity)
+    gen = np.random.default_rng(5)
+    q = dwl["q"]
+    for call in range(6):
+        # kept blocks: a different random draw each call (some repeats of earlier ones)
+        n_cand = [((int(n) - cfg.window + 15) // 16) for n in lens]
+        bidx = np.full((B, Hkv, cfg.k2), -1, dtype=np.int32)
+        nb = np.zeros((B, Hkv), dtype=np.int32)
+        for b in range(B):
+            for hh in range(Hkv):
+                pool = np.arange(cfg.sink // 16, n_cand[b])
+                if call % 2:
+                    pool = pool[: len(pool) // 3]  # overlap with earlier calls
+                pick = np.sort(gen.choice(pool, size=cfg.k2, replace=False))
+                bidx[b, hh] = pick
+                nb[b, hh] = cfg.k2 - (call % 3)
+                bidx[b, hh, nb[b, hh]:] = -1
+        out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
+        lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev)
+        hsa.hsa_attend_cached(hd, q, dwl["k_cache"], dwl["v_cache"], dwl["page_table"],
+                              dwl["seq_lens"], torch.from_numpy(bidx).to(dev),
+                              torch.from_numpy(nb).to(dev), cache, capacity, out, lse, ws)
+        torch.cuda.synchronize()
+        assert hsa.hsa_read_device_error(ws) == 0
+        out_o, lse_o = oracle.attend(od, h["q"], h["k"], h["v"], pt, lens, bidx, nb)
+        H.assert_close(out.cpu().numpy(), out_o, f"call {call} output")
+        np.testing.assert_allclose(lse.cpu().numpy(), lse_o, atol=2e-4, rtol=1e-5)
+        # the cache's state against the model
+        segs = [((b, hh), _segments(lens, cfg.sink, cfg.window, cfg.k2, bidx, nb, b, hh))
+                for b in range(B) for hh in range(Hkv)]
+        model.call(segs, pt)
+        raw = cache.cpu().numpy()
+        off_of = 256
+        off_key = off_of + _up(wl["num_pages"] * Hkv * 4)
+        off_stamp = off_key + _up(capacity * 4)
+        off_data = off_stamp + _up(capacity * 4)
+        as_i32 = lambda o, n: raw[o:o + 4 * n].view(np.int32)
+        assert int(raw[:4].view(np.int32)[0]) == model.step
+        np.testing.assert_array_equal(as_i32(off_of, wl["num_pages"] * Hkv), model.slot_of)
+        np.testing.assert_array_equal(as_i32(off_key, capacity), model.key)
+        np.testing.assert_array_equal(as_i32(off_stamp, capacity), model.stamp)
+        data = raw[off_data:off_data + capacity * 8192].view(np.uint16).reshape(capacity, 2, 16, 128)
+        for v in np.nonzero(model.key)[0]:
+            key = int(model.key[v]) - 1
+            page, hh = key // Hkv, key % Hkv
+            np.testing.assert_array_equal(data[v, 0], h["k"][page, hh])
+            np.testing.assert_array_equal(data[v, 1], h["v"][page, hh])
+
+
+def test_cached_decode_step_matches_the_uncached_one():
+    """Whole steps with host K/V, through the cache and without it: same selection, same
+    outputs within rounding; the new token reaches the cached page (copied again)."""
+    cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None, context_range=(3000, 5000),
+                              batch=2, hq=8, hkv=2, k1=10, k2=8, sink=32, window=64,
+                              paged_permuted=True)
+    wl = W.make_workload(cfg, seed=17, host_pinned=True)
+    hd, od = H.dims_pair(wl)
+    dwl = H.to_cuda(wl)
+    dev = torch.device("cuda")
+    B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
+    stride = (cfg.sink + 15) // 16 + (cfg.window + 15) // 16 + 1 + cfg.k2
+    capacity = 2 * B * Hkv * stride
+    cache = hsa.block_cache(hd, capacity)
+    kq = torch.zeros(dwl["k_cache"].shape, dtype=torch.int8, device=dev)
+    k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
+    hsa.hsa_quantize_keys(hd, dwl["k_cache"], dwl["page_table"], dwl["seq_lens"], 0, 0, kq,
+                          k_scale, hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
+    gen = torch.Generator(device="cpu").manual_seed(3)
+    ws1, ws2 = hsa.workspace(hd, hsa.HSA_OP_STEP), hsa.workspace(hd, hsa.HSA_OP_STEP)
+    for step in range(3):
+        k_new = torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16).to(dev)
+        v_new = torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16).to(dev)
+        res = []
+        for cached, ws in ((True, ws1), (False, ws2)):
+            out = torch.zeros((B, Hq, 128), dtype=torch.float32, device=dev)
+            lse = torch.zeros((B, Hq), dtype=torch.float32, device=dev)
+            bidx = torch.full((B, Hkv, cfg.k2), -7, dtype=torch.int32, device=dev)
+            nb = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+            args = (hd, dwl["q"], k_new, v_new, out, lse, dwl["k_cache"], dwl["v_cache"], kq,
+                    k_scale, dwl["page_table"], dwl["seq_lens"], bidx, nb)
+            if cached:
+                hsa.hsa_decode_step_cached(*args, cache, capacity, ws)
+            else:
+                hsa.hsa_decode_step(*args, ws)
+            torch.cuda.synchronize()
+            assert hsa.hsa_read_device_error(ws) == 0
+            res.append((out.cpu().numpy(), lse.cpu().numpy(), bidx.cpu().numpy(), nb.cpu().numpy()))
+        np.testing.assert_array_equal(res[0][2], res[1][2])
+        np.testing.assert_array_equal(res[0][3], res[1][3])
+        np.testing.assert_allclose(res[0][0], res[1][0], atol=1e-4, rtol=0)
+        np.testing.assert_allclose(res[0][1], res[1][1], atol=1e-4, rtol=0)
