@@ -621,54 +621,80 @@ __global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePl
   }
   __syncthreads();
   const int step = cs.step;
-  const unsigned lt = lanemask_lt();
 
-  // ---- lookups, in segment order; misses are listed in that order
+  // ---- lookups. Thread t takes the segments [t per, (t + 1) per) (per <= 64: the capacity,
+  // at most 32768, holds every segment of a call), eight at a time with their dependent
+  // loads (length, block id, page, slot) issued together; then one scan orders the misses.
   const int F = a.batch * a.hkv * a.seg_stride;
-  for (int f0 = 0; f0 < F; f0 += kPruneThreads) {
-    const int f = f0 + tid;
-    bool miss = false;
-    if (f < F) {
-      const int bh = f / a.seg_stride, i = f % a.seg_stride;
-      const int b = bh / a.hkv, h = bh % a.hkv;
-      int n = a.seq_lens[b];
-      if (n < 0 || n > a.max_pages * kPage) n = 0;
-      const int k = n > 0 ? cache_segment_block(a, b, h, i, n) : -1;
-      int slot = -1;
-      if (k >= 0) {
-        const int page = a.page_table[(size_t)b * a.max_pages + k];
-        if (page < 0 || page >= a.num_pages) {
-          set_error(a.err, kDevErrCheck);
-        } else {
-          const int key = page * a.hkv + h;
-          slot = a.slot_of[key] - 1;
-          if (slot >= 0) {
-            a.slot_stamp[slot] = step;
-            if (k == (n - 1) / kPage) {  // the last token's page: copy it again
-              const int j = atomicAdd(&cs.n_refresh, 1);
-              a.fill[j] = make_int4(slot, page, h, 0);
-            }
-          } else {
-            miss = true;
-          }
-        }
+  const int per = (F + kPruneThreads - 1) / kPruneThreads;
+  const int f_lo = min(F, tid * per), f_hi = min(F, f_lo + per);
+  unsigned long long miss_mask = 0ull;
+  int my_miss = 0;
+  for (int fb = f_lo; fb < f_hi; fb += 8) {
+    int k[8], page[8], slot[8], n[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int f = fb + u;
+      n[u] = f < f_hi ? a.seq_lens[(f / a.seg_stride) / a.hkv] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int f = fb + u;
+      const int bh = f / a.seg_stride;
+      if (n[u] < 0 || n[u] > a.max_pages * kPage) n[u] = 0;
+      k[u] = (f < f_hi && n[u] > 0) ? cache_segment_block(a, bh / a.hkv, bh % a.hkv,
+                                                          f % a.seg_stride, n[u])
+                                    : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int b = ((fb + u) / a.seg_stride) / a.hkv;
+      page[u] = k[u] >= 0 ? a.page_table[(size_t)b * a.max_pages + k[u]] : -1;
+      if (k[u] >= 0 && (page[u] < 0 || page[u] >= a.num_pages)) {
+        set_error(a.err, kDevErrCheck);
+        k[u] = -1;
       }
-      a.seg_slot[f] = slot;  // misses are overwritten below
     }
-    const unsigned bal = __ballot_sync(0xffffffffu, miss);
-    if (lane == 0) cs.warp_cnt[warp] = __popc(bal);
-    __syncthreads();
-    int base = cs.n_miss;
-    for (int w = 0; w < warp; w++) base += cs.warp_cnt[w];
-    if (miss) miss_f[base + __popc(bal & lt)] = f;
-    __syncthreads();
-    if (tid == 0) {
-      int tot = 0;
-      for (int w = 0; w < kPruneWarps; w++) tot += cs.warp_cnt[w];
-      cs.n_miss += tot;
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int h = ((fb + u) / a.seg_stride) % a.hkv;
+      slot[u] = k[u] >= 0 ? a.slot_of[page[u] * a.hkv + h] - 1 : -1;
     }
-    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int f = fb + u;
+      if (f >= f_hi) continue;
+      if (k[u] >= 0 && slot[u] >= 0) {
+        a.slot_stamp[slot[u]] = step;
+        if (k[u] == (n[u] - 1) / kPage) {  // the last token's page: copy it again
+          const int j = atomicAdd(&cs.n_refresh, 1);
+          a.fill[j] = make_int4(slot[u], page[u], (f / a.seg_stride) % a.hkv, 0);
+        }
+      } else if (k[u] >= 0) {
+        miss_mask |= 1ull << (f - f_lo);
+        my_miss++;
+      }
+      a.seg_slot[f] = k[u] >= 0 ? slot[u] : -1;  // misses are overwritten below
+    }
   }
+  // exclusive scan of the per-thread miss counts, then each thread lists its misses in order
+  int incl = my_miss;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) cs.warp_cnt[warp] = incl;
+  __syncthreads();
+  int base = incl - my_miss;
+  for (int w = 0; w < warp; w++) base += cs.warp_cnt[w];
+  if (tid == kPruneThreads - 1) cs.n_miss = base + my_miss;
+  for (int o = 0; miss_mask != 0ull; o++) {
+    const int bit = __ffsll((long long)miss_mask) - 1;
+    miss_mask &= miss_mask - 1;
+    miss_f[base + o] = f_lo + bit;
+  }
+  __syncthreads();
   const int M = cs.n_miss, R = cs.n_refresh;
 
   // ---- victims: the M slots not used by this call with the oldest stamps (lower slot
