@@ -63,6 +63,7 @@ typedef struct {
   int32_t batch, hq, hkv, head_dim, page_size, max_pages_per_seq, num_pages;
   int32_t chunk, block, k1, k2, sink, window;
   double sm_scale; /* <= 0 means 1/sqrt(head_dim) */
+  int32_t chunk0, k0; /* k0 > 0: a first module keeps the top-k0 chunks of chunk0 tokens */
 } oracle_dims;
 
 /* ---------------------------------------------------------------- helpers */
@@ -90,6 +91,8 @@ static int dims_ok(const oracle_dims* d) {
   if (d->page_size <= 0 || d->max_pages_per_seq <= 0 || d->num_pages <= 0) return 0;
   if (d->chunk <= 0 || d->block <= 0 || d->chunk % d->block) return 0;
   if (d->k1 < 0 || d->k2 < 0 || d->sink < 0 || d->window < 0) return 0;
+  if (d->k0 < 0) return 0;
+  if (d->k0 > 0 && (d->chunk0 < d->chunk || d->chunk0 % d->chunk)) return 0;
   return 1;
 }
 
@@ -263,11 +266,16 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
     query_codes_one(d, q, scale, b, h, qq, NULL);
 
     int64_t n_chunk_all = (max_tokens + d->chunk - 1) / d->chunk;
+    const int64_t c0 = d->k0 > 0 ? d->chunk0 : d->chunk; /* coarse chunk of module 0 */
+    int64_t n_coarse_all = (max_tokens + c0 - 1) / c0;
+    int64_t* cmax0 = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_coarse_all + 1));
+    char* cvalid0 = (char*)calloc((size_t)n_coarse_all + 1, 1);
+    char* ckept0 = (char*)calloc((size_t)n_coarse_all + 1, 1);
     int64_t* cmax = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_chunk_all + 1));
     int64_t* bmax = (int64_t*)malloc(sizeof(int64_t) * (size_t)(max_blocks + 1));
     char* cvalid = (char*)calloc((size_t)n_chunk_all + 1, 1);
     char* bvalid = (char*)calloc((size_t)max_blocks + 1, 1);
-    if (!qq || !cmax || !bmax || !cvalid || !bvalid) {
+    if (!qq || !cmax || !bmax || !cvalid || !bvalid || !cmax0 || !cvalid0 || !ckept0) {
 #pragma omp atomic write
       bad = 1;
     } else {
@@ -280,7 +288,9 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
             dot += (int64_t)qq[j * D + c] * (int64_t)kq[cache_index(d, page_table, b, h, t, c)];
           if (dot > g) g = dot;
         }
-        int64_t ci = t / d->chunk, bi = t / d->block;
+        int64_t ci = t / d->chunk, bi = t / d->block, c0i = t / c0;
+        if (!cvalid0[c0i] || g > cmax0[c0i]) cmax0[c0i] = g;
+        cvalid0[c0i] = 1;
         if (!cvalid[ci] || g > cmax[ci]) cmax[ci] = g;
         if (!bvalid[bi] || g > bmax[bi]) bmax[bi] = g;
         cvalid[ci] = 1;
@@ -290,11 +300,25 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
         int32_t* out = block_max + ((int64_t)b * d->hkv + h) * max_blocks;
         for (int64_t k = 0; k < max_blocks; k++) out[k] = bvalid[k] ? (int32_t)bmax[k] : INT32_MIN;
       }
-      /* module 1: top-K1 chunks */
-      ranked* list = (ranked*)malloc(sizeof(ranked) * (size_t)(n_chunk_all + max_blocks + 1));
+      ranked* list = (ranked*)malloc(sizeof(ranked) * (size_t)(n_chunk_all + max_blocks +
+                                                                n_coarse_all + 1));
+      /* module 0 (stacked in front when k0 > 0): top-K0 coarse chunks, by the same order */
+      if (d->k0 > 0) {
+        int64_t n0 = 0;
+        for (int64_t c = 0; c < n_coarse_all; c++)
+          if (cvalid0[c]) {
+            list[n0].score = cmax0[c];
+            list[n0].index = c;
+            n0++;
+          }
+        qsort(list, (size_t)n0, sizeof(ranked), by_score_then_index);
+        int64_t keep0 = n0 < d->k0 ? n0 : d->k0;
+        for (int64_t i = 0; i < keep0; i++) ckept0[list[i].index] = 1;
+      }
+      /* module 1: top-K1 chunks (inside the kept coarse chunks when module 0 runs) */
       int64_t nc = 0;
       for (int64_t c = 0; c < n_chunk_all; c++)
-        if (cvalid[c]) {
+        if (cvalid[c] && (d->k0 == 0 || ckept0[c * d->chunk / c0])) {
           list[nc].score = cmax[c];
           list[nc].index = c;
           nc++;
@@ -325,6 +349,9 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
       free(list);
     }
     free(qq);
+    free(cmax0);
+    free(cvalid0);
+    free(ckept0);
     free(cmax);
     free(bmax);
     free(cvalid);

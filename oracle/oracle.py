@@ -19,7 +19,9 @@ _LIB = None
 class _CDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "hq", "hkv", "head_dim", "page_size", "max_pages_per_seq", "num_pages",
-        "chunk", "block", "k1", "k2", "sink", "window")] + [("sm_scale", ctypes.c_double)]
+        "chunk", "block", "k1", "k2", "sink", "window")] + [("sm_scale", ctypes.c_double),
+                                                            ("chunk0", ctypes.c_int32),
+                                                            ("k0", ctypes.c_int32)]
 
 
 @dataclasses.dataclass
@@ -39,10 +41,12 @@ class Dims:
     sink: int
     window: int
     sm_scale: float = 0.0
+    chunk0: int = 0  # k0 > 0: a first module keeps the top-k0 chunks of chunk0 tokens
+    k0: int = 0
 
     def c(self) -> _CDims:
-        return _CDims(*[int(getattr(self, f[0])) for f in _CDims._fields_[:-1]],
-                      float(self.sm_scale))
+        return _CDims(*[int(getattr(self, f[0])) for f in _CDims._fields_[:13]],
+                      float(self.sm_scale), int(self.chunk0), int(self.k0))
 
     @property
     def group(self) -> int:

@@ -348,6 +348,69 @@ def test_modules_defining_property_brute_force(seed):
                 assert sorted(ranked) == kept_b
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_three_stacked_modules_defining_property_brute_force(seed):
+    """A first module on coarse chunks (chunk0 tokens) keeps the top K0; module 1 ranks only
+    the fine chunks inside them; module 2 as before. Each stage is checked by brute force
+    against its defining property, and with K0 >= K1 the three stages equal the two."""
+    rng = np.random.default_rng(300 + seed)
+    D, hkv, G = 8, 2, 2
+    lens = tuple(int(x) for x in rng.integers(100, 900, size=2))
+    case = random_case(rng, B=2, hq=hkv * G, hkv=hkv, D=D, lens=lens, page=16, perm=True)
+    for b in range(2):
+        case["ks"][b] = np.round(case["ks"][b] * 2) / 2  # frequent ties
+    kc, pt, ln = paged(case["ks"], 16, hkv, None)
+    case.update(k=kc, pt=pt)
+    block, chunk = 16, 32
+    chunk0 = chunk * int(rng.choice([2, 4]))
+    k0, k1, k2 = int(rng.integers(1, 6)), int(rng.integers(1, 12)), int(rng.integers(0, 14))
+    sink, window = int(rng.integers(0, 40)), int(rng.integers(0, 60))
+    d = dims_for(case, hkv * G, hkv, D, chunk=chunk, block=block, k1=k1, k2=k2, sink=sink,
+                 window=window)
+    d.chunk0, d.k0 = chunk0, k0
+    kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, ln)
+    qq, _ = oracle.query_codes(d, bf16_bits(case["q"]), sc)
+    sel = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln)
+    codes = logical_codes(kq, pt, ln, 16, hkv)
+    per, per0 = chunk // block, chunk0 // block
+    for b in range(2):
+        for h in range(hkv):
+            bm = _block_max_by_definition(qq[b, h], codes[b][h], int(ln[b]), sink, window, block)
+            cm0, cm = {}, {}
+            for k, s_ in bm.items():
+                cm0[k // per0] = max(cm0.get(k // per0, s_), s_)
+                cm[k // per] = max(cm.get(k // per, s_), s_)
+            kept0 = sorted(cm0, key=lambda c: (-cm0[c], c))[:k0]
+            for c in kept0:
+                for c2 in cm0:
+                    if c2 not in kept0:
+                        assert _beats(cm0[c], c, cm0[c2], c2)
+            cand1 = [c for c in cm if c * chunk // chunk0 in kept0]
+            kept_c = [c for c in sel["chunk_idx"][b, h] if c >= 0]
+            assert kept_c == sorted(kept_c) and len(kept_c) == min(k1, len(cand1))
+            for c in kept_c:
+                assert c in cand1
+                for c2 in cand1:
+                    if c2 not in kept_c:
+                        assert _beats(cm[c], c, cm[c2], c2)
+            cand2 = [k for k in bm if k // per in kept_c]
+            kept_b = [k for k in sel["block_idx"][b, h] if k >= 0]
+            assert kept_b == sorted(kept_b) and len(kept_b) == min(k2, len(cand2))
+            for k in kept_b:
+                assert k in cand2
+                for k_ in cand2:
+                    if k_ not in kept_b:
+                        assert _beats(bm[k], k, bm[k_], k_)
+    # closed form: a coarse chunk holding a top-K1 fine chunk is itself in the top K1 coarse
+    # chunks, so with K0 >= K1 module 0 removes nothing that module 1 would keep
+    d.k0 = max(k1, 1)
+    three = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln)
+    d.k0 = 0
+    two = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln)
+    for key in ("chunk_idx", "n_chunks", "block_idx", "n_blocks"):
+        np.testing.assert_array_equal(three[key], two[key])
+
+
 def test_candidate_region_masks_sink_and_window_tokens():
     """A huge key in the sink part of a block that straddles the sink boundary, and one in
     the window, must not lift any block score."""
