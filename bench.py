@@ -671,7 +671,8 @@ def main():
     if not args.no_extra:
         # the batched paged configuration and the 3M-token offloaded one (K/V in pinned host
         # memory, read over the host link by the attend kernel)
-        for name, dense in (("paged-b8-32k-128k", True), ("llama3-8b-3m-offload", False)):
+        for name, dense in (("paged-b8-32k-128k", True), ("llama3-8b-3m-offload", False),
+                            ("llama3-8b-1m-3mod", False)):
             r = gpu_case_numbers(name, rank, device, min(args.steps, 500), args.warmup, None,
                                  peak, world, dense=dense)
             del r["case"]
@@ -681,11 +682,11 @@ def main():
                 **({"host_link_copy_gbs": host_link_copy_gbs(device),
                     "us_per_step_block_cache": r["cached_ms"]["step_cached"] * 1e3,
                     "attend_block_cache_us": r["cached_ms"]["attend_cached"] * 1e3,
-                    "block_cache_slots": Case.CACHE_SLOTS} if not dense else {}),
+                    "block_cache_slots": Case.CACHE_SLOTS} if r["cached_ms"] else {}),
                 "prune_us": r["per_ms"]["prune"] * 1e3, "attend_us": r["per_ms"]["attend"] * 1e3,
                 "dense_us": r["dense_ms"] * 1e3 if dense else None,
                 "score_gbs": r["gbs"]["score"],
-                "attend_gbs" + ("_host_link" if not dense else ""): r["gbs"]["attend"],
+                "attend_gbs" + ("_host_link" if r["cached_ms"] else ""): r["gbs"]["attend"],
                 "bytes": r["bytes"], "quantize_keys_ms": r["quantize_ms"],
             }
     if not args.no_extra and args.config != EXTRA_CONFIG:

@@ -93,6 +93,9 @@ typedef struct hsa_dims {
                                 hsa_append_kv and hsa_decode_step are PINNED HOST memory
                                 (cudaHostAlloc / cudaHostRegister); the kernels read them
                                 through the mapped device aliases */
+  int32_t chunk0;            /* k0 > 0: length of module 0's coarse chunks, a multiple of chunk */
+  int32_t k0;                /* coarse chunks kept by module 0, stacked in front of module 1
+                                (which then ranks only the chunks inside them); 0: no module 0 */
 } hsa_dims;
 
 /* Operation ids for hsa_workspace_bytes. */

@@ -41,10 +41,13 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   if ((long long)d->num_pages * d->hkv * hsa::kPage > INT32_MAX ||
       (long long)d->max_pages_per_seq * hsa::kPage > INT32_MAX / 2)
     return HSA_ERR_UNSUPPORTED;
-  if (d->sink < 0 || d->window < 0 || d->k1 < 0 || d->k2 < 0) return HSA_ERR_INVALID_ARG;
+  if (d->sink < 0 || d->window < 0 || d->k1 < 0 || d->k2 < 0 || d->k0 < 0)
+    return HSA_ERR_INVALID_ARG;
   if (need_prune) {
     if (d->block != hsa::kPage) return HSA_ERR_UNSUPPORTED;
     if (d->chunk <= 0 || d->chunk % d->block != 0) return HSA_ERR_INVALID_ARG;
+    if (d->k0 > 0 && (d->chunk0 < d->chunk || d->chunk0 % d->chunk != 0))
+      return HSA_ERR_INVALID_ARG;
   }
   if (!(d->sm_scale == d->sm_scale)) return HSA_ERR_INVALID_ARG;  // NaN
   s.batch = d->batch;
@@ -58,6 +61,8 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   s.k2 = d->k2;
   s.sink = d->sink;
   s.window = d->window;
+  s.chunk0 = d->k0 > 0 ? d->chunk0 : 0;
+  s.k0 = d->k0;
   s.sm_scale = d->sm_scale > 0.0f ? d->sm_scale : 1.0f / std::sqrt((float)hsa::kHeadDim);
   return HSA_OK;
 }

@@ -12,6 +12,7 @@ namespace hsa {
 struct Shape {
   int batch, hq, hkv, group, max_pages, num_pages;
   int chunk, k1, k2, sink, window;
+  int chunk0, k0;  // module 0 (k0 > 0): coarse chunks of chunk0 tokens, top k0
   float sm_scale;  // resolved (> 0)
 };
 

@@ -48,7 +48,9 @@ struct PruneArgs {
   int32_t* sel_pages;         // nullable, [B][Hkv][K2] beside block_idx
   int* err;
   int hkv, max_pages, chunk_blocks, k1, k2, sink, window;
+  int k0, coarse_chunks;  // module 0: top-k0 coarse chunks of coarse_chunks chunks each
   int vals_cap, cand_cap, kept_cap, row_cap, prow_cap, sel_cap;  // shared-memory array sizes
+  int n0_cap, k0_cap, c1_cap;                                     // module 0's (0 without it)
 };
 
 // Shared scratch of the selection.
@@ -349,6 +351,10 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
   int* row_base = kept_chunks + a.kept_cap;          // row_cap + 4 (16-byte aligned)
   int* prow_base = row_base + (a.row_cap > 0 ? a.row_cap + 4 : 0);  // prow_cap + 4
   int* sel_pos = prow_base + (a.prow_cap > 0 ? a.prow_cap + 4 : 0);  // sel_cap
+  int* vals0 = sel_pos + a.sel_cap;  // module 0 (k0 > 0): n0_cap coarse scores,
+  int* kept0 = vals0 + a.n0_cap;     // k0_cap kept coarse chunks,
+  int* vals1 = kept0 + a.k0_cap;     // c1_cap scores of their fine chunks
+  int* cand1 = vals1 + a.c1_cap;     // and c1_cap fine chunk ids
 
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x;
@@ -425,18 +431,75 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
     __syncthreads();
   }
 
-  // ---- module 1: top-K1 chunks
-  const int keep1 = min(a.k1, n1);
   int T = INT_MIN, need_eq = 0, eq_total = 0;
-  if (keep1 < n1 && keep1 > 0) {
-    const int3 r = kth_largest(vals, n1, keep1, ps, false, 0, 0);
-    T = r.x;
-    need_eq = r.y;
-    eq_total = r.z;
-  }
   int got1 = 0;
-  if (keep1 > 0) {
-    got1 = collect(vals, n1, T, need_eq, eq_total, ps, kept_chunks, c_lo);
+  if (a.k0 > 0) {
+    // ---- module 0 (stacked in front): coarse chunks of R fine chunks, scored by the max of
+    // their fine chunks' scores; top-K0, ascending
+    const int R = a.coarse_chunks;
+    const int g_lo = c_lo / R;
+    const int n0 = n1 > 0 ? (c_lo + n1 - 1) / R - g_lo + 1 : 0;
+    for (int j = tid; j < n0; j += kPruneThreads) {
+      const int f0 = max((g_lo + j) * R, c_lo) - c_lo;
+      const int f1 = min((g_lo + j) * R + R, c_lo + n1) - c_lo;
+      int m = INT_MIN;
+      for (int i = f0; i < f1; i++) m = max(m, vals[i]);
+      vals0[j] = m;
+    }
+    __syncthreads();
+    const int keep0 = min(a.k0, n0);
+    if (keep0 < n0) {
+      const int3 r = kth_largest(vals0, n0, keep0, ps, false, 0, 0);
+      T = r.x;
+      need_eq = r.y;
+      eq_total = r.z;
+    }
+    const int got0 = keep0 > 0 ? collect(vals0, n0, T, need_eq, eq_total, ps, kept0, g_lo) : 0;
+    // ---- module 1 over the kept coarse chunks' fine chunks (ascending; those outside the
+    // candidate region are placeholders), top-K1
+    const int n1c = got0 * R;
+    int valid = 0;
+    for (int x = tid; x < n1c; x += kPruneThreads) {
+      const int c = kept0[x / R] * R + x % R;
+      const bool in = c >= c_lo && c < c_lo + n1;
+      vals1[x] = in ? vals[c - c_lo] : INT_MIN;
+      cand1[x] = c;
+      valid += in;
+    }
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, off);
+    if (lane == 0) ps.tot[warp] = valid;
+    __syncthreads();
+    int n1_valid = 0;
+#pragma unroll
+    for (int w = 0; w < kPruneWarps; w++) n1_valid += ps.tot[w];
+    __syncthreads();
+    const int keep1 = min(a.k1, n1_valid);
+    T = INT_MIN;
+    need_eq = 0;
+    eq_total = 0;
+    if (keep1 < n1_valid && keep1 > 0) {
+      const int3 r = kth_largest(vals1, n1c, keep1, ps, false, 0, 0);
+      T = r.x;
+      need_eq = r.y;
+      eq_total = r.z;
+    }
+    if (keep1 > 0) {
+      got1 = collect(vals1, n1c, T, need_eq, eq_total, ps, kept_chunks, 0);  // positions
+      for (int i = tid; i < got1; i += kPruneThreads) kept_chunks[i] = cand1[kept_chunks[i]];
+      __syncthreads();
+    }
+  } else {
+    // ---- module 1: top-K1 chunks
+    const int keep1 = min(a.k1, n1);
+    if (keep1 < n1 && keep1 > 0) {
+      const int3 r = kth_largest(vals, n1, keep1, ps, false, 0, 0);
+      T = r.x;
+      need_eq = r.y;
+      eq_total = r.z;
+    }
+    if (keep1 > 0) got1 = collect(vals, n1, T, need_eq, eq_total, ps, kept_chunks, c_lo);
   }
   if (a.chunk_idx)
     for (int i = tid; i < a.k1; i += kPruneThreads)
@@ -536,6 +599,15 @@ int prune_caps(const Shape& s, PruneArgs& a, bool stage_pages) {
   a.row_cap = s.max_pages <= kRowCap ? up4(s.max_pages) : 0;
   a.prow_cap = stage_pages ? a.row_cap : 0;
   a.sel_cap = up4(std::max<long long>(std::min<long long>(s.k2, n2max), 1));
+  a.n0_cap = a.k0_cap = a.c1_cap = 0;
+  if (s.k0 > 0) {
+    const long long R = s.chunk0 / s.chunk;
+    const long long n0max = (n1max + R - 1) / R + 1;
+    const long long k0cap = std::min<long long>(s.k0, n0max);
+    a.n0_cap = up4(n0max);
+    a.k0_cap = up4(k0cap);
+    a.c1_cap = up4(k0cap * R);
+  }
   return 0;
 }
 
@@ -543,7 +615,8 @@ size_t prune_smem(const PruneArgs& a) {
   return ((sizeof(PruneShared) + 15) / 16) * 16 +
          sizeof(int) * ((size_t)a.vals_cap + 4 + 2 * (size_t)a.cand_cap + a.kept_cap +
                         (a.row_cap > 0 ? a.row_cap + 4 : 0) +
-                        (a.prow_cap > 0 ? a.prow_cap + 4 : 0) + a.sel_cap);
+                        (a.prow_cap > 0 ? a.prow_cap + 4 : 0) + a.sel_cap + a.n0_cap +
+                        a.k0_cap + 2 * (size_t)a.c1_cap);
 }
 
 
@@ -845,6 +918,8 @@ cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t*
   a.k2 = s.k2;
   a.sink = s.sink;
   a.window = s.window;
+  a.k0 = s.k0;
+  a.coarse_chunks = s.k0 > 0 ? s.chunk0 / s.chunk : 1;
   cudaError_t e = set_kernel_smem(prune_kernel, smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(prune_kernel, dim3(s.hkv, s.batch), dim3(kPruneThreads), smem, st, true, a);

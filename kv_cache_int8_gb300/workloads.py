@@ -49,6 +49,8 @@ class Config:
     planted: int = 8
     needles: int = 0
     kv_on_host: bool = False
+    chunk0: int = 0  # k0 > 0: a pruning module on chunks of chunk0 tokens in front
+    k0: int = 0
 
 
 CONFIGS: Dict[str, Config] = {
@@ -67,6 +69,11 @@ CONFIGS: Dict[str, Config] = {
     # 1M tokens with 64 extra needles per kv head
     "llama3-8b-1m": Config("llama3-8b-1m", 1, 32, 8, 1048576, None,
                            k1=512, k2=256, sink=128, window=2048, needles=64),
+    # the same with three stacked modules: top-256 chunks of 256 tokens, then top-512 of
+    # their 64-token chunks, then top-256 blocks
+    "llama3-8b-1m-3mod": Config("llama3-8b-1m-3mod", 1, 32, 8, 1048576, None,
+                                k1=512, k2=256, sink=128, window=2048, needles=64,
+                                chunk0=256, k0=256),
     # 3M tokens, bf16 K/V in pinned host memory, int8 keys in HBM
     "llama3-8b-3m-offload": Config("llama3-8b-3m-offload", 1, 32, 8, 3145728, None,
                                    k1=512, k2=256, sink=128, window=2048, kv_on_host=True),

@@ -343,3 +343,13 @@ def test_prune_on_synthetic_maxima(max_pages, chunk, with_tiles, dist):
             assert nc[b, h] == len(chunks) and nb[b, h] == len(blocks)
             np.testing.assert_array_equal(ci[b, h], chunks + [-1] * (k1 - len(chunks)))
             np.testing.assert_array_equal(bi[b, h], blocks + [-1] * (k2 - len(blocks)))
+
+
+@pytest.mark.parametrize("chunk,chunk0,k0,k1,k2", [(64, 256, 6, 20, 15), (32, 128, 3, 10, 40),
+                                                   (64, 64, 40, 10, 10), (64, 512, 2, 8, 8),
+                                                   (64, 256, 100, 20, 15)])
+def test_three_stacked_modules(chunk, chunk0, k0, k1, k2):
+    """A first module on coarse chunks in front of the two others (and K0 >= all coarse
+    chunks, where it keeps everything)."""
+    wl = W.make_workload(_cfg(context=30000, batch=2, hq=8, hkv=2), seed=chunk0 + k0)
+    _check(wl, chunk=chunk, chunk0=chunk0, k0=k0, k1=k1, k2=k2, sink=64, window=128)

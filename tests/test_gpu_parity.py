@@ -53,6 +53,11 @@ def test_llama3_8b_1m_sampled_heads():
     _run(wl, bh_pairs=[(0, 0), (0, 5)])
 
 
+def test_llama3_8b_1m_three_modules_sampled_heads():
+    wl = W.make_workload(W.CONFIGS["llama3-8b-1m-3mod"], seed=0, device="cuda")
+    _run(wl, bh_pairs=[(0, 2), (0, 7)])
+
+
 def test_llama3_8b_3m_offloaded_sampled_head():
     torch.cuda.empty_cache()
     wl = W.make_workload(W.CONFIGS["llama3-8b-3m-offload"], seed=0, device="cuda",
