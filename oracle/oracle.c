@@ -27,7 +27,8 @@
  * Readings where the pages are silent (each is listed in the design notes):
  *  - key scale per (sequence, kv head, channel) over the whole context:
  *      s_c = f32(amax_c / 127), code = clamp(rint_even(f32(k / s_c)), -127, 127),
- *      s_c = 0 gives code 0;
+ *      s_c = 0 gives code 0; the 4-bit key format (N4 variant) uses 7 in place of 127
+ *      for the keys (codes in [-7, 7]), the query codes stay 8-bit;
  *  - the key scales are folded into the query, q'_{j,c} = f32(q_{j,c} * s_c), and the
  *    group of G query heads sharing a kv head is quantised with ONE scale
  *      A = max |q'|, sq = f32(A / 127), qq = clamp(rint_even(f32(q' / sq)), -127, 127);
@@ -64,6 +65,7 @@ typedef struct {
   int32_t chunk, block, k1, k2, sink, window;
   double sm_scale; /* <= 0 means 1/sqrt(head_dim) */
   int32_t chunk0, k0; /* k0 > 0: a first module keeps the top-k0 chunks of chunk0 tokens */
+  int32_t key_bits;   /* 4: 4-bit key codes (levels +-7); 0 or 8: 8-bit (levels +-127) */
 } oracle_dims;
 
 /* ---------------------------------------------------------------- helpers */
@@ -93,6 +95,7 @@ static int dims_ok(const oracle_dims* d) {
   if (d->k1 < 0 || d->k2 < 0 || d->sink < 0 || d->window < 0) return 0;
   if (d->k0 < 0) return 0;
   if (d->k0 > 0 && (d->chunk0 < d->chunk || d->chunk0 % d->chunk)) return 0;
+  if (d->key_bits != 0 && d->key_bits != 4 && d->key_bits != 8) return 0;
   return 1;
 }
 
@@ -110,15 +113,20 @@ static int wanted(const int32_t* bh_mask, const oracle_dims* d, int b, int h) {
   return bh_mask == NULL || bh_mask[b * d->hkv + h] != 0;
 }
 
-/* fp32 round-to-nearest-even code of x / s, clamped to the symmetric int8 range. */
-static int8_t int8_code(double x, float s) {
+/* fp32 round-to-nearest-even code of x / s, clamped to the symmetric range [-levels, levels]. */
+static int8_t key_code(double x, float s, int levels) {
   if (s == 0.0f) return 0;
   float ratio = (float)(x / (double)s);
   double r = nearbyint((double)ratio); /* default rounding mode: half to even */
-  if (r > 127.0) r = 127.0;
-  if (r < -127.0) r = -127.0;
+  if (r > levels) r = levels;
+  if (r < -levels) r = -levels;
   return (int8_t)r;
 }
+
+static int8_t int8_code(double x, float s) { return key_code(x, s, 127); }
+
+/* Largest key code: 127 for 8-bit keys, 7 for the 4-bit key format. */
+static int key_levels(const oracle_dims* d) { return d->key_bits == 4 ? 7 : 127; }
 
 /* ----------------------------------------------- key scales and int8 codes */
 
@@ -142,11 +150,12 @@ int oracle_quantize_keys(const oracle_dims* d, const uint16_t* k, const int32_t*
         double x = fabs(bf16_value(k[cache_index(d, page_table, b, h, t, c)]));
         if (x > amax) amax = x;
       }
-      float s = (float)(amax / 127.0);
+      const int levels = key_levels(d);
+      float s = (float)(amax / (double)levels);
       scale[((int64_t)b * d->hkv + h) * D + c] = s;
       for (int64_t t = 0; t < n; t++) {
         size_t i = cache_index(d, page_table, b, h, t, c);
-        kq[i] = int8_code(bf16_value(k[i]), s);
+        kq[i] = key_code(bf16_value(k[i]), s, levels);
       }
       int64_t end = ((n + d->page_size - 1) / d->page_size) * d->page_size;
       for (int64_t t = n; t < end; t++) kq[cache_index(d, page_table, b, h, t, c)] = 0;
@@ -169,7 +178,8 @@ int oracle_quantize_append(const oracle_dims* d, const uint16_t* k, const int32_
       for (int64_t t = t0; t < n; t++)
         for (int c = 0; c < d->head_dim; c++) {
           size_t i = cache_index(d, page_table, b, h, t, c);
-          kq[i] = int8_code(bf16_value(k[i]), scale[((int64_t)b * d->hkv + h) * d->head_dim + c]);
+          kq[i] = key_code(bf16_value(k[i]), scale[((int64_t)b * d->hkv + h) * d->head_dim + c],
+                           key_levels(d));
         }
   }
   return 0;

@@ -21,7 +21,8 @@ class _CDims(ctypes.Structure):
         "batch", "hq", "hkv", "head_dim", "page_size", "max_pages_per_seq", "num_pages",
         "chunk", "block", "k1", "k2", "sink", "window")] + [("sm_scale", ctypes.c_double),
                                                             ("chunk0", ctypes.c_int32),
-                                                            ("k0", ctypes.c_int32)]
+                                                            ("k0", ctypes.c_int32),
+                                                            ("key_bits", ctypes.c_int32)]
 
 
 @dataclasses.dataclass
@@ -43,10 +44,12 @@ class Dims:
     sm_scale: float = 0.0
     chunk0: int = 0  # k0 > 0: a first module keeps the top-k0 chunks of chunk0 tokens
     k0: int = 0
+    key_bits: int = 0  # 4: 4-bit key codes (levels +-7); 0 or 8: 8-bit
 
     def c(self) -> _CDims:
         return _CDims(*[int(getattr(self, f[0])) for f in _CDims._fields_[:13]],
-                      float(self.sm_scale), int(self.chunk0), int(self.k0))
+                      float(self.sm_scale), int(self.chunk0), int(self.k0),
+                      int(self.key_bits))
 
     @property
     def group(self) -> int:

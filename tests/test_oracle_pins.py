@@ -200,6 +200,53 @@ def test_key_code_error_bound_and_extremes():
         np.testing.assert_array_equal(sc[b], (amax / 127.0).astype(np.float32))
 
 
+def test_four_bit_key_codes_worked_example():
+    """The 4-bit key format by hand: one channel holding 1.75, -0.875, 0.625, 0.25, 0 (all
+    exact in bf16): amax 1.75, s = f32(1.75 / 7) = 0.25 exactly; k / s = 7, -3.5, 2.5, 1, 0
+    -> codes 7, -4, 2, 1, 0 (halves to even); the other channels are zero (scale 0)."""
+    vals = [1.75, -0.875, 0.625, 0.25, 0.0]
+    D = 8
+    k = np.zeros((1, len(vals), D), dtype=np.float32)
+    k[0, :, 3] = vals
+    kc, pt, ln = paged([k], 16, 1)
+    d = Dims(batch=1, hq=1, hkv=1, head_dim=D, page_size=16, max_pages_per_seq=pt.shape[1],
+             num_pages=kc.shape[0], chunk=16, block=16, k1=1, k2=1, sink=0, window=0,
+             key_bits=4)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, ln)
+    assert sc[0, 0, 3] == np.float32(0.25) and (np.delete(sc[0, 0], 3) == 0).all()
+    assert kq[0, 0, :5, 3].tolist() == [7, -4, 2, 1, 0]
+    assert (np.delete(kq[0, 0, :5], 3, axis=1) == 0).all()
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_four_bit_key_codes_bound_and_append(seed):
+    """4-bit codes lie in [-7, 7], reach +-7 at the channel maximum, reconstruct within half a
+    step (the fp32 quotient's own rounding aside), and the append of a token with the stored
+    scales saturates at +-7."""
+    rng = np.random.default_rng(60 + seed)
+    case = random_case(rng, B=1, hq=4, hkv=2, D=16, lens=(150,))
+    d = dims_for(case, 4, 2, 16)
+    d.key_bits = 4
+    kb = bf16_bits(case["k"])
+    kq, sc = oracle.quantize_keys(d, kb, case["pt"], case["lens"])
+    codes = logical_codes(kq, case["pt"], case["lens"], 16, 2)[0]       # [Hkv][N][D]
+    k = case["ks"][0]
+    assert codes.min() >= -7 and codes.max() <= 7
+    for h in range(2):
+        s = sc[0, h].astype(np.float64)
+        err = np.abs(codes[h] * s[None, :] - k[h])
+        assert (err <= s[None, :] * (0.5 + 2.0 ** -17)).all()
+        amax_t = np.abs(k[h]).argmax(axis=0)
+        assert (np.abs(codes[h][amax_t, np.arange(16)]) == 7).all()
+    # append: a token far beyond the stored scales saturates
+    kc2 = case["k"].copy()
+    n = int(case["lens"][0])
+    kc2[case["pt"][0, (n - 1) // 16], :, (n - 1) % 16, :] = 100.0
+    kq2 = oracle.quantize_append(d, bf16_bits(kc2), case["pt"], case["lens"], -1, sc, kq)
+    last = logical_codes(kq2, case["pt"], case["lens"], 16, 2)[0][:, n - 1, :]
+    assert ((last == 7) | (sc[0] == 0)).all()
+
+
 @pytest.mark.parametrize("m", [-3, 2])
 def test_power_of_two_rescale_invariance(m):
     rng = np.random.default_rng(2)
