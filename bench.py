@@ -187,7 +187,8 @@ class Case:
         self.d = hsa.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv,
                           max_pages_per_seq=wl["max_pages"], num_pages=wl["num_pages"],
                           chunk=cfg.chunk, k1=cfg.k1, k2=cfg.k2, sink=cfg.sink,
-                          window=cfg.window, kv_on_host=cfg.kv_on_host)
+                          window=cfg.window, kv_on_host=cfg.kv_on_host, chunk0=cfg.chunk0,
+                          k0=cfg.k0, key_bits=cfg.key_bits)
         d = self.d
         B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
         self.q = wl["q"]
@@ -198,7 +199,9 @@ class Case:
         else:
             self.k = [wl["k_cache"], wl["k_cache"].clone()]
             self.v = [wl["v_cache"], wl["v_cache"].clone()]
-        self.kq = [torch.zeros(self.k[0].shape, dtype=torch.int8, device=device) for _ in range(2)]
+        kq_shape = list(self.k[0].shape)
+        kq_shape[-1] = kq_shape[-1] * cfg.key_bits // 8  # 4-bit codes: two per byte
+        self.kq = [torch.zeros(kq_shape, dtype=torch.int8, device=device) for _ in range(2)]
         self.ks = [torch.zeros((B, Hkv, 128), dtype=torch.float32, device=device)
                    for _ in range(2)]
         wq = hsa.workspace(d, hsa.HSA_OP_QUANTIZE)
@@ -355,7 +358,7 @@ class Case:
     def bytes_score(self):
         c = self.cfg
         blocks = sum(max(0, -(-(n - c.window) // 16) - c.sink // 16) for n in self.wl["lens"])
-        return (c.hkv * self.candidate_tokens() * 128 + c.batch * c.hq * 128 * 2 +
+        return (c.hkv * self.candidate_tokens() * 128 * c.key_bits // 8 + c.batch * c.hq * 128 * 2 +
                 c.batch * c.hkv * 128 * 4 + c.hkv * blocks * 4)
 
     def bytes_attend(self):
@@ -543,7 +546,7 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int):
     od = oracle.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, head_dim=128, page_size=16,
                      max_pages_per_seq=wl["max_pages"], num_pages=wl["num_pages"],
                      chunk=cfg.chunk, block=16, k1=cfg.k1, k2=cfg.k2, sink=cfg.sink,
-                     window=cfg.window)
+                     window=cfg.window, chunk0=cfg.chunk0, k0=cfg.k0, key_bits=cfg.key_bits)
     q, k, v = (W.to_numpy_bits(wl[x]) for x in ("q", "k_cache", "v_cache"))
     pt, lens = wl["page_table"].numpy(), wl["seq_lens"].numpy()
     kq, sc = oracle.quantize_keys(od, k, pt, lens)             # cache state, not per step
@@ -613,10 +616,11 @@ def profile_steps(name, device, steps, warmup):
 
 
 def workload_text(cfg):
+    mod0 = f"chunk0 {cfg.chunk0} keep K0 {cfg.k0}, " if cfg.k0 > 0 else ""
     return (f"{cfg.name}: batch {cfg.batch}, Hq {cfg.hq}, Hkv {cfg.hkv}, d 128, context "
-            f"{cfg.context}, chunk {cfg.chunk} keep K1 {cfg.k1}, block 16 keep K2 {cfg.k2}, "
-            f"sink {cfg.sink}, window {cfg.window}; bf16 K/V in 16-token pages, int8 "
-            f"per-channel keys")
+            f"{cfg.context}, {mod0}chunk {cfg.chunk} keep K1 {cfg.k1}, block 16 keep K2 "
+            f"{cfg.k2}, sink {cfg.sink}, window {cfg.window}; bf16 K/V in 16-token pages, "
+            f"int{cfg.key_bits} per-channel keys")
 
 
 def main():
@@ -672,7 +676,8 @@ def main():
         # the batched paged configuration and the 3M-token offloaded one (K/V in pinned host
         # memory, read over the host link by the attend kernel)
         for name, dense in (("paged-b8-32k-128k", True), ("llama3-8b-3m-offload", False),
-                            ("llama3-8b-1m-3mod", False)):
+                            ("llama3-8b-1m-3mod", True), ("llama3-8b-128k-int4", True),
+                            ("llama3-8b-1m-int4", True)):
             r = gpu_case_numbers(name, rank, device, min(args.steps, 500), args.warmup, None,
                                  peak, world, dense=dense)
             del r["case"]
@@ -685,6 +690,7 @@ def main():
                     "block_cache_slots": Case.CACHE_SLOTS} if r["cached_ms"] else {}),
                 "prune_us": r["per_ms"]["prune"] * 1e3, "attend_us": r["per_ms"]["attend"] * 1e3,
                 "dense_us": r["dense_ms"] * 1e3 if dense else None,
+                "recall_vs_dense": r["recall"] if dense else None,
                 "score_gbs": r["gbs"]["score"],
                 "attend_gbs" + ("_host_link" if r["cached_ms"] else ""): r["gbs"]["attend"],
                 "bytes": r["bytes"], "quantize_keys_ms": r["quantize_ms"],

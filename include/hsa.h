@@ -96,6 +96,9 @@ typedef struct hsa_dims {
   int32_t chunk0;            /* k0 > 0: length of module 0's coarse chunks, a multiple of chunk */
   int32_t k0;                /* coarse chunks kept by module 0, stacked in front of module 1
                                 (which then ranks only the chunks inside them); 0: no module 0 */
+  int32_t key_bits;          /* key codes: 0 or 8 = 8-bit (kq int8 [num_pages][hkv][16][128]);
+                                4 = 4-bit (scale amax / 7, codes in [-7, 7], two per byte: kq
+                                [num_pages][hkv][16][64] bytes, channel 2i in the low nibble) */
 } hsa_dims;
 
 /* Operation ids for hsa_workspace_bytes. */
@@ -117,14 +120,16 @@ const char* hsa_status_string(int32_t status);
 /*
  * Key quantisation (HCAttention abstract: quantised keys kept on the GPU;
  * "KV Cache 与长上下文推理", section "KV Cache 量化": INT8 keys).
- *  mode 0 (FULL): k_scale[b][h][c] = f32(amax / 127) over tokens t < N_b, and the codes
+ *  mode 0 (FULL): k_scale[b][h][c] = f32(amax / L) over tokens t < N_b, and the codes
  *    of every token t < N_b; slots of a last page past N_b get code 0. Needs
- *    HSA_OP_QUANTIZE workspace.
+ *    HSA_OP_QUANTIZE workspace. L = 127 for 8-bit codes, 7 for 4-bit (d->key_bits).
  *  mode 1 (APPEND): codes of tokens [append_from, N_b) of every sequence with the
  *    stored k_scale (append_from < 0: each sequence's last token); values beyond the
- *    stored range saturate at +-127. Workspace may be NULL.
- * k_cache: bf16 paged cache (device, or pinned host when d->kv_on_host). kq: int8
- * paged codes, same layout. k_scale: f32 [batch][hkv][128].
+ *    stored range saturate at +-L. Workspace may be NULL.
+ * k_cache: bf16 paged cache (device, or pinned host when d->kv_on_host). kq: paged codes
+ * on the device, int8 [num_pages][hkv][16][128], or with d->key_bits == 4 two's-complement
+ * nibbles [num_pages][hkv][16][64] bytes (channel 2i in the low nibble of byte i, 2i + 1
+ * in the high one). k_scale: f32 [batch][hkv][128].
  */
 int32_t hsa_quantize_keys(const hsa_dims* d, const void* k_cache, const int32_t* page_table,
                           const int32_t* seq_lens, int32_t mode, int32_t append_from,
@@ -135,7 +140,8 @@ int32_t hsa_quantize_keys(const hsa_dims* d, const void* k_cache, const int32_t*
  * Decode-step append ("KV Cache 与长上下文推理", section "KV Cache 回顾": each step
  * computes the new token's k and v and appends them to the cache). Writes k_new and
  * v_new (bf16 [batch][hkv][128]) into slot N_b - 1 of each sequence's bf16 caches and
- * the new key's int8 codes into kq with the stored k_scale (saturating).
+ * the new key's codes into kq (in d->key_bits' format) with the stored k_scale
+ * (saturating).
  */
 int32_t hsa_append_kv(const hsa_dims* d, const void* k_new, const void* v_new, void* k_cache,
                       void* v_cache, int8_t* kq, const float* k_scale,

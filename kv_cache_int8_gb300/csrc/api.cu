@@ -50,6 +50,7 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
       return HSA_ERR_INVALID_ARG;
   }
   if (!(d->sm_scale == d->sm_scale)) return HSA_ERR_INVALID_ARG;  // NaN
+  if (d->key_bits != 0 && d->key_bits != 4 && d->key_bits != 8) return HSA_ERR_UNSUPPORTED;
   s.batch = d->batch;
   s.hq = d->hq;
   s.hkv = d->hkv;
@@ -63,6 +64,7 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   s.window = d->window;
   s.chunk0 = d->k0 > 0 ? d->chunk0 : 0;
   s.k0 = d->k0;
+  s.key_bits = d->key_bits == 4 ? 4 : 8;
   s.sm_scale = d->sm_scale > 0.0f ? d->sm_scale : 1.0f / std::sqrt((float)hsa::kHeadDim);
   return HSA_OK;
 }
@@ -210,17 +212,18 @@ int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map) {
     CUtensorMap map;
   };
   thread_local Last last;
-  const long long rows = (long long)s.num_pages * s.hkv * hsa::kPage;
+  // 8-bit codes: one 128-byte row per token, 16 rows a block; 4-bit: two tokens a row
+  const int rows_per_block = s.key_bits == 4 ? hsa::kPage / 2 : hsa::kPage;
+  const long long rows = (long long)s.num_pages * s.hkv * rows_per_block;
   if (last.kq == kq && last.rows == rows) {
     *map = last.map;
     return HSA_OK;
   }
   auto fn = encode_fn();
   if (fn == nullptr) return HSA_ERR_CUDA;
-  cuuint64_t dims[2] = {(cuuint64_t)hsa::kHeadDim,
-                        (cuuint64_t)s.num_pages * s.hkv * hsa::kPage};
+  cuuint64_t dims[2] = {(cuuint64_t)hsa::kHeadDim, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)hsa::kHeadDim};
-  cuuint32_t box[2] = {(cuuint32_t)hsa::kHeadDim, (cuuint32_t)hsa::kPage};
+  cuuint32_t box[2] = {(cuuint32_t)hsa::kHeadDim, (cuuint32_t)rows_per_block};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(kq), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -236,11 +236,17 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 // ----------------------------------------------------- int8 code (fp32 RN)
 
-// clamp(rint_half_even(f32(x / s)), -127, 127); s == 0 gives 0.
-__device__ __forceinline__ int int8_code(float x, float s) {
+// clamp(rint_half_even(f32(x / s)), -levels, levels); s == 0 gives 0.
+__device__ __forceinline__ int key_code(float x, float s, int levels) {
   if (s == 0.0f) return 0;
   int r = __float2int_rn(__fdiv_rn(x, s));
-  return max(-127, min(127, r));
+  return max(-levels, min(levels, r));
 }
+
+// clamp(rint_half_even(f32(x / s)), -127, 127); s == 0 gives 0.
+__device__ __forceinline__ int int8_code(float x, float s) { return key_code(x, s, 127); }
+
+// Largest key code of a key format: 127 for 8-bit codes, 7 for 4-bit codes.
+__host__ __device__ __forceinline__ int key_levels(int bits) { return bits == 4 ? 7 : 127; }
 
 }  // namespace hsa

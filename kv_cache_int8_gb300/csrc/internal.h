@@ -13,6 +13,7 @@ struct Shape {
   int batch, hq, hkv, group, max_pages, num_pages;
   int chunk, k1, k2, sink, window;
   int chunk0, k0;  // module 0 (k0 > 0): coarse chunks of chunk0 tokens, top k0
+  int key_bits;    // 8: 8-bit key codes [page][hkv][16][128]; 4: 4-bit, [page][hkv][16][64] bytes
   float sm_scale;  // resolved (> 0)
 };
 

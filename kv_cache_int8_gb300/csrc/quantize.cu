@@ -32,11 +32,29 @@ __device__ __forceinline__ void unpack8(const uint4& u, float f[8]) {
   f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
 }
 
+// Eight 4-bit codes in one word: code 2i in the low nibble of byte i, code 2i + 1 in the high.
+__device__ __forceinline__ uint32_t pack_codes4(const int c[8]) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 4; i++)
+    r |= (uint32_t)((c[2 * i] & 0xF) | ((c[2 * i + 1] & 0xF) << 4)) << (8 * i);
+  return r;
+}
+
 __device__ __forceinline__ uint2 pack_codes(const int c[8]) {
   uint2 r;
   r.x = (c[0] & 0xFF) | ((c[1] & 0xFF) << 8) | ((c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
   r.y = (c[4] & 0xFF) | ((c[5] & 0xFF) << 8) | ((c[6] & 0xFF) << 16) | ((uint32_t)(c[7] & 0xFF) << 24);
   return r;
+}
+
+// The codes of 8 consecutive channels at element offset `off` of the key-code cache:
+// 8 bytes of 8-bit codes, or 4 bytes of 4-bit codes at half the offset.
+__device__ __forceinline__ void store_codes(int8_t* kq, size_t off, const int c[8], int bits) {
+  if (bits == 4)
+    *reinterpret_cast<uint32_t*>(kq + off / 2) = pack_codes4(c);
+  else
+    *reinterpret_cast<uint2*>(kq + off) = pack_codes(c);
 }
 
 // Pass 1 of full quantisation: amax per (b, h, channel) over tokens t < N_b, as the bit
@@ -84,14 +102,16 @@ __global__ void __launch_bounds__(kThreads) key_amax_kernel(
 }
 
 // Pass 2 (full) or append: codes of tokens [t_begin, N_b) with per-channel scales
-// (full: s = f32(amax / 127), also stored; append: the stored scales). Full mode zeroes
-// the codes of last-page slots past N_b.
+// (full: s = f32(amax / levels), also stored, levels 127 for 8-bit and 7 for 4-bit codes;
+// append: the stored scales). Full mode zeroes the codes of last-page slots past N_b.
 __global__ void __launch_bounds__(kThreads) key_codes_kernel(
     const __nv_bfloat16* __restrict__ k_cache, const int32_t* __restrict__ page_table,
     const int32_t* __restrict__ seq_lens, const unsigned* __restrict__ amax_bits,
     const float* __restrict__ k_scale_in, float* __restrict__ k_scale_out, int append_from,
-    int full, int8_t* __restrict__ kq, int hkv, int max_pages, int num_pages, int* err) {
+    int full, int8_t* __restrict__ kq, int hkv, int max_pages, int num_pages, int* err,
+    int bits) {
   const int b = blockIdx.z, h = blockIdx.y;
+  const int levels = key_levels(bits);
   const int slot = threadIdx.x >> 4, grp = threadIdx.x & 15;
   const int n = seq_lens[b];
   if (!seq_ok(n, max_pages)) {
@@ -102,7 +122,8 @@ __global__ void __launch_bounds__(kThreads) key_codes_kernel(
   float s[8];
 #pragma unroll
   for (int i = 0; i < 8; i++)
-    s[i] = full ? __fdiv_rn(__uint_as_float(amax_bits[sbase + i]), 127.0f) : k_scale_in[sbase + i];
+    s[i] = full ? __fdiv_rn(__uint_as_float(amax_bits[sbase + i]), (float)levels)
+                : k_scale_in[sbase + i];
   if (full && blockIdx.x == 0 && slot == 0) {
 #pragma unroll
     for (int i = 0; i < 8; i++) k_scale_out[sbase + i] = s[i];
@@ -127,13 +148,13 @@ __global__ void __launch_bounds__(kThreads) key_codes_kernel(
       float f[8];
       unpack8(ldg128_nc(k_cache + off), f);
 #pragma unroll
-      for (int i = 0; i < 8; i++) c[i] = int8_code(f[i], s[i]);
+      for (int i = 0; i < 8; i++) c[i] = key_code(f[i], s[i], levels);
     } else {
       if (!full) continue;
 #pragma unroll
       for (int i = 0; i < 8; i++) c[i] = 0;
     }
-    *reinterpret_cast<uint2*>(kq + off) = pack_codes(c);
+    store_codes(kq, off, c, bits);
   }
 }
 
@@ -148,18 +169,18 @@ __device__ __forceinline__ void append_body(const uint4* __restrict__ k_new,
                                             int8_t* kq, const float* __restrict__ k_scale,
                                             const int32_t* __restrict__ page_table,
                                             const int32_t* __restrict__ seq_lens, int hkv,
-                                            int max_pages, int num_pages, int* err);
+                                            int max_pages, int num_pages, int* err, int bits);
 
 __global__ void append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                                  __nv_bfloat16* k_cache, __nv_bfloat16* v_cache, int8_t* kq,
                                  const float* __restrict__ k_scale,
                                  const int32_t* __restrict__ page_table,
                                  const int32_t* __restrict__ seq_lens, int hkv, int max_pages,
-                                 int num_pages, int* err, int beside) {
+                                 int num_pages, int* err, int beside, int bits) {
   if (!beside) grid_dep_wait();
   grid_dep_launch();
   append_body(k_new, v_new, k_cache, v_cache, kq, k_scale, page_table, seq_lens, hkv, max_pages,
-              num_pages, err);
+              num_pages, err, bits);
   grid_dep_wait();
 }
 
@@ -169,7 +190,7 @@ __device__ __forceinline__ void append_body(const uint4* __restrict__ k_new,
                                             int8_t* kq, const float* __restrict__ k_scale,
                                             const int32_t* __restrict__ page_table,
                                             const int32_t* __restrict__ seq_lens, int hkv,
-                                            int max_pages, int num_pages, int* err) {
+                                            int max_pages, int num_pages, int* err, int bits) {
   const int b = blockIdx.x;
   const int h = threadIdx.x >> 4, grp = threadIdx.x & 15;
   if (h >= hkv) return;
@@ -194,8 +215,8 @@ __device__ __forceinline__ void append_body(const uint4* __restrict__ k_new,
   const float* s = k_scale + ((size_t)b * hkv + h) * kHeadDim + grp * 8;
   int c[8];
 #pragma unroll
-  for (int i = 0; i < 8; i++) c[i] = int8_code(f[i], s[i]);
-  *reinterpret_cast<uint2*>(kq + off) = pack_codes(c);
+  for (int i = 0; i < 8; i++) c[i] = key_code(f[i], s[i], key_levels(bits));
+  store_codes(kq, off, c, bits);
 }
 
 }  // namespace
@@ -221,7 +242,7 @@ cudaError_t launch_key_codes(const Shape& s, const void* k_cache, const int32_t*
   key_codes_kernel<<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(k_cache),
                                               page_table, seq_lens, amax_bits, k_scale_in,
                                               k_scale_out, append_from, full ? 1 : 0, kq, s.hkv,
-                                              s.max_pages, s.num_pages, err);
+                                              s.max_pages, s.num_pages, err, s.key_bits);
   return cudaGetLastError();
 }
 
@@ -279,7 +300,7 @@ cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_ne
                        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
                        static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache),
                        kq, k_scale, page_table, seq_lens, s.hkv, s.max_pages, s.num_pages, err,
-                       beside ? 1 : 0);
+                       beside ? 1 : 0, s.key_bits);
 }
 
 }  // namespace hsa

@@ -103,9 +103,37 @@ __device__ __forceinline__ void load_query_codes(int (&qq)[G][32], const ScoreAr
   }
 }
 
+// The query code words of the 4-bit key format: word w of head j becomes the codes of
+// channels 8w, 8w+2, 8w+4, 8w+6 (qq[j][w]) and 8w+1, ..., 8w+7 (qq[j][16 + w]), the even and
+// odd channels that one word of packed key nibbles holds.
 template <int G>
+__device__ __forceinline__ void split_query_codes(int (&qq)[G][32]) {
+#pragma unroll
+  for (int j = 0; j < G; j++) {
+    int o[16];
+#pragma unroll
+    for (int w = 0; w < 16; w++) {
+      // reads words 2w and 2w + 1, never yet overwritten (only words below w are)
+      const int e = (int)__byte_perm(qq[j][2 * w], qq[j][2 * w + 1], 0x6420);
+      o[w] = (int)__byte_perm(qq[j][2 * w], qq[j][2 * w + 1], 0x7531);
+      qq[j][w] = e;
+    }
+#pragma unroll
+    for (int w = 0; w < 16; w++) qq[j][16 + w] = o[w];
+  }
+}
+
+// KB4: 4-bit key codes. Two tokens share a 128-byte row of the TMA box (a block is 8 rows,
+// 1 KiB); each 32-bit word holds 8 channels as two's-complement nibbles. Moved into the high
+// half of their bytes (the even channels shifted up by 4, the odd ones masked in place), the
+// nibbles read as signed bytes equal to 16 x code, so two signed dp4a per word give 16 x the
+// dot product, exactly; one arithmetic shift by 4 takes the factor off (|16 x dot| stays
+// below 127 x 128 x 128 x 16 < 2^31).
+template <int G, bool KB4>
 __global__ void __launch_bounds__(kScoreThreads, 2)
     score_blocks_kernel(const __grid_constant__ CUtensorMap kq_map, const ScoreArgs a) {
+  constexpr int kRowsPerBlock = KB4 ? kPage / 2 : kPage;  // rows of the TMA box per block
+  constexpr int kBlockBytes = KB4 ? kBlockBytesI8 / 2 : kBlockBytesI8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -192,7 +220,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
             set_error(a.err, kDevErrCheck);
             continue;
           }
-          rows[i] = (pg[i] * a.hkv + h) * kPage;
+          rows[i] = (pg[i] * a.hkv + h) * kRowsPerBlock;
         }
       }
       const int n = min(32, f1 - f0 - jb);
@@ -209,12 +237,12 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
           } else {
             uint32_t bytes = 0;
 #pragma unroll
-            for (int q = 0; q < kTileBlocks; q++) bytes += rr[q] >= 0 ? kBlockBytesI8 : 0;
+            for (int q = 0; q < kTileBlocks; q++) bytes += rr[q] >= 0 ? kBlockBytes : 0;
             mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
             for (int q = 0; q < kTileBlocks; q++)
               if (rr[q] >= 0)
-                tma_load_2d_hint(ring + s * kStageBytes + q * kBlockBytesI8, &kq_map, 0, rr[q],
+                tma_load_2d_hint(ring + s * kStageBytes + q * kBlockBytes, &kq_map, 0, rr[q],
                                  &full[s], policy);
           }
         }
@@ -249,6 +277,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     const int tile = sr.tile_lo + r % sr.ntile;
     if (b != cur_b || h != cur_h) {
       load_query_codes<G>(qq, a, b, h, lane);
+      if constexpr (KB4) split_query_codes<G>(qq);
       cur_b = b;
       cur_h = h;
     }
@@ -268,15 +297,37 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
       int acc[G];
 #pragma unroll
       for (int jj = 0; jj < G; jj++) acc[jj] = 0;
+      if constexpr (KB4) {
+        // token `row` is half `row & 1` of 128-byte row `row >> 1` of the tile
+        const int r = row >> 1, sub = row & 1;
+        const uint32_t rb = sbase + r * 128;
 #pragma unroll
-      for (int c = 0; c < 8; c++) {
-        const uint4 kv = lds128(rbase + ((c ^ (row & 7)) << 4));
+        for (int c = 0; c < 4; c++) {
+          const uint4 kv = lds128(rb + (((sub * 4 + c) ^ (r & 7)) << 4));
+          const uint32_t wv[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-        for (int jj = 0; jj < G; jj++) {
-          acc[jj] = __dp4a((int)kv.x, qq[jj][4 * c + 0], acc[jj]);
-          acc[jj] = __dp4a((int)kv.y, qq[jj][4 * c + 1], acc[jj]);
-          acc[jj] = __dp4a((int)kv.z, qq[jj][4 * c + 2], acc[jj]);
-          acc[jj] = __dp4a((int)kv.w, qq[jj][4 * c + 3], acc[jj]);
+          for (int m = 0; m < 4; m++) {
+            const int ev = (int)((wv[m] << 4) & 0xF0F0F0F0u), od = (int)(wv[m] & 0xF0F0F0F0u);
+#pragma unroll
+            for (int jj = 0; jj < G; jj++) {
+              acc[jj] = __dp4a(ev, qq[jj][4 * c + m], acc[jj]);
+              acc[jj] = __dp4a(od, qq[jj][16 + 4 * c + m], acc[jj]);
+            }
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < G; jj++) acc[jj] >>= 4;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          const uint4 kv = lds128(rbase + ((c ^ (row & 7)) << 4));
+#pragma unroll
+          for (int jj = 0; jj < G; jj++) {
+            acc[jj] = __dp4a((int)kv.x, qq[jj][4 * c + 0], acc[jj]);
+            acc[jj] = __dp4a((int)kv.y, qq[jj][4 * c + 1], acc[jj]);
+            acc[jj] = __dp4a((int)kv.z, qq[jj][4 * c + 2], acc[jj]);
+            acc[jj] = __dp4a((int)kv.w, qq[jj][4 * c + 3], acc[jj]);
+          }
         }
       }
       int g = acc[0];
@@ -335,32 +386,20 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const
   const long long tiles_max =
       (long long)s.batch * s.hkv * ((s.max_pages + kTileBlocks - 1) / kTileBlocks + 1);
   const int grid = (int)std::min<long long>(tiles_max, 2LL * num_sms);
+  const bool kb4 = s.key_bits == 4;
+  auto go = [&](auto kernel) {
+    cudaError_t e = set_kernel_smem(kernel, smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kernel, dim3(grid), dim3(kScoreThreads), smem, st, true, kq_map, a);
+  };
   cudaError_t e;
   switch (s.group) {
-    case 1:
-      e = set_kernel_smem(score_blocks_kernel<1>, smem);
-      if (e != cudaSuccess) return e;
-      e = launch_kernel(score_blocks_kernel<1>, dim3(grid), dim3(kScoreThreads), smem, st, true,
-                        kq_map, a);
-      if (e != cudaSuccess) return e;
-      break;
-    case 2:
-      e = set_kernel_smem(score_blocks_kernel<2>, smem);
-      if (e != cudaSuccess) return e;
-      e = launch_kernel(score_blocks_kernel<2>, dim3(grid), dim3(kScoreThreads), smem, st, true,
-                        kq_map, a);
-      if (e != cudaSuccess) return e;
-      break;
-    case 4:
-      e = set_kernel_smem(score_blocks_kernel<4>, smem);
-      if (e != cudaSuccess) return e;
-      e = launch_kernel(score_blocks_kernel<4>, dim3(grid), dim3(kScoreThreads), smem, st, true,
-                        kq_map, a);
-      if (e != cudaSuccess) return e;
-      break;
-    default:
-      return cudaErrorInvalidValue;
+    case 1: e = kb4 ? go(score_blocks_kernel<1, true>) : go(score_blocks_kernel<1, false>); break;
+    case 2: e = kb4 ? go(score_blocks_kernel<2, true>) : go(score_blocks_kernel<2, false>); break;
+    case 4: e = kb4 ? go(score_blocks_kernel<4, true>) : go(score_blocks_kernel<4, false>); break;
+    default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -51,6 +51,7 @@ class Config:
     kv_on_host: bool = False
     chunk0: int = 0  # k0 > 0: a pruning module on chunks of chunk0 tokens in front
     k0: int = 0
+    key_bits: int = 8  # key codes: 8-bit, or 4-bit (two per byte)
 
 
 CONFIGS: Dict[str, Config] = {
@@ -74,6 +75,11 @@ CONFIGS: Dict[str, Config] = {
     "llama3-8b-1m-3mod": Config("llama3-8b-1m-3mod", 1, 32, 8, 1048576, None,
                                 k1=512, k2=256, sink=128, window=2048, needles=64,
                                 chunk0=256, k0=256),
+    # the 128K and 1M steps with 4-bit key codes (half the bytes the scorer reads)
+    "llama3-8b-128k-int4": Config("llama3-8b-128k-int4", 1, 32, 8, 131072, None,
+                                  k1=256, k2=128, sink=128, window=1024, key_bits=4),
+    "llama3-8b-1m-int4": Config("llama3-8b-1m-int4", 1, 32, 8, 1048576, None,
+                                k1=512, k2=256, sink=128, window=2048, needles=64, key_bits=4),
     # 3M tokens, bf16 K/V in pinned host memory, int8 keys in HBM
     "llama3-8b-3m-offload": Config("llama3-8b-3m-offload", 1, 32, 8, 3145728, None,
                                    k1=512, k2=256, sink=128, window=2048, kv_on_host=True),

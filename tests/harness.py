@@ -18,22 +18,42 @@ MAX_REL_L2 = 5e-3
 
 def dims_pair(wl: dict, **over):
     """(hsa.Dims, oracle.Dims) for a workload, with optional overrides of k1, k2, sink,
-    window, chunk."""
+    window, chunk, chunk0, k0, key_bits."""
     cfg = wl["config"]
     p = dict(k1=cfg.k1, k2=cfg.k2, sink=cfg.sink, window=cfg.window, chunk=cfg.chunk,
-             chunk0=cfg.chunk0, k0=cfg.k0)
+             chunk0=cfg.chunk0, k0=cfg.k0, key_bits=cfg.key_bits)
     p.update(over)
     hd = hsa.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, max_pages_per_seq=wl["max_pages"],
                   num_pages=wl["num_pages"], chunk=p["chunk"], k1=p["k1"], k2=p["k2"],
                   sink=p["sink"], window=p["window"],
                   kv_on_host=wl["k_cache"].device.type == "cpu" and wl["k_cache"].is_pinned(),
-                  chunk0=p["chunk0"], k0=p["k0"])
+                  chunk0=p["chunk0"], k0=p["k0"], key_bits=p["key_bits"])
     od = oracle.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, head_dim=W.HEAD_DIM,
                      page_size=W.PAGE, max_pages_per_seq=wl["max_pages"],
                      num_pages=wl["num_pages"], chunk=p["chunk"], block=16, k1=p["k1"],
                      k2=p["k2"], sink=p["sink"], window=p["window"], chunk0=p["chunk0"],
-                     k0=p["k0"])
+                     k0=p["k0"], key_bits=p["key_bits"])
     return hd, od
+
+
+def kq_like(k_cache: torch.Tensor, d: hsa.Dims) -> torch.Tensor:
+    """A zeroed device key-code cache for a bf16 cache of shape [P][Hkv][16][128]: int8
+    codes of the same shape, or with 4-bit codes [P][Hkv][16][64] bytes."""
+    shape = list(k_cache.shape)
+    if d.key_bits == 4:
+        shape[-1] //= 2
+    return torch.zeros(shape, dtype=torch.int8, device="cuda")
+
+
+def unpack_codes(kq: np.ndarray, key_bits: int) -> np.ndarray:
+    """The codes of a key-code cache as int8 [..][128]: 8-bit codes as they are; 4-bit ones
+    from their two's-complement nibbles (channel 2i in the low nibble of byte i)."""
+    if key_bits != 4:
+        return kq
+    u = kq.view(np.uint8).astype(np.int16)
+    lo = ((u & 0xF) ^ 8) - 8
+    hi = ((u >> 4) ^ 8) - 8
+    return np.stack([lo, hi], axis=-1).reshape(*kq.shape[:-1], 2 * kq.shape[-1]).astype(np.int8)
 
 
 def to_cuda(wl: dict) -> dict:
@@ -50,7 +70,7 @@ def gpu_step(wl: dict, d: hsa.Dims, dense: bool = True) -> dict:
     """Quantise the keys, score, prune, attend (and dense decode) through the C ABI."""
     dev = torch.device("cuda")
     B, Hq, Hkv = d.batch, d.hq, d.hkv
-    kq = torch.zeros(wl["k_cache"].shape, dtype=torch.int8, device=dev)
+    kq = kq_like(wl["k_cache"], d)
     k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
     wq = hsa.workspace(d, hsa.HSA_OP_QUANTIZE)
     hsa.hsa_quantize_keys(d, wl["k_cache"], wl["page_table"], wl["seq_lens"], 0, 0, kq, k_scale, wq)
@@ -97,7 +117,9 @@ def gpu_step(wl: dict, d: hsa.Dims, dense: bool = True) -> dict:
     torch.cuda.synchronize()
     for name, w in (("quantize", wq), ("select", ws), ("attend", wa)):
         assert hsa.hsa_read_device_error(w) == 0, f"device error word set by {name}"
-    return {k: v.cpu().numpy() for k, v in res.items()}
+    res = {k: v.cpu().numpy() for k, v in res.items()}
+    res["kq"] = unpack_codes(res["kq"], d.key_bits)
+    return res
 
 
 def host_arrays(wl: dict) -> dict:

@@ -21,12 +21,13 @@ def _clone(t):
     return t.clone().pin_memory() if t.device.type == "cpu" else t.clone()
 
 
-@pytest.mark.parametrize("refresh,on_host", [(3, False), (2, True), (1, False)])
-def test_decode_loop_with_selection_reuse(refresh, on_host):
+@pytest.mark.parametrize("refresh,on_host,key_bits", [(3, False, 8), (2, True, 8), (1, False, 8),
+                                                       (2, False, 4)])
+def test_decode_loop_with_selection_reuse(refresh, on_host, key_bits):
     steps = 6
     cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None,
                               context_range=(3000, 6000), batch=2, hq=8, hkv=2, k1=12, k2=10,
-                              sink=32, window=96, paged_permuted=True)
+                              sink=32, window=96, paged_permuted=True, key_bits=key_bits)
     wl = W.make_workload(cfg, seed=77 + refresh, host_pinned=on_host)
     hd, od = H.dims_pair(wl)
     dwl = H.to_cuda(wl)
@@ -36,7 +37,7 @@ def test_decode_loop_with_selection_reuse(refresh, on_host):
     start = wl["seq_lens"] - steps
     pt = wl["page_table"].numpy()
     kc, vc = _clone(dwl["k_cache"]), _clone(dwl["v_cache"])
-    kq = torch.zeros(kc.shape, dtype=torch.int8, device=dev)
+    kq = H.kq_like(kc, hd)
     k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
     hsa.hsa_quantize_keys(hd, kc, dwl["page_table"], start.to(dev), 0, 0, kq, k_scale,
                           hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
@@ -73,7 +74,7 @@ def test_decode_loop_with_selection_reuse(refresh, on_host):
         np.testing.assert_array_equal(W.to_numpy_bits(kc.cpu()), k_host)
         np.testing.assert_array_equal(W.to_numpy_bits(vc.cpu()), v_host)
         kq_o = oracle.quantize_append(od, k_host, pt, lens.numpy(), -1, sc_o, kq_o)
-        np.testing.assert_array_equal(kq.cpu().numpy(), kq_o)
+        np.testing.assert_array_equal(H.unpack_codes(kq.cpu().numpy(), key_bits), kq_o)
         qb = W.to_numpy_bits(q)
         if full:
             sel = oracle.select(od, qb, sc_o, kq_o, pt, lens.numpy())

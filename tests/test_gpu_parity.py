@@ -2,6 +2,8 @@
 inputs. Integer outputs (key codes and scales, block maxima, kept chunk and block indices
 and counts) must match bit for bit; attention outputs must satisfy max|err| <= 1e-2 and
 relative L2 <= 5e-3 against the fp64 oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -56,6 +58,32 @@ def test_llama3_8b_1m_sampled_heads():
 def test_llama3_8b_1m_three_modules_sampled_heads():
     wl = W.make_workload(W.CONFIGS["llama3-8b-1m-3mod"], seed=0, device="cuda")
     _run(wl, bh_pairs=[(0, 2), (0, 7)])
+
+
+def test_tiny_8k_four_bit_keys():
+    """4-bit key codes: codes (unpacked from their nibbles), scales amax / 7, block maxima
+    and selections bit-exact against the oracle's 4-bit format; outputs within tolerance."""
+    wl = W.make_workload(W.CONFIGS["tiny-8k"], seed=4)
+    stats, g, o = _run(wl, key_bits=4)
+    assert np.abs(g["kq"]).max() == 7
+
+
+def test_paged_batch_four_bit_keys():
+    """Ragged lengths, a permuted page pool and last pages past N_b with 4-bit codes."""
+    cfg = dataclasses.replace(W.CONFIGS["paged-b8-32k-128k"], context_range=(1000, 9000),
+                              batch=3, key_bits=4)
+    wl = W.make_workload(cfg, seed=8)
+    _run(wl)
+
+
+def test_llama3_8b_128k_four_bit_keys_full():
+    wl = W.make_workload(W.CONFIGS["llama3-8b-128k-int4"], seed=0, device="cuda")
+    _run(wl)
+
+
+def test_llama3_8b_1m_four_bit_keys_sampled_heads():
+    wl = W.make_workload(W.CONFIGS["llama3-8b-1m-int4"], seed=0, device="cuda")
+    _run(wl, bh_pairs=[(0, 1), (0, 6)])
 
 
 def test_llama3_8b_3m_offloaded_sampled_head():
