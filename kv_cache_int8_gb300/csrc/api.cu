@@ -201,22 +201,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view of the int8 code cache: rows of 128 bytes, one per (page, head, slot); a box is
-// one (page, head) block of 16 rows, stored with the 128-byte swizzle.
-int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map) {
-  // the map depends only on the base pointer and the row count: the last one of this thread
-  // is reused
+// Two views of the key-code cache, both stored with the 128-byte swizzle. map: 2-D, rows of
+// 128 bytes (one token of 8-bit codes, two of 4-bit codes), a box is one (page, head) block.
+// map4: 4-D [page][head][row][128 B], a box is the blocks of one head in 4 consecutive pages
+// (one copy instead of four where the page table is contiguous).
+int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map, CUtensorMap* map4) {
+  // the maps depend only on the base pointer and the shape: the last pair of this thread is
+  // reused
   struct Last {
     const int8_t* kq = nullptr;
-    long long rows = -1;
-    CUtensorMap map;
+    long long pages = -1;
+    int hkv = -1, rows_per_block = -1;
+    CUtensorMap map, map4;
   };
   thread_local Last last;
   // 8-bit codes: one 128-byte row per token, 16 rows a block; 4-bit: two tokens a row
   const int rows_per_block = s.key_bits == 4 ? hsa::kPage / 2 : hsa::kPage;
   const long long rows = (long long)s.num_pages * s.hkv * rows_per_block;
-  if (last.kq == kq && last.rows == rows) {
+  if (last.kq == kq && last.pages == s.num_pages && last.hkv == s.hkv &&
+      last.rows_per_block == rows_per_block) {
     *map = last.map;
+    *map4 = last.map4;
     return HSA_OK;
   }
   auto fn = encode_fn();
@@ -224,14 +229,26 @@ int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map) {
   cuuint64_t dims[2] = {(cuuint64_t)hsa::kHeadDim, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)hsa::kHeadDim};
   cuuint32_t box[2] = {(cuuint32_t)hsa::kHeadDim, (cuuint32_t)rows_per_block};
-  cuuint32_t estr[2] = {1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(kq), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return HSA_ERR_CUDA;
+  const cuuint64_t blk = (cuuint64_t)rows_per_block * hsa::kHeadDim;  // bytes per block
+  cuuint64_t dims4[4] = {(cuuint64_t)hsa::kHeadDim, (cuuint64_t)rows_per_block,
+                         (cuuint64_t)s.hkv, (cuuint64_t)s.num_pages};
+  cuuint64_t strides4[3] = {(cuuint64_t)hsa::kHeadDim, blk, blk * s.hkv};
+  cuuint32_t box4[4] = {(cuuint32_t)hsa::kHeadDim, (cuuint32_t)rows_per_block, 1, 4};
+  r = fn(map4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<int8_t*>(kq), dims4, strides4, box4,
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return HSA_ERR_CUDA;
   last.kq = kq;
-  last.rows = rows;
+  last.pages = s.num_pages;
+  last.hkv = s.hkv;
+  last.rows_per_block = rows_per_block;
   last.map = *map;
+  last.map4 = *map4;
   return HSA_OK;
 }
 
@@ -268,11 +285,11 @@ inline cudaStream_t as_stream(void* p) { return reinterpret_cast<cudaStream_t>(p
 int32_t do_score(const Shape& s, const void* q, const int8_t* kq, const float* k_scale,
                  const int32_t* page_table, const int32_t* seq_lens, int32_t* block_max,
                  int32_t* tile_max, int* err, cudaStream_t st) {
-  CUtensorMap map;
-  int32_t rc = encode_kq_map(s, kq, &map);
+  CUtensorMap map, map4;
+  int32_t rc = encode_kq_map(s, kq, &map, &map4);
   if (rc != HSA_OK) return rc;
-  return cuda_status(hsa::launch_score_blocks(s, map, q, k_scale, page_table, seq_lens, block_max,
-                                              tile_max, err, num_sms(), st));
+  return cuda_status(hsa::launch_score_blocks(s, map, map4, q, k_scale, page_table, seq_lens,
+                                              block_max, tile_max, err, num_sms(), st));
 }
 
 int32_t check_prune_fits(const Shape& s) {

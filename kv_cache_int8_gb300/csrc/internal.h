@@ -41,7 +41,8 @@ cudaError_t launch_stage_io(const Shape& s, const void* q, const void* k_new, co
 // block_max: [B][Hkv][max_pages]; tile_max (nullable): [B][Hkv][score_max_tiles], the max of
 // each 64-token tile, which the prune kernel uses as the chunk score when chunks are 64.
 int score_max_tiles(const Shape& s);
-cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const void* q,
+cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
+                                const CUtensorMap& kq_map4, const void* q,
                                 const float* k_scale, const int32_t* page_table,
                                 const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
                                 int* err, int num_sms, cudaStream_t st);

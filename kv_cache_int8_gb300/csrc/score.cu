@@ -1,38 +1,71 @@
-// score.cu -- global int8 scoring of every candidate token.
+// score.cu -- global scoring of every candidate token over the quantised keys.
 //
 // Sources: "HCAttention: Extreme KV cache compression via heterogeneous attention computing
 // for LLMs", abstract and contribution list (global approximate attention scoring over the
 // GPU-resident quantised keys); "KV Cache 与长上下文推理", section "MQA 与 GQA" (G query heads
-// share one kv head); InfiniteHiP article (163.com), section "实现 7.24 倍的端到端解码加速"
-// (each chunk's best token is what the pruning module ranks: here exact per-block and
-// per-64-token-tile maxima of the token scores).
+// share one kv head) and section "KV Cache 量化" (INT8 and INT4 key formats); InfiniteHiP
+// article (163.com), section "实现 7.24 倍的端到端解码加速" (each chunk's best token is what
+// the pruning module ranks: here exact per-block and per-64-token-tile maxima of the token
+// scores).
 //
 // score_blocks_kernel (the HBM-bound scan): a persistent grid walks the flattened list of
 // 64-token tiles (sequence, kv head, tile). One producer lane per CTA streams each tile's
-// four 2 KiB (page, head) blocks into a shared-memory ring with TMA tensor copies
-// (128-byte swizzle, so the token-per-lane reads below are bank-conflict free) and
-// mbarrier transaction counts. Consumer warps own fixed ring slots; lane = token, the
-// G x 32 packed int8 query words sit in registers, dp4a gives the G exact int32 dot
-// products, their max is the token score and a 16-lane max gives the block maximum.
+// four (page, head) blocks into a shared-memory ring with TMA tensor copies (one 4-page copy
+// where the pages are consecutive; 128-byte swizzle, so the token-per-lane reads below are
+// bank-conflict free) and mbarrier transaction counts. Consumer warps own fixed ring slots;
+// lane = token (two tokens per lane, the tile's two halves), dp4a gives the G exact int32
+// dot products, their max is the token score and a 16-lane max gives the block maximum.
+// 8-bit codes with G <= 4 keep the G x 32 packed query words in registers; 4-bit codes and
+// G = 8 read them from a per-warp shared-memory copy, which leaves room for more warps.
 #include <algorithm>
 #include <climits>
 
 #include "common.cuh"
 #include "internal.h"
 
+// Tuning of the 4-bit-code instances: consumer warps per CTA, resident CTAs per SM and the
+// ring of one CTA (KiB). Measured on GB300 at 1M tokens: 4 warps x 3 CTAs with a 64 KiB ring
+// beats 8 x 2 (113 against 141 us); 4 x 4 with 48 KiB rings is no faster.
+#ifndef HSA_SCORE_QS_WARPS
+#define HSA_SCORE_QS_WARPS 4
+#endif
+#ifndef HSA_SCORE_QS_CTAS
+#define HSA_SCORE_QS_CTAS 3
+#endif
+#ifndef HSA_SCORE_QS_RING_KB
+#define HSA_SCORE_QS_RING_KB 64
+#endif
+
 namespace hsa {
 namespace {
 
 // ------------------------------------------------------------------ scorer
 
-constexpr int kTileBlocks = 4;                             // blocks per ring slot (64 tokens)
+constexpr int kTileBlocks = 4;                  // blocks per ring slot (64 tokens)
 constexpr int kTileTokens = kTileBlocks * kPage;
-constexpr int kStageBytes = kTileBlocks * kBlockBytesI8;   // 8 KiB
-constexpr int kScoreWarps = 4;                             // consumer warps
-constexpr int kScoreStages = 8;                            // ring slots (multiple of kScoreWarps)
-constexpr int kScoreThreads = (kScoreWarps + 1) * 32;
-constexpr int kMaxBatch = 1024;
-static_assert(kScoreStages % kScoreWarps == 0, "each consumer warp owns fixed ring slots");
+constexpr int kMaxBatch = 1024;                 // sequences (the tile prefix sums in shared memory)
+
+// Launch shape and shared-memory layout of one scorer instance.
+template <int G, bool KB4>
+struct ScoreCfg {
+  static constexpr bool kQSmem = KB4 || G > 4;  // query words in shared memory
+  static constexpr int kWarps = KB4 ? HSA_SCORE_QS_WARPS : 4;  // consumer warps
+  static constexpr int kThreads = (kWarps + 1) * 32;
+  static constexpr int kCtasPerSm = KB4 ? HSA_SCORE_QS_CTAS : (G > 4 ? 3 : 2);
+  // 8-bit codes: one 128-byte row per token; 4-bit codes: two tokens per row
+  static constexpr int kRowsPerBlock = KB4 ? kPage / 2 : kPage;
+  static constexpr int kBlockBytes = kRowsPerBlock * kHeadDim;
+  static constexpr int kSlotBytes = kTileBlocks * kBlockBytes;
+  static constexpr int kRingBytes = (KB4 ? HSA_SCORE_QS_RING_KB : 64) * 1024;  // ring of one CTA
+  static constexpr int kStages = kRingBytes / kSlotBytes;
+  static_assert(kStages % kWarps == 0 && kStages / kWarps >= 2,
+                "every consumer warp owns at least two fixed ring slots");
+  static constexpr int kQWords = kQSmem ? kWarps * G * 32 : 0;
+  static size_t smem_bytes(int batch) {
+    return 1024 + kRingBytes + 2 * kStages * sizeof(uint64_t) + kQWords * sizeof(int) +
+           (batch + 1) * sizeof(int);
+  }
+};
 
 struct ScoreArgs {
   const __nv_bfloat16* q;
@@ -69,11 +102,10 @@ __device__ __forceinline__ SeqRange seq_range(const ScoreArgs& a, int b) {
   return r;
 }
 
-// Query folding and quantisation for (b, h), executed by one whole warp. Lane l computes
-// channels [4l, 4l+4) of each of the G heads; the packed code words are then broadcast so
-// that every lane holds all G x 32 words (uniform registers of the dot-product loop).
+// Query folding and quantisation for (b, h), executed by one whole warp: lane l returns the
+// packed codes of channels [4l, 4l+4) of each of the G heads.
 template <int G>
-__device__ __forceinline__ void load_query_codes(int (&qq)[G][32], const ScoreArgs& a, int b,
+__device__ __forceinline__ void fold_query_words(int (&word)[G], const ScoreArgs& a, int b,
                                                  int h, int lane) {
   const float4 s4 =
       *reinterpret_cast<const float4*>(a.k_scale + ((size_t)b * a.hkv + h) * kHeadDim + 4 * lane);
@@ -95,57 +127,78 @@ __device__ __forceinline__ void load_query_codes(int (&qq)[G][32], const ScoreAr
   const float sq = __fdiv_rn(amax, 127.0f);
 #pragma unroll
   for (int j = 0; j < G; j++) {
-    int word = 0;
+    int v = 0;
 #pragma unroll
-    for (int i = 0; i < 4; i++) word |= (int8_code(qp[j][i], sq) & 0xFF) << (8 * i);
-#pragma unroll
-    for (int c = 0; c < 32; c++) qq[j][c] = __shfl_sync(0xffffffffu, word, c);
+    for (int i = 0; i < 4; i++) v |= (int8_code(qp[j][i], sq) & 0xFF) << (8 * i);
+    word[j] = v;
   }
 }
 
-// The query code words of the 4-bit key format: word w of head j becomes the codes of
-// channels 8w, 8w+2, 8w+4, 8w+6 (qq[j][w]) and 8w+1, ..., 8w+7 (qq[j][16 + w]), the even and
-// odd channels that one word of packed key nibbles holds.
+// Register copy: every lane holds all G x 32 words (word c of head j = channels 4c..4c+3).
 template <int G>
-__device__ __forceinline__ void split_query_codes(int (&qq)[G][32]) {
+__device__ __forceinline__ void load_query_codes(int (&qq)[G][32], const ScoreArgs& a, int b,
+                                                 int h, int lane) {
+  int word[G];
+  fold_query_words<G>(word, a, b, h, lane);
+#pragma unroll
+  for (int j = 0; j < G; j++)
+#pragma unroll
+    for (int c = 0; c < 32; c++) qq[j][c] = __shfl_sync(0xffffffffu, word[j], c);
+}
+
+// Shared-memory copy qs[G][32] of the warp. 8-bit keys: word c of head j = channels
+// 4c..4c+3. 4-bit keys: words 0..15 hold channels 8w, 8w+2, 8w+4, 8w+6 and words 16..31
+// channels 8w+1, ..., 8w+7: the even and odd channels that one word of packed key nibbles
+// holds.
+template <int G, bool KB4>
+__device__ __forceinline__ void store_query_codes(int* qs, const ScoreArgs& a, int b, int h,
+                                                  int lane) {
+  int word[G];
+  fold_query_words<G>(word, a, b, h, lane);
 #pragma unroll
   for (int j = 0; j < G; j++) {
-    int o[16];
-#pragma unroll
-    for (int w = 0; w < 16; w++) {
-      // reads words 2w and 2w + 1, never yet overwritten (only words below w are)
-      const int e = (int)__byte_perm(qq[j][2 * w], qq[j][2 * w + 1], 0x6420);
-      o[w] = (int)__byte_perm(qq[j][2 * w], qq[j][2 * w + 1], 0x7531);
-      qq[j][w] = e;
+    int v = word[j];
+    if constexpr (KB4) {
+      // lane l < 16: even channels of words 2l and 2l + 1; lane l >= 16: their odd channels
+      const int p = 2 * (lane & 15);
+      const int w0 = __shfl_sync(0xffffffffu, v, p), w1 = __shfl_sync(0xffffffffu, v, p + 1);
+      v = (int)__byte_perm(w0, w1, lane < 16 ? 0x6420 : 0x7531);
     }
-#pragma unroll
-    for (int w = 0; w < 16; w++) qq[j][16 + w] = o[w];
+    qs[j * 32 + lane] = v;
   }
 }
 
-// KB4: 4-bit key codes. Two tokens share a 128-byte row of the TMA box (a block is 8 rows,
-// 1 KiB); each 32-bit word holds 8 channels as two's-complement nibbles. Moved into the high
-// half of their bytes (the even channels shifted up by 4, the odd ones masked in place), the
-// nibbles read as signed bytes equal to 16 x code, so two signed dp4a per word give 16 x the
-// dot product, exactly; one arithmetic shift by 4 takes the factor off (|16 x dot| stays
+// 4-bit codes: a 32-bit word holds 8 channels as two's-complement nibbles. Moved into the
+// high half of their bytes (the even channels shifted up by 4, the odd ones masked in place),
+// the nibbles read as signed bytes equal to 16 x code, so two signed dp4a per word give 16 x
+// the dot product, exactly; one arithmetic shift by 4 takes the factor off (|16 x dot| stays
 // below 127 x 128 x 128 x 16 < 2^31).
+__device__ __forceinline__ int nibbles_even(uint32_t w) { return (int)((w << 4) & 0xF0F0F0F0u); }
+__device__ __forceinline__ int nibbles_odd(uint32_t w) { return (int)(w & 0xF0F0F0F0u); }
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
+  return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
+}
+
 template <int G, bool KB4>
-__global__ void __launch_bounds__(kScoreThreads, 2)
-    score_blocks_kernel(const __grid_constant__ CUtensorMap kq_map, const ScoreArgs a) {
-  constexpr int kRowsPerBlock = KB4 ? kPage / 2 : kPage;  // rows of the TMA box per block
-  constexpr int kBlockBytes = KB4 ? kBlockBytesI8 / 2 : kBlockBytesI8;
+__global__ void __launch_bounds__(ScoreCfg<G, KB4>::kThreads, ScoreCfg<G, KB4>::kCtasPerSm)
+    score_blocks_kernel(const __grid_constant__ CUtensorMap kq_map,
+                        const __grid_constant__ CUtensorMap kq_map4, const ScoreArgs a) {
+  using C = ScoreCfg<G, KB4>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kScoreStages * kStageBytes);
-  uint64_t* empty = full + kScoreStages;
-  int* prefix = reinterpret_cast<int*>(empty + kScoreStages);  // [batch + 1] tiles before b
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
+  uint64_t* empty = full + kStages;
+  int* qbuf = reinterpret_cast<int*>(empty + kStages);  // [consumer warp][G][32] (kQSmem)
+  int* prefix = qbuf + C::kQWords;                       // [batch + 1] tiles before b
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kScoreStages; s++) {
+    for (int s = 0; s < kStages; s++) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -154,7 +207,10 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   // inputs may come from the previous kernel of the stream; then let the next one launch
   grid_dep_wait();
   grid_dep_launch();
-  if (warp == kScoreWarps && lane == 0) tma_prefetch_descriptor(&kq_map);
+  if (warp == C::kWarps && lane == 0) {
+    tma_prefetch_descriptor(&kq_map);
+    tma_prefetch_descriptor(&kq_map4);
+  }
   // tiles per sequence (x hkv), exclusive prefix sum by warp 0
   if (warp == 0) {
     int carry = 0;
@@ -187,10 +243,11 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   int b = 0;
   while (prefix[b + 1] <= f0) b++;
 
-  if (warp == kScoreWarps) {
+  if (warp == C::kWarps) {
     // ------------------------------------------------------------ producer
     // The whole warp resolves the page ids of the next 32 tiles at once (one coalesced
-    // round trip), then lane 0 issues their copies in order as ring slots free up.
+    // round trip), then lane 0 issues their copies in order as ring slots free up: one copy
+    // of the four blocks when they sit in consecutive pages, else one copy per block.
     bool ok = true;
     const uint64_t policy = l2_evict_first_policy();  // each code is read once
     int bw = b;  // sequence of tile f0 + jb (warp-uniform)
@@ -199,6 +256,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
       int rows[kTileBlocks];
 #pragma unroll
       for (int i = 0; i < kTileBlocks; i++) rows[i] = -1;
+      int run_page = -1, run_head = 0;  // first page of 4 consecutive ones, and the head
       if (f < f1) {
         int bl = bw;
         while (prefix[bl + 1] <= f) bl++;
@@ -220,7 +278,14 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
             set_error(a.err, kDevErrCheck);
             continue;
           }
-          rows[i] = (pg[i] * a.hkv + h) * kRowsPerBlock;
+          rows[i] = (pg[i] * a.hkv + h) * C::kRowsPerBlock;
+        }
+        bool run = rows[0] >= 0;
+#pragma unroll
+        for (int i = 1; i < kTileBlocks; i++) run = run && rows[i] >= 0 && pg[i] == pg[0] + i;
+        if (run) {
+          run_page = pg[0];
+          run_head = h;
         }
       }
       const int n = min(32, f1 - f0 - jb);
@@ -228,22 +293,28 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
         int rr[kTileBlocks];
 #pragma unroll
         for (int q = 0; q < kTileBlocks; q++) rr[q] = __shfl_sync(0xffffffffu, rows[q], i);
+        const int rp = __shfl_sync(0xffffffffu, run_page, i);
+        const int rh = __shfl_sync(0xffffffffu, run_head, i);
         if (lane == 0) {
           const int j = jb + i;
-          const int s = j % kScoreStages;
-          if (j >= kScoreStages && !mbar_wait(&empty[s], ((j / kScoreStages) - 1) & 1)) {
+          const int s = j % kStages;
+          if (j >= kStages && !mbar_wait(&empty[s], ((j / kStages) - 1) & 1)) {
             set_error(a.err, kDevErrTimeout);
             ok = false;
           } else {
             uint32_t bytes = 0;
 #pragma unroll
-            for (int q = 0; q < kTileBlocks; q++) bytes += rr[q] >= 0 ? kBlockBytes : 0;
+            for (int q = 0; q < kTileBlocks; q++) bytes += rr[q] >= 0 ? C::kBlockBytes : 0;
             mbar_arrive_expect_tx(&full[s], bytes);
+            uint8_t* dst = ring + s * C::kSlotBytes;
+            if (rp >= 0) {
+              tma_load_4d_hint(dst, &kq_map4, 0, 0, rh, rp, &full[s], policy);
+            } else {
 #pragma unroll
-            for (int q = 0; q < kTileBlocks; q++)
-              if (rr[q] >= 0)
-                tma_load_2d_hint(ring + s * kStageBytes + q * kBlockBytes, &kq_map, 0, rr[q],
-                                 &full[s], policy);
+              for (int q = 0; q < kTileBlocks; q++)
+                if (rr[q] >= 0)
+                  tma_load_2d_hint(dst + q * C::kBlockBytes, &kq_map, 0, rr[q], &full[s], policy);
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -256,17 +327,19 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     if (!ok && lane == 0) {
       // let the copies already issued land before the CTA exits (bounded)
       const int issued = f1 - f0;
-      for (int j = max(0, issued - kScoreStages); j < issued; j++)
-        mbar_wait(&full[j % kScoreStages], (j / kScoreStages) & 1);
+      for (int j = max(0, issued - kStages); j < issued; j++)
+        mbar_wait(&full[j % kStages], (j / kStages) & 1);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  int qq[G][32];
+  int qq[C::kQSmem ? 1 : G][32];  // register copy of the query words (8-bit codes, G <= 4)
+  int* qs = qbuf + (C::kQSmem ? warp * G * 32 : 0);
+  const uint32_t qs_addr = smem_addr(qs);
   int cur_b = -1, cur_h = -1;
   SeqRange sr = seq_range(a, b);
-  for (int j = warp; f0 + j < f1; j += kScoreWarps) {
+  for (int j = warp; f0 + j < f1; j += C::kWarps) {
     const int f = f0 + j;
     while (prefix[b + 1] <= f) {
       b++;
@@ -276,63 +349,93 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     const int h = r / sr.ntile;
     const int tile = sr.tile_lo + r % sr.ntile;
     if (b != cur_b || h != cur_h) {
-      load_query_codes<G>(qq, a, b, h, lane);
-      if constexpr (KB4) split_query_codes<G>(qq);
+      if constexpr (C::kQSmem) {
+        __syncwarp();  // every lane is done reading the previous words
+        store_query_codes<G, KB4>(qs, a, b, h, lane);
+        __syncwarp();
+      } else {
+        load_query_codes<G>(qq, a, b, h, lane);
+      }
       cur_b = b;
       cur_h = h;
     }
-    const int s = j % kScoreStages;
-    if (!mbar_wait(&full[s], (j / kScoreStages) & 1)) {
+    const int s = j % kStages;
+    if (!mbar_wait(&full[s], (j / kStages) & 1)) {
       set_error(a.err, kDevErrTimeout);
       break;
     }
-    const uint32_t sbase = smem_addr(ring + s * kStageBytes);
+    const uint32_t sbase = smem_addr(ring + s * C::kSlotBytes);
     int32_t* out = a.block_max + ((size_t)b * a.hkv + h) * a.max_pages;
+    // both 32-token halves of the tile at once (lane = token `half * 32 + lane`)
+    int acc[2][G];
+#pragma unroll
+    for (int half = 0; half < 2; half++)
+#pragma unroll
+      for (int jj = 0; jj < G; jj++) acc[half][jj] = 0;
+    if constexpr (KB4) {
+      // token `row` is half `row & 1` of 128-byte row `row >> 1` of the tile; the row's
+      // swizzle phase (row >> 1) & 7 is the same for both halves
+      const int sub = lane & 1, ph = (lane >> 1) & 7;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        int ev[2][4], od[2][4];
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+          const uint4 kv =
+              lds128(sbase + (half * 16 + (lane >> 1)) * 128 + (((sub * 4 + c) ^ ph) << 4));
+#pragma unroll
+          for (int m = 0; m < 4; m++) {
+            ev[half][m] = nibbles_even(word_of(kv, m));
+            od[half][m] = nibbles_odd(word_of(kv, m));
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < G; jj++) {
+          const uint4 qe = lds128(qs_addr + (jj * 32 + 4 * c) * 4);
+          const uint4 qo = lds128(qs_addr + (jj * 32 + 16 + 4 * c) * 4);
+#pragma unroll
+          for (int m = 0; m < 4; m++)
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+              acc[half][jj] = __dp4a(ev[half][m], (int)word_of(qe, m), acc[half][jj]);
+              acc[half][jj] = __dp4a(od[half][m], (int)word_of(qo, m), acc[half][jj]);
+            }
+        }
+      }
+#pragma unroll
+      for (int half = 0; half < 2; half++)
+#pragma unroll
+        for (int jj = 0; jj < G; jj++) acc[half][jj] >>= 4;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; c++) {
+        uint4 kv[2];
+#pragma unroll
+        for (int half = 0; half < 2; half++)
+          kv[half] = lds128(sbase + (half * 32 + lane) * kHeadDim + ((c ^ (lane & 7)) << 4));
+#pragma unroll
+        for (int jj = 0; jj < G; jj++) {
+          uint4 qv;
+          if constexpr (C::kQSmem) {
+            qv = lds128(qs_addr + (jj * 32 + 4 * c) * 4);
+          } else {
+            qv = make_uint4(qq[jj][4 * c], qq[jj][4 * c + 1], qq[jj][4 * c + 2], qq[jj][4 * c + 3]);
+          }
+#pragma unroll
+          for (int half = 0; half < 2; half++)
+#pragma unroll
+            for (int m = 0; m < 4; m++)
+              acc[half][jj] = __dp4a((int)word_of(kv[half], m), (int)word_of(qv, m), acc[half][jj]);
+        }
+      }
+    }
     int tmax = INT_MIN;
 #pragma unroll
     for (int half = 0; half < 2; half++) {
-      const int row = half * 32 + lane;           // token within the tile
-      const int t = tile * kTileTokens + row;
-      const uint32_t rbase = sbase + row * kHeadDim;
-      int acc[G];
+      const int t = tile * kTileTokens + half * 32 + lane;
+      int g = acc[half][0];
 #pragma unroll
-      for (int jj = 0; jj < G; jj++) acc[jj] = 0;
-      if constexpr (KB4) {
-        // token `row` is half `row & 1` of 128-byte row `row >> 1` of the tile
-        const int r = row >> 1, sub = row & 1;
-        const uint32_t rb = sbase + r * 128;
-#pragma unroll
-        for (int c = 0; c < 4; c++) {
-          const uint4 kv = lds128(rb + (((sub * 4 + c) ^ (r & 7)) << 4));
-          const uint32_t wv[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-          for (int m = 0; m < 4; m++) {
-            const int ev = (int)((wv[m] << 4) & 0xF0F0F0F0u), od = (int)(wv[m] & 0xF0F0F0F0u);
-#pragma unroll
-            for (int jj = 0; jj < G; jj++) {
-              acc[jj] = __dp4a(ev, qq[jj][4 * c + m], acc[jj]);
-              acc[jj] = __dp4a(od, qq[jj][16 + 4 * c + m], acc[jj]);
-            }
-          }
-        }
-#pragma unroll
-        for (int jj = 0; jj < G; jj++) acc[jj] >>= 4;
-      } else {
-#pragma unroll
-        for (int c = 0; c < 8; c++) {
-          const uint4 kv = lds128(rbase + ((c ^ (row & 7)) << 4));
-#pragma unroll
-          for (int jj = 0; jj < G; jj++) {
-            acc[jj] = __dp4a((int)kv.x, qq[jj][4 * c + 0], acc[jj]);
-            acc[jj] = __dp4a((int)kv.y, qq[jj][4 * c + 1], acc[jj]);
-            acc[jj] = __dp4a((int)kv.z, qq[jj][4 * c + 2], acc[jj]);
-            acc[jj] = __dp4a((int)kv.w, qq[jj][4 * c + 3], acc[jj]);
-          }
-        }
-      }
-      int g = acc[0];
-#pragma unroll
-      for (int jj = 1; jj < G; jj++) g = max(g, acc[jj]);
+      for (int jj = 1; jj < G; jj++) g = max(g, acc[half][jj]);
       if (t < sr.lo || t >= sr.hi) g = INT_MIN;
       g = max(g, __shfl_xor_sync(0xffffffffu, g, 8));
       g = max(g, __shfl_xor_sync(0xffffffffu, g, 4));
@@ -352,16 +455,12 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   }
 }
 
-size_t score_smem_bytes(int batch) {
-  return 1024 + kScoreStages * kStageBytes + 2 * kScoreStages * sizeof(uint64_t) +
-         (batch + 1) * sizeof(int);
-}
-
 }  // namespace
 
 int score_max_tiles(const Shape& s) { return (s.max_pages + kTileBlocks - 1) / kTileBlocks; }
 
-cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const void* q,
+cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
+                                const CUtensorMap& kq_map4, const void* q,
                                 const float* k_scale, const int32_t* page_table,
                                 const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
                                 int* err, int num_sms, cudaStream_t st) {
@@ -381,24 +480,33 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map, const
   a.num_pages = s.num_pages;
   a.sink = s.sink;
   a.window = s.window;
-  const size_t smem = score_smem_bytes(s.batch);
   // upper bound of the tile count; the kernel splits the true count evenly
   const long long tiles_max =
       (long long)s.batch * s.hkv * ((s.max_pages + kTileBlocks - 1) / kTileBlocks + 1);
-  const int grid = (int)std::min<long long>(tiles_max, 2LL * num_sms);
-  const bool kb4 = s.key_bits == 4;
-  auto go = [&](auto kernel) {
+  auto go = [&](auto kernel, auto cfg) {
+    using C = decltype(cfg);
+    const size_t smem = C::smem_bytes(s.batch);
+    const int grid = (int)std::min<long long>(tiles_max, (long long)C::kCtasPerSm * num_sms);
     cudaError_t e = set_kernel_smem(kernel, smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(kernel, dim3(grid), dim3(kScoreThreads), smem, st, true, kq_map, a);
+    return launch_kernel(kernel, dim3(grid), dim3(C::kThreads), smem, st, true, kq_map, kq_map4,
+                         a);
   };
+#define HSA_SCORE_CASE(g)                                                          \
+  case g:                                                                          \
+    e = s.key_bits == 4 ? go(score_blocks_kernel<g, true>, ScoreCfg<g, true>{})    \
+                        : go(score_blocks_kernel<g, false>, ScoreCfg<g, false>{}); \
+    break;
   cudaError_t e;
   switch (s.group) {
-    case 1: e = kb4 ? go(score_blocks_kernel<1, true>) : go(score_blocks_kernel<1, false>); break;
-    case 2: e = kb4 ? go(score_blocks_kernel<2, true>) : go(score_blocks_kernel<2, false>); break;
-    case 4: e = kb4 ? go(score_blocks_kernel<4, true>) : go(score_blocks_kernel<4, false>); break;
-    default: return cudaErrorInvalidValue;
+    HSA_SCORE_CASE(1)
+    HSA_SCORE_CASE(2)
+    HSA_SCORE_CASE(4)
+    HSA_SCORE_CASE(8)
+    default:
+      return cudaErrorInvalidValue;
   }
+#undef HSA_SCORE_CASE
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
