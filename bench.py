@@ -677,7 +677,7 @@ def main():
         # memory, read over the host link by the attend kernel)
         for name, dense in (("paged-b8-32k-128k", True), ("llama3-8b-3m-offload", False),
                             ("llama3-8b-1m-3mod", True), ("llama3-8b-128k-int4", True),
-                            ("llama3-8b-1m-int4", True)):
+                            ("llama3-8b-1m-int4", True), ("llama3-70b-128k", True)):
             r = gpu_case_numbers(name, rank, device, min(args.steps, 500), args.warmup, None,
                                  peak, world, dense=dense)
             del r["case"]

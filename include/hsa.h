@@ -66,7 +66,7 @@ extern "C" {
 enum hsa_status {
   HSA_OK = 0,
   HSA_ERR_INVALID_ARG = 1,          /* null pointer, bad size, misaligned pointer */
-  HSA_ERR_UNSUPPORTED = 2,          /* head_dim != 128, page/block != 16, group not 1/2/4, ... */
+  HSA_ERR_UNSUPPORTED = 2,          /* head_dim != 128, page/block != 16, group not 1/2/4/8, ... */
   HSA_ERR_CUDA = 3,                 /* a CUDA runtime call or a launch failed */
   HSA_ERR_TIMEOUT = 4,              /* a bounded device wait ran out (reported by the error word) */
   HSA_ERR_WORKSPACE_TOO_SMALL = 5,
@@ -77,7 +77,7 @@ enum hsa_status {
 typedef struct hsa_dims {
   int32_t batch;             /* sequences in the step (>= 1) */
   int32_t hq;                /* query heads */
-  int32_t hkv;               /* key/value heads; hq % hkv == 0 and hq / hkv in {1, 2, 4} */
+  int32_t hkv;               /* key/value heads; hq % hkv == 0 and hq / hkv in {1, 2, 4, 8} */
   int32_t head_dim;          /* must be 128 */
   int32_t page_size;         /* must be 16 */
   int32_t max_pages_per_seq; /* row length of page_table (>= 1) */

@@ -36,7 +36,7 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   if (d->hq % d->hkv != 0) return HSA_ERR_INVALID_ARG;
   if (d->head_dim != hsa::kHeadDim || d->page_size != hsa::kPage) return HSA_ERR_UNSUPPORTED;
   const int g = d->hq / d->hkv;
-  if (g != 1 && g != 2 && g != 4) return HSA_ERR_UNSUPPORTED;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return HSA_ERR_UNSUPPORTED;
   if (d->batch > kMaxBatch || d->hkv > kMaxHkv) return HSA_ERR_UNSUPPORTED;
   if ((long long)d->num_pages * d->hkv * hsa::kPage > INT32_MAX ||
       (long long)d->max_pages_per_seq * hsa::kPage > INT32_MAX / 2)

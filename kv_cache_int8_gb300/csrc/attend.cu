@@ -60,7 +60,7 @@ constexpr int kStages = 8;
 // HBM path, sparse attend: 8 compute warps + the producer. A CTA of it does not fit beside a
 // prune CTA (the three warps on one SM sub-partition take its register file), so the prune
 // keeps its SMs to itself; the attend's grid leaves those SMs free (HSA_SPARSE_RESERVE).
-constexpr int kSparseWarps = HSA_SPARSE_WARPS, kSparseStages = 2 * HSA_SPARSE_WARPS;
+constexpr int kSparseWarps = HSA_SPARSE_WARPS;  // ring: two slots per compute warp
 constexpr int kDenseWarps = 4, kDenseStages = 8;     // HBM path, dense decode
 constexpr int kSlotBytes = 2 * kBlockBytesBf16;  // K page + V page of one head
 constexpr int kHostThreads = kCompute;
@@ -69,6 +69,9 @@ constexpr int kMaxSplits = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNeg = -FLT_MAX;                 // "no token" score
+
+// Per-head slots of the shared scratch areas: 4 for groups of up to 4 query heads, else 8.
+__host__ __device__ constexpr int head_slots(int G) { return G <= 4 ? 4 : 8; }
 
 struct AttArgs {
   const __nv_bfloat16* q;
@@ -183,26 +186,45 @@ __device__ __forceinline__ void compute_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
 }
 
-// Shared memory of the compute warps besides the K/V slots.
+// Shared memory of the compute warps besides the K/V slots (H = head_slots(G)).
+template <int H>
 struct Scratch {
-  float score[kPage][4];  // per token, per head (log2-scaled logits)
-  float prob[kPage][4];   // softmax weights of the segment
-  float rescale[4];       // factor applied to the running state of each head
-  float m[4], l[4];       // final running max / sum per head
+  float score[kPage][H];  // per token, per head (log2-scaled logits)
+  float prob[kPage][H];   // softmax weights of the segment
+  float rescale[H];       // factor applied to the running state of each head
+  float m[H], l[H];       // final running max / sum per head
 };
 
 // Running state of one lane.
 template <int G>
 struct State {
+  static constexpr int kOwn = (G + kWarps - 1) / kWarps;  // heads owned by one warp
   float acc[G][2];  // weighted value sums, 2 channels x G heads
-  float m, l;       // running max / sum of head `warp` (meaningful in warps < G, lane 0)
+  float m[kOwn], l[kOwn];  // running max / sum of heads warp + kWarps i (lane 0 meaningful)
 };
 
 // The G dot products of a token, reduced over its 8 lanes: afterwards lane `sl` holds the
 // full score of head hidx(sl). Partner lanes exchange halves of their vectors at each step.
 template <int G>
 __device__ __forceinline__ float reduce_scores(float (&v)[G], int sl, int& hidx) {
-  if constexpr (G == 4) {
+  if constexpr (G == 8) {
+    const bool b2 = sl & 4, b1 = sl & 2, b0 = sl & 1;
+    float u[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const float r = __shfl_xor_sync(0xffffffffu, b2 ? v[i] : v[4 + i], 4);
+      u[i] = (b2 ? v[4 + i] : v[i]) + r;  // head (b2 ? 4 : 0) + i
+    }
+    float w2[2];
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+      const float r = __shfl_xor_sync(0xffffffffu, b1 ? u[i] : u[2 + i], 2);
+      w2[i] = (b1 ? u[2 + i] : u[i]) + r;  // head (b2 ? 4 : 0) + (b1 ? 2 : 0) + i
+    }
+    const float r = __shfl_xor_sync(0xffffffffu, b0 ? w2[0] : w2[1], 1);
+    hidx = sl;
+    return (b0 ? w2[1] : w2[0]) + r;
+  } else if constexpr (G == 4) {
     const bool b2 = sl & 4, b1 = sl & 2;
     const float s0 = b2 ? v[0] : v[2], s1 = b2 ? v[1] : v[3];
     const float r0 = __shfl_xor_sync(0xffffffffu, s0, 4);
@@ -250,8 +272,9 @@ __device__ __forceinline__ void load_query(float (&qf)[G][16], const AttArgs& a,
 // value accumulation. Called by the 128 compute threads together.
 template <int G>
 __device__ __forceinline__ void process_segment(State<G>& st, const float (&qf)[G][16],
-                                                Scratch& sc, uint32_t slot, int k, int t0,
-                                                int t1) {
+                                                Scratch<head_slots(G)>& sc, uint32_t slot,
+                                                int k, int t0, int t1) {
+  constexpr int H = head_slots(G);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // scores
   {
@@ -276,22 +299,26 @@ __device__ __forceinline__ void process_segment(State<G>& st, const float (&qf)[
     if ((sl & (kOwners - 1)) == 0) sc.score[r][hidx] = (t >= t0 && t < t1) ? s : kNeg;
   }
   compute_bar();
-  // softmax of the segment, one warp per head (lanes 0..15 carry the 16 tokens)
-  if (warp < G) {
-    const float s = lane < kPage ? sc.score[lane][warp] : kNeg;
+  // softmax of the segment, one warp per head (warp w owns heads w, w + 4; lanes 0..15
+  // carry the 16 tokens)
+#pragma unroll
+  for (int i = 0; i < State<G>::kOwn; i++) {
+    const int hh = warp + kWarps * i;
+    if (hh >= G) continue;
+    const float s = lane < kPage ? sc.score[lane][hh] : kNeg;
     float mx = s;
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    const float m_new = fmaxf(st.m, mx);
-    const float c = exp2f(st.m - m_new);
+    const float m_new = fmaxf(st.m[i], mx);
+    const float c = exp2f(st.m[i] - m_new);
     const float p = s == kNeg ? 0.0f : exp2f(s - m_new);
     float ps = p;
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-    st.l = st.l * c + ps;
-    st.m = m_new;
-    if (lane < kPage) sc.prob[lane][warp] = p;
-    if (lane == 0) sc.rescale[warp] = c;
+    st.l[i] = st.l[i] * c + ps;
+    st.m[i] = m_new;
+    if (lane < kPage) sc.prob[lane][hh] = p;
+    if (lane == 0) sc.rescale[hh] = c;
   }
   compute_bar();
   // values
@@ -313,8 +340,15 @@ __device__ __forceinline__ void process_segment(State<G>& st, const float (&qf)[
       uint32_t w;
       asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(vb + (th * 8 + tt) * kHeadDim * 2));
       const float lo = bf16_lo(w), hi = bf16_hi(w);
-      const float4 p4 = *reinterpret_cast<const float4*>(sc.prob[th * 8 + tt]);
-      const float p[4] = {p4.x, p4.y, p4.z, p4.w};
+      float p[H];
+#pragma unroll
+      for (int q4 = 0; q4 < H / 4; q4++) {
+        const float4 p4 = *reinterpret_cast<const float4*>(&sc.prob[th * 8 + tt][4 * q4]);
+        p[4 * q4] = p4.x;
+        p[4 * q4 + 1] = p4.y;
+        p[4 * q4 + 2] = p4.z;
+        p[4 * q4 + 3] = p4.w;
+      }
 #pragma unroll
       for (int j = 0; j < G; j++) {
         st.acc[j][0] = fmaf(p[j], lo, st.acc[j][0]);
@@ -434,8 +468,8 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
 // Block-level state (host path): the two token halves merged into o[G][128]; m, l from the
 // softmax warps. `red` holds at least G * 128 + 8 floats.
 template <int G>
-__device__ void finish(const AttArgs& a, State<G>& st, Scratch& sc, int b, int h, int split,
-                       float* red) {
+__device__ void finish(const AttArgs& a, State<G>& st, Scratch<head_slots(G)>& sc, int b, int h,
+                       int split, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int d = (warp & 1) * 64 + 2 * lane;
   if (warp < kWarps && (warp >> 1) == 1) {
@@ -445,9 +479,13 @@ __device__ void finish(const AttArgs& a, State<G>& st, Scratch& sc, int b, int h
       red[j * kHeadDim + d + 1] = st.acc[j][1];
     }
   }
-  if (warp < G && lane == 0) {
-    sc.m[warp] = st.m;
-    sc.l[warp] = st.l;
+#pragma unroll
+  for (int i = 0; i < State<G>::kOwn; i++) {
+    const int hh = warp + kWarps * i;
+    if (hh < G && lane == 0) {
+      sc.m[hh] = st.m[i];
+      sc.l[hh] = st.l[i];
+    }
   }
   __syncthreads();
   if (warp < kWarps && (warp >> 1) == 0) {
@@ -465,8 +503,11 @@ template <int G>
 __device__ __forceinline__ void init_state(State<G>& st) {
 #pragma unroll
   for (int j = 0; j < G; j++) st.acc[j][0] = st.acc[j][1] = 0.0f;
-  st.m = kNeg;
-  st.l = 0.0f;
+#pragma unroll
+  for (int i = 0; i < State<G>::kOwn; i++) {
+    st.m[i] = kNeg;
+    st.l[i] = 0.0f;
+  }
 }
 
 size_t red_floats(int G) {
@@ -482,9 +523,10 @@ size_t red_floats(int G) {
 // kept by every lane of that head; the weights go through the warp's own shared scratch
 // to the value phase, where lane l owns channels 4l .. 4l + 3 of all G heads.
 
+template <int H>
 struct WarpScratch {
-  float prob[kPage][4];  // weights of the segment's tokens, per head
-  float rescale[4];      // factor applied to the running sums of each head
+  float prob[kPage][H];  // weights of the segment's tokens, per head
+  float rescale[H];      // factor applied to the running sums of each head
   float pad[4];
 };
 
@@ -496,8 +538,9 @@ struct WarpState {
 
 template <int G>
 __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)[G][16],
-                                             WarpScratch& ws, uint32_t slot, int k, int t0,
-                                             int t1) {
+                                             WarpScratch<head_slots(G)>& ws, uint32_t slot,
+                                             int k, int t0, int t1) {
+  constexpr int H = head_slots(G);
   const int lane = threadIdx.x & 31;
   const int g = lane >> 3, sl = lane & 7;
   float sc[4];
@@ -545,8 +588,15 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
   }
   __syncwarp();
   // values: lane owns channels 4 lane .. 4 lane + 3
-  const float4 c4 = *reinterpret_cast<const float4*>(ws.rescale);
-  const float cj[4] = {c4.x, c4.y, c4.z, c4.w};
+  float cj[H];
+#pragma unroll
+  for (int q4 = 0; q4 < H / 4; q4++) {
+    const float4 c4 = *reinterpret_cast<const float4*>(&ws.rescale[4 * q4]);
+    cj[4 * q4] = c4.x;
+    cj[4 * q4 + 1] = c4.y;
+    cj[4 * q4 + 2] = c4.z;
+    cj[4 * q4 + 3] = c4.w;
+  }
 #pragma unroll
   for (int j = 0; j < G; j++)
 #pragma unroll
@@ -559,8 +609,15 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
     uint32_t w0, w1;
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(vb + r * kHeadDim * 2));
     const float vf[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
-    const float4 p4 = *reinterpret_cast<const float4*>(ws.prob[r]);
-    const float pj[4] = {p4.x, p4.y, p4.z, p4.w};
+    float pj[H];
+#pragma unroll
+    for (int q4 = 0; q4 < H / 4; q4++) {
+      const float4 p4 = *reinterpret_cast<const float4*>(&ws.prob[r][4 * q4]);
+      pj[4 * q4] = p4.x;
+      pj[4 * q4 + 1] = p4.y;
+      pj[4 * q4 + 2] = p4.z;
+      pj[4 * q4 + 3] = p4.w;
+    }
 #pragma unroll
     for (int j = 0; j < G; j++)
 #pragma unroll
@@ -573,17 +630,19 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
 // slots, enough for every segment of a CTA to be in flight at once; dense decode uses 4 and 8
 // with three CTAs per SM.
 template <int G, bool DENSE, int W, int NS>
-__global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_kernel(const AttArgs a) {
+__global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
+    attend_tma_kernel(const AttArgs a) {
   static_assert(NS % W == 0, "each compute warp owns fixed ring slots");
+  constexpr int H = head_slots(G);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * kSlotBytes);
   uint64_t* empty = full + NS;
-  WarpScratch* wscr = reinterpret_cast<WarpScratch*>(empty + NS);  // [W]
-  float* mstate = reinterpret_cast<float*>(wscr + W);             // [W][2][4]
-  int4* meta = reinterpret_cast<int4*>(mstate + 2 * W * 4);       // [NS] (k, t0, t1)
+  WarpScratch<H>* wscr = reinterpret_cast<WarpScratch<H>*>(empty + NS);  // [W]
+  float* mstate = reinterpret_cast<float*>(wscr + W);                    // [W][2][H]
+  int4* meta = reinterpret_cast<int4*>(mstate + 2 * W * H);              // [NS] (k, t0, t1)
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -722,17 +781,18 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
   __syncthreads();
   // merge the warps: o[j][d] = sum_w acc_w * 2^(m_w - M_j), l likewise
   float* o = reinterpret_cast<float*>(ring);  // [W][G][128], then the merged [G][128]
-  float* mw = mstate;                          // [W][4] max, then [W][4] sum
-  float* lw = mstate + W * 4;
+  float* mw = mstate;                          // [W][H] max, then [W][H] sum
+  float* lw = mstate + W * H;
   if (warp < W) {
     const int sl = lane & 7;
     constexpr int kOwners = 8 / G;
     int hidx = 0;
+    if constexpr (G == 8) hidx = sl;
     if constexpr (G == 4) hidx = ((sl & 4) ? 2 : 0) + ((sl & 2) ? 1 : 0);
     if constexpr (G == 2) hidx = (sl & 4) ? 1 : 0;
     if (lane < 8 && (sl & (kOwners - 1)) == 0) {
-      mw[warp * 4 + hidx] = st.m;
-      lw[warp * 4 + hidx] = st.l;
+      mw[warp * H + hidx] = st.m;
+      lw[warp * H + hidx] = st.l;
     }
 #pragma unroll
     for (int j = 0; j < G; j++)
@@ -741,19 +801,19 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
   }
   __syncthreads();
   float* mo = o + W * G * kHeadDim;  // merged [G][128]
-  float* mm = mo + G * kHeadDim;          // [4]
-  float* ml = mm + 4;                     // [4]
+  float* mm = mo + G * kHeadDim;          // [H]
+  float* ml = mm + H;                     // [H]
   if (tid < W * 32) {
     for (int x = tid; x < G * kHeadDim; x += W * 32) {
       const int j = x / kHeadDim, d = x % kHeadDim;
       float M = kNeg;
 #pragma unroll
-      for (int w = 0; w < W; w++) M = fmaxf(M, mw[w * 4 + j]);
+      for (int w = 0; w < W; w++) M = fmaxf(M, mw[w * H + j]);
       float O = 0.0f, L = 0.0f;
 #pragma unroll
       for (int w = 0; w < W; w++) {
-        const float lv = lw[w * 4 + j];
-        const float wt = lv > 0.0f ? exp2f(mw[w * 4 + j] - M) : 0.0f;
+        const float lv = lw[w * H + j];
+        const float wt = lv > 0.0f ? exp2f(mw[w * H + j] - M) : 0.0f;
         O = fmaf(o[(w * G + j) * kHeadDim + d], wt, O);
         L = fmaf(lv, wt, L);
       }
@@ -771,13 +831,14 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 ? 3 : 1)) attend_tma_ker
 // ---------------------------------------------------------- mapped-host path
 
 template <int G, bool DENSE>
-__global__ void __launch_bounds__(kHostThreads, 3) attend_host_kernel(const AttArgs a) {
+__global__ void __launch_bounds__(kHostThreads, G <= 4 ? 3 : 2) attend_host_kernel(const AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint8_t* slots = smem;  // two slots: the segment in use and the next one
-  Scratch& sc = *reinterpret_cast<Scratch*>(smem + 2 * kSlotBytes);
-  float* red = reinterpret_cast<float*>(smem + 2 * kSlotBytes + sizeof(Scratch));
+  using Sc = Scratch<head_slots(G)>;
+  Sc& sc = *reinterpret_cast<Sc*>(smem + 2 * kSlotBytes);
+  float* red = reinterpret_cast<float*>(smem + 2 * kSlotBytes + sizeof(Sc));
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -873,29 +934,35 @@ __global__ void __launch_bounds__(256) cache_fill_kernel(const int4* fill, const
   }
 }
 
-template <int W, int NS>
+template <int G, int W, int NS>
 constexpr size_t tma_smem() {
-  // the merge area ((W + 1) * G * 128 + 8 floats) fits in the ring
-  return 128 + (size_t)NS * kSlotBytes + 2 * NS * sizeof(uint64_t) + W * sizeof(WarpScratch) +
-         2 * W * 4 * sizeof(float) + NS * sizeof(int4);
+  constexpr int H = head_slots(G);
+  // the merge area ((W + 1) * G * 128 + 2 * H floats) fits in the ring
+  static_assert(((W + 1) * G * kHeadDim + 2 * H) * sizeof(float) <= (size_t)NS * kSlotBytes,
+                "merge area");
+  return 128 + (size_t)NS * kSlotBytes + 2 * NS * sizeof(uint64_t) +
+         W * sizeof(WarpScratch<H>) + 2 * W * H * sizeof(float) + NS * sizeof(int4);
 }
 
-size_t host_smem(int G) {
-  return 128 + 2 * kSlotBytes + sizeof(Scratch) + red_floats(G) * sizeof(float);
+template <int G>
+size_t host_smem() {
+  return 128 + 2 * kSlotBytes + sizeof(Scratch<head_slots(G)>) + red_floats(G) * sizeof(float);
 }
 static_assert(kStages % kWarps == 0, "each compute warp owns fixed ring slots");
 
 template <int G, bool DENSE>
 cudaError_t launch_g(AttArgs a, dim3 grid, bool host, cudaStream_t st) {
   if (host) {
-    const size_t smem = host_smem(G);
+    const size_t smem = host_smem<G>();
     cudaError_t e = set_kernel_smem(attend_host_kernel<G, DENSE>, smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(attend_host_kernel<G, DENSE>, grid, dim3(kHostThreads), smem, st, true, a);
   }
-  constexpr int W = DENSE ? kDenseWarps : kSparseWarps;
-  constexpr int NS = DENSE ? kDenseStages : kSparseStages;
-  constexpr size_t smem = tma_smem<W, NS>();
+  // groups of 8 hold 8 x 16 query floats per lane: at most two warps per SM sub-partition
+  // (registers), so the sparse attend takes 7 compute warps there
+  constexpr int W = DENSE ? kDenseWarps : (G > 4 ? 7 : kSparseWarps);
+  constexpr int NS = DENSE ? kDenseStages : 2 * W;
+  constexpr size_t smem = tma_smem<G, W, NS>();
   auto kern = attend_tma_kernel<G, DENSE, W, NS>;
   cudaError_t e = set_kernel_smem(kern, smem);
   if (e != cudaSuccess) return e;
@@ -975,6 +1042,8 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
       return dense ? launch_g<2, true>(a, grid, host, st) : launch_g<2, false>(a, grid, host, st);
     case 4:
       return dense ? launch_g<4, true>(a, grid, host, st) : launch_g<4, false>(a, grid, host, st);
+    case 8:
+      return dense ? launch_g<8, true>(a, grid, host, st) : launch_g<8, false>(a, grid, host, st);
     default:
       return cudaErrorInvalidValue;
   }

@@ -75,6 +75,9 @@ CONFIGS: Dict[str, Config] = {
     "llama3-8b-1m-3mod": Config("llama3-8b-1m-3mod", 1, 32, 8, 1048576, None,
                                 k1=512, k2=256, sink=128, window=2048, needles=64,
                                 chunk0=256, k0=256),
+    # a 128K step with groups of 8 query heads (Llama-3-70B-shaped attention layer)
+    "llama3-70b-128k": Config("llama3-70b-128k", 1, 64, 8, 131072, None,
+                              k1=256, k2=128, sink=128, window=1024),
     # the 128K and 1M steps with 4-bit key codes (half the bytes the scorer reads)
     "llama3-8b-128k-int4": Config("llama3-8b-128k-int4", 1, 32, 8, 131072, None,
                                   k1=256, k2=128, sink=128, window=1024, key_bits=4),

@@ -71,10 +71,18 @@ def test_workspace_sizes(lib):
     assert lib.hsa_workspace_bytes(d, lib.HSA_OP_SELECT) >= 8 * 8192 * 4 + 256
     assert lib.hsa_workspace_bytes(_dims(lib, head_dim=64), 0) == 0
     assert lib.hsa_workspace_bytes(_dims(lib, hq=12, hkv=8), 0) == 0
+    # groups of 1, 2, 4 and 8 query heads per kv head; 4-bit and 8-bit key codes
+    for hq in (8, 16, 32, 64):
+        assert lib.hsa_workspace_bytes(_dims(lib, hq=hq, hkv=8), 0) > 0
+    assert lib.hsa_workspace_bytes(_dims(lib, hq=48, hkv=8), 0) == 0
+    for bits in (0, 4, 8):
+        assert lib.hsa_workspace_bytes(_dims(lib, key_bits=bits), 0) > 0
+    assert lib.hsa_workspace_bytes(_dims(lib, key_bits=2), 0) == 0
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(head_dim=64), 2), (dict(page_size=32), 2), (dict(block=32), 2), (dict(hq=24), 2),
+    (dict(hq=128), 2), (dict(key_bits=6), 2),
     (dict(hq=30), 1), (dict(batch=0), 1), (dict(k1=-1), 1), (dict(window=-3), 1),
     (dict(chunk=40), 1), (dict(chunk=0), 1), (dict(batch=2000), 2),
 ])

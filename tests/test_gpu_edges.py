@@ -66,9 +66,11 @@ def test_other_chunk_sizes(chunk):
     _check(wl, chunk=chunk, k1=40, k2=30, sink=64, window=128)
 
 
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (4, 1)])
-def test_group_sizes(hq, hkv):
-    wl = W.make_workload(_cfg(context=12345, batch=2, hq=hq, hkv=hkv, k1=20, k2=17), seed=hq + hkv)
+@pytest.mark.parametrize("hq,hkv,key_bits", [(8, 8, 8), (8, 4, 8), (4, 1, 8), (16, 2, 8),
+                                              (8, 1, 8), (16, 2, 4), (8, 4, 4), (8, 8, 4)])
+def test_group_sizes(hq, hkv, key_bits):
+    wl = W.make_workload(_cfg(context=12345, batch=2, hq=hq, hkv=hkv, k1=20, k2=17,
+                              key_bits=key_bits), seed=hq + hkv)
     _check(wl, sink=40, window=200)
 
 
@@ -210,14 +212,16 @@ def _clone(t):
     return t.clone().pin_memory() if t.device.type == "cpu" else t.clone()
 
 
-@pytest.mark.parametrize("window,k1,k2,on_host", [(0, 6, 9, False), (1, 6, 9, False),
-                                                  (5, 3, 0, False), (300, 8, 8, False),
-                                                  (0, 6, 9, True), (300, 8, 8, True)])
-def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2, on_host):
+@pytest.mark.parametrize("window,k1,k2,on_host,hq", [(0, 6, 9, False, 8), (1, 6, 9, False, 8),
+                                                     (5, 3, 0, False, 8), (300, 8, 8, False, 8),
+                                                     (0, 6, 9, True, 8), (300, 8, 8, True, 8),
+                                                     (300, 8, 8, False, 16), (40, 8, 8, True, 16)])
+def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2, on_host, hq):
     """The whole step (append ordered before or beside the scorer, prune, attend with the
     sink and window pages fetched early) equals the separate calls bit for bit, and the
-    oracle on the appended cache; also with K/V in mapped pinned host memory."""
-    cfg = _cfg(context=None, context_range=(700, 5000), batch=3, hq=8, hkv=2, k1=k1, k2=k2,
+    oracle on the appended cache; also with K/V in mapped pinned host memory, and with
+    groups of 8 query heads."""
+    cfg = _cfg(context=None, context_range=(700, 5000), batch=3, hq=hq, hkv=2, k1=k1, k2=k2,
                sink=20, window=window, paged_permuted=True)
     wl = W.make_workload(cfg, seed=40 + window, host_pinned=on_host)
     hd, od = H.dims_pair(wl)

@@ -60,6 +60,13 @@ def test_llama3_8b_1m_three_modules_sampled_heads():
     _run(wl, bh_pairs=[(0, 2), (0, 7)])
 
 
+def test_llama3_70b_shaped_128k_groups_of_8_sampled_heads():
+    """64 query heads over 8 kv heads: the scorer's max over 8 heads, the attention of 8
+    heads per kv head."""
+    wl = W.make_workload(W.CONFIGS["llama3-70b-128k"], seed=0, device="cuda")
+    _run(wl, bh_pairs=[(0, 0), (0, 7)])
+
+
 def test_tiny_8k_four_bit_keys():
     """4-bit key codes: codes (unpacked from their nibbles), scales amax / 7, block maxima
     and selections bit-exact against the oracle's 4-bit format; outputs within tolerance."""
