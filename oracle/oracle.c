@@ -66,7 +66,12 @@ typedef struct {
   double sm_scale; /* <= 0 means 1/sqrt(head_dim) */
   int32_t chunk0, k0; /* k0 > 0: a first module keeps the top-k0 chunks of chunk0 tokens */
   int32_t key_bits;   /* 4: 4-bit key codes (levels +-7); 0 or 8: 8-bit (levels +-127) */
+  int32_t per_head;   /* 1: every query head selects its own chunks and blocks (N3 variant) */
 } oracle_dims;
+
+/* Rows of the selection outputs per sequence: one per kv head (the group shares one
+ * selection), or one per query head with per-head selection. */
+static int sel_rows(const oracle_dims* d) { return d->per_head ? d->hq : d->hkv; }
 
 /* ---------------------------------------------------------------- helpers */
 
@@ -253,7 +258,10 @@ static int by_index(const void* a, const void* b) {
  * Outputs (per (b, h)): block_max [B][Hkv][max_pages_per_seq*page_size/block]
  * (INT32_MIN where a block has no token in C; nullable), chunk_idx [B][Hkv][K1]
  * and block_idx [B][Hkv][K2] ascending and padded with -1, n_chunks / n_blocks
- * [B][Hkv] (nullable). */
+ * [B][Hkv] (nullable).
+ * Per-head selection (d->per_head; [HiP] prunes every attention head on its own): the
+ * same query codes, but every query head j ranks its own token scores qq_j . kq_t, with
+ * no max over the group; the outputs then have one row per query head ([B][Hq][..]). */
 int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, const int8_t* kq,
                   const int32_t* page_table, const int32_t* lens, const int32_t* bh_mask,
                   int32_t* block_max, int32_t* chunk_idx, int32_t* n_chunks, int32_t* block_idx,
@@ -273,99 +281,106 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
     int64_t n = lens[b];
     int64_t lo = d->sink, hi = n - d->window; /* C = [lo, hi) */
     int8_t* qq = (int8_t*)malloc((size_t)G * D);
-    query_codes_one(d, q, scale, b, h, qq, NULL);
+    if (qq) query_codes_one(d, q, scale, b, h, qq, NULL);
+    const int nrow = d->per_head ? G : 1;
+    for (int rj = 0; rj < nrow; rj++) {
+      /* the output row, and the query heads whose scores it ranks: [j_lo, j_hi) */
+      const int64_t row =
+          d->per_head ? (int64_t)b * d->hq + h * G + rj : (int64_t)b * d->hkv + h;
+      const int j_lo = d->per_head ? rj : 0, j_hi = d->per_head ? rj + 1 : G;
 
-    int64_t n_chunk_all = (max_tokens + d->chunk - 1) / d->chunk;
-    const int64_t c0 = d->k0 > 0 ? d->chunk0 : d->chunk; /* coarse chunk of module 0 */
-    int64_t n_coarse_all = (max_tokens + c0 - 1) / c0;
-    int64_t* cmax0 = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_coarse_all + 1));
-    char* cvalid0 = (char*)calloc((size_t)n_coarse_all + 1, 1);
-    char* ckept0 = (char*)calloc((size_t)n_coarse_all + 1, 1);
-    int64_t* cmax = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_chunk_all + 1));
-    int64_t* bmax = (int64_t*)malloc(sizeof(int64_t) * (size_t)(max_blocks + 1));
-    char* cvalid = (char*)calloc((size_t)n_chunk_all + 1, 1);
-    char* bvalid = (char*)calloc((size_t)max_blocks + 1, 1);
-    if (!qq || !cmax || !bmax || !cvalid || !bvalid || !cmax0 || !cvalid0 || !ckept0) {
-#pragma omp atomic write
-      bad = 1;
-    } else {
-      /* token scores, folded straight into the chunk and block maxima */
-      for (int64_t t = lo; t < hi; t++) {
-        int64_t g = INT64_MIN;
-        for (int j = 0; j < G; j++) {
-          int64_t dot = 0;
-          for (int c = 0; c < D; c++)
-            dot += (int64_t)qq[j * D + c] * (int64_t)kq[cache_index(d, page_table, b, h, t, c)];
-          if (dot > g) g = dot;
-        }
-        int64_t ci = t / d->chunk, bi = t / d->block, c0i = t / c0;
-        if (!cvalid0[c0i] || g > cmax0[c0i]) cmax0[c0i] = g;
-        cvalid0[c0i] = 1;
-        if (!cvalid[ci] || g > cmax[ci]) cmax[ci] = g;
-        if (!bvalid[bi] || g > bmax[bi]) bmax[bi] = g;
-        cvalid[ci] = 1;
-        bvalid[bi] = 1;
-      }
-      if (block_max) {
-        int32_t* out = block_max + ((int64_t)b * d->hkv + h) * max_blocks;
-        for (int64_t k = 0; k < max_blocks; k++) out[k] = bvalid[k] ? (int32_t)bmax[k] : INT32_MIN;
-      }
-      ranked* list = (ranked*)malloc(sizeof(ranked) * (size_t)(n_chunk_all + max_blocks +
-                                                                n_coarse_all + 1));
-      /* module 0 (stacked in front when k0 > 0): top-K0 coarse chunks, by the same order */
-      if (d->k0 > 0) {
-        int64_t n0 = 0;
-        for (int64_t c = 0; c < n_coarse_all; c++)
-          if (cvalid0[c]) {
-            list[n0].score = cmax0[c];
-            list[n0].index = c;
-            n0++;
+      int64_t n_chunk_all = (max_tokens + d->chunk - 1) / d->chunk;
+      const int64_t c0 = d->k0 > 0 ? d->chunk0 : d->chunk; /* coarse chunk of module 0 */
+      int64_t n_coarse_all = (max_tokens + c0 - 1) / c0;
+      int64_t* cmax0 = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_coarse_all + 1));
+      char* cvalid0 = (char*)calloc((size_t)n_coarse_all + 1, 1);
+      char* ckept0 = (char*)calloc((size_t)n_coarse_all + 1, 1);
+      int64_t* cmax = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_chunk_all + 1));
+      int64_t* bmax = (int64_t*)malloc(sizeof(int64_t) * (size_t)(max_blocks + 1));
+      char* cvalid = (char*)calloc((size_t)n_chunk_all + 1, 1);
+      char* bvalid = (char*)calloc((size_t)max_blocks + 1, 1);
+      if (!qq || !cmax || !bmax || !cvalid || !bvalid || !cmax0 || !cvalid0 || !ckept0) {
+  #pragma omp atomic write
+        bad = 1;
+      } else {
+        /* token scores, folded straight into the chunk and block maxima */
+        for (int64_t t = lo; t < hi; t++) {
+          int64_t g = INT64_MIN;
+          for (int j = j_lo; j < j_hi; j++) {
+            int64_t dot = 0;
+            for (int c = 0; c < D; c++)
+              dot += (int64_t)qq[j * D + c] * (int64_t)kq[cache_index(d, page_table, b, h, t, c)];
+            if (dot > g) g = dot;
           }
-        qsort(list, (size_t)n0, sizeof(ranked), by_score_then_index);
-        int64_t keep0 = n0 < d->k0 ? n0 : d->k0;
-        for (int64_t i = 0; i < keep0; i++) ckept0[list[i].index] = 1;
-      }
-      /* module 1: top-K1 chunks (inside the kept coarse chunks when module 0 runs) */
-      int64_t nc = 0;
-      for (int64_t c = 0; c < n_chunk_all; c++)
-        if (cvalid[c] && (d->k0 == 0 || ckept0[c * d->chunk / c0])) {
-          list[nc].score = cmax[c];
-          list[nc].index = c;
-          nc++;
+          int64_t ci = t / d->chunk, bi = t / d->block, c0i = t / c0;
+          if (!cvalid0[c0i] || g > cmax0[c0i]) cmax0[c0i] = g;
+          cvalid0[c0i] = 1;
+          if (!cvalid[ci] || g > cmax[ci]) cmax[ci] = g;
+          if (!bvalid[bi] || g > bmax[bi]) bmax[bi] = g;
+          cvalid[ci] = 1;
+          bvalid[bi] = 1;
         }
-      qsort(list, (size_t)nc, sizeof(ranked), by_score_then_index);
-      int64_t keep1 = nc < d->k1 ? nc : d->k1;
-      qsort(list, (size_t)keep1, sizeof(ranked), by_index);
-      int32_t* cout = chunk_idx + ((int64_t)b * d->hkv + h) * d->k1;
-      for (int64_t i = 0; i < d->k1; i++) cout[i] = i < keep1 ? (int32_t)list[i].index : -1;
-      if (n_chunks) n_chunks[b * d->hkv + h] = (int32_t)keep1;
-      /* module 2: the kept chunks' blocks, top-K2 */
-      ranked* blist = list + keep1;
-      int64_t nb = 0;
-      const int per = d->chunk / d->block;
-      for (int64_t i = 0; i < keep1; i++)
-        for (int64_t k = list[i].index * per; k < (list[i].index + 1) * per; k++)
-          if (k < max_blocks && bvalid[k]) {
-            blist[nb].score = bmax[k];
-            blist[nb].index = k;
-            nb++;
+        if (block_max) {
+          int32_t* out = block_max + row * max_blocks;
+          for (int64_t k = 0; k < max_blocks; k++) out[k] = bvalid[k] ? (int32_t)bmax[k] : INT32_MIN;
+        }
+        ranked* list = (ranked*)malloc(sizeof(ranked) * (size_t)(n_chunk_all + max_blocks +
+                                                                  n_coarse_all + 1));
+        /* module 0 (stacked in front when k0 > 0): top-K0 coarse chunks, by the same order */
+        if (d->k0 > 0) {
+          int64_t n0 = 0;
+          for (int64_t c = 0; c < n_coarse_all; c++)
+            if (cvalid0[c]) {
+              list[n0].score = cmax0[c];
+              list[n0].index = c;
+              n0++;
+            }
+          qsort(list, (size_t)n0, sizeof(ranked), by_score_then_index);
+          int64_t keep0 = n0 < d->k0 ? n0 : d->k0;
+          for (int64_t i = 0; i < keep0; i++) ckept0[list[i].index] = 1;
+        }
+        /* module 1: top-K1 chunks (inside the kept coarse chunks when module 0 runs) */
+        int64_t nc = 0;
+        for (int64_t c = 0; c < n_chunk_all; c++)
+          if (cvalid[c] && (d->k0 == 0 || ckept0[c * d->chunk / c0])) {
+            list[nc].score = cmax[c];
+            list[nc].index = c;
+            nc++;
           }
-      qsort(blist, (size_t)nb, sizeof(ranked), by_score_then_index);
-      int64_t keep2 = nb < d->k2 ? nb : d->k2;
-      qsort(blist, (size_t)keep2, sizeof(ranked), by_index);
-      int32_t* bout = block_idx + ((int64_t)b * d->hkv + h) * d->k2;
-      for (int64_t i = 0; i < d->k2; i++) bout[i] = i < keep2 ? (int32_t)blist[i].index : -1;
-      if (n_blocks) n_blocks[b * d->hkv + h] = (int32_t)keep2;
-      free(list);
+        qsort(list, (size_t)nc, sizeof(ranked), by_score_then_index);
+        int64_t keep1 = nc < d->k1 ? nc : d->k1;
+        qsort(list, (size_t)keep1, sizeof(ranked), by_index);
+        int32_t* cout = chunk_idx + row * d->k1;
+        for (int64_t i = 0; i < d->k1; i++) cout[i] = i < keep1 ? (int32_t)list[i].index : -1;
+        if (n_chunks) n_chunks[row] = (int32_t)keep1;
+        /* module 2: the kept chunks' blocks, top-K2 */
+        ranked* blist = list + keep1;
+        int64_t nb = 0;
+        const int per = d->chunk / d->block;
+        for (int64_t i = 0; i < keep1; i++)
+          for (int64_t k = list[i].index * per; k < (list[i].index + 1) * per; k++)
+            if (k < max_blocks && bvalid[k]) {
+              blist[nb].score = bmax[k];
+              blist[nb].index = k;
+              nb++;
+            }
+        qsort(blist, (size_t)nb, sizeof(ranked), by_score_then_index);
+        int64_t keep2 = nb < d->k2 ? nb : d->k2;
+        qsort(blist, (size_t)keep2, sizeof(ranked), by_index);
+        int32_t* bout = block_idx + row * d->k2;
+        for (int64_t i = 0; i < d->k2; i++) bout[i] = i < keep2 ? (int32_t)blist[i].index : -1;
+        if (n_blocks) n_blocks[row] = (int32_t)keep2;
+        free(list);
+      }
+      free(cmax0);
+      free(cvalid0);
+      free(ckept0);
+      free(cmax);
+      free(bmax);
+      free(cvalid);
+      free(bvalid);
     }
     free(qq);
-    free(cmax0);
-    free(cvalid0);
-    free(ckept0);
-    free(cmax);
-    free(bmax);
-    free(cvalid);
-    free(bvalid);
   }
   return bad ? 3 : 0;
 }
@@ -412,8 +427,10 @@ static int attention_common(const oracle_dims* d, const uint16_t* q, const uint1
         bad = 1;
         continue;
       }
-      int nk = n_blocks ? n_blocks[b * d->hkv + h] : d->k2;
-      const int32_t* list = block_idx + ((int64_t)b * d->hkv + h) * d->k2;
+      /* the selection row of query head j: its kv head's, or its own (per-head selection) */
+      const int64_t row = d->per_head ? (int64_t)bj : (int64_t)b * d->hkv + h;
+      int nk = n_blocks ? n_blocks[row] : d->k2;
+      const int32_t* list = block_idx + row * d->k2;
       for (int i = 0; i < nk && i < d->k2; i++)
         if (list[i] >= 0 && list[i] < max_blocks) kept[list[i]] = 1;
     }

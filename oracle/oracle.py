@@ -22,7 +22,8 @@ class _CDims(ctypes.Structure):
         "chunk", "block", "k1", "k2", "sink", "window")] + [("sm_scale", ctypes.c_double),
                                                             ("chunk0", ctypes.c_int32),
                                                             ("k0", ctypes.c_int32),
-                                                            ("key_bits", ctypes.c_int32)]
+                                                            ("key_bits", ctypes.c_int32),
+                                                            ("per_head", ctypes.c_int32)]
 
 
 @dataclasses.dataclass
@@ -45,11 +46,17 @@ class Dims:
     chunk0: int = 0  # k0 > 0: a first module keeps the top-k0 chunks of chunk0 tokens
     k0: int = 0
     key_bits: int = 0  # 4: 4-bit key codes (levels +-7); 0 or 8: 8-bit
+    per_head: int = 0  # 1: every query head selects its own chunks and blocks
 
     def c(self) -> _CDims:
         return _CDims(*[int(getattr(self, f[0])) for f in _CDims._fields_[:13]],
                       float(self.sm_scale), int(self.chunk0), int(self.k0),
-                      int(self.key_bits))
+                      int(self.key_bits), int(self.per_head))
+
+    @property
+    def sel_rows(self) -> int:
+        """Selection rows per sequence: kv heads, or query heads with per-head selection."""
+        return self.hq if self.per_head else self.hkv
 
     @property
     def group(self) -> int:
@@ -150,10 +157,12 @@ def query_codes(d: Dims, q: np.ndarray, k_scale: np.ndarray):
 
 def select(d: Dims, q: np.ndarray, k_scale: np.ndarray, kq: np.ndarray, page_table, seq_lens,
            bh_mask=None, want_block_max: bool = False):
-    """The two pruning modules. Returns a dict with chunk_idx [B][Hkv][K1],
-    n_chunks [B][Hkv], block_idx [B][Hkv][K2], n_blocks [B][Hkv] and, on request,
-    block_max [B][Hkv][max_blocks] (INT32_MIN where a block has no candidate token)."""
-    B, H = d.batch, d.hkv
+    """The two pruning modules. Returns a dict with chunk_idx [B][R][K1],
+    n_chunks [B][R], block_idx [B][R][K2], n_blocks [B][R] and, on request,
+    block_max [B][R][max_blocks] (INT32_MIN where a block has no candidate token); R is
+    Hkv, or Hq with per-head selection. bh_mask [B][Hkv] selects kv heads (all rows of a
+    selected kv head are computed)."""
+    B, H = d.batch, d.sel_rows
     out = {
         "chunk_idx": np.full((B, H, max(d.k1, 0)), -1, dtype=np.int32),
         "n_chunks": np.zeros((B, H), dtype=np.int32),

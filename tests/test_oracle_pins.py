@@ -458,6 +458,112 @@ def test_three_stacked_modules_defining_property_brute_force(seed):
         np.testing.assert_array_equal(three[key], two[key])
 
 
+@pytest.mark.parametrize("seed", range(5))
+def test_per_head_selection_defining_property_brute_force(seed):
+    """Per-head selection (InfiniteHiP article, stacked modules: every head prunes on its
+    own): each query head ranks its own integer dot products, with the group's shared
+    query codes and no max over the group. Checked by brute force row by row, and by the
+    closed form that a kv head's shared block maximum is the max of its heads' maxima."""
+    rng = np.random.default_rng(500 + seed)
+    D, hkv, G = 8, 2, 2 + 2 * (seed % 2)
+    lens = tuple(int(x) for x in rng.integers(60, 600, size=2))
+    case = random_case(rng, B=2, hq=hkv * G, hkv=hkv, D=D, lens=lens, page=16, perm=True)
+    for b in range(2):
+        case["ks"][b] = np.round(case["ks"][b] * 2) / 2  # frequent ties
+    kc, pt, ln = paged(case["ks"], 16, hkv, None)
+    case.update(k=kc, pt=pt)
+    k1, k2 = int(rng.integers(1, 9)), int(rng.integers(0, 12))
+    sink, window = int(rng.integers(0, 40)), int(rng.integers(0, 60))
+    d = dims_for(case, hkv * G, hkv, D, chunk=32, block=16, k1=k1, k2=k2, sink=sink,
+                 window=window)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, ln)
+    qq, _ = oracle.query_codes(d, bf16_bits(case["q"]), sc)
+    shared = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln, want_block_max=True)
+    d.per_head = 1
+    ph = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln, want_block_max=True)
+    assert ph["block_idx"].shape == (2, hkv * G, k2)
+    codes = logical_codes(kq, pt, ln, 16, hkv)
+    for b in range(2):
+        for h in range(hkv):
+            for j in range(G):
+                row = h * G + j
+                bm = _block_max_by_definition(qq[b, h, j:j + 1], codes[b][h], int(ln[b]), sink,
+                                              window, 16)
+                got = ph["block_max"][b, row]
+                for k in range(got.size):
+                    assert got[k] == bm.get(k, INT32_MIN)
+                cm = {}
+                for k, s_ in bm.items():
+                    cm[k // 2] = max(cm.get(k // 2, s_), s_)
+                kept_c = [c for c in ph["chunk_idx"][b, row] if c >= 0]
+                assert kept_c == sorted(kept_c) and len(kept_c) == min(k1, len(cm))
+                for c in kept_c:
+                    for c2 in cm:
+                        if c2 not in kept_c:
+                            assert _beats(cm[c], c, cm[c2], c2)
+                cand = [k for k in bm if k // 2 in kept_c]
+                kept_b = [k for k in ph["block_idx"][b, row] if k >= 0]
+                assert kept_b == sorted(kept_b) and len(kept_b) == min(k2, len(cand))
+                assert ph["n_blocks"][b, row] == len(kept_b)
+                for k in kept_b:
+                    for k_ in cand:
+                        if k_ not in kept_b:
+                            assert _beats(bm[k], k, bm[k_], k_)
+            # max over the group commutes with the per-block max
+            np.testing.assert_array_equal(
+                shared["block_max"][b, h], ph["block_max"][b, h * G:(h + 1) * G].max(axis=0))
+
+
+def test_per_head_selection_special_cases():
+    """One query head per kv head: per-head selection is the shared one. Identical query
+    heads in a group: every head's row is the group's shared selection."""
+    rng = np.random.default_rng(77)
+    case = random_case(rng, B=2, hq=2, hkv=2, D=8, lens=(300, 410), page=16)
+    d = dims_for(case, 2, 2, 8, k1=5, k2=7, sink=16, window=32)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(case["k"]), case["pt"], case["lens"])
+    a = oracle.select(d, bf16_bits(case["q"]), sc, kq, case["pt"], case["lens"])
+    d.per_head = 1
+    b_ = oracle.select(d, bf16_bits(case["q"]), sc, kq, case["pt"], case["lens"])
+    for key in a:
+        np.testing.assert_array_equal(a[key], b_[key])
+    case = random_case(rng, B=1, hq=8, hkv=2, D=8, lens=(500,), page=16)
+    case["q"][0, 4:8] = case["q"][0, 4]
+    case["q"][0, 0:4] = case["q"][0, 1]
+    d = dims_for(case, 8, 2, 8, k1=6, k2=9, sink=16, window=32)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(case["k"]), case["pt"], case["lens"])
+    shared = oracle.select(d, bf16_bits(case["q"]), sc, kq, case["pt"], case["lens"])
+    d.per_head = 1
+    ph = oracle.select(d, bf16_bits(case["q"]), sc, kq, case["pt"], case["lens"])
+    for key in shared:
+        for j in range(8):
+            np.testing.assert_array_equal(ph[key][0, j], shared[key][0, j // 4])
+
+
+def test_per_head_attention_reads_each_heads_own_row():
+    """With per-head selection query head j attends to the blocks of row j: the same as a
+    shared-selection attention whose kv head row holds head j's list."""
+    rng = np.random.default_rng(78)
+    case = random_case(rng, B=1, hq=4, hkv=2, D=8, lens=(400,), page=16)
+    d = dims_for(case, 4, 2, 8, k1=8, k2=6, sink=16, window=32)
+    kb, vb, qb = bf16_bits(case["k"]), bf16_bits(case["v"]), bf16_bits(case["q"])
+    n_cand = (400 - 32) // 16
+    lists = np.stack([np.sort(rng.choice(np.arange(1, n_cand), size=6, replace=False))
+                      for _ in range(4)]).astype(np.int32)[None]
+    counts = np.array([[6, 5, 3, 0]], dtype=np.int32)
+    d.per_head = 1
+    out_ph, lse_ph = oracle.attend(d, qb, kb, vb, case["pt"], case["lens"], lists, counts)
+    d.per_head = 0
+    for j in range(4):
+        h = j // 2
+        row = np.full((1, 2, 6), -1, dtype=np.int32)
+        row[0, h] = lists[0, j]
+        cnt = np.zeros((1, 2), dtype=np.int32)
+        cnt[0, h] = counts[0, j]
+        out_s, lse_s = oracle.attend(d, qb, kb, vb, case["pt"], case["lens"], row, cnt)
+        np.testing.assert_array_equal(out_ph[0, j], out_s[0, j])
+        assert lse_ph[0, j] == lse_s[0, j]
+
+
 def test_candidate_region_masks_sink_and_window_tokens():
     """A huge key in the sink part of a block that straddles the sink boundary, and one in
     the window, must not lift any block score."""
