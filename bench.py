@@ -188,8 +188,9 @@ class Case:
                           max_pages_per_seq=wl["max_pages"], num_pages=wl["num_pages"],
                           chunk=cfg.chunk, k1=cfg.k1, k2=cfg.k2, sink=cfg.sink,
                           window=cfg.window, kv_on_host=cfg.kv_on_host, chunk0=cfg.chunk0,
-                          k0=cfg.k0, key_bits=cfg.key_bits)
+                          k0=cfg.k0, key_bits=cfg.key_bits, per_head=cfg.per_head)
         d = self.d
+        R = cfg.hq if cfg.per_head else cfg.hkv  # selection rows per sequence
         B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
         self.q = wl["q"]
         self.pt, self.lens = wl["page_table"], wl["seq_lens"]
@@ -230,13 +231,13 @@ class Case:
             self.cache_capacity = self.CACHE_SLOTS
             self.cache = hsa.block_cache(d, self.cache_capacity)
             self.ws_cached = hsa.workspace(d, hsa.HSA_OP_CACHED)
-        self.bm = torch.zeros((B, Hkv, d.max_pages_per_seq), dtype=torch.int32, device=device)
-        self.tm = torch.zeros((B, Hkv, (d.max_pages_per_seq + 3) // 4), dtype=torch.int32,
+        self.bm = torch.zeros((B, R, d.max_pages_per_seq), dtype=torch.int32, device=device)
+        self.tm = torch.zeros((B, R, (d.max_pages_per_seq + 3) // 4), dtype=torch.int32,
                               device=device)
-        self.chunk_idx = torch.zeros((B, Hkv, max(d.k1, 1)), dtype=torch.int32, device=device)
-        self.n_chunks = torch.zeros((B, Hkv), dtype=torch.int32, device=device)
-        self.block_idx = torch.zeros((B, Hkv, max(d.k2, 1)), dtype=torch.int32, device=device)
-        self.n_blocks = torch.zeros((B, Hkv), dtype=torch.int32, device=device)
+        self.chunk_idx = torch.zeros((B, R, max(d.k1, 1)), dtype=torch.int32, device=device)
+        self.n_chunks = torch.zeros((B, R), dtype=torch.int32, device=device)
+        self.block_idx = torch.zeros((B, R, max(d.k2, 1)), dtype=torch.int32, device=device)
+        self.n_blocks = torch.zeros((B, R), dtype=torch.int32, device=device)
         self.out = torch.zeros((B, Hq, 128), dtype=torch.float32, device=device)
         self.lse = torch.zeros((B, Hq), dtype=torch.float32, device=device)
         self.out_d = torch.zeros_like(self.out)
@@ -339,8 +340,9 @@ class Case:
         return sum(max(0, n - c.window - c.sink) for n in self.wl["lens"])
 
     def attended_tokens(self):
-        """|T| summed over (sequence, kv head): sink + window + the kept blocks' candidate
-        tokens, from the selection of the last step."""
+        """|T| summed over (sequence, selection row): sink + window + the kept blocks'
+        candidate tokens, from the selection of the last step. A row is a kv head, or a
+        query head with per-head selection (whose K/V are then read once per query head)."""
         c = self.cfg
         nb = self.n_blocks.cpu()
         bi = self.block_idx.cpu()
@@ -349,7 +351,7 @@ class Case:
             sink_end = min(c.sink, n)
             w0 = max(n - c.window, sink_end)
             base = sink_end + (n - w0)
-            for h in range(c.hkv):
+            for h in range(nb.shape[1]):
                 total += base
                 for k in bi[b, h, : int(nb[b, h])].tolist():
                     total += max(0, min(16 * k + 16, n - c.window) - max(16 * k, c.sink))
@@ -359,7 +361,7 @@ class Case:
         c = self.cfg
         blocks = sum(max(0, -(-(n - c.window) // 16) - c.sink // 16) for n in self.wl["lens"])
         return (c.hkv * self.candidate_tokens() * 128 * c.key_bits // 8 + c.batch * c.hq * 128 * 2 +
-                c.batch * c.hkv * 128 * 4 + c.hkv * blocks * 4)
+                c.batch * c.hkv * 128 * 4 + self.bm.shape[1] * blocks * 4)
 
     def bytes_attend(self):
         c = self.cfg
@@ -546,7 +548,8 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int):
     od = oracle.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, head_dim=128, page_size=16,
                      max_pages_per_seq=wl["max_pages"], num_pages=wl["num_pages"],
                      chunk=cfg.chunk, block=16, k1=cfg.k1, k2=cfg.k2, sink=cfg.sink,
-                     window=cfg.window, chunk0=cfg.chunk0, k0=cfg.k0, key_bits=cfg.key_bits)
+                     window=cfg.window, chunk0=cfg.chunk0, k0=cfg.k0, key_bits=cfg.key_bits,
+                     per_head=cfg.per_head)
     q, k, v = (W.to_numpy_bits(wl[x]) for x in ("q", "k_cache", "v_cache"))
     pt, lens = wl["page_table"].numpy(), wl["seq_lens"].numpy()
     kq, sc = oracle.quantize_keys(od, k, pt, lens)             # cache state, not per step
@@ -620,7 +623,8 @@ def workload_text(cfg):
     return (f"{cfg.name}: batch {cfg.batch}, Hq {cfg.hq}, Hkv {cfg.hkv}, d 128, context "
             f"{cfg.context}, {mod0}chunk {cfg.chunk} keep K1 {cfg.k1}, block 16 keep K2 "
             f"{cfg.k2}, sink {cfg.sink}, window {cfg.window}; bf16 K/V in 16-token pages, "
-            f"int{cfg.key_bits} per-channel keys")
+            f"int{cfg.key_bits} per-channel keys"
+            + ("; per-head selection" if cfg.per_head else ""))
 
 
 def main():
@@ -677,7 +681,8 @@ def main():
         # memory, read over the host link by the attend kernel)
         for name, dense in (("paged-b8-32k-128k", True), ("llama3-8b-3m-offload", False),
                             ("llama3-8b-1m-3mod", True), ("llama3-8b-128k-int4", True),
-                            ("llama3-8b-1m-int4", True), ("llama3-70b-128k", True)):
+                            ("llama3-8b-1m-int4", True), ("llama3-70b-128k", True),
+                            ("llama3-8b-128k-perhead", True)):
             r = gpu_case_numbers(name, rank, device, min(args.steps, 500), args.warmup, None,
                                  peak, world, dense=dense)
             del r["case"]

@@ -99,6 +99,14 @@ typedef struct hsa_dims {
   int32_t key_bits;          /* key codes: 0 or 8 = 8-bit (kq int8 [num_pages][hkv][16][128]);
                                 4 = 4-bit (scale amax / 7, codes in [-7, 7], two per byte: kq
                                 [num_pages][hkv][16][64] bytes, channel 2i in the low nibble) */
+  int32_t per_head;          /* 0: the G query heads of a kv head share one selection (token
+                                score = max over the group); 1: per-head selection (InfiniteHiP
+                                article: every head is pruned on its own): each query head
+                                ranks its own scores (same query codes), and every selection
+                                array has one row per QUERY head: block_max / tile_max
+                                [batch][hq][..], chunk_idx / block_idx [batch][hq][k1 / k2],
+                                n_chunks / n_blocks [batch][hq]; the attention of query head
+                                j then reads row j. Not with the block cache (UNSUPPORTED). */
 } hsa_dims;
 
 /* Operation ids for hsa_workspace_bytes. */

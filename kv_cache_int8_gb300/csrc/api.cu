@@ -51,6 +51,7 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   }
   if (!(d->sm_scale == d->sm_scale)) return HSA_ERR_INVALID_ARG;  // NaN
   if (d->key_bits != 0 && d->key_bits != 4 && d->key_bits != 8) return HSA_ERR_UNSUPPORTED;
+  if (d->per_head != 0 && d->per_head != 1) return HSA_ERR_INVALID_ARG;
   s.batch = d->batch;
   s.hq = d->hq;
   s.hkv = d->hkv;
@@ -65,15 +66,36 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   s.chunk0 = d->k0 > 0 ? d->chunk0 : 0;
   s.k0 = d->k0;
   s.key_bits = d->key_bits == 4 ? 4 : 8;
+  s.per_head = d->per_head;
+  s.kv_div = 1;
   s.sm_scale = d->sm_scale > 0.0f ? d->sm_scale : 1.0f / std::sqrt((float)hsa::kHeadDim);
   return HSA_OK;
 }
 
 // ---- workspace layouts
 size_t quantize_ws(const Shape& s) { return kErrBytes + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 4); }
-size_t select_bm_bytes(const Shape& s) { return up((size_t)s.batch * s.hkv * s.max_pages * 4); }
+size_t select_bm_bytes(const Shape& s) {
+  return up((size_t)s.batch * s.sel_rows() * s.max_pages * 4);
+}
 size_t select_tm_bytes(const Shape& s) {
-  return up((size_t)s.batch * s.hkv * hsa::score_max_tiles(s) * 4);
+  return up((size_t)s.batch * s.sel_rows() * hsa::score_max_tiles(s) * 4);
+}
+// The prune works on selection rows: one per kv head, or one per query head.
+Shape prune_shape(const Shape& s) {
+  Shape p = s;
+  p.hkv = s.sel_rows();
+  return p;
+}
+// The sparse attention with per-head selection: one attention row per query head (group of
+// one), reading K/V of kv head row / kv_div.
+Shape attend_shape(const Shape& s, bool dense) {
+  Shape a = s;
+  if (s.per_head && !dense) {
+    a.hkv = s.hq;
+    a.group = 1;
+    a.kv_div = s.group;
+  }
+  return a;
 }
 size_t select_ws(const Shape& s) { return kErrBytes + select_bm_bytes(s) + select_tm_bytes(s); }
 struct AttendLayout {
@@ -82,7 +104,7 @@ struct AttendLayout {
 AttendLayout attend_layout(const Shape& s, size_t base) {
   AttendLayout l;
   l.counters = base;
-  l.part_ml = l.counters + up((size_t)s.batch * s.hkv * 4);
+  l.part_ml = l.counters + up((size_t)s.batch * s.sel_rows() * 4);
   l.part_o = l.part_ml + up((size_t)s.batch * s.hq * kMaxSplits * 2 * 4);
   l.end = l.part_o + up((size_t)s.batch * s.hq * kMaxSplits * hsa::kHeadDim * 4);
   return l;
@@ -153,9 +175,9 @@ StepLayout step_layout(const Shape& s) {
   l.block_max = kErrBytes;
   l.tile_max = l.block_max + select_bm_bytes(s);
   l.block_idx = l.tile_max + select_tm_bytes(s);
-  l.n_blocks = l.block_idx + up((size_t)s.batch * s.hkv * std::max(s.k2, 1) * 4);
-  l.sel_pages = l.n_blocks + up((size_t)s.batch * s.hkv * 4);
-  l.q = l.sel_pages + up((size_t)s.batch * s.hkv * std::max(s.k2, 1) * 4);
+  l.n_blocks = l.block_idx + up((size_t)s.batch * s.sel_rows() * std::max(s.k2, 1) * 4);
+  l.sel_pages = l.n_blocks + up((size_t)s.batch * s.sel_rows() * 4);
+  l.q = l.sel_pages + up((size_t)s.batch * s.sel_rows() * std::max(s.k2, 1) * 4);
   l.k_new = l.q + up((size_t)s.batch * s.hq * hsa::kHeadDim * 2);
   l.v_new = l.k_new + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 2);
   l.out = l.v_new + up((size_t)s.batch * s.hkv * hsa::kHeadDim * 2);
@@ -292,7 +314,8 @@ int32_t do_score(const Shape& s, const void* q, const int8_t* kq, const float* k
                                               block_max, tile_max, err, num_sms(), st));
 }
 
-int32_t check_prune_fits(const Shape& s) {
+int32_t check_prune_fits(const Shape& s0) {
+  const Shape s = prune_shape(s0);
   const long long n1max = ((long long)s.max_pages * hsa::kPage + s.chunk - 1) / s.chunk;
   if (n1max > hsa::prune_max_chunks()) return HSA_ERR_UNSUPPORTED;
   if (hsa::prune_smem_bytes(s) > 227 * 1024) return HSA_ERR_UNSUPPORTED;
@@ -314,9 +337,10 @@ int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, 
   buf.counters = reinterpret_cast<int*>(ws + l.counters);
   buf.part_ml = reinterpret_cast<float*>(ws + l.part_ml);
   buf.part_o = reinterpret_cast<float*>(ws + l.part_o);
-  buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(s, dense, host, num_sms()));
   buf.sel_pages = sel_pages;
-  return cuda_status(hsa::launch_attend(s, dense, host, q, kd, vd, pt, lens, bidx, nb, out, lse,
+  const Shape sa = attend_shape(s, dense);
+  buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(sa, dense, host, num_sms()));
+  return cuda_status(hsa::launch_attend(sa, dense, host, q, kd, vd, pt, lens, bidx, nb, out, lse,
                                         buf, reinterpret_cast<int*>(ws), st, early));
 }
 
@@ -476,8 +500,8 @@ int32_t hsa_prune(const hsa_dims* d, const int32_t* seq_lens, const int32_t* blo
   if (!aligned(block_max, 16) || !aligned(tile_max, 16)) return HSA_ERR_INVALID_ARG;
   rc = check_prune_fits(s);
   if (rc != HSA_OK) return rc;
-  return cuda_status(hsa::launch_prune(s, seq_lens, block_max, tile_max, chunk_idx, n_chunks,
-                                       block_idx, n_blocks, nullptr, nullptr, nullptr,
+  return cuda_status(hsa::launch_prune(prune_shape(s), seq_lens, block_max, tile_max, chunk_idx,
+                                       n_chunks, block_idx, n_blocks, nullptr, nullptr, nullptr,
                                        as_stream(stream)));
 }
 
@@ -502,9 +526,8 @@ int32_t hsa_select(const hsa_dims* d, const void* q, const int8_t* kq, const flo
   cudaStream_t st = as_stream(stream);
   rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st);
   if (rc != HSA_OK) return rc;
-  return cuda_status(
-      hsa::launch_prune(s, seq_lens, bm, tm, chunk_idx, n_chunks, block_idx, n_blocks, nullptr,
-                        nullptr, err, st));
+  return cuda_status(hsa::launch_prune(prune_shape(s), seq_lens, bm, tm, chunk_idx, n_chunks,
+                                       block_idx, n_blocks, nullptr, nullptr, err, st));
 }
 
 int32_t hsa_attend(const hsa_dims* d, const void* q, const void* k_cache, const void* v_cache,
@@ -554,6 +577,7 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
   int32_t rc = check_dims(d, s, !reuse);
   if (rc != HSA_OK) return rc;
   if (block_cache != nullptr) {
+    if (s.per_head) return HSA_ERR_UNSUPPORTED;  // the cache plan works per kv head
     if (!d->kv_on_host || !aligned(block_cache, kAlign)) return HSA_ERR_INVALID_ARG;
     rc = check_cache_capacity(s, capacity);
     if (rc != HSA_OK) return rc;
@@ -654,8 +678,8 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
   }
   // the prune also resolves the kept blocks' pages, so the attend needs one round trip for them
   int32_t* sel_pages = reinterpret_cast<int32_t*>(ws + l.sel_pages);
-  e = hsa::launch_prune(s, seq_lens, bm, tm, nullptr, nullptr, bidx, nb, page_table, sel_pages,
-                        err, st);
+  e = hsa::launch_prune(prune_shape(s), seq_lens, bm, tm, nullptr, nullptr, bidx, nb, page_table,
+                        sel_pages, err, st);
   if (e != cudaSuccess) return HSA_ERR_CUDA;
   rc = block_cache ? do_attend_cached(s, q, kd, vd, page_table, seq_lens, bidx, nb, out, lse, ws,
                                       l.att, l.cache, block_cache, capacity, st)
@@ -679,7 +703,7 @@ int32_t hsa_decode_step_cached(const hsa_dims* d, const hsa_step_io* io, void* k
 
 size_t hsa_block_cache_bytes(const hsa_dims* d, int32_t capacity) {
   Shape s;
-  if (check_dims(d, s, false) != HSA_OK) return 0;
+  if (check_dims(d, s, false) != HSA_OK || s.per_head) return 0;
   if (check_cache_capacity(s, capacity) != HSA_OK) return 0;
   return cache_layout(s, capacity).end;
 }
@@ -698,6 +722,7 @@ int32_t hsa_attend_cached(const hsa_dims* d, const void* q, const void* k_cache,
     return HSA_ERR_INVALID_ARG;
   if (!d->kv_on_host || !aligned(q, 16) || !aligned(out, 16) || !aligned(block_cache, kAlign))
     return HSA_ERR_INVALID_ARG;
+  if (s.per_head) return HSA_ERR_UNSUPPORTED;  // the cache plan works per kv head
   rc = check_cache_capacity(s, capacity);
   if (rc != HSA_OK) return rc;
   rc = check_ws(s, workspace, workspace_bytes, cached_ws(s));
@@ -807,8 +832,8 @@ int32_t hsa_select_noalloc(const hsa_dims* d, const void* q, const int8_t* kq,
   // reported (there is no error word).
   rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, nullptr, st);
   if (rc != HSA_OK) return rc;
-  return cuda_status(hsa::launch_prune(s, seq_lens, bm, tm, chunk_idx, n_chunks, block_idx,
-                                       n_blocks, nullptr, nullptr, nullptr, st));
+  return cuda_status(hsa::launch_prune(prune_shape(s), seq_lens, bm, tm, chunk_idx, n_chunks,
+                                       block_idx, n_blocks, nullptr, nullptr, nullptr, st));
 }
 
 }  // extern "C"

@@ -92,6 +92,8 @@ struct AttArgs {
   int* counters;
   int* err;
   int hkv, max_pages, num_pages, k2, sink, window, nsplit;
+  int kv_heads, kv_div;  // K/V heads of the cache; attention rows per kv head (row h reads
+                         // kv head h / kv_div: hq / hkv with per-head selection, else 1)
   float qscale;  // sm_scale * log2(e)
   int early;     // K/V, q, page table are ready before the selection (whole decode step)
 };
@@ -742,7 +744,8 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
             if (pq >= 0) {
               // a page of the cache, or one slot (K block then V block) of the block cache
               const size_t off = a.seg_slots ? (size_t)pq * (2 * kPage * kHeadDim)
-                                             : ((size_t)pq * a.hkv + h) * kPage * kHeadDim;
+                                             : ((size_t)pq * a.kv_heads + h / a.kv_div) *
+                                                   kPage * kHeadDim;
               mbar_arrive_expect_tx(&full[s], kSlotBytes);
               bulk_load_hint(ring + s * kSlotBytes, a.k + off, kBlockBytesBf16, &full[s], policy);
               bulk_load_hint(ring + s * kSlotBytes + kBlockBytesBf16, a.v + off, kBlockBytesBf16,
@@ -868,7 +871,7 @@ __global__ void __launch_bounds__(kHostThreads, G <= 4 ? 3 : 2) attend_host_kern
       t0 = t1 = 0;
       return;
     }
-    const size_t off = ((size_t)page * a.hkv + h) * kPage * kHeadDim;
+    const size_t off = ((size_t)page * a.kv_heads + h / a.kv_div) * kPage * kHeadDim;
     const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k + off);
     const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v + off);
     buf[0] = ldg128_nc(kp + tid * 16);
@@ -1026,6 +1029,8 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
   a.counters = buf.counters;
   a.err = err;
   a.hkv = s.hkv;
+  a.kv_div = s.kv_div;
+  a.kv_heads = s.hkv / s.kv_div;
   a.max_pages = s.max_pages;
   a.num_pages = buf.seg_slots ? buf.cache_capacity : s.num_pages;
   a.k2 = s.k2;

@@ -180,7 +180,9 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
   return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
 
-template <int G, bool KB4>
+// PH: per-head selection, the maxima of every query head (rows b * hq + h * G + j) rather
+// than of the group's token scores.
+template <int G, bool KB4, bool PH>
 __global__ void __launch_bounds__(ScoreCfg<G, KB4>::kThreads, ScoreCfg<G, KB4>::kCtasPerSm)
     score_blocks_kernel(const __grid_constant__ CUtensorMap kq_map,
                         const __grid_constant__ CUtensorMap kq_map4, const ScoreArgs a) {
@@ -365,7 +367,6 @@ __global__ void __launch_bounds__(ScoreCfg<G, KB4>::kThreads, ScoreCfg<G, KB4>::
       break;
     }
     const uint32_t sbase = smem_addr(ring + s * C::kSlotBytes);
-    int32_t* out = a.block_max + ((size_t)b * a.hkv + h) * a.max_pages;
     // both 32-token halves of the tile at once (lane = token `half * 32 + lane`)
     int acc[2][G];
 #pragma unroll
@@ -429,27 +430,35 @@ __global__ void __launch_bounds__(ScoreCfg<G, KB4>::kThreads, ScoreCfg<G, KB4>::
         }
       }
     }
-    int tmax = INT_MIN;
+    // block and tile maxima of the token scores (the max over the group's heads), or of each
+    // head's own dot products with per-head selection
+    constexpr int kRows = PH ? G : 1;
 #pragma unroll
-    for (int half = 0; half < 2; half++) {
-      const int t = tile * kTileTokens + half * 32 + lane;
-      int g = acc[half][0];
+    for (int jr = 0; jr < kRows; jr++) {
+      const size_t row = PH ? ((size_t)b * a.hkv + h) * G + jr : (size_t)b * a.hkv + h;
+      int tmax = INT_MIN;
 #pragma unroll
-      for (int jj = 1; jj < G; jj++) g = max(g, acc[half][jj]);
-      if (t < sr.lo || t >= sr.hi) g = INT_MIN;
-      g = max(g, __shfl_xor_sync(0xffffffffu, g, 8));
-      g = max(g, __shfl_xor_sync(0xffffffffu, g, 4));
-      g = max(g, __shfl_xor_sync(0xffffffffu, g, 2));
-      g = max(g, __shfl_xor_sync(0xffffffffu, g, 1));
-      if ((lane & 15) == 0) {
-        const int k = tile * kTileBlocks + half * 2 + (lane >> 4);
-        if (k >= sr.k_lo && k < sr.k_hi) out[k] = g;
+      for (int half = 0; half < 2; half++) {
+        const int t = tile * kTileTokens + half * 32 + lane;
+        int g = acc[half][PH ? jr : 0];
+        if constexpr (!PH) {
+#pragma unroll
+          for (int jj = 1; jj < G; jj++) g = max(g, acc[half][jj]);
+        }
+        if (t < sr.lo || t >= sr.hi) g = INT_MIN;
+        g = max(g, __shfl_xor_sync(0xffffffffu, g, 8));
+        g = max(g, __shfl_xor_sync(0xffffffffu, g, 4));
+        g = max(g, __shfl_xor_sync(0xffffffffu, g, 2));
+        g = max(g, __shfl_xor_sync(0xffffffffu, g, 1));
+        if ((lane & 15) == 0) {
+          const int k = tile * kTileBlocks + half * 2 + (lane >> 4);
+          if (k >= sr.k_lo && k < sr.k_hi) a.block_max[row * a.max_pages + k] = g;
+        }
+        tmax = max(tmax, g);
       }
-      tmax = max(tmax, g);
+      tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+      if (a.tile_max != nullptr && lane == 0) a.tile_max[row * a.max_tiles + tile] = tmax;
     }
-    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-    if (a.tile_max != nullptr && lane == 0)
-      a.tile_max[((size_t)b * a.hkv + h) * a.max_tiles + tile] = tmax;
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
@@ -492,10 +501,14 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
     return launch_kernel(kernel, dim3(grid), dim3(C::kThreads), smem, st, true, kq_map, kq_map4,
                          a);
   };
-#define HSA_SCORE_CASE(g)                                                          \
-  case g:                                                                          \
-    e = s.key_bits == 4 ? go(score_blocks_kernel<g, true>, ScoreCfg<g, true>{})    \
-                        : go(score_blocks_kernel<g, false>, ScoreCfg<g, false>{}); \
+#define HSA_SCORE_CASE(g)                                                               \
+  case g:                                                                               \
+    if (s.per_head)                                                                     \
+      e = s.key_bits == 4 ? go(score_blocks_kernel<g, true, true>, ScoreCfg<g, true>{}) \
+                          : go(score_blocks_kernel<g, false, true>, ScoreCfg<g, false>{}); \
+    else                                                                                \
+      e = s.key_bits == 4 ? go(score_blocks_kernel<g, true, false>, ScoreCfg<g, true>{}) \
+                          : go(score_blocks_kernel<g, false, false>, ScoreCfg<g, false>{}); \
     break;
   cudaError_t e;
   switch (s.group) {

@@ -52,6 +52,7 @@ class Config:
     chunk0: int = 0  # k0 > 0: a pruning module on chunks of chunk0 tokens in front
     k0: int = 0
     key_bits: int = 8  # key codes: 8-bit, or 4-bit (two per byte)
+    per_head: int = 0  # 1: every query head selects its own blocks
 
 
 CONFIGS: Dict[str, Config] = {
@@ -78,6 +79,9 @@ CONFIGS: Dict[str, Config] = {
     # a 128K step with groups of 8 query heads (Llama-3-70B-shaped attention layer)
     "llama3-70b-128k": Config("llama3-70b-128k", 1, 64, 8, 131072, None,
                               k1=256, k2=128, sink=128, window=1024),
+    # the 128K step with per-head selection (every query head keeps its own 128 blocks)
+    "llama3-8b-128k-perhead": Config("llama3-8b-128k-perhead", 1, 32, 8, 131072, None,
+                                     k1=256, k2=128, sink=128, window=1024, per_head=1),
     # the 128K and 1M steps with 4-bit key codes (half the bytes the scorer reads)
     "llama3-8b-128k-int4": Config("llama3-8b-128k-int4", 1, 32, 8, 131072, None,
                                   k1=256, k2=128, sink=128, window=1024, key_bits=4),

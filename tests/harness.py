@@ -18,21 +18,22 @@ MAX_REL_L2 = 5e-3
 
 def dims_pair(wl: dict, **over):
     """(hsa.Dims, oracle.Dims) for a workload, with optional overrides of k1, k2, sink,
-    window, chunk, chunk0, k0, key_bits."""
+    window, chunk, chunk0, k0, key_bits, per_head."""
     cfg = wl["config"]
     p = dict(k1=cfg.k1, k2=cfg.k2, sink=cfg.sink, window=cfg.window, chunk=cfg.chunk,
-             chunk0=cfg.chunk0, k0=cfg.k0, key_bits=cfg.key_bits)
+             chunk0=cfg.chunk0, k0=cfg.k0, key_bits=cfg.key_bits, per_head=0)
     p.update(over)
     hd = hsa.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, max_pages_per_seq=wl["max_pages"],
                   num_pages=wl["num_pages"], chunk=p["chunk"], k1=p["k1"], k2=p["k2"],
                   sink=p["sink"], window=p["window"],
                   kv_on_host=wl["k_cache"].device.type == "cpu" and wl["k_cache"].is_pinned(),
-                  chunk0=p["chunk0"], k0=p["k0"], key_bits=p["key_bits"])
+                  chunk0=p["chunk0"], k0=p["k0"], key_bits=p["key_bits"],
+                  per_head=p["per_head"])
     od = oracle.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, head_dim=W.HEAD_DIM,
                      page_size=W.PAGE, max_pages_per_seq=wl["max_pages"],
                      num_pages=wl["num_pages"], chunk=p["chunk"], block=16, k1=p["k1"],
                      k2=p["k2"], sink=p["sink"], window=p["window"], chunk0=p["chunk0"],
-                     k0=p["k0"], key_bits=p["key_bits"])
+                     k0=p["k0"], key_bits=p["key_bits"], per_head=p["per_head"])
     return hd, od
 
 
@@ -70,22 +71,23 @@ def gpu_step(wl: dict, d: hsa.Dims, dense: bool = True) -> dict:
     """Quantise the keys, score, prune, attend (and dense decode) through the C ABI."""
     dev = torch.device("cuda")
     B, Hq, Hkv = d.batch, d.hq, d.hkv
+    R = Hq if d.per_head else Hkv  # selection rows per sequence
     kq = kq_like(wl["k_cache"], d)
     k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
     wq = hsa.workspace(d, hsa.HSA_OP_QUANTIZE)
     hsa.hsa_quantize_keys(d, wl["k_cache"], wl["page_table"], wl["seq_lens"], 0, 0, kq, k_scale, wq)
-    bm = torch.full((B, Hkv, d.max_pages_per_seq), INT32_MIN, dtype=torch.int32, device=dev)
+    bm = torch.full((B, R, d.max_pages_per_seq), INT32_MIN, dtype=torch.int32, device=dev)
     hsa.hsa_score_blocks(d, wl["q"], kq, k_scale, wl["page_table"], wl["seq_lens"], bm)
-    chunk_idx = torch.full((B, Hkv, max(d.k1, 1)), -7, dtype=torch.int32, device=dev)
-    n_chunks = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
-    block_idx = torch.full((B, Hkv, max(d.k2, 1)), -7, dtype=torch.int32, device=dev)
-    n_blocks = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+    chunk_idx = torch.full((B, R, max(d.k1, 1)), -7, dtype=torch.int32, device=dev)
+    n_chunks = torch.full((B, R), -7, dtype=torch.int32, device=dev)
+    block_idx = torch.full((B, R, max(d.k2, 1)), -7, dtype=torch.int32, device=dev)
+    n_blocks = torch.full((B, R), -7, dtype=torch.int32, device=dev)
     ws = hsa.workspace(d, hsa.HSA_OP_SELECT)
     hsa.hsa_select(d, wl["q"], kq, k_scale, wl["page_table"], wl["seq_lens"], chunk_idx, n_chunks,
                    block_idx, n_blocks, ws)
     # the split entry points (score with per-tile maxima, then prune) agree with hsa_select
     bm2 = torch.full_like(bm, INT32_MIN)
-    tm = torch.full((B, Hkv, (d.max_pages_per_seq + 3) // 4), INT32_MIN, dtype=torch.int32,
+    tm = torch.full((B, R, (d.max_pages_per_seq + 3) // 4), INT32_MIN, dtype=torch.int32,
                     device=dev)
     hsa.hsa_score_blocks(d, wl["q"], kq, k_scale, wl["page_table"], wl["seq_lens"], bm2, tm)
     bi2 = torch.full_like(block_idx, -7)
@@ -95,8 +97,8 @@ def gpu_step(wl: dict, d: hsa.Dims, dense: bool = True) -> dict:
     torch.cuda.synchronize()
     assert torch.equal(bm2, bm)
     k_tiles = tm.shape[-1]
-    pad = torch.full((B, Hkv, 4 * k_tiles - bm.shape[-1]), INT32_MIN, dtype=torch.int32, device=dev)
-    assert torch.equal(tm, torch.cat([bm, pad], dim=-1).view(B, Hkv, k_tiles, 4).amax(-1))
+    pad = torch.full((B, R, 4 * k_tiles - bm.shape[-1]), INT32_MIN, dtype=torch.int32, device=dev)
+    assert torch.equal(tm, torch.cat([bm, pad], dim=-1).view(B, R, k_tiles, 4).amax(-1))
     assert torch.equal(bi2, block_idx) and torch.equal(nb2, n_blocks)
     assert torch.equal(ci2, chunk_idx)
     wa = hsa.workspace(d, hsa.HSA_OP_ATTEND)
@@ -172,18 +174,20 @@ def logical_rows(arr: np.ndarray, pt: np.ndarray, lens, b: int, h: int) -> np.nd
 
 
 def compare_step(g: dict, o: dict, h: dict, od: oracle.Dims, bh_pairs, dense: bool = True):
-    """Bit-exact integer outputs and toleranced float outputs on the (b, h) pairs given."""
+    """Bit-exact integer outputs and toleranced float outputs on the (b, h) pairs given
+    (with per-head selection, the selection rows of every query head of kv head h)."""
     G = od.hq // od.hkv
     stats = []
     for b, hh in bh_pairs:
         np.testing.assert_array_equal(g["k_scale"][b, hh], o["k_scale"][b, hh])
         np.testing.assert_array_equal(logical_rows(g["kq"], h["pt"], h["lens"], b, hh),
                                       logical_rows(o["kq"], h["pt"], h["lens"], b, hh))
-        np.testing.assert_array_equal(g["block_max"][b, hh], o["block_max"][b, hh])
-        np.testing.assert_array_equal(g["chunk_idx"][b, hh], o["chunk_idx"][b, hh])
-        np.testing.assert_array_equal(g["n_chunks"][b, hh], o["n_chunks"][b, hh])
-        np.testing.assert_array_equal(g["block_idx"][b, hh], o["block_idx"][b, hh])
-        np.testing.assert_array_equal(g["n_blocks"][b, hh], o["n_blocks"][b, hh])
+        for r in (range(hh * G, hh * G + G) if od.per_head else (hh,)):
+            np.testing.assert_array_equal(g["block_max"][b, r], o["block_max"][b, r])
+            np.testing.assert_array_equal(g["chunk_idx"][b, r], o["chunk_idx"][b, r])
+            np.testing.assert_array_equal(g["n_chunks"][b, r], o["n_chunks"][b, r])
+            np.testing.assert_array_equal(g["block_idx"][b, r], o["block_idx"][b, r])
+            np.testing.assert_array_equal(g["n_blocks"][b, r], o["n_blocks"][b, r])
         rows = slice(hh * G, (hh + 1) * G)
         stats.append(assert_close(g["out"][b, rows], o["out"][b, rows], f"sparse out b{b} h{hh}"))
         np.testing.assert_allclose(g["lse"][b, rows], o["lse"][b, rows], atol=2e-4, rtol=1e-5)

@@ -74,6 +74,20 @@ def test_group_sizes(hq, hkv, key_bits):
     _check(wl, sink=40, window=200)
 
 
+@pytest.mark.parametrize("hq,hkv,key_bits,chunk", [(8, 2, 8, 64), (16, 2, 8, 64), (8, 2, 4, 64),
+                                                    (4, 1, 8, 32), (8, 8, 8, 64)])
+def test_per_head_selection(hq, hkv, key_bits, chunk):
+    """Every query head selects its own chunks and blocks: per-head block and tile maxima,
+    one selection row per query head, each head's attention over its own row."""
+    wl = W.make_workload(_cfg(context=None, context_range=(900, 7000), batch=2, hq=hq, hkv=hkv,
+                              paged_permuted=True, key_bits=key_bits), seed=60 + hq + key_bits)
+    g, o = _check(wl, per_head=1, chunk=chunk, k1=12, k2=10, sink=24, window=150)
+    # the heads of a group do not all keep the same blocks
+    if hq // hkv > 1:
+        assert any(not np.array_equal(g["block_idx"][b, 0], g["block_idx"][b, 1])
+                   for b in range(2))
+
+
 def test_unaligned_sink_and_window():
     wl = W.make_workload(_cfg(context=7777, batch=3, hq=8, hkv=2), seed=21)
     _check(wl, k1=11, k2=19, sink=37, window=101)
@@ -212,23 +226,25 @@ def _clone(t):
     return t.clone().pin_memory() if t.device.type == "cpu" else t.clone()
 
 
-@pytest.mark.parametrize("window,k1,k2,on_host,hq", [(0, 6, 9, False, 8), (1, 6, 9, False, 8),
-                                                     (5, 3, 0, False, 8), (300, 8, 8, False, 8),
-                                                     (0, 6, 9, True, 8), (300, 8, 8, True, 8),
-                                                     (300, 8, 8, False, 16), (40, 8, 8, True, 16)])
-def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2, on_host, hq):
+@pytest.mark.parametrize("window,k1,k2,on_host,hq,per_head", [
+    (0, 6, 9, False, 8, 0), (1, 6, 9, False, 8, 0), (5, 3, 0, False, 8, 0),
+    (300, 8, 8, False, 8, 0), (0, 6, 9, True, 8, 0), (300, 8, 8, True, 8, 0),
+    (300, 8, 8, False, 16, 0), (40, 8, 8, True, 16, 0),
+    (0, 6, 9, False, 8, 1), (300, 8, 8, False, 8, 1), (40, 8, 8, True, 16, 1)])
+def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2, on_host, hq, per_head):
     """The whole step (append ordered before or beside the scorer, prune, attend with the
     sink and window pages fetched early) equals the separate calls bit for bit, and the
-    oracle on the appended cache; also with K/V in mapped pinned host memory, and with
-    groups of 8 query heads."""
+    oracle on the appended cache; also with K/V in mapped pinned host memory, with groups
+    of 8 query heads, and with per-head selection."""
     cfg = _cfg(context=None, context_range=(700, 5000), batch=3, hq=hq, hkv=2, k1=k1, k2=k2,
                sink=20, window=window, paged_permuted=True)
     wl = W.make_workload(cfg, seed=40 + window, host_pinned=on_host)
-    hd, od = H.dims_pair(wl)
+    hd, od = H.dims_pair(wl, per_head=per_head)
     assert bool(hd.kv_on_host) == on_host
     dwl = H.to_cuda(wl)
     dev = torch.device("cuda")
     B, Hkv = cfg.batch, cfg.hkv
+    R = cfg.hq if per_head else Hkv  # selection rows per sequence
     gen = torch.Generator(device="cpu").manual_seed(7 + window)
     k_new = torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16)
     v_new = torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16)
@@ -240,8 +256,8 @@ def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2, on_host, 
     kc1, vc1, kq1 = _clone(dwl["k_cache"]), _clone(dwl["v_cache"]), kq.clone()
     out1 = torch.zeros((B, cfg.hq, 128), dtype=torch.float32, device=dev)
     lse1 = torch.zeros((B, cfg.hq), dtype=torch.float32, device=dev)
-    bidx1 = torch.full((B, Hkv, max(k2, 1)), -7, dtype=torch.int32, device=dev)
-    nb1 = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+    bidx1 = torch.full((B, R, max(k2, 1)), -7, dtype=torch.int32, device=dev)
+    nb1 = torch.full((B, R), -7, dtype=torch.int32, device=dev)
     wst = hsa.workspace(hd, hsa.HSA_OP_STEP)
     for _ in range(2):  # the second call finds the first call's workspace contents
         hsa.hsa_decode_step(hd, dwl["q"], k_new.cuda(), v_new.cuda(), out1, lse1, kc1, vc1, kq1,

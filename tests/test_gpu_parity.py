@@ -67,6 +67,13 @@ def test_llama3_70b_shaped_128k_groups_of_8_sampled_heads():
     _run(wl, bh_pairs=[(0, 0), (0, 7)])
 
 
+def test_llama3_8b_128k_per_head_selection_sampled_heads():
+    """Per-head selection at 128K: the 4 query heads of kv heads 1 and 6, each on its own
+    selection row."""
+    wl = W.make_workload(W.CONFIGS["llama3-8b-128k"], seed=0, device="cuda")
+    _run(wl, bh_pairs=[(0, 1), (0, 6)], per_head=1)
+
+
 def test_tiny_8k_four_bit_keys():
     """4-bit key codes: codes (unpacked from their nibbles), scales amax / 7, block maxima
     and selections bit-exact against the oracle's 4-bit format; outputs within tolerance."""
