@@ -45,13 +45,14 @@ constexpr int kTileBlocks = 4;                  // blocks per ring slot (64 toke
 constexpr int kTileTokens = kTileBlocks * kPage;
 constexpr int kMaxBatch = 1024;                 // sequences (the tile prefix sums in shared memory)
 
-// Launch shape and shared-memory layout of one scorer instance.
-template <int G, bool KB4>
+// Launch shape and shared-memory layout of one scorer instance (PH: per-head maxima, whose
+// epilogue needs the registers the query words would take).
+template <int G, bool KB4, bool PH>
 struct ScoreCfg {
-  static constexpr bool kQSmem = KB4 || G > 4;  // query words in shared memory
+  static constexpr bool kQSmem = KB4 || G > 4 || PH;  // query words in shared memory
   static constexpr int kWarps = KB4 ? HSA_SCORE_QS_WARPS : 4;  // consumer warps
   static constexpr int kThreads = (kWarps + 1) * 32;
-  static constexpr int kCtasPerSm = KB4 ? HSA_SCORE_QS_CTAS : (G > 4 ? 3 : 2);
+  static constexpr int kCtasPerSm = KB4 ? HSA_SCORE_QS_CTAS : (kQSmem ? 3 : 2);
   // 8-bit codes: one 128-byte row per token; 4-bit codes: two tokens per row
   static constexpr int kRowsPerBlock = KB4 ? kPage / 2 : kPage;
   static constexpr int kBlockBytes = kRowsPerBlock * kHeadDim;
@@ -183,10 +184,10 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
 // PH: per-head selection, the maxima of every query head (rows b * hq + h * G + j) rather
 // than of the group's token scores.
 template <int G, bool KB4, bool PH>
-__global__ void __launch_bounds__(ScoreCfg<G, KB4>::kThreads, ScoreCfg<G, KB4>::kCtasPerSm)
+__global__ void __launch_bounds__(ScoreCfg<G, KB4, PH>::kThreads, ScoreCfg<G, KB4, PH>::kCtasPerSm)
     score_blocks_kernel(const __grid_constant__ CUtensorMap kq_map,
                         const __grid_constant__ CUtensorMap kq_map4, const ScoreArgs a) {
-  using C = ScoreCfg<G, KB4>;
+  using C = ScoreCfg<G, KB4, PH>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -504,11 +505,13 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
 #define HSA_SCORE_CASE(g)                                                               \
   case g:                                                                               \
     if (s.per_head)                                                                     \
-      e = s.key_bits == 4 ? go(score_blocks_kernel<g, true, true>, ScoreCfg<g, true>{}) \
-                          : go(score_blocks_kernel<g, false, true>, ScoreCfg<g, false>{}); \
+      e = s.key_bits == 4                                                               \
+              ? go(score_blocks_kernel<g, true, true>, ScoreCfg<g, true, true>{})       \
+              : go(score_blocks_kernel<g, false, true>, ScoreCfg<g, false, true>{});    \
     else                                                                                \
-      e = s.key_bits == 4 ? go(score_blocks_kernel<g, true, false>, ScoreCfg<g, true>{}) \
-                          : go(score_blocks_kernel<g, false, false>, ScoreCfg<g, false>{}); \
+      e = s.key_bits == 4                                                               \
+              ? go(score_blocks_kernel<g, true, false>, ScoreCfg<g, true, false>{})     \
+              : go(score_blocks_kernel<g, false, false>, ScoreCfg<g, false, false>{});  \
     break;
   cudaError_t e;
   switch (s.group) {
