@@ -221,14 +221,14 @@ typedef struct hsa_step_io {
   const void* v_new;  /* bf16 [batch][hkv][128]: the new token's value */
   float* out;         /* f32 [batch][hq][128] */
   float* lse;         /* f32 [batch][hq] (nullable) */
-  int32_t io_on_host; /* 1: the five pointers above are PINNED HOST memory. When all of it
-                         is mapped into the device (cudaHostGetDevicePointer succeeds: the
-                         default for pinned memory with unified addressing), a kernel reads
-                         the inputs and the attention writes the outputs over the host link;
-                         otherwise the call copies the inputs in and the outputs back with
-                         cudaMemcpyAsync. Either way everything is ordered on `stream`: the
-                         caller synchronises it before reading the outputs or reusing the
-                         inputs. */
+  int32_t io_on_host; /* 1: the five pointers above are PINNED HOST memory. When the device
+                         addresses all of it (it reads host memory through the host's page
+                         tables, or cudaHostGetDevicePointer succeeds: the default for pinned
+                         memory with unified addressing), a kernel reads the inputs and the
+                         attention writes the outputs over the host link; otherwise the call
+                         copies the inputs in and the outputs back with cudaMemcpyAsync.
+                         Either way everything is ordered on `stream`: the caller
+                         synchronises it before reading the outputs or reusing the inputs. */
 } hsa_step_io;
 
 /*

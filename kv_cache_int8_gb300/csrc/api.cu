@@ -274,8 +274,36 @@ int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map, CUtens
   return HSA_OK;
 }
 
-// Device alias of a mapped pinned host buffer; false (error state cleared) if it has none.
+// Whether kernels of the current device address host memory by its host pointers: the GPU
+// reaches pageable memory through the host's own page tables (address translation services
+// over a coherent link), so a host buffer, pinned or not, needs no alias lookup. Queried once
+// per device; the lookups it saves cost a few microseconds each per call.
+bool host_pointers_direct() {
+  static std::atomic<int> cache[64];  // 0 unknown, 1 direct, 2 aliases needed
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  int v = cache[dev].load();
+  if (v == 0) {
+    int pageable = 0, host_tables = 0;
+    if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&host_tables, cudaDevAttrPageableMemoryAccessUsesHostPageTables,
+                               dev) != cudaSuccess) {
+      cudaGetLastError();
+      pageable = 0;
+    }
+    v = (pageable && host_tables) ? 1 : 2;
+    cache[dev].store(v);
+  }
+  return v == 1;
+}
+
+// Device alias of a host buffer the GPU can address (mapped pinned memory, or any host
+// memory with host_pointers_direct); false (error state cleared) if it has none.
 bool host_alias(const void* p, void** out) {
+  if (host_pointers_direct()) {
+    *out = const_cast<void*>(p);
+    return true;
+  }
   void* dp = nullptr;
   if (cudaHostGetDevicePointer(&dp, const_cast<void*>(p), 0) != cudaSuccess || dp == nullptr) {
     cudaGetLastError();
@@ -287,7 +315,7 @@ bool host_alias(const void* p, void** out) {
 
 // Device alias of a pinned host buffer (kv_on_host) or the pointer itself.
 int32_t kv_pointer(const hsa_dims* d, const void* p, const void** out) {
-  if (!d->kv_on_host) {
+  if (!d->kv_on_host || host_pointers_direct()) {
     *out = p;
     return HSA_OK;
   }

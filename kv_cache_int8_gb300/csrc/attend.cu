@@ -699,8 +699,7 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
       // fetched before the wait for the selection
       const int jend = jb < n_pre ? min(n_pre, jb + 32) : min(cnt, jb + 32);
       if (!have_sel && jb >= n_pre) {
-        grid_dep_wait();
-        read_selection(S, a, b, h);
+        grid_dep_wait();  // the kept blocks come from the previous kernel
         have_sel = true;
       }
       int k = 0, t0 = 0, t1 = 0, page = -1;
@@ -712,12 +711,14 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
           if (t0 < t1)
             page = a.seg_slots ? a.seg_slots[sbase + i] : a.page_table[(size_t)b * a.max_pages + k];
         } else {
-          // a kept block: its id and (when given) its page are read in the same round trip
-          // as the count of kept blocks (both lists hold K2 entries; r < K2)
+          // a kept block: the count of kept blocks, its id and (when given) its page, all in
+          // one round trip (both lists hold K2 entries; r < K2)
           const int r = i - n_sw;
           const size_t at = ((size_t)b * a.hkv + h) * a.k2 + r;
+          const int nb = a.n_blocks[(size_t)b * a.hkv + h];
           const int kk = a.block_idx[at];
           const int pp = a.seg_slots ? a.seg_slots[sbase + i] : (a.sel_pages ? a.sel_pages[at] : -1);
+          S.n_sel = max(0, min(nb, S.n_sel_max));
           kept_segment(S, r, kk, a.sink, k, t0, t1);
           if (t0 < t1)
             page = (a.seg_slots || a.sel_pages) ? pp : a.page_table[(size_t)b * a.max_pages + k];
@@ -729,6 +730,29 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
         if (page < 0) t0 = t1 = 0;
       }
       const int n = jend - jb;
+      // A copy of segment j goes to ring slot j % NS once that slot's previous segment is
+      // done. While the batch uses every slot for the first time (no waits), each lane
+      // issues its own segment's copies, all lanes at once; otherwise lane 0 issues them
+      // in order, waiting for slots as they free up.
+      if (jend <= NS) {
+        if (lane < n) {
+          const int s = jb + lane;
+          meta[s] = make_int4(k, t0, t1, 0);
+          if (page >= 0) {
+            const size_t off = a.seg_slots ? (size_t)page * (2 * kPage * kHeadDim)
+                                           : ((size_t)page * a.kv_heads + h / a.kv_div) *
+                                                 kPage * kHeadDim;
+            mbar_arrive_expect_tx(&full[s], kSlotBytes);
+            bulk_load_hint(ring + s * kSlotBytes, a.k + off, kBlockBytesBf16, &full[s], policy);
+            bulk_load_hint(ring + s * kSlotBytes + kBlockBytesBf16, a.v + off, kBlockBytesBf16,
+                           &full[s], policy);
+          } else {
+            mbar_arrive(&full[s]);
+          }
+        }
+        jb = jend;
+        continue;
+      }
       for (int q = 0; q < n; q++) {
         const int kq = __shfl_sync(0xffffffffu, k, q);
         const int t0q = __shfl_sync(0xffffffffu, t0, q);

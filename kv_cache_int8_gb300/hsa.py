@@ -152,8 +152,13 @@ def _p(t) -> Optional[int]:
     return t.data_ptr()
 
 
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream=None) -> int:
     if stream is None:
+        if _RAW_STREAM is not None:  # the current stream's handle without a Stream object
+            return _RAW_STREAM(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
