@@ -731,10 +731,11 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
       }
       const int n = jend - jb;
       // A copy of segment j goes to ring slot j % NS once that slot's previous segment is
-      // done. While the batch uses every slot for the first time (no waits), each lane
-      // issues its own segment's copies, all lanes at once; otherwise lane 0 issues them
-      // in order, waiting for slots as they free up.
-      if (jend <= NS) {
+      // done. While a sparse batch uses every slot for the first time (no waits), each lane
+      // issues its own segment's copies, all lanes at once; otherwise lane 0 issues them in
+      // order, waiting for slots as they free up (dense decode always: its long contiguous
+      // ranges never fit the ring, and the extra path measurably slowed it).
+      if (!DENSE && jend <= NS) {
         if (lane < n) {
           const int s = jb + lane;
           meta[s] = make_int4(k, t0, t1, 0);
