@@ -78,6 +78,15 @@ def test_workspace_sizes(lib):
     for bits in (0, 4, 8):
         assert lib.hsa_workspace_bytes(_dims(lib, key_bits=bits), 0) > 0
     assert lib.hsa_workspace_bytes(_dims(lib, key_bits=2), 0) == 0
+    # per-head selection: one selection row per query head (4x the block maxima here)
+    sel = lib.hsa_workspace_bytes(_dims(lib), lib.HSA_OP_SELECT)
+    sel_ph = lib.hsa_workspace_bytes(_dims(lib, per_head=1), lib.HSA_OP_SELECT)
+    assert sel_ph >= 4 * (sel - 256)
+    assert lib.hsa_workspace_bytes(_dims(lib, per_head=2), 0) == 0
+    # the block cache plan works per kv head: no cache with per-head selection
+    host = dict(kv_on_host=True, k2=16, sink=64, window=256)
+    assert lib.load().hsa_block_cache_bytes(_dims(lib, **host).c(), 4096) > 0
+    assert lib.load().hsa_block_cache_bytes(_dims(lib, per_head=1, **host).c(), 4096) == 0
 
 
 @pytest.mark.parametrize("kw,code", [
