@@ -264,6 +264,31 @@ def hsa_decode_step(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_
         _stream(stream)))
 
 
+class DecodeStep:
+    """hsa_decode_step over a fixed set of buffers, for a decode loop that calls it every
+    step: the C arguments are marshalled once, so a call costs the C call alone. The
+    buffers' contents may change between calls (new q / k_new / v_new, longer seq_lens);
+    the buffers themselves must stay alive and in place."""
+
+    def __init__(self, d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_scale,
+                 page_table, seq_lens, block_idx, n_blocks, ws, io_on_host: bool = False,
+                 stream=None):
+        self._keep = (q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_scale, page_table,
+                      seq_lens, block_idx, n_blocks, ws)
+        self._cd = d.c()
+        self._io = hsa_step_io(_p(q), _p(k_new), _p(v_new), _p(out), _p(lse),
+                               1 if io_on_host else 0)
+        self._fn = load().hsa_decode_step
+        self._args = (ctypes.byref(self._cd), ctypes.byref(self._io), _p(k_cache), _p(v_cache),
+                      _p(kq), _p(k_scale), _p(page_table), _p(seq_lens), _p(block_idx),
+                      _p(n_blocks), _p(ws), ws.numel(), _stream(stream))
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != HSA_OK:
+            _check("hsa_decode_step", rc)
+
+
 def hsa_decode_step_reuse(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_scale,
                           page_table, seq_lens, block_idx, n_blocks, ws, io_on_host: bool = False,
                           stream=None) -> None:

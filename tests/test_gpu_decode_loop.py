@@ -21,6 +21,57 @@ def _clone(t):
     return t.clone().pin_memory() if t.device.type == "cpu" else t.clone()
 
 
+def test_prepared_decode_step_equals_the_plain_call():
+    """hsa.DecodeStep (arguments marshalled once) gives the same bits as hsa_decode_step,
+    with host I/O, over several steps whose inputs change in place."""
+    cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None,
+                              context_range=(2000, 4000), batch=2, hq=8, hkv=2, k1=10, k2=8,
+                              sink=32, window=64, paged_permuted=True)
+    wl = W.make_workload(cfg, seed=5)
+    hd, _ = H.dims_pair(wl)
+    dwl = H.to_cuda(wl)
+    dev = torch.device("cuda")
+    B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
+    kq = H.kq_like(dwl["k_cache"], hd)
+    k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
+    hsa.hsa_quantize_keys(hd, dwl["k_cache"], dwl["page_table"], dwl["seq_lens"], 0, 0, kq,
+                          k_scale, hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
+    gen = torch.Generator(device="cpu").manual_seed(9)
+    res = []
+    for prepared in (False, True):
+        kc, vc, kqc = dwl["k_cache"].clone(), dwl["v_cache"].clone(), kq.clone()
+        q = torch.zeros((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
+        kn = torch.zeros((B, Hkv, 128), dtype=torch.bfloat16).pin_memory()
+        vn = torch.zeros((B, Hkv, 128), dtype=torch.bfloat16).pin_memory()
+        out = torch.zeros((B, Hq, 128), dtype=torch.float32).pin_memory()
+        lse = torch.zeros((B, Hq), dtype=torch.float32).pin_memory()
+        lens = dwl["seq_lens"].clone()
+        ws = hsa.workspace(hd, hsa.HSA_OP_STEP)
+        args = (hd, q, kn, vn, out, lse, kc, vc, kqc, k_scale, dwl["page_table"], lens, None,
+                None, ws)
+        step = hsa.DecodeStep(*args, io_on_host=True) if prepared else None
+        gen.manual_seed(9)
+        outs = []
+        for i in range(3):
+            q.copy_(torch.randn((B, Hq, 128), generator=gen).to(torch.bfloat16))
+            kn.copy_(torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16))
+            vn.copy_(torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16))
+            if i:
+                lens.sub_(1)  # the step before: one token shorter, same buffers
+            if prepared:
+                step()
+            else:
+                hsa.hsa_decode_step(*args, io_on_host=True)
+            torch.cuda.synchronize()
+            assert hsa.hsa_read_device_error(ws) == 0
+            outs.append((out.clone(), lse.clone()))
+        res.append((outs, kc, vc, kqc))
+    for (o1, l1), (o2, l2) in zip(res[0][0], res[1][0]):
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for a, b in zip(res[0][1:], res[1][1:]):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("refresh,on_host,key_bits", [(3, False, 8), (2, True, 8), (1, False, 8),
                                                        (2, False, 4)])
 def test_decode_loop_with_selection_reuse(refresh, on_host, key_bits):
