@@ -35,6 +35,19 @@
 #ifndef HSA_SCORE_QS_RING_KB
 #define HSA_SCORE_QS_RING_KB 64
 #endif
+// The same for the 8-bit-code instances that keep the query words in registers. Measured on
+// GB300 (one-launch graphs, 128K / 1M): 4 warps x 2 CTAs with 64 KiB rings 27.1 / 157.7 us;
+// 8 x 1 with 128 KiB 34.7 / 214.9; 4 x 2 with 96 KiB 27.3 / 165.8; 2 x 3 with 64 KiB
+// 29.8 / 171.1.
+#ifndef HSA_SCORE_WARPS
+#define HSA_SCORE_WARPS 4
+#endif
+#ifndef HSA_SCORE_CTAS
+#define HSA_SCORE_CTAS 2
+#endif
+#ifndef HSA_SCORE_RING_KB
+#define HSA_SCORE_RING_KB 64
+#endif
 
 namespace hsa {
 namespace {
@@ -50,14 +63,15 @@ constexpr int kMaxBatch = 1024;                 // sequences (the tile prefix su
 template <int G, bool KB4, bool PH>
 struct ScoreCfg {
   static constexpr bool kQSmem = KB4 || G > 4 || PH;  // query words in shared memory
-  static constexpr int kWarps = KB4 ? HSA_SCORE_QS_WARPS : 4;  // consumer warps
+  static constexpr int kWarps = KB4 ? HSA_SCORE_QS_WARPS : (kQSmem ? 4 : HSA_SCORE_WARPS);
   static constexpr int kThreads = (kWarps + 1) * 32;
-  static constexpr int kCtasPerSm = KB4 ? HSA_SCORE_QS_CTAS : (kQSmem ? 3 : 2);
+  static constexpr int kCtasPerSm = KB4 ? HSA_SCORE_QS_CTAS : (kQSmem ? 3 : HSA_SCORE_CTAS);
   // 8-bit codes: one 128-byte row per token; 4-bit codes: two tokens per row
   static constexpr int kRowsPerBlock = KB4 ? kPage / 2 : kPage;
   static constexpr int kBlockBytes = kRowsPerBlock * kHeadDim;
   static constexpr int kSlotBytes = kTileBlocks * kBlockBytes;
-  static constexpr int kRingBytes = (KB4 ? HSA_SCORE_QS_RING_KB : 64) * 1024;  // ring of one CTA
+  static constexpr int kRingBytes =
+      (KB4 ? HSA_SCORE_QS_RING_KB : (kQSmem ? 64 : HSA_SCORE_RING_KB)) * 1024;  // one CTA's ring
   static constexpr int kStages = kRingBytes / kSlotBytes;
   static_assert(kStages % kWarps == 0 && kStages / kWarps >= 2,
                 "every consumer warp owns at least two fixed ring slots");
