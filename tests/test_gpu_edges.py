@@ -47,6 +47,20 @@ def test_mixed_batch_permuted_pages():
     _check(wl)
 
 
+def test_empty_sequence_in_a_batch():
+    """A sequence of length 0 beside others: zero scales and codes, nothing selected, output
+    0 and lse -inf for its heads; the other sequences as usual (dense decode too)."""
+    cfg = _cfg(context=None, context_range=(600, 3000), batch=3, hq=8, hkv=2, k1=6, k2=7,
+               sink=20, window=50, paged_permuted=True)
+    wl = W.make_workload(cfg, seed=13)
+    wl["seq_lens"][1] = 0
+    wl["lens"][1] = 0
+    g, o = _check(wl)
+    assert (g["n_blocks"][1] == 0).all() and (g["k_scale"][1] == 0).all()
+    assert (g["out"][1] == 0).all() and np.isneginf(g["lse"][1]).all()
+    assert (g["out_dense"][1] == 0).all() and np.isneginf(g["lse_dense"][1]).all()
+
+
 @pytest.mark.parametrize("k1,k2", [(0, 0), (0, 5), (5, 0), (1, 1), (3, 40)])
 def test_small_and_zero_budgets(k1, k2):
     wl = W.make_workload(_cfg(context=4099, batch=2, hq=8, hkv=2), seed=11)
