@@ -107,8 +107,8 @@ struct Segments {
 };
 
 // The attended set as a list of segments: the sink pages, the window pages, then up to K2
-// kept blocks. Everything but the number of kept blocks (n_sel, see read_selection) is
-// known from the sequence length alone.
+// kept blocks. Everything but the number of kept blocks (n_sel: read_selection, or the HBM
+// path's producer with the kept ids) is known from the sequence length alone.
 template <bool DENSE>
 __device__ __forceinline__ Segments make_segments(const AttArgs& a, int b, int h) {
   Segments s;
