@@ -72,15 +72,16 @@ def test_prepared_decode_step_equals_the_plain_call():
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("refresh,on_host,key_bits", [(3, False, 8), (2, True, 8), (1, False, 8),
-                                                       (2, False, 4)])
-def test_decode_loop_with_selection_reuse(refresh, on_host, key_bits):
+@pytest.mark.parametrize("refresh,on_host,key_bits,per_head", [(3, False, 8, 0), (2, True, 8, 0),
+                                                                (1, False, 8, 0), (2, False, 4, 0),
+                                                                (2, False, 8, 1)])
+def test_decode_loop_with_selection_reuse(refresh, on_host, key_bits, per_head):
     steps = 6
     cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None,
                               context_range=(3000, 6000), batch=2, hq=8, hkv=2, k1=12, k2=10,
                               sink=32, window=96, paged_permuted=True, key_bits=key_bits)
     wl = W.make_workload(cfg, seed=77 + refresh, host_pinned=on_host)
-    hd, od = H.dims_pair(wl)
+    hd, od = H.dims_pair(wl, per_head=per_head)
     dwl = H.to_cuda(wl)
     dev = torch.device("cuda")
     B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
@@ -100,8 +101,9 @@ def test_decode_loop_with_selection_reuse(refresh, on_host, key_bits):
 
     gen = torch.Generator(device="cpu").manual_seed(1234 + refresh)
     ws = hsa.workspace(hd, hsa.HSA_OP_STEP)
-    bidx = torch.full((B, Hkv, cfg.k2), -7, dtype=torch.int32, device=dev)
-    nb = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev)
+    R = Hq if per_head else Hkv  # selection rows per sequence
+    bidx = torch.full((B, R, cfg.k2), -7, dtype=torch.int32, device=dev)
+    nb = torch.full((B, R), -7, dtype=torch.int32, device=dev)
     sel = None
     for i in range(steps):
         lens = start + 1 + i
