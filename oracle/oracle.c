@@ -67,6 +67,7 @@ typedef struct {
   int32_t chunk0, k0; /* k0 > 0: a first module keeps the top-k0 chunks of chunk0 tokens */
   int32_t key_bits;   /* 4: 4-bit key codes (levels +-7); 0 or 8: 8-bit (levels +-127) */
   int32_t per_head;   /* 1: every query head selects its own chunks and blocks (N3 variant) */
+  int32_t key_fp8;    /* 1: FP8 E4M3 key codes (scale amax / 448, fp32 scores; N4 variant) */
 } oracle_dims;
 
 /* Rows of the selection outputs per sequence: one per kv head (the group shares one
@@ -101,6 +102,7 @@ static int dims_ok(const oracle_dims* d) {
   if (d->k0 < 0) return 0;
   if (d->k0 > 0 && (d->chunk0 < d->chunk || d->chunk0 % d->chunk)) return 0;
   if (d->key_bits != 0 && d->key_bits != 4 && d->key_bits != 8) return 0;
+  if (d->key_fp8 != 0 && (d->key_fp8 != 1 || d->key_bits == 4)) return 0;
   return 1;
 }
 
@@ -133,6 +135,54 @@ static int8_t int8_code(double x, float s) { return key_code(x, s, 127); }
 /* Largest key code: 127 for 8-bit keys, 7 for the 4-bit key format. */
 static int key_levels(const oracle_dims* d) { return d->key_bits == 4 ? 7 : 127; }
 
+/* ------------------------------------------------------------ FP8 keys */
+
+/* [KVN] "KV Cache 量化" (FP8 KV caches). E4M3: sign, 4 exponent bits (bias 7), 3 mantissa
+ * bits, no infinities, S.1111.111 is NaN, so the largest finite magnitude is
+ * 1.75 * 2^8 = 448; exponent field 0 holds the subnormals m * 2^-9. */
+static float e4m3_value(uint8_t code) {
+  const int e = (code >> 3) & 15, m = code & 7;
+  const double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+  return (float)((code & 0x80) ? -v : v);
+}
+
+/* The E4M3 code of x: round to nearest, ties to the even mantissa; magnitudes from 448 up
+ * give 448 (saturating); a zero result keeps the sign of x. */
+static uint8_t e4m3_code(float x) {
+  const uint8_t sign = signbit(x) ? 0x80 : 0;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7E; /* exponent field 15, mantissa 6 */
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal grid 2^-9; 8 steps give the smallest normal, whose code is also 8 */
+    return sign | (uint8_t)nearbyint(ldexp(a, 9));
+  }
+  int p;
+  frexp(a, &p);                              /* a = f * 2^p, f in [0.5, 1) */
+  int e = p - 1;                             /* a in [2^e, 2^(e+1)) */
+  double q = nearbyint(ldexp(a, 3 - e));     /* 8 .. 16, in steps of 2^(e-3) */
+  if (q == 16.0) {
+    q = 8.0;
+    e += 1;
+  }
+  return sign | (uint8_t)(((e + 7) << 3) | ((int)q - 8));
+}
+
+/* The key code of x / s in the key format of d (int8 codes hold the E4M3 bits as is). */
+static int8_t format_code(const oracle_dims* d, double x, float s) {
+  if (!d->key_fp8) return key_code(x, s, key_levels(d));
+  if (s == 0.0f) return 0;
+  return (int8_t)e4m3_code((float)(x / (double)s));
+}
+
+/* Ordered integer of a float score: a < b as floats exactly when key(a) < key(b); both
+ * zeros map to 0. The selection then ranks FP8 scores as it ranks integer scores. */
+static int32_t ordered_key(float f) {
+  f = f + 0.0f; /* -0 -> +0 */
+  int32_t bits;
+  memcpy(&bits, &f, sizeof bits);
+  return bits >= 0 ? bits : bits ^ 0x7FFFFFFF;
+}
+
 /* ----------------------------------------------- key scales and int8 codes */
 
 /* [HCA] quantised keys on the GPU; [KVN] "KV Cache 量化" (INT8 keys).
@@ -155,12 +205,12 @@ int oracle_quantize_keys(const oracle_dims* d, const uint16_t* k, const int32_t*
         double x = fabs(bf16_value(k[cache_index(d, page_table, b, h, t, c)]));
         if (x > amax) amax = x;
       }
-      const int levels = key_levels(d);
-      float s = (float)(amax / (double)levels);
+      const double levels = d->key_fp8 ? 448.0 : (double)key_levels(d);
+      float s = (float)(amax / levels);
       scale[((int64_t)b * d->hkv + h) * D + c] = s;
       for (int64_t t = 0; t < n; t++) {
         size_t i = cache_index(d, page_table, b, h, t, c);
-        kq[i] = key_code(bf16_value(k[i]), s, levels);
+        kq[i] = format_code(d, bf16_value(k[i]), s);
       }
       int64_t end = ((n + d->page_size - 1) / d->page_size) * d->page_size;
       for (int64_t t = n; t < end; t++) kq[cache_index(d, page_table, b, h, t, c)] = 0;
@@ -183,8 +233,8 @@ int oracle_quantize_append(const oracle_dims* d, const uint16_t* k, const int32_
       for (int64_t t = t0; t < n; t++)
         for (int c = 0; c < d->head_dim; c++) {
           size_t i = cache_index(d, page_table, b, h, t, c);
-          kq[i] = key_code(bf16_value(k[i]), scale[((int64_t)b * d->hkv + h) * d->head_dim + c],
-                           key_levels(d));
+          kq[i] = format_code(d, bf16_value(k[i]),
+                              scale[((int64_t)b * d->hkv + h) * d->head_dim + c]);
         }
   }
   return 0;
@@ -214,6 +264,16 @@ static void query_codes_one(const oracle_dims* d, const uint16_t* q, const float
     for (int c = 0; c < D; c++) qq[j * D + c] = int8_code((double)qf[j * D + c], sq);
   if (sq_out) *sq_out = sq;
   free(qf);
+}
+
+/* FP8 keys: the folded query q'_{j,c} = f32(q_{j,c} * s_c) itself, [G][D], not quantised. */
+static void query_folded(const oracle_dims* d, const uint16_t* q, const float* scale, int b,
+                         int h, float* qf) {
+  const int D = d->head_dim, G = d->hq / d->hkv;
+  const float* s = scale + ((int64_t)b * d->hkv + h) * D;
+  for (int j = 0; j < G; j++)
+    for (int c = 0; c < D; c++)
+      qf[j * D + c] = (float)(bf16_value(q[((int64_t)b * d->hq + h * G + j) * D + c]) * (double)s[c]);
 }
 
 int oracle_query_codes(const oracle_dims* d, const uint16_t* q, const float* scale, int8_t* qq,
@@ -282,6 +342,8 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
     int64_t lo = d->sink, hi = n - d->window; /* C = [lo, hi) */
     int8_t* qq = (int8_t*)malloc((size_t)G * D);
     if (qq) query_codes_one(d, q, scale, b, h, qq, NULL);
+    float* qf = d->key_fp8 ? (float*)malloc(sizeof(float) * (size_t)G * D) : NULL;
+    if (qf) query_folded(d, q, scale, b, h, qf);
     const int nrow = d->per_head ? G : 1;
     for (int rj = 0; rj < nrow; rj++) {
       /* the output row, and the query heads whose scores it ranks: [j_lo, j_hi) */
@@ -299,8 +361,9 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
       int64_t* bmax = (int64_t*)malloc(sizeof(int64_t) * (size_t)(max_blocks + 1));
       char* cvalid = (char*)calloc((size_t)n_chunk_all + 1, 1);
       char* bvalid = (char*)calloc((size_t)max_blocks + 1, 1);
-      if (!qq || !cmax || !bmax || !cvalid || !bvalid || !cmax0 || !cvalid0 || !ckept0) {
-  #pragma omp atomic write
+      if (!qq || (d->key_fp8 && !qf) || !cmax || !bmax || !cvalid || !bvalid || !cmax0 ||
+          !cvalid0 || !ckept0) {
+#pragma omp atomic write
         bad = 1;
       } else {
         /* token scores, folded straight into the chunk and block maxima */
@@ -308,8 +371,18 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
           int64_t g = INT64_MIN;
           for (int j = j_lo; j < j_hi; j++) {
             int64_t dot = 0;
-            for (int c = 0; c < D; c++)
-              dot += (int64_t)qq[j * D + c] * (int64_t)kq[cache_index(d, page_table, b, h, t, c)];
+            if (d->key_fp8) {
+              /* FP8 keys: the fp32 dot of the folded query with the E4M3 values, one fused
+               * multiply-add per channel in channel order, as an ordered integer */
+              float acc = 0.0f;
+              for (int c = 0; c < D; c++)
+                acc = fmaf(qf[j * D + c],
+                           e4m3_value((uint8_t)kq[cache_index(d, page_table, b, h, t, c)]), acc);
+              dot = ordered_key(acc);
+            } else {
+              for (int c = 0; c < D; c++)
+                dot += (int64_t)qq[j * D + c] * (int64_t)kq[cache_index(d, page_table, b, h, t, c)];
+            }
             if (dot > g) g = dot;
           }
           int64_t ci = t / d->chunk, bi = t / d->block, c0i = t / c0;
@@ -381,6 +454,7 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
       free(bvalid);
     }
     free(qq);
+    free(qf);
   }
   return bad ? 3 : 0;
 }

@@ -23,7 +23,8 @@ class _CDims(ctypes.Structure):
                                                             ("chunk0", ctypes.c_int32),
                                                             ("k0", ctypes.c_int32),
                                                             ("key_bits", ctypes.c_int32),
-                                                            ("per_head", ctypes.c_int32)]
+                                                            ("per_head", ctypes.c_int32),
+                                                            ("key_fp8", ctypes.c_int32)]
 
 
 @dataclasses.dataclass
@@ -47,11 +48,12 @@ class Dims:
     k0: int = 0
     key_bits: int = 0  # 4: 4-bit key codes (levels +-7); 0 or 8: 8-bit
     per_head: int = 0  # 1: every query head selects its own chunks and blocks
+    key_fp8: int = 0  # 1: FP8 E4M3 key codes (int8 arrays hold their bits), fp32 scores
 
     def c(self) -> _CDims:
         return _CDims(*[int(getattr(self, f[0])) for f in _CDims._fields_[:13]],
                       float(self.sm_scale), int(self.chunk0), int(self.k0),
-                      int(self.key_bits), int(self.per_head))
+                      int(self.key_bits), int(self.per_head), int(self.key_fp8))
 
     @property
     def sel_rows(self) -> int:

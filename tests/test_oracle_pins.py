@@ -564,6 +564,132 @@ def test_per_head_attention_reads_each_heads_own_row():
         assert lse_ph[0, j] == lse_s[0, j]
 
 
+# ------------------------------------------------------------------ FP8 keys
+
+def _ordered_to_float(keys):
+    """Inverse of the oracle's ordered integer of an fp32 score."""
+    k = np.asarray(keys, dtype=np.int64)
+    bits = np.where(k >= 0, k, k ^ 0x7FFFFFFF).astype(np.int64) & 0xFFFFFFFF
+    return bits.astype(np.uint32).view(np.float32)
+
+
+def test_fp8_key_codes_match_the_library_conversion():
+    """FP8 keys ("KV Cache 与长上下文推理", section "KV Cache 量化": FP8 KV caches): scale
+    f32(amax / 448), code = E4M3 of f32(k / s), rounded to nearest with ties to even. Pinned
+    against PyTorch's float8_e4m3fn conversion (every |x| here is at most 448, where the
+    two agree), and the decoded codes against the half-step bound."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    case = random_case(rng, B=2, hq=4, hkv=2, D=16, lens=(70, 45), page=16, perm=True)
+    for b in range(2):  # wide dynamic range: tiny, subnormal-range and large values
+        case["ks"][b] = to_bf16(case["ks"][b] * np.exp2(rng.integers(-12, 6, size=(2, 1, 16))))
+    kc, pt, ln = paged(case["ks"], 16, 2, None)
+    d = dims_for(dict(case, k=kc, pt=pt), 4, 2, 16)
+    d.key_fp8 = 1
+    kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, ln)
+    for b in range(2):
+        for h in range(2):
+            n = int(ln[b])
+            keys = case["ks"][b][h].astype(np.float32)                   # [n][D]
+            amax = np.abs(keys).max(axis=0)
+            s = (amax.astype(np.float64) / 448.0).astype(np.float32)
+            np.testing.assert_array_equal(sc[b, h], s)
+            x = (keys / s).astype(np.float32)                             # f32 quotient
+            assert np.abs(x).max() <= 448.0 + 1e-3
+            want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            got = logical_codes(kq, pt, ln, 16, 2)[b][h].view(np.uint8)[:n]
+            np.testing.assert_array_equal(got, want)
+            dec = torch.from_numpy(got.copy()).view(torch.float8_e4m3fn).float().numpy()
+            # half a step of the E4M3 grid: 2^-4 relative for normals, 2^-10 absolute below
+            bound = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10)
+            assert np.all(np.abs(dec - x) <= bound)
+
+
+def test_fp8_worked_examples_and_saturating_append():
+    """Hand-worked E4M3 codes with s = 1 (amax 448): 1.0625 ties to 1.0 (even mantissa),
+    1.1875 ties to 1.25, 3 x 2^-10 ties to 2^-8 and 2^-10 to 0 on the subnormal grid, -0 keeps
+    its sign; an appended key beyond the stored range saturates at +-448."""
+    d = Dims(batch=1, hq=1, hkv=1, head_dim=4, page_size=16, max_pages_per_seq=1,
+             num_pages=1, chunk=16, block=16, k1=1, k2=1, sink=0, window=0, key_fp8=1)
+    k = np.zeros((1, 1, 16, 4), np.float32)
+    k[0, 0, :8, 0] = [448.0, 1.0625, 1.1875, 3 * 2.0 ** -10, 2.0 ** -10, -1.0625, -0.0, 7.5]
+    pt, ln = np.zeros((1, 1), np.int32), np.array([8], np.int32)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(k), pt, ln)
+    assert sc[0, 0, 0] == 1.0 and sc[0, 0, 1] == 0.0
+    # codes: sign | exponent field << 3 | mantissa
+    assert kq[0, 0, :8, 0].view(np.uint8).tolist() == [0x7E, 0x38, 0x3A, 0x02, 0x00, 0xB8, 0x80,
+                                                      0x4F]
+    assert (kq[0, 0, :8, 1:] == 0).all() and (kq[0, 0, 8:] == 0).all()
+    k[0, 0, 8, 0] = 1000.0
+    k[0, 0, 8, 1] = -600.0
+    ln2 = np.array([9], np.int32)
+    kq2 = oracle.quantize_append(d, bf16_bits(k), pt, ln2, -1, sc, kq)
+    assert kq2[0, 0, 8, 0].view(np.uint8) == 0x7E  # +448
+    assert kq2[0, 0, 8, 1] == 0  # channel 1 has scale 0: code 0
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_fp8_scores_exact_on_representable_inputs(seed):
+    """Keys that are E4M3 integers times s = 1/8 and queries that are small integers make
+    every product and partial sum exact in fp32, so the fp32 scores must equal the exact
+    rational dot products: block maxima (max over the group, candidate tokens only) checked
+    against exact arithmetic, and both modules against their defining property."""
+    rng = np.random.default_rng(700 + seed)
+    D, hkv, G = 16, 2, 2
+    grid = np.array([v for v in range(1, 449) if v <= 16 or (v <= 32 and v % 2 == 0) or
+                     (v <= 64 and v % 4 == 0) or (v <= 128 and v % 8 == 0) or
+                     (v <= 256 and v % 16 == 0) or v % 32 == 0 and v <= 448], dtype=np.float64)
+    lens = tuple(int(x) for x in rng.integers(100, 500, size=2))
+    ks = []
+    for n in lens:
+        x = rng.choice(grid[grid <= 64], size=(hkv, n, D)) * rng.choice([-1, 1], size=(hkv, n, D))
+        x[:, rng.integers(0, n), :] = 448.0  # amax 448 in every channel: s = 448/8/448 = 1/8
+        ks.append((x / 8.0).astype(np.float32))
+    kc, pt, ln = paged(ks, 16, hkv, None)
+    qint = rng.integers(-8, 9, size=(2, hkv * G, D))
+    case = dict(k=kc, pt=pt, lens=ln, page=16)
+    k1, k2 = int(rng.integers(1, 8)), int(rng.integers(1, 10))
+    sink, window = int(rng.integers(0, 30)), int(rng.integers(0, 50))
+    d = dims_for(case, hkv * G, hkv, D, chunk=32, block=16, k1=k1, k2=k2, sink=sink,
+                 window=window)
+    d.key_fp8 = 1
+    q = qint.astype(np.float32)
+    kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, ln)
+    assert np.all(sc == np.float32(1.0 / 8.0))
+    sel = oracle.select(d, bf16_bits(q), sc, kq, pt, ln, want_block_max=True)
+    for b in range(2):
+        n = int(ln[b])
+        for h in range(hkv):
+            keys8 = (ks[b][h].astype(np.float64) * 8).astype(np.int64)  # exact E4M3 values
+            bm = {}
+            for t in range(sink, n - window):
+                # q' = q / 8 exactly, key value = keys8: score = sum(q * keys8) / 8
+                g = max(int(np.dot(qint[b, h * G + j], keys8[t])) for j in range(G))
+                bm[t // 16] = max(bm.get(t // 16, g), g)
+            got = _ordered_to_float(sel["block_max"][b, h])
+            for kk in range(got.size):
+                if kk in bm:
+                    assert got[kk] == bm[kk] / 8.0
+                else:
+                    assert sel["block_max"][b, h, kk] == INT32_MIN
+            cm = {}
+            for kk, s_ in bm.items():
+                cm[kk // 2] = max(cm.get(kk // 2, s_), s_)
+            kept_c = [c for c in sel["chunk_idx"][b, h] if c >= 0]
+            assert len(kept_c) == min(k1, len(cm))
+            for c in kept_c:
+                for c2 in cm:
+                    if c2 not in kept_c:
+                        assert _beats(cm[c], c, cm[c2], c2)
+            cand = [kk for kk in bm if kk // 2 in kept_c]
+            kept_b = [kk for kk in sel["block_idx"][b, h] if kk >= 0]
+            assert len(kept_b) == min(k2, len(cand))
+            for kk in kept_b:
+                for k_ in cand:
+                    if k_ not in kept_b:
+                        assert _beats(bm[kk], kk, bm[k_], k_)
+
+
 def test_candidate_region_masks_sink_and_window_tokens():
     """A huge key in the sink part of a block that straddles the sink boundary, and one in
     the window, must not lift any block score."""
