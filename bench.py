@@ -188,7 +188,8 @@ class Case:
                           max_pages_per_seq=wl["max_pages"], num_pages=wl["num_pages"],
                           chunk=cfg.chunk, k1=cfg.k1, k2=cfg.k2, sink=cfg.sink,
                           window=cfg.window, kv_on_host=cfg.kv_on_host, chunk0=cfg.chunk0,
-                          k0=cfg.k0, key_bits=cfg.key_bits, per_head=cfg.per_head)
+                          k0=cfg.k0, key_bits=cfg.key_bits, per_head=cfg.per_head,
+                          key_fp8=cfg.key_fp8)
         d = self.d
         R = cfg.hq if cfg.per_head else cfg.hkv  # selection rows per sequence
         B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
@@ -554,7 +555,7 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
                      max_pages_per_seq=wl["max_pages"], num_pages=wl["num_pages"],
                      chunk=cfg.chunk, block=16, k1=cfg.k1, k2=cfg.k2, sink=cfg.sink,
                      window=cfg.window, chunk0=cfg.chunk0, k0=cfg.k0, key_bits=cfg.key_bits,
-                     per_head=cfg.per_head)
+                     per_head=cfg.per_head, key_fp8=cfg.key_fp8)
     q, k, v = (W.to_numpy_bits(wl[x]) for x in ("q", "k_cache", "v_cache"))
     pt, lens = wl["page_table"].numpy(), wl["seq_lens"].numpy()
     kq, sc = oracle.quantize_keys(od, k, pt, lens)             # cache state, not per step
@@ -643,7 +644,7 @@ def workload_text(cfg):
     return (f"{cfg.name}: batch {cfg.batch}, Hq {cfg.hq}, Hkv {cfg.hkv}, d 128, context "
             f"{cfg.context}, {mod0}chunk {cfg.chunk} keep K1 {cfg.k1}, block 16 keep K2 "
             f"{cfg.k2}, sink {cfg.sink}, window {cfg.window}; bf16 K/V in 16-token pages, "
-            f"int{cfg.key_bits} per-channel keys"
+            + ("FP8 E4M3" if cfg.key_fp8 else f"int{cfg.key_bits}") + " per-channel keys"
             + ("; per-head selection" if cfg.per_head else ""))
 
 
@@ -702,7 +703,7 @@ def main():
         for name, dense in (("paged-b8-32k-128k", True), ("llama3-8b-3m-offload", False),
                             ("llama3-8b-1m-3mod", True), ("llama3-8b-128k-int4", True),
                             ("llama3-8b-1m-int4", True), ("llama3-70b-128k", True),
-                            ("llama3-8b-128k-perhead", True)):
+                            ("llama3-8b-128k-perhead", True), ("llama3-8b-128k-fp8", True)):
             r = gpu_case_numbers(name, rank, device, min(args.steps, 500), args.warmup, None,
                                  peak, world, dense=dense)
             del r["case"]

@@ -107,6 +107,15 @@ typedef struct hsa_dims {
                                 [batch][hq][..], chunk_idx / block_idx [batch][hq][k1 / k2],
                                 n_chunks / n_blocks [batch][hq]; the attention of query head
                                 j then reads row j. Not with the block cache (UNSUPPORTED). */
+  int32_t key_fp8;           /* 0: integer key codes (key_bits); 1: FP8 E4M3 key codes, in the
+                                8-bit layout (kq [num_pages][hkv][16][128] bytes; key_bits 0 or
+                                8, else UNSUPPORTED): s = f32(amax / 448), code = E4M3 of
+                                f32(k / s) rounded to nearest even, saturating at +-448; the
+                                query is folded (q' = f32(q * s)) but not quantised and a
+                                token's score is the fp32 fused multiply-add chain over the
+                                channels in order; block_max / tile_max then hold the scores'
+                                order-preserving integer images (bits, negative ones with the
+                                magnitude bits flipped) */
 } hsa_dims;
 
 /* Operation ids for hsa_workspace_bytes. */

@@ -52,6 +52,8 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   if (!(d->sm_scale == d->sm_scale)) return HSA_ERR_INVALID_ARG;  // NaN
   if (d->key_bits != 0 && d->key_bits != 4 && d->key_bits != 8) return HSA_ERR_UNSUPPORTED;
   if (d->per_head != 0 && d->per_head != 1) return HSA_ERR_INVALID_ARG;
+  if (d->key_fp8 != 0 && d->key_fp8 != 1) return HSA_ERR_INVALID_ARG;
+  if (d->key_fp8 && d->key_bits == 4) return HSA_ERR_UNSUPPORTED;
   s.batch = d->batch;
   s.hq = d->hq;
   s.hkv = d->hkv;
@@ -67,6 +69,7 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   s.k0 = d->k0;
   s.key_bits = d->key_bits == 4 ? 4 : 8;
   s.per_head = d->per_head;
+  s.key_fp8 = d->key_fp8;
   s.kv_div = 1;
   s.sm_scale = d->sm_scale > 0.0f ? d->sm_scale : 1.0f / std::sqrt((float)hsa::kHeadDim);
   return HSA_OK;

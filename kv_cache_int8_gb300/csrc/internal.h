@@ -15,6 +15,7 @@ struct Shape {
   int chunk0, k0;  // module 0 (k0 > 0): coarse chunks of chunk0 tokens, top k0
   int key_bits;    // 8: 8-bit key codes [page][hkv][16][128]; 4: 4-bit, [page][hkv][16][64] bytes
   int per_head;    // 1: every query head selects its own blocks (rows = hq, not hkv)
+  int key_fp8;     // 1: FP8 E4M3 key codes (8-bit layout), fp32 scores
   int kv_div = 1;  // attention rows per kv head (hq / hkv for a per-head attention launch)
   float sm_scale;  // resolved (> 0)
   // rows of the selection (block and tile maxima, kept chunks and blocks) per sequence

@@ -57,6 +57,42 @@ __device__ __forceinline__ void store_codes(int8_t* kq, size_t off, const int c[
     *reinterpret_cast<uint2*>(kq + off) = pack_codes(c);
 }
 
+// Key formats: the integer code widths 8 and 4, and FP8 E4M3 codes (8-bit layout).
+constexpr int kFmtFp8 = 0xF8;
+
+// Divisor of amax giving the key scale: the largest code magnitude of the format.
+__device__ __forceinline__ float scale_divisor(int fmt) {
+  return fmt == kFmtFp8 ? 448.0f : (float)key_levels(fmt);
+}
+
+// E4M3 codes of four f32 values (byte i of the result <- x[i]): round to nearest even,
+// saturating at +-448.
+__device__ __forceinline__ uint32_t e4m3x4(const float x[4]) {
+  unsigned short lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x[1]), "f"(x[0]));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x[3]), "f"(x[2]));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// The codes of the 8 values f (channel scales s) at element offset `off`, in format fmt:
+// integer codes clamp(rint_even(f32(f / s)), +-levels), or E4M3 codes of f32(f / s); a zero
+// scale gives code 0.
+__device__ __forceinline__ void store_key_codes(int8_t* kq, size_t off, const float f[8],
+                                                const float s[8], int fmt) {
+  if (fmt == kFmtFp8) {
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) x[i] = s[i] == 0.0f ? 0.0f : __fdiv_rn(f[i], s[i]);
+    *reinterpret_cast<uint2*>(kq + off) = make_uint2(e4m3x4(x), e4m3x4(x + 4));
+    return;
+  }
+  const int levels = key_levels(fmt);
+  int c[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) c[i] = key_code(f[i], s[i], levels);
+  store_codes(kq, off, c, fmt);
+}
+
 // Pass 1 of full quantisation: amax per (b, h, channel) over tokens t < N_b, as the bit
 // pattern of a non-negative float (ordered like the value), merged with atomicMax.
 __global__ void __launch_bounds__(kThreads) key_amax_kernel(
@@ -111,7 +147,6 @@ __global__ void __launch_bounds__(kThreads) key_codes_kernel(
     int full, int8_t* __restrict__ kq, int hkv, int max_pages, int num_pages, int* err,
     int bits) {
   const int b = blockIdx.z, h = blockIdx.y;
-  const int levels = key_levels(bits);
   const int slot = threadIdx.x >> 4, grp = threadIdx.x & 15;
   const int n = seq_lens[b];
   if (!seq_ok(n, max_pages)) {
@@ -122,7 +157,7 @@ __global__ void __launch_bounds__(kThreads) key_codes_kernel(
   float s[8];
 #pragma unroll
   for (int i = 0; i < 8; i++)
-    s[i] = full ? __fdiv_rn(__uint_as_float(amax_bits[sbase + i]), (float)levels)
+    s[i] = full ? __fdiv_rn(__uint_as_float(amax_bits[sbase + i]), scale_divisor(bits))
                 : k_scale_in[sbase + i];
   if (full && blockIdx.x == 0 && slot == 0) {
 #pragma unroll
@@ -143,18 +178,14 @@ __global__ void __launch_bounds__(kThreads) key_codes_kernel(
       continue;
     }
     const size_t off = (((size_t)page * hkv + h) * kPage + slot) * kHeadDim + grp * 8;
-    int c[8];
     if (t < n) {
       float f[8];
       unpack8(ldg128_nc(k_cache + off), f);
-#pragma unroll
-      for (int i = 0; i < 8; i++) c[i] = key_code(f[i], s[i], levels);
-    } else {
-      if (!full) continue;
-#pragma unroll
-      for (int i = 0; i < 8; i++) c[i] = 0;
+      store_key_codes(kq, off, f, s, bits);
+    } else if (full) {
+      const int c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      store_codes(kq, off, c, bits == kFmtFp8 ? 8 : bits);
     }
-    store_codes(kq, off, c, bits);
   }
 }
 
@@ -213,11 +244,11 @@ __device__ __forceinline__ void append_body(const uint4* __restrict__ k_new,
   float f[8];
   unpack8(kv, f);
   const float* s = k_scale + ((size_t)b * hkv + h) * kHeadDim + grp * 8;
-  int c[8];
-#pragma unroll
-  for (int i = 0; i < 8; i++) c[i] = key_code(f[i], s[i], key_levels(bits));
-  store_codes(kq, off, c, bits);
+  store_key_codes(kq, off, f, s, bits);
 }
+
+// The kernels' key-format code of a shape.
+int key_format(const Shape& s) { return s.key_fp8 ? kFmtFp8 : s.key_bits; }
 
 }  // namespace
 
@@ -242,7 +273,7 @@ cudaError_t launch_key_codes(const Shape& s, const void* k_cache, const int32_t*
   key_codes_kernel<<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(k_cache),
                                               page_table, seq_lens, amax_bits, k_scale_in,
                                               k_scale_out, append_from, full ? 1 : 0, kq, s.hkv,
-                                              s.max_pages, s.num_pages, err, s.key_bits);
+                                              s.max_pages, s.num_pages, err, key_format(s));
   return cudaGetLastError();
 }
 
@@ -300,7 +331,7 @@ cudaError_t launch_append_kv(const Shape& s, const void* k_new, const void* v_ne
                        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
                        static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache),
                        kq, k_scale, page_table, seq_lens, s.hkv, s.max_pages, s.num_pages, err,
-                       beside ? 1 : 0, s.key_bits);
+                       beside ? 1 : 0, key_format(s));
 }
 
 }  // namespace hsa

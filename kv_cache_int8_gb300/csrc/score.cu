@@ -19,6 +19,9 @@
 // G = 8 read them from a per-warp shared-memory copy, which leaves room for more warps.
 #include <algorithm>
 #include <climits>
+#include <type_traits>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -58,14 +61,22 @@ constexpr int kTileBlocks = 4;                  // blocks per ring slot (64 toke
 constexpr int kTileTokens = kTileBlocks * kPage;
 constexpr int kMaxBatch = 1024;                 // sequences (the tile prefix sums in shared memory)
 
-// Launch shape and shared-memory layout of one scorer instance (PH: per-head maxima, whose
-// epilogue needs the registers the query words would take).
-template <int G, bool KB4, bool PH>
+// Key formats of the scorer instances.
+constexpr int kKeyInt8 = 0;  // 8-bit integer codes
+constexpr int kKeyInt4 = 1;  // 4-bit integer codes, two per byte
+constexpr int kKeyFp8 = 2;   // FP8 E4M3 codes: fp32 scores
+
+// Launch shape and shared-memory layout of one scorer instance (KF: key format; PH:
+// per-head maxima, whose epilogue needs the registers the query words would take).
+template <int G, int KF, bool PH>
 struct ScoreCfg {
-  static constexpr bool kQSmem = KB4 || G > 4 || PH;  // query words in shared memory
+  static constexpr bool KB4 = KF == kKeyInt4;
+  static constexpr bool kQSmem = KF != kKeyInt8 || G > 4 || PH;  // query in shared memory
   static constexpr int kWarps = KB4 ? HSA_SCORE_QS_WARPS : (kQSmem ? 4 : HSA_SCORE_WARPS);
   static constexpr int kThreads = (kWarps + 1) * 32;
-  static constexpr int kCtasPerSm = KB4 ? HSA_SCORE_QS_CTAS : (kQSmem ? 3 : HSA_SCORE_CTAS);
+  // FP8 with 8 heads: the fp32 query of 4 warps takes 16 KiB, so 2 CTAs fit per SM
+  static constexpr int kCtasPerSm =
+      KB4 ? HSA_SCORE_QS_CTAS : (KF == kKeyFp8 && G > 4 ? 2 : (kQSmem ? 3 : HSA_SCORE_CTAS));
   // 8-bit codes: one 128-byte row per token; 4-bit codes: two tokens per row
   static constexpr int kRowsPerBlock = KB4 ? kPage / 2 : kPage;
   static constexpr int kBlockBytes = kRowsPerBlock * kHeadDim;
@@ -75,7 +86,9 @@ struct ScoreCfg {
   static constexpr int kStages = kRingBytes / kSlotBytes;
   static_assert(kStages % kWarps == 0 && kStages / kWarps >= 2,
                 "every consumer warp owns at least two fixed ring slots");
-  static constexpr int kQWords = kQSmem ? kWarps * G * 32 : 0;
+  // words of a warp's query copy: G x 32 code words, or G x 128 fp32 values (FP8 keys)
+  static constexpr int kQWarpWords = KF == kKeyFp8 ? G * kHeadDim : G * 32;
+  static constexpr int kQWords = kQSmem ? kWarps * kQWarpWords : 0;
   static size_t smem_bytes(int batch) {
     return 1024 + kRingBytes + 2 * kStages * sizeof(uint64_t) + kQWords * sizeof(int) +
            (batch + 1) * sizeof(int);
@@ -183,6 +196,42 @@ __device__ __forceinline__ void store_query_codes(int* qs, const ScoreArgs& a, i
   }
 }
 
+// FP8 keys: the warp's shared-memory copy of the folded query itself, qs[G][128] fp32,
+// q'_{j,c} = f32(q_{j,c} * s_c) (lane l computes channels [4l, 4l+4) of each head).
+template <int G>
+__device__ __forceinline__ void store_query_folded(float* qs, const ScoreArgs& a, int b, int h,
+                                                   int lane) {
+  const float4 s4 =
+      *reinterpret_cast<const float4*>(a.k_scale + ((size_t)b * a.hkv + h) * kHeadDim + 4 * lane);
+#pragma unroll
+  for (int j = 0; j < G; j++) {
+    const uint2 w = *reinterpret_cast<const uint2*>(
+        a.q + ((size_t)b * a.hkv * G + (size_t)h * G + j) * kHeadDim + 4 * lane);
+    *reinterpret_cast<float4*>(qs + j * kHeadDim + 4 * lane) =
+        make_float4(__fmul_rn(bf16_lo(w.x), s4.x), __fmul_rn(bf16_hi(w.x), s4.y),
+                    __fmul_rn(bf16_lo(w.y), s4.z), __fmul_rn(bf16_hi(w.y), s4.w));
+  }
+}
+
+// The exact values of four E4M3 codes (byte i of w -> f[i]), through f16 (exact: every
+// E4M3 value is an f16 value).
+__device__ __forceinline__ void e4m3x4_to_float(uint32_t w, float* f) {
+  uint32_t h01, h23;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((unsigned short)(w & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((unsigned short)(w >> 16)));
+  f[0] = __half2float(__ushort_as_half((unsigned short)(h01 & 0xFFFFu)));
+  f[1] = __half2float(__ushort_as_half((unsigned short)(h01 >> 16)));
+  f[2] = __half2float(__ushort_as_half((unsigned short)(h23 & 0xFFFFu)));
+  f[3] = __half2float(__ushort_as_half((unsigned short)(h23 >> 16)));
+}
+
+// Order-preserving integer of an fp32 score (both zeros map to 0): the block and tile maxima
+// of FP8 scores are then taken, written and ranked as integers.
+__device__ __forceinline__ int ordered_key(float f) {
+  const int bits = __float_as_int(f + 0.0f);  // -0 -> +0
+  return bits >= 0 ? bits : bits ^ 0x7FFFFFFF;
+}
+
 // 4-bit codes: a 32-bit word holds 8 channels as two's-complement nibbles. Moved into the
 // high half of their bytes (the even channels shifted up by 4, the odd ones masked in place),
 // the nibbles read as signed bytes equal to 16 x code, so two signed dp4a per word give 16 x
@@ -197,11 +246,12 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
 
 // PH: per-head selection, the maxima of every query head (rows b * hq + h * G + j) rather
 // than of the group's token scores.
-template <int G, bool KB4, bool PH>
-__global__ void __launch_bounds__(ScoreCfg<G, KB4, PH>::kThreads, ScoreCfg<G, KB4, PH>::kCtasPerSm)
+template <int G, int KF, bool PH>
+__global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF, PH>::kCtasPerSm)
     score_blocks_kernel(const __grid_constant__ CUtensorMap kq_map,
                         const __grid_constant__ CUtensorMap kq_map4, const ScoreArgs a) {
-  using C = ScoreCfg<G, KB4, PH>;
+  using C = ScoreCfg<G, KF, PH>;
+  constexpr bool KB4 = C::KB4;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -352,7 +402,7 @@ __global__ void __launch_bounds__(ScoreCfg<G, KB4, PH>::kThreads, ScoreCfg<G, KB
 
   // -------------------------------------------------------------- consumers
   int qq[C::kQSmem ? 1 : G][32];  // register copy of the query words (8-bit codes, G <= 4)
-  int* qs = qbuf + (C::kQSmem ? warp * G * 32 : 0);
+  int* qs = qbuf + (C::kQSmem ? warp * C::kQWarpWords : 0);
   const uint32_t qs_addr = smem_addr(qs);
   int cur_b = -1, cur_h = -1;
   SeqRange sr = seq_range(a, b);
@@ -368,7 +418,10 @@ __global__ void __launch_bounds__(ScoreCfg<G, KB4, PH>::kThreads, ScoreCfg<G, KB
     if (b != cur_b || h != cur_h) {
       if constexpr (C::kQSmem) {
         __syncwarp();  // every lane is done reading the previous words
-        store_query_codes<G, KB4>(qs, a, b, h, lane);
+        if constexpr (KF == kKeyFp8)
+          store_query_folded<G>(reinterpret_cast<float*>(qs), a, b, h, lane);
+        else
+          store_query_codes<G, KB4>(qs, a, b, h, lane);
         __syncwarp();
       } else {
         load_query_codes<G>(qq, a, b, h, lane);
@@ -422,6 +475,43 @@ __global__ void __launch_bounds__(ScoreCfg<G, KB4, PH>::kThreads, ScoreCfg<G, KB
       for (int half = 0; half < 2; half++)
 #pragma unroll
         for (int jj = 0; jj < G; jj++) acc[half][jj] >>= 4;
+    } else if constexpr (KF == kKeyFp8) {
+      // fp32 scores: one fused multiply-add per channel, in channel order, of the folded
+      // query with the exact values of the E4M3 codes; then their order-preserving integers
+      float facc[2][G];
+#pragma unroll
+      for (int half = 0; half < 2; half++)
+#pragma unroll
+        for (int jj = 0; jj < G; jj++) facc[half][jj] = 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < 8; c++) {  // channels 16c .. 16c + 15
+        float x[2][16];
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+          const uint4 kv =
+              lds128(sbase + (half * 32 + lane) * kHeadDim + ((c ^ (lane & 7)) << 4));
+#pragma unroll
+          for (int m = 0; m < 4; m++) e4m3x4_to_float(word_of(kv, m), &x[half][4 * m]);
+        }
+#pragma unroll
+        for (int jj = 0; jj < G; jj++) {
+#pragma unroll
+          for (int i4 = 0; i4 < 4; i4++) {
+            const uint4 q4 = lds128(qs_addr + (jj * kHeadDim + 16 * c + 4 * i4) * 4);
+            const float qv[4] = {__uint_as_float(q4.x), __uint_as_float(q4.y),
+                                 __uint_as_float(q4.z), __uint_as_float(q4.w)};
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+              for (int half = 0; half < 2; half++)
+                facc[half][jj] = __fmaf_rn(qv[i], x[half][4 * i4 + i], facc[half][jj]);
+          }
+        }
+      }
+#pragma unroll
+      for (int half = 0; half < 2; half++)
+#pragma unroll
+        for (int jj = 0; jj < G; jj++) acc[half][jj] = ordered_key(facc[half][jj]);
     } else {
 #pragma unroll
       for (int c = 0; c < 8; c++) {
@@ -516,16 +606,23 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
     return launch_kernel(kernel, dim3(grid), dim3(C::kThreads), smem, st, true, kq_map, kq_map4,
                          a);
   };
-#define HSA_SCORE_CASE(g)                                                               \
-  case g:                                                                               \
-    if (s.per_head)                                                                     \
-      e = s.key_bits == 4                                                               \
-              ? go(score_blocks_kernel<g, true, true>, ScoreCfg<g, true, true>{})       \
-              : go(score_blocks_kernel<g, false, true>, ScoreCfg<g, false, true>{});    \
-    else                                                                                \
-      e = s.key_bits == 4                                                               \
-              ? go(score_blocks_kernel<g, true, false>, ScoreCfg<g, true, false>{})     \
-              : go(score_blocks_kernel<g, false, false>, ScoreCfg<g, false, false>{});  \
+  const int kf = s.key_fp8 ? kKeyFp8 : (s.key_bits == 4 ? kKeyInt4 : kKeyInt8);
+  auto go_kf = [&](auto g_, auto ph_) {
+    constexpr int g = decltype(g_)::value;
+    constexpr bool ph = decltype(ph_)::value;
+    switch (kf) {
+      case kKeyInt4:
+        return go(score_blocks_kernel<g, kKeyInt4, ph>, ScoreCfg<g, kKeyInt4, ph>{});
+      case kKeyFp8:
+        return go(score_blocks_kernel<g, kKeyFp8, ph>, ScoreCfg<g, kKeyFp8, ph>{});
+      default:
+        return go(score_blocks_kernel<g, kKeyInt8, ph>, ScoreCfg<g, kKeyInt8, ph>{});
+    }
+  };
+#define HSA_SCORE_CASE(g)                                                    \
+  case g:                                                                    \
+    e = s.per_head ? go_kf(std::integral_constant<int, g>{}, std::true_type{}) \
+                   : go_kf(std::integral_constant<int, g>{}, std::false_type{}); \
     break;
   cudaError_t e;
   switch (s.group) {

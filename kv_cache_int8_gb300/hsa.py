@@ -53,7 +53,7 @@ class hsa_dims(ctypes.Structure):
         "chunk", "block", "k1", "k2", "sink", "window")] + [
         ("sm_scale", ctypes.c_float), ("kv_on_host", ctypes.c_int32),
         ("chunk0", ctypes.c_int32), ("k0", ctypes.c_int32), ("key_bits", ctypes.c_int32),
-        ("per_head", ctypes.c_int32)]
+        ("per_head", ctypes.c_int32), ("key_fp8", ctypes.c_int32)]
 
 
 class hsa_step_io(ctypes.Structure):
@@ -86,13 +86,15 @@ class Dims:
     k0: int = 0
     key_bits: int = 0  # 4: 4-bit key codes, two per byte; 0 or 8: 8-bit
     per_head: int = 0  # 1: every query head selects its own blocks (rows = hq)
+    key_fp8: int = 0  # 1: FP8 E4M3 key codes (8-bit layout), fp32 scores
 
     def c(self) -> hsa_dims:
         """The C struct, built once per set of field values (every call of a step passes it)."""
         key = (self.batch, self.hq, self.hkv, self.head_dim, self.page_size,
                self.max_pages_per_seq, self.num_pages, self.chunk, self.block, self.k1,
                self.k2, self.sink, self.window, float(self.sm_scale),
-               1 if self.kv_on_host else 0, self.chunk0, self.k0, self.key_bits, self.per_head)
+               1 if self.kv_on_host else 0, self.chunk0, self.k0, self.key_bits, self.per_head,
+               self.key_fp8)
         c = _DIMS_CACHE.get(key)
         if c is None:
             if len(_DIMS_CACHE) > 256:

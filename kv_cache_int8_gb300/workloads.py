@@ -53,6 +53,7 @@ class Config:
     k0: int = 0
     key_bits: int = 8  # key codes: 8-bit, or 4-bit (two per byte)
     per_head: int = 0  # 1: every query head selects its own blocks
+    key_fp8: int = 0  # 1: FP8 E4M3 key codes
 
 
 CONFIGS: Dict[str, Config] = {
@@ -82,6 +83,9 @@ CONFIGS: Dict[str, Config] = {
     # the 128K step with per-head selection (every query head keeps its own 128 blocks)
     "llama3-8b-128k-perhead": Config("llama3-8b-128k-perhead", 1, 32, 8, 131072, None,
                                      k1=256, k2=128, sink=128, window=1024, per_head=1),
+    # the 128K step with FP8 E4M3 key codes (fp32 scores)
+    "llama3-8b-128k-fp8": Config("llama3-8b-128k-fp8", 1, 32, 8, 131072, None,
+                                 k1=256, k2=128, sink=128, window=1024, key_fp8=1),
     # the 128K and 1M steps with 4-bit key codes (half the bytes the scorer reads)
     "llama3-8b-128k-int4": Config("llama3-8b-128k-int4", 1, 32, 8, 131072, None,
                                   k1=256, k2=128, sink=128, window=1024, key_bits=4),

@@ -21,19 +21,21 @@ def dims_pair(wl: dict, **over):
     window, chunk, chunk0, k0, key_bits, per_head."""
     cfg = wl["config"]
     p = dict(k1=cfg.k1, k2=cfg.k2, sink=cfg.sink, window=cfg.window, chunk=cfg.chunk,
-             chunk0=cfg.chunk0, k0=cfg.k0, key_bits=cfg.key_bits, per_head=0)
+             chunk0=cfg.chunk0, k0=cfg.k0, key_bits=cfg.key_bits, per_head=0,
+             key_fp8=cfg.key_fp8)
     p.update(over)
     hd = hsa.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, max_pages_per_seq=wl["max_pages"],
                   num_pages=wl["num_pages"], chunk=p["chunk"], k1=p["k1"], k2=p["k2"],
                   sink=p["sink"], window=p["window"],
                   kv_on_host=wl["k_cache"].device.type == "cpu" and wl["k_cache"].is_pinned(),
                   chunk0=p["chunk0"], k0=p["k0"], key_bits=p["key_bits"],
-                  per_head=p["per_head"])
+                  per_head=p["per_head"], key_fp8=p["key_fp8"])
     od = oracle.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, head_dim=W.HEAD_DIM,
                      page_size=W.PAGE, max_pages_per_seq=wl["max_pages"],
                      num_pages=wl["num_pages"], chunk=p["chunk"], block=16, k1=p["k1"],
                      k2=p["k2"], sink=p["sink"], window=p["window"], chunk0=p["chunk0"],
-                     k0=p["k0"], key_bits=p["key_bits"], per_head=p["per_head"])
+                     k0=p["k0"], key_bits=p["key_bits"], per_head=p["per_head"],
+                     key_fp8=p["key_fp8"])
     return hd, od
 
 

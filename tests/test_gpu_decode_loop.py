@@ -72,14 +72,15 @@ def test_prepared_decode_step_equals_the_plain_call():
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("refresh,on_host,key_bits,per_head", [(3, False, 8, 0), (2, True, 8, 0),
-                                                                (1, False, 8, 0), (2, False, 4, 0),
-                                                                (2, False, 8, 1)])
-def test_decode_loop_with_selection_reuse(refresh, on_host, key_bits, per_head):
+@pytest.mark.parametrize("refresh,on_host,key_bits,per_head,fp8", [
+    (3, False, 8, 0, 0), (2, True, 8, 0, 0), (1, False, 8, 0, 0), (2, False, 4, 0, 0),
+    (2, False, 8, 1, 0), (2, False, 8, 0, 1)])
+def test_decode_loop_with_selection_reuse(refresh, on_host, key_bits, per_head, fp8):
     steps = 6
     cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None,
                               context_range=(3000, 6000), batch=2, hq=8, hkv=2, k1=12, k2=10,
-                              sink=32, window=96, paged_permuted=True, key_bits=key_bits)
+                              sink=32, window=96, paged_permuted=True, key_bits=key_bits,
+                              key_fp8=fp8)
     wl = W.make_workload(cfg, seed=77 + refresh, host_pinned=on_host)
     hd, od = H.dims_pair(wl, per_head=per_head)
     dwl = H.to_cuda(wl)

@@ -102,6 +102,17 @@ def test_per_head_selection(hq, hkv, key_bits, chunk):
                    for b in range(2))
 
 
+@pytest.mark.parametrize("hq,hkv,per_head", [(8, 2, 0), (16, 2, 0), (4, 1, 0), (8, 2, 1)])
+def test_fp8_keys(hq, hkv, per_head):
+    """FP8 E4M3 key codes: scales amax / 448, codes, fp32 block maxima (as ordered
+    integers) and selections bit-exact against the oracle; outputs within tolerance."""
+    wl = W.make_workload(_cfg(context=None, context_range=(900, 7000), batch=2, hq=hq, hkv=hkv,
+                              paged_permuted=True, key_fp8=1), seed=80 + hq + per_head)
+    g, o = _check(wl, per_head=per_head, k1=12, k2=10, sink=24, window=150)
+    codes = g["kq"].view(np.uint8)
+    assert (codes & 0x7F).max() == 0x7E  # the channel maxima code as +-448
+
+
 def test_unaligned_sink_and_window():
     wl = W.make_workload(_cfg(context=7777, batch=3, hq=8, hkv=2), seed=21)
     _check(wl, k1=11, k2=19, sink=37, window=101)

@@ -74,6 +74,11 @@ def test_llama3_8b_128k_per_head_selection_sampled_heads():
     _run(wl, bh_pairs=[(0, 1), (0, 6)], per_head=1)
 
 
+def test_llama3_8b_128k_fp8_keys_full():
+    wl = W.make_workload(W.CONFIGS["llama3-8b-128k-fp8"], seed=0, device="cuda")
+    _run(wl)
+
+
 def test_tiny_8k_four_bit_keys():
     """4-bit key codes: codes (unpacked from their nibbles), scales amax / 7, block maxima
     and selections bit-exact against the oracle's 4-bit format; outputs within tolerance."""
