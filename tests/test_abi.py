@@ -83,6 +83,10 @@ def test_workspace_sizes(lib):
     sel_ph = lib.hsa_workspace_bytes(_dims(lib, per_head=1), lib.HSA_OP_SELECT)
     assert sel_ph >= 4 * (sel - 256)
     assert lib.hsa_workspace_bytes(_dims(lib, per_head=2), 0) == 0
+    # FP8 keys: 8-bit layout only
+    assert lib.hsa_workspace_bytes(_dims(lib, key_fp8=1), 0) > 0
+    assert lib.hsa_workspace_bytes(_dims(lib, key_fp8=1, key_bits=4), 0) == 0
+    assert lib.hsa_workspace_bytes(_dims(lib, key_fp8=2), 0) == 0
     # the block cache plan works per kv head: no cache with per-head selection
     host = dict(kv_on_host=True, k2=16, sink=64, window=256)
     assert lib.load().hsa_block_cache_bytes(_dims(lib, **host).c(), 4096) > 0
