@@ -3,10 +3,10 @@
 // Sources: "HCAttention: Extreme KV cache compression via heterogeneous attention computing
 // for LLMs", abstract and contribution list (global approximate attention scoring over the
 // GPU-resident quantised keys); "KV Cache 与长上下文推理", section "MQA 与 GQA" (G query heads
-// share one kv head) and section "KV Cache 量化" (INT8 and INT4 key formats); InfiniteHiP
-// article (163.com), section "实现 7.24 倍的端到端解码加速" (each chunk's best token is what
-// the pruning module ranks: here exact per-block and per-64-token-tile maxima of the token
-// scores).
+// share one kv head) and section "KV Cache 量化" (INT8, INT4 and FP8 key formats);
+// InfiniteHiP article (163.com), section "实现 7.24 倍的端到端解码加速" (each chunk's best
+// token is what the pruning module ranks: here exact per-block and per-64-token-tile maxima
+// of the token scores; every head pruned on its own with per-head selection).
 //
 // score_blocks_kernel (the HBM-bound scan): a persistent grid walks the flattened list of
 // 64-token tiles (sequence, kv head, tile). One producer lane per CTA streams each tile's
@@ -15,8 +15,10 @@
 // bank-conflict free) and mbarrier transaction counts. Consumer warps own fixed ring slots;
 // lane = token (two tokens per lane, the tile's two halves), dp4a gives the G exact int32
 // dot products, their max is the token score and a 16-lane max gives the block maximum.
-// 8-bit codes with G <= 4 keep the G x 32 packed query words in registers; 4-bit codes and
-// G = 8 read them from a per-warp shared-memory copy, which leaves room for more warps.
+// 8-bit codes with G <= 4 keep the G x 32 packed query words in registers; 4-bit codes, G = 8
+// and per-head maxima read them from a per-warp shared-memory copy, which leaves room for
+// more warps. FP8 codes: fp32 scores, one fused multiply-add per channel in channel order
+// from the warp's fp32 query copy, whose maxima go on as order-preserving integers.
 #include <algorithm>
 #include <climits>
 #include <type_traits>
