@@ -188,20 +188,17 @@ cudaError_t set_kernel_smem(Kernel kernel, size_t dynamic_bytes) {
   if (e != cudaSuccess) return e;
   const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
   SmemAttrCache& c = smem_attr_cache();
-  {
-    std::lock_guard<std::mutex> g(c.mu);
-    const auto it = c.bytes.find(key);
-    if (it != c.bytes.end() && it->second >= dynamic_bytes) return cudaSuccess;
-  }
+  // under the lock, so that concurrent callers never lower a limit another one relies on
+  std::lock_guard<std::mutex> g(c.mu);
+  const auto it = c.bytes.find(key);
+  if (it != c.bytes.end() && it->second >= dynamic_bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)dynamic_bytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> g(c.mu);
-  size_t& have = c.bytes[key];
-  have = std::max(have, dynamic_bytes);
+  c.bytes[key] = dynamic_bytes;
   return cudaSuccess;
 }
 
