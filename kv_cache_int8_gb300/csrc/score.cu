@@ -93,7 +93,7 @@ struct ScoreCfg {
   static constexpr int kQWords = kQSmem ? kWarps * kQWarpWords : 0;
   static size_t smem_bytes(int batch) {
     return 1024 + kRingBytes + 2 * kStages * sizeof(uint64_t) + kQWords * sizeof(int) +
-           (batch + 1) * sizeof(int);
+           (2 * batch + 1) * sizeof(int);
   }
 };
 
@@ -115,9 +115,9 @@ struct SeqRange {
   int tile_lo, ntile;  // tiles covering [k_lo, k_hi)
 };
 
-__device__ __forceinline__ SeqRange seq_range(const ScoreArgs& a, int b) {
+// From the sequence length n (read once per CTA into shared memory).
+__device__ __forceinline__ SeqRange seq_range(const ScoreArgs& a, int n) {
   SeqRange r;
-  const int n = a.seq_lens[b];
   r.lo = a.sink;
   r.hi = n - a.window;
   if (n < 0 || n > a.max_pages * kPage || r.hi <= r.lo) {
@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF,
   uint64_t* empty = full + kStages;
   int* qbuf = reinterpret_cast<int*>(empty + kStages);  // [consumer warp][G][32] (kQSmem)
   int* prefix = qbuf + C::kQWords;                       // [batch + 1] tiles before b
+  int* lens = prefix + a.batch + 1;                      // [batch] sequence lengths
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -289,7 +290,8 @@ __global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF,
       if (b < a.batch) {
         const int n = a.seq_lens[b];
         if (n < 0 || n > a.max_pages * kPage) set_error(a.err, kDevErrCheck);
-        v = seq_range(a, b).ntile * a.hkv;
+        lens[b] = n;
+        v = seq_range(a, n).ntile * a.hkv;
       }
       int x = v;
 #pragma unroll
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF,
       if (f < f1) {
         int bl = bw;
         while (prefix[bl + 1] <= f) bl++;
-        const SeqRange sr = seq_range(a, bl);
+        const SeqRange sr = seq_range(a, lens[bl]);
         const int r = f - prefix[bl];
         const int h = r / sr.ntile;
         const int tile = sr.tile_lo + r % sr.ntile;
@@ -407,12 +409,12 @@ __global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF,
   int* qs = qbuf + (C::kQSmem ? warp * C::kQWarpWords : 0);
   const uint32_t qs_addr = smem_addr(qs);
   int cur_b = -1, cur_h = -1;
-  SeqRange sr = seq_range(a, b);
+  SeqRange sr = seq_range(a, lens[b]);
   for (int j = warp; f0 + j < f1; j += C::kWarps) {
     const int f = f0 + j;
     while (prefix[b + 1] <= f) {
       b++;
-      sr = seq_range(a, b);
+      sr = seq_range(a, lens[b]);
     }
     const int r = f - prefix[b];
     const int h = r / sr.ntile;
