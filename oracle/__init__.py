@@ -9,6 +9,7 @@ brute force, closed forms and special cases); none is "parity unpinned".
 from .oracle import (  # noqa: F401
     Dims,
     attend,
+    block_mass,
     dense,
     num_threads,
     quantize_append,

@@ -37,7 +37,10 @@
  *    and only their tokens inside C count; a chunk or block with no token in C is
  *    never selected;
  *  - ties: the lower index wins at both levels; index lists are returned ascending;
- *  - attended set T = [0, min(S,N)) u [max(N-W, min(S,N)), N) u (kept blocks n C).
+ *  - attended set T = [0, min(S,N)) u [max(N-W, min(S,N)), N) u (kept blocks n C);
+ *  - the "cumulative magnitude" of a KV block ([HCA], eviction from the GPU cache) is the
+ *    softmax probability its attended tokens receive, summed over the group's query heads
+ *    and accumulated over the decode calls.
  *
  * Precision: attention in fp64 from the exact bf16 values. The quantisation steps
  * decide integers in IEEE fp32, emulated as ONE fp64 operation followed by a cast to
@@ -477,12 +480,14 @@ static int attended(const oracle_dims* d, int64_t n, int64_t t, const char* kept
 /* [KVN] "KV Cache 回顾": out = softmax(q K_T^T / sqrt(d)) V_T over the attended set T,
  * in fp64 from the exact bf16 values; lse = log sum_t exp(l_t). When `all` is set, T
  * is the whole context [0, N) (dense decode). When `recall` is given, the function
- * instead returns sum_{t in T} p_t with p the dense softmax over [0, N). */
+ * instead returns sum_{t in T} p_t with p the dense softmax over [0, N). When `mass` is
+ * given, it instead returns, for every block, the softmax probability over T that the
+ * block's attended tokens receive: mass [B][Hq][max_blocks]. */
 static int attention_common(const oracle_dims* d, const uint16_t* q, const uint16_t* k,
                             const uint16_t* v, const int32_t* page_table, const int32_t* lens,
                             const int32_t* block_idx, const int32_t* n_blocks,
                             const int32_t* qh_mask, int all, double* out, double* lse,
-                            double* recall) {
+                            double* recall, double* mass) {
   const int D = d->head_dim, G = d->hq / d->hkv;
   const double scale = d->sm_scale > 0 ? d->sm_scale : 1.0 / sqrt((double)D);
   const int64_t max_tokens = (int64_t)d->max_pages_per_seq * d->page_size;
@@ -539,6 +544,11 @@ static int attention_common(const oracle_dims* d, const uint16_t* q, const uint1
     }
     if (recall) {
       recall[bj] = n > 0 ? zt / z : 0.0;
+    } else if (mass) {
+      double* row = mass + (int64_t)bj * max_blocks;
+      for (int64_t i = 0; i < max_blocks; i++) row[i] = 0.0;
+      for (int64_t t = 0; t < n; t++)
+        if (attended(d, n, t, kept)) row[t / d->block] += exp(logit[t] - m) / z;
     } else {
       double* o = out + (int64_t)bj * D;
       for (int c = 0; c < D; c++) o[c] = 0.0;
@@ -566,7 +576,7 @@ int oracle_attend(const oracle_dims* d, const uint16_t* q, const uint16_t* k, co
   for (int b = 0; b < d->batch; b++)
     if (!seq_ok(d, page_table, lens, b)) return 2;
   return attention_common(d, q, k, v, page_table, lens, block_idx, n_blocks, qh_mask, 0, out, lse,
-                          NULL);
+                          NULL, NULL);
 }
 
 /* Dense decode attention over the whole context [0, N). */
@@ -576,7 +586,8 @@ int oracle_dense(const oracle_dims* d, const uint16_t* q, const uint16_t* k, con
   if (!dims_ok(d) || !q || !k || !v || !page_table || !lens || !out) return 1;
   for (int b = 0; b < d->batch; b++)
     if (!seq_ok(d, page_table, lens, b)) return 2;
-  return attention_common(d, q, k, v, page_table, lens, NULL, NULL, qh_mask, 1, out, lse, NULL);
+  return attention_common(d, q, k, v, page_table, lens, NULL, NULL, qh_mask, 1, out, lse, NULL,
+                          NULL);
 }
 
 /* Attention-mass recall of T against dense attention ([HiP], latency section: recall of
@@ -588,7 +599,23 @@ int oracle_recall(const oracle_dims* d, const uint16_t* q, const uint16_t* k,
   for (int b = 0; b < d->batch; b++)
     if (!seq_ok(d, page_table, lens, b)) return 2;
   return attention_common(d, q, k, NULL, page_table, lens, block_idx, n_blocks, qh_mask, 0, NULL,
-                          NULL, recall);
+                          NULL, recall, NULL);
+}
+
+/* Attention mass of every block under the sparse attention of one call: mass [B][Hq][max
+ * blocks], the softmax probability over T that the block's attended tokens receive from
+ * query head j (zero for blocks outside T). Summed over the G query heads of a kv head and
+ * accumulated over the calls, it is the cumulative magnitude by which the block cache evicts
+ * ([HCA] contribution list: dynamic, reversible eviction of the least important KV pairs from
+ * the GPU cache by a cumulative-magnitude criterion; the evicted pairs stay in host memory). */
+int oracle_block_mass(const oracle_dims* d, const uint16_t* q, const uint16_t* k,
+                      const int32_t* page_table, const int32_t* lens, const int32_t* block_idx,
+                      const int32_t* n_blocks, double* mass) {
+  if (!dims_ok(d) || !q || !k || !page_table || !lens || !block_idx || !mass) return 1;
+  for (int b = 0; b < d->batch; b++)
+    if (!seq_ok(d, page_table, lens, b)) return 2;
+  return attention_common(d, q, k, NULL, page_table, lens, block_idx, n_blocks, NULL, 0, NULL,
+                          NULL, NULL, mass);
 }
 
 int oracle_num_threads(void) {

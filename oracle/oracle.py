@@ -84,6 +84,7 @@ def _lib():
             "oracle_attend": [D, P, P, P, P, P, P, P, P, P, P],
             "oracle_dense": [D, P, P, P, P, P, P, P, P],
             "oracle_recall": [D, P, P, P, P, P, P, P, P],
+            "oracle_block_mass": [D, P, P, P, P, P, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -221,3 +222,17 @@ def recall(d: Dims, q, k, page_table, seq_lens, block_idx, n_blocks, qh_mask=Non
                                 _ptr(None if qh_mask is None else _i32(qh_mask)), _ptr(r)),
            "oracle_recall")
     return r
+
+
+def block_mass(d: Dims, q, k, page_table, seq_lens, block_idx, n_blocks):
+    """Attention mass of every block under one call's sparse attention, [B][Hq][max_blocks]:
+    the softmax probability over the attended set that the block's attended tokens receive
+    from each query head. Summed over a kv head's query heads and accumulated over calls it
+    is the block cache's cumulative-magnitude eviction key."""
+    m = np.zeros((d.batch, d.hq, d.max_blocks), dtype=np.float64)
+    cd = d.c()
+    _check(_lib().oracle_block_mass(ctypes.byref(cd), _ptr(_u16(q)), _ptr(_u16(k)),
+                                    _ptr(_i32(page_table)), _ptr(_i32(seq_lens)),
+                                    _ptr(_i32(block_idx)), _ptr(_i32(n_blocks)), _ptr(m)),
+           "oracle_block_mass")
+    return m

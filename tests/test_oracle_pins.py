@@ -851,3 +851,70 @@ def test_tokens_past_the_end_are_ignored():
     for key in ("block_idx", "chunk_idx", "block_max"):
         np.testing.assert_array_equal(res1[2][key], res2[2][key])
     np.testing.assert_array_equal(res1[3], res2[3])
+
+
+# ------------------------------------------------- block attention mass (cache eviction)
+
+def test_block_mass_is_the_dense_softmax_when_everything_is_kept():
+    """Every block kept, no sink or window: the mass of block k for head j is the sum over
+    its tokens of scipy's softmax of the dense logits, and each head's masses sum to 1."""
+    rng = np.random.default_rng(41)
+    case = random_case(rng, B=2, hq=4, hkv=2, D=16, lens=(150, 97), page=16, perm=True)
+    d = dims_for(case, 4, 2, 16, chunk=32, block=16, k1=100, k2=100, sink=0, window=0)
+    _, _, sel, _, _ = run_all(d, case)
+    m = oracle.block_mass(d, bf16_bits(case["q"]), bf16_bits(case["k"]), case["pt"], case["lens"],
+                          sel["block_idx"], sel["n_blocks"])
+    for b, n in enumerate(case["lens"]):
+        for j in range(4):
+            keys = case["ks"][b][j // 2].astype(np.float64)              # [n][D]
+            p = softmax(keys @ case["q"][b, j].astype(np.float64) / 4.0)
+            want = np.zeros(d.max_blocks)
+            np.add.at(want, np.arange(n) // 16, p)
+            np.testing.assert_allclose(m[b, j], want, atol=1e-13)
+            assert abs(m[b, j].sum() - 1.0) < 1e-12
+
+
+def test_block_mass_identical_keys_is_token_count_over_t():
+    """All keys equal: the softmax is uniform over T, so block k receives |T n k| / |T|
+    (sink 10 and window 15 cut blocks 0 and 11 short)."""
+    rng = np.random.default_rng(42)
+    n, D = 200, 8
+    key = to_bf16(rng.standard_normal(D))
+    kc, pt, ln = paged([np.tile(key, (1, n, 1)).astype(np.float32)], 16, 1)
+    q = to_bf16(rng.standard_normal((1, 2, D)))
+    d = Dims(1, 2, 1, D, 16, pt.shape[1], kc.shape[0], 32, 16, 0, 2, 10, 15)
+    bidx = np.array([[[3, 7]]], np.int32)
+    m = oracle.block_mass(d, bf16_bits(q), bf16_bits(kc), pt, ln, bidx, np.array([[2]], np.int32))
+    want = np.zeros(d.max_blocks)
+    want[0] = 10            # sink: tokens 0..9
+    want[3] = want[7] = 16  # kept blocks, inside the candidate region [10, 185)
+    want[11] = 7            # window: tokens 185..199 -> block 11 holds 185..191
+    want[12] = 8            # and block 12 holds 192..199
+    want /= want.sum()      # |T| = 10 + 32 + 15 = 57
+    for j in range(2):
+        np.testing.assert_allclose(m[0, j], want, atol=1e-14)
+
+
+def test_block_mass_restriction_identity():
+    """Mass over the sparse set T = dense mass / recall on T's blocks, zero elsewhere (sink
+    and window are whole blocks here, so every block is in T entirely or not at all)."""
+    rng = np.random.default_rng(43)
+    case = random_case(rng, B=1, hq=4, hkv=1, D=8, lens=(410,), page=16)
+    d = dims_for(case, 4, 1, 8, chunk=32, block=16, k1=4, k2=5, sink=16, window=26)
+    _, _, sel, _, _ = run_all(d, case)
+    qb, kb = bf16_bits(case["q"]), bf16_bits(case["k"])
+    ms = oracle.block_mass(d, qb, kb, case["pt"], case["lens"], sel["block_idx"], sel["n_blocks"])
+    every = np.arange(d.max_blocks, dtype=np.int32)[None, None, :]
+    dd = dims_for(case, 4, 1, 8, chunk=32, block=16, k1=d.max_blocks, k2=d.max_blocks, sink=0,
+                  window=0)
+    md = oracle.block_mass(dd, qb, kb, case["pt"], case["lens"], every,
+                           np.array([[d.max_blocks]], np.int32))
+    r = oracle.recall(d, qb, kb, case["pt"], case["lens"], sel["block_idx"], sel["n_blocks"])
+    in_t = {0, 24, 25}   # sink: block 0; window: tokens 384..409
+    in_t |= {int(k) for k in sel["block_idx"][0, 0, : sel["n_blocks"][0, 0]]}
+    for j in range(4):
+        for k in range(d.max_blocks):
+            if k in in_t:
+                assert abs(ms[0, j, k] * r[0, j] - md[0, j, k]) < 1e-13
+            else:
+                assert ms[0, j, k] == 0.0
