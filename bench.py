@@ -17,6 +17,7 @@ host cores instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -177,7 +178,7 @@ class Case:
         cfg = self.cfg
         self.kernels = self.KERNELS if dense else tuple(k for k in self.KERNELS if k != "dense")
         if cfg.kv_on_host:  # the step and the attention through the GPU block cache too
-            self.kernels = self.kernels + ("step_cached", "attend_cached")
+            self.kernels = self.kernels + ("step_cached", "attend_cached", "step_cached_mass")
         # offloaded K/V: one pinned host copy (both "replicas" alias it; steps are separated by
         # an L2 flush instead, see timed_steps)
         wl = W.make_workload(cfg, seed=seed, device=str(device), host_pinned=cfg.kv_on_host)
@@ -233,6 +234,10 @@ class Case:
             self.cache_capacity = self.CACHE_SLOTS
             self.cache = hsa.block_cache(d, self.cache_capacity)
             self.ws_cached = hsa.workspace(d, hsa.HSA_OP_CACHED)
+            # the same cache under the cumulative-attention-mass eviction policy
+            self.d_mass = dataclasses.replace(d, cache_policy=1)
+            self.cache_mass = hsa.block_cache(self.d_mass, self.cache_capacity)
+            self.ws_step_mass = hsa.workspace(self.d_mass, hsa.HSA_OP_STEP)
         self.bm = torch.zeros((B, R, d.max_pages_per_seq), dtype=torch.int32, device=device)
         self.tm = torch.zeros((B, R, (d.max_pages_per_seq + 3) // 4), dtype=torch.int32,
                               device=device)
@@ -256,6 +261,12 @@ class Case:
                                         self.lse, self.k[r], self.v[r], self.kq[r], self.ks[r],
                                         self.pt, self.lens, self.block_idx, self.n_blocks,
                                         self.cache, self.cache_capacity, self.ws_step)
+
+    def step_cached_mass(self, r):
+        self.hsa.hsa_decode_step_cached(self.d_mass, self.q, self.k_new, self.v_new, self.out,
+                                        self.lse, self.k[r], self.v[r], self.kq[r], self.ks[r],
+                                        self.pt, self.lens, self.block_idx, self.n_blocks,
+                                        self.cache_mass, self.cache_capacity, self.ws_step_mass)
 
     def attend_cached(self, r):
         self.hsa.hsa_attend_cached(self.d, self.q, self.k[r], self.v[r], self.pt, self.lens,
@@ -530,8 +541,9 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
     lper, _ = timed_steps(case, lsteps, ("loop", "reuse"))
     cached = {}
     if getattr(case, "cache", None) is not None:
-        timed_steps(case, 3, ("step_cached", "attend_cached"))
-        cached, _ = timed_steps(case, max(3, min(steps, 300)), ("step_cached", "attend_cached"))
+        names_c = ("step_cached", "attend_cached", "step_cached_mass")
+        timed_steps(case, 3, names_c)
+        cached, _ = timed_steps(case, max(3, min(steps, 300)), names_c)
     # kernel breakdown: the average launch duration of each of the four kernels
     bsteps = max(3, min(steps // 10, 200))
     per = burst_times(case, names, bsteps)
@@ -540,7 +552,8 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
     else:
         dper = {"dense": float("nan")}
     for w in (case.ws_step, case.ws_sel, case.ws_att, case.ws_den) + (
-            (case.ws_cached,) if getattr(case, "cache", None) is not None else ()):
+            (case.ws_cached, case.ws_step_mass) if getattr(case, "cache", None) is not None
+            else ()):
         code = hsa.hsa_read_device_error(w)
         assert code == 0, f"device error word {code}"
     recall = torch.exp(case.lse.double() - case.lse_d.double())  # restriction identity
@@ -752,6 +765,7 @@ def main():
                 **({"host_link_copy_gbs": host_link_copy_gbs(device),
                     "us_per_step_block_cache": r["cached_ms"]["step_cached"] * 1e3,
                     "attend_block_cache_us": r["cached_ms"]["attend_cached"] * 1e3,
+                    "us_per_step_block_cache_mass_policy": r["cached_ms"]["step_cached_mass"] * 1e3,
                     "block_cache_slots": Case.CACHE_SLOTS} if r["cached_ms"] else {}),
                 "prune_us": r["per_ms"]["prune"] * 1e3, "attend_us": r["per_ms"]["attend"] * 1e3,
                 "dense_us": r["dense_ms"] * 1e3 if dense else None,

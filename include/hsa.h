@@ -116,6 +116,11 @@ typedef struct hsa_dims {
                                 channels in order; block_max / tile_max then hold the scores'
                                 order-preserving integer images (bits, negative ones with the
                                 magnitude bits flipped) */
+  int32_t cache_policy;      /* victims of the GPU block cache (hsa_attend_cached,
+                                hsa_decode_step_cached): 0 = least recently used; 1 = least
+                                cumulative attention mass (HCAttention: reversible eviction of
+                                the least important KV blocks by a cumulative-magnitude
+                                criterion); other values INVALID_ARG */
 } hsa_dims;
 
 /* Operation ids for hsa_workspace_bytes. */
@@ -276,14 +281,32 @@ int32_t hsa_decode_step_reuse(const hsa_dims* d, const hsa_step_io* io, void* k_
  * and the calls HSA_ERR_INVALID_ARG / HSA_ERR_UNSUPPORTED.
  *
  * Each call: its blocks (sink pages, window pages, kept blocks of every sequence and kv head)
- * are looked up; a hit counts as a use; every miss takes the slot, among those this call
- * does not use, that was used longest ago (ties: the lower slot), and is copied in over the
- * host link; the page that holds each sequence's last token is copied again on every call
- * (the append writes it). The host K/V of pages held in the cache must not change otherwise.
- * Two sequences may not share a page (reported as HSA_ERR_DEVICE_CHECK through the error
- * word).
+ * are looked up; a hit counts as a use; every miss takes a slot among those this call does
+ * not use and is copied in over the host link; the page that holds each sequence's last token
+ * is copied again on every call (the append writes it). The host K/V of pages held in the
+ * cache must not change otherwise. Two sequences may not share a page (reported as
+ * HSA_ERR_DEVICE_CHECK through the error word). The victims, taken in ascending slot order by
+ * the misses in call order, are the free slots (lower slot first), then:
+ *  - d->cache_policy 0: the slots used longest ago (ties: the lower slot);
+ *  - d->cache_policy 1 (HCAttention excerpt, contribution list: dynamic, reversible eviction
+ *    of the least important KV pairs from the GPU cache by a cumulative-magnitude
+ *    criterion): the slots whose blocks have the least cumulative attention mass (ties: the
+ *    lower slot). The buffer keeps, for every (page, kv head) block, the sum over calls of the
+ *    softmax probability that the block's attended tokens received from the kv head's query
+ *    heads (fp32, zero until the block is first attended); each cached call adds its own.
+ *    An evicted block keeps its sum and stays in host memory, so it returns when selected.
+ *    hsa_block_cache_mass reads the sums. Needs at most 8192 segments per (sequence, kv
+ *    head), ceil(sink / 16) + ceil(window / 16) + 1 + k2 <= 8192 (else UNSUPPORTED), and
+ *    distinct block ids in each block_idx row (as hsa_prune writes them).
  */
 size_t hsa_block_cache_bytes(const hsa_dims* d, int32_t capacity);
+
+/*
+ * Device pointer to the block cache's cumulative attention masses inside `block_cache`:
+ * float [num_pages][hkv], entry page * hkv + h for (page, kv head h), updated by the cached
+ * calls under cache_policy 1 (left at zero under policy 0). NULL if d or capacity is invalid.
+ */
+float* hsa_block_cache_mass(const hsa_dims* d, void* block_cache, int32_t capacity);
 
 /*
  * hsa_attend for K/V in pinned host memory (d->kv_on_host = 1, mapped) through the block

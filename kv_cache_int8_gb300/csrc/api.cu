@@ -54,6 +54,7 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   if (d->per_head != 0 && d->per_head != 1) return HSA_ERR_INVALID_ARG;
   if (d->key_fp8 != 0 && d->key_fp8 != 1) return HSA_ERR_INVALID_ARG;
   if (d->key_fp8 && d->key_bits == 4) return HSA_ERR_UNSUPPORTED;
+  if (d->cache_policy != 0 && d->cache_policy != 1) return HSA_ERR_INVALID_ARG;
   s.batch = d->batch;
   s.hq = d->hq;
   s.hkv = d->hkv;
@@ -70,6 +71,7 @@ int32_t check_dims(const hsa_dims* d, Shape& s, bool need_prune) {
   s.key_bits = d->key_bits == 4 ? 4 : 8;
   s.per_head = d->per_head;
   s.key_fp8 = d->key_fp8;
+  s.cache_policy = d->cache_policy;
   s.kv_div = 1;
   s.sm_scale = d->sm_scale > 0.0f ? d->sm_scale : 1.0f / std::sqrt((float)hsa::kHeadDim);
   return HSA_OK;
@@ -114,9 +116,10 @@ AttendLayout attend_layout(const Shape& s, size_t base) {
 }
 size_t attend_ws(const Shape& s) { return attend_layout(s, kErrBytes).end; }
 
-// Per-call scratch of the block cache: seg_slot [B][Hkv][stride], the fill list, its count.
+// Per-call scratch of the block cache: seg_slot [B][Hkv][stride], the fill list, its count,
+// and with cache policy 1 each segment's log-sum-exp per query head, seg_l2 [..][stride][G].
 struct CacheScratch {
-  size_t seg_slot, fill, n_fill, end;
+  size_t seg_slot, fill, n_fill, seg_l2, end;
 };
 CacheScratch cache_scratch(const Shape& s, size_t base) {
   const size_t F = (size_t)s.batch * s.hkv * hsa::block_cache_seg_stride(s);
@@ -124,7 +127,8 @@ CacheScratch cache_scratch(const Shape& s, size_t base) {
   c.seg_slot = base;
   c.fill = c.seg_slot + up(F * 4);
   c.n_fill = c.fill + up(F * 16);
-  c.end = c.n_fill + kAlign;
+  c.seg_l2 = c.n_fill + kAlign;
+  c.end = c.seg_l2 + (s.cache_policy == 1 ? up(F * s.group * 4) : 0);
   return c;
 }
 size_t cached_ws(const Shape& s) {
@@ -132,17 +136,19 @@ size_t cached_ws(const Shape& s) {
 }
 
 // The block cache buffer: header, slot_of [num_pages * hkv], slot_key / slot_stamp
-// [capacity], data [capacity][8 KiB].
+// [capacity], mass [num_pages * hkv] (fp32 cumulative attention mass), data [capacity][8 KiB].
 constexpr int kMaxCacheSlots = 32768;
+constexpr int kMaxMassSegments = 8192;  // segments per (sequence, kv head), cache policy 1
 struct CacheLayout {
-  size_t slot_of, slot_key, slot_stamp, data, end;
+  size_t slot_of, slot_key, slot_stamp, mass, data, end;
 };
 CacheLayout cache_layout(const Shape& s, int capacity) {
   CacheLayout l;
   l.slot_of = kAlign;
   l.slot_key = l.slot_of + up((size_t)s.num_pages * s.hkv * 4);
   l.slot_stamp = l.slot_key + up((size_t)capacity * 4);
-  l.data = l.slot_stamp + up((size_t)capacity * 4);
+  l.mass = l.slot_stamp + up((size_t)capacity * 4);
+  l.data = l.mass + up((size_t)s.num_pages * s.hkv * 4);
   l.end = l.data + (size_t)capacity * 2 * hsa::kBlockBytesBf16;
   return l;
 }
@@ -151,6 +157,9 @@ CacheLayout cache_layout(const Shape& s, int capacity) {
 int32_t check_cache_capacity(const Shape& s, int capacity) {
   if (capacity < s.batch * s.hkv * hsa::block_cache_seg_stride(s)) return HSA_ERR_INVALID_ARG;
   if (capacity > kMaxCacheSlots) return HSA_ERR_UNSUPPORTED;
+  // the mass policy's combine stages two words a segment in the attention's ring
+  if (s.cache_policy == 1 && hsa::block_cache_seg_stride(s) > kMaxMassSegments)
+    return HSA_ERR_UNSUPPORTED;
   if (hsa::block_cache_plan_smem(s, capacity) > 227 * 1024) return HSA_ERR_UNSUPPORTED;
   return HSA_OK;
 }
@@ -162,6 +171,7 @@ hsa::BlockCache block_cache_at(const Shape& s, void* buf, int capacity) {
   c.slot_of = reinterpret_cast<int32_t*>(p + l.slot_of);
   c.slot_key = reinterpret_cast<int32_t*>(p + l.slot_key);
   c.slot_stamp = reinterpret_cast<int32_t*>(p + l.slot_stamp);
+  c.mass = reinterpret_cast<float*>(p + l.mass);
   c.data = p + l.data;
   c.capacity = capacity;
   return c;
@@ -375,7 +385,7 @@ int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, 
                                         buf, reinterpret_cast<int*>(ws), st, early));
 }
 
-// The attention over K/V in host memory through the block cache: plan (lookups, LRU victims),
+// The attention over K/V in host memory through the block cache: plan (lookups, victims),
 // fill (the misses copied in over the host link), then the HBM attention reading the slots.
 // kd / vd: device aliases of the host K/V.
 int32_t do_attend_cached(const Shape& s, const void* q, const void* kd, const void* vd,
@@ -401,6 +411,11 @@ int32_t do_attend_cached(const Shape& s, const void* q, const void* kd, const vo
   buf.seg_slots = seg_slot;
   buf.seg_stride = hsa::block_cache_seg_stride(s);
   buf.cache_capacity = capacity;
+  if (s.cache_policy == 1) {
+    buf.seg_l2 = reinterpret_cast<float*>(ws + cs.seg_l2);
+    buf.mass = c.mass;
+    buf.slot_key = c.slot_key;
+  }
   const char* data = static_cast<const char*>(c.data);
   return cuda_status(hsa::launch_attend(s, false, false, q, data, data + hsa::kBlockBytesBf16, pt,
                                         lens, bidx, nb, out, lse, buf, err, st, false));
@@ -737,6 +752,13 @@ size_t hsa_block_cache_bytes(const hsa_dims* d, int32_t capacity) {
   if (check_dims(d, s, false) != HSA_OK || s.per_head) return 0;
   if (check_cache_capacity(s, capacity) != HSA_OK) return 0;
   return cache_layout(s, capacity).end;
+}
+
+float* hsa_block_cache_mass(const hsa_dims* d, void* block_cache, int32_t capacity) {
+  Shape s;
+  if (!block_cache || check_dims(d, s, false) != HSA_OK || s.per_head) return nullptr;
+  if (check_cache_capacity(s, capacity) != HSA_OK) return nullptr;
+  return block_cache_at(s, block_cache, capacity).mass;
 }
 
 int32_t hsa_attend_cached(const hsa_dims* d, const void* q, const void* k_cache,

@@ -85,6 +85,12 @@ struct AttArgs {
   const int32_t* seg_slots;  // nullable: block-cache slot of every segment (then k / v point
                              // at the cache's K and V halves and num_pages is its capacity)
   int seg_stride;
+  // nullable, with seg_slots (block cache, cumulative-mass policy): seg_l2 [B][Hkv][seg_stride]
+  // [G] gets each segment's log-sum-exp (log2 domain) per query head; the last CTA of (b, h)
+  // adds each segment's attention mass to mass[slot_key[slot] - 1]
+  float* seg_l2;
+  float* mass;
+  const int32_t* slot_key;
   float* out;
   float* lse;
   float* part_ml;
@@ -366,11 +372,63 @@ __device__ __forceinline__ void process_segment(State<G>& st, const float (&qf)[
 // CTA of (b, h) to finish. `red` (shared, at least G * kMaxSplits + 8 floats) may alias
 // `o`. Called by all threads of the CTA after the merged state is complete. NB: splits a
 // thread of the combine loads per round trip.
-template <int G, int NB>
+// Cumulative-mass cache policy: adds each attended segment's attention mass, summed over the
+// G query heads (p = 2^(seg_l2 - lse2) per head), to the cumulative mass of the block that its
+// cache slot holds. One CTA per (b, h), once the final log-sum-exp lse2[j] of every head is
+// known. A block can be two segments of one call: the sink's last page or the window's first
+// page when either is partial, and a kept block or the other of the two (same slot). Such a
+// block's masses are summed, in segment order, by the boundary segment that holds it, so that
+// every entry is written by one thread and the result does not depend on timing. scratch:
+// 2 * seg_stride words of shared memory.
+template <int G>
+__device__ void add_segment_mass(const AttArgs& a, int b, int h, const float* lse2,
+                                 float* scratch) {
+  const Segments S = make_segments<false>(a, b, h);
+  const int n = a.seg_stride;
+  int* slot_s = reinterpret_cast<int*>(scratch);
+  float* w_s = scratch + n;
+  const size_t sbase = ((size_t)b * a.hkv + h) * n;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    int slot = a.seg_slots[sbase + i];
+    if (slot >= a.num_pages) slot = -1;  // num_pages: the cache's capacity here
+    float w = 0.0f;
+    if (slot >= 0) {
+      const float* l2 = a.seg_l2 + (sbase + i) * G;
+#pragma unroll
+      for (int j = 0; j < G; j++) {
+        const float v = __ldcg(l2 + j);
+        if (v > kNeg) w += exp2f(v - lse2[j]);
+      }
+    }
+    slot_s[i] = slot;
+    w_s[i] = w;
+  }
+  __syncthreads();
+  const int bs = S.n_sink - 1;                  // the sink's last segment, or -1
+  const int bw = S.n_win > 0 ? S.n_sink : -1;   // the window's first segment, or -1
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int slot = slot_s[i];
+    if (slot < 0) continue;
+    const int owner = (bs >= 0 && slot_s[bs] == slot) ? bs
+                      : (bw >= 0 && slot_s[bw] == slot) ? bw : i;
+    if (owner != i) continue;
+    float w = w_s[i];
+    if (i == bs || i == bw) {
+      w = 0.0f;
+      for (int j = 0; j < n; j++)
+        if (slot_s[j] == slot) w += w_s[j];
+    }
+    const int key = a.slot_key[slot] - 1;
+    if (key >= 0) a.mass[key] += w;
+  }
+}
+
+template <int G, int NB, bool MASS = false>
 __device__ void finish_common(const AttArgs& a, int b, int h, int split, const float* o,
                               const float* m, const float* l, float* red, int nthreads) {
   const int tid = threadIdx.x;
   __shared__ int is_last;
+  __shared__ float lse2[8];  // final log-sum-exp per head, log2 domain (cumulative-mass policy)
   const int hq = a.hkv * G;
   if (tid < nthreads) {
     for (int x = tid; x < G * kHeadDim; x += nthreads) {
@@ -380,6 +438,7 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
       if (a.nsplit == 1) {
         a.out[row * kHeadDim + d] = L > 0.0f ? o[x] / L : 0.0f;
         if (d == 0 && a.lse) a.lse[row] = L > 0.0f ? (m[j] + log2f(L)) * kLn2 : -INFINITY;
+        if (MASS && d == 0) lse2[j] = L > 0.0f ? m[j] + log2f(L) : kNeg;
       } else {
         const size_t p = row * a.nsplit + split;
         a.part_o[p * kHeadDim + d] = o[x];
@@ -387,7 +446,13 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
       }
     }
   }
-  if (a.nsplit == 1) return;
+  if (a.nsplit == 1) {
+    if constexpr (MASS) {
+      __syncthreads();
+      add_segment_mass<G>(a, b, h, lse2, red);
+    }
+    return;
+  }
   // One acquire-release increment by thread 0 between two CTA barriers: the first barrier
   // orders every thread's partial writes before the release, the second orders the last
   // CTA's reads of the other partials after the acquire (the pattern of a grid barrier).
@@ -404,7 +469,6 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
   // seen so far; then the two threads of a pair (adjacent lanes) merge their states. Both
   // 2 * G * 32 and the block size are multiples of 32, so every warp takes part in an
   // iteration with all its lanes or not at all.
-  (void)red;
   const int per = (a.nsplit + 1) >> 1;
   for (int x = tid; x < 2 * G * 32; x += blockDim.x) {
     const int it = x >> 1, half = x & 1;
@@ -462,7 +526,12 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
       *reinterpret_cast<float4*>(a.out + row * kHeadDim + d4) =
           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       if (d4 == 0 && a.lse) a.lse[row] = L > 0.0f ? (Mn + log2f(L)) * kLn2 : -INFINITY;
+      if (MASS && d4 == 0) lse2[j] = L > 0.0f ? Mn + log2f(L) : kNeg;
     }
+  }
+  if constexpr (MASS) {
+    __syncthreads();
+    add_segment_mass<G>(a, b, h, lse2, red);
   }
   if (tid == 0) a.counters[(size_t)b * a.hkv + h] = 0;
 }
@@ -538,10 +607,12 @@ struct WarpState {
   float m, l;       // running max / sum of head hidx (this lane's head)
 };
 
+// seg_out (nullable): receives the segment's log-sum-exp of the scaled scores (log2 domain)
+// of each query head, m + log2(sum 2^(s - m)).
 template <int G>
 __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)[G][16],
                                              WarpScratch<head_slots(G)>& ws, uint32_t slot,
-                                             int k, int t0, int t1) {
+                                             int k, int t0, int t1, float* seg_out) {
   constexpr int H = head_slots(G);
   const int lane = threadIdx.x & 31;
   const int g = lane >> 3, sl = lane & 7;
@@ -583,6 +654,8 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
   st.l = st.l * c + ps;
   st.m = m_new;
   constexpr int kOwners = 8 / G;  // lanes of a group holding the same head; the first writes
+  if (seg_out != nullptr && g == 0 && (sl & (kOwners - 1)) == 0)
+    seg_out[hidx] = ps > 0.0f ? m_new + log2f(ps) : kNeg;
   if ((sl & (kOwners - 1)) == 0) {
 #pragma unroll
     for (int it = 0; it < 4; it++) ws.prob[4 * it + g][hidx] = p[it];
@@ -631,7 +704,9 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
 // W compute warps and NS ring slots (NS a multiple of W): the sparse path uses 8 warps and 16
 // slots, enough for every segment of a CTA to be in flight at once; dense decode uses 4 and 8
 // with three CTAs per SM.
-template <int G, bool DENSE, int W, int NS>
+// MASS: the block cache's cumulative-mass policy (a.seg_l2 set): every segment's log-sum-exp
+// per head is written out for the combine, which adds the segments' attention mass.
+template <int G, bool DENSE, int W, int NS, bool MASS>
 __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
     attend_tma_kernel(const AttArgs a) {
   static_assert(NS % W == 0, "each compute warp owns fixed ring slots");
@@ -799,8 +874,14 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
         break;
       }
       const int4 m4 = meta[s];  // written before the producer's arrive on full[s]
+      float* seg_out = nullptr;
+      if constexpr (MASS)
+        seg_out = a.seg_l2 + (((size_t)b * a.hkv + h) * a.seg_stride + first + j * stride) * G;
       if (m4.y < m4.z)
-        warp_segment<G>(st, qf, wscr[warp], smem_addr(ring + s * kSlotBytes), m4.x, m4.y, m4.z);
+        warp_segment<G>(st, qf, wscr[warp], smem_addr(ring + s * kSlotBytes), m4.x, m4.y, m4.z,
+                        seg_out);
+      else if (MASS && lane < G)
+        seg_out[lane] = kNeg;  // no token: no mass
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -853,7 +934,7 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
     }
   }
   __syncthreads();
-  finish_common<G, DENSE ? 8 : 16>(a, b, h, split, mo, mm, ml, o, W * 32);
+  finish_common<G, DENSE ? 8 : 16, MASS>(a, b, h, split, mo, mm, ml, o, W * 32);
 }
 
 // ---------------------------------------------------------- mapped-host path
@@ -991,7 +1072,9 @@ cudaError_t launch_g(AttArgs a, dim3 grid, bool host, cudaStream_t st) {
   constexpr int W = DENSE ? kDenseWarps : (G > 4 ? 7 : kSparseWarps);
   constexpr int NS = DENSE ? kDenseStages : 2 * W;
   constexpr size_t smem = tma_smem<G, W, NS>();
-  auto kern = attend_tma_kernel<G, DENSE, W, NS>;
+  auto kern = attend_tma_kernel<G, DENSE, W, NS, false>;
+  if constexpr (!DENSE)
+    if (a.seg_l2 != nullptr) kern = attend_tma_kernel<G, false, W, NS, true>;
   cudaError_t e = set_kernel_smem(kern, smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, grid, dim3((W + 1) * 32), smem, st, true, a);
@@ -1047,6 +1130,9 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
   a.sel_pages = buf.sel_pages;
   a.seg_slots = buf.seg_slots;
   a.seg_stride = buf.seg_stride;
+  a.seg_l2 = buf.seg_slots ? buf.seg_l2 : nullptr;
+  a.mass = buf.mass;
+  a.slot_key = buf.slot_key;
   a.out = out;
   a.lse = lse;
   a.part_ml = buf.part_ml;

@@ -16,6 +16,7 @@ struct Shape {
   int key_bits;    // 8: 8-bit key codes [page][hkv][16][128]; 4: 4-bit, [page][hkv][16][64] bytes
   int per_head;    // 1: every query head selects its own blocks (rows = hq, not hkv)
   int key_fp8;     // 1: FP8 E4M3 key codes (8-bit layout), fp32 scores
+  int cache_policy;  // block cache victims: 0 least recently used, 1 least cumulative mass
   int kv_div = 1;  // attention rows per kv head (hq / hkv for a per-head attention launch)
   float sm_scale;  // resolved (> 0)
   // rows of the selection (block and tile maxima, kept chunks and blocks) per sequence
@@ -68,14 +69,16 @@ struct BlockCache {
   int32_t* slot_of;     // [num_pages * hkv]: slot + 1, 0 when absent
   int32_t* slot_key;    // [capacity]: page * hkv + head + 1, 0 when free
   int32_t* slot_stamp;  // [capacity]: last step that used the slot
+  float* mass;          // [num_pages * hkv]: cumulative attention mass of every block
   void* data;           // [capacity][2][16][128] bf16: K block then V block of each slot
   int capacity;
 };
 // Segments per (sequence, kv head) in the plan's seg_slot and fill arrays.
 int block_cache_seg_stride(const Shape& s);
 size_t block_cache_plan_smem(const Shape& s, int capacity);
-// One CTA: looks up the attention's segments, picks LRU victims for the misses, writes
-// seg_slot [B][Hkv][stride] and the fill list (int4 [B * Hkv * stride], count in n_fill).
+// One CTA: looks up the attention's segments, picks the victims for the misses (least
+// recently used, or least cumulative mass with s.cache_policy 1), writes seg_slot
+// [B][Hkv][stride] and the fill list (int4 [B * Hkv * stride], count in n_fill).
 cudaError_t launch_cache_plan(const Shape& s, const int32_t* seq_lens, const int32_t* page_table,
                               const int32_t* block_idx, const int32_t* n_blocks,
                               const BlockCache& c, int32_t* seg_slot, void* fill,
@@ -94,6 +97,12 @@ struct AttendBuffers {
   const int32_t* seg_slots = nullptr;  // optional: block-cache slots of the segments (then
   int seg_stride = 0;                  // k / v are the cache's K and V halves)
   int cache_capacity = 0;
+  // optional, with seg_slots (cache policy 1): seg_l2 [B][Hkv][seg_stride][G] scratch for
+  // each segment's log2-domain log-sum-exp per query head; the last CTA of (b, h) adds each
+  // segment's attention mass to mass[slot_key[slot] - 1]
+  float* seg_l2 = nullptr;
+  float* mass = nullptr;
+  const int32_t* slot_key = nullptr;
 };
 // Copies the block cache's fill list (from launch_cache_plan) in from host memory:
 // k_host / v_host are device aliases of the pinned host K/V.

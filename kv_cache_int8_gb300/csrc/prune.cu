@@ -641,6 +641,8 @@ struct CachePlanArgs {
   int32_t* slot_of;          // [num_pages * hkv]: slot + 1, 0 when absent
   int32_t* slot_key;         // [capacity]: page * hkv + head + 1, 0 when free
   int32_t* slot_stamp;       // [capacity]: last step that used the slot, 0 never
+  const float* mass;         // nullable: [num_pages * hkv] cumulative attention mass; victims
+                             // by least mass instead of least recent use
   int32_t* seg_slot;         // [B][Hkv][seg_stride]: slot of each segment, -1 empty
   int4* fill;                // [B * Hkv * seg_stride]: (slot, page, head) to copy in
   int32_t* n_fill;
@@ -674,6 +676,22 @@ __device__ int cache_segment_block(const CachePlanArgs& a, int b, int h, int i, 
   // a kept block is attended only inside the candidate region
   if (max(k * kPage, a.sink) >= min(k * kPage + kPage, cand_hi)) return -1;
   return k;
+}
+
+// A block can be two segments of one call: the sink's last page or the window's first page
+// when either is partial, and a kept block (or the other of the two). Returns the index of
+// the earlier segment of (b, h) holding block k of segment i, or -1: the later one takes the
+// earlier one's slot and is neither looked up nor filled on its own.
+__device__ int cache_segment_alias(const CachePlanArgs& a, int i, int n, int k) {
+  const int sink_end = min(a.sink, n);
+  const int n_sink = (sink_end + kPage - 1) / kPage;
+  const int w0 = max(n - a.window, sink_end);
+  const int n_win = w0 < n ? (n + kPage - 1) / kPage - w0 / kPage : 0;
+  if (i < n_sink) return -1;
+  if (n_sink > 0 && k == n_sink - 1) return n_sink - 1;
+  if (i < n_sink + n_win) return -1;
+  if (n_win > 0 && k == w0 / kPage) return n_sink;
+  return -1;
 }
 
 __global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePlanArgs a) {
@@ -710,6 +728,7 @@ __global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePl
       const int f = fb + u;
       n[u] = f < f_hi ? a.seq_lens[(f / a.seg_stride) / a.hkv] : 0;
     }
+    int alias[8];
 #pragma unroll
     for (int u = 0; u < 8; u++) {
       const int f = fb + u;
@@ -718,6 +737,8 @@ __global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePl
       k[u] = (f < f_hi && n[u] > 0) ? cache_segment_block(a, bh / a.hkv, bh % a.hkv,
                                                           f % a.seg_stride, n[u])
                                     : -1;
+      alias[u] = k[u] >= 0 ? cache_segment_alias(a, f % a.seg_stride, n[u], k[u]) : -1;
+      if (alias[u] >= 0) k[u] = -1;  // resolved after the victims are placed
     }
 #pragma unroll
     for (int u = 0; u < 8; u++) {
@@ -747,7 +768,8 @@ __global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePl
         miss_mask |= 1ull << (f - f_lo);
         my_miss++;
       }
-      a.seg_slot[f] = k[u] >= 0 ? slot[u] : -1;  // misses are overwritten below
+      // misses are overwritten below; an alias holds -2 - (its segment's index)
+      a.seg_slot[f] = k[u] >= 0 ? slot[u] : (alias[u] >= 0 ? -2 - alias[u] : -1);
     }
   }
   // exclusive scan of the per-thread miss counts, then each thread lists its misses in order
@@ -771,13 +793,21 @@ __global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePl
   const int M = cs.n_miss, R = cs.n_refresh;
 
   // ---- victims: the M slots not used by this call with the oldest stamps (lower slot
-  // first), ascending by slot; the fill list holds the refreshes, then the misses
+  // first), ascending by slot; the fill list holds the refreshes, then the misses. With the
+  // mass policy: the free slots, then the least cumulative attention mass (the masses are
+  // non-negative, so their fp32 bits order them; a free slot ranks above every block).
   int got = 0;
   if (M > 0) {
     int valid = 0;
     for (int s = tid; s < a.capacity; s += kPruneThreads) {
       const int st = a.slot_stamp[s];
-      vals[s] = st < step ? -st : INT_MIN;
+      int v = -st;
+      if (a.mass) {
+        const int key = a.slot_key[s] - 1;
+        const float w = key >= 0 ? a.mass[key] : 0.0f;
+        v = key < 0 ? 1 : -(w > 0.0f ? min(__float_as_int(w), 0x7F800000) : 0);
+      }
+      vals[s] = st < step ? v : INT_MIN;
       valid += st < step;
     }
 #pragma unroll
@@ -820,8 +850,13 @@ __global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePl
     a.fill[R + j] = make_int4(v, page, h, 0);
   }
   __syncthreads();
-  // two segments of one call on the same (page, head) (pages shared between sequences) are
-  // not supported: reported through the error word
+  // every alias takes the slot of the segment it repeats (a hit's, or a miss's just placed)
+  for (int f = f_lo; f < f_hi; f++) {
+    const int sv = a.seg_slot[f];
+    if (sv <= -2) a.seg_slot[f] = a.seg_slot[(f / a.seg_stride) * a.seg_stride + (-2 - sv)];
+  }
+  // two segments of one call on the same (page, head) otherwise (pages shared between
+  // sequences) are not supported: reported through the error word
   for (int j = tid; j < got; j += kPruneThreads) {
     const int v = victims[j];
     if (a.slot_of[a.slot_key[v] - 1] != v + 1) set_error(a.err, kDevErrCheck);
@@ -859,6 +894,7 @@ cudaError_t launch_cache_plan(const Shape& s, const int32_t* seq_lens, const int
   a.slot_of = c.slot_of;
   a.slot_key = c.slot_key;
   a.slot_stamp = c.slot_stamp;
+  a.mass = s.cache_policy == 1 ? c.mass : nullptr;
   a.seg_slot = seg_slot;
   a.fill = static_cast<int4*>(fill);
   a.n_fill = n_fill;

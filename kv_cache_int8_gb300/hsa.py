@@ -37,7 +37,8 @@ EXPORTS = (
     "hsa_workspace_bytes", "hsa_status_string", "hsa_quantize_keys", "hsa_append_kv",
     "hsa_score_blocks", "hsa_prune", "hsa_select", "hsa_attend", "dense_decode",
     "hsa_decode_step", "hsa_decode_step_reuse", "hsa_read_device_error", "hsa_select_noalloc",
-    "hsa_block_cache_bytes", "hsa_attend_cached", "hsa_decode_step_cached",
+    "hsa_block_cache_bytes", "hsa_block_cache_mass", "hsa_attend_cached",
+    "hsa_decode_step_cached",
 )
 
 
@@ -53,7 +54,8 @@ class hsa_dims(ctypes.Structure):
         "chunk", "block", "k1", "k2", "sink", "window")] + [
         ("sm_scale", ctypes.c_float), ("kv_on_host", ctypes.c_int32),
         ("chunk0", ctypes.c_int32), ("k0", ctypes.c_int32), ("key_bits", ctypes.c_int32),
-        ("per_head", ctypes.c_int32), ("key_fp8", ctypes.c_int32)]
+        ("per_head", ctypes.c_int32), ("key_fp8", ctypes.c_int32),
+        ("cache_policy", ctypes.c_int32)]
 
 
 class hsa_step_io(ctypes.Structure):
@@ -87,6 +89,7 @@ class Dims:
     key_bits: int = 0  # 4: 4-bit key codes, two per byte; 0 or 8: 8-bit
     per_head: int = 0  # 1: every query head selects its own blocks (rows = hq)
     key_fp8: int = 0  # 1: FP8 E4M3 key codes (8-bit layout), fp32 scores
+    cache_policy: int = 0  # block cache victims: 0 least recently used, 1 least cumulative mass
 
     def c(self) -> hsa_dims:
         """The C struct, built once per set of field values (every call of a step passes it)."""
@@ -94,7 +97,7 @@ class Dims:
                self.max_pages_per_seq, self.num_pages, self.chunk, self.block, self.k1,
                self.k2, self.sink, self.window, float(self.sm_scale),
                1 if self.kv_on_host else 0, self.chunk0, self.k0, self.key_bits, self.per_head,
-               self.key_fp8)
+               self.key_fp8, self.cache_policy)
         c = _DIMS_CACHE.get(key)
         if c is None:
             if len(_DIMS_CACHE) > 256:
@@ -132,6 +135,7 @@ def load(path: Optional[str] = None):
         "hsa_decode_step_reuse": (I32, [D, ctypes.POINTER(hsa_step_io), P, P, P, P, P, P, P, P,
                                         P, SZ, P]),
         "hsa_block_cache_bytes": (SZ, [D, I32]),
+        "hsa_block_cache_mass": (P, [D, P, I32]),
         "hsa_attend_cached": (I32, [D, P, P, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
         "hsa_decode_step_cached": (I32, [D, ctypes.POINTER(hsa_step_io), P, P, P, P, P, P, P, P,
                                          P, I32, P, SZ, P]),
@@ -309,6 +313,17 @@ def block_cache(d: Dims, capacity: int):
     if n == 0:
         raise HsaError("hsa_block_cache_bytes", HSA_ERR_INVALID_ARG, "capacity or shape rejected")
     return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+
+def block_cache_mass(d: Dims, cache, capacity: int):
+    """The block cache's cumulative attention masses: a float32 [num_pages][hkv] view into
+    `cache` (see hsa_block_cache_mass)."""
+    ptr = load().hsa_block_cache_mass(ctypes.byref(d.c()), _p(cache), capacity)
+    if not ptr:
+        raise HsaError("hsa_block_cache_mass", HSA_ERR_INVALID_ARG, "shape or capacity rejected")
+    off = ptr - cache.data_ptr()
+    n = d.num_pages * d.hkv
+    return cache[off: off + 4 * n].view(torch.float32).view(d.num_pages, d.hkv)
 
 
 def hsa_attend_cached(d: Dims, q, k_cache, v_cache, page_table, seq_lens, block_idx, n_blocks,

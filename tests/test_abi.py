@@ -91,6 +91,19 @@ def test_workspace_sizes(lib):
     host = dict(kv_on_host=True, k2=16, sink=64, window=256)
     assert lib.load().hsa_block_cache_bytes(_dims(lib, **host).c(), 4096) > 0
     assert lib.load().hsa_block_cache_bytes(_dims(lib, per_head=1, **host).c(), 4096) == 0
+    # cache policies: 0 least recently used, 1 least cumulative attention mass; the buffer
+    # holds the masses under both, and the cached workspace grows by the per-segment sums
+    lru, mass = _dims(lib, **host), _dims(lib, cache_policy=1, **host)
+    cache = lib.load().hsa_block_cache_bytes(lru.c(), 4096)
+    assert lib.load().hsa_block_cache_bytes(mass.c(), 4096) == cache
+    assert cache >= 4096 * 8192 + 2 * 8 * 8192 * 4  # data + slot_of + masses (8192 pages)
+    assert (lib.hsa_workspace_bytes(mass, lib.HSA_OP_CACHED) >
+            lib.hsa_workspace_bytes(lru, lib.HSA_OP_CACHED))
+    assert lib.hsa_workspace_bytes(_dims(lib, cache_policy=2, **host), lib.HSA_OP_CACHED) == 0
+    assert lib.load().hsa_block_cache_mass(mass.c(), None, 4096) is None  # null buffer
+    base = 1 << 20
+    off = lib.load().hsa_block_cache_mass(mass.c(), base, 4096) - base
+    assert 0 < off and off % 16 == 0 and off + 8 * 8192 * 4 <= cache
 
 
 @pytest.mark.parametrize("kw,code", [
