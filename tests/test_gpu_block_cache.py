@@ -239,14 +239,15 @@ def _check_mass_victims(prev_key, used, new_key, misses, mass, capacity):
             assert mr >= mv - 1e-5 * (1.0 + mv), (v, r, mv, mr)
 
 
-@pytest.mark.parametrize("sink,window", [(32, 64), (40, 72)])
-def test_block_cache_cumulative_mass_policy(sink, window):
+@pytest.mark.parametrize("sink,window,hq", [(32, 64, 8), (40, 72, 8), (40, 72, 2), (40, 72, 4),
+                                            (40, 72, 16)])
+def test_block_cache_cumulative_mass_policy(sink, window, hq):
     """HCAttention's reversible eviction read as a cache policy: the blocks with the least
     cumulative attention mass leave the cache first and stay in host memory. With a sink and
     window that end inside a page, some calls keep the two blocks that straddle them, so one
     block is two segments of a call (its masses must add up)."""
     cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None, context_range=(2000, 4000),
-                              batch=2, hq=8, hkv=2, k1=20, k2=12, sink=sink, window=window,
+                              batch=2, hq=hq, hkv=2, k1=20, k2=12, sink=sink, window=window,
                               paged_permuted=True)
     wl = W.make_workload(cfg, seed=93, host_pinned=True)
     hd, od = H.dims_pair(wl)
