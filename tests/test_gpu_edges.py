@@ -47,6 +47,20 @@ def test_mixed_batch_permuted_pages():
     _check(wl)
 
 
+@pytest.mark.parametrize("batch", [33, 300])
+def test_large_batch_of_short_sequences(batch):
+    """Many sequences (the scorer's per-CTA length and tile-prefix tables span several warp
+    passes; one prune CTA and a split-K grid per sequence and kv head), some of length 0."""
+    cfg = _cfg(context=None, context_range=(0, 900), batch=batch, hq=8, hkv=2, k1=4, k2=5,
+               sink=16, window=48, paged_permuted=True)
+    wl = W.make_workload(cfg, seed=batch)
+    for i in (3, batch - 1):
+        wl["seq_lens"][i] = 0
+        wl["lens"][i] = 0
+    g, _ = _check(wl, dense=False)
+    assert (g["n_blocks"][3] == 0).all() and (g["n_blocks"][batch - 1] == 0).all()
+
+
 def test_empty_sequence_in_a_batch():
     """A sequence of length 0 beside others: zero scales and codes, nothing selected, output
     0 and lse -inf for its heads; the other sequences as usual (dense decode too)."""
