@@ -506,7 +506,7 @@ def e2e_steps(case, steps: int):
     # the decode-loop form of the public call: arguments marshalled once per buffer set
     calls = [hsa.DecodeStep(case.d, q_h, kn_h, vn_h, out_h, lse_h, case.k[r], case.v[r],
                             case.kq[r], case.ks[r], case.pt, case.lens, None, None, case.ws_step,
-                            io_on_host=True) for r in range(2)]
+                            io_on_host=True, graph=True) for r in range(2)]
     times = []
     for i in range(steps + 3):
         r = i & 1
@@ -840,7 +840,8 @@ def main():
             "value": job_value(e2e_ms, world), "unit": "us/step", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "path": "hsa_decode_step (through hsa.DecodeStep, the decode-loop form of the "
-                    "binding: arguments marshalled once per buffer set) with pinned host "
+                    "binding: arguments marshalled once per buffer set, the step replayed from "
+                    "the CUDA graph it records on its first call) with pinned host "
                     "q/k_new/v_new/out/lse (mapped: a kernel stages the inputs, the attention "
                     "writes the outputs to host memory), synchronised per step"},
         "gpu_launches": 4 * args.steps,

@@ -274,25 +274,45 @@ class DecodeStep:
     """hsa_decode_step over a fixed set of buffers, for a decode loop that calls it every
     step: the C arguments are marshalled once, so a call costs the C call alone. The
     buffers' contents may change between calls (new q / k_new / v_new, longer seq_lens);
-    the buffers themselves must stay alive and in place."""
+    the buffers themselves must stay alive and in place.
+
+    graph=True: the first call runs the step and then records it into a CUDA graph; every
+    later call replays the graph on the current stream (one launch instead of one per
+    kernel). The kernels read every input from its buffer, so replays see new contents; the
+    descriptor and the buffers are those of the recording."""
 
     def __init__(self, d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_scale,
                  page_table, seq_lens, block_idx, n_blocks, ws, io_on_host: bool = False,
-                 stream=None):
+                 stream=None, graph: bool = False):
         self._keep = (q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_scale, page_table,
                       seq_lens, block_idx, n_blocks, ws)
         self._cd = d.c()
         self._io = hsa_step_io(_p(q), _p(k_new), _p(v_new), _p(out), _p(lse),
                                1 if io_on_host else 0)
         self._fn = load().hsa_decode_step
-        self._args = (ctypes.byref(self._cd), ctypes.byref(self._io), _p(k_cache), _p(v_cache),
+        self._head = (ctypes.byref(self._cd), ctypes.byref(self._io), _p(k_cache), _p(v_cache),
                       _p(kq), _p(k_scale), _p(page_table), _p(seq_lens), _p(block_idx),
-                      _p(n_blocks), _p(ws), ws.numel(), _stream(stream))
+                      _p(n_blocks), _p(ws), ws.numel())
+        self._args = self._head + (_stream(stream),)
+        self._use_graph = graph
+        self._graph = None
 
-    def __call__(self) -> None:
-        rc = self._fn(*self._args)
+    def _run(self, args) -> None:
+        rc = self._fn(*args)
         if rc != HSA_OK:
             _check("hsa_decode_step", rc)
+
+    def __call__(self) -> None:
+        if self._graph is not None:
+            self._graph.replay()
+            return
+        self._run(self._args)
+        if self._use_graph:
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):  # the step's launches, on the recording stream
+                self._run(self._head + (_stream(None),))
+            self._graph = g
 
 
 def hsa_decode_step_reuse(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache, kq, k_scale,

@@ -22,8 +22,9 @@ def _clone(t):
 
 
 def test_prepared_decode_step_equals_the_plain_call():
-    """hsa.DecodeStep (arguments marshalled once) gives the same bits as hsa_decode_step,
-    with host I/O, over several steps whose inputs change in place."""
+    """hsa.DecodeStep (arguments marshalled once), and the same replayed from a CUDA graph,
+    give the same bits as hsa_decode_step, with host I/O, over several steps whose inputs
+    change in place."""
     cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None,
                               context_range=(2000, 4000), batch=2, hq=8, hkv=2, k1=10, k2=8,
                               sink=32, window=64, paged_permuted=True)
@@ -38,7 +39,7 @@ def test_prepared_decode_step_equals_the_plain_call():
                           k_scale, hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
     gen = torch.Generator(device="cpu").manual_seed(9)
     res = []
-    for prepared in (False, True):
+    for mode in ("plain", "prepared", "graph"):
         kc, vc, kqc = dwl["k_cache"].clone(), dwl["v_cache"].clone(), kq.clone()
         q = torch.zeros((B, Hq, 128), dtype=torch.bfloat16).pin_memory()
         kn = torch.zeros((B, Hkv, 128), dtype=torch.bfloat16).pin_memory()
@@ -49,7 +50,8 @@ def test_prepared_decode_step_equals_the_plain_call():
         ws = hsa.workspace(hd, hsa.HSA_OP_STEP)
         args = (hd, q, kn, vn, out, lse, kc, vc, kqc, k_scale, dwl["page_table"], lens, None,
                 None, ws)
-        step = hsa.DecodeStep(*args, io_on_host=True) if prepared else None
+        step = (hsa.DecodeStep(*args, io_on_host=True, graph=mode == "graph")
+                if mode != "plain" else None)
         gen.manual_seed(9)
         outs = []
         for i in range(3):
@@ -58,7 +60,7 @@ def test_prepared_decode_step_equals_the_plain_call():
             vn.copy_(torch.randn((B, Hkv, 128), generator=gen).to(torch.bfloat16))
             if i:
                 lens.sub_(1)  # the step before: one token shorter, same buffers
-            if prepared:
+            if step is not None:
                 step()
             else:
                 hsa.hsa_decode_step(*args, io_on_host=True)
@@ -66,10 +68,11 @@ def test_prepared_decode_step_equals_the_plain_call():
             assert hsa.hsa_read_device_error(ws) == 0
             outs.append((out.clone(), lse.clone()))
         res.append((outs, kc, vc, kqc))
-    for (o1, l1), (o2, l2) in zip(res[0][0], res[1][0]):
-        assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    for a, b in zip(res[0][1:], res[1][1:]):
-        assert torch.equal(a, b)
+    for other in res[1:]:
+        for (o1, l1), (o2, l2) in zip(res[0][0], other[0]):
+            assert torch.equal(o1, o2) and torch.equal(l1, l2)
+        for a, b in zip(res[0][1:], other[1:]):
+            assert torch.equal(a, b)
 
 
 @pytest.mark.parametrize("refresh,on_host,key_bits,per_head,fp8", [
