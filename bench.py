@@ -652,6 +652,7 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
+    from kv_cache_int8_gb300 import workloads as W
     budget = float(os.environ.get("HSA_REF_BUDGET_S", "20"))
     us, n, cores, desc, us_1 = oracle_step_sample(args.config, 0, budget, max(1, args.steps),
                                                   warmup=args.warmup)
@@ -661,7 +662,7 @@ def run_reference(args, world, rank):
         "ms_per_step": us / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "int8+f64",
         "data": "synthetic (seeded)", "impl": "reference",
-        "config": {"workload": args.config},
+        "config": {"workload": workload_text(W.CONFIGS[args.config])},
         "cpu_baseline": {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle",
                          "sample": desc, "one_thread_us": us_1},
         "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
