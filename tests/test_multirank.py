@@ -46,3 +46,24 @@ def test_single_rank_is_plain():
     import bench
     assert bench.reduce_max(1.25, 1) == 1.25
     assert bench.job_value(0.1, 1) == pytest.approx(100.0)
+
+
+def test_reference_arm_runs_on_rank_zero_only(capsys, monkeypatch):
+    """The reference arm (the CPU oracle) prints one JSON line on rank 0 and nothing on the
+    other ranks, with the main arm's metric, unit and workload text."""
+    import argparse
+    import json
+
+    import bench
+    from kv_cache_int8_gb300 import workloads as W
+    monkeypatch.setenv("HSA_REF_BUDGET_S", "0.5")
+    args = argparse.Namespace(config="tiny-8k", steps=2, warmup=0, gpus=2)
+    assert bench.run_reference(args, 2, 1) == 0
+    assert capsys.readouterr().out == ""
+    assert bench.run_reference(args, 2, 0) == 0
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "us/step" and line["higher_is_better"] is False
+    assert line["config"]["workload"] == bench.workload_text(W.CONFIGS["tiny-8k"])
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
