@@ -170,3 +170,24 @@ def test_prune_rejects_too_many_chunks(lib):
     with pytest.raises(lib.HsaError) as e:
         lib.hsa_prune(d, ok, ok, None, None, None, ok, ok, stream=0)
     assert e.value.code == lib.HSA_ERR_UNSUPPORTED
+
+
+def _header_struct_fields(name):
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    body = re.search(r"typedef struct %s \{(.*?)\} %s;" % (name, name), text, flags=re.S).group(1)
+    fields = re.finditer(r"(?:const\s+)?(int32_t|float|void)\s*(\*?)\s*(\w+);", body)
+    return [("ptr" if m.group(2) else m.group(1), m.group(3)) for m in fields]
+
+
+@pytest.mark.parametrize("struct", ["hsa_dims", "hsa_step_io"])
+def test_binding_structs_match_the_header(struct):
+    """The ctypes structures of the binding declare the header's fields, in order, with
+    the same C types (a field added on one side only would shift every later one)."""
+    from kv_cache_int8_gb300 import hsa
+    ctype = {"int32_t": ctypes.c_int32, "float": ctypes.c_float, "ptr": ctypes.c_void_p}
+    want = _header_struct_fields(struct)
+    got = getattr(hsa, struct)._fields_
+    assert [n for n, _ in got] == [n for _, n in want]
+    for (gn, gt), (wt, wn) in zip(got, want):
+        assert gt is ctype[wt], gn
