@@ -336,18 +336,22 @@ int32_t hsa_decode_step_cached(const hsa_dims* d, const hsa_step_io* io, void* k
  * embedded in a host program that owns every device allocation through its own pool, or
  * that runs on a latency-critical path where cudaMalloc (which can synchronise the device)
  * is not allowed. Nothing in the method calls for this; the pages have no counterpart.
- * Same arguments and results as hsa_select minus the workspace. Its scratch (block and
- * tile score maxima) is one fixed 4 MiB device array inside the library, held by every GPU
- * that loads the library until the process exits: shapes with
- *   round256(4 * batch * hkv * max_pages_per_seq)
- *   + round256(4 * batch * hkv * ceil(max_pages_per_seq / 4)) > 4 MiB
- * (e.g. more than about 800K 16-token blocks summed over sequences and kv heads) return
- * HSA_ERR_WORKSPACE_TOO_SMALL. The array's device address is looked up on the first call on
- * each device (make that first call before any stream capture). All calls share the array
- * and it keeps the last call's contents (each call writes every entry it then reads, so
- * nothing needs clearing); calls that may overlap on the GPU, on any stream, race on it and
- * must be ordered by the caller. Device-side bounds-check failures are skipped but not
- * reported (there is no error word). Calls no allocating routine.
+ * Same arguments and results as hsa_select minus the workspace. Its scratch (a device error
+ * word, then the block and tile score maxima) is one fixed 4 MiB device array inside the
+ * library, held by every GPU that loads the library until the process exits: shapes with
+ *   256 + round256(4 * batch * rows * max_pages_per_seq)
+ *       + round256(4 * batch * rows * ceil(max_pages_per_seq / 4)) > 4 MiB,
+ * rows = hq with per-head selection (d->per_head = 1), else hkv (e.g. more than about 800K
+ * 16-token blocks summed over sequences and kv heads, G times fewer with per-head
+ * selection), return HSA_ERR_WORKSPACE_TOO_SMALL. The first call on a device loads the
+ * library's device code there (make it before any stream capture); every call looks the
+ * array's device address up in the current context. All calls share the array and it keeps
+ * the last call's contents (each call writes every maximum it then reads, so only the error
+ * word must start at zero, which it does); calls that may overlap on the GPU, on any
+ * stream, race on it and must be ordered by the caller. Device-side failures (a bounds
+ * check, or a bounded wait that ran out, after which the selection may be stale) set the
+ * array's error word: read and clear it with hsa_read_device_error(NULL, stream, &code).
+ * Calls no allocating routine.
  */
 int32_t hsa_select_noalloc(const hsa_dims* d, const void* q, const int8_t* kq,
                            const float* k_scale, const int32_t* page_table,
@@ -356,8 +360,9 @@ int32_t hsa_select_noalloc(const hsa_dims* d, const void* q, const int8_t* kq,
 
 /*
  * Reads and clears the device error word of `workspace` after synchronising `stream`:
- * *code receives HSA_OK, HSA_ERR_TIMEOUT or HSA_ERR_DEVICE_CHECK. This is the one call
- * that synchronises.
+ * *code receives HSA_OK, HSA_ERR_TIMEOUT or HSA_ERR_DEVICE_CHECK. workspace NULL: the error
+ * word of hsa_select_noalloc's fixed scratch array on the current device. This is the one
+ * call that synchronises.
  */
 int32_t hsa_read_device_error(void* workspace, void* stream, int32_t* code);
 

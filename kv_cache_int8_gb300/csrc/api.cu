@@ -341,6 +341,25 @@ int32_t kv_pointer(const hsa_dims* d, const void* p, const void** out) {
   return HSA_OK;
 }
 
+// The scratch of hsa_select_noalloc: one fixed 4 MiB array of device memory that every GPU
+// loading the library holds until the process exits (word 0: its device error word).
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+__device__ __align__(256) static unsigned char g_select_scratch[kNoAllocScratchBytes];
+
+// Device address of g_select_scratch in the current device's context. Host code sees only a
+// stand-in for the array, never its device address; the lookup is a host-side table lookup
+// once the library's device code is loaded (the first lookup on a device loads it), and is
+// made on every call so that it always matches the current context.
+int32_t noalloc_scratch(char** out) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return HSA_ERR_CUDA;
+  }
+  *out = static_cast<char*>(p);
+  return HSA_OK;
+}
+
 inline int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? HSA_OK : HSA_ERR_CUDA; }
 
 inline cudaStream_t as_stream(void* p) { return reinterpret_cast<cudaStream_t>(p); }
@@ -722,6 +741,21 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
                               k_scale, page_table, seq_lens, err, st, true);
     if (e != cudaSuccess) return HSA_ERR_CUDA;
   }
+  // K/V in device memory: the sparse attention runs both pruning modules itself when they
+  // fit its shared memory (no pruning kernel, no kept-block list round trip in between)
+  const Shape sa = attend_shape(s, false);
+  if (block_cache == nullptr && !d->kv_on_host &&
+      hsa::attend_select_supported(sa, aligned(page_table, 16))) {
+    hsa::AttendBuffers buf;
+    buf.counters = reinterpret_cast<int*>(ws + l.att.counters);
+    buf.part_ml = reinterpret_cast<float*>(ws + l.att.part_ml);
+    buf.part_o = reinterpret_cast<float*>(ws + l.att.part_o);
+    buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(sa, false, false, num_sms(), false));
+    e = hsa::launch_attend_select(sa, q, kd, vd, page_table, seq_lens, bm, tm, bidx, nb, out,
+                                  lse, buf, err, st);
+    if (e != cudaSuccess) return HSA_ERR_CUDA;
+    return copy_outputs_back(s, io, out, lse, direct_out, st);
+  }
   // the prune also resolves the kept blocks' pages, so the attend needs one round trip for them
   int32_t* sel_pages = reinterpret_cast<int32_t*>(ws + l.sel_pages);
   e = hsa::launch_prune(prune_shape(s), seq_lens, bm, tm, nullptr, nullptr, bidx, nb, page_table,
@@ -811,8 +845,14 @@ int32_t hsa_decode_step_reuse(const hsa_dims* d, const hsa_step_io* io, void* k_
 }
 
 int32_t hsa_read_device_error(void* workspace, void* stream, int32_t* code) {
-  if (workspace == nullptr || code == nullptr || !aligned(workspace, kAlign))
-    return HSA_ERR_INVALID_ARG;
+  if (code == nullptr) return HSA_ERR_INVALID_ARG;
+  if (workspace == nullptr) {  // the error word of hsa_select_noalloc
+    char* scratch = nullptr;
+    const int32_t rc = noalloc_scratch(&scratch);
+    if (rc != HSA_OK) return rc;
+    workspace = scratch;
+  }
+  if (!aligned(workspace, kAlign)) return HSA_ERR_INVALID_ARG;
   cudaStream_t st = as_stream(stream);
   int v = 0;
   if (cudaStreamSynchronize(st) != cudaSuccess) return HSA_ERR_CUDA;
@@ -825,39 +865,8 @@ int32_t hsa_read_device_error(void* workspace, void* stream, int32_t* code) {
 
 // ---------------------------------------------------------------------------------------
 // hsa_select_noalloc: hsa_select for callers that cannot allocate device memory. Its
-// scratch (the per-block and per-tile score maxima) lives in one fixed array that every
-// GPU loading this library holds until the process exits.
-
-}  // extern "C"
-
-namespace {
-
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
-__device__ __align__(256) static unsigned char g_select_scratch[kNoAllocScratchBytes];
-
-// Device address of g_select_scratch on the current device, looked up once per device
-// (host code only sees a stand-in for the array, never its device address).
-int32_t noalloc_scratch(char** out) {
-  static std::mutex mu;
-  static char* addr[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return HSA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return HSA_ERR_CUDA;
-    }
-    addr[dev] = static_cast<char*>(p);
-  }
-  *out = addr[dev];
-  return HSA_OK;
-}
-
-}  // namespace
-
-extern "C" {
+// scratch (an error word, then the per-block and per-tile score maxima) lives in one fixed
+// array that every GPU loading this library holds until the process exits.
 
 int32_t hsa_select_noalloc(const hsa_dims* d, const void* q, const int8_t* kq,
                            const float* k_scale, const int32_t* page_table,
@@ -871,22 +880,22 @@ int32_t hsa_select_noalloc(const hsa_dims* d, const void* q, const int8_t* kq,
   if (!aligned(q, 16) || !aligned(kq, 16) || !aligned(k_scale, 16)) return HSA_ERR_INVALID_ARG;
   rc = check_prune_fits(s);
   if (rc != HSA_OK) return rc;
-  // block maxima then tile maxima, as in the select workspace (without its error word)
-  if (select_bm_bytes(s) + select_tm_bytes(s) > kNoAllocScratchBytes)
-    return HSA_ERR_WORKSPACE_TOO_SMALL;
+  // the select workspace's layout: error word, block maxima, tile maxima
+  if (select_ws(s) > kNoAllocScratchBytes) return HSA_ERR_WORKSPACE_TOO_SMALL;
   char* scratch = nullptr;
   rc = noalloc_scratch(&scratch);
   if (rc != HSA_OK) return rc;
-  int32_t* bm = reinterpret_cast<int32_t*>(scratch);
-  int32_t* tm = reinterpret_cast<int32_t*>(scratch + select_bm_bytes(s));
+  int* err = reinterpret_cast<int*>(scratch);
+  int32_t* bm = reinterpret_cast<int32_t*>(scratch + kErrBytes);
+  int32_t* tm = reinterpret_cast<int32_t*>(scratch + kErrBytes + select_bm_bytes(s));
   cudaStream_t st = as_stream(stream);
-  // Every entry of the scratch that the prune kernel reads is written by the scorer in the
-  // same call, so nothing has to be cleared; device-side check failures are skipped, not
-  // reported (there is no error word).
-  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, nullptr, st);
+  // Every entry of the maxima that the prune kernel reads is written by the scorer in the
+  // same call, so only the error word has to start at zero: it does (static device memory
+  // starts zeroed) and hsa_read_device_error(NULL, ...) clears it after reading it.
+  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st);
   if (rc != HSA_OK) return rc;
   return cuda_status(hsa::launch_prune(prune_shape(s), seq_lens, bm, tm, chunk_idx, n_chunks,
-                                       block_idx, n_blocks, nullptr, nullptr, nullptr, st));
+                                       block_idx, n_blocks, nullptr, nullptr, err, st));
 }
 
 }  // extern "C"

@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "select.cuh"
 
 // Split-K grid sizing (CTAs per SM); overridable at build time for tuning.
 #ifndef HSA_SPARSE_CTAS_PER_SM
@@ -50,6 +51,11 @@
 #ifndef HSA_SPARSE_RESERVE
 #define HSA_SPARSE_RESERVE 1
 #endif
+// The whole decode step runs the pruning modules inside the sparse attention (0: a pruning
+// kernel, then the sparse attention, as hsa_select + hsa_attend).
+#ifndef HSA_FUSED_SELECT
+#define HSA_FUSED_SELECT 1
+#endif
 
 namespace hsa {
 namespace {
@@ -66,6 +72,7 @@ constexpr int kSlotBytes = 2 * kBlockBytesBf16;  // K page + V page of one head
 constexpr int kHostThreads = kCompute;
 static_assert(kHostThreads * 16 * 2 == kBlockBytesBf16, "a host-path segment copy: 2 x 16 B a thread");
 constexpr int kMaxSplits = 64;
+constexpr int kTileBlocksSel = 4;              // blocks per 64-token chunk (a scorer tile)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNeg = -FLT_MAX;                 // "no token" score
@@ -701,6 +708,65 @@ __device__ __forceinline__ void warp_segment(WarpState<G>& st, const float (&qf)
   __syncwarp();  // the next segment rewrites the scratch
 }
 
+// The W compute warps' running states merged into one per head (o[j][d] = sum over warps of
+// acc_w * 2^(m_w - M_j), l likewise), then the CTA's output or split partial and the combine
+// (finish_common). Called by all threads after a CTA barrier; `ring` (the K/V ring, no
+// longer in use) holds the merge area, `mstate` [2][W][H] floats.
+template <int G, int W, int NB, bool MASS>
+__device__ __forceinline__ void merge_warps(const AttArgs& a, const WarpState<G>& st,
+                                            uint8_t* ring, float* mstate, int b, int h,
+                                            int split) {
+  constexpr int H = head_slots(G);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // merge the warps: o[j][d] = sum_w acc_w * 2^(m_w - M_j), l likewise
+  float* o = reinterpret_cast<float*>(ring);  // [W][G][128], then the merged [G][128]
+  float* mw = mstate;                          // [W][H] max, then [W][H] sum
+  float* lw = mstate + W * H;
+  if (warp < W) {
+    const int sl = lane & 7;
+    constexpr int kOwners = 8 / G;
+    int hidx = 0;
+    if constexpr (G == 8) hidx = sl;
+    if constexpr (G == 4) hidx = ((sl & 4) ? 2 : 0) + ((sl & 2) ? 1 : 0);
+    if constexpr (G == 2) hidx = (sl & 4) ? 1 : 0;
+    if (lane < 8 && (sl & (kOwners - 1)) == 0) {
+      mw[warp * H + hidx] = st.m;
+      lw[warp * H + hidx] = st.l;
+    }
+#pragma unroll
+    for (int j = 0; j < G; j++)
+      *reinterpret_cast<float4*>(o + (warp * G + j) * kHeadDim + 4 * lane) =
+          make_float4(st.acc[j][0], st.acc[j][1], st.acc[j][2], st.acc[j][3]);
+  }
+  __syncthreads();
+  float* mo = o + W * G * kHeadDim;  // merged [G][128]
+  float* mm = mo + G * kHeadDim;          // [H]
+  float* ml = mm + H;                     // [H]
+  if (tid < W * 32) {
+    for (int x = tid; x < G * kHeadDim; x += W * 32) {
+      const int j = x / kHeadDim, d = x % kHeadDim;
+      float M = kNeg;
+#pragma unroll
+      for (int w = 0; w < W; w++) M = fmaxf(M, mw[w * H + j]);
+      float O = 0.0f, L = 0.0f;
+#pragma unroll
+      for (int w = 0; w < W; w++) {
+        const float lv = lw[w * H + j];
+        const float wt = lv > 0.0f ? exp2f(mw[w * H + j] - M) : 0.0f;
+        O = fmaf(o[(w * G + j) * kHeadDim + d], wt, O);
+        L = fmaf(lv, wt, L);
+      }
+      mo[x] = O;
+      if (d == 0) {
+        mm[j] = M;
+        ml[j] = L;
+      }
+    }
+  }
+  __syncthreads();
+  finish_common<G, NB, MASS>(a, b, h, split, mo, mm, ml, o, W * 32);
+}
+
 // W compute warps and NS ring slots (NS a multiple of W): the sparse path uses 8 warps and 16
 // slots, enough for every segment of a CTA to be in flight at once; dense decode uses 4 and 8
 // with three CTAs per SM.
@@ -888,53 +954,372 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
   }
   grid_dep_wait();  // completion of this grid implies completion of the previous one
   __syncthreads();
-  // merge the warps: o[j][d] = sum_w acc_w * 2^(m_w - M_j), l likewise
-  float* o = reinterpret_cast<float*>(ring);  // [W][G][128], then the merged [G][128]
-  float* mw = mstate;                          // [W][H] max, then [W][H] sum
-  float* lw = mstate + W * H;
-  if (warp < W) {
-    const int sl = lane & 7;
-    constexpr int kOwners = 8 / G;
-    int hidx = 0;
-    if constexpr (G == 8) hidx = sl;
-    if constexpr (G == 4) hidx = ((sl & 4) ? 2 : 0) + ((sl & 2) ? 1 : 0);
-    if constexpr (G == 2) hidx = (sl & 4) ? 1 : 0;
-    if (lane < 8 && (sl & (kOwners - 1)) == 0) {
-      mw[warp * H + hidx] = st.m;
-      lw[warp * H + hidx] = st.l;
+  merge_warps<G, W, DENSE ? 8 : 16, MASS>(a, st, ring, mstate, b, h, split);
+}
+
+// ------------------------------------ sparse attention that runs the pruning modules itself
+//
+// The whole decode step's sparse attention for 64-token chunks: every CTA of (sequence b,
+// row h) runs both pruning modules on the scorer's tile maxima (the chunk scores) and block
+// maxima itself, so neither a pruning kernel nor a round trip for its kept-block list stands
+// between the scorer and the attention. The CTAs of a row take the same deterministic steps
+// on the same data and agree on the selection; split 0 writes it out for the caller.
+//
+// Order inside a CTA: the sink and window pages (inputs of the step, except the page that
+// holds the newest token, which the append beside the scorer writes) are copied before the
+// wait for the scorer, and so is the row of page ids when it fits; after the wait the tile
+// maxima (and the row of block maxima when it fits) are staged, all warps select (module 1:
+// top-K1 chunks; module 2: top-K2 blocks of those chunks, select.cuh), the producer issues
+// the kept blocks' copies, and the compute warps process the CTA's segments as in the HBM
+// path above.
+struct SelArgs {
+  const int32_t* block_max;  // [rows][max_pages]
+  const int32_t* tile_max;   // [rows][max_tiles]
+  int32_t* block_idx;        // [rows][k2] out (split 0): kept blocks ascending, -1 padded
+  int32_t* n_blocks;         // [rows] out (split 0)
+  int max_tiles, k1;
+  int a_cap;   // ints of area A: the tile maxima, then module 2's values and block ids
+  int n2_cap;  // module 2's candidates (4 blocks per kept chunk)
+  int k1_cap, k2_cap;
+  int row_cap;   // > 0: the row of block maxima is staged (ints)
+  int prow_cap;  // > 0: the row of page ids is staged (ints)
+};
+
+// Byte offsets of the kernel's dynamic shared memory (after 128-byte alignment).
+struct SelSmem {
+  size_t full, sbar, wscr, mstate, meta, ss, area, kept1, selb, selp, brow, prow, end;
+};
+
+template <int G, int W, int NS>
+__host__ __device__ SelSmem sel_smem_layout(const SelArgs& sa) {
+  constexpr int H = head_slots(G);
+  SelSmem l;
+  size_t o = (size_t)NS * kSlotBytes;  // the K/V ring
+  l.full = o;                          // full [NS], empty [NS]
+  o += 2 * NS * sizeof(uint64_t);
+  l.sbar = o;  // staging barriers: tile maxima, block-maxima row, page row
+  o += 4 * sizeof(uint64_t);
+  l.wscr = o;
+  o += W * sizeof(WarpScratch<H>);
+  l.mstate = o;
+  o += 2 * W * H * sizeof(float);
+  o = (o + 15) / 16 * 16;
+  l.meta = o;
+  o += NS * sizeof(int4);
+  l.ss = o;
+  o += (sizeof(SelectShared) + 15) / 16 * 16;
+  l.area = o;
+  o += (size_t)sa.a_cap * 4;
+  l.kept1 = o;
+  o += (size_t)sa.k1_cap * 4;
+  l.selb = o;
+  o += (size_t)sa.k2_cap * 4;
+  l.selp = o;
+  o += (size_t)sa.k2_cap * 4;
+  l.brow = o;
+  o += sa.row_cap > 0 ? ((size_t)sa.row_cap + 4) * 4 : 0;
+  l.prow = o;
+  o += sa.prow_cap > 0 ? ((size_t)sa.prow_cap + 4) * 4 : 0;
+  l.end = o;
+  return l;
+}
+
+template <int G, int W, int NS>
+__global__ void __launch_bounds__((W + 1) * 32, 1)
+    attend_select_kernel(const AttArgs a, const SelArgs sa) {
+  static_assert(NS % W == 0 && NS <= 32, "each compute warp owns fixed ring slots; one batch");
+  constexpr int NT = (W + 1) * 32;
+  constexpr int P = kTileBlocksSel;  // blocks per 64-token chunk
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  const SelSmem L = sel_smem_layout<G, W, NS>(sa);
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+  uint64_t* empty = full + NS;
+  uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.sbar);
+  WarpScratch<head_slots(G)>* wscr = reinterpret_cast<WarpScratch<head_slots(G)>*>(smem + L.wscr);
+  float* mstate = reinterpret_cast<float*>(smem + L.mstate);
+  int4* meta = reinterpret_cast<int4*>(smem + L.meta);
+  SelectShared& ss = *reinterpret_cast<SelectShared*>(smem + L.ss);
+  int* area = reinterpret_cast<int*>(smem + L.area);
+  int* kept1 = reinterpret_cast<int*>(smem + L.kept1);
+  int* selb = reinterpret_cast<int*>(smem + L.selb);
+  int* selp = reinterpret_cast<int*>(smem + L.selp);
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_dep_launch();
+  const int n_raw = a.seq_lens[b];
+  const bool bad_len = n_raw < 0 || n_raw > a.max_pages * kPage;
+  if (tid == 0 && split == 0 && h == 0 && bad_len) set_error(a.err, kDevErrCheck);
+  Segments S = make_segments<false>(a, b, h);
+  const int first = split, stride = a.nsplit;
+  const int cnt = S.total > split ? (S.total - split + stride - 1) / stride : 0;
+  const int n_sw = S.n_sink + S.n_win;
+  const int n_pre = n_sw <= first ? 0 : min(cnt, (n_sw - first + stride - 1) / stride);
+  // the page of the newest token is written by the append running beside the scorer: its
+  // copy waits for the scorer (whose completion the append's waits for)
+  const int i_last = S.n_win > 0 ? n_sw - 1 : (S.n_sink > 0 && S.sink_end == S.n ? S.n_sink - 1 : -1);
+  const int j_def = (i_last >= first && (i_last - first) % stride == 0) ? (i_last - first) / stride : -1;
+  const int jA = min(n_pre, NS);  // local segments [0, jA) but j_def go out before the wait
+
+  // candidate region in blocks and chunks
+  int k_lo = 0, k_hi = 0, c_lo = 0, n1 = 0;
+  if (S.cand_hi > a.sink && !bad_len) {
+    k_lo = a.sink / kPage;
+    k_hi = (S.cand_hi + kPage - 1) / kPage;
+    c_lo = k_lo / P;
+    n1 = (k_hi + P - 1) / P - c_lo;
+  }
+  const size_t row = (size_t)b * a.hkv + h;
+  const bool use_row = sa.row_cap > 0;
+  const bool use_prow = sa.prow_cap > 0;
+  const StagedRow t_plan = plan_row(area, sa.tile_max + row * sa.max_tiles + c_lo, n1);
+  const StagedRow r_plan =
+      plan_row(reinterpret_cast<int*>(smem + L.brow), sa.block_max + row * a.max_pages + k_lo,
+               use_row ? k_hi - k_lo : 0);
+  const StagedRow p_plan =
+      plan_row(reinterpret_cast<int*>(smem + L.prow), a.page_table + (size_t)b * a.max_pages + k_lo,
+               use_prow ? k_hi - k_lo : 0);
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 3; s++) mbar_init(&sbar[s], 1);
+    fence_barrier_init();
+  }
+  sel_init<NT>(ss);
+  __syncthreads();
+
+  const uint64_t policy = l2_evict_first_policy();  // each K/V page is read once
+  auto issue = [&](int s, int page) {  // the K and V pages of one segment into ring slot s
+    if (page >= 0) {
+      const size_t off = ((size_t)page * a.kv_heads + h / a.kv_div) * kPage * kHeadDim;
+      mbar_arrive_expect_tx(&full[s], kSlotBytes);
+      bulk_load_hint(ring + s * kSlotBytes, a.k + off, kBlockBytesBf16, &full[s], policy);
+      bulk_load_hint(ring + s * kSlotBytes + kBlockBytesBf16, a.v + off, kBlockBytesBf16, &full[s],
+                     policy);
+    } else {
+      mbar_arrive(&full[s]);
+    }
+  };
+  // segment i of the CTA's rows: (k, t0, t1) and its page (-1: nothing to read)
+  auto resolve = [&](int i, int& k, int& t0, int& t1) -> int {
+    int page = -1;
+    if (i < n_sw) {
+      segment_at(S, i, a.sink, k, t0, t1);
+      if (t0 < t1) page = __ldg(a.page_table + (size_t)b * a.max_pages + k);
+    } else {
+      kept_segment(S, i - n_sw, i - n_sw < S.n_sel ? selb[i - n_sw] : -1, a.sink, k, t0, t1);
+      if (t0 < t1)
+        page = use_prow ? selp[i - n_sw] : __ldg(a.page_table + (size_t)b * a.max_pages + k);
+    }
+    if (t0 < t1 && (page < 0 || page >= a.num_pages)) {
+      set_error(a.err, kDevErrCheck);
+      page = -1;
+    }
+    if (page < 0) t0 = t1 = 0;
+    return page;
+  };
+
+  // ---- before the wait: the page row (an input) and the sink / window copies
+  if (warp == W) {
+    if (lane == 0 && use_prow && p_plan.bytes() > 0) {
+      mbar_arrive_expect_tx(&sbar[2], p_plan.bytes());
+      issue_row(p_plan, &sbar[2]);
+    }
+    if (lane < jA && lane != j_def) {
+      int k = 0, t0 = 0, t1 = 0;
+      const int page = resolve(first + lane * stride, k, t0, t1);
+      meta[lane] = make_int4(k, t0, t1, 0);
+      issue(lane, page);
+    }
+  }
+  if (use_prow) tail_row<NT>(p_plan);
+
+  grid_dep_wait();  // the scorer's maxima and the appended token are complete
+
+  // ---- stage the chunk scores (and the row of block maxima)
+  if (tid == 0) {
+    if (t_plan.bytes() > 0) {
+      mbar_arrive_expect_tx(&sbar[0], t_plan.bytes());
+      issue_row(t_plan, &sbar[0]);
+    }
+    if (use_row && r_plan.bytes() > 0) {
+      mbar_arrive_expect_tx(&sbar[1], r_plan.bytes());
+      issue_row(r_plan, &sbar[1]);
+    }
+  }
+  tail_row<NT>(t_plan);
+  if (use_row) tail_row<NT>(r_plan);
+  if (t_plan.bytes() > 0 && !mbar_wait(&sbar[0], 0)) set_error(a.err, kDevErrTimeout);
+  __syncthreads();  // the plain-load tails are visible
+
+  // ---- module 1: top-K1 chunks (ascending)
+  const int* tiles = t_plan.dst();
+  int got1 = 0;
+  const int keep1 = min(sa.k1, n1);
+  if (keep1 > 0) {
+    int T = INT_MIN, need_eq = 0, eq_total = 0;
+    if (keep1 < n1) {
+      const int3 r = sel_kth_largest<NT>(tiles, n1, keep1, ss, false, 0, 0);
+      T = r.x;
+      need_eq = r.y;
+      eq_total = r.z;
+    }
+    got1 = sel_collect<NT>(tiles, n1, T, need_eq, eq_total, ss, kept1, c_lo);
+  }
+
+  // ---- module 2: the kept chunks' blocks (outside the candidate region: placeholders never
+  // kept), top-K2, ascending
+  if (use_row && r_plan.bytes() > 0 && !mbar_wait(&sbar[1], 0)) set_error(a.err, kDevErrTimeout);
+  const int* brow = r_plan.dst();
+  const int32_t* bm = sa.block_max + row * a.max_pages;
+  int* vals2 = area;  // the tile maxima are no longer read (the collect ended on a barrier)
+  int* cand2 = area + sa.n2_cap;
+  const int n2 = got1 * P;
+  int valid = 0, mn2 = INT_MAX, mx2 = INT_MIN;
+  for (int x0 = tid; x0 < n2; x0 += 4 * NT) {
+    int v[4], kk[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int x = x0 + u * NT;
+      kk[u] = x < n2 ? kept1[x / P] * P + x % P : -1;
+      const bool in = kk[u] >= k_lo && kk[u] < k_hi;
+      v[u] = in ? (use_row ? brow[kk[u] - k_lo] : __ldcg(bm + kk[u])) : INT_MIN;
     }
 #pragma unroll
-    for (int j = 0; j < G; j++)
-      *reinterpret_cast<float4*>(o + (warp * G + j) * kHeadDim + 4 * lane) =
-          make_float4(st.acc[j][0], st.acc[j][1], st.acc[j][2], st.acc[j][3]);
-  }
-  __syncthreads();
-  float* mo = o + W * G * kHeadDim;  // merged [G][128]
-  float* mm = mo + G * kHeadDim;          // [H]
-  float* ml = mm + H;                     // [H]
-  if (tid < W * 32) {
-    for (int x = tid; x < G * kHeadDim; x += W * 32) {
-      const int j = x / kHeadDim, d = x % kHeadDim;
-      float M = kNeg;
-#pragma unroll
-      for (int w = 0; w < W; w++) M = fmaxf(M, mw[w * H + j]);
-      float O = 0.0f, L = 0.0f;
-#pragma unroll
-      for (int w = 0; w < W; w++) {
-        const float lv = lw[w * H + j];
-        const float wt = lv > 0.0f ? exp2f(mw[w * H + j] - M) : 0.0f;
-        O = fmaf(o[(w * G + j) * kHeadDim + d], wt, O);
-        L = fmaf(lv, wt, L);
-      }
-      mo[x] = O;
-      if (d == 0) {
-        mm[j] = M;
-        ml[j] = L;
+    for (int u = 0; u < 4; u++) {
+      const int x = x0 + u * NT;
+      if (x < n2) {
+        cand2[x] = kk[u];
+        vals2[x] = v[u];
+        if (v[u] != INT_MIN) {
+          valid++;
+          mn2 = min(mn2, v[u]);
+          mx2 = max(mx2, v[u]);
+        }
       }
     }
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    valid += __shfl_xor_sync(0xffffffffu, valid, off);
+    mn2 = min(mn2, __shfl_xor_sync(0xffffffffu, mn2, off));
+    mx2 = max(mx2, __shfl_xor_sync(0xffffffffu, mx2, off));
+  }
+  if (lane == 0) {
+    ss.wsum[warp] = valid;
+    ss.mn[warp] = mn2;
+    ss.mx[warp] = mx2;
+  }
   __syncthreads();
-  finish_common<G, DENSE ? 8 : 16, MASS>(a, b, h, split, mo, mm, ml, o, W * 32);
+  int n2_valid = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; w++) {
+    n2_valid += ss.wsum[w];
+    mn2 = min(mn2, ss.mn[w]);
+    mx2 = max(mx2, ss.mx[w]);
+  }
+  const int keep2 = min(a.k2, n2_valid);
+  int got2 = 0;
+  if (keep2 > 0) {
+    int T = INT_MIN, need_eq = 0, eq_total = 0;
+    if (keep2 < n2_valid) {
+      const int3 r = sel_kth_largest<NT>(vals2, n2, keep2, ss, true, mn2, mx2);
+      T = r.x;
+      need_eq = r.y;
+      eq_total = r.z;
+    }
+    got2 = sel_collect<NT>(vals2, n2, T, need_eq, eq_total, ss, selb, 0);  // positions
+  } else {
+    __syncthreads();  // every thread has read the per-warp totals
+  }
+  if (use_prow && p_plan.bytes() > 0 && !mbar_wait(&sbar[2], 0)) set_error(a.err, kDevErrTimeout);
+  const int* prow = p_plan.dst();
+  for (int i = tid; i < got2; i += NT) {
+    const int kk = cand2[selb[i]];
+    selb[i] = kk;
+    selp[i] = use_prow ? prow[kk - k_lo] : -1;
+  }
+  __syncthreads();
+  if (split == 0) {
+    for (int i = tid; i < a.k2; i += NT) sa.block_idx[row * a.k2 + i] = i < got2 ? selb[i] : -1;
+    if (tid == 0) sa.n_blocks[row] = got2;
+  }
+  S.n_sel = min(got2, S.n_sel_max);
+
+  WarpState<G> st;
+#pragma unroll
+  for (int j = 0; j < G; j++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) st.acc[j][e] = 0.0f;
+  st.m = kNeg;
+  st.l = 0.0f;
+  if (warp == W) {
+    // ---- producer, after the selection: the deferred page, then the remaining segments
+    // (kept blocks, and sink / window pages beyond the first NS), 32 at a time: the lanes
+    // resolve them together; first uses of a ring slot go out from every lane at once, the
+    // others from lane 0 in order as the slots free up
+    const int has_def = (j_def >= 0 && j_def < jA) ? 1 : 0;
+    const int n_post = has_def + (cnt - jA);
+    bool ok = true;
+    for (int eb = 0; ok && eb < n_post; eb += 32) {
+      const int e = eb + lane;
+      const int j = e < n_post ? ((has_def && e == 0) ? j_def : jA + e - has_def) : -1;
+      int k = 0, t0 = 0, t1 = 0, page = -1;
+      if (j >= 0) page = resolve(first + j * stride, k, t0, t1);
+      if (j >= 0 && j < NS) {
+        meta[j] = make_int4(k, t0, t1, 0);
+        issue(j, page);
+      }
+      const int n = min(32, n_post - eb);
+      for (int q = 0; q < n; q++) {
+        const int jq = __shfl_sync(0xffffffffu, j, q);
+        const int kq = __shfl_sync(0xffffffffu, k, q);
+        const int t0q = __shfl_sync(0xffffffffu, t0, q);
+        const int t1q = __shfl_sync(0xffffffffu, t1, q);
+        const int pq = __shfl_sync(0xffffffffu, page, q);
+        if (jq < NS) continue;  // issued above
+        if (lane == 0) {
+          const int s = jq % NS;
+          if (!mbar_wait(&empty[s], ((jq / NS) - 1) & 1)) {
+            set_error(a.err, kDevErrTimeout);
+            ok = false;
+          } else {
+            meta[s] = make_int4(kq, t0q, t1q, 0);
+            issue(s, pq);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+    }
+    if (!ok && lane == 0) {
+      for (int j = max(0, cnt - NS); j < cnt; j++) mbar_wait(&full[j % NS], (j / NS) & 1);
+    }
+  } else {
+    float qf[G][16];
+    load_query<G>(qf, a, b, h, lane & 7);
+    for (int j = warp; j < cnt; j += W) {
+      const int s = j % NS;
+      if (!mbar_wait(&full[s], (j / NS) & 1)) {
+        set_error(a.err, kDevErrTimeout);
+        break;
+      }
+      const int4 m4 = meta[s];  // written before the producer's arrive on full[s]
+      if (m4.y < m4.z)
+        warp_segment<G>(st, qf, wscr[warp], smem_addr(ring + s * kSlotBytes), m4.x, m4.y, m4.z,
+                        nullptr);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+  __syncthreads();
+  merge_warps<G, W, 16, false>(a, st, ring, mstate, b, h, split);
 }
 
 // ---------------------------------------------------------- mapped-host path
@@ -1080,9 +1465,75 @@ cudaError_t launch_g(AttArgs a, dim3 grid, bool host, cudaStream_t st) {
   return launch_kernel(kern, grid, dim3((W + 1) * 32), smem, st, true, a);
 }
 
+constexpr size_t kSelSmemLimit = 227 * 1024 - 256;  // room for the static shared memory
+
+template <int G, int W, int NS>
+size_t sel_smem_bytes(const SelArgs& sa) {
+  return 128 + sel_smem_layout<G, W, NS>(sa).end;
+}
+
+// Shared-memory capacities of attend_select_kernel for a shape; false when the selection
+// does not fit (then the step runs the pruning kernel and the plain sparse attention). The
+// rows of block maxima and of page ids are staged when they fit too.
+template <int G, int W, int NS>
+bool plan_select(const Shape& s, SelArgs& sa, bool stage_pages) {
+  constexpr int P = kTileBlocksSel;
+  if (!HSA_FUSED_SELECT || s.chunk != P * kPage || s.k0 > 0) return false;
+  auto up4 = [](long long x) { return (int)((x + 3) / 4 * 4); };
+  const long long n1max = ((long long)s.max_pages + P - 1) / P;
+  const long long keep1 = std::min<long long>(s.k1, n1max);
+  const long long n2max = keep1 * P;
+  sa.n2_cap = up4(std::max<long long>(n2max, 1));
+  sa.a_cap = std::max(up4(n1max + 4), 2 * sa.n2_cap);
+  sa.k1_cap = up4(std::max<long long>(keep1, 1));
+  sa.k2_cap = up4(std::max<long long>(std::min<long long>(s.k2, n2max), 1));
+  sa.row_cap = 0;
+  sa.prow_cap = 0;
+  if (sel_smem_bytes<G, W, NS>(sa) > kSelSmemLimit) return false;
+  sa.row_cap = up4(s.max_pages);
+  if (sel_smem_bytes<G, W, NS>(sa) > kSelSmemLimit) sa.row_cap = 0;
+  if (stage_pages) {
+    sa.prow_cap = up4(s.max_pages);
+    if (sel_smem_bytes<G, W, NS>(sa) > kSelSmemLimit) sa.prow_cap = 0;
+  }
+  return true;
+}
+
+// The attention's warps and ring slots for a group size (as launch_g's sparse path).
+template <int G>
+struct SelShape {
+  static constexpr int W = G > 4 ? 7 : kSparseWarps;
+  static constexpr int NS = 2 * W;
+};
+
+template <int G>
+bool plan_select_g(const Shape& s, SelArgs& sa, bool stage_pages) {
+  return plan_select<G, SelShape<G>::W, SelShape<G>::NS>(s, sa, stage_pages);
+}
+
+template <int G>
+cudaError_t launch_select_g(const AttArgs& a, const SelArgs& sa, dim3 grid, cudaStream_t st) {
+  constexpr int W = SelShape<G>::W, NS = SelShape<G>::NS;
+  const size_t smem = sel_smem_bytes<G, W, NS>(sa);
+  auto kern = attend_select_kernel<G, W, NS>;
+  cudaError_t e = set_kernel_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, grid, dim3((W + 1) * 32), smem, st, true, a, sa);
+}
+
+bool plan_select_any(const Shape& s, SelArgs& sa, bool stage_pages) {
+  switch (s.group) {
+    case 1: return plan_select_g<1>(s, sa, stage_pages);
+    case 2: return plan_select_g<2>(s, sa, stage_pages);
+    case 4: return plan_select_g<4>(s, sa, stage_pages);
+    case 8: return plan_select_g<8>(s, sa, stage_pages);
+    default: return false;
+  }
+}
+
 }  // namespace
 
-int attend_splits(const Shape& s, bool dense, bool host, int num_sms) {
+int attend_splits(const Shape& s, bool dense, bool host, int num_sms, bool reserve) {
   const long long units = (long long)s.batch * s.hkv;
   long long segs;
   if (dense) {
@@ -1094,7 +1545,9 @@ int attend_splits(const Shape& s, bool dense, bool host, int num_sms) {
   const int per_sm =
       host ? HSA_HOST_CTAS_PER_SM : (dense ? HSA_DENSE_CTAS_PER_SM : HSA_SPARSE_CTAS_PER_SM);
   long long want = ((long long)num_sms * per_sm + units - 1) / units;
-  if (!dense && !host && HSA_SPARSE_RESERVE && num_sms > units) {
+  // without a pruning kernel beside it: one wave of CTAs, at most one per SM each
+  if (!dense && !host && !reserve) want = std::max<long long>(1, (long long)num_sms * per_sm / units);
+  if (!dense && !host && reserve && HSA_SPARSE_RESERVE && num_sms > units) {
     const long long reserved = std::max<long long>(1, (num_sms - units) / units);
     if (4 * reserved >= 3 * want) want = reserved;
   }
@@ -1162,6 +1615,64 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
       return dense ? launch_g<8, true>(a, grid, host, st) : launch_g<8, false>(a, grid, host, st);
     default:
       return cudaErrorInvalidValue;
+  }
+}
+
+bool attend_select_supported(const Shape& s, bool page_table_aligned) {
+  SelArgs sa;
+  return plan_select_any(s, sa, page_table_aligned);
+}
+
+cudaError_t launch_attend_select(const Shape& s, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* page_table,
+                                 const int32_t* seq_lens, const int32_t* block_max,
+                                 const int32_t* tile_max, int32_t* block_idx, int32_t* n_blocks,
+                                 float* out, float* lse, const AttendBuffers& buf, int* err,
+                                 cudaStream_t st) {
+  if (buf.nsplit < 1 || buf.nsplit > kMaxSplits) return cudaErrorInvalidValue;
+  const bool stage_pages = (reinterpret_cast<uintptr_t>(page_table) & 15) == 0;
+  SelArgs sa;
+  if (!plan_select_any(s, sa, stage_pages)) return cudaErrorInvalidValue;
+  // the staging copies start from the 16-byte boundary at or below a row's first entry
+  if ((reinterpret_cast<uintptr_t>(block_max) & 15) != 0 ||
+      (reinterpret_cast<uintptr_t>(tile_max) & 15) != 0)
+    return cudaErrorInvalidValue;
+  sa.block_max = block_max;
+  sa.tile_max = tile_max;
+  sa.block_idx = block_idx;
+  sa.n_blocks = n_blocks;
+  sa.max_tiles = (s.max_pages + kTileBlocksSel - 1) / kTileBlocksSel;
+  sa.k1 = s.k1;
+  AttArgs a = {};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k_cache);
+  a.v = static_cast<const __nv_bfloat16*>(v_cache);
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.lse = lse;
+  a.part_ml = buf.part_ml;
+  a.part_o = buf.part_o;
+  a.counters = buf.counters;
+  a.err = err;
+  a.hkv = s.hkv;
+  a.kv_div = s.kv_div;
+  a.kv_heads = s.hkv / s.kv_div;
+  a.max_pages = s.max_pages;
+  a.num_pages = s.num_pages;
+  a.k2 = s.k2;
+  a.sink = s.sink;
+  a.window = s.window;
+  a.nsplit = buf.nsplit;
+  a.qscale = s.sm_scale * kLog2e;
+  a.early = 1;
+  dim3 grid(buf.nsplit, s.hkv, s.batch);
+  switch (s.group) {
+    case 1: return launch_select_g<1>(a, sa, grid, st);
+    case 2: return launch_select_g<2>(a, sa, grid, st);
+    case 4: return launch_select_g<4>(a, sa, grid, st);
+    case 8: return launch_select_g<8>(a, sa, grid, st);
+    default: return cudaErrorInvalidValue;
   }
 }
 

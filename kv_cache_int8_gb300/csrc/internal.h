@@ -109,11 +109,25 @@ struct AttendBuffers {
 cudaError_t launch_cache_fill(const Shape& s, const BlockCache& c, const void* fill,
                               const int32_t* n_fill, const void* k_host, const void* v_host,
                               int* err, int num_sms, cudaStream_t st);
-int attend_splits(const Shape& s, bool dense, bool host, int num_sms);
+// reserve: leave SMs to a pruning kernel that runs beside the sparse attention
+int attend_splits(const Shape& s, bool dense, bool host, int num_sms, bool reserve = true);
 cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
                           const void* k_cache, const void* v_cache, const int32_t* page_table,
                           const int32_t* seq_lens, const int32_t* block_idx,
                           const int32_t* n_blocks, float* out, float* lse,
                           const AttendBuffers& buf, int* err, cudaStream_t st, bool early);
+
+// The whole decode step's sparse attention that runs both pruning modules itself (64-token
+// chunks, two modules): s is the attention's shape (rows = selection rows). Reads the
+// scorer's block_max / tile_max, writes the kept blocks to block_idx [rows][k2] and their
+// count to n_blocks [rows] as launch_prune would, and the attention output. Supported when
+// the selection fits the kernel's shared memory (else the pruning kernel and launch_attend).
+bool attend_select_supported(const Shape& s, bool page_table_aligned);
+cudaError_t launch_attend_select(const Shape& s, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* page_table,
+                                 const int32_t* seq_lens, const int32_t* block_max,
+                                 const int32_t* tile_max, int32_t* block_idx, int32_t* n_blocks,
+                                 float* out, float* lse, const AttendBuffers& buf, int* err,
+                                 cudaStream_t st);
 
 }  // namespace hsa

@@ -7,15 +7,16 @@
 // prune_kernel: one CTA per (sequence, kv head). Chunk scores (the scorer's per-tile maxima
 // for 64-token chunks, else the max of their blocks' maxima) are staged in shared memory
 // with bulk copies, and so are the whole row of block maxima and page ids when they fit;
-// the K-th largest value is found by radix selection on 8-bit digits (two CTA barriers a
-// digit); ties at the threshold are broken toward lower indices by ballots over
-// warp-contiguous ranges, which also write the kept indices in ascending order. Module 2
-// repeats this on the blocks of the kept chunks.
+// the K-th largest value is found by counting (select.cuh: a histogram of the values' top
+// 11 bits above the row's minimum, usually one level); ties at the threshold are broken
+// toward lower indices by ballots over warp-contiguous ranges, which also write the kept
+// indices in ascending order. Module 2 repeats this on the blocks of the kept chunks.
 #include <algorithm>
 #include <climits>
 
 #include "common.cuh"
 #include "internal.h"
+#include "select.cuh"
 
 namespace hsa {
 namespace {
@@ -30,10 +31,7 @@ constexpr int kPruneWarps = kPruneThreads / 32;
 constexpr int kMaxChunks = 53248;
 constexpr int kRowCap = 16384;  // block-maxima rows up to this many blocks are staged whole
 constexpr size_t kSmemLimit = 227 * 1024;
-constexpr int kDigitBins = 256;
-constexpr int kHistCopies = kPruneWarps / 2;
-static_assert(kPruneThreads >= kDigitBins && kPruneThreads % 64 == 0,
-              "one scan thread per digit, two warps per histogram");
+static_assert(kPruneThreads >= kSelScan && kPruneThreads % 32 == 0, "selection threads");
 
 struct PruneArgs {
   const int32_t* seq_lens;
@@ -55,292 +53,25 @@ struct PruneArgs {
 
 // Shared scratch of the selection.
 struct PruneShared {
-  unsigned hist[kHistCopies][kDigitBins];  // digit histograms (warp w counts into w / 2), zero
-                                           // between selections
-  int sfx[kDigitBins];                     // per digit: in-group suffix count
-  int tot[kPruneWarps];                    // per-group / per-warp totals
-  int mn[kPruneWarps], mx[kPruneWarps];    // per-warp min / max of the valid values
-  int w_a[kPruneWarps], w_b[kPruneWarps];  // per-warp counts of the collect
-  uint64_t bar[2];                         // staging copies: [0] module 1's, [1] the rest
+  SelectShared sel;  // histogram, per-warp scratch (select.cuh)
+  uint64_t bar[2];   // staging copies: [0] module 1's, [1] the rest
 };
-
-__device__ __forceinline__ unsigned lanemask_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
-// Order-preserving key of a value relative to the smallest valid value; placeholders get 0.
-__device__ __forceinline__ unsigned rel_key(int v, int vmin) {
-  return v == INT_MIN ? 0u : (unsigned)((long long)v - vmin) + 1u;
-}
-
-// A row src[0, n) of ints in global memory (in an array whose base is 16-byte aligned) to be
-// staged in shared memory at dst_base (16-byte aligned, room for n + 3 ints): the copy of
-// src[i] lands at dst_base[o + i]. The 16-byte-aligned span [src - o, src - o + body) is
-// copied in bulk, the ragged tail with plain loads.
-struct StagedRow {
-  const int32_t* s0;  // src - o, 16-byte aligned, inside the array
-  int* dst_base;
-  int o, body, n;
-  __device__ int* dst() const { return dst_base + o; }
-  __device__ uint32_t bytes() const { return (uint32_t)body * 4u; }
-};
-
-__device__ __forceinline__ StagedRow plan_row(int* dst_base, const int32_t* src, int n) {
-  StagedRow r;
-  r.o = (int)((reinterpret_cast<uintptr_t>(src) >> 2) & 3);
-  r.s0 = src - r.o;
-  r.body = ((n + r.o) / 4) * 4;
-  r.dst_base = dst_base;
-  r.n = n;
-  return r;
-}
-
-// Thread 0: the bulk copies of a planned row (at most 64 KiB each), completing on `bar`.
-__device__ __forceinline__ void issue_row(const StagedRow& r, uint64_t* bar) {
-  for (int off = 0; off < r.body; off += 16384)
-    bulk_load(r.dst_base + off, r.s0 + off, (uint32_t)min(16384, r.body - off) * 4u, bar);
-}
-
-// All threads: the ragged tail of a planned row.
-__device__ __forceinline__ void tail_row(const StagedRow& r) {
-  for (int i = r.body + threadIdx.x; i < r.n + r.o; i += kPruneThreads)
-    r.dst_base[i] = __ldg(r.s0 + i);
-}
 
 // Issue (thread 0) and tail of a planned row; returns where src[0] lands.
 __device__ __forceinline__ int* stage(const StagedRow& r, uint64_t* bar) {
   if (threadIdx.x == 0) issue_row(r, bar);
-  tail_row(r);
+  tail_row<kPruneThreads>(r);
   return r.dst();
 }
 
-// (min, max) of the valid (not INT_MIN) entries of vals[0, n), for every thread; an empty
-// set gives (INT_MAX, INT_MIN). One CTA barrier.
-__device__ __noinline__ int2 block_min_max(const int* vals, int n, PruneShared& ps) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int mn = INT_MAX, mx = INT_MIN;
-  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * kPruneThreads) {
-    int v[4];
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const int i = i0 + u * kPruneThreads;
-      v[u] = i < n ? vals[i] : INT_MIN;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-      if (v[u] != INT_MIN) {
-        mn = min(mn, v[u]);
-        mx = max(mx, v[u]);
-      }
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  }
-  if (lane == 0) {
-    ps.mn[warp] = mn;
-    ps.mx[warp] = mx;
-  }
-  __syncthreads();
-  mn = ps.mn[0];
-  mx = ps.mx[0];
-#pragma unroll
-  for (int w = 1; w < kPruneWarps; w++) {
-    mn = min(mn, ps.mn[w]);
-    mx = max(mx, ps.mx[w]);
-  }
-  return make_int2(mn, mx);
-}
-
-// Returns (T, need_eq, eq_total). The K-th largest value T of vals[0, n) (0 < K < number of
-// valid entries), by radix
-// selection on 8-bit digits of the keys rel_key(v, min), from the highest digit in which
-// they can differ. need_eq = K - #(values > T): how many of the entries equal to T are kept
-// (the lowest-index ones); eq_total = #(values == T). The valid values' min and max are
-// computed here unless the caller has them (have_range).
-//
-// Each digit, two CTA barriers: the warps count the matching keys into the histograms (two
-// warps to one, loads batched ahead of the atomics); then threads 0..255 own one digit
-// each, sum it over the histograms (zeroing them for the next digit) and scan within their
-// warp by shuffles, publishing every digit's in-warp suffix count and each warp's total;
-// then every thread finds the digit holding the K-th key from those by itself. The
-// histograms are zero on entry and on return.
-__device__ __noinline__ int3 kth_largest(const int* vals, int n, int K, PruneShared& ps,
-                                         bool have_range, int vmin, int vmax) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
-  if (!have_range) {
-    const int2 r = block_min_max(vals, n, ps);
-    vmin = r.x;
-    vmax = r.y;
-  }
-  int eq_total = 0;
-  const unsigned kmax = (unsigned)((long long)vmax - vmin) + 1u;
-  int shift = ((31 - __clz(kmax)) / 8) * 8;
-  unsigned prefix = 0;  // decided high bits of T's key
-  int above = 0;        // entries known to lie above T
-  unsigned* hist = ps.hist[warp >> 1];
-  for (;;) {
-    const int hi_shift = shift + 8;
-    for (int i0 = tid; i0 < n; i0 += 4 * kPruneThreads) {
-      unsigned key[4];
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const int i = i0 + u * kPruneThreads;
-        key[u] = i < n ? rel_key(vals[i], vmin) : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const bool match = hi_shift >= 32 || (key[u] >> hi_shift) == (prefix >> hi_shift);
-        if (match && key[u] != 0u) atomicAdd(&hist[(key[u] >> shift) & 0xFF], 1u);
-      }
-    }
-    __syncthreads();
-    if (tid < kDigitBins) {
-      int c = 0;
-#pragma unroll
-      for (int r = 0; r < kHistCopies; r++) {
-        c += ps.hist[r][tid];
-        ps.hist[r][tid] = 0;
-      }
-      // s = matching keys with this digit or a higher one, within this warp's 32 digits
-      int s = c;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_down_sync(0xffffffffu, s, off);
-        if (lane + off < 32) s += y;
-      }
-      ps.sfx[tid] = s;
-      if (lane == 0) ps.tot[warp] = s;
-    }
-    __syncthreads();
-    // the digit group (32 digits) holding the K-th key, then the digit within it
-    int hi_groups = 0, g = kDigitBins / 32 - 1;
-    for (; g > 0; g--) {
-      if (above + hi_groups + ps.tot[g] >= K) break;
-      hi_groups += ps.tot[g];
-    }
-    const int base = above + hi_groups;
-    const int sl = base + ps.sfx[g * 32 + lane];  // keys at or above digit 32 g + lane
-    const unsigned ok = __ballot_sync(0xffffffffu, sl >= K);
-    const int dl = 31 - __clz(ok);  // the highest digit of the group whose suffix reaches K
-    const int d = g * 32 + dl;
-    const int in_digit = ps.sfx[d] - (dl < 31 ? ps.sfx[d + 1] : 0);
-    prefix |= (unsigned)d << shift;
-    above = base + ps.sfx[d] - in_digit;  // keys strictly above digit d
-    if (shift == 0) {
-      eq_total = in_digit;
-      break;
-    }
-    shift -= 8;
-  }
-  __syncthreads();
-  return make_int3((int)((long long)vmin + (long long)prefix - 1), K - above, eq_total);
-}
-
-// Emits, in ascending index order, every i with vals[i] > T plus the first need_eq indices
-// with vals[i] == T, writing out[position] = add + i; returns how many. Warp w owns a contiguous
-// range, read 4 x 32 entries at a time; positions come from ballots (one CTA barrier for
-// the per-warp counts). When all entries equal to T are kept (need_eq == eq_total), or none
-// are, the test is a plain threshold and no tie ranks are needed.
-__device__ __noinline__ int collect(const int* vals, int n, int T, int need_eq, int eq_total,
-                                    PruneShared& ps, int* out, int add) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per = ((n + kPruneWarps * 32 - 1) / (kPruneWarps * 32)) * 32;
-  const int w0 = min(n, warp * per), w1 = min(n, w0 + per);
-  const unsigned lt = lanemask_lt();
-  const bool ties_split = need_eq > 0 && need_eq < eq_total;
-  // threshold form: keep v > t_lo (placeholders INT_MIN are never kept: t_lo >= INT_MIN)
-  const int t_lo = (need_eq > 0 && !ties_split) ? T - 1 : T;
-  if (!ties_split) {
-    int cnt = 0;
-    for (int i0 = w0; i0 < w1; i0 += 128) {
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const int i = i0 + 32 * u + lane;
-        cnt += (i < w1 && vals[i] > t_lo) ? 1 : 0;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-    if (lane == 0) ps.w_a[warp] = cnt;
-    __syncthreads();
-    int pos = 0, total = 0;
-    for (int w = 0; w < kPruneWarps; w++) {
-      if (w == warp) pos = total;
-      total += ps.w_a[w];
-    }
-    for (int i0 = w0; i0 < w1; i0 += 128) {
-      bool take[4];
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const int i = i0 + 32 * u + lane;
-        take[u] = i < w1 && vals[i] > t_lo;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const unsigned tm = __ballot_sync(0xffffffffu, take[u]);
-        if (take[u]) out[pos + __popc(tm & lt)] = add + i0 + 32 * u + lane;
-        pos += __popc(tm);
-      }
-    }
-    __syncthreads();
-    return total;
-  }
-  int n_gt = 0, n_eq = 0;
-  for (int i = w0 + lane; i < w1; i += 32) {
-    n_gt += vals[i] > T;
-    n_eq += vals[i] == T;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    n_gt += __shfl_xor_sync(0xffffffffu, n_gt, off);
-    n_eq += __shfl_xor_sync(0xffffffffu, n_eq, off);
-  }
-  if (lane == 0) {
-    ps.w_a[warp] = n_gt;
-    ps.w_b[warp] = n_eq;
-  }
-  __syncthreads();
-  // per warp: entries kept = all above T plus the ties still allowed after the earlier warps
-  int eq_acc = 0, pos = 0, total = 0, eq_base = 0;
-  for (int w = 0; w < kPruneWarps; w++) {
-    const int kept_w = ps.w_a[w] + min(max(need_eq - eq_acc, 0), ps.w_b[w]);
-    if (w == warp) {
-      pos = total;
-      eq_base = eq_acc;
-    }
-    total += kept_w;
-    eq_acc += ps.w_b[w];
-  }
-  for (int i0 = w0; i0 < w1; i0 += 32) {
-    const int i = i0 + lane;
-    const int v = i < w1 ? vals[i] : INT_MIN;
-    const bool gt = i < w1 && v > T, eq = i < w1 && v == T;
-    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
-    const bool take = gt || (eq && eq_base + __popc(eqm & lt) < need_eq);
-    const unsigned tm = __ballot_sync(0xffffffffu, take);
-    if (take) out[pos + __popc(tm & lt)] = add + i;
-    eq_base += __popc(eqm);
-    pos += __popc(tm);
-  }
-  __syncthreads();
-  return total;
-}
-
-// At most 40 registers a thread (three 512-thread CTAs' worth per SM): a prune CTA and a
-// CTA of the sparse attend, which is launched while the prune runs, then fit on one SM
-// together, and no attend CTA has to wait for the prune to leave its SM.
+// At most 64 registers a thread (two 512-thread CTAs' worth per SM).
 //
 // Shared memory: PruneShared, vals [vals_cap + 4], cand [cand_cap] (module 2's block ids),
 // cand_page [cand_cap] (with
 // sel_pages), kept [kept_cap], row [row_cap + 4] (the sequence's block maxima, staged whole
 // when they fit), prow [prow_cap + 4] (its page ids, with sel_pages), sel_pos [sel_cap]
 // (module 2's kept positions in cand).
-__global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_kernel(const PruneArgs a) {
+__global__ void __launch_bounds__(kPruneThreads, 1024 / kPruneThreads) prune_kernel(const PruneArgs a) {
   extern __shared__ __align__(16) unsigned char psmem_raw[];
   PruneShared& ps = *reinterpret_cast<PruneShared*>(psmem_raw);
   int* arr = reinterpret_cast<int*>(psmem_raw + ((sizeof(PruneShared) + 15) / 16) * 16);
@@ -363,7 +94,7 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
     mbar_init(&ps.bar[1], 1);
     fence_barrier_init();
   }
-  for (int i = tid; i < kHistCopies * kDigitBins; i += kPruneThreads) (&ps.hist[0][0])[i] = 0u;
+  sel_init<kPruneThreads>(ps.sel);
   // the sequence length is an input of the step, not written by the previous kernel: it is
   // read before the wait
   const int n = a.seq_lens[b];
@@ -449,12 +180,15 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
     __syncthreads();
     const int keep0 = min(a.k0, n0);
     if (keep0 < n0) {
-      const int3 r = kth_largest(vals0, n0, keep0, ps, false, 0, 0);
+      const int3 r = sel_kth_largest<kPruneThreads>(vals0, n0, keep0, ps.sel, false, 0, 0);
       T = r.x;
       need_eq = r.y;
       eq_total = r.z;
     }
-    const int got0 = keep0 > 0 ? collect(vals0, n0, T, need_eq, eq_total, ps, kept0, g_lo) : 0;
+    const int got0 =
+        keep0 > 0
+            ? sel_collect<kPruneThreads>(vals0, n0, T, need_eq, eq_total, ps.sel, kept0, g_lo)
+            : 0;
     // ---- module 1 over the kept coarse chunks' fine chunks (ascending; those outside the
     // candidate region are placeholders), top-K1
     const int n1c = got0 * R;
@@ -469,24 +203,25 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
     const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, off);
-    if (lane == 0) ps.tot[warp] = valid;
+    if (lane == 0) ps.sel.wsum[warp] = valid;
     __syncthreads();
     int n1_valid = 0;
 #pragma unroll
-    for (int w = 0; w < kPruneWarps; w++) n1_valid += ps.tot[w];
+    for (int w = 0; w < kPruneWarps; w++) n1_valid += ps.sel.wsum[w];
     __syncthreads();
     const int keep1 = min(a.k1, n1_valid);
     T = INT_MIN;
     need_eq = 0;
     eq_total = 0;
     if (keep1 < n1_valid && keep1 > 0) {
-      const int3 r = kth_largest(vals1, n1c, keep1, ps, false, 0, 0);
+      const int3 r = sel_kth_largest<kPruneThreads>(vals1, n1c, keep1, ps.sel, false, 0, 0);
       T = r.x;
       need_eq = r.y;
       eq_total = r.z;
     }
     if (keep1 > 0) {
-      got1 = collect(vals1, n1c, T, need_eq, eq_total, ps, kept_chunks, 0);  // positions
+      // positions in vals1
+      got1 = sel_collect<kPruneThreads>(vals1, n1c, T, need_eq, eq_total, ps.sel, kept_chunks, 0);
       for (int i = tid; i < got1; i += kPruneThreads) kept_chunks[i] = cand1[kept_chunks[i]];
       __syncthreads();
     }
@@ -494,12 +229,13 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
     // ---- module 1: top-K1 chunks
     const int keep1 = min(a.k1, n1);
     if (keep1 < n1 && keep1 > 0) {
-      const int3 r = kth_largest(vals, n1, keep1, ps, false, 0, 0);
+      const int3 r = sel_kth_largest<kPruneThreads>(vals, n1, keep1, ps.sel, false, 0, 0);
       T = r.x;
       need_eq = r.y;
       eq_total = r.z;
     }
-    if (keep1 > 0) got1 = collect(vals, n1, T, need_eq, eq_total, ps, kept_chunks, c_lo);
+    if (keep1 > 0)
+      got1 = sel_collect<kPruneThreads>(vals, n1, T, need_eq, eq_total, ps.sel, kept_chunks, c_lo);
   }
   if (a.chunk_idx)
     for (int i = tid; i < a.k1; i += kPruneThreads)
@@ -548,17 +284,17 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
     mx2 = max(mx2, __shfl_xor_sync(0xffffffffu, mx2, off));
   }
   if (lane == 0) {
-    ps.tot[warp] = valid_local;
-    ps.mn[warp] = mn2;
-    ps.mx[warp] = mx2;
+    ps.sel.wsum[warp] = valid_local;
+    ps.sel.mn[warp] = mn2;
+    ps.sel.mx[warp] = mx2;
   }
   __syncthreads();
   int n2_valid = 0;
 #pragma unroll
   for (int w = 0; w < kPruneWarps; w++) {
-    n2_valid += ps.tot[w];
-    mn2 = min(mn2, ps.mn[w]);
-    mx2 = max(mx2, ps.mx[w]);
+    n2_valid += ps.sel.wsum[w];
+    mn2 = min(mn2, ps.sel.mn[w]);
+    mx2 = max(mx2, ps.sel.mx[w]);
   }
   __syncthreads();
   const int keep2 = min(a.k2, n2_valid);
@@ -566,14 +302,14 @@ __global__ void __launch_bounds__(kPruneThreads, 1536 / kPruneThreads) prune_ker
   need_eq = 0;
   eq_total = 0;
   if (keep2 < n2_valid && keep2 > 0) {
-    const int3 r = kth_largest(vals, n2, keep2, ps, true, mn2, mx2);
+    const int3 r = sel_kth_largest<kPruneThreads>(vals, n2, keep2, ps.sel, true, mn2, mx2);
     T = r.x;
     need_eq = r.y;
     eq_total = r.z;
   }
   int got2 = 0;
   if (keep2 > 0) {
-    got2 = collect(vals, n2, T, need_eq, eq_total, ps, sel_pos, 0);
+    got2 = sel_collect<kPruneThreads>(vals, n2, T, need_eq, eq_total, ps.sel, sel_pos, 0);
   }
   for (int i = tid; i < a.k2; i += kPruneThreads) {
     const int x = i < got2 ? sel_pos[i] : -1;
@@ -651,7 +387,7 @@ struct CachePlanArgs {
 };
 
 struct CachePlanShared {
-  PruneShared ps;
+  SelectShared ps;
   int warp_cnt[kPruneWarps];  // per-warp counts of one 512-entry chunk
   int step, n_miss, n_refresh;
 };
@@ -701,7 +437,7 @@ __global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePl
   int* miss_f = vals + a.capacity;              // [B * Hkv * seg_stride] segment of miss j
   int* victims = miss_f + a.batch * a.hkv * a.seg_stride;  // same size
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kHistCopies * kDigitBins; i += kPruneThreads) (&cs.ps.hist[0][0])[i] = 0u;
+  sel_init<kPruneThreads>(cs.ps);
   grid_dep_wait();  // the selection and the cache state come from earlier kernels
   grid_dep_launch();
   if (tid == 0) {
@@ -812,22 +548,22 @@ __global__ void __launch_bounds__(kPruneThreads) cache_plan_kernel(const CachePl
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) valid += __shfl_xor_sync(0xffffffffu, valid, off);
-    if (lane == 0) cs.ps.tot[warp] = valid;
+    if (lane == 0) cs.ps.wsum[warp] = valid;
     __syncthreads();
     int n_valid = 0;
-    for (int w = 0; w < kPruneWarps; w++) n_valid += cs.ps.tot[w];
+    for (int w = 0; w < kPruneWarps; w++) n_valid += cs.ps.wsum[w];
     __syncthreads();
     if (n_valid < M) {
       if (tid == 0) set_error(a.err, kDevErrCheck);  // capacity below the call's working set
     } else {
       int T = INT_MIN, need_eq = 0, eq_total = 0;
       if (M < n_valid) {
-        const int3 r = kth_largest(vals, a.capacity, M, cs.ps, false, 0, 0);
+        const int3 r = sel_kth_largest<kPruneThreads>(vals, a.capacity, M, cs.ps, false, 0, 0);
         T = r.x;
         need_eq = r.y;
         eq_total = r.z;
       }
-      got = collect(vals, a.capacity, T, need_eq, eq_total, cs.ps, victims, 0);
+      got = sel_collect<kPruneThreads>(vals, a.capacity, T, need_eq, eq_total, cs.ps, victims, 0);
     }
   }
   // evict the victims' old keys first (none of them is looked up by this call)

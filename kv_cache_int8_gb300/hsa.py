@@ -367,6 +367,8 @@ def hsa_decode_step_cached(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache,
 
 
 def hsa_read_device_error(ws, stream=None) -> int:
+    """Reads and clears a workspace's device error word (ws None: the error word of
+    hsa_select_noalloc's fixed scratch array)."""
     code = ctypes.c_int32(0)
     _check("hsa_read_device_error", load().hsa_read_device_error(
         _p(ws), _stream(stream), ctypes.byref(code)))

@@ -11,10 +11,12 @@ from .oracle import (  # noqa: F401
     attend,
     block_mass,
     dense,
+    fp8_block_scores,
     num_threads,
     quantize_append,
     quantize_keys,
     query_codes,
     recall,
     select,
+    selection_within_bounds,
 )

@@ -70,7 +70,7 @@ typedef struct {
   int32_t chunk0, k0; /* k0 > 0: a first module keeps the top-k0 chunks of chunk0 tokens */
   int32_t key_bits;   /* 4: 4-bit key codes (levels +-7); 0 or 8: 8-bit (levels +-127) */
   int32_t per_head;   /* 1: every query head selects its own chunks and blocks (N3 variant) */
-  int32_t key_fp8;    /* 1: FP8 E4M3 key codes (scale amax / 448, fp32 scores; N4 variant) */
+  int32_t key_fp8;    /* 1: FP8 E4M3 key codes (scale amax / 448, real-valued scores; N4 variant) */
 } oracle_dims;
 
 /* Rows of the selection outputs per sequence: one per kv head (the group shares one
@@ -178,12 +178,46 @@ static int8_t format_code(const oracle_dims* d, double x, float s) {
 }
 
 /* Ordered integer of a float score: a < b as floats exactly when key(a) < key(b); both
- * zeros map to 0. The selection then ranks FP8 scores as it ranks integer scores. */
+ * zeros map to 0 (the block_max output of FP8 selections). */
 static int32_t ordered_key(float f) {
   f = f + 0.0f; /* -0 -> +0 */
   int32_t bits;
   memcpy(&bits, &f, sizeof bits);
   return bits >= 0 ? bits : bits ^ 0x7FFFFFFF;
+}
+
+/* The same for an fp64 score: the selection ranks FP8 scores as it ranks integer scores. */
+static int64_t ordered_key64(double x) {
+  x = x + 0.0; /* -0 -> +0 */
+  int64_t bits;
+  memcpy(&bits, &x, sizeof bits);
+  return bits >= 0 ? bits : bits ^ INT64_MAX;
+}
+
+/* FP8 keys: the score of head j for token t is the dot of the folded fp32 query with the
+ * E4M3 values, sum_c q'_{j,c} x_{t,c}. The pages fix no precision or order for it, so the
+ * oracle takes the sum itself: every product is exact in fp64 (24 + 4 significant bits)
+ * and the fp64 sum of 128 of them is within 127 * 2^-53 * sum |q' x| of the exact value.
+ * An fp32 evaluation with one rounding per term (a chain of fused multiply-adds, in any
+ * order) is within gamma_n * sum |q' x| of the exact value (Higham, "Accuracy and Stability
+ * of Numerical Algorithms", recursive summation: gamma_n = n u / (1 - n u), u = 2^-24,
+ * n = the number of terms); *abs_sum receives sum |q' x|. */
+static double fp8_dot(const oracle_dims* d, const float* qf_j, const int8_t* kq,
+                      const int32_t* page_table, int b, int h, int64_t t, double* abs_sum) {
+  double acc = 0.0, mag = 0.0;
+  for (int c = 0; c < d->head_dim; c++) {
+    const double p =
+        (double)qf_j[c] * (double)e4m3_value((uint8_t)kq[cache_index(d, page_table, b, h, t, c)]);
+    acc += p;
+    mag += fabs(p);
+  }
+  *abs_sum = mag;
+  return acc;
+}
+
+static double fp32_chain_gamma(int n) {
+  const double u = ldexp(1.0, -24);
+  return n * u / (1.0 - n * u);
 }
 
 /* ----------------------------------------------- key scales and int8 codes */
@@ -375,13 +409,10 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
           for (int j = j_lo; j < j_hi; j++) {
             int64_t dot = 0;
             if (d->key_fp8) {
-              /* FP8 keys: the fp32 dot of the folded query with the E4M3 values, one fused
-               * multiply-add per channel in channel order, as an ordered integer */
-              float acc = 0.0f;
-              for (int c = 0; c < D; c++)
-                acc = fmaf(qf[j * D + c],
-                           e4m3_value((uint8_t)kq[cache_index(d, page_table, b, h, t, c)]), acc);
-              dot = ordered_key(acc);
+              /* FP8 keys: the dot of the folded query with the E4M3 values (fp8_dot), ranked
+               * through its ordered integer */
+              double mag;
+              dot = ordered_key64(fp8_dot(d, qf + j * D, kq, page_table, b, h, t, &mag));
             } else {
               for (int c = 0; c < D; c++)
                 dot += (int64_t)qq[j * D + c] * (int64_t)kq[cache_index(d, page_table, b, h, t, c)];
@@ -397,8 +428,21 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
           bvalid[bi] = 1;
         }
         if (block_max) {
+          /* FP8 keys: the ordered integer of the block maximum rounded to fp32 (the exact
+           * maxima and their bounds: oracle_fp8_block_scores) */
           int32_t* out = block_max + row * max_blocks;
-          for (int64_t k = 0; k < max_blocks; k++) out[k] = bvalid[k] ? (int32_t)bmax[k] : INT32_MIN;
+          for (int64_t k = 0; k < max_blocks; k++) {
+            int32_t v = INT32_MIN;
+            if (bvalid[k] && d->key_fp8) {
+              const int64_t bits = bmax[k] >= 0 ? bmax[k] : bmax[k] ^ INT64_MAX;
+              double x;
+              memcpy(&x, &bits, sizeof x);
+              v = ordered_key((float)x);
+            } else if (bvalid[k]) {
+              v = (int32_t)bmax[k];
+            }
+            out[k] = v;
+          }
         }
         ranked* list = (ranked*)malloc(sizeof(ranked) * (size_t)(n_chunk_all + max_blocks +
                                                                   n_coarse_all + 1));
@@ -457,6 +501,64 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
       free(bvalid);
     }
     free(qq);
+    free(qf);
+  }
+  return bad ? 3 : 0;
+}
+
+/* FP8 keys: for every selection row and block, the exact block score (the max over the
+ * block's candidate tokens of the token score, the max over the row's query heads of
+ * fp8_dot) in block_score [B][R][max_blocks] (-inf where the block has no candidate
+ * token), and in block_bound the largest gamma_n * sum |q' x| over those (token, head)
+ * pairs, n = head_dim: a block maximum computed from fp32 sums with one rounding per term
+ * lies within block_bound of block_score (the max of perturbed values moves by at most the
+ * largest perturbation). R and bh_mask as in oracle_select. */
+int oracle_fp8_block_scores(const oracle_dims* d, const uint16_t* q, const float* scale,
+                            const int8_t* kq, const int32_t* page_table, const int32_t* lens,
+                            const int32_t* bh_mask, double* block_score, double* block_bound) {
+  if (!dims_ok(d) || !d->key_fp8 || !q || !scale || !kq || !page_table || !lens ||
+      !block_score || !block_bound)
+    return 1;
+  for (int b = 0; b < d->batch; b++)
+    if (!seq_ok(d, page_table, lens, b)) return 2;
+  const int D = d->head_dim, G = d->hq / d->hkv;
+  const int64_t max_tokens = (int64_t)d->max_pages_per_seq * d->page_size;
+  const int64_t max_blocks = (max_tokens + d->block - 1) / d->block;
+  const double gamma = fp32_chain_gamma(D);
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int bh = 0; bh < d->batch * d->hkv; bh++) {
+    const int b = bh / d->hkv, h = bh % d->hkv;
+    if (!wanted(bh_mask, d, b, h)) continue;
+    float* qf = (float*)malloc(sizeof(float) * (size_t)G * D);
+    if (!qf) {
+#pragma omp atomic write
+      bad = 1;
+      continue;
+    }
+    query_folded(d, q, scale, b, h, qf);
+    const int64_t n = lens[b], lo = d->sink, hi = n - d->window;
+    const int nrow = d->per_head ? G : 1;
+    for (int rj = 0; rj < nrow; rj++) {
+      const int64_t row =
+          d->per_head ? (int64_t)b * d->hq + h * G + rj : (int64_t)b * d->hkv + h;
+      const int j_lo = d->per_head ? rj : 0, j_hi = d->per_head ? rj + 1 : G;
+      double* sc = block_score + row * max_blocks;
+      double* bd = block_bound + row * max_blocks;
+      for (int64_t k = 0; k < max_blocks; k++) {
+        sc[k] = -HUGE_VAL;
+        bd[k] = 0.0;
+      }
+      for (int64_t t = lo; t < hi; t++) {
+        const int64_t k = t / d->block;
+        for (int j = j_lo; j < j_hi; j++) {
+          double mag;
+          const double s = fp8_dot(d, qf + j * D, kq, page_table, b, h, t, &mag);
+          if (s > sc[k]) sc[k] = s;
+          if (gamma * mag > bd[k]) bd[k] = gamma * mag;
+        }
+      }
+    }
     free(qf);
   }
   return bad ? 3 : 0;

@@ -85,6 +85,7 @@ def _lib():
             "oracle_dense": [D, P, P, P, P, P, P, P, P],
             "oracle_recall": [D, P, P, P, P, P, P, P, P],
             "oracle_block_mass": [D, P, P, P, P, P, P, P],
+            "oracle_fp8_block_scores": [D, P, P, P, P, P, P, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -185,6 +186,84 @@ def select(d: Dims, q: np.ndarray, k_scale: np.ndarray, kq: np.ndarray, page_tab
     if want_block_max:
         out["block_max"] = bm
     return out
+
+
+def fp8_block_scores(d: Dims, q: np.ndarray, k_scale: np.ndarray, kq: np.ndarray, page_table,
+                     seq_lens, bh_mask=None):
+    """FP8 keys: (score, bound), both f64 [B][R][max_blocks]. score = the exact block score
+    (max over the block's candidate tokens and the row's query heads of the dot of the folded
+    fp32 query with the E4M3 values; -inf where the block has no candidate token); bound =
+    Higham's gamma_128 times the largest sum |q' x| among those: any fp32 evaluation of the
+    dots with one rounding per term gives block maxima within `bound` of `score`."""
+    assert d.key_fp8 == 1
+    B, H = d.batch, d.sel_rows
+    score = np.zeros((B, H, d.max_blocks), dtype=np.float64)
+    bound = np.zeros((B, H, d.max_blocks), dtype=np.float64)
+    cd = d.c()
+    kq = np.ascontiguousarray(kq)
+    assert kq.dtype == np.int8
+    _check(_lib().oracle_fp8_block_scores(
+        ctypes.byref(cd), _ptr(_u16(q)), _ptr(np.ascontiguousarray(k_scale, dtype=np.float32)),
+        _ptr(kq), _ptr(_i32(page_table)), _ptr(_i32(seq_lens)),
+        _ptr(None if bh_mask is None else _i32(bh_mask)), _ptr(score), _ptr(bound)),
+        "oracle_fp8_block_scores")
+    return score, bound
+
+
+def selection_within_bounds(d: Dims, seq_lens, score: np.ndarray, bound: np.ndarray,
+                            chunk_idx, n_chunks, block_idx, n_blocks, rows=None):
+    """Whether a selection is one of the two modules' results for block scores known only to
+    within `bound` of `score` (fp8_block_scores): per row, the counts are min(K1, #valid
+    chunks) and min(K2, #candidate blocks of the kept chunks), the lists ascending and -1
+    padded, and no dropped chunk (block) beats a kept one by more than their two bounds. A
+    chunk's score is the max of its blocks' scores, its bound the max of their bounds.
+    Returns a list of violations (empty: valid). rows: (b, r) pairs to check (all if None)."""
+    P = d.chunk // d.block
+    bad = []
+    B, R = score.shape[:2]
+    for b, r in (rows if rows is not None else [(b, r) for b in range(B) for r in range(R)]):
+        valid = np.isfinite(score[b, r])
+        n_ch = -(-score.shape[2] // P)
+        cs = np.full(n_ch, -np.inf)
+        cb = np.zeros(n_ch)
+        for k in np.nonzero(valid)[0]:
+            cs[k // P] = max(cs[k // P], score[b, r, k])
+            cb[k // P] = max(cb[k // P], bound[b, r, k])
+        cvalid = np.nonzero(np.isfinite(cs))[0]
+        nc = int(n_chunks[b, r])
+        kept_c = [int(c) for c in chunk_idx[b, r][:nc]]
+        if nc != min(d.k1, cvalid.size):
+            bad.append((b, r, "chunk count", nc, min(d.k1, cvalid.size)))
+        if any(c < 0 for c in kept_c) or kept_c != sorted(set(kept_c)) or \
+                any(int(c) != -1 for c in chunk_idx[b, r][nc:]):
+            bad.append((b, r, "chunk list", kept_c))
+            continue
+        if any(not np.isfinite(cs[c]) for c in kept_c):
+            bad.append((b, r, "invalid chunk kept"))
+            continue
+        dropped_c = np.setdiff1d(cvalid, kept_c)
+        if dropped_c.size and kept_c:
+            worst_kept = min(kept_c, key=lambda c: cs[c] + cb[c])
+            best_drop = dropped_c[np.argmax(cs[dropped_c] - cb[dropped_c])]
+            if cs[best_drop] - cb[best_drop] > cs[worst_kept] + cb[worst_kept]:
+                bad.append((b, r, "chunk order", int(best_drop), worst_kept))
+        cand = [k for c in kept_c for k in range(c * P, c * P + P) if k < valid.size and valid[k]]
+        nb = int(n_blocks[b, r])
+        kept_b = [int(k) for k in block_idx[b, r][:nb]]
+        if nb != min(d.k2, len(cand)):
+            bad.append((b, r, "block count", nb, min(d.k2, len(cand))))
+        if kept_b != sorted(set(kept_b)) or any(int(k) != -1 for k in block_idx[b, r][nb:]) \
+                or not set(kept_b) <= set(cand):
+            bad.append((b, r, "block list", kept_b))
+            continue
+        dropped_b = np.array(sorted(set(cand) - set(kept_b)), dtype=np.int64)
+        if dropped_b.size and kept_b:
+            s_, e_ = score[b, r], bound[b, r]
+            worst_kept = min(kept_b, key=lambda k: s_[k] + e_[k])
+            best_drop = dropped_b[np.argmax(s_[dropped_b] - e_[dropped_b])]
+            if s_[best_drop] - e_[best_drop] > s_[worst_kept] + e_[worst_kept]:
+                bad.append((b, r, "block order", int(best_drop), worst_kept))
+    return bad
 
 
 def attend(d: Dims, q, k, v, page_table, seq_lens, block_idx, n_blocks, qh_mask=None):

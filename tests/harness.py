@@ -118,12 +118,45 @@ def gpu_step(wl: dict, d: hsa.Dims, dense: bool = True) -> dict:
         hsa.dense_decode(d, wl["q"], wl["k_cache"], wl["v_cache"], wl["page_table"],
                          wl["seq_lens"], out_d, lse_d, wd)
         res["out_dense"], res["lse_dense"] = out_d, lse_d
+    res.update(step_by_reappend(wl, d, kq, k_scale))
     torch.cuda.synchronize()
     for name, w in (("quantize", wq), ("select", ws), ("attend", wa)):
         assert hsa.hsa_read_device_error(w) == 0, f"device error word set by {name}"
     res = {k: v.cpu().numpy() for k, v in res.items()}
     res["kq"] = unpack_codes(res["kq"], d.key_bits)
     return res
+
+
+def step_by_reappend(wl: dict, d: hsa.Dims, kq: torch.Tensor, k_scale: torch.Tensor) -> dict:
+    """The whole decode step (hsa_decode_step: append, scorer, both modules, attention, in
+    the launch configuration the benchmark times) on the same inputs: every sequence's token
+    at slot N_b - 1 is appended again with its own K/V bits, whose codes come out the same
+    from the stored scales, so the cache is unchanged and the step's selection and output
+    are those of the separate calls. Returns step_block_idx / step_n_blocks / step_out /
+    step_lse, or nothing when a sequence is empty (there is no token to append)."""
+    lens = wl["seq_lens"]
+    if int(lens.min()) < 1:
+        return {}
+    dev = torch.device("cuda")
+    B, Hq = d.batch, d.hq
+    R = Hq if d.per_head else d.hkv
+    n = lens.long() - 1
+    pages = wl["page_table"].long().gather(1, (n // 16).unsqueeze(1)).squeeze(1)
+    kc, vc = wl["k_cache"], wl["v_cache"]
+    idx_p, idx_s = pages.to(kc.device), (n % 16).to(kc.device)
+    k_new = kc[idx_p, :, idx_s, :].to(dev).contiguous()
+    v_new = vc[idx_p, :, idx_s, :].to(dev).contiguous()
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev)
+    bidx = torch.full((B, R, max(d.k2, 1)), -7, dtype=torch.int32, device=dev)
+    nb = torch.full((B, R), -7, dtype=torch.int32, device=dev)
+    wst = hsa.workspace(d, hsa.HSA_OP_STEP)
+    hsa.hsa_decode_step(d, wl["q"], k_new, v_new, out, lse, kc, vc, kq, k_scale,
+                        wl["page_table"], lens, bidx, nb, wst)
+    torch.cuda.synchronize()
+    assert hsa.hsa_read_device_error(wst) == 0, "device error word set by the decode step"
+    return {"step_block_idx": bidx[..., :d.k2], "step_n_blocks": nb, "step_out": out,
+            "step_lse": lse}
 
 
 def host_arrays(wl: dict) -> dict:
@@ -143,6 +176,9 @@ def oracle_step(h: dict, od: oracle.Dims, bh_mask=None, qh_mask=None, dense: boo
     out, lse = oracle.attend(od, h["q"], h["k"], h["v"], h["pt"], h["lens"], sel["block_idx"],
                              sel["n_blocks"], qh_mask=qh_mask)
     res = dict(sel, kq=kq, k_scale=sc, out=out, lse=lse)
+    if od.key_fp8:  # exact block scores and the fp32 bound around them
+        res["fp8_score"], res["fp8_bound"] = oracle.fp8_block_scores(
+            od, h["q"], sc, kq, h["pt"], h["lens"], bh_mask=bh_mask)
     if dense:
         res["out_dense"], res["lse_dense"] = oracle.dense(od, h["q"], h["k"], h["v"], h["pt"],
                                                           h["lens"], qh_mask=qh_mask)
@@ -175,24 +211,74 @@ def logical_rows(arr: np.ndarray, pt: np.ndarray, lens, b: int, h: int) -> np.nd
     return rows[:n]
 
 
+def ordered_to_float(keys) -> np.ndarray:
+    """fp32 values of the order-preserving integers that FP8 block maxima are kept as."""
+    k = np.asarray(keys, dtype=np.int64)
+    bits = np.where(k >= 0, k, k ^ 0x7FFFFFFF).astype(np.int64) & 0xFFFFFFFF
+    return bits.astype(np.uint32).view(np.float32)
+
+
+def fp8_reference(g: dict, o: dict, h: dict, od: oracle.Dims, bh_pairs):
+    """FP8 keys, whose fp32 scores the pages fix in no order: the GPU's block maxima within
+    the fp32 bound of the exact ones, its selection valid for scores known to that bound
+    (oracle.selection_within_bounds), and the oracle's attention over the GPU's own
+    selection, which the outputs are then compared with. Returns (out, lse)."""
+    G = od.hq // od.hkv
+    rows = [(b, r) for b, hh in bh_pairs
+            for r in (range(hh * G, hh * G + G) if od.per_head else (hh,))]
+    for b, r in rows:
+        valid = np.isfinite(o["fp8_score"][b, r])
+        bm = g["block_max"][b, r]
+        assert (bm[~valid] == INT32_MIN).all()
+        err = np.abs(ordered_to_float(bm[valid]).astype(np.float64) - o["fp8_score"][b, r][valid])
+        assert (err <= o["fp8_bound"][b, r][valid]).all(), "FP8 block maxima outside the bound"
+    bad = oracle.selection_within_bounds(od, h["lens"], o["fp8_score"], o["fp8_bound"],
+                                         g["chunk_idx"], g["n_chunks"], g["block_idx"],
+                                         g["n_blocks"], rows)
+    assert not bad, f"FP8 selection not valid within the fp32 bound: {bad[:4]}"
+    qh_mask = np.zeros((od.batch, od.hq), dtype=np.int32)
+    for b, hh in bh_pairs:
+        qh_mask[b, hh * G:(hh + 1) * G] = 1
+    return oracle.attend(od, h["q"], h["k"], h["v"], h["pt"], h["lens"], g["block_idx"],
+                         g["n_blocks"], qh_mask=qh_mask)
+
+
 def compare_step(g: dict, o: dict, h: dict, od: oracle.Dims, bh_pairs, dense: bool = True):
     """Bit-exact integer outputs and toleranced float outputs on the (b, h) pairs given
-    (with per-head selection, the selection rows of every query head of kv head h)."""
+    (with per-head selection, the selection rows of every query head of kv head h). FP8
+    keys: the selection is checked for validity within the fp32 bound instead
+    (fp8_reference) and the outputs against the oracle's attention over it."""
     G = od.hq // od.hkv
     stats = []
+    fp8 = bool(od.key_fp8)
+    if fp8:
+        o = dict(o)
+        o["out"], o["lse"] = fp8_reference(g, o, h, od, bh_pairs)
     for b, hh in bh_pairs:
         np.testing.assert_array_equal(g["k_scale"][b, hh], o["k_scale"][b, hh])
         np.testing.assert_array_equal(logical_rows(g["kq"], h["pt"], h["lens"], b, hh),
                                       logical_rows(o["kq"], h["pt"], h["lens"], b, hh))
         for r in (range(hh * G, hh * G + G) if od.per_head else (hh,)):
-            np.testing.assert_array_equal(g["block_max"][b, r], o["block_max"][b, r])
-            np.testing.assert_array_equal(g["chunk_idx"][b, r], o["chunk_idx"][b, r])
-            np.testing.assert_array_equal(g["n_chunks"][b, r], o["n_chunks"][b, r])
-            np.testing.assert_array_equal(g["block_idx"][b, r], o["block_idx"][b, r])
-            np.testing.assert_array_equal(g["n_blocks"][b, r], o["n_blocks"][b, r])
+            # FP8: the selection was validated above; the step's must be the same one (the
+            # same fp32 scorer and exact selection on its maxima)
+            want = g if fp8 else o
+            if not fp8:
+                np.testing.assert_array_equal(g["block_max"][b, r], o["block_max"][b, r])
+                np.testing.assert_array_equal(g["chunk_idx"][b, r], o["chunk_idx"][b, r])
+                np.testing.assert_array_equal(g["n_chunks"][b, r], o["n_chunks"][b, r])
+                np.testing.assert_array_equal(g["block_idx"][b, r], o["block_idx"][b, r])
+                np.testing.assert_array_equal(g["n_blocks"][b, r], o["n_blocks"][b, r])
+            if "step_block_idx" in g:  # the whole decode step's own selection
+                np.testing.assert_array_equal(g["step_block_idx"][b, r], want["block_idx"][b, r])
+                np.testing.assert_array_equal(g["step_n_blocks"][b, r], want["n_blocks"][b, r])
         rows = slice(hh * G, (hh + 1) * G)
         stats.append(assert_close(g["out"][b, rows], o["out"][b, rows], f"sparse out b{b} h{hh}"))
         np.testing.assert_allclose(g["lse"][b, rows], o["lse"][b, rows], atol=2e-4, rtol=1e-5)
+        if "step_out" in g:
+            stats.append(assert_close(g["step_out"][b, rows], o["out"][b, rows],
+                                      f"decode-step out b{b} h{hh}"))
+            np.testing.assert_allclose(g["step_lse"][b, rows], o["lse"][b, rows], atol=2e-4,
+                                       rtol=1e-5)
         if dense:
             stats.append(assert_close(g["out_dense"][b, rows], o["out_dense"][b, rows],
                                       f"dense out b{b} h{hh}"))

@@ -133,7 +133,23 @@ def test_decode_loop_with_selection_reuse(refresh, on_host, key_bits, per_head, 
         kq_o = oracle.quantize_append(od, k_host, pt, lens.numpy(), -1, sc_o, kq_o)
         np.testing.assert_array_equal(H.unpack_codes(kq.cpu().numpy(), key_bits), kq_o)
         qb = W.to_numpy_bits(q)
-        if full:
+        if full and fp8:
+            # FP8 scores have no fixed fp32 order: the step's selection equals hsa_select's on
+            # the same state (the same scorer), which must be valid within the fp32 bound
+            ci2 = torch.full((B, R, cfg.k1), -7, dtype=torch.int32, device=dev)
+            nc2 = torch.full((B, R), -7, dtype=torch.int32, device=dev)
+            bi2, nb2 = torch.full_like(bidx, -7), torch.full_like(nb, -7)
+            hsa.hsa_select(hd, q.to(dev), kq, k_scale, dwl["page_table"], lens.to(dev), ci2, nc2,
+                           bi2, nb2, hsa.workspace(hd, hsa.HSA_OP_SELECT))
+            torch.cuda.synchronize()
+            assert torch.equal(bi2, bidx) and torch.equal(nb2, nb)
+            score, bound = oracle.fp8_block_scores(od, qb, sc_o, kq_o, pt, lens.numpy())
+            bad = oracle.selection_within_bounds(od, lens.numpy(), score, bound,
+                                                 ci2.cpu().numpy(), nc2.cpu().numpy(),
+                                                 bidx.cpu().numpy(), nb.cpu().numpy())
+            assert not bad, bad[:4]
+            sel = {"block_idx": bidx.cpu().numpy(), "n_blocks": nb.cpu().numpy()}
+        elif full:
             sel = oracle.select(od, qb, sc_o, kq_o, pt, lens.numpy())
             np.testing.assert_array_equal(nb.cpu().numpy(), sel["n_blocks"])
             np.testing.assert_array_equal(bidx.cpu().numpy(), sel["block_idx"])

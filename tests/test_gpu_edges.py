@@ -118,8 +118,10 @@ def test_per_head_selection(hq, hkv, key_bits, chunk):
 
 @pytest.mark.parametrize("hq,hkv,per_head", [(8, 2, 0), (16, 2, 0), (4, 1, 0), (8, 2, 1)])
 def test_fp8_keys(hq, hkv, per_head):
-    """FP8 E4M3 key codes: scales amax / 448, codes, fp32 block maxima (as ordered
-    integers) and selections bit-exact against the oracle; outputs within tolerance."""
+    """FP8 E4M3 key codes: scales amax / 448 and codes bit-exact against the oracle; the
+    fp32 block maxima (as ordered integers) within the fp32 bound of the exact scores, the
+    selection valid within that bound, the whole step's selection equal to hsa_select's, and
+    outputs within tolerance of the oracle's attention over the GPU's selection."""
     wl = W.make_workload(_cfg(context=None, context_range=(900, 7000), batch=2, hq=hq, hkv=hkv,
                               paged_permuted=True, key_fp8=1), seed=80 + hq + per_head)
     g, o = _check(wl, per_head=per_head, k1=12, k2=10, sink=24, window=150)
@@ -271,10 +273,11 @@ def _clone(t):
     (300, 8, 8, False, 16, 0), (40, 8, 8, True, 16, 0),
     (0, 6, 9, False, 8, 1), (300, 8, 8, False, 8, 1), (40, 8, 8, True, 16, 1)])
 def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2, on_host, hq, per_head):
-    """The whole step (append ordered before or beside the scorer, prune, attend with the
-    sink and window pages fetched early) equals the separate calls bit for bit, and the
-    oracle on the appended cache; also with K/V in mapped pinned host memory, with groups
-    of 8 query heads, and with per-head selection."""
+    """The whole step (append ordered before or beside the scorer, the selection run inside
+    the attention or by the pruning kernel, the sink and window pages fetched early) equals
+    the separate calls (selection and cache bit for bit, outputs up to the order of the
+    split-K sums), and the oracle on the appended cache; also with K/V in mapped pinned host
+    memory, with groups of 8 query heads, and with per-head selection."""
     cfg = _cfg(context=None, context_range=(700, 5000), batch=3, hq=hq, hkv=2, k1=k1, k2=k2,
                sink=20, window=window, paged_permuted=True)
     wl = W.make_workload(cfg, seed=40 + window, host_pinned=on_host)
@@ -317,7 +320,10 @@ def test_decode_step_matches_separate_calls_and_oracle(window, k1, k2, on_host, 
     assert hsa.hsa_read_device_error(wst) == 0
     assert torch.equal(kq1, kq2) and torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
     assert torch.equal(nb1, nb2) and torch.equal(bidx1, bidx2)
-    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    # the step may split the attention over another number of CTAs than hsa_attend (it needs
+    # no SMs for a pruning kernel): the same sums in another order
+    torch.testing.assert_close(out1, out2, rtol=1e-5, atol=1e-5)
+    torch.testing.assert_close(lse1, lse2, rtol=1e-5, atol=1e-5)
     # oracle on the appended cache
     kh, vh = kc2.cpu(), vc2.cpu()
     h = {"q": W.to_numpy_bits(wl["q"]), "k": W.to_numpy_bits(kh), "v": W.to_numpy_bits(vh),

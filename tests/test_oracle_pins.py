@@ -631,9 +631,10 @@ def test_fp8_worked_examples_and_saturating_append():
 @pytest.mark.parametrize("seed", range(4))
 def test_fp8_scores_exact_on_representable_inputs(seed):
     """Keys that are E4M3 integers times s = 1/8 and queries that are small integers make
-    every product and partial sum exact in fp32, so the fp32 scores must equal the exact
-    rational dot products: block maxima (max over the group, candidate tokens only) checked
-    against exact arithmetic, and both modules against their defining property."""
+    every product and partial sum exact, so the scores must equal the exact rational dot
+    products: block maxima (max over the group, candidate tokens only) checked against exact
+    arithmetic (the exact scores of fp8_block_scores and the fp32 block_max output alike),
+    and both modules against their defining property."""
     rng = np.random.default_rng(700 + seed)
     D, hkv, G = 16, 2, 2
     grid = np.array([v for v in range(1, 449) if v <= 16 or (v <= 32 and v % 2 == 0) or
@@ -657,6 +658,7 @@ def test_fp8_scores_exact_on_representable_inputs(seed):
     kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, ln)
     assert np.all(sc == np.float32(1.0 / 8.0))
     sel = oracle.select(d, bf16_bits(q), sc, kq, pt, ln, want_block_max=True)
+    exact, bound = oracle.fp8_block_scores(d, bf16_bits(q), sc, kq, pt, ln)
     for b in range(2):
         n = int(ln[b])
         for h in range(hkv):
@@ -670,8 +672,10 @@ def test_fp8_scores_exact_on_representable_inputs(seed):
             for kk in range(got.size):
                 if kk in bm:
                     assert got[kk] == bm[kk] / 8.0
+                    assert exact[b, h, kk] == bm[kk] / 8.0 and bound[b, h, kk] > 0
                 else:
                     assert sel["block_max"][b, h, kk] == INT32_MIN
+                    assert exact[b, h, kk] == -np.inf
             cm = {}
             for kk, s_ in bm.items():
                 cm[kk // 2] = max(cm.get(kk // 2, s_), s_)
@@ -688,6 +692,136 @@ def test_fp8_scores_exact_on_representable_inputs(seed):
                 for k_ in cand:
                     if k_ not in kept_b:
                         assert _beats(bm[kk], kk, bm[k_], k_)
+
+
+def _fma32(a, b, c):
+    """IEEE fp32 fused multiply-add a * b + c with one rounding, for float32 arrays: the
+    product is exact in fp64, TwoSum gives the fp64 sum's exact error, and a sum that lands
+    exactly halfway between two fp32 values is settled by that error's sign."""
+    a64, b64, c64 = (np.asarray(x, dtype=np.float64) for x in (a, b, c))
+    p = a64 * b64
+    s = p + c64
+    bv = s - p
+    err = (p - (s - bv)) + (c64 - bv)
+    r = s.astype(np.float32)
+    r64 = r.astype(np.float64)
+    other = np.nextafter(r, np.where(s > r64, np.float32(np.inf), np.float32(-np.inf)))
+    o64 = other.astype(np.float64)
+    mid = (s != r64) & (s == (r64 + o64) / 2)
+    fix = mid & (err != 0) & ((err > 0) == (o64 > r64))
+    return np.where(fix, other, r)
+
+
+def test_fma32_emulation_worked_examples():
+    """The fp32 fused multiply-add emulation: exact cases, a product below half an ulp of
+    the addend that a separately rounded product would lose, and a sum that an fp64 add
+    leaves exactly halfway between two fp32 values (settled by the exact remainder)."""
+    f = np.float32
+    assert _fma32(f(3), f(5), f(7)) == f(22)
+    # 1 + 2^-24 * (1 + 2^-23): the exact sum lies just above the midpoint 1 + 2^-24
+    a, b = f(2.0 ** -24), f(1 + 2.0 ** -23)
+    assert _fma32(a, b, f(1.0)) == np.nextafter(f(1.0), f(2.0))
+    # a product of 2^-24 exactly: a tie, to even (1.0)
+    assert _fma32(f(2.0 ** -12), f(2.0 ** -12), f(1.0)) == f(1.0)
+    # fp64 rounds 1 + 2^-24 + 2^-80 to the midpoint 1 + 2^-24; the remainder decides: up
+    a, b = f(2.0 ** -24 * (1 + 2.0 ** -23)), f(1 + 2.0 ** -23)
+    exact_above_mid = _fma32(a, b, f(1.0))
+    assert exact_above_mid == np.nextafter(f(1.0), f(2.0))
+
+
+def _two_modules(bm_row, k1, k2, per):
+    """Both modules by their definition on one row of block scores (-inf: no candidate)."""
+    cs = {}
+    for k in np.nonzero(np.isfinite(bm_row))[0]:
+        cs[k // per] = max(cs.get(k // per, -np.inf), bm_row[k])
+    kept_c = sorted(sorted(cs, key=lambda c: (-cs[c], c))[:k1])
+    cand = [k for c in kept_c for k in range(c * per, c * per + per)
+            if k < bm_row.size and np.isfinite(bm_row[k])]
+    return kept_c, sorted(sorted(cand, key=lambda k: (-bm_row[k], k))[:k2])
+
+
+def _as_selection(d, rows):
+    """[1][R][K] padded arrays of (kept chunks, kept blocks) lists, one per row."""
+    R = len(rows)
+    ci = np.full((1, R, d.k1), -1, np.int32)
+    bi = np.full((1, R, d.k2), -1, np.int32)
+    nc = np.zeros((1, R), np.int32)
+    nb = np.zeros((1, R), np.int32)
+    for r, (kc, kb) in enumerate(rows):
+        ci[0, r, :len(kc)] = kc
+        bi[0, r, :len(kb)] = kb
+        nc[0, r], nb[0, r] = len(kc), len(kb)
+    return ci, nc, bi, nb
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_fp8_exact_scores_bound_an_fp32_chain(seed):
+    """FP8 scores on inputs fp32 cannot represent exactly. The oracle's exact block scores
+    (fp8_block_scores) against an fp32 chain of fused multiply-adds in channel order,
+    emulated here with one rounding per term: every chain block maximum lies within the
+    oracle's bound, some differ from the exact score (the bound is exercised), and the
+    bound equals Higham's gamma_128 (recursive summation, u = 2^-24) times the largest
+    sum |q' x| of the block computed here. The validity check accepts the chain's own
+    two-module selection and the oracle's, and rejects one kept block swapped for a clearly
+    worse candidate, and a count one short (the weakest kept block left out)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(900 + seed)
+    D, hkv, G = 128, 2, 4
+    n = int(rng.integers(300, 700))
+    case = random_case(rng, B=1, hq=hkv * G, hkv=hkv, D=D, lens=(n,), perm=True)
+    for h in range(hkv):  # outlier channels, as in the workloads
+        case["ks"][0][h][:, rng.choice(D, 4, replace=False)] *= 8
+    case["k"], case["pt"], case["lens"] = paged(case["ks"], 16, hkv, rng.permutation(
+        case["k"].shape[0]))
+    k1, k2, sink, window, per = 6, 9, 16, 40, 4
+    d = dims_for(case, hkv * G, hkv, D, chunk=64, block=16, k1=k1, k2=k2, sink=sink,
+                 window=window)
+    d.key_fp8 = 1
+    kb, qb = bf16_bits(case["k"]), bf16_bits(case["q"])
+    kq, sc = oracle.quantize_keys(d, kb, case["pt"], case["lens"])
+    score, bound = oracle.fp8_block_scores(d, qb, sc, kq, case["pt"], case["lens"])
+    codes = logical_codes(kq, case["pt"], case["lens"], 16, hkv)[0]  # [Hkv][n][D]
+    x = torch.from_numpy(codes.view(np.uint8).copy()).view(torch.float8_e4m3fn).float().numpy()
+    u = 2.0 ** -24
+    gamma = 128 * u / (1 - 128 * u)
+    rows = []
+    for h in range(hkv):
+        qf = case["q"][0, h * G:(h + 1) * G].astype(np.float32) * sc[0, h]  # fp32 products
+        acc = np.zeros((G, n), np.float32)
+        for c in range(D):
+            acc = _fma32(np.broadcast_to(qf[:, c:c + 1], (G, n)),
+                         np.broadcast_to(x[h, :, c], (G, n)), acc)
+        mag = np.abs(qf.astype(np.float64)[:, None, :] * x[h].astype(np.float64)[None]).sum(-1)
+        chain = np.full(d.max_blocks, -np.inf)
+        want_bound = np.zeros(d.max_blocks)
+        for t in range(sink, n - window):
+            chain[t // 16] = max(chain[t // 16], acc[:, t].max())
+            want_bound[t // 16] = max(want_bound[t // 16], gamma * mag[:, t].max())
+        valid = np.isfinite(score[0, h])
+        assert (np.isfinite(chain) == valid).all()
+        diff = np.abs(chain[valid] - score[0, h][valid])
+        assert (diff <= bound[0, h][valid]).all()
+        assert (diff > 0).any()
+        np.testing.assert_allclose(bound[0, h][valid], want_bound[valid], rtol=1e-12)
+        rows.append(_two_modules(chain, k1, k2, per))
+    lens = case["lens"]
+    assert oracle.selection_within_bounds(d, lens, score, bound, *_as_selection(d, rows)) == []
+    sel = oracle.select(d, qb, sc, kq, case["pt"], lens)
+    assert oracle.selection_within_bounds(d, lens, score, bound, sel["chunk_idx"],
+                                          sel["n_chunks"], sel["block_idx"],
+                                          sel["n_blocks"]) == []
+    # planted mistakes: the best kept block replaced by the worst candidate; a short count
+    kc0, kb0 = rows[0]
+    cand = [k for c in kc0 for k in range(c * per, c * per + per) if np.isfinite(score[0, 0, k])]
+    best = max(kb0, key=lambda k: score[0, 0, k])
+    worst = min(set(cand) - set(kb0), key=lambda k: score[0, 0, k])
+    assert score[0, 0, best] - bound[0, 0, best] > score[0, 0, worst] + bound[0, 0, worst]
+    swapped = [(kc0, sorted(set(kb0) - {best} | {worst}))] + rows[1:]
+    bad = oracle.selection_within_bounds(d, lens, score, bound, *_as_selection(d, swapped))
+    assert [v[2] for v in bad] == ["block order"]
+    short = [(kc0, sorted(set(kb0) - {min(kb0, key=lambda k: score[0, 0, k])}))] + rows[1:]
+    bad = oracle.selection_within_bounds(d, lens, score, bound, *_as_selection(d, short))
+    assert [v[2] for v in bad] == ["block count"]
 
 
 def test_candidate_region_masks_sink_and_window_tokens():

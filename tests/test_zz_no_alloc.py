@@ -26,22 +26,27 @@ def _inputs(wl, d):
 
 def _outputs(d):
     dev = torch.device("cuda")
-    return (torch.full((d.batch, d.hkv, d.k1), -7, dtype=torch.int32, device=dev),
-            torch.full((d.batch, d.hkv), -7, dtype=torch.int32, device=dev),
-            torch.full((d.batch, d.hkv, d.k2), -7, dtype=torch.int32, device=dev),
-            torch.full((d.batch, d.hkv), -7, dtype=torch.int32, device=dev))
+    rows = d.hq if d.per_head else d.hkv  # selection rows per sequence
+    return (torch.full((d.batch, rows, d.k1), -7, dtype=torch.int32, device=dev),
+            torch.full((d.batch, rows), -7, dtype=torch.int32, device=dev),
+            torch.full((d.batch, rows, d.k2), -7, dtype=torch.int32, device=dev),
+            torch.full((d.batch, rows), -7, dtype=torch.int32, device=dev))
 
 
 def test_noalloc_select_matches_workspace_select_twice():
-    """Two calls in a row on different shapes (the second one finds the first one's data in
-    the shared array) give exactly the index sets and counts of hsa_select."""
+    """Calls in a row on different shapes (each one finds the previous one's data in the
+    shared array), with shared and per-head selection, give exactly the index sets and
+    counts of hsa_select, and leave the array's error word clear."""
     cases = [
-        W.make_workload(W.with_context(W.CONFIGS["llama3-8b-128k"], 50001), seed=3,
-                        device="cuda"),
-        W.make_workload(W.CONFIGS["paged-b8-32k-128k"], seed=4, device="cuda"),
+        (W.make_workload(W.with_context(W.CONFIGS["llama3-8b-128k"], 50001), seed=3,
+                         device="cuda"), 0),
+        (W.make_workload(W.CONFIGS["paged-b8-32k-128k"], seed=4, device="cuda"), 0),
+        (W.make_workload(W.with_context(W.CONFIGS["llama3-8b-128k"], 30000), seed=5,
+                         device="cuda"), 1),
     ]
-    for wl in cases:
-        d, _ = H.dims_pair(wl)
+    assert hsa.hsa_read_device_error(None) == 0
+    for wl, per_head in cases:
+        d, _ = H.dims_pair(wl, per_head=per_head)
         dwl, kq, k_scale = _inputs(wl, d)
         ref = _outputs(d)
         hsa.hsa_select(d, dwl["q"], kq, k_scale, dwl["page_table"], dwl["seq_lens"], *ref,
@@ -53,6 +58,7 @@ def test_noalloc_select_matches_workspace_select_twice():
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
         assert int(got[3].min()) > 0
+        assert hsa.hsa_read_device_error(None) == 0
 
 
 def test_noalloc_select_rejects_shapes_beyond_its_scratch():
