@@ -178,7 +178,8 @@ hsa::BlockCache block_cache_at(const Shape& s, void* buf, int capacity) {
 }
 
 struct StepLayout {
-  size_t block_max, tile_max, block_idx, n_blocks, sel_pages, q, k_new, v_new, out, lse;
+  size_t block_max, tile_max, row_range, block_idx, n_blocks, sel_pages, q, k_new, v_new, out,
+      lse;
   AttendLayout att;
   CacheScratch cache;
   size_t end;
@@ -187,7 +188,8 @@ StepLayout step_layout(const Shape& s) {
   StepLayout l;
   l.block_max = kErrBytes;
   l.tile_max = l.block_max + select_bm_bytes(s);
-  l.block_idx = l.tile_max + select_tm_bytes(s);
+  l.row_range = l.tile_max + select_tm_bytes(s);  // [B][rows][4] words
+  l.block_idx = l.row_range + up((size_t)s.batch * s.sel_rows() * 16);
   l.n_blocks = l.block_idx + up((size_t)s.batch * s.sel_rows() * std::max(s.k2, 1) * 4);
   l.sel_pages = l.n_blocks + up((size_t)s.batch * s.sel_rows() * 4);
   l.q = l.sel_pages + up((size_t)s.batch * s.sel_rows() * std::max(s.k2, 1) * 4);
@@ -366,12 +368,14 @@ inline cudaStream_t as_stream(void* p) { return reinterpret_cast<cudaStream_t>(p
 
 int32_t do_score(const Shape& s, const void* q, const int8_t* kq, const float* k_scale,
                  const int32_t* page_table, const int32_t* seq_lens, int32_t* block_max,
-                 int32_t* tile_max, int* err, cudaStream_t st) {
+                 int32_t* tile_max, int* err, cudaStream_t st, unsigned* row_range = nullptr,
+                 const hsa::AppendArgs* app = nullptr) {
   CUtensorMap map, map4;
   int32_t rc = encode_kq_map(s, kq, &map, &map4);
   if (rc != HSA_OK) return rc;
   return cuda_status(hsa::launch_score_blocks(s, map, map4, q, k_scale, page_table, seq_lens,
-                                              block_max, tile_max, err, num_sms(), st));
+                                              block_max, tile_max, row_range, app, err,
+                                              num_sms(), st));
 }
 
 int32_t check_prune_fits(const Shape& s0) {
@@ -734,25 +738,31 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
                               k_scale, page_table, seq_lens, err, st, false);
     if (e != cudaSuccess) return HSA_ERR_CUDA;
   }
-  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st);
+  // K/V in device memory: the sparse attention runs both pruning modules itself when they
+  // fit its shared memory (no pruning kernel, no kept-block list round trip in between); the
+  // scorer then records each row's range of maxima for its selection
+  // and, with a window, appends the new token itself (one kernel fewer between the two)
+  const Shape sa = attend_shape(s, false);
+  const bool fused = block_cache == nullptr && !d->kv_on_host &&
+                     hsa::attend_select_supported(sa, aligned(page_table, 16));
+  unsigned* row_range = reinterpret_cast<unsigned*>(ws + l.row_range);
+  const hsa::AppendArgs app = {kn, vn, const_cast<void*>(kd), const_cast<void*>(vd), kq};
+  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st,
+                fused ? row_range : nullptr, (fused && beside) ? &app : nullptr);
   if (rc != HSA_OK) return rc;
-  if (beside) {
+  if (beside && !fused) {
     e = hsa::launch_append_kv(s, kn, vn, const_cast<void*>(kd), const_cast<void*>(vd), kq,
                               k_scale, page_table, seq_lens, err, st, true);
     if (e != cudaSuccess) return HSA_ERR_CUDA;
   }
-  // K/V in device memory: the sparse attention runs both pruning modules itself when they
-  // fit its shared memory (no pruning kernel, no kept-block list round trip in between)
-  const Shape sa = attend_shape(s, false);
-  if (block_cache == nullptr && !d->kv_on_host &&
-      hsa::attend_select_supported(sa, aligned(page_table, 16))) {
+  if (fused) {
     hsa::AttendBuffers buf;
     buf.counters = reinterpret_cast<int*>(ws + l.att.counters);
     buf.part_ml = reinterpret_cast<float*>(ws + l.att.part_ml);
     buf.part_o = reinterpret_cast<float*>(ws + l.att.part_o);
     buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(sa, false, false, num_sms(), false));
-    e = hsa::launch_attend_select(sa, q, kd, vd, page_table, seq_lens, bm, tm, bidx, nb, out,
-                                  lse, buf, err, st);
+    e = hsa::launch_attend_select(sa, q, kd, vd, page_table, seq_lens, bm, tm, row_range,
+                                  bidx, nb, out, lse, buf, err, st);
     if (e != cudaSuccess) return HSA_ERR_CUDA;
     return copy_outputs_back(s, io, out, lse, direct_out, st);
   }

@@ -73,6 +73,7 @@ constexpr int kHostThreads = kCompute;
 static_assert(kHostThreads * 16 * 2 == kBlockBytesBf16, "a host-path segment copy: 2 x 16 B a thread");
 constexpr int kMaxSplits = 64;
 constexpr int kTileBlocksSel = 4;              // blocks per 64-token chunk (a scorer tile)
+constexpr int kSelRegVals = 8;  // values a thread of the selecting attention keeps in registers
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNeg = -FLT_MAX;                 // "no token" score
@@ -109,6 +110,7 @@ struct AttArgs {
                          // kv head h / kv_div: hq / hkv with per-head selection, else 1)
   float qscale;  // sm_scale * log2(e)
   int early;     // K/V, q, page table are ready before the selection (whole decode step)
+  unsigned* row_range;  // nullable: [rows][4] words that the last CTA of a row clears
 };
 
 struct Segments {
@@ -454,6 +456,8 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
     }
   }
   if (a.nsplit == 1) {
+    if (a.row_range != nullptr && tid == 0)
+      *reinterpret_cast<uint4*>(a.row_range + ((size_t)b * a.hkv + h) * 4) = make_uint4(0, 0, 0, 0);
     if constexpr (MASS) {
       __syncthreads();
       add_segment_mass<G>(a, b, h, lse2, red);
@@ -541,6 +545,8 @@ __device__ void finish_common(const AttArgs& a, int b, int h, int split, const f
     add_segment_mass<G>(a, b, h, lse2, red);
   }
   if (tid == 0) a.counters[(size_t)b * a.hkv + h] = 0;
+  if (a.row_range != nullptr && tid == 0)
+    *reinterpret_cast<uint4*>(a.row_range + ((size_t)b * a.hkv + h) * 4) = make_uint4(0, 0, 0, 0);
 }
 
 // Block-level state (host path): the two token halves merged into o[G][128]; m, l from the
@@ -969,14 +975,16 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 4 && G <= 4 ? 3 : 1))
 // holds the newest token, which the append beside the scorer writes) are copied before the
 // wait for the scorer, and so is the row of page ids when it fits; after the wait the tile
 // maxima (and the row of block maxima when it fits) are staged, all warps select (module 1:
-// top-K1 chunks; module 2: top-K2 blocks of those chunks, select.cuh), the producer issues
+// top-K1 chunks; module 2: top-K2 blocks of those chunks; select.cuh's three-barrier path
+// on the value range the scorer recorded, its general path otherwise), the producer issues
 // the kept blocks' copies, and the compute warps process the CTA's segments as in the HBM
-// path above.
+// path above. The last CTA of a row clears the row's range words for the next step.
 struct SelArgs {
   const int32_t* block_max;  // [rows][max_pages]
   const int32_t* tile_max;   // [rows][max_tiles]
   int32_t* block_idx;        // [rows][k2] out (split 0): kept blocks ascending, -1 padded
   int32_t* n_blocks;         // [rows] out (split 0)
+  const unsigned* row_range;  // [rows][4] the scorer's range of each row's maxima
   int max_tiles, k1;
   int a_cap;   // ints of area A: the tile maxima, then module 2's values and block ids
   int n2_cap;  // module 2's candidates (4 blocks per kept chunk)
@@ -1126,16 +1134,25 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
   };
 
   // ---- before the wait: the page row (an input) and the sink / window copies
+  // the deferred segment is resolved here too (only its copy waits), by lane j_def
+  int def_k = 0, def_t0 = 0, def_t1 = 0, def_page = -1;
   if (warp == W) {
     if (lane == 0 && use_prow && p_plan.bytes() > 0) {
       mbar_arrive_expect_tx(&sbar[2], p_plan.bytes());
       issue_row(p_plan, &sbar[2]);
     }
-    if (lane < jA && lane != j_def) {
+    if (lane < jA) {
       int k = 0, t0 = 0, t1 = 0;
       const int page = resolve(first + lane * stride, k, t0, t1);
-      meta[lane] = make_int4(k, t0, t1, 0);
-      issue(lane, page);
+      if (lane != j_def) {
+        meta[lane] = make_int4(k, t0, t1, 0);
+        issue(lane, page);
+      } else {
+        def_k = k;
+        def_t0 = t0;
+        def_t1 = t1;
+        def_page = page;
+      }
     }
   }
   if (use_prow) tail_row<NT>(p_plan);
@@ -1153,24 +1170,36 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
       issue_row(r_plan, &sbar[1]);
     }
   }
+  // the row's range of tile and block maxima, recorded by the scorer (zero: none)
+  const uint4 rr = __ldcg(reinterpret_cast<const uint4*>(sa.row_range) + row);
+  const int t_max = (int)(rr.x ^ 0x80000000u), t_min = (int)(~rr.y ^ 0x80000000u);
+  const int b_max = (int)(rr.z ^ 0x80000000u), b_min = (int)(~rr.w ^ 0x80000000u);
   tail_row<NT>(t_plan);
   if (use_row) tail_row<NT>(r_plan);
   if (t_plan.bytes() > 0 && !mbar_wait(&sbar[0], 0)) set_error(a.err, kDevErrTimeout);
   __syncthreads();  // the plain-load tails are visible
 
-  // ---- module 1: top-K1 chunks (ascending)
+  // ---- module 1: top-K1 chunks (ascending); the fast path when the scorer's range is known
   const int* tiles = t_plan.dst();
-  int got1 = 0;
+  int got1 = -1;
   const int keep1 = min(sa.k1, n1);
-  if (keep1 > 0) {
-    int T = INT_MIN, need_eq = 0, eq_total = 0;
-    if (keep1 < n1) {
-      const int3 r = sel_kth_largest<NT>(tiles, n1, keep1, ss, false, 0, 0);
-      T = r.x;
-      need_eq = r.y;
-      eq_total = r.z;
+  constexpr int kRegVals = kSelRegVals;
+  if (n1 > 0 && n1 <= kRegVals * NT && rr.x != 0u && rr.y != 0u) {
+    auto get1 = [&](int x) { return make_int2(tiles[x], c_lo + x); };
+    got1 = sel_fast_reg<NT, kRegVals>(get1, n1, sa.k1, t_min, t_max, ss, kept1);
+  }
+  if (got1 < 0) {
+    got1 = 0;
+    if (keep1 > 0) {
+      int T = INT_MIN, need_eq = 0, eq_total = 0;
+      if (keep1 < n1) {
+        const int3 r = sel_kth_largest<NT>(tiles, n1, keep1, ss, false, 0, 0);
+        T = r.x;
+        need_eq = r.y;
+        eq_total = r.z;
+      }
+      got1 = sel_collect<NT>(tiles, n1, T, need_eq, eq_total, ss, kept1, c_lo);
     }
-    got1 = sel_collect<NT>(tiles, n1, T, need_eq, eq_total, ss, kept1, c_lo);
   }
 
   // ---- module 2: the kept chunks' blocks (outside the candidate region: placeholders never
@@ -1180,68 +1209,79 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
   const int32_t* bm = sa.block_max + row * a.max_pages;
   int* vals2 = area;  // the tile maxima are no longer read (the collect ended on a barrier)
   int* cand2 = area + sa.n2_cap;
+  // the fast path produces the kept block ids straight from registers; otherwise the
+  // candidates are laid out (vals2 / cand2) for the general path, which writes positions
   const int n2 = got1 * P;
-  int valid = 0, mn2 = INT_MAX, mx2 = INT_MIN;
-  for (int x0 = tid; x0 < n2; x0 += 4 * NT) {
-    int v[4], kk[4];
+  const bool range2 = rr.z != 0u && rr.w != 0u;
+  auto get2 = [&](int x) {
+    const int kk = kept1[x / P] * P + x % P;
+    const bool in = kk >= k_lo && kk < k_hi;
+    return make_int2(in ? (use_row ? brow[kk - k_lo] : __ldcg(bm + kk)) : INT_MIN, kk);
+  };
+  int got2 = -1;
+  bool ids = false;  // selb holds block ids (fast path) rather than positions in cand2
+  if (range2 && n2 > 0 && n2 <= kRegVals * NT) {
+    got2 = sel_fast_reg<NT, kRegVals>(get2, n2, a.k2, b_min, b_max, ss, selb);
+    ids = got2 >= 0;
+  }
+  if (got2 < 0) {
+    int valid = 0, mn2 = INT_MAX, mx2 = INT_MIN;
+    for (int x0 = tid; x0 < n2; x0 += 4 * NT) {
+      int2 e[4];
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const int x = x0 + u * NT;
-      kk[u] = x < n2 ? kept1[x / P] * P + x % P : -1;
-      const bool in = kk[u] >= k_lo && kk[u] < k_hi;
-      v[u] = in ? (use_row ? brow[kk[u] - k_lo] : __ldcg(bm + kk[u])) : INT_MIN;
-    }
+      for (int u = 0; u < 4; u++) e[u] = x0 + u * NT < n2 ? get2(x0 + u * NT) : make_int2(INT_MIN, -1);
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const int x = x0 + u * NT;
-      if (x < n2) {
-        cand2[x] = kk[u];
-        vals2[x] = v[u];
-        if (v[u] != INT_MIN) {
-          valid++;
-          mn2 = min(mn2, v[u]);
-          mx2 = max(mx2, v[u]);
+      for (int u = 0; u < 4; u++) {
+        const int x = x0 + u * NT;
+        if (x < n2) {
+          cand2[x] = e[u].y;
+          vals2[x] = e[u].x;
+          if (e[u].x != INT_MIN) {
+            valid++;
+            mn2 = min(mn2, e[u].x);
+            mx2 = max(mx2, e[u].x);
+          }
         }
       }
     }
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    valid += __shfl_xor_sync(0xffffffffu, valid, off);
-    mn2 = min(mn2, __shfl_xor_sync(0xffffffffu, mn2, off));
-    mx2 = max(mx2, __shfl_xor_sync(0xffffffffu, mx2, off));
-  }
-  if (lane == 0) {
-    ss.wsum[warp] = valid;
-    ss.mn[warp] = mn2;
-    ss.mx[warp] = mx2;
-  }
-  __syncthreads();
-  int n2_valid = 0;
-#pragma unroll
-  for (int w = 0; w < NT / 32; w++) {
-    n2_valid += ss.wsum[w];
-    mn2 = min(mn2, ss.mn[w]);
-    mx2 = max(mx2, ss.mx[w]);
-  }
-  const int keep2 = min(a.k2, n2_valid);
-  int got2 = 0;
-  if (keep2 > 0) {
-    int T = INT_MIN, need_eq = 0, eq_total = 0;
-    if (keep2 < n2_valid) {
-      const int3 r = sel_kth_largest<NT>(vals2, n2, keep2, ss, true, mn2, mx2);
-      T = r.x;
-      need_eq = r.y;
-      eq_total = r.z;
+    for (int off = 16; off > 0; off >>= 1) {
+      valid += __shfl_xor_sync(0xffffffffu, valid, off);
+      mn2 = min(mn2, __shfl_xor_sync(0xffffffffu, mn2, off));
+      mx2 = max(mx2, __shfl_xor_sync(0xffffffffu, mx2, off));
     }
-    got2 = sel_collect<NT>(vals2, n2, T, need_eq, eq_total, ss, selb, 0);  // positions
-  } else {
-    __syncthreads();  // every thread has read the per-warp totals
+    if (lane == 0) {
+      ss.wsum[warp] = valid;
+      ss.mn[warp] = mn2;
+      ss.mx[warp] = mx2;
+    }
+    __syncthreads();
+    int n2_valid = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; w++) {
+      n2_valid += ss.wsum[w];
+      mn2 = min(mn2, ss.mn[w]);
+      mx2 = max(mx2, ss.mx[w]);
+    }
+    const int keep2 = min(a.k2, n2_valid);
+    got2 = 0;
+    if (keep2 > 0) {
+      int T = INT_MIN, need_eq = 0, eq_total = 0;
+      if (keep2 < n2_valid) {
+        const int3 r = sel_kth_largest<NT>(vals2, n2, keep2, ss, true, mn2, mx2);
+        T = r.x;
+        need_eq = r.y;
+        eq_total = r.z;
+      }
+      got2 = sel_collect<NT>(vals2, n2, T, need_eq, eq_total, ss, selb, 0);  // positions
+    } else {
+      __syncthreads();  // every thread has read the per-warp totals
+    }
   }
   if (use_prow && p_plan.bytes() > 0 && !mbar_wait(&sbar[2], 0)) set_error(a.err, kDevErrTimeout);
   const int* prow = p_plan.dst();
   for (int i = tid; i < got2; i += NT) {
-    const int kk = cand2[selb[i]];
+    const int kk = ids ? selb[i] : cand2[selb[i]];
     selb[i] = kk;
     selp[i] = use_prow ? prow[kk - k_lo] : -1;
   }
@@ -1264,12 +1304,20 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
     // (kept blocks, and sink / window pages beyond the first NS), 32 at a time: the lanes
     // resolve them together; first uses of a ring slot go out from every lane at once, the
     // others from lane 0 in order as the slots free up
-    const int has_def = (j_def >= 0 && j_def < jA) ? 1 : 0;
-    const int n_post = has_def + (cnt - jA);
+    if (j_def >= 0 && j_def < jA) {  // resolved before the wait by lane j_def
+      const int kd = __shfl_sync(0xffffffffu, def_k, j_def);
+      const int t0d = __shfl_sync(0xffffffffu, def_t0, j_def);
+      const int t1d = __shfl_sync(0xffffffffu, def_t1, j_def);
+      const int pd = __shfl_sync(0xffffffffu, def_page, j_def);
+      if (lane == 0) {
+        meta[j_def] = make_int4(kd, t0d, t1d, 0);
+        issue(j_def, pd);
+      }
+    }
+    const int n_post = cnt - jA;
     bool ok = true;
     for (int eb = 0; ok && eb < n_post; eb += 32) {
-      const int e = eb + lane;
-      const int j = e < n_post ? ((has_def && e == 0) ? j_def : jA + e - has_def) : -1;
+      const int j = eb + lane < n_post ? jA + eb + lane : -1;
       int k = 0, t0 = 0, t1 = 0, page = -1;
       if (j >= 0) page = resolve(first + j * stride, k, t0, t1);
       if (j >= 0 && j < NS) {
@@ -1481,6 +1529,11 @@ bool plan_select(const Shape& s, SelArgs& sa, bool stage_pages) {
   if (!HSA_FUSED_SELECT || s.chunk != P * kPage || s.k0 > 0) return false;
   auto up4 = [](long long x) { return (int)((x + 3) / 4 * 4); };
   const long long n1max = ((long long)s.max_pages + P - 1) / P;
+  // Measured on GB300: the kernel beats the pruning kernel + plain attention when every
+  // thread holds its share of a row's chunk scores in registers (rows of up to 8 x threads
+  // chunks: the 128K-token configurations); longer rows go to the pruning kernel, whose
+  // 512 threads select them faster (1M tokens: 196.4 against 198.0 us a step).
+  if (n1max > (long long)kSelRegVals * (W + 1) * 32) return false;
   const long long keep1 = std::min<long long>(s.k1, n1max);
   const long long n2max = keep1 * P;
   sa.n2_cap = up4(std::max<long long>(n2max, 1));
@@ -1603,6 +1656,7 @@ cudaError_t launch_attend(const Shape& s, bool dense, bool host, const void* q,
   a.nsplit = buf.nsplit;
   a.qscale = s.sm_scale * kLog2e;
   a.early = (early && !host) ? 1 : 0;
+  a.row_range = nullptr;
   dim3 grid(buf.nsplit, s.hkv, s.batch);
   switch (s.group) {
     case 1:
@@ -1626,9 +1680,9 @@ bool attend_select_supported(const Shape& s, bool page_table_aligned) {
 cudaError_t launch_attend_select(const Shape& s, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* page_table,
                                  const int32_t* seq_lens, const int32_t* block_max,
-                                 const int32_t* tile_max, int32_t* block_idx, int32_t* n_blocks,
-                                 float* out, float* lse, const AttendBuffers& buf, int* err,
-                                 cudaStream_t st) {
+                                 const int32_t* tile_max, unsigned* row_range,
+                                 int32_t* block_idx, int32_t* n_blocks, float* out, float* lse,
+                                 const AttendBuffers& buf, int* err, cudaStream_t st) {
   if (buf.nsplit < 1 || buf.nsplit > kMaxSplits) return cudaErrorInvalidValue;
   const bool stage_pages = (reinterpret_cast<uintptr_t>(page_table) & 15) == 0;
   SelArgs sa;
@@ -1637,8 +1691,11 @@ cudaError_t launch_attend_select(const Shape& s, const void* q, const void* k_ca
   if ((reinterpret_cast<uintptr_t>(block_max) & 15) != 0 ||
       (reinterpret_cast<uintptr_t>(tile_max) & 15) != 0)
     return cudaErrorInvalidValue;
+  if (row_range == nullptr || (reinterpret_cast<uintptr_t>(row_range) & 15) != 0)
+    return cudaErrorInvalidValue;
   sa.block_max = block_max;
   sa.tile_max = tile_max;
+  sa.row_range = row_range;
   sa.block_idx = block_idx;
   sa.n_blocks = n_blocks;
   sa.max_tiles = (s.max_pages + kTileBlocksSel - 1) / kTileBlocksSel;
@@ -1666,6 +1723,7 @@ cudaError_t launch_attend_select(const Shape& s, const void* q, const void* k_ca
   a.nsplit = buf.nsplit;
   a.qscale = s.sm_scale * kLog2e;
   a.early = 1;
+  a.row_range = row_range;
   dim3 grid(buf.nsplit, s.hkv, s.batch);
   switch (s.group) {
     case 1: return launch_select_g<1>(a, sa, grid, st);

@@ -46,12 +46,27 @@ cudaError_t launch_stage_io(const Shape& s, const void* q, const void* k_new, co
 // ---- score.cu
 // block_max: [B][Hkv][max_pages]; tile_max (nullable): [B][Hkv][score_max_tiles], the max of
 // each 64-token tile, which the prune kernel uses as the chunk score when chunks are 64.
+// row_range (nullable): [rows][4] words raised by atomicMax to the row's range of maxima,
+// (max tile, ~min tile, max block, ~min block) as order-preserving unsigned images
+// ((unsigned)v ^ 0x80000000); zero before the scorer runs (a word left from an earlier call
+// only widens the range); launch_attend_select reads and clears them.
+// app (nullable): the decode step's append of the new token (k_new, v_new [B][Hkv][128] bf16
+// into slot N_b - 1 of k_cache / v_cache, its codes into kq), done by the scorer's last CTA
+// beside its scan; only valid when that slot is not a candidate (a window of >= 1 token).
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  int8_t* kq;
+};
 int score_max_tiles(const Shape& s);
 cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
                                 const CUtensorMap& kq_map4, const void* q,
                                 const float* k_scale, const int32_t* page_table,
                                 const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
-                                int* err, int num_sms, cudaStream_t st);
+                                unsigned* row_range, const AppendArgs* app, int* err,
+                                int num_sms, cudaStream_t st);
 
 // ---- prune.cu
 // page_table / sel_pages (both nullable): also write the page of every kept block into
@@ -126,8 +141,8 @@ bool attend_select_supported(const Shape& s, bool page_table_aligned);
 cudaError_t launch_attend_select(const Shape& s, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* page_table,
                                  const int32_t* seq_lens, const int32_t* block_max,
-                                 const int32_t* tile_max, int32_t* block_idx, int32_t* n_blocks,
-                                 float* out, float* lse, const AttendBuffers& buf, int* err,
-                                 cudaStream_t st);
+                                 const int32_t* tile_max, unsigned* row_range,
+                                 int32_t* block_idx, int32_t* n_blocks, float* out, float* lse,
+                                 const AttendBuffers& buf, int* err, cudaStream_t st);
 
 }  // namespace hsa

@@ -12,11 +12,14 @@
 // Data: a CTA owns one (sequence, kv head) and a run of pages; thread t owns token slot
 // t / 16 and the 8 channels [8 (t % 16), 8 (t % 16) + 8) of every page it visits, so each
 // warp reads 512 contiguous bytes of bf16 per page with 16-byte loads.
+#include "append.cuh"
 #include "common.cuh"
 #include "internal.h"
 
 namespace hsa {
 namespace {
+
+using namespace append_detail;
 
 constexpr int kThreads = 256;        // 16 slots x 16 channel groups of 8
 constexpr int kPagesPerCta = 32;
@@ -25,72 +28,9 @@ __device__ __forceinline__ bool seq_ok(int n, int max_pages) {
   return n >= 0 && n <= max_pages * kPage;
 }
 
-__device__ __forceinline__ void unpack8(const uint4& u, float f[8]) {
-  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
-  f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
-  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
-  f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
-}
-
-// Eight 4-bit codes in one word: code 2i in the low nibble of byte i, code 2i + 1 in the high.
-__device__ __forceinline__ uint32_t pack_codes4(const int c[8]) {
-  uint32_t r = 0;
-#pragma unroll
-  for (int i = 0; i < 4; i++)
-    r |= (uint32_t)((c[2 * i] & 0xF) | ((c[2 * i + 1] & 0xF) << 4)) << (8 * i);
-  return r;
-}
-
-__device__ __forceinline__ uint2 pack_codes(const int c[8]) {
-  uint2 r;
-  r.x = (c[0] & 0xFF) | ((c[1] & 0xFF) << 8) | ((c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
-  r.y = (c[4] & 0xFF) | ((c[5] & 0xFF) << 8) | ((c[6] & 0xFF) << 16) | ((uint32_t)(c[7] & 0xFF) << 24);
-  return r;
-}
-
-// The codes of 8 consecutive channels at element offset `off` of the key-code cache:
-// 8 bytes of 8-bit codes, or 4 bytes of 4-bit codes at half the offset.
-__device__ __forceinline__ void store_codes(int8_t* kq, size_t off, const int c[8], int bits) {
-  if (bits == 4)
-    *reinterpret_cast<uint32_t*>(kq + off / 2) = pack_codes4(c);
-  else
-    *reinterpret_cast<uint2*>(kq + off) = pack_codes(c);
-}
-
-// Key formats: the integer code widths 8 and 4, and FP8 E4M3 codes (8-bit layout).
-constexpr int kFmtFp8 = 0xF8;
-
 // Divisor of amax giving the key scale: the largest code magnitude of the format.
 __device__ __forceinline__ float scale_divisor(int fmt) {
   return fmt == kFmtFp8 ? 448.0f : (float)key_levels(fmt);
-}
-
-// E4M3 codes of four f32 values (byte i of the result <- x[i]): round to nearest even,
-// saturating at +-448.
-__device__ __forceinline__ uint32_t e4m3x4(const float x[4]) {
-  unsigned short lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x[1]), "f"(x[0]));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x[3]), "f"(x[2]));
-  return (uint32_t)lo | ((uint32_t)hi << 16);
-}
-
-// The codes of the 8 values f (channel scales s) at element offset `off`, in format fmt:
-// integer codes clamp(rint_even(f32(f / s)), +-levels), or E4M3 codes of f32(f / s); a zero
-// scale gives code 0.
-__device__ __forceinline__ void store_key_codes(int8_t* kq, size_t off, const float f[8],
-                                                const float s[8], int fmt) {
-  if (fmt == kFmtFp8) {
-    float x[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++) x[i] = s[i] == 0.0f ? 0.0f : __fdiv_rn(f[i], s[i]);
-    *reinterpret_cast<uint2*>(kq + off) = make_uint2(e4m3x4(x), e4m3x4(x + 4));
-    return;
-  }
-  const int levels = key_levels(fmt);
-  int c[8];
-#pragma unroll
-  for (int i = 0; i < 8; i++) c[i] = key_code(f[i], s[i], levels);
-  store_codes(kq, off, c, fmt);
 }
 
 // Pass 1 of full quantisation: amax per (b, h, channel) over tokens t < N_b, as the bit
@@ -194,13 +134,6 @@ __global__ void __launch_bounds__(kThreads) key_codes_kernel(
 // With `beside` (whole decode step only, where the predecessor is the scorer, which neither
 // writes this kernel's inputs nor reads the slot it writes) the kernel runs concurrently
 // with its predecessor and waits for it only before exiting; otherwise it waits first.
-__device__ __forceinline__ void append_body(const uint4* __restrict__ k_new,
-                                            const uint4* __restrict__ v_new,
-                                            __nv_bfloat16* k_cache, __nv_bfloat16* v_cache,
-                                            int8_t* kq, const float* __restrict__ k_scale,
-                                            const int32_t* __restrict__ page_table,
-                                            const int32_t* __restrict__ seq_lens, int hkv,
-                                            int max_pages, int num_pages, int* err, int bits);
 
 __global__ void append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
                                  __nv_bfloat16* k_cache, __nv_bfloat16* v_cache, int8_t* kq,
@@ -210,42 +143,11 @@ __global__ void append_kv_kernel(const uint4* __restrict__ k_new, const uint4* _
                                  int num_pages, int* err, int beside, int bits) {
   if (!beside) grid_dep_wait();
   grid_dep_launch();
-  append_body(k_new, v_new, k_cache, v_cache, kq, k_scale, page_table, seq_lens, hkv, max_pages,
-              num_pages, err, bits);
+  append_token(blockIdx.x, threadIdx.x, k_new, v_new, k_cache, v_cache, kq, k_scale, page_table,
+               seq_lens, hkv, max_pages, num_pages, err, bits);
   grid_dep_wait();
 }
 
-__device__ __forceinline__ void append_body(const uint4* __restrict__ k_new,
-                                            const uint4* __restrict__ v_new,
-                                            __nv_bfloat16* k_cache, __nv_bfloat16* v_cache,
-                                            int8_t* kq, const float* __restrict__ k_scale,
-                                            const int32_t* __restrict__ page_table,
-                                            const int32_t* __restrict__ seq_lens, int hkv,
-                                            int max_pages, int num_pages, int* err, int bits) {
-  const int b = blockIdx.x;
-  const int h = threadIdx.x >> 4, grp = threadIdx.x & 15;
-  if (h >= hkv) return;
-  const int n = seq_lens[b];
-  if (n < 1 || n > max_pages * kPage) {
-    set_error(err, kDevErrCheck);
-    return;
-  }
-  const int t = n - 1;
-  const int page = page_table[(size_t)b * max_pages + t / kPage];
-  if (page < 0 || page >= num_pages) {
-    set_error(err, kDevErrCheck);
-    return;
-  }
-  const size_t off = (((size_t)page * hkv + h) * kPage + t % kPage) * kHeadDim + grp * 8;
-  const size_t src = ((size_t)b * hkv + h) * (kHeadDim / 8) + grp;
-  const uint4 kv = k_new[src];
-  *reinterpret_cast<uint4*>(k_cache + off) = kv;
-  *reinterpret_cast<uint4*>(v_cache + off) = v_new[src];
-  float f[8];
-  unpack8(kv, f);
-  const float* s = k_scale + ((size_t)b * hkv + h) * kHeadDim + grp * 8;
-  store_key_codes(kq, off, f, s, bits);
-}
 
 // The kernels' key-format code of a shape.
 int key_format(const Shape& s) { return s.key_fp8 ? kFmtFp8 : s.key_bits; }

@@ -25,6 +25,7 @@
 
 #include <cuda_fp16.h>
 
+#include "append.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -104,6 +105,17 @@ struct ScoreArgs {
   const int32_t* seq_lens;
   int32_t* block_max;
   int32_t* tile_max;  // nullable: max of each 64-token tile's blocks (= chunk max for chunk 64)
+  // nullable: [rows][4] running range of each row's maxima, order-preserving unsigned words
+  // raised with atomicMax (zero: empty): max tile, ~min tile, max block, ~min block
+  unsigned* row_range;
+  // nullable: the decode step's append, done by the last CTA beside the scan (the new token
+  // at slot N - 1 is never a candidate: the step has a window of at least one token)
+  const uint4* k_new;
+  const uint4* v_new;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  int8_t* kq_out;
+  int key_fmt;
   int* err;
   int batch, hkv, max_pages, max_tiles, num_pages, sink, window;
 };
@@ -246,6 +258,9 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
   return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
 
+// Order-preserving unsigned image of an int (for atomicMax on the row ranges).
+__device__ __forceinline__ unsigned range_key(int v) { return (unsigned)v ^ 0x80000000u; }
+
 // PH: per-head selection, the maxima of every query head (rows b * hq + h * G + j) rather
 // than of the group's token scores.
 template <int G, int KF, bool PH>
@@ -306,9 +321,19 @@ __global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF,
   }
   __syncthreads();
 
+  // the CTA that appends (the last) takes about 1.5 us worth of tiles fewer
   const long long total = prefix[a.batch];
-  const int f0 = (int)(total * blockIdx.x / gridDim.x);
-  const int f1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  const long long hcap = a.k_new != nullptr ? (KB4 ? 8 : 4) : 0;
+  const int f0 = (int)((total + hcap) * blockIdx.x / gridDim.x);
+  const int f1 = (int)min(total, (total + hcap) * (blockIdx.x + 1) / gridDim.x);
+  if (a.k_new != nullptr && blockIdx.x == gridDim.x - 1 && warp < C::kWarps) {
+    // the append (its producer warp is already streaming this CTA's tiles)
+    const int per_seq = a.hkv * 16;
+    for (int i = threadIdx.x; i < a.batch * per_seq; i += C::kWarps * 32)
+      append_token(i / per_seq, i % per_seq, a.k_new, a.v_new, a.k_cache, a.v_cache, a.kq_out,
+                   a.k_scale, a.page_table, a.seq_lens, a.hkv, a.max_pages, a.num_pages, a.err,
+                   a.key_fmt);
+  }
   if (f0 >= f1) return;
 
   int b = 0;
@@ -410,6 +435,23 @@ __global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF,
   const uint32_t qs_addr = smem_addr(qs);
   int cur_b = -1, cur_h = -1;
   SeqRange sr = seq_range(a, lens[b]);
+  // this lane's running range of the current (b, h)'s maxima, flushed when (b, h) changes
+  constexpr int kRows = PH ? G : 1;
+  unsigned rng[kRows][4];
+#pragma unroll
+  for (int jr = 0; jr < kRows; jr++) rng[jr][0] = rng[jr][1] = rng[jr][2] = rng[jr][3] = 0u;
+  auto flush_range = [&](int fb, int fh) {
+#pragma unroll
+    for (int jr = 0; jr < kRows; jr++) {
+      const size_t row = PH ? ((size_t)fb * a.hkv + fh) * G + jr : (size_t)fb * a.hkv + fh;
+#pragma unroll
+      for (int w = 0; w < 4; w++) {
+        const unsigned v = __reduce_max_sync(0xffffffffu, rng[jr][w]);
+        if (lane == 0 && v != 0u) atomicMax(a.row_range + row * 4 + w, v);
+        rng[jr][w] = 0u;
+      }
+    }
+  };
   for (int j = warp; f0 + j < f1; j += C::kWarps) {
     const int f = f0 + j;
     while (prefix[b + 1] <= f) {
@@ -420,6 +462,7 @@ __global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF,
     const int h = r / sr.ntile;
     const int tile = sr.tile_lo + r % sr.ntile;
     if (b != cur_b || h != cur_h) {
+      if (a.row_range != nullptr && cur_b >= 0) flush_range(cur_b, cur_h);
       if constexpr (C::kQSmem) {
         __syncwarp();  // every lane is done reading the previous words
         if constexpr (KF == kKeyFp8)
@@ -541,7 +584,6 @@ __global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF,
     }
     // block and tile maxima of the token scores (the max over the group's heads), or of each
     // head's own dot products with per-head selection
-    constexpr int kRows = PH ? G : 1;
 #pragma unroll
     for (int jr = 0; jr < kRows; jr++) {
       const size_t row = PH ? ((size_t)b * a.hkv + h) * G + jr : (size_t)b * a.hkv + h;
@@ -561,16 +603,25 @@ __global__ void __launch_bounds__(ScoreCfg<G, KF, PH>::kThreads, ScoreCfg<G, KF,
         g = max(g, __shfl_xor_sync(0xffffffffu, g, 1));
         if ((lane & 15) == 0) {
           const int k = tile * kTileBlocks + half * 2 + (lane >> 4);
-          if (k >= sr.k_lo && k < sr.k_hi) a.block_max[row * a.max_pages + k] = g;
+          if (k >= sr.k_lo && k < sr.k_hi) {
+            a.block_max[row * a.max_pages + k] = g;
+            rng[jr][2] = max(rng[jr][2], range_key(g));
+            rng[jr][3] = max(rng[jr][3], ~range_key(g));
+          }
         }
         tmax = max(tmax, g);
       }
       tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
       if (a.tile_max != nullptr && lane == 0) a.tile_max[row * a.max_tiles + tile] = tmax;
+      if (lane == 0) {
+        rng[jr][0] = max(rng[jr][0], range_key(tmax));
+        rng[jr][1] = max(rng[jr][1], ~range_key(tmax));
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
+  if (a.row_range != nullptr && cur_b >= 0) flush_range(cur_b, cur_h);
 }
 
 }  // namespace
@@ -581,7 +632,8 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
                                 const CUtensorMap& kq_map4, const void* q,
                                 const float* k_scale, const int32_t* page_table,
                                 const int32_t* seq_lens, int32_t* block_max, int32_t* tile_max,
-                                int* err, int num_sms, cudaStream_t st) {
+                                unsigned* row_range, const AppendArgs* app, int* err,
+                                int num_sms, cudaStream_t st) {
   if (s.batch > kMaxBatch) return cudaErrorInvalidValue;
   ScoreArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -590,6 +642,13 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
   a.seq_lens = seq_lens;
   a.block_max = block_max;
   a.tile_max = tile_max;
+  a.row_range = row_range;
+  a.k_new = app ? static_cast<const uint4*>(app->k_new) : nullptr;
+  a.v_new = app ? static_cast<const uint4*>(app->v_new) : nullptr;
+  a.k_cache = app ? static_cast<__nv_bfloat16*>(app->k_cache) : nullptr;
+  a.v_cache = app ? static_cast<__nv_bfloat16*>(app->v_cache) : nullptr;
+  a.kq_out = app ? app->kq : nullptr;
+  a.key_fmt = s.key_fp8 ? append_detail::kFmtFp8 : s.key_bits;
   a.err = err;
   a.batch = s.batch;
   a.hkv = s.hkv;

@@ -18,6 +18,11 @@
 
 #include "common.cuh"
 
+// Out-of-line by default; a build may define HSA_SEL_NOINLINE to choose.
+#ifndef HSA_SEL_NOINLINE
+#define HSA_SEL_NOINLINE __noinline__
+#endif
+
 namespace hsa {
 
 constexpr int kSelDigitBits = 11;
@@ -36,6 +41,8 @@ struct SelectShared {
   int cand[kSelSmall];                     // the values of a small bin
   int n_cand;
   int res[3];                              // located bin or value; keys above it; its count
+  unsigned fhist[512];                     // the fast path's histogram (kFastBins), zero
+  int cand_i[kSelSmall];                   // the fast path: indices of the small bin's values
 };
 
 __device__ __forceinline__ unsigned sel_lanemask_lt() {
@@ -44,17 +51,33 @@ __device__ __forceinline__ unsigned sel_lanemask_lt() {
   return m;
 }
 
+// Shared-memory atomics by the shared-window address: the helpers below reach their
+// scratch through references, which the compiler sees as generic addresses.
+// (No memory clobber: loads may be scheduled across it; every later read of the counters
+// comes after a barrier.)
+__device__ __forceinline__ void sel_red_add(unsigned* p, unsigned v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v));
+}
+
+__device__ __forceinline__ int sel_atom_add(int* p, int v) {
+  int old;
+  asm volatile("atom.shared.add.s32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v)
+               : "memory");
+  return old;
+}
+
 // All NT threads; a CTA barrier must follow before the first selection.
 template <int NT>
 __device__ __forceinline__ void sel_init(SelectShared& ss) {
   for (int i = threadIdx.x; i < kSelBins; i += NT) ss.hist[i] = 0u;
+  for (int i = threadIdx.x; i < 512; i += NT) ss.fhist[i] = 0u;
   if (threadIdx.x == 0) ss.n_cand = 0;
 }
 
 // (min, max) of the valid (not INT_MIN) entries of vals[0, n), for every thread; an empty
 // set gives (INT_MAX, INT_MIN). One CTA barrier.
 template <int NT>
-__device__ __noinline__ int2 sel_min_max(const int* vals, int n, SelectShared& ss) {
+__device__ HSA_SEL_NOINLINE int2 sel_min_max(const int* vals, int n, SelectShared& ss) {
   constexpr int kWarps = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int mn = INT_MAX, mx = INT_MIN;
@@ -105,7 +128,7 @@ __device__ __noinline__ int2 sel_min_max(const int* vals, int n, SelectShared& s
 // keys is gathered and ranked by one warp; otherwise the next level counts the next 11 bits
 // of the keys in that bin. Per level: 3 CTA barriers (4 when the small bin is ranked).
 template <int NT>
-__device__ __noinline__ int3 sel_kth_largest(const int* vals, int n, int K, SelectShared& ss,
+__device__ HSA_SEL_NOINLINE int3 sel_kth_largest(const int* vals, int n, int K, SelectShared& ss,
                                              bool have_range, int vmin, int vmax) {
   static_assert(NT >= kSelScan && NT % 32 == 0 && NT <= 32 * kSelMaxWarps, "thread count");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -133,7 +156,7 @@ __device__ __noinline__ int3 sel_kth_largest(const int* vals, int n, int K, Sele
         const unsigned key = (unsigned)v[u] - umin;
         const bool m = v[u] != INT_MIN &&
                        (match_shift >= 32 || (key >> match_shift) == (prefix >> match_shift));
-        if (m) atomicAdd(&ss.hist[(key >> shift) & (kSelBins - 1)], 1u);
+        if (m) sel_red_add(&ss.hist[(key >> shift) & (kSelBins - 1)], 1u);
       }
     }
     __syncthreads();
@@ -197,7 +220,7 @@ __device__ __noinline__ int3 sel_kth_largest(const int* vals, int n, int K, Sele
         for (int u = 0; u < 4; u++) {
           const unsigned key = (unsigned)v[u] - umin;
           if (v[u] != INT_MIN && (key >> match_shift) == (prefix >> match_shift))
-            ss.cand[atomicAdd(&ss.n_cand, 1)] = v[u];
+            ss.cand[sel_atom_add(&ss.n_cand, 1)] = v[u];
         }
       }
       __syncthreads();
@@ -231,7 +254,7 @@ __device__ __noinline__ int3 sel_kth_largest(const int* vals, int n, int K, Sele
 // barrier for the per-warp counts). When all entries equal to T are kept (need_eq ==
 // eq_total), or none are, the test is a plain threshold and no tie ranks are needed.
 template <int NT>
-__device__ __noinline__ int sel_collect(const int* vals, int n, int T, int need_eq, int eq_total,
+__device__ HSA_SEL_NOINLINE int sel_collect(const int* vals, int n, int T, int need_eq, int eq_total,
                                         SelectShared& ss, int* out, int add) {
   constexpr int kWarps = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -317,6 +340,236 @@ __device__ __noinline__ int sel_collect(const int* vals, int n, int T, int need_
   }
   __syncthreads();
   return total;
+}
+
+// ------------------------------------------------ fast path: range known, three barriers
+//
+// When the values' range [vmin, vmax] is known before the selection (the scorer records each
+// row's range of maxima) and every thread can hold its share of the row in registers, a
+// 512-bin histogram of the keys' top 9 bits above vmin is built in the pass that reads the
+// values. Every warp then finds the bin d holding the K-th largest key from the histogram by
+// itself (no scan barrier). When d holds at most 32 values (the usual case: the tile maxima
+// of a 128K-token row put a few values in that bin) one pass gathers them with their indices
+// and counts, per thread, the values in higher bins; every warp ranks the gathered values by
+// itself, which gives T and which equal values are kept; the thread's values, still in
+// registers, are then written in ascending order. Three CTA barriers in all. A larger bin
+// returns -1 and the caller takes the general path (sel_kth_largest, sel_collect).
+constexpr int kFastBinBits = 9;
+constexpr int kFastBins = 1 << kFastBinBits;
+
+__device__ __forceinline__ int fast_shift(int vmin, int vmax) {
+  const unsigned range = (unsigned)vmax - (unsigned)vmin;
+  return max(0, (32 - __clz(range)) - kFastBinBits);
+}
+
+// Bin of v (a value inside the range; clamped, so that a value outside it cannot index past
+// the histogram).
+__device__ __forceinline__ int fast_bin(int v, unsigned umin, int shift) {
+  return (int)min(((unsigned)v - umin) >> shift, (unsigned)(kFastBins - 1));
+}
+
+// Every warp: (d, keys in higher bins, keys in d) for the K-th largest key (0 < K <= the
+// histogram's total). Lane l reads bins 4l..4l+3 of each group of 128 (conflict-free 16-byte
+// reads); warp sums give the groups' totals.
+__device__ __forceinline__ int3 fast_locate(const unsigned* fhist, int K) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t hb = smem_addr(fhist);
+  int part[kFastBins / 128], tot[kFastBins / 128];
+  uint4 c[kFastBins / 128];
+#pragma unroll
+  for (int g = 0; g < kFastBins / 128; g++) c[g] = lds128(hb + (128 * g + 4 * lane) * 4);
+#pragma unroll
+  for (int g = 0; g < kFastBins / 128; g++) {
+    part[g] = (int)(c[g].x + c[g].y + c[g].z + c[g].w);
+    tot[g] = __reduce_add_sync(0xffffffffu, part[g]);
+  }
+  int acc = 0, mine = 0, gsel = 0;
+  uint4 cm = make_uint4(0u, 0u, 0u, 0u);
+  bool found = false;
+#pragma unroll
+  for (int g = kFastBins / 128 - 1; g >= 0; g--) {
+    if (!found && acc + tot[g] >= K) {
+      found = true;
+      gsel = g;
+      mine = part[g];
+      cm = c[g];
+    } else if (!found) {
+      acc += tot[g];
+    }
+  }
+  int incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, incl, off);
+    if (lane + off < 32) incl += y;
+  }
+  const int excl = incl - mine;
+  const int L = __ffs(__ballot_sync(0xffffffffu, acc + excl < K && K <= acc + incl)) - 1;
+  int d = 0, above = 0, cnt = 0;
+  if (lane == L) {
+    const int cb[4] = {(int)cm.x, (int)cm.y, (int)cm.z, (int)cm.w};
+    int a2 = acc + excl;
+    bool f2 = false;
+#pragma unroll
+    for (int b = 3; b >= 0; b--) {
+      if (!f2 && a2 + cb[b] >= K) {
+        f2 = true;
+        d = 128 * gsel + 4 * lane + b;
+        cnt = cb[b];
+      } else if (!f2) {
+        a2 += cb[b];
+      }
+    }
+    above = a2;
+  }
+  return make_int3(__shfl_sync(0xffffffffu, d, L), __shfl_sync(0xffffffffu, above, L),
+                   __shfl_sync(0xffffffffu, cnt, L));
+}
+
+// The fast path for rows of at most R values a thread: each thread keeps its contiguous
+// span of values in registers across the three passes (histogram, gather, write), so a
+// pass is a few instructions a value; the ranking loops run over the bin's count. get(x)
+// returns (value, id) of entry x (value INT_MIN: no candidate); out receives the kept
+// entries' ids in ascending order of x. Returns min(K, valid entries), or -1 (nothing
+// written) when the K-th key's bin holds more than kSelSmall values. Expects fhist and
+// n_cand zero and leaves them zero; three CTA barriers (two when everything is kept).
+template <int NT, int R, typename Get>
+__device__ __forceinline__ int sel_fast_reg(Get get, int n, int K, int vmin, int vmax,
+                                            SelectShared& ss, int* out) {
+  constexpr int kWarps = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned lt = sel_lanemask_lt();
+  const unsigned umin = (unsigned)vmin;
+  const int shift = fast_shift(vmin, vmax);
+  const int per = (n + NT - 1) / NT;  // <= R (the caller checks n <= R * NT)
+  const int x0 = min(n, tid * per), nv = min(n, x0 + per) - x0;
+  int v[R], id[R];
+  unsigned kb[R];
+  int valid = 0;
+#pragma unroll
+  for (int r = 0; r < R; r++) {  // all loads first
+    const int2 e = r < nv ? get(x0 + r) : make_int2(INT_MIN, -1);
+    v[r] = e.x;
+    id[r] = e.y;
+  }
+#pragma unroll
+  for (int r = 0; r < R; r++) {
+    kb[r] = min(((unsigned)v[r] - umin) >> shift, (unsigned)(kFastBins - 1));
+    if (v[r] != INT_MIN) {
+      valid++;
+      sel_red_add(&ss.fhist[kb[r]], 1u);
+    }
+  }
+  const int valid_w = __reduce_add_sync(0xffffffffu, valid);
+  if (lane == 0) ss.wsum[warp] = valid_w;
+  __syncthreads();
+  int n_valid = 0, vbase = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; w++) {
+    const int c = ss.wsum[w];
+    n_valid += c;
+    vbase += w < warp ? c : 0;
+  }
+  const int keep_n = min(K, n_valid);
+  if (keep_n == n_valid) {  // everything valid is kept (also keep_n == 0)
+    int incl = valid;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int pos = vbase + incl - valid;
+#pragma unroll
+    for (int r = 0; r < R; r++)
+      if (v[r] != INT_MIN) out[pos++] = id[r];
+    for (int i = tid; i < kFastBins; i += NT) ss.fhist[i] = 0u;
+    __syncthreads();
+    return keep_n;
+  }
+  const int3 loc = fast_locate(ss.fhist, keep_n);
+  const unsigned d = (unsigned)loc.x;
+  const int above = loc.y, cnt = loc.z;
+  if (cnt > kSelSmall) {
+    __syncthreads();  // every warp has read the histogram and the per-warp counts
+    for (int i = tid; i < kFastBins; i += NT) ss.fhist[i] = 0u;
+    __syncthreads();
+    return -1;
+  }
+  int gt = 0;
+#pragma unroll
+  for (int r = 0; r < R; r++) {
+    if (v[r] == INT_MIN) continue;
+    if (kb[r] > d) {
+      gt++;
+    } else if (kb[r] == d) {
+      const int slot = sel_atom_add(&ss.n_cand, 1);
+      if (slot < kSelSmall) {  // (the histogram counted exactly these)
+        ss.cand[slot] = v[r];
+        ss.cand_i[slot] = x0 + r;
+      }
+    }
+  }
+  const int gt_w = __reduce_add_sync(0xffffffffu, gt);
+  if (lane == 0) ss.w_b[warp] = gt_w;
+  __syncthreads();
+  // every warp ranks the bin's values
+  const int c = lane < cnt ? ss.cand[lane] : INT_MIN;
+  const int ci = lane < cnt ? ss.cand_i[lane] : INT_MAX;
+  int gtc = 0, gec = 0;
+  for (int j = 0; j < cnt; j++) {
+    const int cj = __shfl_sync(0xffffffffu, c, j);
+    gtc += cj > c ? 1 : 0;
+    gec += cj >= c ? 1 : 0;
+  }
+  const int need = keep_n - above;
+  const int L = __ffs(__ballot_sync(0xffffffffu, lane < cnt && gtc < need && need <= gec)) - 1;
+  const int T = __shfl_sync(0xffffffffu, c, L);
+  const int need_eq = need - __shfl_sync(0xffffffffu, gtc, L);
+  const int eq_total = __popc(__ballot_sync(0xffffffffu, lane < cnt && c == T));
+  const bool split = need_eq < eq_total;  // only some of the values equal to T are kept
+  bool kp = lane < cnt && c >= T;
+  if (split) {  // rare: ties at the threshold, ranked by index
+    int eq_before = 0;
+    for (int j = 0; j < cnt; j++) {
+      const int cj = __shfl_sync(0xffffffffu, c, j);
+      const int cij = __shfl_sync(0xffffffffu, ci, j);
+      eq_before += (cj == T && cij < ci) ? 1 : 0;
+    }
+    kp = lane < cnt && (c > T || (c == T && eq_before < need_eq));
+  }
+  const unsigned keep = __ballot_sync(0xffffffffu, kp);
+  const int w_first = min(n, warp * 32 * per);
+  int base = __popc(__ballot_sync(0xffffffffu, kp && ci < w_first));
+#pragma unroll
+  for (int w = 0; w < kWarps; w++) base += w < warp ? ss.w_b[w] : 0;
+  bool tk[R];
+  int mine = 0;
+#pragma unroll
+  for (int r = 0; r < R; r++) {
+    bool t = v[r] != INT_MIN && (kb[r] > d || (kb[r] == d && v[r] >= T));
+    if (split && v[r] == T) {
+      int k = 0;
+      for (unsigned m = keep; m != 0u; m &= m - 1)
+        k += ss.cand_i[__ffs(m) - 1] == x0 + r ? 1 : 0;
+      t = k > 0;
+    }
+    tk[r] = t;
+    mine += t ? 1 : 0;
+  }
+  int incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  int pos = base + incl - mine;
+#pragma unroll
+  for (int r = 0; r < R; r++)
+    if (tk[r]) out[pos++] = id[r];
+  for (int i = tid; i < kFastBins; i += NT) ss.fhist[i] = 0u;
+  if (tid == 0) ss.n_cand = 0;
+  __syncthreads();
+  return keep_n;
 }
 
 // A row src[0, n) of ints in global memory (in an array whose base is 16-byte aligned) to be
