@@ -65,9 +65,16 @@ def barrier(world: int) -> None:
 
 
 def job_value(step_ms_max: float, world: int) -> float:
-    """Whole-job µs per decode step: every rank runs its own independent decode problem,
-    so N ranks complete N steps in the slowest rank's step time."""
-    return step_ms_max * 1e3 / world
+    """µs per decode step of the job: every rank runs its own independent decode problem, so
+    a step of the job takes the slowest rank's step time (a latency; N replicas do not make
+    a step faster)."""
+    return step_ms_max * 1e3
+
+
+def job_steps_per_s(step_ms_max: float, world: int) -> float:
+    """Aggregate decode steps per second of the whole job: N independent replicas complete N
+    steps in the slowest rank's step time."""
+    return world / (step_ms_max * 1e-3)
 
 
 # ------------------------------------------------------------ measurement
@@ -494,7 +501,12 @@ def burst_times(case, names, reps: int):
 
 
 def e2e_steps(case, steps: int):
-    """The public whole-step call with pinned host inputs/outputs, synchronised per step."""
+    """The public whole-step call with pinned host inputs and outputs, timed by the host
+    clock (time.perf_counter) around the call and the stream's synchronisation, per step:
+    the plain call through the binding (every argument marshalled, the kernels launched one
+    by one), and its decode-loop form hsa.DecodeStep (arguments marshalled once, the step
+    replayed from the CUDA graph it records on its first call), the latter also with CUDA
+    events on the stream. Returns ({form: mean us}, h2d bytes, d2h bytes)."""
     torch, hsa = case.torch, case.hsa
     c = case.cfg
     q_h = case.q.cpu().pin_memory()
@@ -502,23 +514,42 @@ def e2e_steps(case, steps: int):
     vn_h = case.v_new.cpu().pin_memory()
     out_h = torch.zeros((c.batch, c.hq, 128), dtype=torch.float32).pin_memory()
     lse_h = torch.zeros((c.batch, c.hq), dtype=torch.float32).pin_memory()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # the decode-loop form of the public call: arguments marshalled once per buffer set
-    calls = [hsa.DecodeStep(case.d, q_h, kn_h, vn_h, out_h, lse_h, case.k[r], case.v[r],
+    stream = torch.cuda.current_stream()
+
+    def plain(r):
+        hsa.hsa_decode_step(case.d, q_h, kn_h, vn_h, out_h, lse_h, case.k[r], case.v[r],
                             case.kq[r], case.ks[r], case.pt, case.lens, None, None, case.ws_step,
-                            io_on_host=True, graph=True) for r in range(2)]
-    times = []
+                            io_on_host=True)
+
+    graphs = [hsa.DecodeStep(case.d, q_h, kn_h, vn_h, out_h, lse_h, case.k[r], case.v[r],
+                             case.kq[r], case.ks[r], case.pt, case.lens, None, None,
+                             case.ws_step, io_on_host=True, graph=True) for r in range(2)]
+
+    def host_clock(fn):
+        times = []
+        for i in range(steps + 3):
+            t0 = time.perf_counter()
+            fn(i & 1)
+            stream.synchronize()
+            t1 = time.perf_counter()
+            if i >= 3:
+                times.append((t1 - t0) * 1e6)
+        return statistics.fmean(times)
+
+    res = {"plain_call_us": host_clock(plain), "decode_step_graph_us": host_clock(lambda r: graphs[r]())}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = []
     for i in range(steps + 3):
-        r = i & 1
         e0.record()
-        calls[r]()
+        graphs[i & 1]()
         e1.record()
         e1.synchronize()
         if i >= 3:
-            times.append(e0.elapsed_time(e1))
+            ev.append(e0.elapsed_time(e1) * 1e3)
+    res["decode_step_graph_events_us"] = statistics.fmean(ev)
     h2d = q_h.numel() * 2 + kn_h.numel() * 2 + vn_h.numel() * 2
     d2h = out_h.numel() * 4 + lse_h.numel() * 4
-    return statistics.fmean(times), h2d, d2h
+    return res, h2d, d2h
 
 
 def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, dense=True):
@@ -562,6 +593,7 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
     sel_ms = per["score"] + per["prune"]
     res = {
         "case": case,
+        "dims": case.d,
         "step_ms": step_ms,
         "latency_ms": latency_ms,
         "loop_step_ms": lper["loop"] / case.REFRESH,
@@ -590,7 +622,7 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
 # ------------------------------------------------------------- CPU oracle
 
 def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
-                       warmup: int = 0):
+                       warmup: int = 0, one_thread: bool = True):
     """Time the CPU oracle's per-step work (append codes, query codes + scoring + both
     modules, sparse attention): whole steps, the oracle's OpenMP loop spreading the
     (sequence, kv head) pairs over the host cores, until `budget_s` seconds or `max_samples`
@@ -601,7 +633,15 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
     import oracle
     from kv_cache_int8_gb300 import workloads as W
     cfg = W.CONFIGS[name]
-    wl = W.make_workload(cfg, seed=seed, device="cpu")
+    gen_dev = "cpu"
+    if cfg.context is None or cfg.context > (1 << 17):  # large inputs: drawn on the GPU
+        import torch
+        gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = W.make_workload(cfg, seed=seed, device=gen_dev)
+    if gen_dev != "cpu":
+        wl = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in wl.items()}
+        import torch
+        torch.cuda.empty_cache()
     od = oracle.Dims(batch=cfg.batch, hq=cfg.hq, hkv=cfg.hkv, head_dim=128, page_size=16,
                      max_pages_per_seq=wl["max_pages"], num_pages=wl["num_pages"],
                      chunk=cfg.chunk, block=16, k1=cfg.k1, k2=cfg.k2, sink=cfg.sink,
@@ -631,7 +671,7 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
     threads = min(oracle.num_threads(), len(pairs))
     # one thread: each pair once (the OpenMP loop then has one pair to hand out)
     t1 = 0.0
-    for b, h in pairs:
+    for b, h in (pairs if one_thread else ()):
         bh = np.zeros((cfg.batch, cfg.hkv), dtype=np.int32)
         bh[b, h] = 1
         qh = np.zeros((cfg.batch, cfg.hq), dtype=np.int32)
@@ -642,8 +682,8 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
     us_1 = t1 * 1e6
     desc = (f"{n} whole steps ({name}: append codes, query codes, int8 scoring of the whole "
             f"context, both modules, sparse attention), the {len(pairs)} (sequence, kv head) "
-            f"pairs spread over {threads} threads; one thread, pair by pair: "
-            f"{us_1 / 1e3:.1f} ms per step")
+            f"pairs spread over {threads} threads of the host's {os.cpu_count()} cores"
+            + (f"; one thread, pair by pair: {us_1 / 1e3:.1f} ms per step" if one_thread else ""))
     return us_step, n, threads, desc, us_1
 
 
@@ -740,10 +780,10 @@ def main():
                                 world)
     case = main_res["case"]
     step_ms = reduce_max(main_res["step_ms"], world)
-    e2e_ms, h2d, d2h = (None, 0, 0)
+    e2e, h2d, d2h = (None, 0, 0)
     if not args.no_e2e:
-        e2e_ms, h2d, d2h = e2e_steps(case, min(args.steps, 1000))
-        e2e_ms = reduce_max(e2e_ms, world)
+        e2e, h2d, d2h = e2e_steps(case, min(args.steps, 1000))
+        e2e = {k: reduce_max(v, world) for k, v in e2e.items()}
     clocks = sampler.summary() if sampler else None
     del case, main_res["case"]
     torch.cuda.empty_cache()
@@ -797,15 +837,27 @@ def main():
     cpu = None
     if not args.no_cpu_baseline:
         us, n, cores, desc, us_1 = oracle_step_sample(args.config, 0, 15.0, 10 ** 9, warmup=1)
-        cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": desc,
-               "one_thread_us": us_1}
+        cpu = {"value": us, "unit": "us/step", "cores": cores, "host_cores": os.cpu_count(),
+               "kind": "oracle", "sample": desc, "one_thread_us": us_1, "per_config": {}}
+        # the oracle on the other headline configurations, a few steps each
+        for name in (() if args.no_extra else (EXTRA_CONFIG, "paged-b8-32k-128k")):
+            if name == args.config:
+                continue
+            us_c, n_c, cores_c, desc_c, _ = oracle_step_sample(name, 0, 4.0, 10 ** 9,
+                                                               warmup=1, one_thread=False)
+            cpu["per_config"][name] = {"value": us_c, "unit": "us/step", "steps": n_c,
+                                       "cores": cores_c, "sample": desc_c}
 
     per = main_res["per_ms"]
+    from kv_cache_int8_gb300 import hsa as hsa_mod
+    d0 = main_res["dims"]
+    kernels_per_step = hsa_mod.hsa_decode_step_kernels(d0)
     traffic = traffic_record("score.cu", "score_blocks_llama3-8b-128k.md")
     cfg = W.CONFIGS[args.config]
     line = {
         "metric": METRIC,
         "value": job_value(step_ms, world),
+        "job_steps_per_s": job_steps_per_s(step_ms, world),
         "unit": "us/step",
         "n_gpus": world,
         "steps": args.steps,
@@ -820,7 +872,12 @@ def main():
         "config": {
             "workload": workload_text(cfg),
             "step": "append new token + int8 scoring + 2 pruning modules + split-K attention "
-                    "(hsa_decode_step: 4 kernels, one CUDA graph)",
+                    f"(hsa_decode_step: {kernels_per_step} kernels: the scorer, which also "
+                    "appends the token and records each row's range of maxima, and the "
+                    "attention, which runs both pruning modules itself; steps replayed from "
+                    "CUDA graphs)" if kernels_per_step == 2 else
+                    f"append new token + int8 scoring + 2 pruning modules + split-K attention "
+                    f"(hsa_decode_step: {kernels_per_step} kernels, CUDA graphs)",
             "l2": "2 cache replicas alternate: every step reads data the previous step did not "
                   "touch (more than the 129 MB L2)",
             "parallelism": f"replicas x{world} (independent decode problems per GPU)",
@@ -837,15 +894,20 @@ def main():
             "algorithmic_bytes_per_launch": main_res["bytes"]["score"],
         },
         "cpu_baseline": cpu,
-        "e2e": None if e2e_ms is None else {
-            "value": job_value(e2e_ms, world), "unit": "us/step", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
-            "path": "hsa_decode_step (through hsa.DecodeStep, the decode-loop form of the "
-                    "binding: arguments marshalled once per buffer set, the step replayed from "
-                    "the CUDA graph it records on its first call) with pinned host "
-                    "q/k_new/v_new/out/lse (mapped: a kernel stages the inputs, the attention "
-                    "writes the outputs to host memory), synchronised per step"},
-        "gpu_launches": 4 * args.steps,
+        "e2e": None if e2e is None else {
+            "value": job_value(e2e["plain_call_us"] * 1e-3, world), "unit": "us/step",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "hsa_decode_step called through the binding (ctypes, every argument "
+                    "marshalled per call) with pinned host q/k_new/v_new/out/lse (mapped: a "
+                    "kernel stages the inputs, the attention writes the outputs to host "
+                    "memory); host clock (time.perf_counter) around the call and the stream's "
+                    "synchronisation, mean over steps",
+            "decode_step_graph_us": e2e["decode_step_graph_us"],
+            "decode_step_graph_events_us": e2e["decode_step_graph_events_us"],
+            "forms": "decode_step_graph_us: hsa.DecodeStep (the decode-loop form: arguments "
+                     "marshalled once, the step replayed from a CUDA graph), host clock; "
+                     "decode_step_graph_events_us: the same with CUDA events on the stream"},
+        "gpu_launches": kernels_per_step * args.steps,
         "timing": "value: K whole steps (hsa_decode_step with device buffers) back to back, "
                   "replayed from a CUDA graph of 10 steps (cache replicas alternating), one "
                   "pair of CUDA events around all K, the same method as the dense decode and "

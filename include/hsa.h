@@ -359,6 +359,16 @@ int32_t hsa_select_noalloc(const hsa_dims* d, const void* q, const int8_t* kq,
                            int32_t* block_idx, int32_t* n_blocks, void* stream);
 
 /*
+ * The number of kernels hsa_decode_step launches for d with device-memory inputs and a
+ * 16-byte-aligned page table: 2 when the sparse attention runs the pruning modules itself
+ * (64-token chunks, two modules, rows of up to 2048 chunk scores for 8 query heads a kv
+ * head or 2304 otherwise, K/V in device memory) and the scorer appends the new token
+ * (window >= 1), 3 with no window (the append first), else 4 (scorer, append, pruning
+ * kernel, attention). Host I/O adds a staging kernel. -1 for an invalid d.
+ */
+int32_t hsa_decode_step_kernels(const hsa_dims* d);
+
+/*
  * Reads and clears the device error word of `workspace` after synchronising `stream`:
  * *code receives HSA_OK, HSA_ERR_TIMEOUT or HSA_ERR_DEVICE_CHECK. workspace NULL: the error
  * word of hsa_select_noalloc's fixed scratch array on the current device. This is the one

@@ -779,6 +779,15 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
   return copy_outputs_back(s, io, out, lse, direct_out, st);
 }
 
+int32_t hsa_decode_step_kernels(const hsa_dims* d) {
+  Shape s;
+  if (check_dims(d, s, true) != HSA_OK) return -1;
+  const bool fused = !d->kv_on_host &&
+                     hsa::attend_select_supported(attend_shape(s, false), true);
+  if (fused) return s.window >= 1 ? 2 : 3;  // (append,) scorer with its ranges, selecting attend
+  return 4;                                 // scorer, append, pruning kernel, attend
+}
+
 int32_t hsa_decode_step_cached(const hsa_dims* d, const hsa_step_io* io, void* k_cache,
                                void* v_cache, int8_t* kq, const float* k_scale,
                                const int32_t* page_table, const int32_t* seq_lens,

@@ -37,6 +37,7 @@ EXPORTS = (
     "hsa_workspace_bytes", "hsa_status_string", "hsa_quantize_keys", "hsa_append_kv",
     "hsa_score_blocks", "hsa_prune", "hsa_select", "hsa_attend", "dense_decode",
     "hsa_decode_step", "hsa_decode_step_reuse", "hsa_read_device_error", "hsa_select_noalloc",
+    "hsa_decode_step_kernels",
     "hsa_block_cache_bytes", "hsa_block_cache_mass", "hsa_attend_cached",
     "hsa_decode_step_cached",
 )
@@ -141,6 +142,7 @@ def load(path: Optional[str] = None):
                                          P, I32, P, SZ, P]),
         "hsa_read_device_error": (I32, [P, P, ctypes.POINTER(I32)]),
         "hsa_select_noalloc": (I32, [D, P, P, P, P, P, P, P, P, P, P]),
+        "hsa_decode_step_kernels": (I32, [D]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -364,6 +366,11 @@ def hsa_decode_step_cached(d: Dims, q, k_new, v_new, out, lse, k_cache, v_cache,
         ctypes.byref(cd), ctypes.byref(io), _p(k_cache), _p(v_cache), _p(kq), _p(k_scale),
         _p(page_table), _p(seq_lens), _p(block_idx), _p(n_blocks), _p(cache), capacity, _p(ws),
         ws.numel(), _stream(stream)))
+
+
+def hsa_decode_step_kernels(d: Dims) -> int:
+    """Kernels that hsa_decode_step launches for d (device I/O)."""
+    return int(load().hsa_decode_step_kernels(ctypes.byref(d.c())))
 
 
 def hsa_read_device_error(ws, stream=None) -> int:

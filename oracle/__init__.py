@@ -6,6 +6,7 @@ CPU-baseline leg may import this package. It shares no code with the CUDA librar
 Every function is pinned by the tests in ``tests/test_oracle_*.py`` (worked examples,
 brute force, closed forms and special cases); none is "parity unpinned".
 """
+from .cache import CacheState, cache_plan, call_segments  # noqa: F401
 from .oracle import (  # noqa: F401
     Dims,
     attend,

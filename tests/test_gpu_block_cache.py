@@ -1,10 +1,11 @@
 """The GPU block cache in front of K/V in host memory: attention through the cache against
-the oracle, the cache's state after every call against an LRU model written here (hits
-refresh a block's age; misses take the slots used longest ago, lower slot first; the page
-holding a sequence's last token is copied again), and the cached blocks' bytes against the
-host K/V. Under the cumulative-mass policy: every block's accumulated attention mass against
-the oracle's per-call block masses, and each call's victims against that policy's rule
-(free slots, then least cumulative mass; near-equal masses may go either way)."""
+the oracle, the cache's state after every call against the oracle's cache plan
+(oracle.cache_plan: hits refresh a block's stamp; misses take the slots used longest ago,
+lower slot first; the page holding a sequence's last token is copied again), and the cached
+blocks' bytes against the host K/V. Under the cumulative-mass policy: every block's
+accumulated attention mass against the oracle's per-call block masses, and the cache's state
+after every call against the oracle's plan under that policy given the masses the GPU held
+before the call (free slots, then least cumulative mass, lower slot first)."""
 import dataclasses
 
 import numpy as np
@@ -23,69 +24,11 @@ def _up(x):
     return (x + 255) // 256 * 256
 
 
-def _segments(lens, sink, window, k2, bidx, nb, b, h):
-    """Blocks of the call's segments of (b, h) in the attention's order (None: empty)."""
-    n = int(lens[b])
-    sink_end = min(sink, n)
-    n_sink = (sink_end + 15) // 16
-    cand_hi = n - window
-    n_sel_max = k2 if cand_hi > sink else 0
-    w0 = max(n - window, sink_end)
-    win_k0 = w0 // 16
-    n_win = (n + 15) // 16 - win_k0 if w0 < n else 0
-    stride = (sink + 15) // 16 + (window + 15) // 16 + 1 + k2
-    out = []
-    for i in range(stride):
-        if i < n_sink:
-            out.append(i)
-        elif i < n_sink + n_win:
-            out.append(win_k0 + i - n_sink)
-        else:
-            r = i - n_sink - n_win
-            k = None
-            if r < min(max(int(nb[b, h]), 0), n_sel_max):
-                kk = int(bidx[b, h, r])
-                if 0 <= kk < (n + 15) // 16 and max(kk * 16, sink) < min(kk * 16 + 16, cand_hi):
-                    k = kk
-            out.append(k)
-    return out
-
-
-class LruModel:
-    def __init__(self, num_pages, hkv, capacity):
-        self.hkv, self.cap = hkv, capacity
-        self.slot_of = np.zeros(num_pages * hkv, dtype=np.int64)   # slot + 1
-        self.key = np.zeros(capacity, dtype=np.int64)              # key + 1
-        self.stamp = np.zeros(capacity, dtype=np.int64)
-        self.step = 0
-
-    def call(self, segs_by_bh, pt):
-        self.step += 1
-        misses, seen = [], set()
-        for (b, h), segs in segs_by_bh:
-            for k in segs:
-                if k is None:
-                    continue
-                key = int(pt[b, k]) * self.hkv + h
-                if key in seen:  # a block that is two segments of the call: one lookup
-                    continue
-                seen.add(key)
-                s = self.slot_of[key] - 1
-                if s >= 0:
-                    self.stamp[s] = self.step
-                else:
-                    misses.append(key)
-        free = [s for s in range(self.cap) if self.stamp[s] < self.step]
-        victims = sorted(free, key=lambda s: (self.stamp[s], s))[:len(misses)]
-        victims.sort()
-        for v in victims:
-            if self.key[v] > 0:
-                self.slot_of[self.key[v] - 1] = 0
-        for v, key in zip(victims, misses):
-            self.slot_of[key] = v + 1
-            self.key[v] = key + 1
-            self.stamp[v] = self.step
-        return len(misses)
+def _calls(lens, cfg, bidx, nb, B, Hkv):
+    """The oracle cache plan's view of one call: ((b, h), segments, last block) in order."""
+    return [((b, hh), oracle.call_segments(int(lens[b]), cfg.sink, cfg.window, cfg.k2,
+                                            bidx[b, hh], nb[b, hh]), (int(lens[b]) - 1) // 16)
+            for b in range(B) for hh in range(Hkv)]
 
 
 @pytest.mark.parametrize("sink,window", [(32, 64), (40, 72)])
@@ -107,7 +50,7 @@ def test_block_cache_lru_and_attention(sink, window):
     ws = hsa.workspace(hd, hsa.HSA_OP_CACHED)
     h = H.host_arrays(wl)
     pt, lens = h["pt"], h["lens"]
-    model = LruModel(wl["num_pages"], Hkv, capacity)
+    model = oracle.CacheState.empty(wl["num_pages"] * Hkv, capacity)
     gen = np.random.default_rng(5)
     q = dwl["q"]
     for call in range(6):
@@ -139,10 +82,8 @@ def test_block_cache_lru_and_attention(sink, window):
         out_o, lse_o = oracle.attend(od, h["q"], h["k"], h["v"], pt, lens, bidx, nb)
         H.assert_close(out.cpu().numpy(), out_o, f"call {call} output")
         np.testing.assert_allclose(lse.cpu().numpy(), lse_o, atol=2e-4, rtol=1e-5)
-        # the cache's state against the model
-        segs = [((b, hh), _segments(lens, cfg.sink, cfg.window, cfg.k2, bidx, nb, b, hh))
-                for b in range(B) for hh in range(Hkv)]
-        model.call(segs, pt)
+        # the cache's state against the oracle's plan
+        oracle.cache_plan(model, _calls(lens, cfg, bidx, nb, B, Hkv), pt, Hkv, policy=0)
         raw = cache.cpu().numpy()
         off_of = 256
         off_key = off_of + _up(wl["num_pages"] * Hkv * 4)
@@ -152,12 +93,12 @@ def test_block_cache_lru_and_attention(sink, window):
         as_i32 = lambda o, n: raw[o:o + 4 * n].view(np.int32)
         assert int(raw[:4].view(np.int32)[0]) == model.step
         np.testing.assert_array_equal(as_i32(off_of, wl["num_pages"] * Hkv), model.slot_of)
-        np.testing.assert_array_equal(as_i32(off_key, capacity), model.key)
+        np.testing.assert_array_equal(as_i32(off_key, capacity), model.key_of)
         np.testing.assert_array_equal(as_i32(off_stamp, capacity), model.stamp)
         assert not raw[off_mass:off_data].any()  # no masses under the LRU policy
         data = raw[off_data:off_data + capacity * 8192].view(np.uint16).reshape(capacity, 2, 16, 128)
-        for v in np.nonzero(model.key)[0]:
-            key = int(model.key[v]) - 1
+        for v in np.nonzero(model.key_of)[0]:
+            key = int(model.key_of[v]) - 1
             page, hh = key // Hkv, key % Hkv
             np.testing.assert_array_equal(data[v, 0], h["k"][page, hh])
             np.testing.assert_array_equal(data[v, 1], h["v"][page, hh])
@@ -215,30 +156,6 @@ def test_cached_decode_step_matches_the_uncached_one(policy):
         assert total == 0.0
 
 
-def _check_mass_victims(prev_key, used, new_key, misses, mass, capacity):
-    """The victims of one call under the cumulative-mass policy, read off the slots whose key
-    changed: exactly one per miss, all unused by the call, taken in ascending slot order by
-    the misses in call order, and the first ones by the rule (free slots, lower first; then
-    least cumulative mass, lower slot first), where masses within the fp32 accumulation error
-    of each other may rank either way."""
-    victims = sorted(int(s) for s in np.nonzero(new_key != prev_key)[0])
-    assert len(victims) == len(misses)
-    for v, key in zip(victims, misses):
-        assert v not in used and new_key[v] == key + 1
-    unused = [s for s in range(capacity) if s not in used]
-    rest = sorted(set(unused) - set(victims))
-    free_rest = [s for s in rest if prev_key[s] == 0]
-    for v in victims:
-        if prev_key[v] == 0:  # a free victim: no lower free slot left out
-            assert all(s > v for s in free_rest)
-            continue
-        assert not free_rest, "an occupied slot was evicted while a free one stayed"
-        mv = mass[prev_key[v] - 1]
-        for r in rest:
-            mr = mass[prev_key[r] - 1]
-            assert mr >= mv - 1e-5 * (1.0 + mv), (v, r, mv, mr)
-
-
 @pytest.mark.parametrize("sink,window,hq", [(32, 64, 8), (40, 72, 8), (40, 72, 2), (40, 72, 4),
                                             (40, 72, 16)])
 def test_block_cache_cumulative_mass_policy(sink, window, hq):
@@ -265,13 +182,12 @@ def test_block_cache_cumulative_mass_policy(sink, window, hq):
     pt, lens = h["pt"], h["lens"]
     num_pages = wl["num_pages"]
     want_mass = np.zeros(num_pages * Hkv)
-    slot_of = np.zeros(num_pages * Hkv, dtype=np.int64)
-    key = np.zeros(capacity, dtype=np.int64)
-    stamp = np.zeros(capacity, dtype=np.int64)
+    model = oracle.CacheState.empty(num_pages * Hkv, capacity)
     gen = np.random.default_rng(7)
     qgen = torch.Generator(device="cpu").manual_seed(11)
     raw_i32 = lambda raw, o, n: raw[o:o + 4 * n].view(np.int32).astype(np.int64)
-    off_key = 256 + _up(num_pages * Hkv * 4)
+    off_of = 256
+    off_key = off_of + _up(num_pages * Hkv * 4)
     off_stamp = off_key + _up(capacity * 4)
     for call in range(1, 9):
         q = torch.randn((B, Hq, 128), generator=qgen).to(torch.bfloat16)
@@ -294,6 +210,7 @@ def test_block_cache_cumulative_mass_policy(sink, window, hq):
                 bidx[b, hh, nb[b, hh]:] = -1
         out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
         lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev)
+        gpu_mass = mass_view.cpu().numpy().reshape(-1).astype(np.float64)  # before the call
         hsa.hsa_attend_cached(hd, q.to(dev), dwl["k_cache"], dwl["v_cache"], dwl["page_table"],
                               dwl["seq_lens"], torch.from_numpy(bidx).to(dev),
                               torch.from_numpy(nb).to(dev), cache, capacity, out, lse, ws)
@@ -302,31 +219,15 @@ def test_block_cache_cumulative_mass_policy(sink, window, hq):
         qb = W.to_numpy_bits(q)
         out_o, lse_o = oracle.attend(od, qb, h["k"], h["v"], pt, lens, bidx, nb)
         H.assert_close(out.cpu().numpy(), out_o, f"call {call} output")
-        # the victims of this call, judged by the masses of the earlier calls
-        misses, used, seen = [], set(), set()
-        for b in range(B):
-            for hh in range(Hkv):
-                for k in _segments(lens, cfg.sink, cfg.window, cfg.k2, bidx, nb, b, hh):
-                    if k is None:
-                        continue
-                    kk = int(pt[b, k]) * Hkv + hh
-                    if kk in seen:
-                        continue
-                    seen.add(kk)
-                    if slot_of[kk] > 0:
-                        used.add(int(slot_of[kk]) - 1)
-                    else:
-                        misses.append(kk)
+        # the cache's state against the oracle's plan under this policy, given the masses the
+        # GPU held before the call (fp32, as the GPU ranks them)
+        oracle.cache_plan(model, _calls(lens, cfg, bidx, nb, B, Hkv), pt, Hkv, policy=1,
+                          mass=gpu_mass)
         raw = cache.cpu().numpy()
-        new_key = raw_i32(raw, off_key, capacity)
-        _check_mass_victims(key, used, new_key, misses, want_mass, capacity)
-        for v in np.nonzero(new_key != key)[0]:
-            if key[v] > 0:
-                slot_of[key[v] - 1] = 0
-            slot_of[new_key[v] - 1] = v + 1
-        key = new_key
-        stamp = raw_i32(raw, off_stamp, capacity)
-        assert all(stamp[s] == call for s in used)
+        assert int(raw[:4].view(np.int32)[0]) == model.step
+        np.testing.assert_array_equal(raw_i32(raw, off_of, num_pages * Hkv), model.slot_of)
+        np.testing.assert_array_equal(raw_i32(raw, off_key, capacity), model.key_of)
+        np.testing.assert_array_equal(raw_i32(raw, off_stamp, capacity), model.stamp)
         # this call's attention mass of every block, summed over each kv head's query heads
         m = oracle.block_mass(od, qb, h["k"], pt, lens, bidx, nb)        # [B][Hq][blocks]
         for b in range(B):

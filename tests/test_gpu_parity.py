@@ -50,14 +50,16 @@ def test_paged_batch_full(name):
     _run(wl)
 
 
-def test_llama3_8b_1m_sampled_heads():
+def test_llama3_8b_1m_full():
+    """1M tokens, all 8 kv heads: codes, scales, block maxima, both modules' index sets and
+    the whole step's selection bit-exact; outputs within tolerance."""
     wl = W.make_workload(W.CONFIGS["llama3-8b-1m"], seed=0, device="cuda")
-    _run(wl, bh_pairs=[(0, 0), (0, 5)])
+    _run(wl)
 
 
-def test_llama3_8b_1m_three_modules_sampled_heads():
+def test_llama3_8b_1m_three_modules_full():
     wl = W.make_workload(W.CONFIGS["llama3-8b-1m-3mod"], seed=0, device="cuda")
-    _run(wl, bh_pairs=[(0, 2), (0, 7)])
+    _run(wl)
 
 
 def test_llama3_70b_shaped_128k_groups_of_8_sampled_heads():
@@ -100,17 +102,18 @@ def test_llama3_8b_128k_four_bit_keys_full():
     _run(wl)
 
 
-def test_llama3_8b_1m_four_bit_keys_sampled_heads():
+def test_llama3_8b_1m_four_bit_keys_full():
     wl = W.make_workload(W.CONFIGS["llama3-8b-1m-int4"], seed=0, device="cuda")
-    _run(wl, bh_pairs=[(0, 1), (0, 6)])
+    _run(wl)
 
 
-def test_llama3_8b_3m_offloaded_sampled_head():
+def test_llama3_8b_3m_offloaded_four_heads():
+    """3M tokens with K/V in pinned host memory: kv heads 0, 3, 5 and 7."""
     torch.cuda.empty_cache()
     wl = W.make_workload(W.CONFIGS["llama3-8b-3m-offload"], seed=0, device="cuda",
                          host_pinned=True)
     assert wl["k_cache"].is_pinned() and wl["v_cache"].is_pinned()
-    _run(wl, bh_pairs=[(0, 3)], dense=False)
+    _run(wl, bh_pairs=[(0, 0), (0, 3), (0, 5), (0, 7)], dense=False)
 
 
 def test_deterministic_repeat():

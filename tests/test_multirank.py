@@ -1,6 +1,7 @@
 """The benchmark's multi-rank host logic on CPU: two gloo ranks, each timing its own
-independent decode problem; the job's step time is the max over ranks and the whole-job
-value divides it by the rank count (weak scaling, no data-path collective)."""
+independent decode problem; the job's step time (the value) is the max over ranks, a
+latency that replicas do not shorten, and the job's aggregate steps per second is the rank
+count over that time (weak scaling, no data-path collective)."""
 import os
 import socket
 
@@ -26,7 +27,7 @@ def _worker(rank, world, port, out):
         step_ms = 0.050 + 0.010 * rank          # rank 1 is the slower one
         worst = bench.reduce_max(step_ms, world)
         bench.barrier(world)
-        out[rank] = (worst, bench.job_value(worst, world))
+        out[rank] = (worst, bench.job_value(worst, world), bench.job_steps_per_s(worst, world))
     finally:
         dist.destroy_process_group()
 
@@ -37,15 +38,17 @@ def test_two_gloo_ranks_max_and_job_value():
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     for rank in range(world):
-        worst, value = out[rank]
+        worst, value, steps_per_s = out[rank]
         assert worst == pytest.approx(0.060)
-        assert value == pytest.approx(0.060 * 1e3 / 2)
+        assert value == pytest.approx(60.0)  # µs per step: the slowest rank's, not divided
+        assert steps_per_s == pytest.approx(2 / 0.060e-3)
 
 
 def test_single_rank_is_plain():
     import bench
     assert bench.reduce_max(1.25, 1) == 1.25
     assert bench.job_value(0.1, 1) == pytest.approx(100.0)
+    assert bench.job_steps_per_s(0.1, 1) == pytest.approx(10000.0)
 
 
 def test_reference_arm_runs_on_rank_zero_only(capsys, monkeypatch):
