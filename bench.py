@@ -687,6 +687,11 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
     return us_step, n, threads, desc, us_1
 
 
+def W_CONFIGS():
+    from kv_cache_int8_gb300 import workloads as W
+    return W.CONFIGS
+
+
 # ------------------------------------------------------------------ main
 
 def run_reference(args, world, rank):
@@ -713,21 +718,23 @@ def run_reference(args, world, rank):
 
 def profile_steps(name, device, steps, warmup):
     """Direct launches of the whole step (and of dense decode) for a profiler's launch list:
-    `warmup` steps, then `steps` steps and steps // 2 dense decodes, replicas alternating."""
+    `warmup` steps, then `steps` steps and steps // 2 dense decodes, replicas alternating
+    (no dense decode when K/V live in host memory)."""
     import torch
-    case = Case(name, 0, device)
+    case = Case(name, 0, device, dense=not W_CONFIGS()[name].kv_on_host)
     for i in range(warmup):
         case.step(i & 1)
     torch.cuda.synchronize()
     for i in range(steps):
         case.step(i & 1)
-    for i in range(steps // 2):
+    n_dense = steps // 2 if "dense" in case.kernels else 0
+    for i in range(n_dense):
         case.dense(i & 1)
     torch.cuda.synchronize()
     for w in (case.ws_step, case.ws_den):
         code = case.hsa.hsa_read_device_error(w)
         assert code == 0, f"device error word {code}"
-    print(f"profiled {steps} steps and {steps // 2} dense decodes of {name}")
+    print(f"profiled {steps} steps and {n_dense} dense decodes of {name}")
     return 0
 
 

@@ -1184,10 +1184,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
   int got1 = -1;
   const int keep1 = min(sa.k1, n1);
   constexpr int kRegVals = kSelRegVals;
-  if (n1 > 0 && n1 <= kRegVals * NT && rr.x != 0u && rr.y != 0u) {
-    auto get1 = [&](int x) { return make_int2(tiles[x], c_lo + x); };
-    got1 = sel_fast_reg<NT, kRegVals>(get1, n1, sa.k1, t_min, t_max, ss, kept1);
-  }
+  if (n1 > 0 && n1 <= kRegVals * NT && rr.x != 0u && rr.y != 0u)
+    got1 = sel_fast_row<NT, kRegVals>(SelRow{tiles, nullptr, c_lo}, n1, sa.k1, t_min, t_max, ss,
+                                      kept1);
   if (got1 < 0) {
     got1 = 0;
     if (keep1 > 0) {
@@ -1209,41 +1208,42 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
   const int32_t* bm = sa.block_max + row * a.max_pages;
   int* vals2 = area;  // the tile maxima are no longer read (the collect ended on a barrier)
   int* cand2 = area + sa.n2_cap;
-  // the fast path produces the kept block ids straight from registers; otherwise the
-  // candidates are laid out (vals2 / cand2) for the general path, which writes positions
+  // the candidates laid out as (vals2, cand2); the fast path writes the kept block ids, the
+  // general path positions in cand2
   const int n2 = got1 * P;
   const bool range2 = rr.z != 0u && rr.w != 0u;
-  auto get2 = [&](int x) {
-    const int kk = kept1[x / P] * P + x % P;
-    const bool in = kk >= k_lo && kk < k_hi;
-    return make_int2(in ? (use_row ? brow[kk - k_lo] : __ldcg(bm + kk)) : INT_MIN, kk);
-  };
-  int got2 = -1;
-  bool ids = false;  // selb holds block ids (fast path) rather than positions in cand2
-  if (range2 && n2 > 0 && n2 <= kRegVals * NT) {
-    got2 = sel_fast_reg<NT, kRegVals>(get2, n2, a.k2, b_min, b_max, ss, selb);
-    ids = got2 >= 0;
-  }
-  if (got2 < 0) {
-    int valid = 0, mn2 = INT_MAX, mx2 = INT_MIN;
-    for (int x0 = tid; x0 < n2; x0 += 4 * NT) {
-      int2 e[4];
+  int valid = 0, mn2 = INT_MAX, mx2 = INT_MIN;
+  for (int x0 = tid; x0 < n2; x0 += 4 * NT) {
+    int v[4], kk[4];
 #pragma unroll
-      for (int u = 0; u < 4; u++) e[u] = x0 + u * NT < n2 ? get2(x0 + u * NT) : make_int2(INT_MIN, -1);
+    for (int u = 0; u < 4; u++) {
+      const int x = x0 + u * NT;
+      kk[u] = x < n2 ? kept1[x / P] * P + x % P : -1;
+      const bool in = kk[u] >= k_lo && kk[u] < k_hi;
+      v[u] = in ? (use_row ? brow[kk[u] - k_lo] : __ldcg(bm + kk[u])) : INT_MIN;
+    }
 #pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const int x = x0 + u * NT;
-        if (x < n2) {
-          cand2[x] = e[u].y;
-          vals2[x] = e[u].x;
-          if (e[u].x != INT_MIN) {
-            valid++;
-            mn2 = min(mn2, e[u].x);
-            mx2 = max(mx2, e[u].x);
-          }
+    for (int u = 0; u < 4; u++) {
+      const int x = x0 + u * NT;
+      if (x < n2) {
+        cand2[x] = kk[u];
+        vals2[x] = v[u];
+        if (v[u] != INT_MIN) {
+          valid++;
+          mn2 = min(mn2, v[u]);
+          mx2 = max(mx2, v[u]);
         }
       }
     }
+  }
+  int got2 = -1;
+  bool ids = false;  // selb holds block ids (fast path) rather than positions in cand2
+  if (range2 && n2 > 0 && n2 <= kRegVals * NT) {
+    __syncthreads();  // the candidates are laid out
+    got2 = sel_fast_row<NT, kRegVals>(SelRow{vals2, cand2, 0}, n2, a.k2, b_min, b_max, ss, selb);
+    ids = got2 >= 0;
+  }
+  if (got2 < 0) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       valid += __shfl_xor_sync(0xffffffffu, valid, off);

@@ -433,6 +433,17 @@ __device__ __forceinline__ int3 fast_locate(const unsigned* fhist, int K) {
 // entries' ids in ascending order of x. Returns min(K, valid entries), or -1 (nothing
 // written) when the K-th key's bin holds more than kSelSmall values. Expects fhist and
 // n_cand zero and leaves them zero; three CTA barriers (two when everything is kept).
+// The entries of a row for sel_fast_reg: value vals[x] and id ids[x] (ids nullable: id =
+// add + x). One type for every caller, so that the selection's code exists once.
+struct SelRow {
+  const int* vals;
+  const int* ids;
+  int add;
+  __device__ __forceinline__ int2 operator()(int x) const {
+    return make_int2(vals[x], ids != nullptr ? ids[x] : add + x);
+  }
+};
+
 template <int NT, int R, typename Get>
 __device__ __forceinline__ int sel_fast_reg(Get get, int n, int K, int vmin, int vmax,
                                             SelectShared& ss, int* out) {
@@ -570,6 +581,13 @@ __device__ __forceinline__ int sel_fast_reg(Get get, int n, int K, int vmin, int
   if (tid == 0) ss.n_cand = 0;
   __syncthreads();
   return keep_n;
+}
+
+// sel_fast_reg on a SelRow, out of line (one copy of the code for every call site).
+template <int NT, int R>
+__device__ __noinline__ int sel_fast_row(SelRow row, int n, int K, int vmin, int vmax,
+                                         SelectShared& ss, int* out) {
+  return sel_fast_reg<NT, R>(row, n, K, vmin, vmax, ss, out);
 }
 
 // A row src[0, n) of ints in global memory (in an array whose base is 16-byte aligned) to be

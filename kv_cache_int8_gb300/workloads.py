@@ -94,6 +94,10 @@ CONFIGS: Dict[str, Config] = {
     # 3M tokens, bf16 K/V in pinned host memory, int8 keys in HBM
     "llama3-8b-3m-offload": Config("llama3-8b-3m-offload", 1, 32, 8, 3145728, None,
                                    k1=512, k2=256, sink=128, window=2048, kv_on_host=True),
+    # the offloaded step at 1M tokens: the same attended set (K2, sink, window), so the same
+    # bytes over the host link per step, with a third of the scan (profiler captures)
+    "llama3-8b-1m-offload": Config("llama3-8b-1m-offload", 1, 32, 8, 1048576, None,
+                                   k1=512, k2=256, sink=128, window=2048, kv_on_host=True),
 }
 
 ORDER: List[str] = ["tiny-8k", "llama3-8b-128k", "paged-b8-32k-128k", "llama3-8b-1m",

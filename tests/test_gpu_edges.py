@@ -151,7 +151,8 @@ def test_many_ties_lower_index_wins():
 
 def test_append_then_step_matches_oracle():
     """hsa_append_kv writes the new token and its codes with the stored scales; the whole
-    step entry point gives the same result as the separate calls."""
+    step entry point gives the same result as the separate calls (selection, cache and codes
+    bit for bit; outputs up to the order of the split-K sums)."""
     cfg = _cfg(context=None, context_range=(3000, 9000), batch=3, hq=8, hkv=2, k1=12, k2=10,
                sink=32, window=96, paged_permuted=True)
     wl = W.make_workload(cfg, seed=31)
@@ -214,7 +215,10 @@ def test_append_then_step_matches_oracle():
                    lse_b, hsa.workspace(hd, hsa.HSA_OP_ATTEND))
     torch.cuda.synchronize()
     assert torch.equal(bidx, bidx2) and torch.equal(nb, nb2)
-    assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+    # the step's attention may split and merge its partials differently: the same sums in
+    # another order
+    torch.testing.assert_close(out_a, out_b, rtol=1e-5, atol=1e-5)
+    torch.testing.assert_close(lse_a, lse_b, rtol=1e-5, atol=1e-5)
     assert torch.equal(kq4, kq2) and torch.equal(kc4, kc2)
     # whole step with pinned host io
     q_h = wl["q"].pin_memory()
