@@ -243,23 +243,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // map4: 4-D [page][head][row][128 B], a box is the blocks of one head in 4 consecutive pages
 // (one copy instead of four where the page table is contiguous).
 int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map, CUtensorMap* map4) {
-  // the maps depend only on the base pointer and the shape: the last pair of this thread is
-  // reused
-  struct Last {
+  // the maps depend only on the base pointer and the shape: this thread keeps the pairs of
+  // the last kKeep code caches it saw (a model's layers each have their own), replaced in turn
+  struct Entry {
     const int8_t* kq = nullptr;
     long long pages = -1;
     int hkv = -1, rows_per_block = -1;
     CUtensorMap map, map4;
   };
-  thread_local Last last;
+  constexpr int kKeep = 64;
+  thread_local Entry kept[kKeep];
+  thread_local int next = 0;
   // 8-bit codes: one 128-byte row per token, 16 rows a block; 4-bit: two tokens a row
   const int rows_per_block = s.key_bits == 4 ? hsa::kPage / 2 : hsa::kPage;
   const long long rows = (long long)s.num_pages * s.hkv * rows_per_block;
-  if (last.kq == kq && last.pages == s.num_pages && last.hkv == s.hkv &&
-      last.rows_per_block == rows_per_block) {
-    *map = last.map;
-    *map4 = last.map4;
-    return HSA_OK;
+  for (int i = 0; i < kKeep; i++) {
+    const Entry& e = kept[i];
+    if (e.kq == kq && e.pages == s.num_pages && e.hkv == s.hkv &&
+        e.rows_per_block == rows_per_block) {
+      *map = e.map;
+      *map4 = e.map4;
+      return HSA_OK;
+    }
   }
   auto fn = encode_fn();
   if (fn == nullptr) return HSA_ERR_CUDA;
@@ -280,12 +285,14 @@ int32_t encode_kq_map(const Shape& s, const int8_t* kq, CUtensorMap* map, CUtens
          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return HSA_ERR_CUDA;
-  last.kq = kq;
-  last.pages = s.num_pages;
-  last.hkv = s.hkv;
-  last.rows_per_block = rows_per_block;
-  last.map = *map;
-  last.map4 = *map4;
+  Entry& e = kept[next];
+  next = (next + 1) % kKeep;
+  e.kq = kq;
+  e.pages = s.num_pages;
+  e.hkv = s.hkv;
+  e.rows_per_block = rows_per_block;
+  e.map = *map;
+  e.map4 = *map4;
   return HSA_OK;
 }
 

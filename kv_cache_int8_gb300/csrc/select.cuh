@@ -431,8 +431,9 @@ __device__ __forceinline__ int3 fast_locate(const unsigned* fhist, int K) {
 // pass is a few instructions a value; the ranking loops run over the bin's count. get(x)
 // returns (value, id) of entry x (value INT_MIN: no candidate); out receives the kept
 // entries' ids in ascending order of x. Returns min(K, valid entries), or -1 (nothing
-// written) when the K-th key's bin holds more than kSelSmall values. Expects fhist and
-// n_cand zero and leaves them zero; three CTA barriers (two when everything is kept).
+// written) when the K-th key's bin holds more than kSelSmall values; K <= 0 writes nothing
+// and returns 0. Expects fhist and n_cand zero and leaves them zero; three CTA barriers (two
+// when everything is kept, none when K <= 0).
 // The entries of a row for sel_fast_reg: value vals[x] and id ids[x] (ids nullable: id =
 // add + x). One type for every caller, so that the selection's code exists once.
 struct SelRow {
@@ -448,6 +449,7 @@ template <int NT, int R, typename Get>
 __device__ __forceinline__ int sel_fast_reg(Get get, int n, int K, int vmin, int vmax,
                                             SelectShared& ss, int* out) {
   constexpr int kWarps = NT / 32;
+  if (K <= 0) return 0;  // keeps nothing (the same in every thread: no barrier is skipped)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt = sel_lanemask_lt();
   const unsigned umin = (unsigned)vmin;

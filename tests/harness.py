@@ -218,14 +218,19 @@ def ordered_to_float(keys) -> np.ndarray:
     return bits.astype(np.uint32).view(np.float32)
 
 
-def fp8_reference(g: dict, o: dict, h: dict, od: oracle.Dims, bh_pairs):
-    """FP8 keys, whose fp32 scores the pages fix in no order: the GPU's block maxima within
-    the fp32 bound of the exact ones, its selection valid for scores known to that bound
-    (oracle.selection_within_bounds), and the oracle's attention over the GPU's own
-    selection, which the outputs are then compared with. Returns (out, lse)."""
+def fp8_rows(od: oracle.Dims, bh_pairs):
+    """The selection rows of the (b, kv head) pairs: the kv head's row, or with per-head
+    selection the rows of its query heads."""
     G = od.hq // od.hkv
-    rows = [(b, r) for b, hh in bh_pairs
+    return [(b, r) for b, hh in bh_pairs
             for r in (range(hh * G, hh * G + G) if od.per_head else (hh,))]
+
+
+def fp8_validity(g: dict, o: dict, h: dict, od: oracle.Dims, bh_pairs):
+    """FP8 keys, whose fp32 scores the pages fix in no order: the GPU's block maxima within
+    the fp32 bound of the exact ones and its selection valid for scores known to that bound
+    (oracle.selection_within_bounds)."""
+    rows = fp8_rows(od, bh_pairs)
     for b, r in rows:
         valid = np.isfinite(o["fp8_score"][b, r])
         bm = g["block_max"][b, r]
@@ -236,6 +241,13 @@ def fp8_reference(g: dict, o: dict, h: dict, od: oracle.Dims, bh_pairs):
                                          g["chunk_idx"], g["n_chunks"], g["block_idx"],
                                          g["n_blocks"], rows)
     assert not bad, f"FP8 selection not valid within the fp32 bound: {bad[:4]}"
+
+
+def fp8_reference(g: dict, o: dict, h: dict, od: oracle.Dims, bh_pairs):
+    """fp8_validity, then the oracle's attention over the GPU's own selection, which the
+    outputs are then compared with. Returns (out, lse)."""
+    G = od.hq // od.hkv
+    fp8_validity(g, o, h, od, bh_pairs)
     qh_mask = np.zeros((od.batch, od.hq), dtype=np.int32)
     for b, hh in bh_pairs:
         qh_mask[b, hh * G:(hh + 1) * G] = 1

@@ -129,6 +129,30 @@ def test_fp8_keys(hq, hkv, per_head):
     assert (codes & 0x7F).max() == 0x7E  # the channel maxima code as +-448
 
 
+@pytest.mark.parametrize("scale_exp", [11, 16])
+def test_fp8_keys_large_query(scale_exp):
+    """FP8 keys with the query scaled by 2^11 and 2^16 (folded query values past 2^7, fp32
+    scores in the tens of thousands): block maxima within the fp32 bound of the exact scores,
+    the selection valid within it, and the whole step's selection equal to hsa_select's.
+    (Logits that large leave the fp32 attention itself outside the output tolerance, so
+    outputs are not compared here.)"""
+    wl = W.make_workload(_cfg(context=None, context_range=(900, 7000), batch=2, hq=8, hkv=2,
+                              paged_permuted=True, key_fp8=1), seed=90 + scale_exp)
+    wl["q"] = (wl["q"].float() * 2.0 ** scale_exp).to(torch.bfloat16)
+    hd, od = H.dims_pair(wl, k1=12, k2=10, sink=24, window=150)
+    h = H.host_arrays(wl)
+    g = H.gpu_step(H.to_cuda(wl), hd, dense=False)
+    o = H.oracle_step(h, od, dense=False)
+    pairs = [(b, hh) for b in range(od.batch) for hh in range(od.hkv)]
+    H.fp8_validity(g, o, h, od, pairs)
+    np.testing.assert_array_equal(g["step_block_idx"], g["block_idx"])
+    np.testing.assert_array_equal(g["step_n_blocks"], g["n_blocks"])
+    B, hkv = od.batch, od.hkv
+    q = wl["q"].float().view(B, hkv, od.hq // hkv, 128)
+    q_fold = (q * torch.from_numpy(g["k_scale"]).view(B, hkv, 1, 128)).abs().amax()
+    assert q_fold >= 2.0 ** 7
+
+
 def test_unaligned_sink_and_window():
     wl = W.make_workload(_cfg(context=7777, batch=3, hq=8, hkv=2), seed=21)
     _check(wl, k1=11, k2=19, sink=37, window=101)
