@@ -907,8 +907,10 @@ def main():
             "path": "hsa_decode_step called through the binding (ctypes, every argument "
                     "marshalled per call) with pinned host q/k_new/v_new/out/lse (mapped: a "
                     "kernel stages the inputs, the attention writes the outputs to host "
-                    "memory); host clock (time.perf_counter) around the call and the stream's "
-                    "synchronisation, mean over steps",
+                    "memory; the two replica buffer sets alternate, and the library replays "
+                    "the CUDA graph it recorded at the first call with each set); host clock "
+                    "(time.perf_counter) around the call and the stream's synchronisation, "
+                    "mean over steps",
             "decode_step_graph_us": e2e["decode_step_graph_us"],
             "decode_step_graph_events_us": e2e["decode_step_graph_events_us"],
             "forms": "decode_step_graph_us: hsa.DecodeStep (the decode-loop form: arguments "

@@ -23,9 +23,10 @@
  *
  * Conventions shared by every call:
  *  - Every pointer is a DEVICE pointer unless a flag below says otherwise. The caller
- *    owns every buffer and the stream; the library never allocates or frees memory,
- *    never synchronises (except hsa_read_device_error, which says so), and never
- *    aborts or traps. `stream` is a cudaStream_t (NULL = legacy default stream).
+ *    owns every buffer and the stream; the library never allocates or frees memory
+ *    (hsa_decode_step's recorded graphs aside: see there), never synchronises (except
+ *    hsa_read_device_error, which says so), and never aborts or traps. `stream` is a
+ *    cudaStream_t (NULL = legacy default stream).
  *  - Paged cache layout: [num_pages][hkv][page_size=16][head_dim=128], bf16 for K and
  *    V, int8 for the key codes; token t of sequence b lives in page
  *    page_table[b * max_pages_per_seq + t / 16], slot t % 16. page_table is int32
@@ -249,6 +250,13 @@ typedef struct hsa_step_io {
  * One whole decode step: hsa_append_kv, hsa_select, hsa_attend on `stream`. seq_lens
  * already count the new token. block_idx / n_blocks receive the selection (device,
  * nullable: then the HSA_OP_STEP workspace holds it). Needs HSA_OP_STEP workspace.
+ * The kernels read every input from its buffer when they run, so the first call with a
+ * given set of argument values (the dims, the io struct's fields, every pointer, the
+ * workspace size, the current device) records its launches into a CUDA graph, and later
+ * calls with the same values launch that graph on `stream`: one launch a step in a decode
+ * loop. The 64 most recently used sets are kept (CUDA driver resources, never freed before
+ * exit). Calls on a stream that is being captured, or with the environment variable
+ * HSA_STEP_GRAPHS=0, launch the kernels one by one. Results are the same either way.
  */
 int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache, void* v_cache,
                         int8_t* kq, const float* k_scale, const int32_t* page_table,

@@ -6,7 +6,10 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/hsa.h"
 #include "common.cuh"
@@ -852,12 +855,115 @@ int32_t hsa_attend_cached(const hsa_dims* d, const void* q, const void* k_cache,
                           l, cache_scratch(s, l.end), block_cache, capacity, as_stream(stream));
 }
 
+// ---- recorded steps
+// A decode loop calls hsa_decode_step with the same arguments every step: new contents, the
+// same buffers. The kernels read every input from its buffer when they run, so the launches
+// of one argument set are recorded once into a CUDA graph and replayed: one graph launch per
+// call instead of one launch per kernel (host time that the GPU otherwise waits through).
+// Keyed by every argument value and the device; the most recently used kStepGraphs sets are
+// kept. Not used while the caller's stream is being captured (the caller's graph then
+// records the kernels themselves), nor with HSA_STEP_GRAPHS=0 in the environment.
+struct StepKey {
+  hsa_dims d;
+  hsa_step_io io;
+  const void* ptr[9];
+  size_t ws_bytes;
+  int device;
+};
+
+struct StepGraph {
+  StepKey key;
+  cudaGraphExec_t exec;
+  unsigned long long used;
+};
+
+constexpr size_t kStepGraphs = 64;
+
+bool step_graphs_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("HSA_STEP_GRAPHS");
+    return e == nullptr || std::strcmp(e, "0") != 0;
+  }();
+  return on;
+}
+
+// This thread's stream for recording on `device` (created once, never destroyed: the
+// recorded graphs are launched on the caller's stream).
+cudaStream_t record_stream(int device) {
+  thread_local cudaStream_t streams[64] = {};
+  if (device < 0 || device >= 64) return nullptr;
+  if (streams[device] == nullptr &&
+      cudaStreamCreateWithFlags(&streams[device], cudaStreamNonBlocking) != cudaSuccess)
+    streams[device] = nullptr;
+  return streams[device];
+}
+
 int32_t hsa_decode_step(const hsa_dims* d, const hsa_step_io* io, void* k_cache, void* v_cache,
                         int8_t* kq, const float* k_scale, const int32_t* page_table,
                         const int32_t* seq_lens, int32_t* block_idx, int32_t* n_blocks,
                         void* workspace, size_t workspace_bytes, void* stream) {
-  return decode_step_impl(d, io, k_cache, v_cache, kq, k_scale, page_table, seq_lens, block_idx,
-                          n_blocks, workspace, workspace_bytes, stream, false);
+  auto direct = [&](void* s) {
+    return decode_step_impl(d, io, k_cache, v_cache, kq, k_scale, page_table, seq_lens,
+                            block_idx, n_blocks, workspace, workspace_bytes, s, false);
+  };
+  cudaStream_t st = as_stream(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  int dev = -1;
+  if (!step_graphs_enabled() || d == nullptr || io == nullptr ||
+      cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone ||
+      cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return direct(stream);
+  }
+  StepKey key;
+  std::memset(&key, 0, sizeof(key));  // padding included: keys compare as bytes
+  key.d = *d;
+  key.io = *io;
+  const void* ptr[9] = {k_cache, v_cache, kq, k_scale, page_table, seq_lens, block_idx,
+                        n_blocks, workspace};
+  std::memcpy(key.ptr, ptr, sizeof(ptr));
+  key.ws_bytes = workspace_bytes;
+  key.device = dev;
+  static std::mutex mu;
+  static std::vector<StepGraph>* graphs = new std::vector<StepGraph>();  // kept to exit
+  static unsigned long long clock = 0;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (StepGraph& e : *graphs) {
+      if (std::memcmp(&e.key, &key, sizeof(key)) == 0) {
+        e.used = ++clock;
+        return cudaGraphLaunch(e.exec, st) == cudaSuccess ? HSA_OK : HSA_ERR_CUDA;
+      }
+    }
+  }
+  // record the step's launches on this thread's stream, then launch the graph on `stream`
+  cudaStream_t rec = record_stream(dev);
+  if (rec == nullptr || cudaStreamBeginCapture(rec, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return direct(stream);
+  }
+  const int32_t rc = direct(rec);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(rec, &graph);
+  cudaGraphExec_t exec = nullptr;
+  if (rc == HSA_OK && ec == cudaSuccess && graph != nullptr &&
+      cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+    exec = nullptr;
+  if (graph != nullptr) cudaGraphDestroy(graph);
+  cudaGetLastError();
+  if (rc != HSA_OK && rc != HSA_ERR_CUDA) return rc;  // rejected arguments: nothing launched
+  if (exec == nullptr) return direct(stream);         // something could not be recorded
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (graphs->size() >= kStepGraphs) {
+      auto old = std::min_element(graphs->begin(), graphs->end(),
+                                  [](const StepGraph& a, const StepGraph& b) { return a.used < b.used; });
+      cudaGraphExecDestroy(old->exec);
+      graphs->erase(old);
+    }
+    graphs->push_back(StepGraph{key, exec, ++clock});
+  }
+  return cudaGraphLaunch(exec, st) == cudaSuccess ? HSA_OK : HSA_ERR_CUDA;
 }
 
 int32_t hsa_decode_step_reuse(const hsa_dims* d, const hsa_step_io* io, void* k_cache,

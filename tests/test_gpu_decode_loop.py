@@ -24,7 +24,9 @@ def _clone(t):
 def test_prepared_decode_step_equals_the_plain_call():
     """hsa.DecodeStep (arguments marshalled once), and the same replayed from a CUDA graph,
     give the same bits as hsa_decode_step, with host I/O, over several steps whose inputs
-    change in place."""
+    change in place. The plain calls after the first replay the library's own recording of
+    the step; the captured graph holds the kernels launched one by one (a stream that is
+    being captured is not recorded again), so the two launch paths are compared."""
     cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None,
                               context_range=(2000, 4000), batch=2, hq=8, hkv=2, k1=10, k2=8,
                               sink=32, window=64, paged_permuted=True)
