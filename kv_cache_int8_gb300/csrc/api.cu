@@ -750,15 +750,16 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
   }
   // K/V in device memory: the sparse attention runs both pruning modules itself when they
   // fit its shared memory (no pruning kernel, no kept-block list round trip in between); the
-  // scorer then records each row's range of maxima for its selection
-  // and, with a window, appends the new token itself (one kernel fewer between the two)
+  // scorer then, with a window, appends the new token itself (one kernel fewer between the
+  // two). Either way the scorer records each row's range of maxima for the selection, and
+  // whichever kernel selects clears them.
   const Shape sa = attend_shape(s, false);
   const bool fused = block_cache == nullptr && !d->kv_on_host &&
                      hsa::attend_select_supported(sa, aligned(page_table, 16));
   unsigned* row_range = reinterpret_cast<unsigned*>(ws + l.row_range);
   const hsa::AppendArgs app = {kn, vn, const_cast<void*>(kd), const_cast<void*>(vd), kq};
-  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st,
-                fused ? row_range : nullptr, (fused && beside) ? &app : nullptr);
+  rc = do_score(s, q, kq, k_scale, page_table, seq_lens, bm, tm, err, st, row_range,
+                (fused && beside) ? &app : nullptr);
   if (rc != HSA_OK) return rc;
   if (beside && !fused) {
     e = hsa::launch_append_kv(s, kn, vn, const_cast<void*>(kd), const_cast<void*>(vd), kq,
@@ -779,7 +780,7 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
   // the prune also resolves the kept blocks' pages, so the attend needs one round trip for them
   int32_t* sel_pages = reinterpret_cast<int32_t*>(ws + l.sel_pages);
   e = hsa::launch_prune(prune_shape(s), seq_lens, bm, tm, nullptr, nullptr, bidx, nb, page_table,
-                        sel_pages, err, st);
+                        sel_pages, err, st, row_range);
   if (e != cudaSuccess) return HSA_ERR_CUDA;
   rc = block_cache ? do_attend_cached(s, q, kd, vd, page_table, seq_lens, bidx, nb, out, lse, ws,
                                       l.att, l.cache, block_cache, capacity, st)

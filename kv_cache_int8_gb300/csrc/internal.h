@@ -71,10 +71,13 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
 // ---- prune.cu
 // page_table / sel_pages (both nullable): also write the page of every kept block into
 // sel_pages [B][Hkv][K2], entries [0, n_blocks) (for launch_attend's sel_pages).
+// row_range (nullable): the scorer's range of each row's maxima (launch_score_blocks);
+// module 1 then skips its min/max pass, and the prune clears the words for the next step.
 cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t* block_max,
                          const int32_t* tile_max, int32_t* chunk_idx, int32_t* n_chunks,
                          int32_t* block_idx, int32_t* n_blocks, const int32_t* page_table,
-                         int32_t* sel_pages, int* err, cudaStream_t st);
+                         int32_t* sel_pages, int* err, cudaStream_t st,
+                         unsigned* row_range = nullptr);
 int prune_max_chunks();
 size_t prune_smem_bytes(const Shape& s);
 

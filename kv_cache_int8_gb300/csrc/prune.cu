@@ -28,6 +28,9 @@ namespace {
 #endif
 constexpr int kPruneThreads = HSA_PRUNE_THREADS;  // overridable at build time for tuning
 constexpr int kPruneWarps = kPruneThreads / 32;
+#ifndef HSA_PRUNE_RANGE
+#define HSA_PRUNE_RANGE 1
+#endif
 constexpr int kMaxChunks = 53248;
 constexpr int kRowCap = 16384;  // block-maxima rows up to this many blocks are staged whole
 constexpr size_t kSmemLimit = 227 * 1024;
@@ -44,6 +47,7 @@ struct PruneArgs {
   int32_t* n_blocks;
   const int32_t* page_table;  // with sel_pages: the page of every kept block is written too
   int32_t* sel_pages;         // nullable, [B][Hkv][K2] beside block_idx
+  unsigned* row_range;        // nullable, [rows][4]: the scorer's range of the maxima
   int* err;
   int hkv, max_pages, chunk_blocks, k1, k2, sink, window;
   int k0, coarse_chunks;  // module 0: top-k0 coarse chunks of coarse_chunks chunks each
@@ -115,7 +119,18 @@ __global__ void __launch_bounds__(kPruneThreads, 1024 / kPruneThreads) prune_ker
   }
   const int32_t* bm = a.block_max + ((size_t)b * a.hkv + h) * a.max_pages;
   const size_t bh = (size_t)b * a.hkv + h;
-  __syncthreads();  // the barrier's initialisation is visible
+  // the scorer's range of the row's tile maxima (zero: not recorded); cleared once read
+  uint4 rr = make_uint4(0u, 0u, 0u, 0u);
+  if (a.row_range != nullptr) rr = __ldcg(reinterpret_cast<const uint4*>(a.row_range) + bh);
+  __syncthreads();  // the barrier's initialisation is visible; every thread has read rr
+  if (a.row_range != nullptr && tid == 0)
+    *reinterpret_cast<uint4*>(a.row_range + bh * 4) = make_uint4(0u, 0u, 0u, 0u);
+  // module 1's values lie in the range of the tile maxima (64-token chunks: they are the
+  // tile maxima) or else in that of the block maxima (a chunk's score is its best block's)
+  const bool c64 = a.chunk_blocks == 4;
+  const unsigned r_hi = c64 ? rr.x : rr.z, r_lo = c64 ? rr.y : rr.w;
+  const bool t_range = HSA_PRUNE_RANGE && r_hi != 0u && r_lo != 0u;
+  const int t_max = (int)(r_hi ^ 0x80000000u), t_min = (int)(~r_lo ^ 0x80000000u);
 
   // ---- stage the scores: the 64-token tile maxima when the scorer wrote them (chunk c of 64
   // tokens == tile c) on barrier 0, the whole row of block maxima and of page ids when they
@@ -226,10 +241,10 @@ __global__ void __launch_bounds__(kPruneThreads, 1024 / kPruneThreads) prune_ker
       __syncthreads();
     }
   } else {
-    // ---- module 1: top-K1 chunks
+    // ---- module 1: top-K1 chunks (within the recorded range when there is one)
     const int keep1 = min(a.k1, n1);
     if (keep1 < n1 && keep1 > 0) {
-      const int3 r = sel_kth_largest<kPruneThreads>(vals, n1, keep1, ps.sel, false, 0, 0);
+      const int3 r = sel_kth_largest<kPruneThreads>(vals, n1, keep1, ps.sel, t_range, t_min, t_max);
       T = r.x;
       need_eq = r.y;
       eq_total = r.z;
@@ -660,8 +675,10 @@ size_t prune_smem_bytes(const Shape& s) {
 cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t* block_max,
                          const int32_t* tile_max, int32_t* chunk_idx, int32_t* n_chunks,
                          int32_t* block_idx, int32_t* n_blocks, const int32_t* page_table,
-                         int32_t* sel_pages, int* err, cudaStream_t st) {
+                         int32_t* sel_pages, int* err, cudaStream_t st, unsigned* row_range) {
   if (sel_pages != nullptr && page_table == nullptr) return cudaErrorInvalidValue;
+  if (row_range != nullptr && (reinterpret_cast<uintptr_t>(row_range) & 15) != 0)
+    return cudaErrorInvalidValue;
   PruneArgs a;
   const bool stage_pages =
       sel_pages != nullptr && (reinterpret_cast<uintptr_t>(page_table) & 15) == 0;
@@ -682,6 +699,7 @@ cudaError_t launch_prune(const Shape& s, const int32_t* seq_lens, const int32_t*
   a.n_blocks = n_blocks;
   a.page_table = page_table;
   a.sel_pages = sel_pages;
+  a.row_range = row_range;
   a.err = err;
   a.hkv = s.hkv;
   a.max_pages = s.max_pages;
