@@ -624,11 +624,12 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
 def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
                        warmup: int = 0, one_thread: bool = True):
     """Time the CPU oracle's per-step work (append codes, query codes + scoring + both
-    modules, sparse attention): whole steps, the oracle's OpenMP loop spreading the
-    (sequence, kv head) pairs over the host cores, until `budget_s` seconds or `max_samples`
-    steps, after `warmup` untimed steps; then one pair at a time on one thread, once per
-    pair, scaled to a whole step. Returns (µs per whole step on the cores, steps, threads
-    used, description, µs per whole step on one thread)."""
+    modules, sparse attention): whole steps, the oracle's OpenMP loops spreading each
+    (sequence, kv head) pair's token blocks (scoring) and the pairs (attention) over the
+    host cores, until `budget_s` seconds or `max_samples` steps, after `warmup` untimed
+    steps; then one pair at a time on one thread, once per pair, scaled to a whole step.
+    Returns (µs per whole step on the cores, steps, threads used, description, µs per whole
+    step on one thread)."""
     import numpy as np
     import oracle
     from kv_cache_int8_gb300 import workloads as W
@@ -668,9 +669,11 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
         t_total += time.perf_counter() - t0
         n += 1
     us_step = t_total / max(n, 1) * 1e6
-    threads = min(oracle.num_threads(), len(pairs))
-    # one thread: each pair once (the OpenMP loop then has one pair to hand out)
+    threads = oracle.num_threads()
+    # one thread: each pair once
     t1 = 0.0
+    if one_thread:
+        oracle.set_num_threads(1)
     for b, h in (pairs if one_thread else ()):
         bh = np.zeros((cfg.batch, cfg.hkv), dtype=np.int32)
         bh[b, h] = 1
@@ -679,10 +682,13 @@ def oracle_step_sample(name: str, seed: int, budget_s: float, max_samples: int,
         t0 = time.perf_counter()
         step(bh, qh)
         t1 += time.perf_counter() - t0
+    if one_thread:
+        oracle.set_num_threads(threads)
     us_1 = t1 * 1e6
     desc = (f"{n} whole steps ({name}: append codes, query codes, int8 scoring of the whole "
-            f"context, both modules, sparse attention), the {len(pairs)} (sequence, kv head) "
-            f"pairs spread over {threads} threads of the host's {os.cpu_count()} cores"
+            f"context, both modules, sparse attention), each of the {len(pairs)} (sequence, "
+            f"kv head) pairs' token blocks spread over {threads} threads of the host's "
+            f"{os.cpu_count()} cores"
             + (f"; one thread, pair by pair: {us_1 / 1e3:.1f} ms per step" if one_thread else ""))
     return us_step, n, threads, desc, us_1
 

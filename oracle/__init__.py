@@ -20,4 +20,5 @@ from .oracle import (  # noqa: F401
     recall,
     select,
     selection_within_bounds,
+    set_num_threads,
 )

@@ -27,7 +27,7 @@ def build(force: bool = False) -> str:
         subprocess.run(_BASE + ["-fopenmp", SRC, "-o", tmp, "-lm"], check=True,
                        capture_output=True, text=True)
     except subprocess.CalledProcessError:
-        # OpenMP only spreads independent (sequence, head) pairs over cores.
+        # OpenMP only spreads independent work (pairs, blocks of tokens) over cores.
         subprocess.run(_BASE + [SRC, "-o", tmp, "-lm"], check=True, capture_output=True, text=True)
     os.replace(tmp, LIB)
     return LIB

@@ -371,7 +371,7 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
   const int64_t max_tokens = (int64_t)d->max_pages_per_seq * d->page_size;
   const int64_t max_blocks = (max_tokens + d->block - 1) / d->block;
   int bad = 0;
-#pragma omp parallel for schedule(dynamic, 1)
+  /* one (sequence, kv head) at a time; its token scores are spread over the threads */
   for (int bh = 0; bh < d->batch * d->hkv; bh++) {
     int b = bh / d->hkv, h = bh % d->hkv;
     if (!wanted(bh_mask, d, b, h)) continue;
@@ -400,32 +400,44 @@ int oracle_select(const oracle_dims* d, const uint16_t* q, const float* scale, c
       char* bvalid = (char*)calloc((size_t)max_blocks + 1, 1);
       if (!qq || (d->key_fp8 && !qf) || !cmax || !bmax || !cvalid || !bvalid || !cmax0 ||
           !cvalid0 || !ckept0) {
-#pragma omp atomic write
         bad = 1;
       } else {
-        /* token scores, folded straight into the chunk and block maxima */
-        for (int64_t t = lo; t < hi; t++) {
-          int64_t g = INT64_MIN;
-          for (int j = j_lo; j < j_hi; j++) {
-            int64_t dot = 0;
-            if (d->key_fp8) {
-              /* FP8 keys: the dot of the folded query with the E4M3 values (fp8_dot), ranked
-               * through its ordered integer */
-              double mag;
-              dot = ordered_key64(fp8_dot(d, qf + j * D, kq, page_table, b, h, t, &mag));
-            } else {
-              for (int c = 0; c < D; c++)
-                dot += (int64_t)qq[j * D + c] * (int64_t)kq[cache_index(d, page_table, b, h, t, c)];
+        /* token scores, folded into the block maxima: a block is a range of tokens of its
+         * own, so the blocks are scored in parallel; a chunk's maximum is then the maximum
+         * of its blocks' (blocks nest in chunks, chunks in coarse chunks) */
+        const int64_t kb_lo = hi > lo ? lo / d->block : 0;
+        const int64_t kb_hi = hi > lo ? (hi + d->block - 1) / d->block : 0;
+#pragma omp parallel for schedule(static)
+        for (int64_t k = kb_lo; k < kb_hi; k++) {
+          const int64_t t0 = k * d->block > lo ? k * d->block : lo;
+          const int64_t t1 = (k + 1) * d->block < hi ? (k + 1) * d->block : hi;
+          for (int64_t t = t0; t < t1; t++) {
+            int64_t g = INT64_MIN;
+            for (int j = j_lo; j < j_hi; j++) {
+              int64_t dot = 0;
+              if (d->key_fp8) {
+                /* FP8 keys: the dot of the folded query with the E4M3 values (fp8_dot),
+                 * ranked through its ordered integer */
+                double mag;
+                dot = ordered_key64(fp8_dot(d, qf + j * D, kq, page_table, b, h, t, &mag));
+              } else {
+                for (int c = 0; c < D; c++)
+                  dot += (int64_t)qq[j * D + c] *
+                         (int64_t)kq[cache_index(d, page_table, b, h, t, c)];
+              }
+              if (dot > g) g = dot;
             }
-            if (dot > g) g = dot;
+            if (!bvalid[k] || g > bmax[k]) bmax[k] = g;
+            bvalid[k] = 1;
           }
-          int64_t ci = t / d->chunk, bi = t / d->block, c0i = t / c0;
-          if (!cvalid0[c0i] || g > cmax0[c0i]) cmax0[c0i] = g;
+        }
+        for (int64_t k = kb_lo; k < kb_hi; k++) {
+          if (!bvalid[k]) continue;
+          const int64_t ci = k * d->block / d->chunk, c0i = k * d->block / c0;
+          if (!cvalid0[c0i] || bmax[k] > cmax0[c0i]) cmax0[c0i] = bmax[k];
           cvalid0[c0i] = 1;
-          if (!cvalid[ci] || g > cmax[ci]) cmax[ci] = g;
-          if (!bvalid[bi] || g > bmax[bi]) bmax[bi] = g;
+          if (!cvalid[ci] || bmax[k] > cmax[ci]) cmax[ci] = bmax[k];
           cvalid[ci] = 1;
-          bvalid[bi] = 1;
         }
         if (block_max) {
           /* FP8 keys: the ordered integer of the block maximum rounded to fp32 (the exact
@@ -725,5 +737,14 @@ int oracle_num_threads(void) {
   return omp_get_max_threads();
 #else
   return 1;
+#endif
+}
+
+/* The threads later calls may use (n >= 1); a timing of one thread sets 1, then restores. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
 #endif
 }

@@ -92,6 +92,8 @@ def _lib():
             fn.argtypes = args
             fn.restype = ctypes.c_int
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
         _LIB = lib
     return _LIB
 
@@ -120,6 +122,11 @@ def _check(rc: int, name: str) -> None:
 
 def num_threads() -> int:
     return int(_lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """The threads later oracle calls may use (n >= 1)."""
+    _lib().oracle_set_num_threads(int(n))
 
 
 def quantize_keys(d: Dims, k: np.ndarray, page_table, seq_lens, bh_mask=None):
