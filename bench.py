@@ -257,7 +257,8 @@ class Case:
         self.out_d = torch.zeros_like(self.out)
         self.lse_d = torch.zeros_like(self.lse)
 
-    # the whole step, its four kernels one at a time, and the dense comparison, on replica r
+    # the whole step, the pruning form's four kernels one at a time (the per-kernel
+    # breakdown), and the dense comparison, on replica r
     def step(self, r):
         self.hsa.hsa_decode_step(self.d, self.q, self.k_new, self.v_new, self.out, self.lse,
                                  self.k[r], self.v[r], self.kq[r], self.ks[r], self.pt,
@@ -575,7 +576,8 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
         names_c = ("step_cached", "attend_cached", "step_cached_mass")
         timed_steps(case, 3, names_c)
         cached, _ = timed_steps(case, max(3, min(steps, 300)), names_c)
-    # kernel breakdown: the average launch duration of each of the four kernels
+    # kernel breakdown: the average launch duration of each of the pruning form's four
+    # kernels (the scorer's is the roofline's)
     bsteps = max(3, min(steps // 10, 200))
     per = burst_times(case, names, bsteps)
     if dense:
@@ -926,9 +928,11 @@ def main():
         "timing": "value: K whole steps (hsa_decode_step with device buffers) back to back, "
                   "replayed from a CUDA graph of 10 steps (cache replicas alternating), one "
                   "pair of CUDA events around all K, the same method as the dense decode and "
-                  "the per-kernel breakdown (graphs of 10 back-to-back launches of one kernel); "
-                  "step_latency_us: one step per graph replay, events around each replay "
-                  "(includes the graph launch)",
+                  "the per-kernel breakdown (graphs of 10 back-to-back launches of one kernel: "
+                  "the pruning form's append, scorer, pruning kernel and attention, through "
+                  "their own entry points; at 128K the step itself runs the scorer and the "
+                  "selecting attention); step_latency_us: one step per graph replay, events "
+                  "around each replay (includes the graph launch)",
         "step_latency_us": main_res["latency_ms"] * 1e3,
         "clocks": clocks,
         "breakdown_us": {k: v * 1e3 for k, v in per.items()},

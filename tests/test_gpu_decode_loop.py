@@ -77,6 +77,50 @@ def test_prepared_decode_step_equals_the_plain_call():
             assert torch.equal(a, b)
 
 
+def test_recorded_steps_beyond_the_kept_sets():
+    """hsa_decode_step keeps the recordings of its 64 most recently used argument sets: 70
+    calls with 70 output buffers (70 sets) on the same inputs, then the first set again
+    (recorded anew after its eviction), all give the bits of the first call; an argument
+    error is still returned before anything is recorded or launched."""
+    cfg = dataclasses.replace(W.CONFIGS["llama3-8b-128k"], context=None,
+                              context_range=(2000, 4000), batch=2, hq=8, hkv=2, k1=10, k2=8,
+                              sink=32, window=64, paged_permuted=True)
+    wl = W.make_workload(cfg, seed=6)
+    hd, _ = H.dims_pair(wl)
+    dwl = H.to_cuda(wl)
+    dev = torch.device("cuda")
+    B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
+    kq = H.kq_like(dwl["k_cache"], hd)
+    k_scale = torch.zeros((B, Hkv, 128), dtype=torch.float32, device=dev)
+    hsa.hsa_quantize_keys(hd, dwl["k_cache"], dwl["page_table"], dwl["seq_lens"], 0, 0, kq,
+                          k_scale, hsa.workspace(hd, hsa.HSA_OP_QUANTIZE))
+    lens = dwl["seq_lens"]
+    n = lens.long() - 1
+    pages = dwl["page_table"].long().gather(1, (n // 16).unsqueeze(1)).squeeze(1)
+    k_new = dwl["k_cache"][pages, :, n % 16, :].contiguous()  # re-append the last token
+    v_new = dwl["v_cache"][pages, :, n % 16, :].contiguous()
+    ws = hsa.workspace(hd, hsa.HSA_OP_STEP)
+
+    def call(out, lse):
+        hsa.hsa_decode_step(hd, dwl["q"], k_new, v_new, out, lse, dwl["k_cache"], dwl["v_cache"],
+                            kq, k_scale, dwl["page_table"], lens, None, None, ws)
+
+    outs = [(torch.full((B, Hq, 128), float("nan"), device=dev),
+             torch.full((B, Hq), float("nan"), device=dev)) for _ in range(70)]
+    for o, l in outs:
+        call(o, l)
+    o0, l0 = outs[0]
+    o0.fill_(float("nan"))
+    call(o0, l0)  # the first set, evicted by the 69 after it
+    torch.cuda.synchronize()
+    assert hsa.hsa_read_device_error(ws) == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+    with pytest.raises(hsa.HsaError):
+        hsa.hsa_decode_step(hd, dwl["q"], k_new, v_new, o0, l0, dwl["k_cache"], dwl["v_cache"],
+                            kq, k_scale, dwl["page_table"], lens, None, None, ws[:64])
+
+
 @pytest.mark.parametrize("refresh,on_host,key_bits,per_head,fp8", [
     (3, False, 8, 0, 0), (2, True, 8, 0, 0), (1, False, 8, 0, 0), (2, False, 4, 0, 0),
     (2, False, 8, 1, 0), (2, False, 8, 0, 1)])
