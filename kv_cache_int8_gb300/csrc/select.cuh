@@ -451,7 +451,6 @@ __device__ __forceinline__ int sel_fast_reg(Get get, int n, int K, int vmin, int
   constexpr int kWarps = NT / 32;
   if (K <= 0) return 0;  // keeps nothing (the same in every thread: no barrier is skipped)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned lt = sel_lanemask_lt();
   const unsigned umin = (unsigned)vmin;
   const int shift = fast_shift(vmin, vmax);
   const int per = (n + NT - 1) / NT;  // <= R (the caller checks n <= R * NT)
