@@ -64,9 +64,9 @@ constexpr int kTileBlocks = 4;                  // blocks per ring slot (64 toke
 constexpr int kTileTokens = kTileBlocks * kPage;
 constexpr int kMaxBatch = 1024;                 // sequences (the tile prefix sums in shared memory)
 // 8-bit codes, up to 4 heads: short scans (at most kShortScanTiles tiles) run the
-// shared-memory-query shape, 3 CTAs a SM with fewer tiles each, which ends the scan sooner
-// inside the step (128K: 43.9 against 45.4 us a step); long ones keep the query words in
-// registers, 2 CTAs a SM (1M: 194.3 against 196.6 us).
+// shared-memory-query shape, more and smaller CTAs with fewer tiles each, which end the scan
+// sooner inside the step (128K: 43.6 against 45.4 us a step); long ones keep the query words
+// in registers, 2 CTAs a SM (1M: 194.3 against 196.6 us with the query in shared memory).
 constexpr long long kShortScanTiles = 32768;
 
 // Key formats of the scorer instances.
@@ -76,21 +76,41 @@ constexpr int kKeyFp8 = 2;   // FP8 E4M3 codes: fp32 scores
 
 // Launch shape and shared-memory layout of one scorer instance (KF: key format; PH:
 // per-head maxima, whose epilogue needs the registers the query words would take).
+// The short-scan shape (8-bit codes, up to 4 heads, query in shared memory): consumer
+// warps, CTAs a SM and ring KiB a CTA. Measured at 128K (step / scorer alone, us): 2 x 5 with
+// 32 KiB rings 43.6 / 23.3; 3 x 4, 48 KiB 43.7 / 23.9; 4 x 3, 64 KiB 43.8 / 23.8; 2 x 4,
+// 32 KiB 44.4 / 23.8; 4 x 2, 64 KiB 45.3 / 24.3.
+#ifndef HSA_SCORE_Q8_WARPS
+#define HSA_SCORE_Q8_WARPS 2
+#endif
+#ifndef HSA_SCORE_Q8_CTAS
+#define HSA_SCORE_Q8_CTAS 5
+#endif
+#ifndef HSA_SCORE_Q8_RING_KB
+#define HSA_SCORE_Q8_RING_KB 32
+#endif
+
 template <int G, int KF, bool PH, bool QS = false>
 struct ScoreCfg {
   static constexpr bool KB4 = KF == kKeyInt4;
   static constexpr bool kQSmem = KF != kKeyInt8 || G > 4 || PH || QS;  // query in shared memory
-  static constexpr int kWarps = KB4 ? HSA_SCORE_QS_WARPS : (kQSmem ? 4 : HSA_SCORE_WARPS);
+  static constexpr bool kShort = QS && KF == kKeyInt8 && G <= 4 && !PH;  // the short-scan shape
+  static constexpr int kWarps =
+      KB4 ? HSA_SCORE_QS_WARPS : (kShort ? HSA_SCORE_Q8_WARPS : (kQSmem ? 4 : HSA_SCORE_WARPS));
   static constexpr int kThreads = (kWarps + 1) * 32;
   // FP8 with 8 heads: the fp32 query of 4 warps takes 16 KiB, so 2 CTAs fit per SM
   static constexpr int kCtasPerSm =
-      KB4 ? HSA_SCORE_QS_CTAS : (KF == kKeyFp8 && G > 4 ? 2 : (kQSmem ? 3 : HSA_SCORE_CTAS));
+      KB4 ? HSA_SCORE_QS_CTAS
+          : (kShort ? HSA_SCORE_Q8_CTAS
+                    : (KF == kKeyFp8 && G > 4 ? 2 : (kQSmem ? 3 : HSA_SCORE_CTAS)));
   // 8-bit codes: one 128-byte row per token; 4-bit codes: two tokens per row
   static constexpr int kRowsPerBlock = KB4 ? kPage / 2 : kPage;
   static constexpr int kBlockBytes = kRowsPerBlock * kHeadDim;
   static constexpr int kSlotBytes = kTileBlocks * kBlockBytes;
   static constexpr int kRingBytes =
-      (KB4 ? HSA_SCORE_QS_RING_KB : (kQSmem ? 64 : HSA_SCORE_RING_KB)) * 1024;  // one CTA's ring
+      (KB4 ? HSA_SCORE_QS_RING_KB
+           : (kShort ? HSA_SCORE_Q8_RING_KB : (kQSmem ? 64 : HSA_SCORE_RING_KB))) *
+      1024;  // one CTA's ring
   static constexpr int kStages = kRingBytes / kSlotBytes;
   static_assert(kStages % kWarps == 0 && kStages / kWarps >= 2,
                 "every consumer warp owns at least two fixed ring slots");
