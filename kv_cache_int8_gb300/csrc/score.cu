@@ -63,11 +63,15 @@ namespace {
 constexpr int kTileBlocks = 4;                  // blocks per ring slot (64 tokens)
 constexpr int kTileTokens = kTileBlocks * kPage;
 constexpr int kMaxBatch = 1024;                 // sequences (the tile prefix sums in shared memory)
-// 8-bit codes, up to 4 heads: short scans (at most kShortScanTiles tiles) run the
-// shared-memory-query shape, more and smaller CTAs with fewer tiles each, which end the scan
-// sooner inside the step (128K: 43.6 against 45.4 us a step); long ones keep the query words
-// in registers, 2 CTAs a SM (1M: 194.3 against 196.6 us with the query in shared memory).
-constexpr long long kShortScanTiles = 32768;
+// 8-bit codes, up to 4 heads: short scans (at most kShortScanTiles tiles) and batches of
+// several sequences run the shared-memory-query shape, more and smaller CTAs with fewer tiles
+// each (128K: 43.6 against 45.4 us a step; 8 sequences of 32K-128K tokens in permuted pages:
+// 122.7 against 125.8 us); one long sequence keeps the query words in registers, 2 CTAs a SM
+// (1M: 194.4 against 197.8 us with the short shape).
+#ifndef HSA_SCORE_SHORT_TILES
+#define HSA_SCORE_SHORT_TILES 32768
+#endif
+constexpr long long kShortScanTiles = HSA_SCORE_SHORT_TILES;
 
 // Key formats of the scorer instances.
 constexpr int kKeyInt8 = 0;  // 8-bit integer codes
@@ -90,26 +94,42 @@ constexpr int kKeyFp8 = 2;   // FP8 E4M3 codes: fp32 scores
 #define HSA_SCORE_Q8_RING_KB 32
 #endif
 
+// FP8 codes with up to 4 heads: consumer warps, CTAs a SM and ring KiB a CTA.
+#ifndef HSA_SCORE_F8_WARPS
+#define HSA_SCORE_F8_WARPS 4
+#endif
+#ifndef HSA_SCORE_F8_CTAS
+#define HSA_SCORE_F8_CTAS 3
+#endif
+#ifndef HSA_SCORE_F8_RING_KB
+#define HSA_SCORE_F8_RING_KB 64
+#endif
+
 template <int G, int KF, bool PH, bool QS = false>
 struct ScoreCfg {
   static constexpr bool KB4 = KF == kKeyInt4;
   static constexpr bool kQSmem = KF != kKeyInt8 || G > 4 || PH || QS;  // query in shared memory
   static constexpr bool kShort = QS && KF == kKeyInt8 && G <= 4 && !PH;  // the short-scan shape
+  static constexpr bool kF8 = KF == kKeyFp8 && G <= 4;
   static constexpr int kWarps =
-      KB4 ? HSA_SCORE_QS_WARPS : (kShort ? HSA_SCORE_Q8_WARPS : (kQSmem ? 4 : HSA_SCORE_WARPS));
+      KB4 ? HSA_SCORE_QS_WARPS
+          : (kShort ? HSA_SCORE_Q8_WARPS
+                    : (kF8 ? HSA_SCORE_F8_WARPS : (kQSmem ? 4 : HSA_SCORE_WARPS)));
   static constexpr int kThreads = (kWarps + 1) * 32;
   // FP8 with 8 heads: the fp32 query of 4 warps takes 16 KiB, so 2 CTAs fit per SM
   static constexpr int kCtasPerSm =
       KB4 ? HSA_SCORE_QS_CTAS
           : (kShort ? HSA_SCORE_Q8_CTAS
-                    : (KF == kKeyFp8 && G > 4 ? 2 : (kQSmem ? 3 : HSA_SCORE_CTAS)));
+                    : (kF8 ? HSA_SCORE_F8_CTAS
+                           : (KF == kKeyFp8 && G > 4 ? 2 : (kQSmem ? 3 : HSA_SCORE_CTAS))));
   // 8-bit codes: one 128-byte row per token; 4-bit codes: two tokens per row
   static constexpr int kRowsPerBlock = KB4 ? kPage / 2 : kPage;
   static constexpr int kBlockBytes = kRowsPerBlock * kHeadDim;
   static constexpr int kSlotBytes = kTileBlocks * kBlockBytes;
   static constexpr int kRingBytes =
       (KB4 ? HSA_SCORE_QS_RING_KB
-           : (kShort ? HSA_SCORE_Q8_RING_KB : (kQSmem ? 64 : HSA_SCORE_RING_KB))) *
+           : (kShort ? HSA_SCORE_Q8_RING_KB
+                     : (kF8 ? HSA_SCORE_F8_RING_KB : (kQSmem ? 64 : HSA_SCORE_RING_KB)))) *
       1024;  // one CTA's ring
   static constexpr int kStages = kRingBytes / kSlotBytes;
   static_assert(kStages % kWarps == 0 && kStages / kWarps >= 2,
@@ -706,7 +726,7 @@ cudaError_t launch_score_blocks(const Shape& s, const CUtensorMap& kq_map,
         return go(score_blocks_kernel<g, kKeyFp8, ph>, ScoreCfg<g, kKeyFp8, ph>{});
       default:
         if constexpr (g <= 4 && !ph) {
-          if (tiles_max <= kShortScanTiles)
+          if (tiles_max <= kShortScanTiles || s.batch > 1)
             return go(score_blocks_kernel<g, kKeyInt8, ph, true>, ScoreCfg<g, kKeyInt8, ph, true>{});
         }
         return go(score_blocks_kernel<g, kKeyInt8, ph>, ScoreCfg<g, kKeyInt8, ph>{});
