@@ -779,8 +779,10 @@ static int32_t decode_step_impl(const hsa_dims* d, const hsa_step_io* io, void* 
   }
   // the prune also resolves the kept blocks' pages, so the attend needs one round trip for them
   int32_t* sel_pages = reinterpret_cast<int32_t*>(ws + l.sel_pages);
-  e = hsa::launch_prune(prune_shape(s), seq_lens, bm, tm, nullptr, nullptr, bidx, nb, page_table,
-                        sel_pages, err, st, row_range);
+  Shape ps = prune_shape(s);
+  ps.k1 = module1_keep(ps);  // no chunk ids are output: the same kept blocks
+  e = hsa::launch_prune(ps, seq_lens, bm, tm, nullptr, nullptr, bidx, nb, page_table, sel_pages,
+                        err, st, row_range);
   if (e != cudaSuccess) return HSA_ERR_CUDA;
   rc = block_cache ? do_attend_cached(s, q, kd, vd, page_table, seq_lens, bidx, nb, out, lse, ws,
                                       l.att, l.cache, block_cache, capacity, st)

@@ -1534,7 +1534,7 @@ bool plan_select(const Shape& s, SelArgs& sa, bool stage_pages) {
   // chunks: the 128K-token configurations); longer rows go to the pruning kernel, whose
   // 512 threads select them faster (1M tokens: 196.4 against 198.0 us a step).
   if (n1max > (long long)kSelRegVals * (W + 1) * 32) return false;
-  const long long keep1 = std::min<long long>(s.k1, n1max);
+  const long long keep1 = std::min<long long>(module1_keep(s), n1max);
   const long long n2max = keep1 * P;
   sa.n2_cap = up4(std::max<long long>(n2max, 1));
   sa.a_cap = std::max(up4(n1max + 4), 2 * sa.n2_cap);
@@ -1699,7 +1699,7 @@ cudaError_t launch_attend_select(const Shape& s, const void* q, const void* k_ca
   sa.block_idx = block_idx;
   sa.n_blocks = n_blocks;
   sa.max_tiles = (s.max_pages + kTileBlocksSel - 1) / kTileBlocksSel;
-  sa.k1 = s.k1;
+  sa.k1 = module1_keep(s);
   AttArgs a = {};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k_cache);

@@ -395,6 +395,31 @@ def test_modules_defining_property_brute_force(seed):
                 assert sorted(ranked) == kept_b
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_module1_keeping_k2_chunks_keeps_the_same_blocks(seed):
+    """With K1 >= K2, module 1 keeping only the top K2 chunks leaves module 2's kept blocks
+    unchanged: every chunk ranked above a kept block's chunk holds a block ranked above that
+    block. The whole decode step relies on this (it outputs no chunk ids)."""
+    rng = np.random.default_rng(700 + seed)
+    D, hkv, G = 8, 2, 2
+    lens = tuple(int(x) for x in rng.integers(64, 900, size=2))
+    case = random_case(rng, B=2, hq=hkv * G, hkv=hkv, D=D, lens=lens, page=16, perm=True)
+    for b in range(2):
+        case["ks"][b] = np.round(case["ks"][b] * 2) / 2  # frequent ties
+    kc, pt, ln = paged(case["ks"], 16, hkv, None)
+    case.update(k=kc, pt=pt)
+    k2 = int(rng.integers(1, 10))
+    k1 = k2 + int(rng.integers(0, 8))
+    d = dims_for(case, hkv * G, hkv, D, chunk=64, block=16, k1=k1, k2=k2,
+                 sink=int(rng.integers(0, 40)), window=int(rng.integers(1, 60)))
+    kq, sc = oracle.quantize_keys(d, bf16_bits(kc), pt, ln)
+    full = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln)
+    d.k1 = k2
+    short = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln)
+    np.testing.assert_array_equal(full["block_idx"], short["block_idx"])
+    np.testing.assert_array_equal(full["n_blocks"], short["n_blocks"])
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_three_stacked_modules_defining_property_brute_force(seed):
     """A first module on coarse chunks (chunk0 tokens) keeps the top K0; module 1 ranks only
