@@ -168,11 +168,13 @@ def traffic_record(kernel_file: str, summary_name: str):
 # -------------------------------------------------------------- GPU arm
 
 class Case:
-    """One workload resident on the GPU: two cache replicas, their int8 codes and scales,
-    buffers, and the captured graphs."""
+    """One workload resident on the GPU: cache replicas (two, or five when one replica's key
+    codes are smaller than L2), their int8 codes and scales, buffers, and the captured
+    graphs."""
 
     KERNELS = ("step", "append", "score", "prune", "attend", "dense")
-    BURST = 10
+    BURST = 10  # a multiple of every replica count
+    L2_BYTES = 129 << 20
     REFRESH = 4
     CACHE_SLOTS = 8192  # GPU block cache of the offloaded case: 64 MiB of K/V blocks
 
@@ -204,24 +206,32 @@ class Case:
         B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
         self.q = wl["q"]
         self.pt, self.lens = wl["page_table"], wl["seq_lens"]
+        # replicas: consecutive steps read different ones, and between two reads of the same
+        # replica's key codes the steps read more than twice L2 of other codes (4-bit codes
+        # at 128K tokens, 67 MB a replica, take five)
+        kq_shape = list(wl["k_cache"].shape)
+        kq_shape[-1] = kq_shape[-1] * cfg.key_bits // 8  # 4-bit codes: two per byte
+        codes = cfg.hkv * sum(wl["lens"]) * 128 * cfg.key_bits // 8
+        self.nrep = 2 if cfg.kv_on_host or codes >= self.L2_BYTES else 5
         if cfg.kv_on_host:
             self.k = [wl["k_cache"], wl["k_cache"]]
             self.v = [wl["v_cache"], wl["v_cache"]]
         else:
-            self.k = [wl["k_cache"], wl["k_cache"].clone()]
-            self.v = [wl["v_cache"], wl["v_cache"].clone()]
-        kq_shape = list(self.k[0].shape)
-        kq_shape[-1] = kq_shape[-1] * cfg.key_bits // 8  # 4-bit codes: two per byte
-        self.kq = [torch.zeros(kq_shape, dtype=torch.int8, device=device) for _ in range(2)]
+            self.k = [wl["k_cache"]] + [wl["k_cache"].clone() for _ in range(self.nrep - 1)]
+            self.v = [wl["v_cache"]] + [wl["v_cache"].clone() for _ in range(self.nrep - 1)]
+        self.kq = [torch.zeros(kq_shape, dtype=torch.int8, device=device)
+                   for _ in range(self.nrep)]
         self.ks = [torch.zeros((B, Hkv, 128), dtype=torch.float32, device=device)
-                   for _ in range(2)]
+                   for _ in range(self.nrep)]
         wq = hsa.workspace(d, hsa.HSA_OP_QUANTIZE)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record()
         hsa.hsa_quantize_keys(d, self.k[0], self.pt, self.lens, 0, 0, self.kq[0], self.ks[0], wq)
         e1.record()
-        hsa.hsa_quantize_keys(d, self.k[1], self.pt, self.lens, 0, 0, self.kq[1], self.ks[1], wq)
+        for r in range(1, self.nrep):
+            hsa.hsa_quantize_keys(d, self.k[r], self.pt, self.lens, 0, 0, self.kq[r], self.ks[r],
+                                  wq)
         torch.cuda.synchronize()
         self.quantize_ms = e0.elapsed_time(e1)
         # the new token of the step: re-append the current last token (cache unchanged)
@@ -314,23 +324,23 @@ class Case:
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
-            for r in range(2):
+            for r in range(self.nrep):
                 for name in self.kernels:
                     getattr(self, name)(r)
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
-        for r in range(2):
+        for r in range(self.nrep):
             for name in self.kernels:
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
                     getattr(self, name)(r)
                 self.graphs[(name, r)] = g
         # the decode loop: a whole step, then REFRESH - 1 steps reusing its selection
-        for r in range(2):
+        for r in range(self.nrep):
             self.step(r)
             self.reuse(r)
         torch.cuda.synchronize()
-        for r in range(2):
+        for r in range(self.nrep):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 self.step(r)
@@ -349,7 +359,7 @@ class Case:
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
                     for i in range(self.BURST):
-                        getattr(self, name)(i & 1)
+                        getattr(self, name)(i % self.nrep)
                 self.burst[name] = g
         torch.cuda.synchronize()
 
@@ -405,7 +415,7 @@ def timed_steps(case, steps: int, names, sampler=None):
     # a short head start so that the launch queue runs ahead of the GPU
     torch.cuda._sleep(2_000_000)
     for i in range(steps):
-        r = i & 1
+        r = i % case.nrep
         ev = evs[i]
         if case.flush is not None:
             case.flush.fill_(i & 0xFF)  # evict the previous step's data from L2
@@ -437,7 +447,7 @@ def timed_step_run(case, steps: int, sampler=None):
         tail = torch.cuda.CUDAGraph()
         with torch.cuda.graph(tail):
             for i in range(rest):
-                case.step(i & 1)
+                case.step(i % case.nrep)
         tail.replay()
     case.burst["step"].replay()  # untimed: the burst graph's first replay
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -608,6 +618,7 @@ def gpu_case_numbers(name, seed, device, steps, warmup, sampler, peak, world=1, 
                   "dense": case.bytes_dense()},
         "recall": {"mean": float(recall.mean()), "min": float(recall.min())},
         "quantize_ms": case.quantize_ms,
+        "replicas": case.nrep,
     }
     b = res["bytes"]
     res["gbs"] = {
@@ -731,13 +742,13 @@ def profile_steps(name, device, steps, warmup):
     import torch
     case = Case(name, 0, device, dense=not W_CONFIGS()[name].kv_on_host)
     for i in range(warmup):
-        case.step(i & 1)
+        case.step(i % case.nrep)
     torch.cuda.synchronize()
     for i in range(steps):
-        case.step(i & 1)
+        case.step(i % case.nrep)
     n_dense = steps // 2 if "dense" in case.kernels else 0
     for i in range(n_dense):
-        case.dense(i & 1)
+        case.dense(i % case.nrep)
     torch.cuda.synchronize()
     for w in (case.ws_step, case.ws_den):
         code = case.hsa.hsa_read_device_error(w)
@@ -829,6 +840,7 @@ def main():
                 "score_gbs": r["gbs"]["score"],
                 "attend_gbs" + ("_host_link" if r["cached_ms"] else ""): r["gbs"]["attend"],
                 "bytes": r["bytes"], "quantize_keys_ms": r["quantize_ms"],
+                "replicas": r["replicas"],
             }
     if not args.no_extra and args.config != EXTRA_CONFIG:
         r = gpu_case_numbers(EXTRA_CONFIG, rank, device, min(args.steps, 1500), args.warmup, None,
