@@ -53,6 +53,11 @@
 #endif
 // The whole decode step runs the pruning modules inside the sparse attention (0: a pruning
 // kernel, then the sparse attention, as hsa_select + hsa_attend).
+// 1: with K1 >= K2 the selecting attention ranks only the blocks at or above the K2-th
+// largest chunk maximum (sel_blocks_over_threshold), else the two modules' fast paths
+#ifndef HSA_SEL_THRESHOLD
+#define HSA_SEL_THRESHOLD 1
+#endif
 #ifndef HSA_FUSED_SELECT
 #define HSA_FUSED_SELECT 1
 #endif
@@ -1032,6 +1037,182 @@ __host__ __device__ SelSmem sel_smem_layout(const SelArgs& sa) {
   return l;
 }
 
+// The kept blocks of a row when K1 >= K2, by NT threads (all of the CTA). The two modules
+// then keep the top K2 blocks of the candidate region (ranked by maximum, the lower index
+// first among equals), and T1, the K2-th largest chunk maximum, bounds them from below: the
+// top K2 chunks each hold a block equal to their maximum, so at least K2 blocks reach T1.
+// Steps: T1 by the register histogram of the chunk maxima (values in [t_min, t_max]; two CTA
+// barriers); the blocks >= T1 (only chunks >= T1 hold one) written in ascending order to
+// cv / ci (values / ids; cap entries); the n_c - K2 lowest ranked of them (usually a few)
+// taken one a round by warp 0, every kept block then written to its place in selb
+// (ascending: its index among the candidates minus the dropped ones before it); with more
+// than kPeel to drop, the selection of select.cuh over the candidates (values in
+// [T1, vmax]). The kept blocks' pages go to selp (prow staged, else -1). Returns K2, or -1
+// with nothing written (fhist and n_cand left zero) when the row needs the general modules:
+// K2 or fewer valid chunks, a bin of the K2-th value wider than kSelSmall, or more than cap
+// candidates. The same value in every thread.
+template <int NT, int R, int P>
+__device__ __forceinline__ int sel_blocks_over_threshold(const int* tiles, int n1, int c_lo,
+                                                         const int* brow, int k_lo, int k_hi,
+                                                         int K2, int t_min, int t_max, int vmax,
+                                                         const int* prow, int* cv, int* ci,
+                                                         int cap, SelectShared& ss, int* selb,
+                                                         int* selp) {
+  constexpr int kW = NT / 32;
+  constexpr int kPeel = 8;  // at most this many dropped candidates are taken one a round
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned umin = (unsigned)t_min;
+  const int shift = fast_shift(t_min, t_max);
+  const int per = (n1 + NT - 1) / NT;  // <= R (checked by the caller)
+  const int x0 = min(n1, tid * per), nv = min(n1, x0 + per) - x0;
+  int v[R];
+#pragma unroll
+  for (int r = 0; r < R; r++) v[r] = r < nv ? tiles[x0 + r] : INT_MIN;
+  int valid = 0;
+#pragma unroll
+  for (int r = 0; r < R; r++)
+    if (v[r] != INT_MIN) {
+      valid++;
+      sel_red_add(&ss.fhist[fast_bin(v[r], umin, shift)], 1u);
+    }
+  const int vw = __reduce_add_sync(0xffffffffu, valid);
+  if (lane == 0) ss.wsum[warp] = vw;
+  __syncthreads();
+  int n_valid = 0;
+#pragma unroll
+  for (int w = 0; w < kW; w++) n_valid += ss.wsum[w];
+  int3 loc = make_int3(0, 0, 0);
+  if (n_valid > K2) loc = fast_locate(ss.fhist, K2);
+  if (n_valid <= K2 || loc.z > kSelSmall) {
+    __syncthreads();  // every warp has read the histogram
+    for (int i = tid; i < kFastBins; i += NT) ss.fhist[i] = 0u;
+    __syncthreads();
+    return -1;
+  }
+  // T1: the (K2 - above)-th largest value of the located bin, ranked by every warp
+  const int d = loc.x, above = loc.y, cnt = loc.z;
+#pragma unroll
+  for (int r = 0; r < R; r++)
+    if (v[r] != INT_MIN && fast_bin(v[r], umin, shift) == d) {
+      const int slot = sel_atom_add(&ss.n_cand, 1);
+      if (slot < kSelSmall) ss.cand[slot] = v[r];
+    }
+  __syncthreads();
+  int T1;
+  {
+    const int c = lane < cnt ? ss.cand[lane] : INT_MIN;
+    int gtc = 0, gec = 0;
+    for (int j = 0; j < cnt; j++) {
+      const int cj = __shfl_sync(0xffffffffu, c, j);
+      gtc += cj > c ? 1 : 0;
+      gec += cj >= c ? 1 : 0;
+    }
+    const int need = K2 - above;
+    const int L = __ffs(__ballot_sync(0xffffffffu, lane < cnt && gtc < need && need <= gec)) - 1;
+    T1 = __shfl_sync(0xffffffffu, c, L);
+  }
+  // the candidates: blocks >= T1 of the thread's chunks, counted, then placed in order
+  int nc = 0;
+#pragma unroll
+  for (int r = 0; r < R; r++)
+    if (v[r] >= T1 && v[r] != INT_MIN) {
+#pragma unroll
+      for (int q = 0; q < P; q++) {
+        const int kk = (c_lo + x0 + r) * P + q;
+        if (kk >= k_lo && kk < k_hi && brow[kk - k_lo] >= T1) nc++;
+      }
+    }
+  int incl = nc;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) ss.w_a[warp] = incl;
+  for (int i = tid; i < kFastBins; i += NT) ss.fhist[i] = 0u;  // read by every warp above
+  if (tid == 0) ss.n_cand = 0;
+  __syncthreads();
+  int n_c = 0, base = 0;
+#pragma unroll
+  for (int w = 0; w < kW; w++) {
+    n_c += ss.w_a[w];
+    base += w < warp ? ss.w_a[w] : 0;
+  }
+  const int drop = n_c - K2;  // >= 0: the K2 chunks above T1 each hold one
+  if (n_c > cap) return -1;  // nothing written; fhist and n_cand zero
+  int pos = base + incl - nc;
+#pragma unroll
+  for (int r = 0; r < R; r++)
+    if (v[r] >= T1 && v[r] != INT_MIN) {
+#pragma unroll
+      for (int q = 0; q < P; q++) {
+        const int kk = (c_lo + x0 + r) * P + q;
+        if (kk >= k_lo && kk < k_hi) {
+          const int bv = brow[kk - k_lo];
+          if (bv >= T1) {
+            cv[pos] = bv;
+            ci[pos] = kk;
+            pos++;
+          }
+        }
+      }
+    }
+  __syncthreads();
+  if (drop > kPeel) {
+    // many to drop: the register selection over the candidates (ids written in order), else
+    // the radix select and ordered collect (positions among the candidates)
+    int got = sel_fast_row<NT, R>(SelRow{cv, ci, 0}, n_c, K2, T1, vmax, ss, selb);
+    if (got < 0) {
+      const int3 r3 = sel_kth_largest<NT>(cv, n_c, K2, ss, true, T1, vmax);
+      got = sel_collect<NT>(cv, n_c, r3.x, r3.y, r3.z, ss, selb, 0);
+      for (int i = tid; i < got; i += NT) selb[i] = ci[selb[i]];
+    }
+    for (int i = tid; i < K2; i += NT) selp[i] = prow != nullptr ? prow[selb[i] - k_lo] : -1;
+    __syncthreads();
+    return K2;
+  }
+  // a few to drop: the lowest ranked (smallest maximum, the higher index first among equals),
+  // taken one a round by warp 0 (a warp-wide minimum a round)
+  if (drop > 0 && warp == 0) {
+    for (int e = 0; e < drop; e++) {
+      int bv = INT_MAX, bi = -1;
+      for (int i = lane; i < n_c; i += 32) {
+        const int vi = cv[i];  // INT_MAX: taken in an earlier round (scores are far below it)
+        if (vi < bv || (vi == bv && vi != INT_MAX && i > bi)) {
+          bv = vi;
+          bi = i;
+        }
+      }
+      const int mv = __reduce_min_sync(0xffffffffu, bv);
+      const int mi = __reduce_max_sync(0xffffffffu, bv == mv ? bi : -1);
+      if (lane == 0) {
+        ss.cand_i[e] = mi;
+        cv[mi] = INT_MAX;
+      }
+      __syncwarp();
+    }
+  }
+  if (drop > 0) __syncthreads();
+  // every kept candidate's place: its index minus the dropped ones before it
+  for (int i = tid; i < n_c; i += NT) {
+    int before = 0;
+    bool dropped = false;
+    for (int e = 0; e < drop; e++) {
+      const int de = ss.cand_i[e];
+      before += de < i ? 1 : 0;
+      dropped = dropped || de == i;
+    }
+    if (!dropped) {
+      const int kk = ci[i];
+      selb[i - before] = kk;
+      selp[i - before] = prow != nullptr ? prow[kk - k_lo] : -1;
+    }
+  }
+  __syncthreads();  // every thread has read the dropped list
+  if (tid == 0) ss.n_cand = 0;
+  return K2;
+}
+
 template <int G, int W, int NS>
 __global__ void __launch_bounds__((W + 1) * 32, 1)
     attend_select_kernel(const AttArgs a, const SelArgs sa) {
@@ -1179,11 +1360,29 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
   if (t_plan.bytes() > 0 && !mbar_wait(&sbar[0], 0)) set_error(a.err, kDevErrTimeout);
   __syncthreads();  // the plain-load tails are visible
 
-  // ---- module 1: top-K1 chunks (ascending); the fast path when the scorer's range is known
   const int* tiles = t_plan.dst();
+  const int* brow = r_plan.dst();
+  const int* prow = p_plan.dst();
+  constexpr int kRegVals = kSelRegVals;
+  // ---- K1 >= K2 (module 1 keeps K2 chunks): the blocks at or above the K2-th chunk maximum
+  int got2 = -1;
+  bool ids = false;  // selb holds block ids (fast path) rather than positions in cand2
+  bool mapped = false;  // selb / selp hold the kept blocks' ids and pages
+  if (HSA_SEL_THRESHOLD && sa.k1 >= a.k2 && a.k2 > 0 && use_row && n1 > 0 &&
+      n1 <= kRegVals * NT && rr.x != 0u && rr.y != 0u && rr.z != 0u && rr.w != 0u) {
+    bool ok = true;
+    if (r_plan.bytes() > 0 && !mbar_wait(&sbar[1], 0)) ok = false;
+    if (use_prow && p_plan.bytes() > 0 && !mbar_wait(&sbar[2], 0)) ok = false;
+    if (!ok) set_error(a.err, kDevErrTimeout);
+    got2 = sel_blocks_over_threshold<NT, kRegVals, P>(
+        tiles, n1, c_lo, brow, k_lo, k_hi, a.k2, t_min, t_max, b_max, use_prow ? prow : nullptr,
+        area, area + sa.n2_cap, sa.n2_cap, ss, selb, selp);
+    mapped = got2 >= 0;
+  }
+  if (!mapped) {
+  // ---- module 1: top-K1 chunks (ascending); the fast path when the scorer's range is known
   int got1 = -1;
   const int keep1 = min(sa.k1, n1);
-  constexpr int kRegVals = kSelRegVals;
   if (n1 > 0 && n1 <= kRegVals * NT && rr.x != 0u && rr.y != 0u)
     got1 = sel_fast_row<NT, kRegVals>(SelRow{tiles, nullptr, c_lo}, n1, sa.k1, t_min, t_max, ss,
                                       kept1);
@@ -1204,7 +1403,6 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
   // ---- module 2: the kept chunks' blocks (outside the candidate region: placeholders never
   // kept), top-K2, ascending
   if (use_row && r_plan.bytes() > 0 && !mbar_wait(&sbar[1], 0)) set_error(a.err, kDevErrTimeout);
-  const int* brow = r_plan.dst();
   const int32_t* bm = sa.block_max + row * a.max_pages;
   int* vals2 = area;  // the tile maxima are no longer read (the collect ended on a barrier)
   int* cand2 = area + sa.n2_cap;
@@ -1236,8 +1434,6 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
       }
     }
   }
-  int got2 = -1;
-  bool ids = false;  // selb holds block ids (fast path) rather than positions in cand2
   if (range2 && n2 > 0 && n2 <= kRegVals * NT) {
     __syncthreads();  // the candidates are laid out
     got2 = sel_fast_row<NT, kRegVals>(SelRow{vals2, cand2, 0}, n2, a.k2, b_min, b_max, ss, selb);
@@ -1279,13 +1475,13 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
     }
   }
   if (use_prow && p_plan.bytes() > 0 && !mbar_wait(&sbar[2], 0)) set_error(a.err, kDevErrTimeout);
-  const int* prow = p_plan.dst();
   for (int i = tid; i < got2; i += NT) {
     const int kk = ids ? selb[i] : cand2[selb[i]];
     selb[i] = kk;
     selp[i] = use_prow ? prow[kk - k_lo] : -1;
   }
   __syncthreads();
+  }
   if (split == 0) {
     for (int i = tid; i < a.k2; i += NT) sa.block_idx[row * a.k2 + i] = i < got2 ? selb[i] : -1;
     if (tid == 0) sa.n_blocks[row] = got2;

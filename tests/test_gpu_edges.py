@@ -173,6 +173,54 @@ def test_many_ties_lower_index_wins():
     assert g["block_idx"][0, 0].tolist() == list(range(4, 13))
 
 
+@pytest.mark.parametrize("run,k1,k2", [(64, 20, 17), (16, 20, 17), (64, 12, 5),
+                                         (16, 40, 40), (1, 30, 23)])
+def test_selection_with_runs_of_equal_keys(run, k1, k2):
+    """Keys constant over runs of `run` tokens, the runs' keys random (K1 >= K2, as in the
+    128K configurations, where the whole step keeps the blocks at or above the K2-th chunk
+    maximum). Runs of 64: the four blocks of a chunk tie, so about 4 K2 blocks reach that
+    maximum and many are dropped, equal maxima ranked by index; runs of 16: every block has
+    its own maximum and a few are dropped. Selection bit-exact against the oracle."""
+    wl = W.make_workload(_cfg(context=30000, batch=2, hq=8, hkv=2, k1=k1, k2=k2, sink=64,
+                              window=256, paged_permuted=True), seed=71 + run + k2)
+    pt = wl["page_table"].long()
+    gen = torch.Generator(device="cpu").manual_seed(5 + run)
+    for b, n in enumerate(wl["lens"]):
+        vecs = (torch.randn(((n + run - 1) // run, 2, 128), generator=gen) * 2).to(torch.bfloat16)
+        t = torch.arange(n)
+        wl["k_cache"][pt[b, t // 16], :, t % 16] = vecs[t // run]
+    _check(wl)
+
+
+def test_tied_top_chunks_beyond_the_candidate_room():
+    """Eight chunks of each kv head hold, in every token, the key of its first query head's
+    direction, so their maxima tie at the top: with K2 = 5 the blocks at or above the K2-th
+    chunk maximum number 32, more than the 4 K2 the whole step's short path takes (it then
+    runs the general modules). Lowest indices win the ties."""
+    wl = W.make_workload(_cfg(context=20000, batch=1, hq=8, hkv=2, k1=12, k2=5, sink=64,
+                              window=256), seed=37)
+    pt = wl["page_table"].long()
+    n = wl["lens"][0]
+    chunks = [40, 41, 77, 90, 120, 121, 200, 250]
+    for h in range(2):
+        vec = (wl["q"][0, h * 4].float() * 3).to(torch.bfloat16)
+        for c in chunks:
+            t = torch.arange(c * 64, min(n, c * 64 + 64))
+            wl["k_cache"][pt[0, t // 16], h, t % 16] = vec
+    g, o = _check(wl)
+    for h in range(2):
+        assert g["block_idx"][0, h].tolist() == [160, 161, 162, 163, 164]
+
+
+def test_all_equal_keys_with_k1_at_least_k2():
+    """Every chunk and block maximum equal (the K2-th chunk maximum's bin holds them all):
+    the lowest indices are kept."""
+    wl = W.make_workload(_cfg(context=5000, batch=1, hq=4, hkv=1), seed=29)
+    wl["k_cache"][:] = 0.5
+    g, o = _check(wl, k1=12, k2=9, sink=64, window=128)
+    assert g["block_idx"][0, 0].tolist() == list(range(4, 13))
+
+
 def test_append_then_step_matches_oracle():
     """hsa_append_kv writes the new token and its codes with the stored scales; the whole
     step entry point gives the same result as the separate calls (selection, cache and codes
