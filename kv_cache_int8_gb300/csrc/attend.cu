@@ -1171,27 +1171,8 @@ __device__ __forceinline__ int sel_blocks_over_threshold(const int* tiles, int n
     __syncthreads();
     return K2;
   }
-  // a few to drop: the lowest ranked (smallest maximum, the higher index first among equals),
-  // taken one a round by warp 0 (a warp-wide minimum a round)
-  if (drop > 0 && warp == 0) {
-    for (int e = 0; e < drop; e++) {
-      int bv = INT_MAX, bi = -1;
-      for (int i = lane; i < n_c; i += 32) {
-        const int vi = cv[i];  // INT_MAX: taken in an earlier round (scores are far below it)
-        if (vi < bv || (vi == bv && vi != INT_MAX && i > bi)) {
-          bv = vi;
-          bi = i;
-        }
-      }
-      const int mv = __reduce_min_sync(0xffffffffu, bv);
-      const int mi = __reduce_max_sync(0xffffffffu, bv == mv ? bi : -1);
-      if (lane == 0) {
-        ss.cand_i[e] = mi;
-        cv[mi] = INT_MAX;
-      }
-      __syncwarp();
-    }
-  }
+  // a few to drop: the lowest ranked, taken one a round by warp 0
+  if (drop > 0 && warp == 0) sel_peel_lowest(cv, n_c, drop, ss.cand_i);
   if (drop > 0) __syncthreads();
   // every kept candidate's place: its index minus the dropped ones before it
   for (int i = tid; i < n_c; i += NT) {

@@ -28,6 +28,12 @@ namespace {
 #endif
 constexpr int kPruneThreads = HSA_PRUNE_THREADS;  // overridable at build time for tuning
 constexpr int kPruneWarps = kPruneThreads / 32;
+constexpr int kPrunePeel = 8;  // module 2's threshold form: most candidates dropped one a round
+// 1: without chunk outputs and with K1 >= K2, module 2 ranks only the kept chunks' blocks at
+// or above module 1's threshold (see prune_kernel)
+#ifndef HSA_PRUNE_THRESHOLD
+#define HSA_PRUNE_THRESHOLD 1
+#endif
 #ifndef HSA_PRUNE_RANGE
 #define HSA_PRUNE_RANGE 1
 #endif
@@ -59,6 +65,7 @@ struct PruneArgs {
 struct PruneShared {
   SelectShared sel;  // histogram, per-warp scratch (select.cuh)
   uint64_t bar[2];   // staging copies: [0] module 1's, [1] the rest
+  int wcnt[4][kPruneWarps];  // module 2's threshold form: blocks kept by each warp and pass
 };
 
 // Issue (thread 0) and tail of a planned row; returns where src[0] lands.
@@ -265,12 +272,23 @@ __global__ void __launch_bounds__(kPruneThreads, 1024 / kPruneThreads) prune_ker
   const int n2 = got1 * P;
   const int32_t* prow = a.sel_pages ? a.page_table + (size_t)b * a.max_pages : nullptr;
   if (!need1_now && bytes1 > 0 && !mbar_wait(&ps.bar[1], 0)) set_error(a.err, kDevErrTimeout);
+  const int lane = tid & 31, warp = tid >> 5;
+  // Threshold form (no chunk ids are output, K1 >= K2): module 1's threshold T, the K1-th
+  // largest chunk score, is at most the K2-th largest, and the top K2 chunks each hold a block
+  // equal to their score, so every kept block reaches T. Only the blocks >= T take part: laid
+  // out in order (positions by ballots, one barrier), and when a few more than K2 of them
+  // remain, the lowest ranked are taken one a round by warp 0.
+  const bool thr = HSA_PRUNE_THRESHOLD && a.k0 == 0 && a.chunk_idx == nullptr &&
+                   a.n_chunks == nullptr && a.k1 >= a.k2 && a.k2 > 0 &&
+                   n2 <= 4 * kPruneThreads;
   int valid_local = 0, mn2 = INT_MAX, mx2 = INT_MIN;
-  for (int x0 = tid; x0 < n2; x0 += 4 * kPruneThreads) {
+  int n2c = n2;  // entries in vals / cand (/ cand_page)
+  if (thr) {
     int v[4], kk[4], pg[4];
+    unsigned bal[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const int x = x0 + u * kPruneThreads;
+      const int x = tid + u * kPruneThreads;
       kk[u] = x < n2 ? kept_chunks[x / P] * P + x % P : -1;
       const bool in = kk[u] >= k_lo && kk[u] < k_hi;
       v[u] = in ? (use_row ? row[kk[u] - k_lo] : __ldg(bm + kk[u])) : INT_MIN;
@@ -278,20 +296,107 @@ __global__ void __launch_bounds__(kPruneThreads, 1024 / kPruneThreads) prune_ker
     }
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const int x = x0 + u * kPruneThreads;
-      if (x < n2) {
-        cand[x] = kk[u];
-        vals[x] = v[u];
-        if (prow) cand_page[x] = pg[u];
-        if (v[u] != INT_MIN) {
-          valid_local++;
-          mn2 = min(mn2, v[u]);
-          mx2 = max(mx2, v[u]);
+      if (v[u] < T) v[u] = INT_MIN;
+      bal[u] = __ballot_sync(0xffffffffu, v[u] != INT_MIN);
+      if (lane == 0) ps.wcnt[u][warp] = __popc(bal[u]);
+      if (v[u] != INT_MIN) {
+        mn2 = min(mn2, v[u]);
+        mx2 = max(mx2, v[u]);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      mn2 = min(mn2, __shfl_xor_sync(0xffffffffu, mn2, off));
+      mx2 = max(mx2, __shfl_xor_sync(0xffffffffu, mx2, off));
+    }
+    if (lane == 0) {
+      ps.sel.mn[warp] = mn2;
+      ps.sel.mx[warp] = mx2;
+    }
+    __syncthreads();  // (module 1's collect is done with vals: it ended on a barrier)
+    // lane l of every warp reads the counts of warp l & 15 (passes 0-1 in lanes 0-15, 2-3
+    // in lanes 16-31); warp sums give each pass's total and the warps before this one
+    static_assert(kPruneWarps == 16, "two lanes a warp: 16 warps");
+    const int cw = lane & 15, u0 = lane >> 4;
+    const int c0 = ps.wcnt[2 * u0][cw], c1 = ps.wcnt[2 * u0 + 1][cw];
+    mn2 = min(ps.sel.mn[cw], __shfl_xor_sync(0xffffffffu, ps.sel.mn[cw], 16));
+    mx2 = max(ps.sel.mx[cw], __shfl_xor_sync(0xffffffffu, ps.sel.mx[cw], 16));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) {
+      mn2 = min(mn2, __shfl_xor_sync(0xffffffffu, mn2, off));
+      mx2 = max(mx2, __shfl_xor_sync(0xffffffffu, mx2, off));
+    }
+    int tot[4], pre[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int c = (u >> 1) == u0 ? ((u & 1) ? c1 : c0) : 0;
+      tot[u] = __reduce_add_sync(0xffffffffu, c);
+      pre[u] = __reduce_add_sync(0xffffffffu, cw < warp ? c : 0);
+    }
+    n2c = tot[0] + tot[1] + tot[2] + tot[3];
+    const unsigned lt = (1u << lane) - 1u;
+    int before_u = 0;
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      if (v[u] != INT_MIN) {
+        const int pos = before_u + pre[u] + __popc(bal[u] & lt);
+        vals[pos] = v[u];
+        cand[pos] = kk[u];
+        if (prow) cand_page[pos] = pg[u];
+      }
+      before_u += tot[u];
+    }
+    __syncthreads();
+    const int drop = n2c - a.k2;
+    if (drop <= kPrunePeel) {
+      if (drop > 0 && warp == 0) sel_peel_lowest(vals, n2c, drop, ps.sel.cand_i);
+      if (drop > 0) __syncthreads();
+      const int got2 = min(a.k2, n2c);
+      for (int i = tid; i < n2c; i += kPruneThreads) {
+        int before = 0;
+        bool dropped = false;
+        for (int e = 0; e < drop; e++) {
+          const int de = ps.sel.cand_i[e];
+          before += de < i ? 1 : 0;
+          dropped = dropped || de == i;
+        }
+        if (!dropped) {
+          a.block_idx[bh * a.k2 + i - before] = cand[i];
+          if (prow) a.sel_pages[bh * a.k2 + i - before] = cand_page[i];
+        }
+      }
+      for (int i = got2 + tid; i < a.k2; i += kPruneThreads) a.block_idx[bh * a.k2 + i] = -1;
+      if (tid == 0) a.n_blocks[bh] = got2;
+      return;
+    }
+    valid_local = tid == 0 ? n2c : 0;  // the general selection over the n2c laid-out blocks
+  } else {
+    for (int x0 = tid; x0 < n2; x0 += 4 * kPruneThreads) {
+      int v[4], kk[4], pg[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int x = x0 + u * kPruneThreads;
+        kk[u] = x < n2 ? kept_chunks[x / P] * P + x % P : -1;
+        const bool in = kk[u] >= k_lo && kk[u] < k_hi;
+        v[u] = in ? (use_row ? row[kk[u] - k_lo] : __ldg(bm + kk[u])) : INT_MIN;
+        pg[u] = (in && prow) ? (prow_s ? prow_s[kk[u] - k_lo] : __ldg(prow + kk[u])) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int x = x0 + u * kPruneThreads;
+        if (x < n2) {
+          cand[x] = kk[u];
+          vals[x] = v[u];
+          if (prow) cand_page[x] = pg[u];
+          if (v[u] != INT_MIN) {
+            valid_local++;
+            mn2 = min(mn2, v[u]);
+            mx2 = max(mx2, v[u]);
+          }
         }
       }
     }
   }
-  const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     valid_local += __shfl_xor_sync(0xffffffffu, valid_local, off);
@@ -317,14 +422,14 @@ __global__ void __launch_bounds__(kPruneThreads, 1024 / kPruneThreads) prune_ker
   need_eq = 0;
   eq_total = 0;
   if (keep2 < n2_valid && keep2 > 0) {
-    const int3 r = sel_kth_largest<kPruneThreads>(vals, n2, keep2, ps.sel, true, mn2, mx2);
+    const int3 r = sel_kth_largest<kPruneThreads>(vals, n2c, keep2, ps.sel, true, mn2, mx2);
     T = r.x;
     need_eq = r.y;
     eq_total = r.z;
   }
   int got2 = 0;
   if (keep2 > 0) {
-    got2 = sel_collect<kPruneThreads>(vals, n2, T, need_eq, eq_total, ps.sel, sel_pos, 0);
+    got2 = sel_collect<kPruneThreads>(vals, n2c, T, need_eq, eq_total, ps.sel, sel_pos, 0);
   }
   for (int i = tid; i < a.k2; i += kPruneThreads) {
     const int x = i < got2 ? sel_pos[i] : -1;

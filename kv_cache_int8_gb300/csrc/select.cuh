@@ -584,6 +584,50 @@ __device__ __forceinline__ int sel_fast_reg(Get get, int n, int K, int vmin, int
   return keep_n;
 }
 
+// One warp (all its lanes): the `drop` lowest-ranked entries of vals[0, n) (the smallest
+// value, the higher index first among equal values) into out[0, drop), in that order; each
+// is marked taken by INT_MAX in vals (the values must lie below it). A round is a warp-wide
+// minimum over every lane's smallest entry, the lane scanning its entries four at a time
+// with independent partial minima.
+__device__ __forceinline__ void sel_peel_lowest(int* vals, int n, int drop, int* out) {
+  const int lane = threadIdx.x & 31;
+  auto better = [](int v, int i, int bv, int bi) { return v < bv || (v == bv && i > bi); };
+  for (int e = 0; e < drop; e++) {
+    int bv[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX}, bi[4] = {-1, -1, -1, -1};
+    int i = lane;
+    for (; i + 96 < n; i += 128) {
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int v = vals[i + 32 * u];
+        if (better(v, i + 32 * u, bv[u], bi[u])) {
+          bv[u] = v;
+          bi[u] = i + 32 * u;
+        }
+      }
+    }
+    for (; i < n; i += 32) {
+      const int v = vals[i];
+      if (better(v, i, bv[0], bi[0])) {
+        bv[0] = v;
+        bi[0] = i;
+      }
+    }
+#pragma unroll
+    for (int u = 1; u < 4; u++)
+      if (better(bv[u], bi[u], bv[0], bi[0])) {
+        bv[0] = bv[u];
+        bi[0] = bi[u];
+      }
+    const int mv = __reduce_min_sync(0xffffffffu, bv[0]);
+    const int mi = __reduce_max_sync(0xffffffffu, bv[0] == mv ? bi[0] : -1);
+    if (lane == 0) {
+      out[e] = mi;
+      vals[mi] = INT_MAX;
+    }
+    __syncwarp();
+  }
+}
+
 // sel_fast_reg on a SelRow, out of line (one copy of the code for every call site).
 template <int NT, int R>
 __device__ __noinline__ int sel_fast_row(SelRow row, int n, int K, int vmin, int vmax,
