@@ -174,7 +174,7 @@ class Case:
 
     KERNELS = ("step", "append", "score", "prune", "attend", "dense")
     BURST = 10  # a multiple of every replica count
-    L2_BYTES = 129 << 20
+    L2_BYTES = 129_000_000  # GB300: 129 MB
     REFRESH = 4
     CACHE_SLOTS = 8192  # GPU block cache of the offloaded case: 64 MiB of K/V blocks
 
@@ -206,9 +206,10 @@ class Case:
         B, Hq, Hkv = cfg.batch, cfg.hq, cfg.hkv
         self.q = wl["q"]
         self.pt, self.lens = wl["page_table"], wl["seq_lens"]
-        # replicas: consecutive steps read different ones, and between two reads of the same
-        # replica's key codes the steps read more than twice L2 of other codes (4-bit codes
-        # at 128K tokens, 67 MB a replica, take five)
+        # replicas: consecutive steps read different ones; two when one replica's key codes
+        # (the scan of a step) exceed L2, else five, so that between two reads of the same
+        # codes the steps read several times L2 of other data (4-bit codes at 128K tokens,
+        # 67 MB a replica)
         kq_shape = list(wl["k_cache"].shape)
         kq_shape[-1] = kq_shape[-1] * cfg.key_bits // 8  # 4-bit codes: two per byte
         codes = cfg.hkv * sum(wl["lens"]) * 128 * cfg.key_bits // 8
