@@ -418,6 +418,23 @@ def test_module1_keeping_k2_chunks_keeps_the_same_blocks(seed):
     short = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln)
     np.testing.assert_array_equal(full["block_idx"], short["block_idx"])
     np.testing.assert_array_equal(full["n_blocks"], short["n_blocks"])
+    # and every kept block reaches T1, the K2-th largest chunk maximum (the top K2 chunks each
+    # hold a block equal to their maximum), the bound the whole step's selection starts from
+    sel = oracle.select(d, bf16_bits(case["q"]), sc, kq, pt, ln, want_block_max=True)
+    for b in range(2):
+        for h in range(hkv):
+            bm = sel["block_max"][b, h].astype(np.int64)
+            nblk = bm.size
+            cm = np.full((nblk + 3) // 4, INT32_MIN, dtype=np.int64)
+            for k in range(nblk):
+                cm[k // 4] = max(cm[k // 4], bm[k])
+            valid = np.sort(cm[cm != INT32_MIN])[::-1]
+            if valid.size < k2:
+                continue
+            t1 = valid[k2 - 1]
+            kept = [k for k in sel["block_idx"][b, h] if k >= 0]
+            assert len(kept) == k2 and all(bm[k] >= t1 for k in kept)
+            assert (bm >= t1).sum() >= k2
 
 
 @pytest.mark.parametrize("seed", range(6))
