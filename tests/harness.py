@@ -96,7 +96,13 @@ def gpu_step(wl: dict, d: hsa.Dims, dense: bool = True) -> dict:
     nb2 = torch.full_like(n_blocks, -7)
     ci2 = torch.full_like(chunk_idx, -7)
     hsa.hsa_prune(d, wl["seq_lens"], bm2, tm, ci2, None, bi2, nb2)
+    # without chunk outputs (K1 >= K2: module 2 ranks only the blocks at or above module 1's
+    # threshold) the kept blocks are the same
+    bi3 = torch.full_like(block_idx, -7)
+    nb3 = torch.full_like(n_blocks, -7)
+    hsa.hsa_prune(d, wl["seq_lens"], bm2, tm, None, None, bi3, nb3)
     torch.cuda.synchronize()
+    assert torch.equal(bi3, block_idx) and torch.equal(nb3, n_blocks)
     assert torch.equal(bm2, bm)
     k_tiles = tm.shape[-1]
     pad = torch.full((B, R, 4 * k_tiles - bm.shape[-1]), INT32_MIN, dtype=torch.int32, device=dev)
