@@ -58,6 +58,11 @@
 #ifndef HSA_SEL_THRESHOLD
 #define HSA_SEL_THRESHOLD 1
 #endif
+// 1: the selecting attention's CTAs of a row prefetch the candidate blocks' K/V pages into L2
+// (each CTA a 1/nsplit share) as soon as the candidates are known
+#ifndef HSA_SEL_PREFETCH
+#define HSA_SEL_PREFETCH 1
+#endif
 #ifndef HSA_FUSED_SELECT
 #define HSA_FUSED_SELECT 1
 #endif
@@ -1057,7 +1062,10 @@ __device__ __forceinline__ int sel_blocks_over_threshold(const int* tiles, int n
                                                          int K2, int t_min, int t_max, int vmax,
                                                          const int* prow, int* cv, int* ci,
                                                          int cap, SelectShared& ss, int* selb,
-                                                         int* selp) {
+                                                         int* selp, const __nv_bfloat16* k_head,
+                                                         const __nv_bfloat16* v_head,
+                                                         size_t page_elems, int num_pages,
+                                                         int split, int nsplit) {
   constexpr int kW = NT / 32;
   constexpr int kPeel = 8;  // at most this many dropped candidates are taken one a round
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1158,6 +1166,17 @@ __device__ __forceinline__ int sel_blocks_over_threshold(const int* tiles, int n
       }
     }
   __syncthreads();
+  // the kept blocks are among the candidates: warm L2 with their K and V pages now (the row's
+  // CTAs split them by index), so that the copies issued after the selection hit L2
+  if (HSA_SEL_PREFETCH && prow != nullptr) {
+    for (int i = split + tid * nsplit; i < n_c; i += NT * nsplit) {
+      const int page = prow[ci[i] - k_lo];
+      if (page < 0 || page >= num_pages) continue;  // reported when the copy is resolved
+      const size_t off = (size_t)page * page_elems;
+      bulk_prefetch_l2(k_head + off, kBlockBytesBf16);
+      bulk_prefetch_l2(v_head + off, kBlockBytesBf16);
+    }
+  }
   if (drop > kPeel) {
     // many to drop: the register selection over the candidates (ids written in order), else
     // the radix select and ordered collect (positions among the candidates)
@@ -1357,7 +1376,10 @@ __global__ void __launch_bounds__((W + 1) * 32, 1)
     if (!ok) set_error(a.err, kDevErrTimeout);
     got2 = sel_blocks_over_threshold<NT, kRegVals, P>(
         tiles, n1, c_lo, brow, k_lo, k_hi, a.k2, t_min, t_max, b_max, use_prow ? prow : nullptr,
-        area, area + sa.n2_cap, sa.n2_cap, ss, selb, selp);
+        area, area + sa.n2_cap, sa.n2_cap, ss, selb, selp,
+        a.k + (size_t)(h / a.kv_div) * kPage * kHeadDim,
+        a.v + (size_t)(h / a.kv_div) * kPage * kHeadDim, (size_t)a.kv_heads * kPage * kHeadDim,
+        a.num_pages, split, a.nsplit);
     mapped = got2 >= 0;
   }
   if (!mapped) {
