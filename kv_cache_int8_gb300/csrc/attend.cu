@@ -1752,25 +1752,46 @@ bool plan_select(const Shape& s, SelArgs& sa, bool stage_pages) {
 }
 
 // The attention's warps and ring slots for a group size (as launch_g's sparse path).
-template <int G>
+// Launch shapes of the selecting attention: 8 compute warps with two ring slots each (7 for
+// groups of 8 query heads), or, for groups of up to 4 when a CTA's share of a row is at most
+// kSelFewWarps segments, that many compute warps with one slot each, so that no warp takes a
+// second segment: measured on GB300, a 128K step (about 11 segments a CTA) 41.6 against
+// 42.9 us (10 warps: 43.1; 12: 41.7), the batched case of 8 sequences (about 19 a CTA) 120.5
+// against 119.4 us with 11, so it keeps 8.
+#ifndef HSA_SEL_FEW_WARPS
+#define HSA_SEL_FEW_WARPS 11
+#endif
+constexpr int kSelFewWarps = HSA_SEL_FEW_WARPS;
+template <int G, bool FEW = false>
 struct SelShape {
-  static constexpr int W = G > 4 ? 7 : kSparseWarps;
-  static constexpr int NS = 2 * W;
+  static constexpr int W = G > 4 ? 7 : (FEW ? kSelFewWarps : kSparseWarps);
+  static constexpr int NS = FEW && G <= 4 ? kSelFewWarps : 2 * W;
 };
 
+// The capacities are planned for the 8-warp shape, whose shared memory is the larger.
 template <int G>
 bool plan_select_g(const Shape& s, SelArgs& sa, bool stage_pages) {
   return plan_select<G, SelShape<G>::W, SelShape<G>::NS>(s, sa, stage_pages);
 }
 
-template <int G>
-cudaError_t launch_select_g(const AttArgs& a, const SelArgs& sa, dim3 grid, cudaStream_t st) {
-  constexpr int W = SelShape<G>::W, NS = SelShape<G>::NS;
+template <int G, bool FEW>
+cudaError_t launch_select_shape(const AttArgs& a, const SelArgs& sa, dim3 grid,
+                                cudaStream_t st) {
+  constexpr int W = SelShape<G, FEW>::W, NS = SelShape<G, FEW>::NS;
   const size_t smem = sel_smem_bytes<G, W, NS>(sa);
   auto kern = attend_select_kernel<G, W, NS>;
   cudaError_t e = set_kernel_smem(kern, smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, grid, dim3((W + 1) * 32), smem, st, true, a, sa);
+}
+
+template <int G>
+cudaError_t launch_select_g(const AttArgs& a, const SelArgs& sa, dim3 grid, cudaStream_t st,
+                            bool few) {
+  if constexpr (G <= 4 && kSelFewWarps > 0) {  // (0: the 8-warp shape only)
+    if (few) return launch_select_shape<G, true>(a, sa, grid, st);
+  }
+  return launch_select_shape<G, false>(a, sa, grid, st);
 }
 
 bool plan_select_any(const Shape& s, SelArgs& sa, bool stage_pages) {
@@ -1924,11 +1945,16 @@ cudaError_t launch_attend_select(const Shape& s, const void* q, const void* k_ca
   a.early = 1;
   a.row_range = row_range;
   dim3 grid(buf.nsplit, s.hkv, s.batch);
+  // segments of a row at most (sink pages, kept blocks, window pages with a partial one) and
+  // a CTA's share of them
+  const long long segs =
+      (s.sink + kPage - 1) / kPage + s.k2 + (s.window + kPage - 1) / kPage + 1;
+  const bool few = (segs + buf.nsplit - 1) / buf.nsplit <= kSelFewWarps;
   switch (s.group) {
-    case 1: return launch_select_g<1>(a, sa, grid, st);
-    case 2: return launch_select_g<2>(a, sa, grid, st);
-    case 4: return launch_select_g<4>(a, sa, grid, st);
-    case 8: return launch_select_g<8>(a, sa, grid, st);
+    case 1: return launch_select_g<1>(a, sa, grid, st, few);
+    case 2: return launch_select_g<2>(a, sa, grid, st, few);
+    case 4: return launch_select_g<4>(a, sa, grid, st, few);
+    case 8: return launch_select_g<8>(a, sa, grid, st, few);
     default: return cudaErrorInvalidValue;
   }
 }
