@@ -44,7 +44,7 @@
 #define HSA_HOST_CTAS_PER_SM 3
 #endif
 #ifndef HSA_SPARSE_WARPS
-#define HSA_SPARSE_WARPS 8
+#define HSA_SPARSE_WARPS 12
 #endif
 // Sparse attend: leave one SM per (sequence, kv head) to the prune kernel that is still
 // running when the attend starts, when that costs at most a quarter of the splits.
@@ -73,10 +73,15 @@ namespace {
 constexpr int kWarps = 4;                        // compute warps of the host path
 constexpr int kCompute = kWarps * 32;
 constexpr int kStages = 8;
-// HBM path, sparse attend: 8 compute warps + the producer. A CTA of it does not fit beside a
-// prune CTA (the three warps on one SM sub-partition take its register file), so the prune
-// keeps its SMs to itself; the attend's grid leaves those SMs free (HSA_SPARSE_RESERVE).
+// HBM path, sparse attend: for CTAs with many segments 12 compute warps + the producer, two
+// ring slots each (measured on GB300 at 1M tokens, about 22 segments a CTA: the attention
+// 12.9 against 15.6 us with 8 warps, the step 188.0 against 189.5 us; 10 warps 189.4), for
+// fewer segments 8 (a 128K row's reuse step, about 11 a CTA, and the batched case's
+// attention, about 19, measured faster with 8). A CTA of it does not fit beside a prune CTA
+// (registers), so the prune keeps its SMs to itself; the attend's grid leaves those SMs free
+// (HSA_SPARSE_RESERVE).
 constexpr int kSparseWarps = HSA_SPARSE_WARPS;  // ring: two slots per compute warp
+constexpr int kSparseManySegs = 20;
 constexpr int kDenseWarps = 4, kDenseStages = 8;     // HBM path, dense decode
 constexpr int kSlotBytes = 2 * kBlockBytesBf16;  // K page + V page of one head
 constexpr int kHostThreads = kCompute;
@@ -1691,6 +1696,17 @@ size_t host_smem() {
 }
 static_assert(kStages % kWarps == 0, "each compute warp owns fixed ring slots");
 
+template <int G, bool DENSE, int W, int NS>
+cudaError_t launch_tma(const AttArgs& a, dim3 grid, cudaStream_t st) {
+  constexpr size_t smem = tma_smem<G, W, NS>();
+  auto kern = attend_tma_kernel<G, DENSE, W, NS, false>;
+  if constexpr (!DENSE)
+    if (a.seg_l2 != nullptr) kern = attend_tma_kernel<G, false, W, NS, true>;
+  cudaError_t e = set_kernel_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, grid, dim3((W + 1) * 32), smem, st, true, a);
+}
+
 template <int G, bool DENSE>
 cudaError_t launch_g(AttArgs a, dim3 grid, bool host, cudaStream_t st) {
   if (host) {
@@ -1699,17 +1715,21 @@ cudaError_t launch_g(AttArgs a, dim3 grid, bool host, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     return launch_kernel(attend_host_kernel<G, DENSE>, grid, dim3(kHostThreads), smem, st, true, a);
   }
-  // groups of 8 hold 8 x 16 query floats per lane: at most two warps per SM sub-partition
-  // (registers), so the sparse attend takes 7 compute warps there
-  constexpr int W = DENSE ? kDenseWarps : (G > 4 ? 7 : kSparseWarps);
-  constexpr int NS = DENSE ? kDenseStages : 2 * W;
-  constexpr size_t smem = tma_smem<G, W, NS>();
-  auto kern = attend_tma_kernel<G, DENSE, W, NS, false>;
-  if constexpr (!DENSE)
-    if (a.seg_l2 != nullptr) kern = attend_tma_kernel<G, false, W, NS, true>;
-  cudaError_t e = set_kernel_smem(kern, smem);
-  if (e != cudaSuccess) return e;
-  return launch_kernel(kern, grid, dim3((W + 1) * 32), smem, st, true, a);
+  if constexpr (DENSE) {
+    return launch_tma<G, true, kDenseWarps, kDenseStages>(a, grid, st);
+  } else if constexpr (G > 4) {
+    // groups of 8 hold 8 x 16 query floats per lane: at most two warps per SM sub-partition
+    // (registers), so the sparse attend takes 7 compute warps there
+    return launch_tma<G, false, 7, 14>(a, grid, st);
+  } else {
+    // a CTA's share of a row's segments (sink pages, kept blocks, window pages) decides the
+    // shape: kSparseWarps compute warps from kSparseManySegs on, else 8
+    const long long segs =
+        (a.sink + kPage - 1) / kPage + a.k2 + (a.window + kPage - 1) / kPage + 1;
+    if ((segs + a.nsplit - 1) / a.nsplit >= kSparseManySegs)
+      return launch_tma<G, false, kSparseWarps, 2 * kSparseWarps>(a, grid, st);
+    return launch_tma<G, false, 8, 16>(a, grid, st);
+  }
 }
 
 constexpr size_t kSelSmemLimit = 227 * 1024 - 256;  // room for the static shared memory
@@ -1764,7 +1784,7 @@ bool plan_select(const Shape& s, SelArgs& sa, bool stage_pages) {
 constexpr int kSelFewWarps = HSA_SEL_FEW_WARPS;
 template <int G, bool FEW = false>
 struct SelShape {
-  static constexpr int W = G > 4 ? 7 : (FEW ? kSelFewWarps : kSparseWarps);
+  static constexpr int W = G > 4 ? 7 : (FEW ? kSelFewWarps : 8);
   static constexpr int NS = FEW && G <= 4 ? kSelFewWarps : 2 * W;
 };
 
