@@ -413,7 +413,8 @@ int32_t do_attend(const hsa_dims* d, const Shape& s, bool dense, const void* q, 
   buf.part_o = reinterpret_cast<float*>(ws + l.part_o);
   buf.sel_pages = sel_pages;
   const Shape sa = attend_shape(s, dense);
-  buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(sa, dense, host, num_sms()));
+  // SMs are left free only for a pruning kernel that runs beside an early attention
+  buf.nsplit = std::min(kMaxSplits, hsa::attend_splits(sa, dense, host, num_sms(), early));
   return cuda_status(hsa::launch_attend(sa, dense, host, q, kd, vd, pt, lens, bidx, nb, out, lse,
                                         buf, reinterpret_cast<int*>(ws), st, early));
 }

@@ -76,12 +76,19 @@ constexpr int kStages = 8;
 // HBM path, sparse attend: for CTAs with many segments 12 compute warps + the producer, two
 // ring slots each (measured on GB300 at 1M tokens, about 22 segments a CTA: the attention
 // 12.9 against 15.6 us with 8 warps, the step 188.0 against 189.5 us; 10 warps 189.4), for
-// fewer segments 8 (a 128K row's reuse step, about 11 a CTA, and the batched case's
-// attention, about 19, measured faster with 8). A CTA of it does not fit beside a prune CTA
-// (registers), so the prune keeps its SMs to itself; the attend's grid leaves those SMs free
+// fewer segments 8 (the batched case's pruning-form attention, about 19 a CTA, measured
+// faster with 8). A CTA of it does not fit beside a prune CTA (registers), so the prune
+// keeps its SMs to itself; an attention launched early beside it leaves those SMs free
 // (HSA_SPARSE_RESERVE).
 constexpr int kSparseWarps = HSA_SPARSE_WARPS;  // ring: two slots per compute warp
 constexpr int kSparseManySegs = 20;
+// CTAs with at most this many segments take as many compute warps with one slot each, so
+// that no warp takes a second segment (a 128K row's attention called alone, 11 a CTA: the
+// reuse step 16.6 against 17.2 us with 8 warps and two slots)
+#ifndef HSA_SPARSE_FEW_WARPS
+#define HSA_SPARSE_FEW_WARPS 11
+#endif
+constexpr int kSparseFewWarps = HSA_SPARSE_FEW_WARPS;
 constexpr int kDenseWarps = 4, kDenseStages = 8;     // HBM path, dense decode
 constexpr int kSlotBytes = 2 * kBlockBytesBf16;  // K page + V page of one head
 constexpr int kHostThreads = kCompute;
@@ -1726,8 +1733,13 @@ cudaError_t launch_g(AttArgs a, dim3 grid, bool host, cudaStream_t st) {
     // shape: kSparseWarps compute warps from kSparseManySegs on, else 8
     const long long segs =
         (a.sink + kPage - 1) / kPage + a.k2 + (a.window + kPage - 1) / kPage + 1;
-    if ((segs + a.nsplit - 1) / a.nsplit >= kSparseManySegs)
+    const long long per_cta = (segs + a.nsplit - 1) / a.nsplit;
+    if (per_cta >= kSparseManySegs)
       return launch_tma<G, false, kSparseWarps, 2 * kSparseWarps>(a, grid, st);
+    if constexpr (kSparseFewWarps > 0) {
+      if (per_cta <= kSparseFewWarps)
+        return launch_tma<G, false, kSparseFewWarps, kSparseFewWarps>(a, grid, st);
+    }
     return launch_tma<G, false, 8, 16>(a, grid, st);
   }
 }
